@@ -1,0 +1,386 @@
+"""Reference oracle for the compressed-KV decode step.
+
+TEST INFRASTRUCTURE ONLY.  Only the test suite, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` may import this module.  The product path
+(the CUDA library and its Python binding) never calls it, and this module never
+imports the product package: the two share no code.
+
+What it computes, step by step, each citing the page passage it restates:
+
+* ``kv_cache_bytes`` -- the KV-memory closed form of "KV Cache optimization
+  techniques" (metaphor-xennon), section "KV Cache的挑战" (kv_cache_memory_analysis).
+* ``quantize_rows`` -- per-token symmetric quantisation, "KV Cache optimization
+  techniques" section 1.2 (PerTokenKVQuantizer) and "Technical Report: KV Cache
+  Compression for Text-Only LLMs" section 3.2 (quantize_kv): one scale per
+  (token, head) = amax over head_dim / (2^(bits-1) - 1), code = round-half-even
+  of x / scale, clamped.  Computed in IEEE fp32 exactly as the pages' fp32
+  tensors would be (division, not reciprocal multiplication).
+* ``attention`` -- the dense definition softmax(Q K^T / sqrt(d)) V of the
+  Technical Report section 1.1, evaluated in fp64 on the dequantised keys and
+  values (code * scale, section 3.2) and on the bf16 sink tokens (section 3.2:
+  sinks are not quantised).
+* ``h2o_increments`` -- the H2O heavy-hitter score: column sums of the softmax
+  probabilities (Technical Report section 3.4, ``attention_scores.sum(dim=0)``;
+  the survey page's section 3.3 calls it the cumulative attention a token
+  receives from all later tokens).  With grouped-query attention the G query
+  heads that read one KV head all add to that head's score.
+* ``select_h2o`` / ``select_streaming`` -- the kept set: the attention sinks,
+  the recent window, and the top-k of the remaining tokens by accumulated
+  score, ties to the lower position (Technical Report sections 3.3-3.4,
+  "KV Cache optimization techniques" sections 2.2 and 2.4).
+
+Readings where the pages are silent or disagree are listed in the design doc; the
+ones that change arithmetic are restated beside the function they affect.
+
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
+(closed forms, worked examples with exact scales, library witnesses, invariants,
+brute force).  None is "parity unpinned".
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+HEAD_DIM = 128
+NUM_SINK = 4
+
+
+# ---------------------------------------------------------------------------
+# Closed form for KV bytes
+# ---------------------------------------------------------------------------
+
+def kv_cache_bytes(batch: int, seq_len: int, num_layers: int, num_heads: int,
+                   head_dim: int, bytes_per_element: int) -> int:
+    """Bytes held by an uncompressed KV cache.
+
+    "KV Cache optimization techniques", section "KV Cache的挑战": per token the
+    cache holds a key and a value vector for every layer and head, i.e.
+    2 * layers * heads * head_dim * bytes_per_element bytes; the whole cache is
+    that times batch * seq_len.
+    """
+    per_token = 2 * num_layers * num_heads * head_dim * bytes_per_element
+    return per_token * batch * seq_len
+
+
+def kv_cache_gib(batch, seq_len, num_layers, num_heads, head_dim, bytes_per_element) -> float:
+    """The same closed form in GiB (the page divides by 1024**3)."""
+    return kv_cache_bytes(batch, seq_len, num_layers, num_heads, head_dim,
+                          bytes_per_element) / float(1024 ** 3)
+
+
+def stored_bytes_per_token_head(bits: int, head_dim: int = HEAD_DIM,
+                                with_scales: bool = True) -> int:
+    """Bytes one (token, KV head) occupies in the compressed cache: K and V codes
+    (bits/8 bytes per element) plus, optionally, one fp32 scale each for K and V
+    (per-token scales, "KV Cache optimization techniques" section 1.2)."""
+    code_bytes = 2 * (head_dim * bits // 8)
+    return code_bytes + (2 * 4 if with_scales else 0)
+
+
+# ---------------------------------------------------------------------------
+# bf16 helpers (input decoding only: bf16 -> fp32 is exact)
+# ---------------------------------------------------------------------------
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of raw bf16 bit patterns (uint16) to fp32."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32)
+
+
+# ---------------------------------------------------------------------------
+# Per-token quantisation
+# ---------------------------------------------------------------------------
+
+def qmax_for_bits(bits: int) -> int:
+    """2^(bits-1) - 1: 127 for INT8, 7 for INT4 ("KV Cache optimization
+    techniques" section 1.2, ``max_val``)."""
+    if bits not in (4, 8):
+        # The quantiser of section 1.1 raises on unsupported widths.
+        raise ValueError(f"unsupported bits: {bits}")
+    return (1 << (bits - 1)) - 1
+
+
+def code_range(bits: int) -> tuple[int, int]:
+    """Clamp range of the codes.
+
+    INT8: [-127, 127] (Technical Report section 3.2 clamps symmetric; the
+    techniques page clamps to [-128, 127] -- the bound never binds because
+    |x / scale| <= 127 * (1 + 2^-24) rounds to at most 127).
+    INT4: [-8, 7] (techniques page section 1.1); again only [-7, 7] is reached.
+    """
+    return (-127, 127) if bits == 8 else (-8, 7)
+
+
+def quantize_rows(x: np.ndarray, bits: int) -> tuple[np.ndarray, np.ndarray]:
+    """Quantise each row (last axis = head_dim) of an fp32 array.
+
+    Returns (codes as int8 with the same shape as ``x``, scales fp32 of shape
+    ``x.shape[:-1]``).
+
+    Steps, in the order of "KV Cache optimization techniques" section 1.2:
+      1. amax = max |x| over the row (exact in fp32);
+      2. scale = amax / qmax, one IEEE fp32 division (no epsilon: the
+         Technical Report's quantize_kv adds none);
+      3. code = round-half-to-even(x / scale) with an IEEE fp32 division,
+         then clamp to ``code_range(bits)``.
+    A row whose amax is 0 has scale 0 and all codes 0 (0/0 is avoided).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    qmax = np.float32(qmax_for_bits(bits))
+    amax = np.max(np.abs(x), axis=-1)
+    scale = (amax / qmax).astype(np.float32)
+    safe = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = (x / safe[..., None]).astype(np.float32)
+    codes = np.rint(ratio)  # numpy rint: round half to even
+    lo, hi = code_range(bits)
+    codes = np.clip(codes, lo, hi)
+    codes = np.where(scale[..., None] > 0, codes, 0).astype(np.int8)
+    return codes, scale
+
+
+def pack_int4(codes: np.ndarray) -> np.ndarray:
+    """Two INT4 codes per byte: element 2i in the low nibble, 2i+1 in the high
+    nibble, two's complement (the page's ``.to(torch.int4)`` is not a real
+    dtype; this packing is our stated reading)."""
+    c = np.asarray(codes, dtype=np.int8).astype(np.uint8) & np.uint8(0x0F)
+    return (c[..., 0::2] | (c[..., 1::2] << np.uint8(4))).astype(np.uint8)
+
+
+def unpack_int4(packed: np.ndarray) -> np.ndarray:
+    """Inverse of ``pack_int4`` (sign-extends each nibble)."""
+    p = np.asarray(packed, dtype=np.uint8)
+    lo = (p & np.uint8(0x0F)).astype(np.int16)
+    hi = (p >> np.uint8(4)).astype(np.int16)
+    lo = np.where(lo >= 8, lo - 16, lo)
+    hi = np.where(hi >= 8, hi - 16, hi)
+    out = np.empty(p.shape[:-1] + (p.shape[-1] * 2,), dtype=np.int8)
+    out[..., 0::2] = lo
+    out[..., 1::2] = hi
+    return out
+
+
+def dequantize(codes: np.ndarray, scale: np.ndarray) -> np.ndarray:
+    """code * scale in fp64 ("KV Cache optimization techniques" section 1.2,
+    dequantize; Technical Report section 3.2, K_q * scale_k)."""
+    return np.asarray(codes, dtype=np.float64) * np.asarray(scale, dtype=np.float64)[..., None]
+
+
+# ---------------------------------------------------------------------------
+# Attention (fp64 definition)
+# ---------------------------------------------------------------------------
+
+def attention(q: np.ndarray, keys: np.ndarray, values: np.ndarray,
+              sm_scale: float | None = None) -> tuple[np.ndarray, np.ndarray]:
+    """softmax(q K^T * sm_scale) V for a set of query rows, in fp64.
+
+    q: [G, D]; keys, values: [N, D].  Returns (out [G, D], probs [G, N]).
+    sm_scale defaults to 1/sqrt(D) (Technical Report section 1.1).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(keys, dtype=np.float64)
+    v = np.asarray(values, dtype=np.float64)
+    d = q.shape[-1]
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(d)
+    logits = (q @ k.T) * sm_scale
+    m = logits.max(axis=-1, keepdims=True)
+    e = np.exp(logits - m)
+    probs = e / e.sum(axis=-1, keepdims=True)
+    return probs @ v, probs
+
+
+def h2o_increments(probs: np.ndarray) -> np.ndarray:
+    """H2O score added this step to each attended token: the column sum of the
+    softmax probabilities over the query rows that read this KV head
+    (Technical Report section 3.4, ``attention_scores.sum(dim=0)``)."""
+    return np.asarray(probs, dtype=np.float64).sum(axis=0)
+
+
+# ---------------------------------------------------------------------------
+# Selection
+# ---------------------------------------------------------------------------
+
+def select_h2o(pos: np.ndarray, score: np.ndarray, pos_total: int, budget: int,
+               recent: int, n_sink_present: int = NUM_SINK) -> np.ndarray:
+    """Keep-mask over the non-sink tokens of one (sequence, KV head).
+
+    The attention sinks (always kept, not in ``pos``) take ``n_sink_present``
+    places of the budget.  If every token fits, nothing is evicted.  Otherwise
+    the recent window (positions >= pos_total - recent) is kept, and of the
+    other tokens the ``budget - NUM_SINK - recent`` with the largest scores,
+    ties to the lower position (Technical Report section 3.4: keep heavy
+    hitters and recent tokens; "KV Cache optimization techniques" section 2.2:
+    evict once the cache exceeds its limit, keep by top-k of the score).
+    """
+    pos = np.asarray(pos, dtype=np.int64)
+    score = np.asarray(score, dtype=np.float64)
+    n = pos.shape[0]
+    if n_sink_present + n <= budget:
+        return np.ones(n, dtype=bool)
+    heavy = budget - NUM_SINK - recent
+    if heavy < 0:
+        raise ValueError("budget must cover the sinks and the recent window")
+    keep = pos >= pos_total - recent
+    cand = np.nonzero(~keep)[0]
+    # order: score descending, then position ascending
+    order = np.lexsort((pos[cand], -score[cand]))
+    keep[cand[order[:heavy]]] = True
+    return keep
+
+
+def select_streaming(pos: np.ndarray, pos_total: int, window: int,
+                     n_sink_present: int = NUM_SINK) -> np.ndarray:
+    """StreamingLLM keep-mask: the sinks (kept outside this mask) plus the last
+    ``window`` positions (Technical Report section 3.3 SlidingWindow: sink
+    tokens then a deque of the most recent ``window_size`` tokens)."""
+    pos = np.asarray(pos, dtype=np.int64)
+    if pos.shape[0] <= window:
+        return np.ones(pos.shape[0], dtype=bool)
+    return pos >= pos_total - window
+
+
+# ---------------------------------------------------------------------------
+# Dense per-(sequence, KV head) cache that runs the decode step
+# ---------------------------------------------------------------------------
+
+@dataclass
+class HeadState:
+    """Non-sink tokens of one (sequence, KV head), in insertion order."""
+    pos: np.ndarray            # int64 [N]
+    kcodes: np.ndarray         # int8  [N, D]  (unpacked codes)
+    kscale: np.ndarray         # fp32  [N]
+    vcodes: np.ndarray         # int8  [N, D]
+    vscale: np.ndarray         # fp32  [N]
+    score: np.ndarray          # fp64  [N]
+
+
+@dataclass
+class SeqState:
+    pos_total: int = 0
+    sink_k: list = field(default_factory=list)   # per head: fp32 [ns, D]
+    sink_v: list = field(default_factory=list)
+    sink_score: list = field(default_factory=list)  # per head: fp64 [ns]
+    heads: list = field(default_factory=list)   # per head: HeadState
+
+
+def _empty_head(d: int) -> HeadState:
+    return HeadState(np.zeros(0, np.int64), np.zeros((0, d), np.int8), np.zeros(0, np.float32),
+                     np.zeros((0, d), np.int8), np.zeros(0, np.float32), np.zeros(0, np.float64))
+
+
+class OracleCache:
+    """One layer of the compressed cache for a batch of sequences, dense (no
+    paging), evaluated token by token.
+
+    Per decode step the order is append -> attention (the new token attends to
+    itself) -> score accumulation -> select -> evict ("KV Cache optimization
+    techniques" section 2.2: append, then evict once over the limit).
+    """
+
+    def __init__(self, batch: int, num_q_heads: int, num_kv_heads: int, bits: int,
+                 head_dim: int = HEAD_DIM):
+        if num_q_heads % num_kv_heads:
+            raise ValueError("num_q_heads must be a multiple of num_kv_heads")
+        qmax_for_bits(bits)
+        self.batch, self.hq, self.hkv, self.bits, self.d = batch, num_q_heads, num_kv_heads, bits, head_dim
+        self.group = num_q_heads // num_kv_heads
+        self.seqs = []
+        for _ in range(batch):
+            s = SeqState()
+            for _ in range(num_kv_heads):
+                s.sink_k.append(np.zeros((0, head_dim), np.float32))
+                s.sink_v.append(np.zeros((0, head_dim), np.float32))
+                s.sink_score.append(np.zeros(0, np.float64))
+                s.heads.append(_empty_head(head_dim))
+            self.seqs.append(s)
+
+    # -- write path ---------------------------------------------------------
+    def append(self, b: int, k: np.ndarray, v: np.ndarray) -> None:
+        """Append n tokens to sequence b.  k, v: fp32 [Hkv, n, D] (exact bf16
+        values).  Positions < NUM_SINK are stored unquantised (Technical Report
+        section 3.2: sink KV stay in half precision); the others are quantised
+        once, at write time."""
+        s = self.seqs[b]
+        n = k.shape[1]
+        for i in range(n):
+            p = s.pos_total + i
+            for h in range(self.hkv):
+                if p < NUM_SINK:
+                    s.sink_k[h] = np.vstack([s.sink_k[h], k[h, i][None]])
+                    s.sink_v[h] = np.vstack([s.sink_v[h], v[h, i][None]])
+                    s.sink_score[h] = np.append(s.sink_score[h], 0.0)
+        first_q = max(0, NUM_SINK - s.pos_total)
+        if first_q < n:
+            kc, ks = quantize_rows(k[:, first_q:], self.bits)
+            vc, vs = quantize_rows(v[:, first_q:], self.bits)
+            newpos = np.arange(s.pos_total + first_q, s.pos_total + n, dtype=np.int64)
+            for h in range(self.hkv):
+                hs = s.heads[h]
+                hs.pos = np.concatenate([hs.pos, newpos])
+                hs.kcodes = np.concatenate([hs.kcodes, kc[h]])
+                hs.kscale = np.concatenate([hs.kscale, ks[h]])
+                hs.vcodes = np.concatenate([hs.vcodes, vc[h]])
+                hs.vscale = np.concatenate([hs.vscale, vs[h]])
+                hs.score = np.concatenate([hs.score, np.zeros(n - first_q)])
+        s.pos_total += n
+
+    # -- read path ----------------------------------------------------------
+    def attend(self, b: int, q: np.ndarray, sm_scale: float | None = None,
+               accumulate: bool = True) -> np.ndarray:
+        """Decode attention of sequence b.  q: fp32 [Hq, D].  Returns fp64
+        [Hq, D].  Query head j reads KV head j // G (consecutive query heads
+        share a KV head).  With ``accumulate`` the H2O scores of every attended
+        token (sinks included) grow by the column sums of this step's
+        probabilities."""
+        s = self.seqs[b]
+        out = np.zeros((self.hq, self.d), np.float64)
+        for h in range(self.hkv):
+            hs = s.heads[h]
+            keys = np.vstack([s.sink_k[h].astype(np.float64), dequantize(hs.kcodes, hs.kscale)])
+            vals = np.vstack([s.sink_v[h].astype(np.float64), dequantize(hs.vcodes, hs.vscale)])
+            qg = q[h * self.group:(h + 1) * self.group]
+            o, p = attention(qg, keys, vals, sm_scale)
+            out[h * self.group:(h + 1) * self.group] = o
+            if accumulate:
+                inc = h2o_increments(p)
+                ns = s.sink_k[h].shape[0]
+                s.sink_score[h] = s.sink_score[h] + inc[:ns]
+                hs.score = hs.score + inc[ns:]
+        return out
+
+    # -- eviction -----------------------------------------------------------
+    def keep_masks(self, b: int, mode: str, budget: int = 0, recent: int = 0,
+                   window: int = 0) -> list:
+        s = self.seqs[b]
+        masks = []
+        for h in range(self.hkv):
+            hs = s.heads[h]
+            ns = s.sink_k[h].shape[0]
+            if mode == "h2o":
+                masks.append(select_h2o(hs.pos, hs.score, s.pos_total, budget, recent, ns))
+            elif mode == "streaming":
+                masks.append(select_streaming(hs.pos, s.pos_total, window, ns))
+            else:
+                raise ValueError(mode)
+        return masks
+
+    def evict(self, b: int, masks: list) -> None:
+        """Drop the tokens whose mask entry is False (order of the rest kept)."""
+        s = self.seqs[b]
+        for h, m in enumerate(masks):
+            hs = s.heads[h]
+            s.heads[h] = HeadState(hs.pos[m], hs.kcodes[m], hs.kscale[m],
+                                   hs.vcodes[m], hs.vscale[m], hs.score[m])
+
+    def kept_positions(self, b: int, h: int) -> np.ndarray:
+        """Sorted positions of the non-sink tokens held for (b, h)."""
+        return np.sort(self.seqs[b].heads[h].pos)
+
+    def load_head(self, b: int, h: int, pos, kcodes, kscale, vcodes, vscale, score) -> None:
+        """Replace the state of (b, h) (lock-step re-synchronisation)."""
+        self.seqs[b].heads[h] = HeadState(np.asarray(pos, np.int64), np.asarray(kcodes, np.int8),
+                                          np.asarray(kscale, np.float32), np.asarray(vcodes, np.int8),
+                                          np.asarray(vscale, np.float32), np.asarray(score, np.float64))

@@ -1,0 +1,376 @@
+"""Pins of the CPU oracle against what the pages and mathematics fix.
+
+Each test ties one oracle function to something other than itself: values the
+pages print, closed forms, worked examples whose scale is exact, library
+witnesses, invariants and brute force on tiny inputs.
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import kvc_oracle as O
+
+
+def _read_table(path):
+    rows = []
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            rows.append(line.split())
+    return rows
+
+
+# --------------------------------------------------------------------------
+# closed form and ratios
+# --------------------------------------------------------------------------
+
+def test_closed_form_matches_printed_and_report(golden_dir):
+    rows = _read_table(os.path.join(golden_dir, "kv_closed_form.txt"))
+    assert len(rows) == 6
+    for src, seq, bpe, gib in rows:
+        got = O.kv_cache_gib(1, int(seq), 32, 32, 128, int(bpe))
+        assert got == pytest.approx(float(gib), abs=0.005), (src, seq)
+    # the report's per-token figure: 0.5 MB for fp16
+    assert O.kv_cache_bytes(1, 1, 32, 32, 128, 2) == 512 * 1024
+
+
+def test_closed_form_scales_linearly():
+    a = O.kv_cache_bytes(3, 100, 2, 5, 128, 2)
+    assert a == 2 * 2 * 5 * 128 * 2 * 3 * 100
+    assert O.kv_cache_bytes(3, 200, 2, 5, 128, 2) == 2 * a
+
+
+def test_compression_ratios_match_checklist(golden_dir):
+    rows = _read_table(os.path.join(golden_dir, "compression_ratios.txt"))
+    x = np.random.default_rng(0).standard_normal((64, 128)).astype(np.float32)
+    bf16_bytes = x.size * 2
+    for name, bits, ratio in rows:
+        bits = int(bits)
+        if bits == 16:
+            stored = bf16_bytes
+        else:
+            codes, _ = O.quantize_rows(x, bits)
+            stored = (O.pack_int4(codes) if bits == 4 else codes).nbytes
+            assert O.stored_bytes_per_token_head(bits, with_scales=False) / (2 * 128 * 2) == float(ratio)
+        assert stored / bf16_bytes == float(ratio), name
+    # with the two fp32 scales per token-head
+    assert O.stored_bytes_per_token_head(8) == 264
+    assert O.stored_bytes_per_token_head(4) == 136
+
+
+# --------------------------------------------------------------------------
+# quantisation
+# --------------------------------------------------------------------------
+
+def test_quant_worked_int8_exact_scale():
+    # amax = 127 makes the scale exactly 1.0, so the codes are the
+    # round-half-to-even of the inputs (torch.round on the page is half-even).
+    row = np.zeros(128, np.float32)
+    vals = [127.0, 2.5, 3.5, -2.5, 0.5, -0.5, 1.5, -126.5, 0.49999997, 100.25]
+    row[:len(vals)] = vals
+    codes, scale = O.quantize_rows(row[None], 8)
+    assert scale[0] == np.float32(1.0)
+    assert codes[0, :len(vals)].tolist() == [127, 2, 4, -2, 0, 0, 2, -126, 0, 100]
+
+
+def test_quant_worked_int4_exact_scale():
+    row = np.zeros(128, np.float32)
+    vals = [7.0, 1.5, 2.5, -3.5, -6.5, 0.5, -7.0]
+    row[:len(vals)] = vals
+    codes, scale = O.quantize_rows(row[None], 4)
+    assert scale[0] == np.float32(1.0)
+    assert codes[0, :len(vals)].tolist() == [7, 2, 2, -4, -6, 0, -7]
+
+
+def test_quant_power_of_two_scale():
+    # amax = 254 -> scale 2.0 exactly; x = 5 -> 2.5 -> 2; x = 7 -> 3.5 -> 4.
+    row = np.zeros(128, np.float32)
+    row[:3] = [254.0, 5.0, 7.0]
+    codes, scale = O.quantize_rows(row[None], 8)
+    assert scale[0] == np.float32(2.0)
+    assert codes[0, :3].tolist() == [127, 2, 4]
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_quant_invariants(bits):
+    rng = np.random.default_rng(1)
+    x = (rng.standard_normal((500, 128)) * rng.uniform(0.01, 50, (500, 1))).astype(np.float32)
+    codes, scale = O.quantize_rows(x, bits)
+    qmax = 127 if bits == 8 else 7
+    # the amax element maps to +-qmax
+    i = np.argmax(np.abs(x), axis=1)
+    top = codes[np.arange(500), i].astype(int)
+    assert np.all(np.abs(top) == qmax)
+    assert np.all(np.sign(top) == np.sign(x[np.arange(500), i]))
+    # codes stay in range
+    assert codes.min() >= -qmax and codes.max() <= qmax
+    # per-element dequantisation error <= scale/2 (+ fp32 division rounding)
+    err = np.abs(x.astype(np.float64) - O.dequantize(codes, scale))
+    bound = scale.astype(np.float64)[:, None] / 2 + np.abs(x.astype(np.float64)) * 2.0 ** -23
+    assert np.all(err <= bound)
+    # scale is amax / qmax in fp32
+    amax = np.abs(x).max(axis=1)
+    assert np.array_equal(scale, (amax / np.float32(qmax)).astype(np.float32))
+
+
+def test_quant_zero_row():
+    codes, scale = O.quantize_rows(np.zeros((2, 128), np.float32), 8)
+    assert np.all(codes == 0) and np.all(scale == 0)
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_quant_torch_witness(bits):
+    # Library witness: the page's per-token quantiser written with torch ops in
+    # fp32 (without the 1e-8 epsilon).
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal((300, 128)).astype(np.float32)
+    x[:, 7] *= 10
+    t = torch.from_numpy(x)
+    qmax = (1 << (bits - 1)) - 1
+    s = t.abs().amax(dim=-1, keepdim=True) / qmax
+    want = torch.round(t / s).clamp(-qmax - 1, qmax).to(torch.int8).numpy()
+    codes, scale = O.quantize_rows(x, bits)
+    assert np.array_equal(codes, want)
+    assert np.array_equal(scale, s[:, 0].numpy())
+
+
+def test_int4_packing_layout_and_roundtrip():
+    codes = np.zeros(128, np.int8)
+    codes[:4] = [1, -1, -8, 7]
+    p = O.pack_int4(codes[None])[0]
+    assert p[0] == 0xF1 and p[1] == 0x78
+    rng = np.random.default_rng(3)
+    c = rng.integers(-8, 8, (10, 128)).astype(np.int8)
+    assert np.array_equal(O.unpack_int4(O.pack_int4(c)), c)
+
+
+def test_quant_rejects_bits():
+    with pytest.raises(ValueError):
+        O.quantize_rows(np.ones((1, 128), np.float32), 2)
+
+
+def test_bf16_widening_exact():
+    bits = np.array([0x3F80, 0xC000, 0x0000, 0x4049], np.uint16)
+    assert O.bf16_bits_to_f32(bits).tolist() == [1.0, -2.0, 0.0, 3.140625]
+
+
+# --------------------------------------------------------------------------
+# attention
+# --------------------------------------------------------------------------
+
+def test_attention_sdpa_witness():
+    rng = np.random.default_rng(4)
+    q = rng.standard_normal((5, 128))
+    k = rng.standard_normal((37, 128)) * 2
+    v = rng.standard_normal((37, 128))
+    out, probs = O.attention(q, k, v)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q)[None], torch.from_numpy(k)[None], torch.from_numpy(v)[None])[0]
+    assert np.allclose(out, ref.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.allclose(probs.sum(axis=1), 1.0)
+
+
+def test_attention_bruteforce_loops():
+    rng = np.random.default_rng(5)
+    d = 8
+    q = rng.standard_normal((2, d))
+    k = rng.standard_normal((5, d))
+    v = rng.standard_normal((5, d))
+    out, _ = O.attention(q, k, v)
+    for g in range(2):
+        w = [math.exp(sum(q[g, i] * k[t, i] for i in range(d)) / math.sqrt(d)) for t in range(5)]
+        z = sum(w)
+        for j in range(d):
+            assert out[g, j] == pytest.approx(sum(w[t] * v[t, j] for t in range(5)) / z, rel=1e-12)
+
+
+def test_attention_equal_keys_gives_mean_values():
+    rng = np.random.default_rng(6)
+    k = np.tile(rng.standard_normal(128), (20, 1))
+    v = rng.standard_normal((20, 128))
+    out, _ = O.attention(rng.standard_normal((3, 128)), k, v)
+    assert np.allclose(out, v.mean(axis=0)[None], atol=1e-12)
+
+
+def test_attention_planted_token_dominates():
+    rng = np.random.default_rng(7)
+    q = rng.standard_normal((1, 128))
+    k = rng.standard_normal((50, 128)) * 0.1
+    k[17] = q[0] * (30 * math.sqrt(128) / float(q[0] @ q[0]))  # logit +30
+    v = rng.standard_normal((50, 128))
+    out, probs = O.attention(q, k, v)
+    assert probs[0, 17] > 1 - 1e-10
+    assert np.allclose(out[0], v[17], atol=1e-9)
+
+
+def test_attention_permutation_invariant():
+    rng = np.random.default_rng(8)
+    q, k, v = rng.standard_normal((4, 128)), rng.standard_normal((33, 128)), rng.standard_normal((33, 128))
+    perm = rng.permutation(33)
+    a, pa = O.attention(q, k, v)
+    b, pb = O.attention(q, k[perm], v[perm])
+    assert np.allclose(a, b, atol=1e-13)
+    assert np.allclose(pa[:, perm], pb, atol=1e-15)
+
+
+def _fill_cache(bits, B, Hq, Hkv, T, seed):
+    rng = np.random.default_rng(seed)
+    c = O.OracleCache(B, Hq, Hkv, bits)
+    k = rng.standard_normal((B, Hkv, T, 128)).astype(np.float32)
+    v = rng.standard_normal((B, Hkv, T, 128)).astype(np.float32)
+    for b in range(B):
+        c.append(b, k[b], v[b])
+    return c, k, v, rng
+
+
+def test_gqa_grouping_matches_repeat_interleave():
+    # Query head j reads KV head j // G: the layout transformers and vLLM use
+    # (repeat_interleave of the KV heads), checked through torch sdpa.
+    B, Hq, Hkv, T = 1, 6, 2, 23
+    c, k, v, rng = _fill_cache(8, B, Hq, Hkv, T, 9)
+    q = rng.standard_normal((Hq, 128)).astype(np.float32)
+    out = c.attend(0, q, accumulate=False)
+    hs = c.seqs[0]
+    keys, vals = [], []
+    for h in range(Hkv):
+        keys.append(np.vstack([hs.sink_k[h], O.dequantize(hs.heads[h].kcodes, hs.heads[h].kscale)]))
+        vals.append(np.vstack([hs.sink_v[h], O.dequantize(hs.heads[h].vcodes, hs.heads[h].vscale)]))
+    K = torch.from_numpy(np.stack(keys)).double().repeat_interleave(Hq // Hkv, dim=0)
+    V = torch.from_numpy(np.stack(vals)).double().repeat_interleave(Hq // Hkv, dim=0)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q).double()[:, None, :], K, V)[:, 0, :]
+    assert np.allclose(out, ref.numpy(), atol=1e-12)
+
+
+def test_sinks_stored_exactly_and_rest_quantised():
+    c, k, v, _ = _fill_cache(8, 1, 2, 2, 9, 10)
+    s = c.seqs[0]
+    for h in range(2):
+        assert np.array_equal(s.sink_k[h], k[0, h, :4])
+        assert np.array_equal(s.sink_v[h], v[0, h, :4])
+        assert s.heads[h].pos.tolist() == list(range(4, 9))
+        codes, scale = O.quantize_rows(k[0, h, 4:], 8)
+        assert np.array_equal(s.heads[h].kcodes, codes)
+        assert np.array_equal(s.heads[h].kscale, scale)
+
+
+def test_short_context_all_sinks():
+    c, k, v, rng = _fill_cache(8, 1, 1, 1, 3, 11)
+    assert c.seqs[0].heads[0].pos.size == 0
+    q = rng.standard_normal((1, 128)).astype(np.float32)
+    out = c.attend(0, q)
+    ref, _ = O.attention(q, k[0, 0], v[0, 0])
+    assert np.allclose(out, ref, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# scores and selection
+# --------------------------------------------------------------------------
+
+def test_score_increments_sum_to_group_size():
+    B, Hq, Hkv, T = 2, 8, 2, 40
+    c, _, _, rng = _fill_cache(8, B, Hq, Hkv, T, 12)
+    for step in range(3):
+        before = [[c.seqs[b].heads[h].score.sum() + c.seqs[b].sink_score[h].sum() for h in range(Hkv)]
+                  for b in range(B)]
+        for b in range(B):
+            c.attend(b, rng.standard_normal((Hq, 128)).astype(np.float32))
+        for b in range(B):
+            for h in range(Hkv):
+                tot = c.seqs[b].heads[h].score.sum() + c.seqs[b].sink_score[h].sum()
+                assert tot - before[b][h] == pytest.approx(Hq // Hkv, abs=1e-12)
+
+
+def _brute_select(pos, score, pos_total, budget, recent):
+    n = len(pos)
+    if 4 + n <= budget:
+        return set(pos)
+    keep = {p for p in pos if p >= pos_total - recent}
+    cand = sorted(((-s, p) for p, s in zip(pos, score) if p < pos_total - recent))
+    keep |= {p for _, p in cand[:budget - 4 - recent]}
+    return keep
+
+
+def test_select_h2o_bruteforce():
+    rng = np.random.default_rng(13)
+    for trial in range(200):
+        n = int(rng.integers(0, 30))
+        pos_total = 4 + n + int(rng.integers(0, 5))
+        pos = rng.choice(np.arange(4, pos_total), size=n, replace=False)
+        # make the recent window fully present, as it always is in the cache
+        recent = int(rng.integers(0, 6))
+        pos = np.unique(np.concatenate([pos, np.arange(max(4, pos_total - recent), pos_total)]))
+        rng.shuffle(pos)
+        score = rng.integers(0, 4, size=pos.size).astype(np.float64)  # many ties
+        budget = 4 + recent + int(rng.integers(0, 10))
+        keep = O.select_h2o(pos, score, pos_total, budget, recent)
+        assert set(pos[keep].tolist()) == _brute_select(pos.tolist(), score.tolist(), pos_total, budget, recent)
+        if 4 + pos.size > budget:
+            assert keep.sum() == budget - 4
+
+
+def test_select_ties_go_to_lower_position():
+    pos = np.array([10, 5, 7, 20, 21])
+    score = np.array([1.0, 1.0, 1.0, 0.0, 0.0])
+    keep = O.select_h2o(pos, score, pos_total=22, budget=4 + 2 + 2, recent=2)
+    assert sorted(pos[keep].tolist()) == [5, 7, 20, 21]
+
+
+def test_streaming_rule_exact():
+    for n_total, window in [(5000, 2048), (2053, 2048), (2052, 2048), (100, 2048), (40, 8)]:
+        pos = np.arange(4, n_total)
+        keep = O.select_streaming(pos, n_total, window)
+        kept = pos[keep].tolist()
+        if n_total - 4 <= window:
+            assert kept == list(range(4, n_total))
+        else:
+            assert kept == list(range(n_total - window, n_total))
+            assert len(kept) == window
+
+
+def test_identity_budget_covers_context():
+    # Evicting nothing must equal full attention by brute force.
+    B, Hq, Hkv, T = 1, 4, 2, 30
+    c, k, v, rng = _fill_cache(8, B, Hq, Hkv, T, 14)
+    q = rng.standard_normal((Hq, 128)).astype(np.float32)
+    out = c.attend(0, q)
+    masks = c.keep_masks(0, "h2o", budget=4 + T, recent=8)
+    assert all(m.all() for m in masks)
+    c.evict(0, masks)
+    out2 = c.attend(0, q, accumulate=False)
+    assert np.array_equal(out, out2)
+    s = c.seqs[0]
+    for h in range(Hkv):
+        keys = np.vstack([k[0, h, :4], O.dequantize(*O.quantize_rows(k[0, h, 4:], 8))])
+        vals = np.vstack([v[0, h, :4], O.dequantize(*O.quantize_rows(v[0, h, 4:], 8))])
+        for g in range(2):
+            qq = q[h * 2 + g].astype(np.float64)
+            w = np.exp(keys @ qq / math.sqrt(128) - (keys @ qq / math.sqrt(128)).max())
+            assert np.allclose(out[h * 2 + g], (w[:, None] * vals).sum(0) / w.sum(), atol=1e-12)
+
+
+def test_planted_heavy_hitters_kept_tiny_workload():
+    # Tiny single-layer workload: every planted token outside the sinks and the
+    # recent window survives the first eviction (10 planted <= 92 heavy places).
+    from compressed_kv_cache_kvc_gb300 import workloads as W
+    w = W.WORKLOADS["tiny_b1_h8_t512_int8_h2o"]
+    d = W.gen_layer(w, 0)
+    c = O.OracleCache(w.batch, w.num_q_heads, w.num_kv_heads, w.bits)
+    f = O.bf16_bits_to_f32
+    c.append(0, f(d["k"][0]), f(d["v"][0]))
+    c.append(0, f(d["k_new"][0]), f(d["v_new"][0]))
+    c.attend(0, f(d["q"][0]))
+    masks = c.keep_masks(0, "h2o", budget=w.budget, recent=w.recent)
+    c.evict(0, masks)
+    p_total = w.context + 1
+    for h in range(w.num_kv_heads):
+        kept = set(c.kept_positions(0, h).tolist())
+        assert len(kept) == w.budget - 4
+        planted = set(np.nonzero(d["planted"][0, h])[0].tolist())
+        assert planted and planted <= kept | set(range(p_total - w.recent, p_total))
