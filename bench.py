@@ -1,0 +1,442 @@
+"""Benchmark of the compressed-KV decode step on GB300.
+
+A step is one decode step of the whole stack: for every layer,
+quantize-append of the new token, fused-dequant paged decode attention with
+H2O score accumulation, sink/recent/top-k selection and compaction.  The
+workload is the Qwen2.5-14B-shaped stack (48 layers, batch 32, 40 query / 8 KV
+heads, head_dim 128, context 8192, INT4 per-token codes with bf16 sinks, H2O
+budget 2457 = 4 sinks + 512 recent + 1941 heavy hitters), synthetic seeded
+inputs.  Every step starts from the same pre-step state: a device snapshot of
+all layers' caches is copied back before each step, outside the timed region;
+that 14 GB copy also flushes the 129 MB L2, so each timed step reads its KV
+from HBM.
+
+Metric: KV bytes the decode attention must read per step (codes + fp32 scales
+of every pool slot, bf16 sinks) divided by the step time, GB/s; also
+sequence-steps per second.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "qwen14b_b32_gqa5_t8192_int4_h2o_48l"
+METRIC = "decode-attention KV bytes read GB/s (% of GB300 HBM peak); seq·steps/s"
+
+
+def kv_read_bytes_per_step(w, slots_per_head: int, layers: int) -> int:
+    """Algorithmic KV bytes the attention reads in one step: per (sequence, KV
+    head) every pool slot's K and V codes and fp32 scales, plus the 4 bf16
+    sinks' K and V."""
+    per_slot = 2 * (128 * w.bits // 8) + 2 * 4
+    sinks = 4 * 2 * 128 * 2
+    return layers * w.batch * w.num_kv_heads * (slots_per_head * per_slot + sinks)
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (one process per GPU; independent replicas, no
+# collective on the data path)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def shard_range(total: int, world: int, rank: int) -> tuple[int, int]:
+    """Contiguous slice [begin, end) of `total` units for `rank`."""
+    base, extra = divmod(total, world)
+    begin = rank * base + min(rank, extra)
+    return begin, begin + base + (1 if rank < extra else 0)
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle leg (bounded sample of the same workload)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(n_seq: int = 1, reps: int = 1, layer: int = 0):
+    """Time the oracle's decode step on `n_seq` sequences x 8 KV heads of one
+    layer at full context.  Returns (seconds, kv_bytes_read, description)."""
+    import copy
+
+    import numpy as np
+
+    from compressed_kv_cache_kvc_gb300 import workloads as W
+    from oracle import kvc_oracle as O
+    w = W.WORKLOADS[WORKLOAD]
+    d = W.gen_layer(w, layer, batch=n_seq)
+    f = O.bf16_bits_to_f32
+    base = O.OracleCache(n_seq, w.num_q_heads, w.num_kv_heads, w.bits)
+    for b in range(n_seq):
+        base.append(b, f(d["k"][b]), f(d["v"][b]))
+    total = 0.0
+    for _ in range(reps):
+        c = copy.deepcopy(base)
+        t0 = time.perf_counter()
+        for b in range(n_seq):
+            c.append(b, f(d["k_new"][b]), f(d["v_new"][b]))
+            c.attend(b, f(d["q"][b]))
+            c.evict(b, c.keep_masks(b, "h2o", budget=w.budget, recent=w.recent))
+        total += time.perf_counter() - t0
+    slots = w.context + 1 - 4
+    per_seq = kv_read_bytes_per_step(w, slots, 1) // w.batch
+    desc = (f"oracle decode step (append, fp64 attention + H2O, select, evict) of {n_seq} sequence(s) x "
+            f"{w.num_kv_heads} KV heads of one layer at context {w.context}, {reps} rep(s), 1 thread")
+    return total, per_seq * n_seq * reps, desc
+
+
+def run_oracle_child(n_seq: int, reps: int):
+    """Run oracle_sample in a fresh single-threaded process."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"
+    p = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-child", str(n_seq), str(reps)],
+                       capture_output=True, text=True, env=env, timeout=1800)
+    if p.returncode != 0:
+        raise RuntimeError(p.stderr[-2000:])
+    return json.loads(p.stdout.strip().splitlines()[-1])
+
+
+def reference_arm(args):
+    """--impl reference: the oracle timed on the host cores, same metric."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from compressed_kv_cache_kvc_gb300 import workloads as W
+    w = W.WORKLOADS[WORKLOAD]
+    n_seq = 1
+    for _ in range(args.warmup):
+        run_oracle_child(n_seq, 1)
+    secs, nbytes = 0.0, 0
+    desc = ""
+    for _ in range(args.steps):
+        r = run_oracle_child(n_seq, 1)
+        secs += r["seconds"]
+        nbytes += r["bytes"]
+        desc = r["desc"]
+    gbs = nbytes / secs / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "batch": w.batch, "context": w.context,
+                                            "layers": w.layers, "sample": desc},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def gpu_arm(args):
+    import numpy as np
+    import torch
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    from compressed_kv_cache_kvc_gb300 import workloads as W
+    from compressed_kv_cache_kvc_gb300.build import build_library
+    build_library()
+    from compressed_kv_cache_kvc_gb300.cache import KVCache
+
+    w = W.WORKLOADS[WORKLOAD]
+    layers = args.layers or w.layers
+    B, Hq, Hkv, T = w.batch, w.num_q_heads, w.num_kv_heads, w.context
+    mbps = (T + 1 + 15) // 16 + 1
+    nblocks = B * mbps
+    caches, snaps, inputs = [], [], []
+    for l in range(layers):
+        c = KVCache(Hq, Hkv, w.bits, nblocks, B, mbps, device=dev)
+        q, k, v, kn, vn = W.gen_layer_torch(w, l + 1000 * rank, dev)
+        c.quantize_append(k, v)
+        del k, v
+        torch.cuda.synchronize()
+        caches.append(c)
+        snaps.append(c.state_view.clone())
+        inputs.append((q, kn, vn))
+    torch.cuda.synchronize()
+    ws_buf = caches[0].workspace(B)
+    for c in caches:
+        c._ws[ws_buf.numel()] = ws_buf
+    mask = caches[0].new_keep_mask(B)
+    outs = [torch.empty(B, Hq, 128, dtype=torch.bfloat16, device=dev) for _ in range(layers)]
+    slots0 = caches[0].lengths(0)[0]  # pool slots before the step's append
+    kv_bytes = kv_read_bytes_per_step(w, slots0 + 1, layers)
+
+    def restore():
+        for c, s in zip(caches, snaps):
+            c.state_view.copy_(s, non_blocking=True)
+
+    def step(stream=None):
+        n = 0
+        for l, c in enumerate(caches):
+            q, kn, vn = inputs[l]
+            c.quantize_append(kn, vn, stream=stream)
+            n += c.last_launch_count()
+            c.decode_attention(q, out=outs[l], workspace=ws_buf, stream=stream)
+            n += c.last_launch_count()
+            c.h2o_select_evict(B, "h2o", budget=w.budget, recent=w.recent, keep_mask=mask, workspace=ws_buf,
+                               stream=stream)
+            n += c.last_launch_count()
+            c.compact_blocks(mask, B, workspace=ws_buf, stream=stream)
+            n += c.last_launch_count()
+        return n
+
+    def resync():
+        for c in caches:
+            c.sync_host()
+
+    # trace events around every layer's split-K attention kernel
+    tr = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(layers)]
+    for c, (a, b) in zip(caches, tr):
+        a.record()
+        b.record()  # creates the underlying CUDA events
+        c.set_trace_events(a, b)
+
+    stream = torch.cuda.Stream(device=dev)
+    # eager warm-up (sets kernel attributes), then capture one step
+    launches = 0
+    for _ in range(max(1, args.warmup)):
+        restore()
+        torch.cuda.synchronize()
+        resync()
+        with torch.cuda.stream(stream):
+            launches = step()
+        torch.cuda.synchronize()
+    graph = None
+    if not args.eager:
+        restore()
+        torch.cuda.synchronize()
+        resync()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        torch.cuda.synchronize()
+        for _ in range(args.warmup):
+            restore()
+            torch.cuda.synchronize()
+            graph.replay()
+        torch.cuda.synchronize()
+
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    barrier(ws)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    step_ms, attn_ms = [], []
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            restore()
+            if graph is None:
+                torch.cuda.synchronize()
+                resync()
+            ev0.record(stream)
+            if graph is not None:
+                graph.replay()
+            else:
+                step()
+            ev1.record(stream)
+            ev1.synchronize()
+            step_ms.append(ev0.elapsed_time(ev1))
+            attn_ms.extend(a.elapsed_time(b) for a, b in tr)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clocks = sampler.stop() if sampler else None
+    total_ms = sum(step_ms)
+    total_ms_max = reduce_max(total_ms, ws, dev)
+    ms_per_step = total_ms_max / args.steps
+    value = kv_bytes * ws / (ms_per_step * 1e-3) / 1e9
+    seq_steps = B * ws / (ms_per_step * 1e-3)
+    attn_avg_ms = sum(attn_ms) / len(attn_ms)
+    attn_bytes = kv_bytes // layers
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        pass
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    achieved = attn_bytes / (attn_avg_ms * 1e-3) / 1e9
+
+    # e2e through the public API with host buffers: per step, H2D of every
+    # layer's query and new K/V from pinned memory, the step, D2H of outputs
+    h_in = [tuple(t.cpu().pin_memory() for t in inp) for inp in inputs]
+    h_out = [torch.empty(B, Hq, 128, dtype=torch.bfloat16).pin_memory() for _ in range(layers)]
+    d_in = [tuple(torch.empty_like(t) for t in inp) for inp in inputs]
+    h2d = sum(t.numel() * t.element_size() for inp in h_in for t in inp)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    e2e_ms = []
+    e_steps = max(1, min(args.steps, 10))
+    with torch.cuda.stream(stream):
+        for _ in range(e_steps):
+            restore()
+            torch.cuda.synchronize()
+            resync()
+            ev0.record(stream)
+            for l, c in enumerate(caches):
+                for dst, src in zip(d_in[l], h_in[l]):
+                    dst.copy_(src, non_blocking=True)
+                q, kn, vn = d_in[l]
+                c.step(q, kn, vn, mode="h2o", budget=w.budget, recent=w.recent, out=outs[l], keep_mask=mask)
+                h_out[l].copy_(outs[l], non_blocking=True)
+            ev1.record(stream)
+            ev1.synchronize()
+            e2e_ms.append(ev0.elapsed_time(ev1))
+    e2e_step = reduce_max(sum(e2e_ms), ws, dev) / e_steps
+    e2e_value = kv_bytes * ws / (e2e_step * 1e-3) / 1e9
+    for c in caches:
+        st = c.read_status()
+        if st:
+            raise RuntimeError(f"device status {st:#x}")
+
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline and ws == 1:
+        r = run_oracle_child(1, 1)
+        cpu = {"value": r["bytes"] / r["seconds"] / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": r["desc"], "seconds": r["seconds"]}
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "attn_split_int4_traffic.json")
+    if os.path.exists(tpath):
+        try:
+            tj = json.load(open(tpath))
+            traffic = tj.get("dram_bytes_per_launch")
+        except (OSError, ValueError):
+            traffic = None
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int4-codes/f16-mma/f32-accum", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": B, "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": 128,
+                   "context": T, "layers": layers, "bits": w.bits, "budget": w.budget, "recent": w.recent,
+                   "parallelism": f"replicas{ws}", "l2": "state restore copy (>L2) between timed steps",
+                   "cuda_graph": graph is not None},
+        "seq_steps_per_s": seq_steps,
+        "kv_bytes_per_step": kv_bytes,
+        "frac_of_hbm_peak": value / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "kernel": "attn_split_kernel<4>", "bytes_per_launch": attn_bytes,
+                     "avg_launch_ms": attn_avg_ms, "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_step, "path": "KVCache.step per layer, eager, pinned host buffers"},
+        "gpu_launches": launches * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling only)")
+    ap.add_argument("--eager", action="store_true", help="launch each call instead of replaying a CUDA graph")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-child", nargs=2, type=int, default=None, help=argparse.SUPPRESS)
+    args = ap.parse_args()
+    if args.oracle_child is not None:
+        secs, nbytes, desc = oracle_sample(args.oracle_child[0], args.oracle_child[1])
+        print(json.dumps({"seconds": secs, "bytes": nbytes, "desc": desc}))
+        return
+    if args.impl == "reference":
+        reference_arm(args)
+        return
+    gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,152 @@
+// Quantise-on-write of new tokens into the paged pool.
+//
+// Per (token, KV head) row of K and of V ("KV Cache optimization techniques",
+// section 1.2 per-token quantisation; Technical Report section 3.2): amax over
+// the 128 values, scale = amax / qmax in IEEE fp32, code = round-half-even of
+// x / scale (IEEE fp32 division), clamped.  Positions 0..3 are attention sinks
+// and are copied unchanged in bf16 (Technical Report section 3.2).
+//
+// One CTA per sequence: thread 0 takes the pages the new tokens need from the
+// device free-block stack and advances the sequence lengths; after a barrier
+// every warp quantises rows (one warp per 128-value row, 4 values per lane).
+#include "kvc_internal.h"
+
+namespace kvc {
+namespace {
+
+__device__ __forceinline__ float bf16_to_f32(uint32_t bits16) {
+  return __uint_as_float(bits16 << 16);
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(512) append_kernel(DevState s, int seq_begin, int n_new,
+                                                     const uint16_t* __restrict__ kin,
+                                                     const uint16_t* __restrict__ vin) {
+  const int bl = blockIdx.x;
+  const int b = seq_begin + bl;
+  __shared__ int sh_slots, sh_pos, sh_ok;
+  if (threadIdx.x == 0) {
+    const int slots = s.seq_slots[b];
+    const int pos = s.seq_pos[b];
+    const int n_sink_new = min(n_new, max(0, kSinks - pos));
+    const int new_slots = slots + (n_new - n_sink_new);
+    const int old_pages = (slots + kPage - 1) / kPage;
+    const int new_pages = (new_slots + kPage - 1) / kPage;
+    const int need = new_pages - old_pages;
+    int ok = 1;
+    if (new_pages > s.max_bps) {
+      atomicOr(&s.counters[kCtrStatus], kDevTableOverflow);
+      ok = 0;
+    } else if (need > 0) {
+      const int top = atomicSub(&s.counters[kCtrFreeTop], need);
+      if (top - need < 0 || top > s.num_blocks) {
+        atomicAdd(&s.counters[kCtrFreeTop], need);
+        atomicOr(&s.counters[kCtrStatus], kDevOutOfBlocks);
+        ok = 0;
+      } else {
+        int32_t* row = s.block_table + (size_t)b * s.max_bps;
+        for (int j = 0; j < need; ++j) row[old_pages + j] = s.free_stack[top - 1 - j];
+      }
+    }
+    if (ok) {
+      s.seq_slots[b] = new_slots;
+      s.seq_pos[b] = pos + n_new;
+    }
+    sh_slots = slots;
+    sh_pos = pos;
+    sh_ok = ok;
+  }
+  __syncthreads();
+  if (!sh_ok) return;
+
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int hkv = s.hkv;
+  const int total_rows = n_new * hkv * 2;
+  const int first_quant_pos = max(sh_pos, kSinks);
+  constexpr float kQmax = BITS == 8 ? 127.0f : 7.0f;
+  constexpr int kLo = BITS == 8 ? -127 : -8;
+  constexpr int kHi = BITS == 8 ? 127 : 7;
+
+  for (int row = warp; row < total_rows; row += nwarps) {
+    const int kv = row & 1;
+    const int h = (row >> 1) % hkv;
+    const int i = (row >> 1) / hkv;
+    const uint16_t* src = (kv ? vin : kin) + (((size_t)bl * hkv + h) * n_new + i) * kHeadDim;
+    const uint2 raw = *reinterpret_cast<const uint2*>(src + lane * 4);
+    const int p = sh_pos + i;
+    if (p < kSinks) {
+      uint16_t* dst = (kv ? s.sink_v : s.sink_k) + (((size_t)b * hkv + h) * kSinks + p) * kHeadDim;
+      *reinterpret_cast<uint2*>(dst + lane * 4) = raw;
+      if (kv == 0 && lane == 0) s.sink_score[((size_t)b * hkv + h) * kSinks + p] = 0.0f;
+      continue;
+    }
+    float x[4];
+    x[0] = bf16_to_f32(raw.x & 0xFFFFu);
+    x[1] = bf16_to_f32(raw.x >> 16);
+    x[2] = bf16_to_f32(raw.y & 0xFFFFu);
+    x[3] = bf16_to_f32(raw.y >> 16);
+    float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float scale = __fdiv_rn(amax, kQmax);
+    int c[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      int q = 0;
+      if (scale > 0.0f) q = __float2int_rn(__fdiv_rn(x[e], scale));
+      c[e] = min(max(q, kLo), kHi);
+    }
+    const int slot = sh_slots + (p - first_quant_pos);
+    const int page = slot / kPage;
+    const int off = slot % kPage;
+    const int blk = s.block_table[(size_t)b * s.max_bps + page];
+    if ((unsigned)blk >= (unsigned)s.num_blocks) {
+      if (lane == 0) atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
+      continue;
+    }
+    const size_t sidx = ((size_t)blk * hkv + h) * kPage + off;
+    uint8_t* codes = (kv ? s.v_codes : s.k_codes) + sidx * s.row_bytes;
+    if (BITS == 8) {
+      const uint32_t packed = (uint32_t)(c[0] & 0xFF) | ((uint32_t)(c[1] & 0xFF) << 8) |
+                              ((uint32_t)(c[2] & 0xFF) << 16) | ((uint32_t)(c[3] & 0xFF) << 24);
+      *reinterpret_cast<uint32_t*>(codes + lane * 4) = packed;
+    } else {
+      const uint32_t packed = (uint32_t)(c[0] & 0xF) | ((uint32_t)(c[1] & 0xF) << 4) |
+                              ((uint32_t)(c[2] & 0xF) << 8) | ((uint32_t)(c[3] & 0xF) << 12);
+      *reinterpret_cast<uint16_t*>(codes + lane * 2) = (uint16_t)packed;
+    }
+    if (lane == 0) {
+      (kv ? s.v_scale : s.k_scale)[sidx] = scale;
+      if (kv == 0) {
+        s.slot_pos[sidx] = p;
+        s.score[sidx] = 0.0f;
+      }
+    }
+  }
+}
+
+__global__ void fill_free_stack_kernel(int32_t* stack, int n) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) stack[i] = n - 1 - i;
+}
+
+}  // namespace
+
+cudaError_t launch_append(const DevState& s, int seq_begin, int batch, int n_new, const uint16_t* k,
+                          const uint16_t* v, cudaStream_t st) {
+  const int rows = n_new * s.hkv * 2;
+  int threads = 32 * min(16, max(1, rows));
+  if (s.bits == 8)
+    append_kernel<8><<<batch, threads, 0, st>>>(s, seq_begin, n_new, k, v);
+  else
+    append_kernel<4><<<batch, threads, 0, st>>>(s, seq_begin, n_new, k, v);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fill_free_stack(const DevState& s, cudaStream_t st) {
+  fill_free_stack_kernel<<<64, 256, 0, st>>>(s.free_stack, s.num_blocks);
+  return cudaGetLastError();
+}
+
+}  // namespace kvc

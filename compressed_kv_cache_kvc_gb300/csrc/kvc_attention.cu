@@ -1,0 +1,607 @@
+// Split-K paged decode attention with the dequantisation fused into QK^T and
+// PV, and the online-softmax merge with the bf16 attention sinks and the H2O
+// score accumulation.
+//
+// The method: out = softmax(q K^T / sqrt(d)) V (Technical Report, section
+// 1.1), where the pool's keys and values are code * scale (section 3.2, "scores
+// = Q @ (K_q * scale_k).T / sqrt(d); out = softmax(scores) @ (V_q * scale_v)")
+// and the four sinks are bf16 (section 3.2).  H2O adds each token's softmax
+// probability, summed over the query heads of its KV head, to its score
+// (section 3.4).
+//
+// GB300 design
+//   * Grid (split, kv-head, sequence).  A split is a run of 16-token pages of
+//     one (sequence, KV head); its 4 warps take pages round-robin.
+//   * Each warp streams its pages through a private ring of shared-memory
+//     stages with cp.async (16-byte, coalesced: a K or V page of one head is
+//     one contiguous 2 KB (INT8) / 1 KB (INT4) run of the pool).
+//   * Codes are exact small integers, so they are converted to fp16 exactly
+//     (byte-permute + magic-number subtraction, the integer-to-float trick of
+//     Kim et al., "Who Says Elephants Can't Run", 2022) and fed straight from
+//     registers to mma.sync m16n8k16 (fp16 in, fp32 accumulate).  QK^T puts the
+//     16 tokens of a page on M and the G <= 8 query heads on N; PV puts 16
+//     head-dim rows on M and the query heads on N, with P transposed in
+//     registers by movmatrix.  The head-dim order inside a lane is permuted
+//     consistently for Q and K (a dot product does not depend on it).
+//   * The per-token scales stay out of the inner products: logit =
+//     (q' . c) * scale_k * (sm_scale * log2 e * 2^-e_q), and the PV operand is
+//     p * scale_v * 2^-E.  q' = q * 2^e_q and the warp-wide power of two 2^-E
+//     keep both fp16 operands in range without rounding q.
+//   * Online softmax per warp in the log2 domain with a lazy rescale (the
+//     running max moves only when a page exceeds it by 4), then a CTA-level
+//     merge of the warps; the split partials (m, l, o) go to the workspace and
+//     a second kernel merges the splits and the sinks.
+//   * With H2O on, the split kernel writes each slot's fp32 logits; the merge
+//     kernel, once the global (max, sum) of every query head is known, adds
+//     sum_g exp2(logit - M_g) / L_g to every slot's score.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kvc_internal.h"
+
+namespace kvc {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr float kNegBig = -1.0e30f;
+constexpr float kLazy = 4.0f;  // log2 units the running max may lag
+
+template <int BITS>
+struct Geom {
+  static constexpr int kRowBytes = BITS * 16;           // 128 (INT8) or 64 (INT4)
+  static constexpr int kKBytes = BITS == 8 ? 2048 : 1024;
+  static constexpr int kVBytes = BITS == 8 ? 2048 : 1024;
+  static constexpr int kStage = kKBytes + kVBytes + 128;  // + 16 K scales + 16 V scales
+  static constexpr int kStages = BITS == 8 ? 4 : 6;
+  static constexpr int kSmem = kWarps * kStages * kStage;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(src));
+}
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(smem_u32(dst)), "l"(src));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 4 INT8 codes (bytes b0..b3 of w, already XOR 0x80) -> fp16x2 (b0, b1) and (b2, b3).
+__device__ __forceinline__ void i8x4_to_h2(uint32_t wx, uint32_t& lo, uint32_t& hi) {
+  lo = hsub2(prmt(wx, 0x64646464u, 0x4140u), 0x64806480u);
+  hi = hsub2(prmt(wx, 0x64646464u, 0x4342u), 0x64806480u);
+}
+// Byte k of x and byte k of y (INT8 codes) -> fp16x2 (x_k, y_k).
+__device__ __forceinline__ uint32_t i8_pair_to_h2(uint32_t x, uint32_t y, uint32_t sel) {
+  return hsub2((prmt(x, y, sel) & 0x00FF00FFu) ^ 0x64806480u, 0x64806480u);
+}
+// Low nibbles of the two 16-bit halves (INT4 codes) -> fp16x2.
+__device__ __forceinline__ uint32_t i4_lo_to_h2(uint32_t v) {
+  return hsub2((v & 0x000F000Fu) ^ 0x64086408u, 0x64086408u);
+}
+// Bits 4..7 of the two 16-bit halves (INT4 codes) -> fp16x2.
+__device__ __forceinline__ uint32_t i4_hi_to_h2(uint32_t v) {
+  return hfma2((v & 0x00F000F0u) ^ 0x64806480u, 0x2C002C00u /* 1/16 */, 0xD480D480u /* -72 */);
+}
+
+__device__ __forceinline__ float bf16f(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+
+// Unbiased exponent of a positive normal float (floor(log2 x)).
+__device__ __forceinline__ int exponent_of(float x) {
+  return (int)((__float_as_uint(x) >> 23) & 0xFF) - 127;
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int seq_begin,
+                                                                 const uint16_t* __restrict__ q,
+                                                                 float qk_scale_log2, AttnWork w,
+                                                                 int spill) {
+  using Gm = Geom<BITS>;
+  constexpr int STAGES = Gm::kStages;
+  const int split = blockIdx.x;
+  const int h = blockIdx.y;
+  const int bl = blockIdx.z;
+  const int b = seq_begin + bl;
+  const int S = s.seq_slots[b];
+  const int n_pages = (S + kPage - 1) / kPage;
+  const int pg_begin = split * w.pages_per_split;
+  if (pg_begin >= n_pages) return;
+  const int pg_end = min(n_pages, pg_begin + w.pages_per_split);
+  const int G = s.group;
+  const int hkv = s.hkv;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int r = lane >> 2;
+  const int c = lane & 3;
+
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint8_t* ring = smem + warp * STAGES * Gm::kStage;
+
+  // ---- query fragments (B operand of QK^T), scaled by 2^e_g into fp16 range.
+  uint32_t bq[8][2];
+  float cq0, cq1;
+  {
+    float qv[32];
+    const int g = r;
+    if (g < G) {
+      const uint4* src = reinterpret_cast<const uint4*>(q + ((size_t)bl * s.hq + h * G + g) * kHeadDim + 32 * c);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 u = src[i];
+        const uint32_t ws[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          qv[8 * i + 2 * j] = bf16f(ws[j] & 0xFFFFu);
+          qv[8 * i + 2 * j + 1] = bf16f(ws[j] >> 16);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) qv[i] = 0.0f;
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(qv[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    int e = 0;
+    if (amax > 0.0f) e = min(max(14 - exponent_of(amax), -100), 100);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) qv[i] = ldexpf(qv[i], e);
+    if (BITS == 8) {
+#pragma unroll
+      for (int st = 0; st < 8; ++st) {
+        bq[st][0] = pack_half2(qv[4 * st + 0], qv[4 * st + 1]);
+        bq[st][1] = pack_half2(qv[4 * st + 2], qv[4 * st + 3]);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        bq[2 * i][0] = pack_half2(qv[8 * i + 0], qv[8 * i + 4]);
+        bq[2 * i][1] = pack_half2(qv[8 * i + 1], qv[8 * i + 5]);
+        bq[2 * i + 1][0] = pack_half2(qv[8 * i + 2], qv[8 * i + 6]);
+        bq[2 * i + 1][1] = pack_half2(qv[8 * i + 3], qv[8 * i + 7]);
+      }
+    }
+    const int e0 = __shfl_sync(0xffffffffu, e, (2 * c) * 4);
+    const int e1 = __shfl_sync(0xffffffffu, e, (2 * c + 1) * 4);
+    cq0 = ldexpf(qk_scale_log2, -e0);
+    cq1 = ldexpf(qk_scale_log2, -e1);
+  }
+
+  // ---- page pipeline
+  const int n_range = pg_end - pg_begin;
+  const int n_my = n_range > warp ? (n_range - warp + kWarps - 1) / kWarps : 0;
+  const int32_t* bt = s.block_table + (size_t)b * s.max_bps;
+
+  auto issue = [&](int k) {
+    if (k < n_my) {
+      const int page = pg_begin + warp + kWarps * k;
+      const int blk = bt[page];
+      if ((unsigned)blk < (unsigned)s.num_blocks) {
+        uint8_t* st = ring + (k % STAGES) * Gm::kStage;
+        const size_t hp = ((size_t)blk * hkv + h) * kPage;
+        const uint8_t* kb = s.k_codes + hp * Gm::kRowBytes;
+        const uint8_t* vb = s.v_codes + hp * Gm::kRowBytes;
+        if (BITS == 8) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            cp_async16(st + j * 512 + lane * 16, kb + (2 * r + (j >> 1)) * 128 + 32 * c + 16 * (j & 1));
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            cp_async16(st + Gm::kKBytes + j * 512 + lane * 16, vb + (4 * c + j) * 128 + 16 * r);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 2; ++j) cp_async16(st + j * 512 + lane * 16, kb + (2 * r + j) * 64 + 16 * c);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            cp_async8(st + Gm::kKBytes + j * 256 + lane * 8, vb + (4 * c + j) * 64 + 8 * r);
+        }
+        if (lane < 4)
+          cp_async16(st + Gm::kKBytes + Gm::kVBytes + 16 * lane, s.k_scale + hp + 4 * lane);
+        else if (lane < 8)
+          cp_async16(st + Gm::kKBytes + Gm::kVBytes + 64 + 16 * (lane - 4), s.v_scale + hp + 4 * (lane - 4));
+      }
+    }
+    cp_async_commit();
+  };
+
+  float oacc[8][4];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.0f;
+  float m0 = kNegBig, m1 = kNegBig, l0 = 0.0f, l1 = 0.0f;
+  int E = 0;
+  bool e_set = false;
+  float sv_hi = 0.0f;
+  float inv2E = 1.0f;
+
+  float* lg_base = spill ? w.logits + ((size_t)bl * hkv + h) * w.s_cap * G : nullptr;
+
+#pragma unroll 1
+  for (int k = 0; k < STAGES - 1; ++k) issue(k);
+
+#pragma unroll 1
+  for (int k = 0; k < n_my; ++k) {
+    issue(k + STAGES - 1);
+    cp_async_wait<STAGES - 1>();
+    __syncwarp();
+    const uint8_t* st = ring + (k % STAGES) * Gm::kStage;
+    const int page = pg_begin + warp + kWarps * k;
+    const int blk = bt[page];
+    const bool blk_ok = (unsigned)blk < (unsigned)s.num_blocks;
+    if (!blk_ok && lane == 0) atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
+    const int slot0 = page * kPage;
+    const bool v0 = blk_ok && (slot0 + 2 * r < S);
+    const bool v1 = blk_ok && (slot0 + 2 * r + 1 < S);
+    const float2 skv = *reinterpret_cast<const float2*>(st + Gm::kKBytes + Gm::kVBytes + 8 * r);
+    const float2 svv = *reinterpret_cast<const float2*>(st + Gm::kKBytes + Gm::kVBytes + 64 + 8 * r);
+
+    // ---- S = K_codes . q'  (rows: slots 2r and 2r+1, cols: query heads 2c, 2c+1)
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (BITS == 8) {
+      const uint4 ka = *reinterpret_cast<const uint4*>(st + 0 * 512 + lane * 16);
+      const uint4 kb2 = *reinterpret_cast<const uint4*>(st + 1 * 512 + lane * 16);
+      const uint4 kc = *reinterpret_cast<const uint4*>(st + 2 * 512 + lane * 16);
+      const uint4 kd = *reinterpret_cast<const uint4*>(st + 3 * 512 + lane * 16);
+      const uint32_t w0[8] = {ka.x, ka.y, ka.z, ka.w, kb2.x, kb2.y, kb2.z, kb2.w};
+      const uint32_t w1[8] = {kc.x, kc.y, kc.z, kc.w, kd.x, kd.y, kd.z, kd.w};
+#pragma unroll
+      for (int stp = 0; stp < 8; ++stp) {
+        uint32_t a0, a1, a2, a3;
+        i8x4_to_h2(w0[stp] ^ 0x80808080u, a0, a2);
+        i8x4_to_h2(w1[stp] ^ 0x80808080u, a1, a3);
+        mma16816(acc, a0, a1, a2, a3, bq[stp][0], bq[stp][1]);
+      }
+    } else {
+      const uint4 ka = *reinterpret_cast<const uint4*>(st + 0 * 512 + lane * 16);
+      const uint4 kb2 = *reinterpret_cast<const uint4*>(st + 1 * 512 + lane * 16);
+      const uint32_t w0[4] = {ka.x, ka.y, ka.z, ka.w};
+      const uint32_t w1[4] = {kb2.x, kb2.y, kb2.z, kb2.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t x0 = w0[i], x1 = w1[i];
+        const uint32_t x0s = x0 >> 8, x1s = x1 >> 8;
+        mma16816(acc, i4_lo_to_h2(x0), i4_lo_to_h2(x1), i4_hi_to_h2(x0), i4_hi_to_h2(x1), bq[2 * i][0],
+                 bq[2 * i][1]);
+        mma16816(acc, i4_lo_to_h2(x0s), i4_lo_to_h2(x1s), i4_hi_to_h2(x0s), i4_hi_to_h2(x1s),
+                 bq[2 * i + 1][0], bq[2 * i + 1][1]);
+      }
+    }
+    float lg0 = v0 ? acc[0] * skv.x * cq0 : -INFINITY;  // slot 2r,   head 2c
+    float lg1 = v0 ? acc[1] * skv.x * cq1 : -INFINITY;  // slot 2r,   head 2c+1
+    float lg2 = v1 ? acc[2] * skv.y * cq0 : -INFINITY;  // slot 2r+1, head 2c
+    float lg3 = v1 ? acc[3] * skv.y * cq1 : -INFINITY;  // slot 2r+1, head 2c+1
+    if (spill) {
+      const int g0 = 2 * c, g1 = 2 * c + 1;
+      float* row0 = lg_base + (size_t)(slot0 + 2 * r) * G;
+      if (v0) {
+        if (g0 < G) row0[g0] = lg0;
+        if (g1 < G) row0[g1] = lg1;
+      }
+      if (v1) {
+        if (g0 < G) row0[G + g0] = lg2;
+        if (g1 < G) row0[G + g1] = lg3;
+      }
+    }
+    float tm0 = fmaxf(lg0, lg2), tm1 = fmaxf(lg1, lg3);
+    float svm = fmaxf(v0 ? svv.x : 0.0f, v1 ? svv.y : 0.0f);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, o));
+      tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, o));
+      svm = fmaxf(svm, __shfl_xor_sync(0xffffffffu, svm, o));
+    }
+    const bool rescale_e = (svm > sv_hi) || (!e_set && svm > 0.0f);
+    const bool need = (tm0 > m0 + kLazy) || (tm1 > m1 + kLazy) || rescale_e;
+    if (__any_sync(0xffffffffu, need)) {
+      const float nm0 = fmaxf(m0, tm0), nm1 = fmaxf(m1, tm1);
+      const float al0 = fast_exp2(m0 - nm0), al1 = fast_exp2(m1 - nm1);
+      int nE = E;
+      if (rescale_e && svm > 0.0f) nE = min(max(exponent_of(svm), -126), 126);
+      const float f = ldexpf(1.0f, E - nE);
+      const float f0 = al0 * f, f1 = al1 * f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        oacc[j][0] *= f0;
+        oacc[j][2] *= f0;
+        oacc[j][1] *= f1;
+        oacc[j][3] *= f1;
+      }
+      l0 *= al0;
+      l1 *= al1;
+      m0 = nm0;
+      m1 = nm1;
+      if (rescale_e && svm > 0.0f) {
+        E = nE;
+        e_set = true;
+        sv_hi = ldexpf(1.0f, E + 4);
+        inv2E = ldexpf(1.0f, -E);
+      }
+    }
+    const float sn0 = v0 ? svv.x * inv2E : 0.0f;
+    const float sn1 = v1 ? svv.y * inv2E : 0.0f;
+    const float p0 = fast_exp2(lg0 - m0), p1 = fast_exp2(lg1 - m1);
+    const float p2 = fast_exp2(lg2 - m0), p3 = fast_exp2(lg3 - m1);
+    l0 += p0 + p2;
+    l1 += p1 + p3;
+    const uint32_t pb0 = movmatrix_t(pack_half2(p0 * sn0, p1 * sn0));
+    const uint32_t pb1 = movmatrix_t(pack_half2(p2 * sn1, p3 * sn1));
+
+    // ---- O^T += V_codes^T . P~^T   (rows: head-dim 16r + 2j (+1), cols: query heads)
+    if (BITS == 8) {
+      const uint4 r0 = *reinterpret_cast<const uint4*>(st + Gm::kKBytes + 0 * 512 + lane * 16);
+      const uint4 r1 = *reinterpret_cast<const uint4*>(st + Gm::kKBytes + 1 * 512 + lane * 16);
+      const uint4 r2 = *reinterpret_cast<const uint4*>(st + Gm::kKBytes + 2 * 512 + lane * 16);
+      const uint4 r3 = *reinterpret_cast<const uint4*>(st + Gm::kKBytes + 3 * 512 + lane * 16);
+      const uint32_t x0[4] = {r0.x, r0.y, r0.z, r0.w};  // slot 4c
+      const uint32_t x1[4] = {r1.x, r1.y, r1.z, r1.w};  // slot 4c+1
+      const uint32_t x2[4] = {r2.x, r2.y, r2.z, r2.w};  // slot 4c+2
+      const uint32_t x3[4] = {r3.x, r3.y, r3.z, r3.w};  // slot 4c+3
+#pragma unroll
+      for (int wd = 0; wd < 4; ++wd) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int j = 2 * wd + half;
+          const uint32_t sa = (2 * half) | ((2 * half) << 4) | ((4 + 2 * half) << 8) | ((4 + 2 * half) << 12);
+          const uint32_t sb = (2 * half + 1) | ((2 * half + 1) << 4) | ((5 + 2 * half) << 8) | ((5 + 2 * half) << 12);
+          const uint32_t a0 = i8_pair_to_h2(x0[wd], x2[wd], sa);
+          const uint32_t a1 = i8_pair_to_h2(x0[wd], x2[wd], sb);
+          const uint32_t a2 = i8_pair_to_h2(x1[wd], x3[wd], sa);
+          const uint32_t a3 = i8_pair_to_h2(x1[wd], x3[wd], sb);
+          mma16816(oacc[j], a0, a1, a2, a3, pb0, pb1);
+        }
+      }
+    } else {
+      const uint2 r0 = *reinterpret_cast<const uint2*>(st + Gm::kKBytes + 0 * 256 + lane * 8);
+      const uint2 r1 = *reinterpret_cast<const uint2*>(st + Gm::kKBytes + 1 * 256 + lane * 8);
+      const uint2 r2 = *reinterpret_cast<const uint2*>(st + Gm::kKBytes + 2 * 256 + lane * 8);
+      const uint2 r3 = *reinterpret_cast<const uint2*>(st + Gm::kKBytes + 3 * 256 + lane * 8);
+      const uint32_t x0[2] = {r0.x, r0.y};
+      const uint32_t x1[2] = {r1.x, r1.y};
+      const uint32_t x2[2] = {r2.x, r2.y};
+      const uint32_t x3[2] = {r3.x, r3.y};
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const int j = 4 * u + kk;
+          const uint32_t sel = kk | (kk << 4) | ((4 + kk) << 8) | ((4 + kk) << 12);
+          const uint32_t v02 = prmt(x0[u], x2[u], sel);
+          const uint32_t v13 = prmt(x1[u], x3[u], sel);
+          mma16816(oacc[j], i4_lo_to_h2(v02), i4_hi_to_h2(v02), i4_lo_to_h2(v13), i4_hi_to_h2(v13), pb0,
+                   pb1);
+        }
+      }
+    }
+    __syncwarp();
+  }
+  cp_async_wait<0>();
+
+  // ---- per-warp totals
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+  }
+  const float f2E = ldexpf(1.0f, E);
+  __syncthreads();  // every warp is done with its ring: reuse shared memory
+  float* sm_m = reinterpret_cast<float*>(smem);          // [kWarps][8]
+  float* sm_l = sm_m + kWarps * kMaxGroup;               // [kWarps][8]
+  float* sm_o = sm_l + kWarps * kMaxGroup;               // [kWarps][8][128]
+  if (r == 0) {
+    sm_m[warp * kMaxGroup + 2 * c] = m0;
+    sm_m[warp * kMaxGroup + 2 * c + 1] = m1;
+    sm_l[warp * kMaxGroup + 2 * c] = l0;
+    sm_l[warp * kMaxGroup + 2 * c + 1] = l1;
+  }
+  {
+    float* o0 = sm_o + ((size_t)warp * kMaxGroup + 2 * c) * kHeadDim + 16 * r;
+    float* o1 = o0 + kHeadDim;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      o0[2 * j] = oacc[j][0] * f2E;
+      o0[2 * j + 1] = oacc[j][2] * f2E;
+      o1[2 * j] = oacc[j][1] * f2E;
+      o1[2 * j + 1] = oacc[j][3] * f2E;
+    }
+  }
+  __syncthreads();
+  const int d = threadIdx.x;  // 128 threads = head_dim
+  const size_t pbase = (((size_t)bl * hkv + h) * w.nsplit + split) * G;
+  for (int g = 0; g < G; ++g) {
+    float M = kNegBig;
+#pragma unroll
+    for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, sm_m[ww * kMaxGroup + g]);
+    float o = 0.0f, l = 0.0f;
+#pragma unroll
+    for (int ww = 0; ww < kWarps; ++ww) {
+      const float wt = fast_exp2(sm_m[ww * kMaxGroup + g] - M);
+      o += wt * sm_o[((size_t)ww * kMaxGroup + g) * kHeadDim + d];
+      l += wt * sm_l[ww * kMaxGroup + g];
+    }
+    w.part_o[(pbase + g) * kHeadDim + d] = o;
+    if (d == 0) {
+      w.part_ml[(pbase + g) * 2 + 0] = M;
+      w.part_ml[(pbase + g) * 2 + 1] = l;
+    }
+  }
+}
+
+// Merge the splits and the bf16 sinks of one (sequence, KV head); write the
+// bf16 outputs of its G query heads; with H2O on, add this step's
+// probabilities to the sink scores and to every pool slot's score.
+__global__ void __launch_bounds__(128) attn_merge_kernel(DevState s, int seq_begin,
+                                                         const uint16_t* __restrict__ q,
+                                                         uint16_t* __restrict__ out, float qk_scale_log2,
+                                                         AttnWork w, int accumulate) {
+  const int h = blockIdx.x;
+  const int bl = blockIdx.y;
+  const int b = seq_begin + bl;
+  const int G = s.group;
+  const int hkv = s.hkv;
+  const int S = s.seq_slots[b];
+  const int P = s.seq_pos[b];
+  const int ns = min(P, kSinks);
+  const int n_pages = (S + kPage - 1) / kPage;
+  const int nsp = (n_pages + w.pages_per_split - 1) / w.pages_per_split;
+  const int d = threadIdx.x;
+  const int lane = d & 31, warp = d >> 5;
+
+  __shared__ float sh_red[4][kSinks];
+  __shared__ float sh_sl[kMaxGroup][kSinks];
+  __shared__ float sh_M[kMaxGroup], sh_invL[kMaxGroup];
+
+  const uint16_t* sk = s.sink_k + ((size_t)b * hkv + h) * kSinks * kHeadDim;
+  const uint16_t* sv = s.sink_v + ((size_t)b * hkv + h) * kSinks * kHeadDim;
+  for (int g = 0; g < G; ++g) {
+    const int hq = h * G + g;
+    const float qd = bf16f(q[((size_t)bl * s.hq + hq) * kHeadDim + d]);
+    float part[kSinks];
+#pragma unroll
+    for (int j = 0; j < kSinks; ++j) part[j] = j < ns ? qd * bf16f(sk[j * kHeadDim + d]) : 0.0f;
+#pragma unroll
+    for (int j = 0; j < kSinks; ++j)
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) part[j] += __shfl_xor_sync(0xffffffffu, part[j], o);
+    if (lane == 0)
+#pragma unroll
+      for (int j = 0; j < kSinks; ++j) sh_red[warp][j] = part[j];
+    __syncthreads();
+    float sl[kSinks];
+#pragma unroll
+    for (int j = 0; j < kSinks; ++j)
+      sl[j] = j < ns ? (sh_red[0][j] + sh_red[1][j] + sh_red[2][j] + sh_red[3][j]) * qk_scale_log2 : -INFINITY;
+    float M = kNegBig;
+#pragma unroll
+    for (int j = 0; j < kSinks; ++j) M = fmaxf(M, sl[j]);
+    const size_t pbase = ((size_t)bl * hkv + h) * w.nsplit * G;
+    for (int sp = 0; sp < nsp; ++sp) M = fmaxf(M, w.part_ml[(pbase + (size_t)sp * G + g) * 2]);
+    float L = 0.0f, o = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kSinks; ++j) {
+      if (j < ns) {
+        const float e = fast_exp2(sl[j] - M);
+        L += e;
+        o += e * bf16f(sv[j * kHeadDim + d]);
+      }
+    }
+    for (int sp = 0; sp < nsp; ++sp) {
+      const size_t pi = pbase + (size_t)sp * G + g;
+      const float e = fast_exp2(w.part_ml[pi * 2] - M);
+      L += e * w.part_ml[pi * 2 + 1];
+      o += e * w.part_o[pi * kHeadDim + d];
+    }
+    const float res = L > 0.0f ? o / L : 0.0f;
+    out[((size_t)bl * s.hq + hq) * kHeadDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(res));
+    if (d == 0) {
+      sh_M[g] = M;
+      sh_invL[g] = L > 0.0f ? 1.0f / L : 0.0f;
+      w.stats[((size_t)bl * s.hq + hq) * 2 + 0] = M;
+      w.stats[((size_t)bl * s.hq + hq) * 2 + 1] = L;
+#pragma unroll
+      for (int j = 0; j < kSinks; ++j) sh_sl[g][j] = sl[j];
+    }
+    __syncthreads();
+  }
+  if (!accumulate) return;
+  if (d < ns) {
+    float inc = 0.0f;
+    for (int g = 0; g < G; ++g) inc += fast_exp2(sh_sl[g][d] - sh_M[g]) * sh_invL[g];
+    s.sink_score[((size_t)b * hkv + h) * kSinks + d] += inc;
+  }
+  const int32_t* bt = s.block_table + (size_t)b * s.max_bps;
+  const float* lgr = w.logits + ((size_t)bl * hkv + h) * w.s_cap * G;
+  for (int t = d; t < S; t += blockDim.x) {
+    const int blk = bt[t / kPage];
+    if ((unsigned)blk >= (unsigned)s.num_blocks) continue;
+    float inc = 0.0f;
+    for (int g = 0; g < G; ++g) inc += fast_exp2(lgr[(size_t)t * G + g] - sh_M[g]) * sh_invL[g];
+    s.score[((size_t)blk * hkv + h) * kPage + (t % kPage)] += inc;
+  }
+}
+
+// cudaFuncSetAttribute is per device and per kernel: one flag per (BITS, device).
+template <int BITS>
+cudaError_t ensure_split_smem() {
+  static int done[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(attn_split_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Geom<BITS>::kSmem);
+  if (e == cudaSuccess && dev < 64) done[dev] = 1;
+  return e;
+}
+
+}  // namespace
+
+int attention_smem_bytes(int bits) { return bits == 8 ? Geom<8>::kSmem : Geom<4>::kSmem; }
+
+cudaError_t launch_attention_split(const DevState& s, int seq_begin, int batch, const uint16_t* q,
+                                   float qk_scale_log2, const AttnWork& w, bool spill, cudaStream_t st) {
+  dim3 grid(w.nsplit, s.hkv, batch);
+  cudaError_t e;
+  if (s.bits == 8) {
+    e = ensure_split_smem<8>();
+    if (e != cudaSuccess) return e;
+    attn_split_kernel<8><<<grid, kWarps * 32, Geom<8>::kSmem, st>>>(s, seq_begin, q, qk_scale_log2, w, spill);
+  } else {
+    e = ensure_split_smem<4>();
+    if (e != cudaSuccess) return e;
+    attn_split_kernel<4><<<grid, kWarps * 32, Geom<4>::kSmem, st>>>(s, seq_begin, q, qk_scale_log2, w, spill);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attention_merge(const DevState& s, int seq_begin, int batch, const uint16_t* q, uint16_t* out,
+                                   float qk_scale_log2, const AttnWork& w, bool accumulate, cudaStream_t st) {
+  dim3 grid(s.hkv, batch);
+  attn_merge_kernel<<<grid, 128, 0, st>>>(s, seq_begin, q, out, qk_scale_log2, w, accumulate ? 1 : 0);
+  return cudaGetLastError();
+}
+
+}  // namespace kvc

@@ -1,0 +1,487 @@
+// Host side of the C ABI (include/kvc.h): argument validation, the host mirror
+// of the sequence lengths (so that capacity errors are caught before anything
+// is enqueued, as the paged cache's allocate_sequence returns False in
+// "KV Cache optimization techniques" section 3.2), buffer carving, the split-K
+// launch policy, and the kernel launches.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/kvc.h"
+#include "kvc_internal.h"
+
+using kvc::DevState;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kMinPagesPerSplit = 4;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct Layout {
+  size_t off[KVC_BUF_COUNT];
+  size_t size[KVC_BUF_COUNT];
+  size_t total;
+};
+
+bool config_valid(const kvc_config* c) {
+  return c && c->num_q_heads > 0 && c->num_kv_heads > 0 && c->num_blocks > 0 && c->max_batch > 0 &&
+         c->max_blocks_per_seq > 0 && c->num_q_heads % c->num_kv_heads == 0;
+}
+
+kvc_status config_check(const kvc_config* c) {
+  if (!config_valid(c)) return KVC_ERR_INVALID_ARG;
+  if (c->head_dim != kvc::kHeadDim || c->page_size != kvc::kPage || (c->bits != 8 && c->bits != 4) ||
+      c->num_q_heads / c->num_kv_heads > kvc::kMaxGroup)
+    return KVC_ERR_UNSUPPORTED;
+  // 32-bit slot arithmetic inside the kernels
+  if ((double)c->num_blocks * c->num_kv_heads * kvc::kPage * 128 > 1.0e18 ||
+      (double)c->max_blocks_per_seq * kvc::kPage > 2.0e9)
+    return KVC_ERR_UNSUPPORTED;
+  return KVC_OK;
+}
+
+Layout make_layout(const kvc_config* c) {
+  Layout L{};
+  const size_t slots = (size_t)c->num_blocks * c->num_kv_heads * kvc::kPage;
+  const size_t row_bytes = (size_t)kvc::kHeadDim * c->bits / 8;
+  const size_t sinks = (size_t)c->max_batch * c->num_kv_heads * kvc::kSinks;
+  L.size[KVC_BUF_K_CODES] = slots * row_bytes;
+  L.size[KVC_BUF_V_CODES] = slots * row_bytes;
+  L.size[KVC_BUF_K_SCALE] = slots * 4;
+  L.size[KVC_BUF_V_SCALE] = slots * 4;
+  L.size[KVC_BUF_SLOT_POS] = slots * 4;
+  L.size[KVC_BUF_SCORE] = slots * 4;
+  L.size[KVC_BUF_SINK_K] = sinks * kvc::kHeadDim * 2;
+  L.size[KVC_BUF_SINK_V] = sinks * kvc::kHeadDim * 2;
+  L.size[KVC_BUF_SINK_SCORE] = sinks * 4;
+  L.size[KVC_BUF_BLOCK_TABLE] = (size_t)c->max_batch * c->max_blocks_per_seq * 4;
+  L.size[KVC_BUF_SEQ_SLOTS] = (size_t)c->max_batch * 4;
+  L.size[KVC_BUF_SEQ_POS] = (size_t)c->max_batch * 4;
+  L.size[KVC_BUF_FREE_STACK] = (size_t)c->num_blocks * 4;
+  L.size[KVC_BUF_COUNTERS] = (size_t)kvc::kCounters * 4;
+  L.size[KVC_BUF_PLAN] = (size_t)c->max_batch * 2 * 4;
+  size_t o = 0;
+  for (int i = 0; i < KVC_BUF_COUNT; ++i) {
+    L.off[i] = o;
+    o = align_up(o + L.size[i]);
+  }
+  L.total = o;
+  return L;
+}
+
+int pages_of(int slots) { return (slots + kvc::kPage - 1) / kvc::kPage; }
+
+}  // namespace
+
+struct kvc_cache {
+  kvc_config cfg;
+  Layout layout;
+  uint8_t* base;
+  DevState dev;
+  std::vector<int32_t> slots;  // host mirror: pool slots per sequence
+  std::vector<int32_t> pos;    // host mirror: positions seen per sequence
+  // pending selection (kvc_h2o_select_evict -> kvc_compact_blocks)
+  bool plan_pending = false;
+  int32_t plan_begin = 0, plan_batch = 0;
+  std::vector<int32_t> plan_new;
+  void* trace_start = nullptr;
+  void* trace_stop = nullptr;
+  int32_t last_launches = 0;
+  int sm_count = 0;
+};
+
+namespace {
+
+int used_pages(const kvc_cache* c) {
+  long long u = 0;
+  for (int b = 0; b < c->cfg.max_batch; ++b) u += pages_of(c->slots[b]);
+  return (int)u;
+}
+
+bool range_ok(const kvc_cache* c, int32_t seq_begin, int32_t batch) {
+  return seq_begin >= 0 && batch > 0 && (long long)seq_begin + batch <= c->cfg.max_batch;
+}
+
+int s_cap(const kvc_cache* c) { return c->cfg.max_blocks_per_seq * kvc::kPage; }
+
+int max_split_count(const kvc_cache* c) {
+  return (c->cfg.max_blocks_per_seq + kMinPagesPerSplit - 1) / kMinPagesPerSplit;
+}
+
+// Workspace carving (all regions 256-byte aligned).
+struct WsLayout {
+  size_t part_o, part_ml, logits, stats, keys, pos, total;
+};
+
+WsLayout ws_layout(const kvc_cache* c, int batch) {
+  const size_t G = c->cfg.num_q_heads / c->cfg.num_kv_heads;
+  const size_t pairs = (size_t)batch * c->cfg.num_kv_heads;
+  const size_t ns = max_split_count(c);
+  const size_t cap = s_cap(c);
+  WsLayout w{};
+  size_t o = 0;
+  w.part_o = o;
+  o = align_up(o + pairs * ns * G * kvc::kHeadDim * 4);
+  w.part_ml = o;
+  o = align_up(o + pairs * ns * G * 2 * 4);
+  w.logits = o;
+  o = align_up(o + pairs * cap * G * 4);
+  w.stats = o;
+  o = align_up(o + (size_t)batch * c->cfg.num_q_heads * 2 * 4);
+  w.keys = o;
+  o = align_up(o + pairs * cap * 4);
+  w.pos = o;
+  o = align_up(o + pairs * cap * 4);
+  w.total = o;
+  return w;
+}
+
+int sm_count(kvc_cache* c) {
+  if (c->sm_count <= 0) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+      c->sm_count = n;
+    else
+      c->sm_count = 152;
+  }
+  return c->sm_count;
+}
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+int32_t kvc_version(void) { return 100; }
+
+const char* kvc_status_string(kvc_status s) {
+  switch (s) {
+    case KVC_OK: return "ok";
+    case KVC_ERR_INVALID_ARG: return "invalid argument";
+    case KVC_ERR_UNSUPPORTED: return "unsupported configuration";
+    case KVC_ERR_CAPACITY: return "out of cache capacity";
+    case KVC_ERR_CUDA: return "CUDA runtime error";
+    case KVC_ERR_DEVICE: return "device reported an error";
+    case KVC_ERR_STATE: return "call order violated";
+  }
+  return "unknown status";
+}
+
+size_t kvc_state_bytes(const kvc_config* cfg) {
+  if (config_check(cfg) != KVC_OK) return 0;
+  return make_layout(cfg).total;
+}
+
+kvc_status kvc_cache_create(const kvc_config* cfg, void* d_state, size_t state_bytes, kvc_cache** out) {
+  if (!out) return KVC_ERR_INVALID_ARG;
+  *out = nullptr;
+  const kvc_status st = config_check(cfg);
+  if (st != KVC_OK) return st;
+  const Layout L = make_layout(cfg);
+  if (!d_state || !aligned(d_state, kAlign) || state_bytes < L.total) return KVC_ERR_INVALID_ARG;
+  kvc_cache* c = new (std::nothrow) kvc_cache();
+  if (!c) return KVC_ERR_INVALID_ARG;
+  c->cfg = *cfg;
+  c->layout = L;
+  c->base = static_cast<uint8_t*>(d_state);
+  DevState& d = c->dev;
+  uint8_t* b = c->base;
+  d.k_codes = b + L.off[KVC_BUF_K_CODES];
+  d.v_codes = b + L.off[KVC_BUF_V_CODES];
+  d.k_scale = reinterpret_cast<float*>(b + L.off[KVC_BUF_K_SCALE]);
+  d.v_scale = reinterpret_cast<float*>(b + L.off[KVC_BUF_V_SCALE]);
+  d.slot_pos = reinterpret_cast<int32_t*>(b + L.off[KVC_BUF_SLOT_POS]);
+  d.score = reinterpret_cast<float*>(b + L.off[KVC_BUF_SCORE]);
+  d.sink_k = reinterpret_cast<uint16_t*>(b + L.off[KVC_BUF_SINK_K]);
+  d.sink_v = reinterpret_cast<uint16_t*>(b + L.off[KVC_BUF_SINK_V]);
+  d.sink_score = reinterpret_cast<float*>(b + L.off[KVC_BUF_SINK_SCORE]);
+  d.block_table = reinterpret_cast<int32_t*>(b + L.off[KVC_BUF_BLOCK_TABLE]);
+  d.seq_slots = reinterpret_cast<int32_t*>(b + L.off[KVC_BUF_SEQ_SLOTS]);
+  d.seq_pos = reinterpret_cast<int32_t*>(b + L.off[KVC_BUF_SEQ_POS]);
+  d.free_stack = reinterpret_cast<int32_t*>(b + L.off[KVC_BUF_FREE_STACK]);
+  d.counters = reinterpret_cast<int32_t*>(b + L.off[KVC_BUF_COUNTERS]);
+  d.plan = reinterpret_cast<int32_t*>(b + L.off[KVC_BUF_PLAN]);
+  d.hq = cfg->num_q_heads;
+  d.hkv = cfg->num_kv_heads;
+  d.group = cfg->num_q_heads / cfg->num_kv_heads;
+  d.bits = cfg->bits;
+  d.row_bytes = kvc::kHeadDim * cfg->bits / 8;
+  d.num_blocks = cfg->num_blocks;
+  d.max_batch = cfg->max_batch;
+  d.max_bps = cfg->max_blocks_per_seq;
+  c->slots.assign(cfg->max_batch, 0);
+  c->pos.assign(cfg->max_batch, 0);
+  *out = c;
+  return KVC_OK;
+}
+
+void kvc_cache_destroy(kvc_cache* cache) { delete cache; }
+
+kvc_status kvc_cache_buffer(const kvc_cache* c, int32_t which, void** d_ptr, size_t* bytes) {
+  if (!c || which < 0 || which >= KVC_BUF_COUNT) return KVC_ERR_INVALID_ARG;
+  if (d_ptr) *d_ptr = c->base + c->layout.off[which];
+  if (bytes) *bytes = c->layout.size[which];
+  return KVC_OK;
+}
+
+kvc_status kvc_cache_lengths(const kvc_cache* c, int32_t seq, int32_t* slots, int32_t* positions) {
+  if (!c || seq < 0 || seq >= c->cfg.max_batch) return KVC_ERR_INVALID_ARG;
+  if (slots) *slots = c->slots[seq];
+  if (positions) *positions = c->pos[seq];
+  return KVC_OK;
+}
+
+kvc_status kvc_cache_reset(kvc_cache* c, const int32_t* h_block_order, void* stream) {
+  if (!c) return KVC_ERR_INVALID_ARG;
+  const int nb = c->cfg.num_blocks;
+  if (h_block_order) {
+    std::vector<char> seen(nb, 0);
+    for (int i = 0; i < nb; ++i) {
+      const int v = h_block_order[i];
+      if (v < 0 || v >= nb || seen[v]) return KVC_ERR_INVALID_ARG;
+      seen[v] = 1;
+    }
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  c->last_launches = 0;
+  if (cudaMemsetAsync(c->base, 0, c->layout.total, st) != cudaSuccess) return KVC_ERR_CUDA;
+  if (h_block_order) {
+    if (cudaMemcpyAsync(c->dev.free_stack, h_block_order, (size_t)nb * 4, cudaMemcpyHostToDevice, st) !=
+        cudaSuccess)
+      return KVC_ERR_CUDA;
+  } else {
+    if (kvc::launch_fill_free_stack(c->dev, st) != cudaSuccess) return KVC_ERR_CUDA;
+    c->last_launches = 1;
+  }
+  const int32_t top = nb;
+  if (cudaMemcpyAsync(c->dev.counters + kvc::kCtrFreeTop, &top, 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return KVC_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return KVC_ERR_CUDA;
+  std::fill(c->slots.begin(), c->slots.end(), 0);
+  std::fill(c->pos.begin(), c->pos.end(), 0);
+  c->plan_pending = false;
+  return KVC_OK;
+}
+
+kvc_status kvc_cache_sync_host(kvc_cache* c, void* stream) {
+  if (!c) return KVC_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int mb = c->cfg.max_batch;
+  std::vector<int32_t> s(mb), p(mb);
+  if (cudaMemcpyAsync(s.data(), c->dev.seq_slots, (size_t)mb * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemcpyAsync(p.data(), c->dev.seq_pos, (size_t)mb * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return KVC_ERR_CUDA;
+  c->slots = s;
+  c->pos = p;
+  c->plan_pending = false;
+  return KVC_OK;
+}
+
+size_t kvc_workspace_bytes(const kvc_cache* c, int32_t batch) {
+  if (!c || batch <= 0 || batch > c->cfg.max_batch) return 0;
+  return ws_layout(c, batch).total;
+}
+
+kvc_status kvc_quantize_append(kvc_cache* c, int32_t seq_begin, int32_t batch, int32_t n_new, const void* d_k,
+                               const void* d_v, void* stream) {
+  if (!c) return KVC_ERR_INVALID_ARG;
+  c->last_launches = 0;
+  if (!range_ok(c, seq_begin, batch) || n_new < 0) return KVC_ERR_INVALID_ARG;
+  if (n_new == 0) return KVC_OK;
+  if (!d_k || !d_v || !aligned(d_k, 8) || !aligned(d_v, 8)) return KVC_ERR_INVALID_ARG;
+  // capacity, from the host mirror (no device round trip)
+  long long need = 0;
+  std::vector<int32_t> new_slots(batch);
+  for (int i = 0; i < batch; ++i) {
+    const int b = seq_begin + i;
+    const long long n_sink_new = std::min<long long>(n_new, std::max(0, kvc::kSinks - c->pos[b]));
+    const long long ns = c->slots[b] + (n_new - n_sink_new);
+    if ((long long)c->pos[b] + n_new > 2000000000LL) return KVC_ERR_CAPACITY;
+    if ((ns + kvc::kPage - 1) / kvc::kPage > c->cfg.max_blocks_per_seq) return KVC_ERR_CAPACITY;
+    need += pages_of((int)ns) - pages_of(c->slots[b]);
+    new_slots[i] = (int32_t)ns;
+  }
+  if (need > (long long)c->cfg.num_blocks - used_pages(c)) return KVC_ERR_CAPACITY;
+  const cudaError_t e = kvc::launch_append(c->dev, seq_begin, batch, n_new, static_cast<const uint16_t*>(d_k),
+                                           static_cast<const uint16_t*>(d_v), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return KVC_ERR_CUDA;
+  c->last_launches = 1;
+  for (int i = 0; i < batch; ++i) {
+    c->slots[seq_begin + i] = new_slots[i];
+    c->pos[seq_begin + i] += n_new;
+  }
+  c->plan_pending = false;
+  return KVC_OK;
+}
+
+kvc_status kvc_decode_attention(kvc_cache* c, int32_t seq_begin, int32_t batch, const void* d_q, void* d_out,
+                                float sm_scale, int32_t flags, void* d_workspace, size_t workspace_bytes,
+                                void* stream) {
+  if (!c) return KVC_ERR_INVALID_ARG;
+  c->last_launches = 0;
+  if (!range_ok(c, seq_begin, batch)) return KVC_ERR_INVALID_ARG;
+  if (!d_q || !d_out || !aligned(d_q, 16) || !aligned(d_out, 16)) return KVC_ERR_INVALID_ARG;
+  if (!(sm_scale > 0.0f) || !std::isfinite(sm_scale) || (flags & ~KVC_ATTN_ACCUM_H2O)) return KVC_ERR_INVALID_ARG;
+  const WsLayout wl = ws_layout(c, batch);
+  if (!d_workspace || !aligned(d_workspace, kAlign) || workspace_bytes < wl.total) return KVC_ERR_INVALID_ARG;
+  int max_pages = 0;
+  for (int i = 0; i < batch; ++i) {
+    const int b = seq_begin + i;
+    if (c->pos[b] <= 0) return KVC_ERR_INVALID_ARG;  // nothing to attend to
+    max_pages = std::max(max_pages, pages_of(c->slots[b]));
+  }
+  // split-K policy: enough CTAs for several waves of resident blocks, at
+  // least kMinPagesPerSplit pages per split
+  const int pairs = batch * c->cfg.num_kv_heads;
+  const int resident = c->cfg.bits == 8 ? 3 : 4;
+  const int target = 2 * sm_count(c) * resident;
+  int nsplit = 1;
+  int pps = std::max(max_pages, 1);
+  if (max_pages > 0) {
+    nsplit = std::max(1, (target + pairs - 1) / pairs);
+    nsplit = std::min(nsplit, (max_pages + kMinPagesPerSplit - 1) / kMinPagesPerSplit);
+    nsplit = std::max(1, std::min(nsplit, max_split_count(c)));
+    pps = (max_pages + nsplit - 1) / nsplit;
+    nsplit = (max_pages + pps - 1) / pps;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(d_workspace);
+  kvc::AttnWork w{};
+  w.part_o = reinterpret_cast<float*>(ws + wl.part_o);
+  w.part_ml = reinterpret_cast<float*>(ws + wl.part_ml);
+  w.logits = reinterpret_cast<float*>(ws + wl.logits);
+  w.stats = reinterpret_cast<float*>(ws + wl.stats);
+  w.nsplit = nsplit;
+  w.pages_per_split = pps;
+  w.s_cap = s_cap(c);
+  const float qk_scale_log2 = sm_scale * 1.4426950408889634f;
+  const bool h2o = (flags & KVC_ATTN_ACCUM_H2O) != 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool trace = c->trace_start && c->trace_stop;
+  int launches = 0;
+  // under stream capture the trace events become event-record nodes of the graph
+  unsigned rec_flags = cudaEventRecordDefault;
+  if (trace) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return KVC_ERR_CUDA;
+    if (cs == cudaStreamCaptureStatusActive) rec_flags = cudaEventRecordExternal;
+  }
+  if (max_pages > 0) {
+    if (trace && cudaEventRecordWithFlags(static_cast<cudaEvent_t>(c->trace_start), st, rec_flags) != cudaSuccess)
+      return KVC_ERR_CUDA;
+    if (kvc::launch_attention_split(c->dev, seq_begin, batch, static_cast<const uint16_t*>(d_q), qk_scale_log2, w,
+                                    h2o, st) != cudaSuccess)
+      return KVC_ERR_CUDA;
+    ++launches;
+    if (trace && cudaEventRecordWithFlags(static_cast<cudaEvent_t>(c->trace_stop), st, rec_flags) != cudaSuccess)
+      return KVC_ERR_CUDA;
+  }
+  if (kvc::launch_attention_merge(c->dev, seq_begin, batch, static_cast<const uint16_t*>(d_q),
+                                  static_cast<uint16_t*>(d_out), qk_scale_log2, w, h2o, st) != cudaSuccess)
+    return KVC_ERR_CUDA;
+  ++launches;
+  c->last_launches = launches;
+  return KVC_OK;
+}
+
+kvc_status kvc_h2o_select_evict(kvc_cache* c, int32_t seq_begin, int32_t batch, const kvc_evict_params* p,
+                                uint8_t* d_keep_mask, void* d_workspace, size_t workspace_bytes, void* stream) {
+  if (!c) return KVC_ERR_INVALID_ARG;
+  c->last_launches = 0;
+  if (!range_ok(c, seq_begin, batch) || !p || !d_keep_mask) return KVC_ERR_INVALID_ARG;
+  if (p->mode == KVC_EVICT_H2O) {
+    if (p->recent < 0 || p->budget < kvc::kSinks + p->recent) return KVC_ERR_INVALID_ARG;
+  } else if (p->mode == KVC_EVICT_STREAMING) {
+    if (p->window < 1) return KVC_ERR_INVALID_ARG;
+  } else {
+    return KVC_ERR_INVALID_ARG;
+  }
+  const WsLayout wl = ws_layout(c, batch);
+  if (!d_workspace || !aligned(d_workspace, kAlign) || workspace_bytes < wl.total) return KVC_ERR_INVALID_ARG;
+  std::vector<int32_t> plan(batch);
+  int max_s = 0;
+  for (int i = 0; i < batch; ++i) {
+    const int b = seq_begin + i;
+    const int S = c->slots[b], ns = std::min(c->pos[b], kvc::kSinks);
+    int keep;
+    if (p->mode == KVC_EVICT_H2O)
+      keep = (ns + S <= p->budget) ? S : p->budget - kvc::kSinks;
+    else
+      keep = (S <= p->window) ? S : p->window;
+    plan[i] = keep;
+    max_s = std::max(max_s, S);
+  }
+  uint8_t* ws = static_cast<uint8_t*>(d_workspace);
+  kvc::SelectArgs a{};
+  a.mode = p->mode;
+  a.budget = p->budget;
+  a.recent = p->recent;
+  a.window = p->window;
+  a.s_cap = s_cap(c);
+  a.smem_slots = max_s <= kvc::select_max_smem_slots() ? std::max(max_s, 1) : 0;
+  a.g_keys = reinterpret_cast<uint32_t*>(ws + wl.keys);
+  a.g_pos = reinterpret_cast<int32_t*>(ws + wl.pos);
+  if (kvc::launch_select(c->dev, seq_begin, batch, a, d_keep_mask, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return KVC_ERR_CUDA;
+  c->last_launches = 1;
+  c->plan_pending = true;
+  c->plan_begin = seq_begin;
+  c->plan_batch = batch;
+  c->plan_new = plan;
+  return KVC_OK;
+}
+
+kvc_status kvc_compact_blocks(kvc_cache* c, int32_t seq_begin, int32_t batch, const uint8_t* d_keep_mask,
+                              void* d_workspace, size_t workspace_bytes, void* stream) {
+  if (!c) return KVC_ERR_INVALID_ARG;
+  c->last_launches = 0;
+  if (!range_ok(c, seq_begin, batch) || !d_keep_mask) return KVC_ERR_INVALID_ARG;
+  if (!c->plan_pending || c->plan_begin != seq_begin || c->plan_batch != batch) return KVC_ERR_STATE;
+  const WsLayout wl = ws_layout(c, batch);
+  if (!d_workspace || !aligned(d_workspace, kAlign) || workspace_bytes < wl.total) return KVC_ERR_INVALID_ARG;
+  uint8_t* ws = static_cast<uint8_t*>(d_workspace);
+  if (kvc::launch_compact(c->dev, seq_begin, batch, d_keep_mask, s_cap(c), reinterpret_cast<int32_t*>(ws + wl.keys),
+                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return KVC_ERR_CUDA;
+  c->last_launches = 1;
+  for (int i = 0; i < batch; ++i) c->slots[seq_begin + i] = c->plan_new[i];
+  c->plan_pending = false;
+  return KVC_OK;
+}
+
+kvc_status kvc_read_status(kvc_cache* c, int32_t* h_status, void* stream) {
+  if (!c || !h_status) return KVC_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, c->dev.counters + kvc::kCtrStatus, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return KVC_ERR_CUDA;
+  *h_status = v;
+  if (v != 0) {
+    if (cudaMemsetAsync(c->dev.counters + kvc::kCtrStatus, 0, 4, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+      return KVC_ERR_CUDA;
+    return KVC_ERR_DEVICE;
+  }
+  return KVC_OK;
+}
+
+kvc_status kvc_set_trace_events(kvc_cache* c, void* ev_start, void* ev_stop) {
+  if (!c || ((ev_start == nullptr) != (ev_stop == nullptr))) return KVC_ERR_INVALID_ARG;
+  c->trace_start = ev_start;
+  c->trace_stop = ev_stop;
+  return KVC_OK;
+}
+
+int32_t kvc_last_launch_count(const kvc_cache* c) { return c ? c->last_launches : 0; }
+
+}  // extern "C"

@@ -1,0 +1,84 @@
+// Internal declarations shared by the host side (kvc_host.cpp) and the
+// kernels (kvc_*.cu) of the compressed-KV library.  Not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kvc {
+
+constexpr int kHeadDim = 128;
+constexpr int kPage = 16;
+constexpr int kSinks = 4;
+constexpr int kMaxGroup = 8;     // query heads per KV head handled by one MMA column tile
+constexpr int kCounters = 64;    // int32 counters block
+
+// Device view of one layer's cache state (passed to kernels by value).
+struct DevState {
+  uint8_t* k_codes;     // [num_blocks][hkv][16][row_bytes]
+  uint8_t* v_codes;
+  float* k_scale;       // [num_blocks][hkv][16]
+  float* v_scale;
+  int32_t* slot_pos;
+  float* score;
+  uint16_t* sink_k;     // [max_batch][hkv][4][128] bf16
+  uint16_t* sink_v;
+  float* sink_score;    // [max_batch][hkv][4]
+  int32_t* block_table; // [max_batch][max_bps]
+  int32_t* seq_slots;   // [max_batch]
+  int32_t* seq_pos;     // [max_batch]
+  int32_t* free_stack;  // [num_blocks]
+  int32_t* counters;    // [0] free top, [1] status
+  int32_t* plan;        // [max_batch][2]
+  int32_t hq, hkv, group, bits, row_bytes, num_blocks, max_batch, max_bps;
+};
+
+enum { kCtrFreeTop = 0, kCtrStatus = 1 };
+
+// Status bits (mirror kvc.h).
+constexpr int kDevOutOfBlocks = 0x1;
+constexpr int kDevBadBlockId = 0x2;
+constexpr int kDevBadKeepMask = 0x4;
+constexpr int kDevTableOverflow = 0x8;
+constexpr int kDevStackOverflow = 0x10;
+
+// Scratch carved from the caller's workspace for one call.
+struct AttnWork {
+  float* part_o;    // [batch][hkv][nsplit][group][128]
+  float* part_ml;   // [batch][hkv][nsplit][group][2]
+  float* logits;    // [batch][hkv][s_cap][group]  (log2 domain)
+  float* stats;     // [batch][hq][2]  global (M, L) per query head
+  int nsplit;
+  int pages_per_split;
+  int s_cap;
+};
+
+// ---- launchers (return cudaGetLastError of the launch) -------------------
+cudaError_t launch_append(const DevState& s, int seq_begin, int batch, int n_new,
+                          const uint16_t* k, const uint16_t* v, cudaStream_t st);
+cudaError_t launch_fill_free_stack(const DevState& s, cudaStream_t st);
+
+cudaError_t launch_attention_split(const DevState& s, int seq_begin, int batch, const uint16_t* q,
+                                   float qk_scale_log2, const AttnWork& w, bool spill_logits,
+                                   cudaStream_t st);
+cudaError_t launch_attention_merge(const DevState& s, int seq_begin, int batch, const uint16_t* q,
+                                   uint16_t* out, float qk_scale_log2, const AttnWork& w,
+                                   bool accumulate_h2o, cudaStream_t st);
+
+struct SelectArgs {
+  int mode, budget, recent, window;
+  int s_cap;            // mask row stride
+  int smem_slots;       // > 0: keys/pos staged in shared memory (capacity in slots)
+  uint32_t* g_keys;     // global fallback [batch][hkv][s_cap]
+  int32_t* g_pos;
+};
+cudaError_t launch_select(const DevState& s, int seq_begin, int batch, const SelectArgs& a,
+                          uint8_t* keep_mask, cudaStream_t st);
+cudaError_t launch_compact(const DevState& s, int seq_begin, int batch, const uint8_t* keep_mask,
+                           int s_cap, int32_t* g_scratch, cudaStream_t st);
+
+int attention_smem_bytes(int bits);
+int select_max_smem_slots();
+
+}  // namespace kvc

@@ -1,0 +1,240 @@
+/*
+ * kvc.h -- C ABI of the compressed-KV decode step on one GPU (sm_103a).
+ *
+ * One decode step of one layer is four calls, issued in this order on one CUDA
+ * stream:
+ *
+ *   kvc_quantize_append   write the new token's K/V: per-token INT8/INT4 codes
+ *                         into the paged pool, attention sinks kept in bf16;
+ *   kvc_decode_attention  single-query, GQA-aware paged attention with the
+ *                         dequantisation fused into QK^T and PV, plus the H2O
+ *                         heavy-hitter score accumulation;
+ *   kvc_h2o_select_evict  per KV head, choose the kept set (sinks + recent
+ *                         window + top-k heavy hitters, or StreamingLLM);
+ *   kvc_compact_blocks    move the kept tokens into the evicted slots and give
+ *                         the emptied pages back to the pool.
+ *
+ * Sources (page title, section):
+ *   - "KV Cache optimization techniques" (metaphor-xennon): 1.2 per-token
+ *     quantisation, 2.2 H2O, 2.4 StreamingLLM cache, 3.2 PagedAttention cache;
+ *   - "Technical Report: KV Cache Compression for Text-Only Large Language
+ *     Models": 1.1 attention, 3.2 INT8 quantisation with dequantisation fused
+ *     into the attention kernel and sinks kept in half precision, 3.3 sliding
+ *     window, 3.4 H2O eviction;
+ *   - "KV cache eviction and reuse survey" (tbxsx.cn): 3.3 H2O objective.
+ *
+ * Conventions shared by every call
+ *   - The caller owns all device memory and the stream.  The library never
+ *     allocates or frees device memory; pointers are borrowed for the call.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
+ *     void*; NULL = legacy default stream).  Nothing synchronises except
+ *     kvc_read_status, kvc_cache_reset and kvc_cache_sync_host.
+ *   - Errors the host can see (bad arguments, unsupported shapes, pool
+ *     exhaustion, call-order violations) are returned before anything is
+ *     enqueued; the cache is then unchanged.  Errors found on the device set
+ *     bits in a device status word (KVC_DEV_*), read by kvc_read_status; the
+ *     kernels skip the offending access, they never trap.
+ *   - Tensors are row-major and densely packed.  bf16 tensors are raw 16-bit
+ *     words.  "batch" always means the contiguous slice of sequences
+ *     [seq_begin, seq_begin + batch) of the cache.
+ *   - A cache handle is not thread-safe; one handle per layer.
+ */
+#ifndef KVC_H
+#define KVC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KVC_OK = 0,
+  KVC_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, out-of-range value      */
+  KVC_ERR_UNSUPPORTED = 2,  /* head_dim != 128, page_size != 16, bits not 4|8,
+                               more than 8 query heads per KV head             */
+  KVC_ERR_CAPACITY = 3,     /* pool or per-sequence block table would overflow
+                               (the page's allocate_sequence returning False)  */
+  KVC_ERR_CUDA = 4,         /* a CUDA runtime call failed                      */
+  KVC_ERR_DEVICE = 5,       /* kvc_read_status found device status bits set    */
+  KVC_ERR_STATE = 6         /* call order violated (compact without select)    */
+} kvc_status;
+
+/* Device status bits (kvc_read_status). */
+#define KVC_DEV_OUT_OF_BLOCKS   0x1  /* free-block stack ran empty during append */
+#define KVC_DEV_BAD_BLOCK_ID    0x2  /* a block-table entry outside [0, num_blocks) */
+#define KVC_DEV_BAD_KEEP_MASK   0x4  /* keep mask count differs from the plan     */
+#define KVC_DEV_TABLE_OVERFLOW  0x8  /* per-sequence block table overflow         */
+#define KVC_DEV_STACK_OVERFLOW  0x10 /* free-block stack overflow on release      */
+
+/* Geometry of one layer's cache. */
+typedef struct {
+  int32_t num_q_heads;        /* Hq                                             */
+  int32_t num_kv_heads;       /* Hkv; Hq % Hkv == 0 and Hq / Hkv <= 8            */
+  int32_t head_dim;           /* must be 128                                    */
+  int32_t page_size;          /* tokens per block, must be 16                   */
+  int32_t bits;               /* 8 (INT8) or 4 (INT4, two codes per byte)       */
+  int32_t num_blocks;         /* physical blocks in the pool                    */
+  int32_t max_batch;          /* sequences the cache holds                      */
+  int32_t max_blocks_per_seq; /* block-table row length                         */
+} kvc_config;
+
+/* Opaque host handle of one layer's cache (host mirror of the sequence
+ * lengths, buffer offsets, launch policy). */
+typedef struct kvc_cache kvc_cache;
+
+/* Buffers carved out of the caller's state allocation (kvc_cache_buffer). */
+typedef enum {
+  KVC_BUF_K_CODES = 0,    /* u8  [num_blocks][Hkv][16][128*bits/8]; INT4: code
+                             2i in the low nibble of byte i, two's complement */
+  KVC_BUF_V_CODES = 1,    /* same layout as K                                  */
+  KVC_BUF_K_SCALE = 2,    /* f32 [num_blocks][Hkv][16]  amax/127 or amax/7      */
+  KVC_BUF_V_SCALE = 3,    /* f32 [num_blocks][Hkv][16]                          */
+  KVC_BUF_SLOT_POS = 4,   /* i32 [num_blocks][Hkv][16]  token position per slot */
+  KVC_BUF_SCORE = 5,      /* f32 [num_blocks][Hkv][16]  accumulated H2O score   */
+  KVC_BUF_SINK_K = 6,     /* bf16 [max_batch][Hkv][4][128] positions 0..3       */
+  KVC_BUF_SINK_V = 7,     /* bf16 [max_batch][Hkv][4][128]                      */
+  KVC_BUF_SINK_SCORE = 8, /* f32 [max_batch][Hkv][4]                            */
+  KVC_BUF_BLOCK_TABLE = 9,/* i32 [max_batch][max_blocks_per_seq]               */
+  KVC_BUF_SEQ_SLOTS = 10, /* i32 [max_batch]  pool slots in use (non-sink tokens)*/
+  KVC_BUF_SEQ_POS = 11,   /* i32 [max_batch]  positions seen (tokens appended) */
+  KVC_BUF_FREE_STACK = 12,/* i32 [num_blocks] free block ids (stack)            */
+  KVC_BUF_COUNTERS = 13,  /* i32 [64]: [0] free-stack top, [1] status word,
+                             [2..] plan scratch                                */
+  KVC_BUF_PLAN = 14,      /* i32 [max_batch][2] (slots before, slots after) of
+                             the last selection                                */
+  KVC_BUF_COUNT = 15
+} kvc_buffer_id;
+
+/* Flags of kvc_decode_attention. */
+#define KVC_ATTN_ACCUM_H2O 0x1  /* add this step's probabilities to the scores */
+
+/* Eviction modes of kvc_h2o_select_evict. */
+#define KVC_EVICT_H2O       0
+#define KVC_EVICT_STREAMING 1
+
+typedef struct {
+  int32_t mode;    /* KVC_EVICT_H2O or KVC_EVICT_STREAMING                      */
+  int32_t budget;  /* H2O: tokens kept including the 4 sinks; >= 4 + recent    */
+  int32_t recent;  /* H2O: recent window kept unconditionally                  */
+  int32_t window;  /* StreamingLLM: recent window (sinks kept besides it)      */
+} kvc_evict_params;
+
+/* ---------------------------------------------------------------- set-up -- */
+
+/* Bytes of device memory one layer's cache state needs (all buffers above,
+ * each 256-byte aligned).  Returns 0 for an invalid or unsupported config. */
+size_t kvc_state_bytes(const kvc_config* cfg);
+
+/* Create a host handle over caller-owned device memory `d_state` (at least
+ * kvc_state_bytes bytes, 256-byte aligned).  Touches no GPU.  *out receives
+ * the handle; release it with kvc_cache_destroy (which frees host memory only). */
+kvc_status kvc_cache_create(const kvc_config* cfg, void* d_state, size_t state_bytes,
+                            kvc_cache** out);
+void kvc_cache_destroy(kvc_cache* cache);
+
+/* Empty the cache: zero every buffer, fill the free-block stack with
+ * `h_block_order` (host array of num_blocks distinct ids, popped from its end;
+ * NULL = ascending ids) and zero the host mirror.  Synchronises `stream`. */
+kvc_status kvc_cache_reset(kvc_cache* cache, const int32_t* h_block_order, void* stream);
+
+/* Device pointer and size of one buffer of the state (for inspection). */
+kvc_status kvc_cache_buffer(const kvc_cache* cache, int32_t which, void** d_ptr, size_t* bytes);
+
+/* Host mirror of one sequence: pool slots used and positions seen. */
+kvc_status kvc_cache_lengths(const kvc_cache* cache, int32_t seq, int32_t* slots, int32_t* positions);
+
+/* Reload the host mirror from the device state (after the caller restored the
+ * state bytes from a snapshot).  Synchronises `stream`. */
+kvc_status kvc_cache_sync_host(kvc_cache* cache, void* stream);
+
+/* Scratch bytes kvc_decode_attention / kvc_h2o_select_evict /
+ * kvc_compact_blocks need for a slice of `batch` sequences (one size fits all
+ * three calls; the buffer may be reused between calls on the same stream). */
+size_t kvc_workspace_bytes(const kvc_cache* cache, int32_t batch);
+
+/* ---------------------------------------------------------------- step ---- */
+
+/* Quantise-on-write ("KV Cache optimization techniques" 1.2; Technical Report
+ * 3.2).  Appends n_new tokens to each sequence of the slice.
+ *   d_k, d_v: bf16 [batch][Hkv][n_new][128] on the device, 8-byte aligned.
+ * For every (token, KV head) row of K and of V: amax over the 128 values,
+ * scale = amax / 127 (INT8) or amax / 7 (INT4) in IEEE fp32, code =
+ * round-half-even(x / scale) (IEEE fp32 division) clamped to [-127, 127] or
+ * [-8, 7]; a zero row has scale 0 and codes 0.  Tokens at positions 0..3 are
+ * attention sinks: stored unchanged in bf16 and never quantised (Technical
+ * Report 3.2).  New pages come from the device free-block stack; their score
+ * starts at 0.  n_new == 0 is a no-op.
+ * Errors: KVC_ERR_CAPACITY when a sequence would exceed max_blocks_per_seq
+ * pages or the pool has too few free blocks (nothing is written). */
+kvc_status kvc_quantize_append(kvc_cache* cache, int32_t seq_begin, int32_t batch, int32_t n_new,
+                               const void* d_k, const void* d_v, void* stream);
+
+/* Decode attention with fused dequantisation (Technical Report 1.1 and 3.2)
+ * and H2O score accumulation (Technical Report 3.4).
+ *   d_q:   bf16 [batch][Hq][128] one query per head, 16-byte aligned;
+ *   d_out: bf16 [batch][Hq][128].
+ * Query head j reads KV head j / (Hq/Hkv).  For each query head:
+ *   out = softmax(sm_scale * q . k_t) . v_t over the sinks (bf16 values) and
+ *   every pool slot (k_t = code * scale), accumulated in fp32.
+ * With KVC_ATTN_ACCUM_H2O, every attended token's score (sinks included) grows
+ * by the sum over the query heads of its KV head of its softmax probability.
+ * Every sequence of the slice must hold at least one token.
+ * d_workspace: kvc_workspace_bytes(cache, batch) bytes, 256-byte aligned. */
+kvc_status kvc_decode_attention(kvc_cache* cache, int32_t seq_begin, int32_t batch,
+                                const void* d_q, void* d_out, float sm_scale, int32_t flags,
+                                void* d_workspace, size_t workspace_bytes, void* stream);
+
+/* Kept-set selection per (sequence, KV head) ("KV Cache optimization
+ * techniques" 2.2 and 2.4; Technical Report 3.3 and 3.4).
+ * Let S = pool slots, P = positions seen, ns = min(P, 4) sinks.
+ *   H2O: if ns + S <= budget keep everything; otherwise keep the recent
+ *     window (positions >= P - recent) and, of the other slots, the
+ *     budget - 4 - recent with the highest score, ties to the lower position.
+ *   StreamingLLM: if S <= window keep everything; otherwise keep positions
+ *     >= P - window.
+ * The sinks are always kept and are not part of the mask.
+ *   d_keep_mask: u8 [batch][Hkv][max_blocks_per_seq*16], entry t = 1 if pool
+ *   slot t is kept (entries >= S are left unspecified).
+ * Records the plan (S, kept slots) that kvc_compact_blocks applies. */
+kvc_status kvc_h2o_select_evict(kvc_cache* cache, int32_t seq_begin, int32_t batch,
+                                const kvc_evict_params* params, uint8_t* d_keep_mask,
+                                void* d_workspace, size_t workspace_bytes, void* stream);
+
+/* Compaction ("KV Cache optimization techniques" 2.2: gather the kept tokens;
+ * 3.2: release blocks).  With n' kept slots, every evicted slot below n' is
+ * filled, in ascending order, by the kept slots at or above n', in ascending
+ * order (codes, scales, position, score move together); the sequence then
+ * holds n' slots and the pages past ceil(n'/16) return to the free stack.
+ * Attention is invariant under the order of the attended tokens, so the
+ * result attends to exactly the kept set.
+ *   d_keep_mask: the mask kvc_h2o_select_evict wrote for the same slice.
+ * Errors: KVC_ERR_STATE if the slice has no pending selection. */
+kvc_status kvc_compact_blocks(kvc_cache* cache, int32_t seq_begin, int32_t batch,
+                              const uint8_t* d_keep_mask, void* d_workspace,
+                              size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------- misc ---- */
+
+/* Synchronise `stream`, copy the device status word to *h_status and clear
+ * it.  Returns KVC_ERR_DEVICE when any bit was set. */
+kvc_status kvc_read_status(kvc_cache* cache, int32_t* h_status, void* stream);
+
+/* Tracing: when both are non-NULL, the next kvc_decode_attention calls record
+ * `ev_start` (a cudaEvent_t) just before the split-K attention kernel and
+ * `ev_stop` just after it, on the call's stream.  NULL, NULL turns it off. */
+kvc_status kvc_set_trace_events(kvc_cache* cache, void* ev_start, void* ev_stop);
+
+/* Number of kernels the last call on this handle enqueued. */
+int32_t kvc_last_launch_count(const kvc_cache* cache);
+
+const char* kvc_status_string(kvc_status status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int32_t kvc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVC_H */

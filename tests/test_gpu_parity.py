@@ -1,0 +1,361 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Bars (stated here, derived in the design doc):
+  * INT8/INT4 codes, fp32 scales, positions, bf16 sinks: bit-exact;
+  * kept sets: identical when the oracle selects on the GPU's own scores;
+    against the oracle's fp64 scores, different only within 1e-5 relative of
+    the k-th score;
+  * attention outputs (bf16): |gpu - ref| <= 2e-3 + 1e-2 |ref| elementwise;
+  * H2O scores (fp32 vs fp64): |gpu - ref| <= 1e-6 + 1e-4 |ref|.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import kvc_oracle as O
+from tests import kvc_testlib as T
+
+pytestmark = pytest.mark.gpu
+
+SCORE_ATOL, SCORE_RTOL = 1e-6, 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from compressed_kv_cache_kvc_gb300.build import build_library
+    build_library()
+
+
+def _cache(hq, hkv, bits, batch, max_ctx, extra_blocks=0, block_order=None):
+    from compressed_kv_cache_kvc_gb300.cache import KVCache
+    mbps = (max_ctx + 15) // 16 + 2
+    nb = batch * mbps + extra_blocks
+    return KVCache(hq, hkv, bits, nb, batch, mbps, block_order=block_order)
+
+
+def _rand_bits(rng, shape, scale=1.0, outliers=None):
+    from compressed_kv_cache_kvc_gb300.workloads import bf16_bits
+    x = rng.standard_normal(shape).astype(np.float32) * np.float32(scale)
+    if outliers is not None:
+        x[..., outliers] *= 10
+    return bf16_bits(x)
+
+
+def _prefill(cache, k_bits, v_bits, lengths):
+    for b, n in enumerate(lengths):
+        n = int(n)
+        if n == 0:
+            continue
+        k = T.to_dev_bf16(np.ascontiguousarray(k_bits[b:b + 1, :, :n]))
+        v = T.to_dev_bf16(np.ascontiguousarray(v_bits[b:b + 1, :, :n]))
+        cache.quantize_append(k, v, seq_begin=b)
+
+
+def _oracle(hq, bits, k_bits, v_bits, lengths):
+    return T.oracle_from_inputs(hq, bits, k_bits, v_bits, lengths)
+
+
+# ---------------------------------------------------------------------------
+# quantise-on-write
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_append_codes_bit_exact(bits):
+    rng = np.random.default_rng(100 + bits)
+    B, hq, hkv, T_ = 4, 8, 2, 300
+    lengths = [1, 4, 17, 300]          # sinks only / exactly the sinks / page edge / ragged
+    k = _rand_bits(rng, (B, hkv, T_, 128), outliers=[3, 50])
+    v = _rand_bits(rng, (B, hkv, T_, 128))
+    k[2, 0, 9] = 0                     # an all-zero row: scale 0, codes 0
+    cache = _cache(hq, hkv, bits, B, T_ + 8)
+    _prefill(cache, k, v, lengths)
+    # then one batched decode append
+    kn = _rand_bits(rng, (B, hkv, 1, 128))
+    vn = _rand_bits(rng, (B, hkv, 1, 128))
+    cache.quantize_append(T.to_dev_bf16(kn), T.to_dev_bf16(vn))
+    ora = _oracle(hq, bits, k, v, lengths)
+    for b in range(B):
+        ora.append(b, O.bf16_bits_to_f32(kn[b]), O.bf16_bits_to_f32(vn[b]))
+    st = T.StateView(cache)
+    for b in range(B):
+        assert st.slots[b] == max(0, lengths[b] + 1 - 4)
+        assert st.seen[b] == lengths[b] + 1
+        assert cache.lengths(b) == (int(st.slots[b]), int(st.seen[b]))
+        for h in range(hkv):
+            T.check_codes(st, ora, b, h)
+    assert cache.read_status() == 0
+
+
+def test_append_prefill_sink_boundary_split():
+    # sinks arrive over several appends: 2 tokens, then 1, then 5
+    rng = np.random.default_rng(7)
+    hq, hkv = 4, 4
+    cache = _cache(hq, hkv, 8, 1, 64)
+    ora = O.OracleCache(1, hq, hkv, 8)
+    for n in (2, 1, 5, 16, 1):
+        k = _rand_bits(rng, (1, hkv, n, 128))
+        v = _rand_bits(rng, (1, hkv, n, 128))
+        cache.quantize_append(T.to_dev_bf16(k), T.to_dev_bf16(v))
+        ora.append(0, O.bf16_bits_to_f32(k[0]), O.bf16_bits_to_f32(v[0]))
+    st = T.StateView(cache)
+    assert st.seen[0] == 25 and st.slots[0] == 21
+    for h in range(hkv):
+        T.check_codes(st, ora, 0, h)
+
+
+# ---------------------------------------------------------------------------
+# attention (+ H2O score accumulation)
+# ---------------------------------------------------------------------------
+
+ATTN_CASES = [
+    # bits, hq, hkv, context
+    (8, 8, 8, 700),
+    (8, 32, 8, 1000),
+    (4, 40, 8, 999),
+    (8, 8, 1, 333),
+    (4, 4, 4, 50),
+    (8, 10, 2, 3),      # all sinks
+    (4, 8, 2, 5),       # one pool slot
+    (8, 16, 4, 20),     # one full page + ragged tail
+    (4, 6, 2, 4100),    # many splits
+]
+
+
+@pytest.mark.parametrize("bits,hq,hkv,ctx", ATTN_CASES)
+def test_decode_attention_and_scores(bits, hq, hkv, ctx):
+    rng = np.random.default_rng(bits * 1000 + hq * 10 + ctx)
+    B = 2
+    lengths = [ctx, max(1, ctx // 2 + 3)]
+    k = _rand_bits(rng, (B, hkv, ctx, 128), outliers=[1, 2, 77, 100])
+    v = _rand_bits(rng, (B, hkv, ctx, 128))
+    q = _rand_bits(rng, (B, hq, 128))
+    cache = _cache(hq, hkv, bits, B, ctx + 4)
+    _prefill(cache, k, v, lengths)
+    out = cache.decode_attention(T.to_dev_bf16(q), accumulate_h2o=True)
+    gpu = T.bf16_tensor_to_f32(out)
+    ora = _oracle(hq, bits, k, v, lengths)
+    st = T.StateView(cache)
+    for b in range(B):
+        ref = ora.attend(b, O.bf16_bits_to_f32(q[b]), T.sm_scale(), accumulate=True)
+        T.assert_attention_close(gpu[b], ref, f"b={b}")
+        s = ora.seqs[b]
+        for h in range(hkv):
+            pos, *_, sc = st.head(b, h)
+            hs = s.heads[h]
+            want = dict(zip(hs.pos.tolist(), hs.score.tolist()))
+            w = np.array([want[p] for p in pos.tolist()])
+            assert np.all(np.abs(sc - w) <= SCORE_ATOL + SCORE_RTOL * np.abs(w)), (b, h)
+            ns = s.sink_k[h].shape[0]
+            ss = st.sink_score[b, h, :ns]
+            assert np.all(np.abs(ss - s.sink_score[h]) <= SCORE_ATOL + SCORE_RTOL * np.abs(s.sink_score[h]))
+            # invariant: this step's increments sum to the group size
+            assert abs(sc.sum() + ss.sum() - hq // hkv) <= 1e-4 * (hq // hkv)
+    assert cache.read_status() == 0
+
+
+def test_attention_without_h2o_leaves_scores():
+    rng = np.random.default_rng(3)
+    hq, hkv, ctx = 8, 2, 200
+    k = _rand_bits(rng, (1, hkv, ctx, 128))
+    v = _rand_bits(rng, (1, hkv, ctx, 128))
+    q = _rand_bits(rng, (1, hq, 128))
+    cache = _cache(hq, hkv, 8, 1, ctx + 4)
+    _prefill(cache, k, v, [ctx])
+    cache.decode_attention(T.to_dev_bf16(q), accumulate_h2o=False)
+    st = T.StateView(cache)
+    assert np.all(st.head(0, 0)[5] == 0) and np.all(st.sink_score == 0)
+
+
+def test_attention_planted_token_and_scaled_inputs():
+    # a token aligned with q dominates; inputs far from unit scale keep parity
+    rng = np.random.default_rng(11)
+    hq, hkv, ctx = 4, 1, 400
+    from compressed_kv_cache_kvc_gb300.workloads import bf16_bits
+    qf = rng.standard_normal((1, hq, 128)).astype(np.float32) * 3e-3
+    kf = rng.standard_normal((1, hkv, ctx, 128)).astype(np.float32) * 200.0
+    vf = rng.standard_normal((1, hkv, ctx, 128)).astype(np.float32) * 1e-3
+    kf[0, 0, 123] = qf[0].mean(0) * 5e5
+    q, k, v = bf16_bits(qf), bf16_bits(kf), bf16_bits(vf)
+    cache = _cache(hq, hkv, 8, 1, ctx + 4)
+    _prefill(cache, k, v, [ctx])
+    gpu = T.bf16_tensor_to_f32(cache.decode_attention(T.to_dev_bf16(q)))
+    ora = _oracle(hq, 8, k, v, [ctx])
+    ref = ora.attend(0, O.bf16_bits_to_f32(q[0]), T.sm_scale())
+    # relative bound only (outputs are ~1e-3): scale the absolute term
+    err = np.abs(gpu[0] - ref)
+    assert np.all(err <= 2e-3 * 1e-3 + 1e-2 * np.abs(ref)), err.max()
+
+
+# ---------------------------------------------------------------------------
+# the whole step: append -> attention -> select -> compact, in lock-step
+# ---------------------------------------------------------------------------
+
+def _run_steps(hq, hkv, bits, k, v, lengths, steps, mode, budget=0, recent=0, window=0, seed=0,
+               block_order=None):
+    rng = np.random.default_rng(seed)
+    B = k.shape[0]
+    G = hq // hkv
+    cache = _cache(hq, hkv, bits, B, max(lengths) + steps + 4, block_order=block_order)
+    if block_order is not None:
+        pass
+    _prefill(cache, k, v, lengths)
+    ora = _oracle(hq, bits, k, v, lengths)
+    h2o = mode == "h2o"
+    stats = dict(max_err=0.0, tie_diffs=0)
+    for step in range(steps):
+        kn = _rand_bits(rng, (B, hkv, 1, 128))
+        vn = _rand_bits(rng, (B, hkv, 1, 128))
+        q = _rand_bits(rng, (B, hq, 128))
+        cache.quantize_append(T.to_dev_bf16(kn), T.to_dev_bf16(vn))
+        out = cache.decode_attention(T.to_dev_bf16(q), accumulate_h2o=h2o)
+        gpu = T.bf16_tensor_to_f32(out)
+        pre = T.StateView(cache)
+        mask = cache.h2o_select_evict(B, mode=mode, budget=budget, recent=recent, window=window)
+        mask_h = mask.cpu().numpy()
+        cache.compact_blocks(mask, B)
+        post = T.StateView(cache)
+        for b in range(B):
+            ora.append(b, O.bf16_bits_to_f32(kn[b]), O.bf16_bits_to_f32(vn[b]))
+            ref = ora.attend(b, O.bf16_bits_to_f32(q[b]), T.sm_scale(), accumulate=h2o)
+            stats["max_err"] = max(stats["max_err"], T.assert_attention_close(gpu[b], ref, f"step {step} b={b}"))
+            P = int(pre.seen[b])
+            for h in range(hkv):
+                T.check_codes(pre, ora, b, h)
+                pos, kc, ks, vc, vs, sc = pre.head(b, h)
+                S = pos.size
+                kept_gpu = set(pos[mask_h[b, h, :S] == 1].tolist())
+                ns = min(P, 4)
+                hs = ora.seqs[b].heads[h]
+                if h2o:
+                    want = dict(zip(hs.pos.tolist(), hs.score.tolist()))
+                    w = np.array([want[p] for p in pos.tolist()])
+                    assert np.all(np.abs(sc - w) <= SCORE_ATOL + SCORE_RTOL * np.abs(w)), (step, b, h)
+                    # exact: the oracle's rule on the GPU's own scores
+                    exact = O.select_h2o(pos, sc.astype(np.float64), P, budget, recent, ns)
+                    assert set(pos[exact].tolist()) == kept_gpu, (step, b, h)
+                    # against the oracle's own scores: near-ties only
+                    om = O.select_h2o(hs.pos, hs.score, P, budget, recent, ns)
+                    kept_ora = set(hs.pos[om].tolist())
+                    heavy = budget - 4 - recent
+                    if kept_gpu != kept_ora:
+                        stats["tie_diffs"] += 1
+                    assert T.kept_sets_agree(kept_gpu, kept_ora, hs.pos, hs.score, heavy, P - recent), (step, b, h)
+                else:
+                    om = O.select_streaming(hs.pos, P, window, ns)
+                    assert set(hs.pos[om].tolist()) == kept_gpu, (step, b, h)
+                    if S > window:
+                        assert kept_gpu == set(range(P - window, P))
+                # compaction: kept multiset moved intact
+                keep_idx = np.nonzero(mask_h[b, h, :S] == 1)[0]
+                ppos, pkc, pks, pvc, pvs, psc = post.head(b, h)
+                assert ppos.size == keep_idx.size
+                o1 = np.argsort(pos[keep_idx])
+                o2 = np.argsort(ppos)
+                assert np.array_equal(pos[keep_idx][o1], ppos[o2])
+                assert np.array_equal(kc[keep_idx][o1], pkc[o2]) and np.array_equal(vc[keep_idx][o1], pvc[o2])
+                assert np.array_equal(ks[keep_idx][o1].view(np.uint32), pks[o2].view(np.uint32))
+                assert np.array_equal(vs[keep_idx][o1].view(np.uint32), pvs[o2].view(np.uint32))
+                assert np.array_equal(sc[keep_idx][o1].view(np.uint32), psc[o2].view(np.uint32))
+                # kept slots below n' did not move
+                npr = keep_idx.size
+                stay = keep_idx[keep_idx < npr]
+                assert np.array_equal(pos[stay], ppos[stay])
+            T.load_oracle_from_state(ora, post, b)
+        # block conservation: used + free = all, no id twice
+        used = np.concatenate([post.used_blocks(b) for b in range(B)] + [np.zeros(0, np.int32)])
+        top = int(post.counters[0])
+        free = post.free_stack[:top]
+        allb = np.concatenate([used, free])
+        assert allb.size == post.num_blocks and np.unique(allb).size == post.num_blocks
+        assert cache.read_status() == 0
+    return stats
+
+
+def test_tiny_workload_h2o_eight_steps():
+    from compressed_kv_cache_kvc_gb300 import workloads as W
+    w = W.WORKLOADS["tiny_b1_h8_t512_int8_h2o"]
+    d = W.gen_layer(w, 0)
+    st = _run_steps(w.num_q_heads, w.num_kv_heads, w.bits, d["k"], d["v"], d["lengths"], 8, "h2o",
+                    budget=w.budget, recent=w.recent, seed=5)
+    assert st["max_err"] < 2e-2
+
+
+@pytest.mark.parametrize("bits,hq,hkv", [(8, 32, 8), (4, 40, 8), (8, 8, 8)])
+def test_h2o_steps_gqa(bits, hq, hkv):
+    rng = np.random.default_rng(bits + hq)
+    B, ctx = 3, 600
+    lengths = [600, 433, 70]
+    k = _rand_bits(rng, (B, hkv, ctx, 128), outliers=[5, 9, 60, 61])
+    v = _rand_bits(rng, (B, hkv, ctx, 128))
+    _run_steps(hq, hkv, bits, k, v, lengths, 4, "h2o", budget=180, recent=40, seed=bits)
+
+
+def test_h2o_budget_covers_context_is_identity():
+    rng = np.random.default_rng(21)
+    hq, hkv, ctx = 8, 2, 150
+    k = _rand_bits(rng, (1, hkv, ctx, 128))
+    v = _rand_bits(rng, (1, hkv, ctx, 128))
+    _run_steps(hq, hkv, 8, k, v, [ctx], 2, "h2o", budget=4 + ctx + 10, recent=8, seed=1)
+
+
+def test_h2o_zero_heavy_and_only_sinks():
+    rng = np.random.default_rng(22)
+    hq, hkv, ctx = 4, 2, 90
+    k = _rand_bits(rng, (1, hkv, ctx, 128))
+    v = _rand_bits(rng, (1, hkv, ctx, 128))
+    _run_steps(hq, hkv, 8, k, v, [ctx], 2, "h2o", budget=4 + 16, recent=16, seed=2)
+    _run_steps(hq, hkv, 4, k, v, [ctx], 2, "h2o", budget=4, recent=0, seed=3)
+
+
+def test_streaming_ragged_steps():
+    rng = np.random.default_rng(23)
+    hq, hkv = 32, 8
+    lengths = [700, 100, 257, 260, 1000]
+    B, ctx = len(lengths), max(lengths)
+    k = _rand_bits(rng, (B, hkv, ctx, 128))
+    v = _rand_bits(rng, (B, hkv, ctx, 128))
+    _run_steps(hq, hkv, 8, k, v, lengths, 4, "streaming", window=256, seed=4)
+
+
+def test_shuffled_block_order():
+    rng = np.random.default_rng(24)
+    hq, hkv, ctx, B = 8, 8, 300, 2
+    k = _rand_bits(rng, (B, hkv, ctx, 128))
+    v = _rand_bits(rng, (B, hkv, ctx, 128))
+    mbps = (ctx + 3 + 4 + 15) // 16 + 2
+    order = np.random.default_rng(0).permutation(B * mbps).astype(np.int32)
+    _run_steps(hq, hkv, 8, k, v, [ctx, 211], 3, "h2o", budget=64, recent=16, seed=6, block_order=order)
+
+
+def test_capacity_error_leaves_cache_unchanged():
+    from compressed_kv_cache_kvc_gb300 import _lib as L
+    from compressed_kv_cache_kvc_gb300.cache import KVCache
+    rng = np.random.default_rng(25)
+    cache = KVCache(4, 2, 8, num_blocks=3, max_batch=1, max_blocks_per_seq=8)
+    k = _rand_bits(rng, (1, 2, 40, 128))
+    cache.quantize_append(T.to_dev_bf16(k), T.to_dev_bf16(k))  # 36 slots -> 3 blocks
+    before = cache.state_view.clone()
+    k1 = _rand_bits(rng, (1, 2, 13, 128))
+    with pytest.raises(L.KvcError) as ei:
+        cache.quantize_append(T.to_dev_bf16(k1), T.to_dev_bf16(k1))
+    assert ei.value.status == L.KVC_ERR_CAPACITY
+    torch.cuda.synchronize()
+    assert torch.equal(before, cache.state_view)
+    assert cache.lengths(0) == (36, 40)
+
+
+def test_launch_counts():
+    rng = np.random.default_rng(26)
+    cache = _cache(8, 2, 8, 1, 100)
+    k = _rand_bits(rng, (1, 2, 80, 128))
+    cache.quantize_append(T.to_dev_bf16(k), T.to_dev_bf16(k))
+    assert cache.last_launch_count() == 1
+    q = _rand_bits(rng, (1, 8, 128))
+    cache.decode_attention(T.to_dev_bf16(q))
+    assert cache.last_launch_count() == 2
+    m = cache.h2o_select_evict(1, budget=40, recent=8)
+    assert cache.last_launch_count() == 1
+    cache.compact_blocks(m, 1)
+    assert cache.last_launch_count() == 1
