@@ -19,6 +19,7 @@ KVC_ERR_STATE = 6
 KVC_ATTN_ACCUM_H2O = 0x1
 KVC_EVICT_H2O = 0
 KVC_EVICT_STREAMING = 1
+KVC_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 BUF = dict(K_CODES=0, V_CODES=1, K_SCALE=2, V_SCALE=3, SLOT_POS=4, SCORE=5, SINK_K=6, SINK_V=7,
            SINK_SCORE=8, BLOCK_TABLE=9, SEQ_SLOTS=10, SEQ_POS=11, FREE_STACK=12, COUNTERS=13, PLAN=14)
@@ -63,6 +64,7 @@ _SIGS = {
     "kvc_decode_attention": (_I, [_P, _I, _I, _P, _P, ctypes.c_float, _I, _P, _SZ, _P]),
     "kvc_h2o_select_evict": (_I, [_P, _I, _I, ctypes.POINTER(KvcEvictParams), _P, _P, _SZ, _P]),
     "kvc_compact_blocks": (_I, [_P, _I, _I, _P, _P, _SZ, _P]),
+    "kvc_decode_attention_noalloc": (_I, [_P, _I, _I, _P, _P, ctypes.c_float, _I, _P]),
     "kvc_read_status": (_I, [_P, ctypes.POINTER(_I), _P]),
     "kvc_set_trace_events": (_I, [_P, _P, _P]),
     "kvc_last_launch_count": (_I, [_P]),

@@ -215,6 +215,30 @@ kvc_status kvc_compact_blocks(kvc_cache* cache, int32_t seq_begin, int32_t batch
                               const uint8_t* d_keep_mask, void* d_workspace,
                               size_t workspace_bytes, void* stream);
 
+/* Decode attention without a caller-supplied workspace.  The pages have no
+ * counterpart to this call: it exists for callers that cannot allocate device
+ * memory when they run a step (a fixed memory budget set at start-up, a
+ * runtime that forbids allocation after initialisation, a host that owns
+ * every allocation and passes plug-ins only their inputs and outputs).
+ * Same arguments and results as kvc_decode_attention, which it calls; the
+ * workspace is a fixed array of KVC_NOALLOC_SCRATCH_BYTES bytes inside the
+ * library's device image, reserved on every GPU that loads the library and
+ * held until the process exits.  It allocates nothing and calls no
+ * allocating routine.
+ *   - Returns KVC_ERR_CAPACITY, before anything is enqueued, when the slice
+ *     needs more workspace than that (kvc_workspace_bytes(cache, batch) >
+ *     KVC_NOALLOC_SCRATCH_BYTES); use kvc_decode_attention then.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture on the device.
+ *   - All calls share the one array and leave their contents in it; calls
+ *     that overlap on the GPU (other streams or host threads) race.  No part
+ *     of it needs to start at zero. */
+#define KVC_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+kvc_status kvc_decode_attention_noalloc(kvc_cache* cache, int32_t seq_begin, int32_t batch,
+                                        const void* d_q, void* d_out, float sm_scale, int32_t flags,
+                                        void* stream);
+
 /* ---------------------------------------------------------------- misc ---- */
 
 /* Synchronise `stream`, copy the device status word to *h_status and clear
