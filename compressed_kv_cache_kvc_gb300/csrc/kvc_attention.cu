@@ -10,8 +10,10 @@
 // (section 3.4).
 //
 // GB300 design
-//   * Grid (split, kv-head, sequence).  A split is a run of 16-token pages of
-//     one (sequence, KV head); its 4 warps take pages round-robin.
+//   * Stream-K grid: one wave of resident CTAs; the pages of all (sequence,
+//     KV head) pairs are laid end to end and every CTA takes an equal run
+//     (which may span a pair boundary: one partial per pair touched).  Inside
+//     a CTA the 4 warps take the run's pages round-robin.
 //   * Each warp streams its pages through a private ring of shared-memory
 //     stages with cp.async (16-byte, coalesced: a K or V page of one head is
 //     one contiguous 2 KB (INT8) / 1 KB (INT4) run of the pool).
@@ -52,7 +54,8 @@ struct Geom {
   static constexpr int kKBytes = BITS == 8 ? 2048 : 1024;
   static constexpr int kVBytes = BITS == 8 ? 2048 : 1024;
   static constexpr int kStage = kKBytes + kVBytes + 128;  // + 16 K scales + 16 V scales
-  static constexpr int kStages = BITS == 8 ? 4 : 6;
+  static constexpr int kKChunks = BITS == 8 ? 4 : 2;    // 16-byte K chunks per lane per page
+  static constexpr int kStages = BITS == 8 ? 3 : 4;
   static constexpr int kSmem = kWarps * kStages * kStage;
 };
 
@@ -134,349 +137,407 @@ __device__ __forceinline__ int exponent_of(float x) {
   return (int)((__float_as_uint(x) >> 23) & 0xFF) - 127;
 }
 
+// Pages per sequence of the slice, as an exclusive prefix in shared memory:
+// cum[i] = pages of local sequences 0..i-1 (each KV head of a sequence has the
+// same pages).  Warp 0 computes it; every thread returns after the barrier.
+__device__ __forceinline__ void pages_prefix(const DevState& s, int seq_begin, int batch, int* cum) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int carry = 0;
+    if (lane == 0) cum[0] = 0;
+    for (int base = 0; base < batch; base += 32) {
+      const int i = base + lane;
+      int v = i < batch ? (s.seq_slots[seq_begin + i] + kPage - 1) / kPage : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+      }
+      if (i < batch) cum[i + 1] = carry + v;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+  }
+  __syncthreads();
+}
+
+// CTA of the stream-K split that holds flattened page F (see AttnWork).
+__device__ __forceinline__ int cta_of_page(long long F, long long T, int N) {
+  return (int)(((F + 1) * (long long)N - 1) / T);
+}
+
 template <int BITS>
-__global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int seq_begin,
+__global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int seq_begin, int batch,
                                                                  const uint16_t* __restrict__ q,
                                                                  float qk_scale_log2, AttnWork w,
                                                                  int spill) {
   using Gm = Geom<BITS>;
   constexpr int STAGES = Gm::kStages;
-  const int split = blockIdx.x;
-  const int h = blockIdx.y;
-  const int bl = blockIdx.z;
-  const int b = seq_begin + bl;
-  const int S = s.seq_slots[b];
-  const int n_pages = (S + kPage - 1) / kPage;
-  const int pg_begin = split * w.pages_per_split;
-  if (pg_begin >= n_pages) return;
-  const int pg_end = min(n_pages, pg_begin + w.pages_per_split);
+  constexpr int RB = Gm::kRowBytes;
+  __shared__ int cum[kMaxCallBatch + 1];
+  pages_prefix(s, seq_begin, batch, cum);
+
   const int G = s.group;
   const int hkv = s.hkv;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int r = lane >> 2;
   const int c = lane & 3;
+  const long long T = (long long)hkv * cum[batch];
+  const int N = gridDim.x;
+  const int cta = blockIdx.x;
+  long long F = (long long)cta * T / N;
+  const long long F1 = (long long)(cta + 1) * T / N;
 
   extern __shared__ __align__(16) uint8_t smem[];
   uint8_t* ring = smem + warp * STAGES * Gm::kStage;
 
-  // ---- query fragments (B operand of QK^T), scaled by 2^e_g into fp16 range.
-  uint32_t bq[8][2];
-  float cq0, cq1;
-  {
-    float qv[32];
-    const int g = r;
-    if (g < G) {
-      const uint4* src = reinterpret_cast<const uint4*>(q + ((size_t)bl * s.hq + h * G + g) * kHeadDim + 32 * c);
+  // per-lane offsets, within a head-page, of the chunks this lane copies and reads
+  uint32_t k_src[Gm::kKChunks], v_src[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 u = src[i];
-        const uint32_t ws[4] = {u.x, u.y, u.z, u.w};
+  for (int j = 0; j < Gm::kKChunks; ++j)
+    k_src[j] = BITS == 8 ? (2 * r + (j >> 1)) * 128 + 32 * c + 16 * (j & 1) : (2 * r + j) * 64 + 16 * c;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          qv[8 * i + 2 * j] = bf16f(ws[j] & 0xFFFFu);
-          qv[8 * i + 2 * j + 1] = bf16f(ws[j] >> 16);
+  for (int j = 0; j < 4; ++j) v_src[j] = BITS == 8 ? (4 * c + j) * 128 + 16 * r : (4 * c + j) * 64 + 8 * r;
+  const float* sc_src_base = lane < 4 ? s.k_scale : s.v_scale;
+  const uint32_t sc_off = 4 * (lane & 3);
+
+  while (F < F1) {
+    // ---- the (sequence, KV head) pair of page F and this CTA's run of its pages
+    int lo = 0, hi = batch - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((long long)hkv * cum[mid] <= F) lo = mid; else hi = mid - 1;
+    }
+    const int bl = lo;
+    const int b = seq_begin + bl;
+    const int npg = cum[bl + 1] - cum[bl];
+    const long long pbase = (long long)hkv * cum[bl];
+    const int h = (int)((F - pbase) / npg);
+    const long long Pf = pbase + (long long)h * npg;
+    const int pg_a = (int)(F - Pf);
+    const int pg_e = (int)((F1 < Pf + npg ? F1 : Pf + npg) - Pf);
+    const int S = s.seq_slots[b];
+    const int pair = bl * hkv + h;
+
+    // ---- query fragments (B operand of QK^T), scaled by 2^e_g into fp16 range
+    uint32_t bq[8][2];
+    float cq0, cq1;
+    {
+      float qv[32];
+      const int g = r;
+      if (g < G) {
+        const uint4* src =
+            reinterpret_cast<const uint4*>(q + ((size_t)bl * s.hq + h * G + g) * kHeadDim + 32 * c);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 u = src[i];
+          const uint32_t ws[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            qv[8 * i + 2 * j] = bf16f(ws[j] & 0xFFFFu);
+            qv[8 * i + 2 * j + 1] = bf16f(ws[j] >> 16);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) qv[i] = 0.0f;
+      }
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(qv[i]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      int e = 0;
+      if (amax > 0.0f) e = min(max(14 - exponent_of(amax), -100), 100);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) qv[i] = ldexpf(qv[i], e);
+      if (BITS == 8) {
+#pragma unroll
+        for (int st = 0; st < 8; ++st) {
+          bq[st][0] = pack_half2(qv[4 * st + 0], qv[4 * st + 1]);
+          bq[st][1] = pack_half2(qv[4 * st + 2], qv[4 * st + 3]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          bq[2 * i][0] = pack_half2(qv[8 * i + 0], qv[8 * i + 4]);
+          bq[2 * i][1] = pack_half2(qv[8 * i + 1], qv[8 * i + 5]);
+          bq[2 * i + 1][0] = pack_half2(qv[8 * i + 2], qv[8 * i + 6]);
+          bq[2 * i + 1][1] = pack_half2(qv[8 * i + 3], qv[8 * i + 7]);
         }
       }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) qv[i] = 0.0f;
+      const int e0 = __shfl_sync(0xffffffffu, e, (2 * c) * 4);
+      const int e1 = __shfl_sync(0xffffffffu, e, (2 * c + 1) * 4);
+      cq0 = ldexpf(qk_scale_log2, -e0);
+      cq1 = ldexpf(qk_scale_log2, -e1);
     }
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(qv[i]));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    int e = 0;
-    if (amax > 0.0f) e = min(max(14 - exponent_of(amax), -100), 100);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) qv[i] = ldexpf(qv[i], e);
-    if (BITS == 8) {
-#pragma unroll
-      for (int st = 0; st < 8; ++st) {
-        bq[st][0] = pack_half2(qv[4 * st + 0], qv[4 * st + 1]);
-        bq[st][1] = pack_half2(qv[4 * st + 2], qv[4 * st + 3]);
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        bq[2 * i][0] = pack_half2(qv[8 * i + 0], qv[8 * i + 4]);
-        bq[2 * i][1] = pack_half2(qv[8 * i + 1], qv[8 * i + 5]);
-        bq[2 * i + 1][0] = pack_half2(qv[8 * i + 2], qv[8 * i + 6]);
-        bq[2 * i + 1][1] = pack_half2(qv[8 * i + 3], qv[8 * i + 7]);
-      }
-    }
-    const int e0 = __shfl_sync(0xffffffffu, e, (2 * c) * 4);
-    const int e1 = __shfl_sync(0xffffffffu, e, (2 * c + 1) * 4);
-    cq0 = ldexpf(qk_scale_log2, -e0);
-    cq1 = ldexpf(qk_scale_log2, -e1);
-  }
 
-  // ---- page pipeline
-  const int n_range = pg_end - pg_begin;
-  const int n_my = n_range > warp ? (n_range - warp + kWarps - 1) / kWarps : 0;
-  const int32_t* bt = s.block_table + (size_t)b * s.max_bps;
+    // ---- page pipeline: this warp takes pages pg_a + warp, + kWarps, ...
+    const int n_range = pg_e - pg_a;
+    const int n_my = n_range > warp ? (n_range - warp + kWarps - 1) / kWarps : 0;
+    const int32_t* bt = s.block_table + (size_t)b * s.max_bps;
+    uint32_t stage_ok = 0;  // bit k: the page in stage k has a valid block id
+    int st_issue = 0;
 
-  auto issue = [&](int k) {
-    if (k < n_my) {
-      const int page = pg_begin + warp + kWarps * k;
-      const int blk = bt[page];
-      if ((unsigned)blk < (unsigned)s.num_blocks) {
-        uint8_t* st = ring + (k % STAGES) * Gm::kStage;
-        const size_t hp = ((size_t)blk * hkv + h) * kPage;
-        const uint8_t* kb = s.k_codes + hp * Gm::kRowBytes;
-        const uint8_t* vb = s.v_codes + hp * Gm::kRowBytes;
-        if (BITS == 8) {
+    auto issue = [&](int k) {
+      if (k < n_my) {
+        const int page = pg_a + warp + kWarps * k;
+        const int blk = bt[page];
+        const bool ok = (unsigned)blk < (unsigned)s.num_blocks;
+        stage_ok = ok ? (stage_ok | (1u << st_issue)) : (stage_ok & ~(1u << st_issue));
+        if (ok) {
+          uint8_t* st = ring + st_issue * Gm::kStage;
+          const size_t hp = ((size_t)blk * hkv + h) * kPage;
+          const uint8_t* kb = s.k_codes + hp * RB;
+          const uint8_t* vb = s.v_codes + hp * RB;
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            cp_async16(st + j * 512 + lane * 16, kb + (2 * r + (j >> 1)) * 128 + 32 * c + 16 * (j & 1));
+          for (int j = 0; j < Gm::kKChunks; ++j) cp_async16(st + j * 512 + lane * 16, kb + k_src[j]);
+          if (BITS == 8) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            cp_async16(st + Gm::kKBytes + j * 512 + lane * 16, vb + (4 * c + j) * 128 + 16 * r);
-        } else {
+            for (int j = 0; j < 4; ++j) cp_async16(st + Gm::kKBytes + j * 512 + lane * 16, vb + v_src[j]);
+          } else {
 #pragma unroll
-          for (int j = 0; j < 2; ++j) cp_async16(st + j * 512 + lane * 16, kb + (2 * r + j) * 64 + 16 * c);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            cp_async8(st + Gm::kKBytes + j * 256 + lane * 8, vb + (4 * c + j) * 64 + 8 * r);
+            for (int j = 0; j < 4; ++j) cp_async8(st + Gm::kKBytes + j * 256 + lane * 8, vb + v_src[j]);
+          }
+          if (lane < 8) cp_async16(st + Gm::kKBytes + Gm::kVBytes + 16 * lane, sc_src_base + hp + sc_off);
         }
-        if (lane < 4)
-          cp_async16(st + Gm::kKBytes + Gm::kVBytes + 16 * lane, s.k_scale + hp + 4 * lane);
-        else if (lane < 8)
-          cp_async16(st + Gm::kKBytes + Gm::kVBytes + 64 + 16 * (lane - 4), s.v_scale + hp + 4 * (lane - 4));
       }
-    }
-    cp_async_commit();
-  };
+      cp_async_commit();
+      st_issue = st_issue + 1 == STAGES ? 0 : st_issue + 1;
+    };
 
-  float oacc[8][4];
+    float oacc[8][4];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.0f;
-  float m0 = kNegBig, m1 = kNegBig, l0 = 0.0f, l1 = 0.0f;
-  int E = 0;
-  bool e_set = false;
-  float sv_hi = 0.0f;
-  float inv2E = 1.0f;
-
-  float* lg_base = spill ? w.logits + ((size_t)bl * hkv + h) * w.s_cap * G : nullptr;
+    for (int j = 0; j < 8; ++j) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.0f;
+    float m0 = kNegBig, m1 = kNegBig, l0 = 0.0f, l1 = 0.0f;
+    int E = 0;
+    bool e_set = false;
+    float sv_hi = 0.0f;
+    float inv2E = 1.0f;
+    // logits of this pair, [g][slot]; the lane writes slots (2r, 2r+1) of heads 2c and 2c+1
+    float* lg0p = spill && 2 * c < G ? w.logits + ((size_t)pair * G + 2 * c) * w.s_cap + 2 * r : nullptr;
+    float* lg1p = spill && 2 * c + 1 < G ? w.logits + ((size_t)pair * G + 2 * c + 1) * w.s_cap + 2 * r : nullptr;
 
 #pragma unroll 1
-  for (int k = 0; k < STAGES - 1; ++k) issue(k);
+    for (int k = 0; k < STAGES - 1; ++k) issue(k);
 
+    int st_comp = 0;
 #pragma unroll 1
-  for (int k = 0; k < n_my; ++k) {
-    issue(k + STAGES - 1);
-    cp_async_wait<STAGES - 1>();
-    __syncwarp();
-    const uint8_t* st = ring + (k % STAGES) * Gm::kStage;
-    const int page = pg_begin + warp + kWarps * k;
-    const int blk = bt[page];
-    const bool blk_ok = (unsigned)blk < (unsigned)s.num_blocks;
-    if (!blk_ok && lane == 0) atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
-    const int slot0 = page * kPage;
-    const bool v0 = blk_ok && (slot0 + 2 * r < S);
-    const bool v1 = blk_ok && (slot0 + 2 * r + 1 < S);
-    const float2 skv = *reinterpret_cast<const float2*>(st + Gm::kKBytes + Gm::kVBytes + 8 * r);
-    const float2 svv = *reinterpret_cast<const float2*>(st + Gm::kKBytes + Gm::kVBytes + 64 + 8 * r);
+    for (int k = 0; k < n_my; ++k) {
+      issue(k + STAGES - 1);
+      cp_async_wait<STAGES - 1>();
+      __syncwarp();
+      const uint8_t* st = ring + st_comp * Gm::kStage;
+      const int page = pg_a + warp + kWarps * k;
+      const bool blk_ok = (stage_ok >> st_comp) & 1u;
+      if (!blk_ok && lane == 0) atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
+      const int slot0 = page * kPage;
+      const bool v0 = blk_ok && (slot0 + 2 * r < S);
+      const bool v1 = blk_ok && (slot0 + 2 * r + 1 < S);
+      const float2 skv = *reinterpret_cast<const float2*>(st + Gm::kKBytes + Gm::kVBytes + 8 * r);
+      const float2 svv = *reinterpret_cast<const float2*>(st + Gm::kKBytes + Gm::kVBytes + 64 + 8 * r);
 
-    // ---- S = K_codes . q'  (rows: slots 2r and 2r+1, cols: query heads 2c, 2c+1)
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    if (BITS == 8) {
-      const uint4 ka = *reinterpret_cast<const uint4*>(st + 0 * 512 + lane * 16);
-      const uint4 kb2 = *reinterpret_cast<const uint4*>(st + 1 * 512 + lane * 16);
-      const uint4 kc = *reinterpret_cast<const uint4*>(st + 2 * 512 + lane * 16);
-      const uint4 kd = *reinterpret_cast<const uint4*>(st + 3 * 512 + lane * 16);
-      const uint32_t w0[8] = {ka.x, ka.y, ka.z, ka.w, kb2.x, kb2.y, kb2.z, kb2.w};
-      const uint32_t w1[8] = {kc.x, kc.y, kc.z, kc.w, kd.x, kd.y, kd.z, kd.w};
+      // ---- S = K_codes . q'  (rows: slots 2r and 2r+1, cols: query heads 2c, 2c+1)
+      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      if (BITS == 8) {
+        const uint4 ka = *reinterpret_cast<const uint4*>(st + 0 * 512 + lane * 16);
+        const uint4 kb2 = *reinterpret_cast<const uint4*>(st + 1 * 512 + lane * 16);
+        const uint4 kc = *reinterpret_cast<const uint4*>(st + 2 * 512 + lane * 16);
+        const uint4 kd = *reinterpret_cast<const uint4*>(st + 3 * 512 + lane * 16);
+        const uint32_t w0[8] = {ka.x, ka.y, ka.z, ka.w, kb2.x, kb2.y, kb2.z, kb2.w};
+        const uint32_t w1[8] = {kc.x, kc.y, kc.z, kc.w, kd.x, kd.y, kd.z, kd.w};
 #pragma unroll
-      for (int stp = 0; stp < 8; ++stp) {
-        uint32_t a0, a1, a2, a3;
-        i8x4_to_h2(w0[stp] ^ 0x80808080u, a0, a2);
-        i8x4_to_h2(w1[stp] ^ 0x80808080u, a1, a3);
-        mma16816(acc, a0, a1, a2, a3, bq[stp][0], bq[stp][1]);
-      }
-    } else {
-      const uint4 ka = *reinterpret_cast<const uint4*>(st + 0 * 512 + lane * 16);
-      const uint4 kb2 = *reinterpret_cast<const uint4*>(st + 1 * 512 + lane * 16);
-      const uint32_t w0[4] = {ka.x, ka.y, ka.z, ka.w};
-      const uint32_t w1[4] = {kb2.x, kb2.y, kb2.z, kb2.w};
+        for (int stp = 0; stp < 8; ++stp) {
+          uint32_t a0, a1, a2, a3;
+          i8x4_to_h2(w0[stp] ^ 0x80808080u, a0, a2);
+          i8x4_to_h2(w1[stp] ^ 0x80808080u, a1, a3);
+          mma16816(acc, a0, a1, a2, a3, bq[stp][0], bq[stp][1]);
+        }
+      } else {
+        const uint4 ka = *reinterpret_cast<const uint4*>(st + 0 * 512 + lane * 16);
+        const uint4 kb2 = *reinterpret_cast<const uint4*>(st + 1 * 512 + lane * 16);
+        const uint32_t w0[4] = {ka.x, ka.y, ka.z, ka.w};
+        const uint32_t w1[4] = {kb2.x, kb2.y, kb2.z, kb2.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t x0 = w0[i], x1 = w1[i];
-        const uint32_t x0s = x0 >> 8, x1s = x1 >> 8;
-        mma16816(acc, i4_lo_to_h2(x0), i4_lo_to_h2(x1), i4_hi_to_h2(x0), i4_hi_to_h2(x1), bq[2 * i][0],
-                 bq[2 * i][1]);
-        mma16816(acc, i4_lo_to_h2(x0s), i4_lo_to_h2(x1s), i4_hi_to_h2(x0s), i4_hi_to_h2(x1s),
-                 bq[2 * i + 1][0], bq[2 * i + 1][1]);
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t x0 = w0[i], x1 = w1[i];
+          const uint32_t x0s = x0 >> 8, x1s = x1 >> 8;
+          mma16816(acc, i4_lo_to_h2(x0), i4_lo_to_h2(x1), i4_hi_to_h2(x0), i4_hi_to_h2(x1), bq[2 * i][0],
+                   bq[2 * i][1]);
+          mma16816(acc, i4_lo_to_h2(x0s), i4_lo_to_h2(x1s), i4_hi_to_h2(x0s), i4_hi_to_h2(x1s),
+                   bq[2 * i + 1][0], bq[2 * i + 1][1]);
+        }
       }
+      const float lg0 = v0 ? acc[0] * skv.x * cq0 : -INFINITY;  // slot 2r,   head 2c
+      const float lg1 = v0 ? acc[1] * skv.x * cq1 : -INFINITY;  // slot 2r,   head 2c+1
+      const float lg2 = v1 ? acc[2] * skv.y * cq0 : -INFINITY;  // slot 2r+1, head 2c
+      const float lg3 = v1 ? acc[3] * skv.y * cq1 : -INFINITY;  // slot 2r+1, head 2c+1
+      if (lg0p) *reinterpret_cast<float2*>(lg0p + slot0) = make_float2(lg0, lg2);
+      if (lg1p) *reinterpret_cast<float2*>(lg1p + slot0) = make_float2(lg1, lg3);
+
+      // ---- lazy online softmax: reduce and rescale only when some lane's
+      // logit exceeds the running max by kLazy, or a V scale outgrows 2^(E+4)
+      const float svl = fmaxf(v0 ? svv.x : 0.0f, v1 ? svv.y : 0.0f);
+      const bool need = fmaxf(lg0, lg2) > m0 + kLazy || fmaxf(lg1, lg3) > m1 + kLazy || svl > sv_hi ||
+                        (!e_set && svl > 0.0f);
+      if (__any_sync(0xffffffffu, need)) {
+        float tm0 = fmaxf(lg0, lg2), tm1 = fmaxf(lg1, lg3), svm = svl;
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+          tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, o));
+          tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, o));
+          svm = fmaxf(svm, __shfl_xor_sync(0xffffffffu, svm, o));
+        }
+        const float nm0 = fmaxf(m0, tm0), nm1 = fmaxf(m1, tm1);
+        const float al0 = fast_exp2(m0 - nm0), al1 = fast_exp2(m1 - nm1);
+        const bool rescale_e = svm > sv_hi || (!e_set && svm > 0.0f);
+        int nE = E;
+        if (rescale_e) nE = min(max(exponent_of(svm), -126), 126);
+        const float f = ldexpf(1.0f, E - nE);
+        const float f0 = al0 * f, f1 = al1 * f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          oacc[j][0] *= f0;
+          oacc[j][2] *= f0;
+          oacc[j][1] *= f1;
+          oacc[j][3] *= f1;
+        }
+        l0 *= al0;
+        l1 *= al1;
+        m0 = nm0;
+        m1 = nm1;
+        if (rescale_e) {
+          E = nE;
+          e_set = true;
+          sv_hi = ldexpf(1.0f, E + 4);
+          inv2E = ldexpf(1.0f, -E);
+        }
+      }
+      const float sn0 = v0 ? svv.x * inv2E : 0.0f;
+      const float sn1 = v1 ? svv.y * inv2E : 0.0f;
+      const float p0 = fast_exp2(lg0 - m0), p1 = fast_exp2(lg1 - m1);
+      const float p2 = fast_exp2(lg2 - m0), p3 = fast_exp2(lg3 - m1);
+      l0 += p0 + p2;
+      l1 += p1 + p3;
+      const uint32_t pb0 = movmatrix_t(pack_half2(p0 * sn0, p1 * sn0));
+      const uint32_t pb1 = movmatrix_t(pack_half2(p2 * sn1, p3 * sn1));
+
+      // ---- O^T += V_codes^T . P~^T   (rows: head-dim 16r + 2j (+1), cols: query heads)
+      if (BITS == 8) {
+        const uint4 r0 = *reinterpret_cast<const uint4*>(st + Gm::kKBytes + 0 * 512 + lane * 16);
+        const uint4 r1 = *reinterpret_cast<const uint4*>(st + Gm::kKBytes + 1 * 512 + lane * 16);
+        const uint4 r2 = *reinterpret_cast<const uint4*>(st + Gm::kKBytes + 2 * 512 + lane * 16);
+        const uint4 r3 = *reinterpret_cast<const uint4*>(st + Gm::kKBytes + 3 * 512 + lane * 16);
+        const uint32_t x0[4] = {r0.x, r0.y, r0.z, r0.w};  // slot 4c
+        const uint32_t x1[4] = {r1.x, r1.y, r1.z, r1.w};  // slot 4c+1
+        const uint32_t x2[4] = {r2.x, r2.y, r2.z, r2.w};  // slot 4c+2
+        const uint32_t x3[4] = {r3.x, r3.y, r3.z, r3.w};  // slot 4c+3
+#pragma unroll
+        for (int wd = 0; wd < 4; ++wd) {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const int j = 2 * wd + half;
+            const uint32_t sa = (2 * half) | ((2 * half) << 4) | ((4 + 2 * half) << 8) | ((4 + 2 * half) << 12);
+            const uint32_t sb =
+                (2 * half + 1) | ((2 * half + 1) << 4) | ((5 + 2 * half) << 8) | ((5 + 2 * half) << 12);
+            const uint32_t a0 = i8_pair_to_h2(x0[wd], x2[wd], sa);
+            const uint32_t a1 = i8_pair_to_h2(x0[wd], x2[wd], sb);
+            const uint32_t a2 = i8_pair_to_h2(x1[wd], x3[wd], sa);
+            const uint32_t a3 = i8_pair_to_h2(x1[wd], x3[wd], sb);
+            mma16816(oacc[j], a0, a1, a2, a3, pb0, pb1);
+          }
+        }
+      } else {
+        const uint2 r0 = *reinterpret_cast<const uint2*>(st + Gm::kKBytes + 0 * 256 + lane * 8);
+        const uint2 r1 = *reinterpret_cast<const uint2*>(st + Gm::kKBytes + 1 * 256 + lane * 8);
+        const uint2 r2 = *reinterpret_cast<const uint2*>(st + Gm::kKBytes + 2 * 256 + lane * 8);
+        const uint2 r3 = *reinterpret_cast<const uint2*>(st + Gm::kKBytes + 3 * 256 + lane * 8);
+        const uint32_t x0[2] = {r0.x, r0.y};
+        const uint32_t x1[2] = {r1.x, r1.y};
+        const uint32_t x2[2] = {r2.x, r2.y};
+        const uint32_t x3[2] = {r3.x, r3.y};
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const int j = 4 * u + kk;
+            const uint32_t sel = kk | (kk << 4) | ((4 + kk) << 8) | ((4 + kk) << 12);
+            const uint32_t v02 = prmt(x0[u], x2[u], sel);
+            const uint32_t v13 = prmt(x1[u], x3[u], sel);
+            mma16816(oacc[j], i4_lo_to_h2(v02), i4_hi_to_h2(v02), i4_lo_to_h2(v13), i4_hi_to_h2(v13), pb0,
+                     pb1);
+          }
+        }
+      }
+      st_comp = st_comp + 1 == STAGES ? 0 : st_comp + 1;
+      __syncwarp();
     }
-    float lg0 = v0 ? acc[0] * skv.x * cq0 : -INFINITY;  // slot 2r,   head 2c
-    float lg1 = v0 ? acc[1] * skv.x * cq1 : -INFINITY;  // slot 2r,   head 2c+1
-    float lg2 = v1 ? acc[2] * skv.y * cq0 : -INFINITY;  // slot 2r+1, head 2c
-    float lg3 = v1 ? acc[3] * skv.y * cq1 : -INFINITY;  // slot 2r+1, head 2c+1
-    if (spill) {
-      const int g0 = 2 * c, g1 = 2 * c + 1;
-      float* row0 = lg_base + (size_t)(slot0 + 2 * r) * G;
-      if (v0) {
-        if (g0 < G) row0[g0] = lg0;
-        if (g1 < G) row0[g1] = lg1;
-      }
-      if (v1) {
-        if (g0 < G) row0[G + g0] = lg2;
-        if (g1 < G) row0[G + g1] = lg3;
-      }
-    }
-    float tm0 = fmaxf(lg0, lg2), tm1 = fmaxf(lg1, lg3);
-    float svm = fmaxf(v0 ? svv.x : 0.0f, v1 ? svv.y : 0.0f);
+    cp_async_wait<0>();
+
+    // ---- per-warp totals, CTA merge of the 4 warps, partial to the workspace
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
-      tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, o));
-      tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, o));
-      svm = fmaxf(svm, __shfl_xor_sync(0xffffffffu, svm, o));
+      l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
     }
-    const bool rescale_e = (svm > sv_hi) || (!e_set && svm > 0.0f);
-    const bool need = (tm0 > m0 + kLazy) || (tm1 > m1 + kLazy) || rescale_e;
-    if (__any_sync(0xffffffffu, need)) {
-      const float nm0 = fmaxf(m0, tm0), nm1 = fmaxf(m1, tm1);
-      const float al0 = fast_exp2(m0 - nm0), al1 = fast_exp2(m1 - nm1);
-      int nE = E;
-      if (rescale_e && svm > 0.0f) nE = min(max(exponent_of(svm), -126), 126);
-      const float f = ldexpf(1.0f, E - nE);
-      const float f0 = al0 * f, f1 = al1 * f;
+    const float f2E = ldexpf(1.0f, E);
+    __syncthreads();  // every warp is done with its ring: reuse shared memory
+    float* sm_m = reinterpret_cast<float*>(smem);  // [kWarps][8]
+    float* sm_l = sm_m + kWarps * kMaxGroup;       // [kWarps][8]
+    float* sm_o = sm_l + kWarps * kMaxGroup;       // [kWarps][8][128]
+    if (r == 0) {
+      sm_m[warp * kMaxGroup + 2 * c] = m0;
+      sm_m[warp * kMaxGroup + 2 * c + 1] = m1;
+      sm_l[warp * kMaxGroup + 2 * c] = l0;
+      sm_l[warp * kMaxGroup + 2 * c + 1] = l1;
+    }
+    {
+      float* o0 = sm_o + ((size_t)warp * kMaxGroup + 2 * c) * kHeadDim + 16 * r;
+      float* o1 = o0 + kHeadDim;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        oacc[j][0] *= f0;
-        oacc[j][2] *= f0;
-        oacc[j][1] *= f1;
-        oacc[j][3] *= f1;
-      }
-      l0 *= al0;
-      l1 *= al1;
-      m0 = nm0;
-      m1 = nm1;
-      if (rescale_e && svm > 0.0f) {
-        E = nE;
-        e_set = true;
-        sv_hi = ldexpf(1.0f, E + 4);
-        inv2E = ldexpf(1.0f, -E);
+        o0[2 * j] = oacc[j][0] * f2E;
+        o0[2 * j + 1] = oacc[j][2] * f2E;
+        o1[2 * j] = oacc[j][1] * f2E;
+        o1[2 * j + 1] = oacc[j][3] * f2E;
       }
     }
-    const float sn0 = v0 ? svv.x * inv2E : 0.0f;
-    const float sn1 = v1 ? svv.y * inv2E : 0.0f;
-    const float p0 = fast_exp2(lg0 - m0), p1 = fast_exp2(lg1 - m1);
-    const float p2 = fast_exp2(lg2 - m0), p3 = fast_exp2(lg3 - m1);
-    l0 += p0 + p2;
-    l1 += p1 + p3;
-    const uint32_t pb0 = movmatrix_t(pack_half2(p0 * sn0, p1 * sn0));
-    const uint32_t pb1 = movmatrix_t(pack_half2(p2 * sn1, p3 * sn1));
-
-    // ---- O^T += V_codes^T . P~^T   (rows: head-dim 16r + 2j (+1), cols: query heads)
-    if (BITS == 8) {
-      const uint4 r0 = *reinterpret_cast<const uint4*>(st + Gm::kKBytes + 0 * 512 + lane * 16);
-      const uint4 r1 = *reinterpret_cast<const uint4*>(st + Gm::kKBytes + 1 * 512 + lane * 16);
-      const uint4 r2 = *reinterpret_cast<const uint4*>(st + Gm::kKBytes + 2 * 512 + lane * 16);
-      const uint4 r3 = *reinterpret_cast<const uint4*>(st + Gm::kKBytes + 3 * 512 + lane * 16);
-      const uint32_t x0[4] = {r0.x, r0.y, r0.z, r0.w};  // slot 4c
-      const uint32_t x1[4] = {r1.x, r1.y, r1.z, r1.w};  // slot 4c+1
-      const uint32_t x2[4] = {r2.x, r2.y, r2.z, r2.w};  // slot 4c+2
-      const uint32_t x3[4] = {r3.x, r3.y, r3.z, r3.w};  // slot 4c+3
+    __syncthreads();
+    const int d = threadIdx.x;  // 128 threads = head_dim
+    const size_t pslot = (size_t)pair + cta;
+    for (int g = 0; g < G; ++g) {
+      float M = kNegBig;
 #pragma unroll
-      for (int wd = 0; wd < 4; ++wd) {
+      for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, sm_m[ww * kMaxGroup + g]);
+      float o = 0.0f, l = 0.0f;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int j = 2 * wd + half;
-          const uint32_t sa = (2 * half) | ((2 * half) << 4) | ((4 + 2 * half) << 8) | ((4 + 2 * half) << 12);
-          const uint32_t sb = (2 * half + 1) | ((2 * half + 1) << 4) | ((5 + 2 * half) << 8) | ((5 + 2 * half) << 12);
-          const uint32_t a0 = i8_pair_to_h2(x0[wd], x2[wd], sa);
-          const uint32_t a1 = i8_pair_to_h2(x0[wd], x2[wd], sb);
-          const uint32_t a2 = i8_pair_to_h2(x1[wd], x3[wd], sa);
-          const uint32_t a3 = i8_pair_to_h2(x1[wd], x3[wd], sb);
-          mma16816(oacc[j], a0, a1, a2, a3, pb0, pb1);
-        }
+      for (int ww = 0; ww < kWarps; ++ww) {
+        const float wt = fast_exp2(sm_m[ww * kMaxGroup + g] - M);
+        o += wt * sm_o[((size_t)ww * kMaxGroup + g) * kHeadDim + d];
+        l += wt * sm_l[ww * kMaxGroup + g];
       }
-    } else {
-      const uint2 r0 = *reinterpret_cast<const uint2*>(st + Gm::kKBytes + 0 * 256 + lane * 8);
-      const uint2 r1 = *reinterpret_cast<const uint2*>(st + Gm::kKBytes + 1 * 256 + lane * 8);
-      const uint2 r2 = *reinterpret_cast<const uint2*>(st + Gm::kKBytes + 2 * 256 + lane * 8);
-      const uint2 r3 = *reinterpret_cast<const uint2*>(st + Gm::kKBytes + 3 * 256 + lane * 8);
-      const uint32_t x0[2] = {r0.x, r0.y};
-      const uint32_t x1[2] = {r1.x, r1.y};
-      const uint32_t x2[2] = {r2.x, r2.y};
-      const uint32_t x3[2] = {r3.x, r3.y};
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const int j = 4 * u + kk;
-          const uint32_t sel = kk | (kk << 4) | ((4 + kk) << 8) | ((4 + kk) << 12);
-          const uint32_t v02 = prmt(x0[u], x2[u], sel);
-          const uint32_t v13 = prmt(x1[u], x3[u], sel);
-          mma16816(oacc[j], i4_lo_to_h2(v02), i4_hi_to_h2(v02), i4_lo_to_h2(v13), i4_hi_to_h2(v13), pb0,
-                   pb1);
-        }
+      w.part_o[(pslot * G + g) * kHeadDim + d] = o;
+      if (d == 0) {
+        w.part_ml[(pslot * G + g) * 2 + 0] = M;
+        w.part_ml[(pslot * G + g) * 2 + 1] = l;
       }
     }
-    __syncwarp();
-  }
-  cp_async_wait<0>();
-
-  // ---- per-warp totals
-#pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, o);
-  }
-  const float f2E = ldexpf(1.0f, E);
-  __syncthreads();  // every warp is done with its ring: reuse shared memory
-  float* sm_m = reinterpret_cast<float*>(smem);          // [kWarps][8]
-  float* sm_l = sm_m + kWarps * kMaxGroup;               // [kWarps][8]
-  float* sm_o = sm_l + kWarps * kMaxGroup;               // [kWarps][8][128]
-  if (r == 0) {
-    sm_m[warp * kMaxGroup + 2 * c] = m0;
-    sm_m[warp * kMaxGroup + 2 * c + 1] = m1;
-    sm_l[warp * kMaxGroup + 2 * c] = l0;
-    sm_l[warp * kMaxGroup + 2 * c + 1] = l1;
-  }
-  {
-    float* o0 = sm_o + ((size_t)warp * kMaxGroup + 2 * c) * kHeadDim + 16 * r;
-    float* o1 = o0 + kHeadDim;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      o0[2 * j] = oacc[j][0] * f2E;
-      o0[2 * j + 1] = oacc[j][2] * f2E;
-      o1[2 * j] = oacc[j][1] * f2E;
-      o1[2 * j + 1] = oacc[j][3] * f2E;
-    }
-  }
-  __syncthreads();
-  const int d = threadIdx.x;  // 128 threads = head_dim
-  const size_t pbase = (((size_t)bl * hkv + h) * w.nsplit + split) * G;
-  for (int g = 0; g < G; ++g) {
-    float M = kNegBig;
-#pragma unroll
-    for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, sm_m[ww * kMaxGroup + g]);
-    float o = 0.0f, l = 0.0f;
-#pragma unroll
-    for (int ww = 0; ww < kWarps; ++ww) {
-      const float wt = fast_exp2(sm_m[ww * kMaxGroup + g] - M);
-      o += wt * sm_o[((size_t)ww * kMaxGroup + g) * kHeadDim + d];
-      l += wt * sm_l[ww * kMaxGroup + g];
-    }
-    w.part_o[(pbase + g) * kHeadDim + d] = o;
-    if (d == 0) {
-      w.part_ml[(pbase + g) * 2 + 0] = M;
-      w.part_ml[(pbase + g) * 2 + 1] = l;
-    }
+    __syncthreads();  // shared memory is reused by the next pair
+    F = Pf + pg_e;
   }
 }
 
-// Merge the splits and the bf16 sinks of one (sequence, KV head); write the
-// bf16 outputs of its G query heads; with H2O on, add this step's
+// Merge the stream-K partials and the bf16 sinks of one (sequence, KV head);
+// write the bf16 outputs of its G query heads; with H2O on, add this step's
 // probabilities to the sink scores and to every pool slot's score.
-__global__ void __launch_bounds__(128) attn_merge_kernel(DevState s, int seq_begin,
-                                                         const uint16_t* __restrict__ q,
-                                                         uint16_t* __restrict__ out, float qk_scale_log2,
-                                                         AttnWork w, int accumulate) {
+__global__ void __launch_bounds__(1024, 2) attn_merge_kernel(DevState s, int seq_begin, int batch,
+                                                             const uint16_t* __restrict__ q,
+                                                             uint16_t* __restrict__ out, float qk_scale_log2,
+                                                             AttnWork w, int accumulate) {
+  __shared__ int cum[kMaxCallBatch + 1];
+  __shared__ float sh_sl[kMaxGroup][kSinks];
+  __shared__ float sh_M[kMaxGroup], sh_invL[kMaxGroup];
+  pages_prefix(s, seq_begin, batch, cum);
   const int h = blockIdx.x;
   const int bl = blockIdx.y;
   const int b = seq_begin + bl;
@@ -485,80 +546,89 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(DevState s, int seq_beg
   const int S = s.seq_slots[b];
   const int P = s.seq_pos[b];
   const int ns = min(P, kSinks);
-  const int n_pages = (S + kPage - 1) / kPage;
-  const int nsp = (n_pages + w.pages_per_split - 1) / w.pages_per_split;
-  const int d = threadIdx.x;
-  const int lane = d & 31, warp = d >> 5;
-
-  __shared__ float sh_red[4][kSinks];
-  __shared__ float sh_sl[kMaxGroup][kSinks];
-  __shared__ float sh_M[kMaxGroup], sh_invL[kMaxGroup];
-
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int pair = bl * hkv + h;
+  const int npg = cum[bl + 1] - cum[bl];
+  int i_first = 0, i_last = -1;
+  if (npg > 0) {
+    const long long T = (long long)hkv * cum[batch];
+    const long long Pf = (long long)hkv * cum[bl] + (long long)h * npg;
+    i_first = cta_of_page(Pf, T, w.ncta);
+    i_last = cta_of_page(Pf + npg - 1, T, w.ncta);
+  }
   const uint16_t* sk = s.sink_k + ((size_t)b * hkv + h) * kSinks * kHeadDim;
   const uint16_t* sv = s.sink_v + ((size_t)b * hkv + h) * kSinks * kHeadDim;
-  for (int g = 0; g < G; ++g) {
-    const int hq = h * G + g;
-    const float qd = bf16f(q[((size_t)bl * s.hq + hq) * kHeadDim + d]);
-    float part[kSinks];
-#pragma unroll
-    for (int j = 0; j < kSinks; ++j) part[j] = j < ns ? qd * bf16f(sk[j * kHeadDim + d]) : 0.0f;
-#pragma unroll
-    for (int j = 0; j < kSinks; ++j)
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) part[j] += __shfl_xor_sync(0xffffffffu, part[j], o);
-    if (lane == 0)
-#pragma unroll
-      for (int j = 0; j < kSinks; ++j) sh_red[warp][j] = part[j];
-    __syncthreads();
-    float sl[kSinks];
-#pragma unroll
-    for (int j = 0; j < kSinks; ++j)
-      sl[j] = j < ns ? (sh_red[0][j] + sh_red[1][j] + sh_red[2][j] + sh_red[3][j]) * qk_scale_log2 : -INFINITY;
-    float M = kNegBig;
-#pragma unroll
-    for (int j = 0; j < kSinks; ++j) M = fmaxf(M, sl[j]);
-    const size_t pbase = ((size_t)bl * hkv + h) * w.nsplit * G;
-    for (int sp = 0; sp < nsp; ++sp) M = fmaxf(M, w.part_ml[(pbase + (size_t)sp * G + g) * 2]);
-    float L = 0.0f, o = 0.0f;
-#pragma unroll
-    for (int j = 0; j < kSinks; ++j) {
+
+  // sink logits: warp (g, j) = (warp / 4, warp % 4)
+  {
+    const int g = warp >> 2, j = warp & 3;
+    if (g < G) {
+      float part = 0.0f;
       if (j < ns) {
-        const float e = fast_exp2(sl[j] - M);
-        L += e;
-        o += e * bf16f(sv[j * kHeadDim + d]);
+        const uint16_t* qr = q + ((size_t)bl * s.hq + h * G + g) * kHeadDim;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) part += bf16f(qr[lane * 4 + e]) * bf16f(sk[j * kHeadDim + lane * 4 + e]);
       }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+      if (lane == 0) sh_sl[g][j] = j < ns ? part * qk_scale_log2 : -INFINITY;
     }
-    for (int sp = 0; sp < nsp; ++sp) {
-      const size_t pi = pbase + (size_t)sp * G + g;
-      const float e = fast_exp2(w.part_ml[pi * 2] - M);
-      L += e * w.part_ml[pi * 2 + 1];
-      o += e * w.part_o[pi * kHeadDim + d];
+  }
+  __syncthreads();
+  // global max and sum per query head: warp g
+  if (warp < G) {
+    const int g = warp;
+    float M = kNegBig;
+    for (int i = i_first + lane; i <= i_last; i += 32) M = fmaxf(M, w.part_ml[(((size_t)pair + i) * G + g) * 2]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+#pragma unroll
+    for (int j = 0; j < kSinks; ++j) M = fmaxf(M, sh_sl[g][j]);
+    float L = 0.0f;
+    for (int i = i_first + lane; i <= i_last; i += 32) {
+      const size_t pi = ((size_t)pair + i) * G + g;
+      L += fast_exp2(w.part_ml[pi * 2] - M) * w.part_ml[pi * 2 + 1];
     }
-    const float res = L > 0.0f ? o / L : 0.0f;
-    out[((size_t)bl * s.hq + hq) * kHeadDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(res));
-    if (d == 0) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    if (lane == 0) {
+#pragma unroll
+      for (int j = 0; j < kSinks; ++j)
+        if (j < ns) L += fast_exp2(sh_sl[g][j] - M);
       sh_M[g] = M;
       sh_invL[g] = L > 0.0f ? 1.0f / L : 0.0f;
-      w.stats[((size_t)bl * s.hq + hq) * 2 + 0] = M;
-      w.stats[((size_t)bl * s.hq + hq) * 2 + 1] = L;
-#pragma unroll
-      for (int j = 0; j < kSinks; ++j) sh_sl[g][j] = sl[j];
+      w.stats[((size_t)bl * s.hq + h * G + g) * 2 + 0] = M;
+      w.stats[((size_t)bl * s.hq + h * G + g) * 2 + 1] = L;
     }
-    __syncthreads();
+  }
+  __syncthreads();
+  // outputs: thread (g, d)
+  if ((int)threadIdx.x < G * kHeadDim) {
+    const int g = threadIdx.x >> 7, d = threadIdx.x & (kHeadDim - 1);
+    const float M = sh_M[g];
+    float o = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kSinks; ++j)
+      if (j < ns) o += fast_exp2(sh_sl[g][j] - M) * bf16f(sv[j * kHeadDim + d]);
+    for (int i = i_first; i <= i_last; ++i) {
+      const size_t pi = ((size_t)pair + i) * G + g;
+      o += fast_exp2(w.part_ml[pi * 2] - M) * w.part_o[pi * kHeadDim + d];
+    }
+    out[((size_t)bl * s.hq + h * G + g) * kHeadDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(o * sh_invL[g]));
   }
   if (!accumulate) return;
-  if (d < ns) {
+  if ((int)threadIdx.x < ns) {
     float inc = 0.0f;
-    for (int g = 0; g < G; ++g) inc += fast_exp2(sh_sl[g][d] - sh_M[g]) * sh_invL[g];
-    s.sink_score[((size_t)b * hkv + h) * kSinks + d] += inc;
+    for (int g = 0; g < G; ++g) inc += fast_exp2(sh_sl[g][threadIdx.x] - sh_M[g]) * sh_invL[g];
+    s.sink_score[((size_t)b * hkv + h) * kSinks + threadIdx.x] += inc;
   }
   const int32_t* bt = s.block_table + (size_t)b * s.max_bps;
-  const float* lgr = w.logits + ((size_t)bl * hkv + h) * w.s_cap * G;
-  for (int t = d; t < S; t += blockDim.x) {
+  const float* lgr = w.logits + (size_t)pair * G * w.s_cap;
+  for (int t = threadIdx.x; t < S; t += blockDim.x) {
     const int blk = bt[t / kPage];
     if ((unsigned)blk >= (unsigned)s.num_blocks) continue;
     float inc = 0.0f;
-    for (int g = 0; g < G; ++g) inc += fast_exp2(lgr[(size_t)t * G + g] - sh_M[g]) * sh_invL[g];
+    for (int g = 0; g < G; ++g) inc += fast_exp2(lgr[(size_t)g * w.s_cap + t] - sh_M[g]) * sh_invL[g];
     s.score[((size_t)blk * hkv + h) * kPage + (t % kPage)] += inc;
   }
 }
@@ -577,22 +647,41 @@ cudaError_t ensure_split_smem() {
   return e;
 }
 
+template <int BITS>
+int split_ctas_per_sm() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev < 64 && cached[dev] > 0) return cached[dev];
+  if (ensure_split_smem<BITS>() != cudaSuccess) return 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_split_kernel<BITS>, kWarps * 32, Geom<BITS>::kSmem) !=
+          cudaSuccess ||
+      n < 1)
+    n = 1;
+  if (dev < 64) cached[dev] = n;
+  return n;
+}
+
 }  // namespace
 
 int attention_smem_bytes(int bits) { return bits == 8 ? Geom<8>::kSmem : Geom<4>::kSmem; }
 
+int attention_ctas_per_sm(int bits) { return bits == 8 ? split_ctas_per_sm<8>() : split_ctas_per_sm<4>(); }
+
 cudaError_t launch_attention_split(const DevState& s, int seq_begin, int batch, const uint16_t* q,
                                    float qk_scale_log2, const AttnWork& w, bool spill, cudaStream_t st) {
-  dim3 grid(w.nsplit, s.hkv, batch);
   cudaError_t e;
   if (s.bits == 8) {
     e = ensure_split_smem<8>();
     if (e != cudaSuccess) return e;
-    attn_split_kernel<8><<<grid, kWarps * 32, Geom<8>::kSmem, st>>>(s, seq_begin, q, qk_scale_log2, w, spill);
+    attn_split_kernel<8><<<w.ncta, kWarps * 32, Geom<8>::kSmem, st>>>(s, seq_begin, batch, q, qk_scale_log2, w,
+                                                                      spill);
   } else {
     e = ensure_split_smem<4>();
     if (e != cudaSuccess) return e;
-    attn_split_kernel<4><<<grid, kWarps * 32, Geom<4>::kSmem, st>>>(s, seq_begin, q, qk_scale_log2, w, spill);
+    attn_split_kernel<4><<<w.ncta, kWarps * 32, Geom<4>::kSmem, st>>>(s, seq_begin, batch, q, qk_scale_log2, w,
+                                                                      spill);
   }
   return cudaGetLastError();
 }
@@ -600,7 +689,7 @@ cudaError_t launch_attention_split(const DevState& s, int seq_begin, int batch, 
 cudaError_t launch_attention_merge(const DevState& s, int seq_begin, int batch, const uint16_t* q, uint16_t* out,
                                    float qk_scale_log2, const AttnWork& w, bool accumulate, cudaStream_t st) {
   dim3 grid(s.hkv, batch);
-  attn_merge_kernel<<<grid, 128, 0, st>>>(s, seq_begin, q, out, qk_scale_log2, w, accumulate ? 1 : 0);
+  attn_merge_kernel<<<grid, 1024, 0, st>>>(s, seq_begin, batch, q, out, qk_scale_log2, w, accumulate ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -19,7 +19,7 @@ using kvc::DevState;
 namespace {
 
 constexpr size_t kAlign = 256;
-constexpr int kMinPagesPerSplit = 4;
+constexpr int kMinPagesPerCta = 4;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -110,10 +110,6 @@ bool range_ok(const kvc_cache* c, int32_t seq_begin, int32_t batch) {
 
 int s_cap(const kvc_cache* c) { return c->cfg.max_blocks_per_seq * kvc::kPage; }
 
-int max_split_count(const kvc_cache* c) {
-  return (c->cfg.max_blocks_per_seq + kMinPagesPerSplit - 1) / kMinPagesPerSplit;
-}
-
 // Workspace carving (all regions 256-byte aligned).
 struct WsLayout {
   size_t part_o, part_ml, logits, stats, keys, pos, total;
@@ -122,14 +118,14 @@ struct WsLayout {
 WsLayout ws_layout(const kvc_cache* c, int batch) {
   const size_t G = c->cfg.num_q_heads / c->cfg.num_kv_heads;
   const size_t pairs = (size_t)batch * c->cfg.num_kv_heads;
-  const size_t ns = max_split_count(c);
+  const size_t nslots = pairs + kvc::kMaxSplitCtas;  // stream-K partial slots
   const size_t cap = s_cap(c);
   WsLayout w{};
   size_t o = 0;
   w.part_o = o;
-  o = align_up(o + pairs * ns * G * kvc::kHeadDim * 4);
+  o = align_up(o + nslots * G * kvc::kHeadDim * 4);
   w.part_ml = o;
-  o = align_up(o + pairs * ns * G * 2 * 4);
+  o = align_up(o + nslots * G * 2 * 4);
   w.logits = o;
   o = align_up(o + pairs * cap * G * 4);
   w.stats = o;
@@ -333,25 +329,21 @@ kvc_status kvc_decode_attention(kvc_cache* c, int32_t seq_begin, int32_t batch, 
   if (!(sm_scale > 0.0f) || !std::isfinite(sm_scale) || (flags & ~KVC_ATTN_ACCUM_H2O)) return KVC_ERR_INVALID_ARG;
   const WsLayout wl = ws_layout(c, batch);
   if (!d_workspace || !aligned(d_workspace, kAlign) || workspace_bytes < wl.total) return KVC_ERR_INVALID_ARG;
-  int max_pages = 0;
+  if (batch > kvc::kMaxCallBatch) return KVC_ERR_UNSUPPORTED;
+  long long total_pages = 0;
   for (int i = 0; i < batch; ++i) {
     const int b = seq_begin + i;
     if (c->pos[b] <= 0) return KVC_ERR_INVALID_ARG;  // nothing to attend to
-    max_pages = std::max(max_pages, pages_of(c->slots[b]));
+    total_pages += (long long)pages_of(c->slots[b]) * c->cfg.num_kv_heads;
   }
-  // split-K policy: enough CTAs for several waves of resident blocks, at
-  // least kMinPagesPerSplit pages per split
-  const int pairs = batch * c->cfg.num_kv_heads;
-  const int resident = c->cfg.bits == 8 ? 3 : 4;
-  const int target = 2 * sm_count(c) * resident;
-  int nsplit = 1;
-  int pps = std::max(max_pages, 1);
-  if (max_pages > 0) {
-    nsplit = std::max(1, (target + pairs - 1) / pairs);
-    nsplit = std::min(nsplit, (max_pages + kMinPagesPerSplit - 1) / kMinPagesPerSplit);
-    nsplit = std::max(1, std::min(nsplit, max_split_count(c)));
-    pps = (max_pages + nsplit - 1) / nsplit;
-    nsplit = (max_pages + pps - 1) / pps;
+  // stream-K grid: one wave of resident CTAs, each with at least
+  // kMinPagesPerCta pages of the current lengths (any grid size is correct
+  // for any lengths, so a graph replayed at other lengths stays correct)
+  int ncta = 1;
+  if (total_pages > 0) {
+    ncta = sm_count(c) * kvc::attention_ctas_per_sm(c->cfg.bits);
+    ncta = (int)std::min<long long>(ncta, std::max<long long>(1, total_pages / kMinPagesPerCta));
+    ncta = std::max(1, std::min(ncta, kvc::kMaxSplitCtas));
   }
   uint8_t* ws = static_cast<uint8_t*>(d_workspace);
   kvc::AttnWork w{};
@@ -359,8 +351,7 @@ kvc_status kvc_decode_attention(kvc_cache* c, int32_t seq_begin, int32_t batch, 
   w.part_ml = reinterpret_cast<float*>(ws + wl.part_ml);
   w.logits = reinterpret_cast<float*>(ws + wl.logits);
   w.stats = reinterpret_cast<float*>(ws + wl.stats);
-  w.nsplit = nsplit;
-  w.pages_per_split = pps;
+  w.ncta = ncta;
   w.s_cap = s_cap(c);
   const float qk_scale_log2 = sm_scale * 1.4426950408889634f;
   const bool h2o = (flags & KVC_ATTN_ACCUM_H2O) != 0;
@@ -374,7 +365,7 @@ kvc_status kvc_decode_attention(kvc_cache* c, int32_t seq_begin, int32_t batch, 
     if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return KVC_ERR_CUDA;
     if (cs == cudaStreamCaptureStatusActive) rec_flags = cudaEventRecordExternal;
   }
-  if (max_pages > 0) {
+  if (total_pages > 0) {
     if (trace && cudaEventRecordWithFlags(static_cast<cudaEvent_t>(c->trace_start), st, rec_flags) != cudaSuccess)
       return KVC_ERR_CUDA;
     if (kvc::launch_attention_split(c->dev, seq_begin, batch, static_cast<const uint16_t*>(d_q), qk_scale_log2, w,

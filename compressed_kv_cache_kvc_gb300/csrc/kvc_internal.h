@@ -43,16 +43,25 @@ constexpr int kDevBadKeepMask = 0x4;
 constexpr int kDevTableOverflow = 0x8;
 constexpr int kDevStackOverflow = 0x10;
 
-// Scratch carved from the caller's workspace for one call.
+// Scratch carved from the caller's workspace for one attention call.
+//
+// Work split ("stream-K"): the pages of all (sequence, KV head) pairs of the
+// slice are laid end to end (pair p = local_seq * hkv + head, pages in order)
+// and CTA i of the N-CTA grid takes pages [floor(i*T/N), floor((i+1)*T/N)).
+// A CTA writes one partial (m, l, o) per pair it touches, into partial slot
+// p + i; the slots of different (pair, CTA) combinations never collide
+// because both orders run along the same page sequence.
 struct AttnWork {
-  float* part_o;    // [batch][hkv][nsplit][group][128]
-  float* part_ml;   // [batch][hkv][nsplit][group][2]
-  float* logits;    // [batch][hkv][s_cap][group]  (log2 domain)
+  float* part_o;    // [pairs + ncta][group][128]
+  float* part_ml;   // [pairs + ncta][group][2]
+  float* logits;    // [batch][hkv][group][s_cap]  (log2 domain)
   float* stats;     // [batch][hq][2]  global (M, L) per query head
-  int nsplit;
-  int pages_per_split;
+  int ncta;         // grid size of the split kernel
   int s_cap;
 };
+
+constexpr int kMaxCallBatch = 1024;  // sequences per attention call (prefix table in shared memory)
+constexpr int kMaxSplitCtas = 2048;
 
 // ---- launchers (return cudaGetLastError of the launch) -------------------
 cudaError_t launch_append(const DevState& s, int seq_begin, int batch, int n_new,
@@ -79,6 +88,7 @@ cudaError_t launch_compact(const DevState& s, int seq_begin, int batch, const ui
                            int s_cap, int32_t* g_scratch, cudaStream_t st);
 
 int attention_smem_bytes(int bits);
+int attention_ctas_per_sm(int bits);  // resident split CTAs per SM (occupancy API, cached)
 int select_max_smem_slots();
 
 }  // namespace kvc

@@ -218,57 +218,58 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(DevState s, in
   const uint8_t* mrow = mask + ((size_t)bl * s.hkv + h) * s_cap;
   int32_t* holes = scratch + ((size_t)bl * s.hkv + h) * s_cap;
   const int32_t* bt = s.block_table + (size_t)b * s.max_bps;
+  // each thread owns one run of consecutive slots
+  const int run = (S + kCompactThreads - 1) / kCompactThreads;
+  const int t0 = min(S, (int)threadIdx.x * run);
+  const int t1 = min(S, t0 + run);
 
-  // pass 1: holes (evicted slots below n'), in ascending order; count kept
-  int n_holes = 0, n_kept = 0;
-  for (int base = 0; base < S; base += kCompactThreads) {
-    const int t = base + threadIdx.x;
-    const bool kept = t < S && mrow[t] != 0;
-    const bool hole = t < np && !kept;
-    int tot_h, tot_k;
-    const int rank = block_scan<kCompactThreads>(hole ? 1 : 0, sh_warp, &tot_h) - 1;
-    block_scan<kCompactThreads>(kept ? 1 : 0, sh_warp, &tot_k);
-    if (hole) holes[n_holes + rank] = t;
-    n_holes += tot_h;
-    n_kept += tot_k;
+  // pass 1: holes (evicted slots below n') in ascending order; count kept
+  int my_holes = 0, my_kept = 0;
+  for (int t = t0; t < t1; ++t) {
+    const bool kept = mrow[t] != 0;
+    my_kept += kept;
+    my_holes += (t < np && !kept);
   }
-  if (n_kept != np) {
+  int tot_h, tot_k;
+  int pos_h = block_scan<kCompactThreads>(my_holes, sh_warp, &tot_h) - my_holes;
+  block_scan<kCompactThreads>(my_kept, sh_warp, &tot_k);
+  if (tot_k != np) {
     if (threadIdx.x == 0) atomicOr(&s.counters[kCtrStatus], kDevBadKeepMask);
     return;
   }
+  for (int t = t0; t < min(t1, np); ++t)
+    if (mrow[t] == 0) holes[pos_h++] = t;
   __syncthreads();
 
   // pass 2: kept slots at or above n', in ascending order, fill the holes
+  const int a0 = max(t0, np);
+  int my_src = 0;
+  for (int t = a0; t < t1; ++t) my_src += mrow[t] != 0;
+  int tot_s;
+  int rank = block_scan<kCompactThreads>(my_src, sh_warp, &tot_s) - my_src;
   const int rb = s.row_bytes;
-  int done = 0;
-  for (int base = np; base < S; base += kCompactThreads) {
-    const int t = base + threadIdx.x;
-    const bool src = t < S && mrow[t] != 0;
-    int tot;
-    const int rank = block_scan<kCompactThreads>(src ? 1 : 0, sh_warp, &tot) - 1;
-    if (src) {
-      const int dst = holes[done + rank];
-      bool ok1, ok2;
-      const size_t si = slot_index(s, bt, h, t, ok1);
-      const size_t di = slot_index(s, bt, h, dst, ok2);
-      if (ok1 && ok2) {
-        const uint4* ks = reinterpret_cast<const uint4*>(s.k_codes + si * rb);
-        const uint4* vs = reinterpret_cast<const uint4*>(s.v_codes + si * rb);
-        uint4* kd = reinterpret_cast<uint4*>(s.k_codes + di * rb);
-        uint4* vd = reinterpret_cast<uint4*>(s.v_codes + di * rb);
-        for (int i = 0; i < rb / 16; ++i) {
-          kd[i] = ks[i];
-          vd[i] = vs[i];
-        }
-        s.k_scale[di] = s.k_scale[si];
-        s.v_scale[di] = s.v_scale[si];
-        s.slot_pos[di] = s.slot_pos[si];
-        s.score[di] = s.score[si];
-      } else {
-        atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
-      }
+  for (int t = a0; t < t1; ++t) {
+    if (mrow[t] == 0) continue;
+    const int dst = holes[rank++];
+    bool ok1, ok2;
+    const size_t si = slot_index(s, bt, h, t, ok1);
+    const size_t di = slot_index(s, bt, h, dst, ok2);
+    if (!(ok1 && ok2)) {
+      atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
+      continue;
     }
-    done += tot;
+    const uint4* ks = reinterpret_cast<const uint4*>(s.k_codes + si * rb);
+    const uint4* vs = reinterpret_cast<const uint4*>(s.v_codes + si * rb);
+    uint4* kd = reinterpret_cast<uint4*>(s.k_codes + di * rb);
+    uint4* vd = reinterpret_cast<uint4*>(s.v_codes + di * rb);
+    for (int i = 0; i < rb / 16; ++i) {
+      kd[i] = ks[i];
+      vd[i] = vs[i];
+    }
+    s.k_scale[di] = s.k_scale[si];
+    s.v_scale[di] = s.v_scale[si];
+    s.slot_pos[di] = s.slot_pos[si];
+    s.score[di] = s.score[si];
   }
 
   // release the emptied pages (all KV heads share the page structure)
