@@ -47,6 +47,8 @@ namespace {
 constexpr int kWarps = 4;
 constexpr float kNegBig = -1.0e30f;
 constexpr float kLazy = 4.0f;  // log2 units the running max may lag
+constexpr int kMergeBtStage = 2048;
+constexpr int kMergeThreads = 512;  // block-table entries staged in shared memory (32768 slots)
 
 template <int BITS>
 struct Geom {
@@ -530,7 +532,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
 // Merge the stream-K partials and the bf16 sinks of one (sequence, KV head);
 // write the bf16 outputs of its G query heads; with H2O on, add this step's
 // probabilities to the sink scores and to every pool slot's score.
-__global__ void __launch_bounds__(1024, 2) attn_merge_kernel(DevState s, int seq_begin, int batch,
+__global__ void __launch_bounds__(kMergeThreads, 2) attn_merge_kernel(DevState s, int seq_begin, int batch,
                                                              const uint16_t* __restrict__ q,
                                                              uint16_t* __restrict__ out, float qk_scale_log2,
                                                              AttnWork w, int accumulate) {
@@ -559,9 +561,9 @@ __global__ void __launch_bounds__(1024, 2) attn_merge_kernel(DevState s, int seq
   const uint16_t* sk = s.sink_k + ((size_t)b * hkv + h) * kSinks * kHeadDim;
   const uint16_t* sv = s.sink_v + ((size_t)b * hkv + h) * kSinks * kHeadDim;
 
-  // sink logits: warp (g, j) = (warp / 4, warp % 4)
-  {
-    const int g = warp >> 2, j = warp & 3;
+  // sink logits: warp task (g, j) = (task / 4, task % 4)
+  for (int task = warp; task < kMaxGroup * kSinks; task += kMergeThreads / 32) {
+    const int g = task >> 2, j = task & 3;
     if (g < G) {
       float part = 0.0f;
       if (j < ns) {
@@ -603,8 +605,8 @@ __global__ void __launch_bounds__(1024, 2) attn_merge_kernel(DevState s, int seq
   }
   __syncthreads();
   // outputs: thread (g, d)
-  if ((int)threadIdx.x < G * kHeadDim) {
-    const int g = threadIdx.x >> 7, d = threadIdx.x & (kHeadDim - 1);
+  for (int gd = threadIdx.x; gd < G * kHeadDim; gd += kMergeThreads) {
+    const int g = gd >> 7, d = gd & (kHeadDim - 1);
     const float M = sh_M[g];
     float o = 0.0f;
 #pragma unroll
@@ -622,14 +624,43 @@ __global__ void __launch_bounds__(1024, 2) attn_merge_kernel(DevState s, int seq
     for (int g = 0; g < G; ++g) inc += fast_exp2(sh_sl[g][threadIdx.x] - sh_M[g]) * sh_invL[g];
     s.sink_score[((size_t)b * hkv + h) * kSinks + threadIdx.x] += inc;
   }
+  // score pass: the sequence's block-table row is staged in shared memory
+  // (when it fits) and each thread handles 4 slots with all loads issued first
+  __shared__ int32_t sh_bt[kMergeBtStage];
   const int32_t* bt = s.block_table + (size_t)b * s.max_bps;
+  const int npages = (S + kPage - 1) / kPage;
+  const int32_t* btp = bt;
+  if (npages <= kMergeBtStage) {
+    for (int i = threadIdx.x; i < npages; i += blockDim.x) sh_bt[i] = bt[i];
+    btp = sh_bt;
+  }
+  __syncthreads();
   const float* lgr = w.logits + (size_t)pair * G * w.s_cap;
-  for (int t = threadIdx.x; t < S; t += blockDim.x) {
-    const int blk = bt[t / kPage];
-    if ((unsigned)blk >= (unsigned)s.num_blocks) continue;
-    float inc = 0.0f;
-    for (int g = 0; g < G; ++g) inc += fast_exp2(lgr[(size_t)g * w.s_cap + t] - sh_M[g]) * sh_invL[g];
-    s.score[((size_t)blk * hkv + h) * kPage + (t % kPage)] += inc;
+  const int nt = blockDim.x;
+  for (int t0 = threadIdx.x; t0 < S; t0 += 4 * nt) {
+    int blk[4];
+    float inc[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int t = t0 + u * nt;
+      blk[u] = t < S ? btp[t / kPage] : -1;
+      inc[u] = 0.0f;
+    }
+    for (int g = 0; g < G; ++g) {
+      const float* lrow = lgr + (size_t)g * w.s_cap;
+      const float M = sh_M[g], iL = sh_invL[g];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int t = t0 + u * nt;
+        if (t < S) inc[u] += fast_exp2(lrow[t] - M) * iL;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int t = t0 + u * nt;
+      if (t < S && (unsigned)blk[u] < (unsigned)s.num_blocks)
+        s.score[((size_t)blk[u] * hkv + h) * kPage + (t % kPage)] += inc[u];
+    }
   }
 }
 
@@ -689,7 +720,7 @@ cudaError_t launch_attention_split(const DevState& s, int seq_begin, int batch, 
 cudaError_t launch_attention_merge(const DevState& s, int seq_begin, int batch, const uint16_t* q, uint16_t* out,
                                    float qk_scale_log2, const AttnWork& w, bool accumulate, cudaStream_t st) {
   dim3 grid(s.hkv, batch);
-  attn_merge_kernel<<<grid, 1024, 0, st>>>(s, seq_begin, batch, q, out, qk_scale_log2, w, accumulate ? 1 : 0);
+  attn_merge_kernel<<<grid, kMergeThreads, 0, st>>>(s, seq_begin, batch, q, out, qk_scale_log2, w, accumulate ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -40,7 +40,7 @@ kvc_status config_check(const kvc_config* c) {
       c->num_q_heads / c->num_kv_heads > kvc::kMaxGroup)
     return KVC_ERR_UNSUPPORTED;
   // 32-bit slot arithmetic inside the kernels
-  if ((double)c->num_blocks * c->num_kv_heads * kvc::kPage * 128 > 1.0e18 ||
+  if ((double)c->num_blocks * c->num_kv_heads * kvc::kPage >= 2147483647.0 ||
       (double)c->max_blocks_per_seq * kvc::kPage > 2.0e9)
     return KVC_ERR_UNSUPPORTED;
   return KVC_OK;
@@ -439,8 +439,17 @@ kvc_status kvc_compact_blocks(kvc_cache* c, int32_t seq_begin, int32_t batch, co
   if (!c->plan_pending || c->plan_begin != seq_begin || c->plan_batch != batch) return KVC_ERR_STATE;
   const WsLayout wl = ws_layout(c, batch);
   if (!d_workspace || !aligned(d_workspace, kAlign) || workspace_bytes < wl.total) return KVC_ERR_INVALID_ARG;
+  if (!aligned(d_keep_mask, 16)) return KVC_ERR_INVALID_ARG;
   uint8_t* ws = static_cast<uint8_t*>(d_workspace);
+  // largest move count of the slice: min(kept, evicted) per sequence
+  int max_moves = 0;
+  for (int i = 0; i < batch; ++i) {
+    const int S = c->slots[seq_begin + i], np = c->plan_new[i];
+    if (np < S) max_moves = std::max(max_moves, std::min(np, S - np));
+  }
+  const int smem_moves = max_moves <= kvc::compact_max_smem_moves() ? std::max(max_moves, 1) : 0;
   if (kvc::launch_compact(c->dev, seq_begin, batch, d_keep_mask, s_cap(c), reinterpret_cast<int32_t*>(ws + wl.keys),
+                          reinterpret_cast<int32_t*>(ws + wl.pos), smem_moves,
                           static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return KVC_ERR_CUDA;
   c->last_launches = 1;

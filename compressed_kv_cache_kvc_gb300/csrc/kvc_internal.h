@@ -84,8 +84,12 @@ struct SelectArgs {
 };
 cudaError_t launch_select(const DevState& s, int seq_begin, int batch, const SelectArgs& a,
                           uint8_t* keep_mask, cudaStream_t st);
+// g_holes / g_srcs: [batch][hkv][s_cap] move lists in the workspace, used when
+// smem_moves == 0; otherwise both lists (smem_moves entries each) live in
+// shared memory.
 cudaError_t launch_compact(const DevState& s, int seq_begin, int batch, const uint8_t* keep_mask,
-                           int s_cap, int32_t* g_scratch, cudaStream_t st);
+                           int s_cap, int32_t* g_holes, int32_t* g_srcs, int smem_moves, cudaStream_t st);
+int compact_max_smem_moves();
 
 int attention_smem_bytes(int bits);
 int attention_ctas_per_sm(int bits);  // resident split CTAs per SM (occupancy API, cached)

@@ -24,7 +24,8 @@ namespace kvc {
 namespace {
 
 constexpr int kSelThreads = 1024;
-constexpr int kCompactThreads = 512;
+constexpr int kCompactThreads = 1024;
+constexpr int kSelBtStage = 2048;  // block-table entries staged in shared memory
 
 __device__ __forceinline__ size_t slot_index(const DevState& s, const int32_t* bt, int h, int t, bool& ok) {
   const int blk = bt[t / kPage];
@@ -167,20 +168,44 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(DevState s, int seq
   }
   const int32_t* bt = s.block_table + (size_t)b * s.max_bps;
   const bool h2o = a.mode == 0;
-  for (int t = threadIdx.x; t < S; t += blockDim.x) {
-    bool ok;
-    const size_t idx = slot_index(s, bt, h, t, ok);
-    const int p = ok ? s.slot_pos[idx] : -1;
-    uint32_t key = 0;
-    if (!ok) {
-      atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
-    } else if (p >= thr) {
-      key = 0xFFFFFFFFu;
-    } else if (h2o) {
-      key = __float_as_uint(fmaxf(s.score[idx], 0.0f));
+  // stage the block-table row in shared memory when it fits
+  __shared__ int32_t sh_bt[kSelBtStage];
+  const int npages = (S + kPage - 1) / kPage;
+  const int32_t* btp = bt;
+  if (npages <= kSelBtStage) {
+    for (int i = threadIdx.x; i < npages; i += blockDim.x) sh_bt[i] = bt[i];
+    btp = sh_bt;
+  }
+  __syncthreads();
+  const int nt = blockDim.x;
+  for (int t0 = threadIdx.x; t0 < S; t0 += 4 * nt) {
+    int p[4];
+    float sc[4];
+    bool ok[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int t = t0 + u * nt;
+      const int blk = t < S ? btp[t / kPage] : 0;
+      ok[u] = t < S && (unsigned)blk < (unsigned)s.num_blocks;
+      const size_t idx = ((size_t)(ok[u] ? blk : 0) * s.hkv + h) * kPage + (t % kPage);
+      p[u] = ok[u] ? s.slot_pos[idx] : -1;
+      sc[u] = (ok[u] && h2o) ? s.score[idx] : 0.0f;
     }
-    keys[t] = key;
-    pos[t] = p;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int t = t0 + u * nt;
+      if (t >= S) continue;
+      uint32_t key = 0;
+      if (!ok[u]) {
+        atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
+      } else if (p[u] >= thr) {
+        key = 0xFFFFFFFFu;
+      } else if (h2o) {
+        key = __float_as_uint(fmaxf(sc[u], 0.0f));
+      }
+      keys[t] = key;
+      pos[t] = p[u];
+    }
   }
   __syncthreads();
 
@@ -205,9 +230,17 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(DevState s, int seq
   }
 }
 
+// Compaction of one (KV head, sequence).  Phase 1 (tiles of 16 slots per
+// thread): the keep-mask bytes of a thread's 16 slots come in one 16-byte
+// load; block scans give every hole (evicted slot below n') and every source
+// (kept slot at or above n') its rank, and the physical pool index of the
+// i-th hole and of the i-th source go to two lists.  Phase 2: each warp moves
+// several (source -> hole) rows at once, lanes splitting a row 4 bytes each,
+// all loads of a batch issued before its stores.
 __global__ void __launch_bounds__(kCompactThreads) compact_kernel(DevState s, int seq_begin,
                                                                  const uint8_t* __restrict__ mask, int s_cap,
-                                                                 int32_t* __restrict__ scratch) {
+                                                                 int32_t* __restrict__ g_holes,
+                                                                 int32_t* __restrict__ g_srcs, int smem_moves) {
   const int h = blockIdx.x;
   const int bl = blockIdx.y;
   const int b = seq_begin + bl;
@@ -215,63 +248,101 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(DevState s, in
   const int np = s.plan[2 * b + 1];
   if (np >= S) return;
   __shared__ int sh_warp[32];
-  const uint8_t* mrow = mask + ((size_t)bl * s.hkv + h) * s_cap;
-  int32_t* holes = scratch + ((size_t)bl * s.hkv + h) * s_cap;
+  extern __shared__ __align__(16) int32_t dyn_lists[];
+  const size_t pair = (size_t)bl * s.hkv + h;
+  const uint8_t* mrow = mask + pair * s_cap;
+  int32_t* holes = smem_moves > 0 ? dyn_lists : g_holes + pair * s_cap;
+  int32_t* srcs = smem_moves > 0 ? dyn_lists + smem_moves : g_srcs + pair * s_cap;
   const int32_t* bt = s.block_table + (size_t)b * s.max_bps;
-  // each thread owns one run of consecutive slots
-  const int run = (S + kCompactThreads - 1) / kCompactThreads;
-  const int t0 = min(S, (int)threadIdx.x * run);
-  const int t1 = min(S, t0 + run);
+  const int hkv = s.hkv;
 
-  // pass 1: holes (evicted slots below n') in ascending order; count kept
-  int my_holes = 0, my_kept = 0;
-  for (int t = t0; t < t1; ++t) {
-    const bool kept = mrow[t] != 0;
-    my_kept += kept;
-    my_holes += (t < np && !kept);
+  int hole_base = 0, src_base = 0, kept_total = 0;
+  for (int tile0 = 0; tile0 < S; tile0 += kCompactThreads * 16) {
+    const int t0 = tile0 + threadIdx.x * 16;
+    uint32_t kept_bits = 0;
+    if (t0 < S) {
+      const uint4 m = *reinterpret_cast<const uint4*>(mrow + t0);
+      const uint32_t wv[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (((wv[i >> 2] >> (8 * (i & 3))) & 0xFFu) != 0 && t0 + i < S) kept_bits |= 1u << i;
+    }
+    // bit i of `below` is set when slot t0 + i < n'
+    const int nb = min(max(np - t0, 0), 16);
+    const uint32_t below = nb >= 16 ? 0xFFFFu : ((1u << nb) - 1u);
+    const int nv = min(max(S - t0, 0), 16);
+    const uint32_t valid = nv >= 16 ? 0xFFFFu : ((1u << nv) - 1u);
+    const uint32_t hole_bits = ~kept_bits & below & valid;
+    const uint32_t src_bits = kept_bits & ~below;
+    const int nh = __popc(hole_bits), ns = __popc(src_bits), nk = __popc(kept_bits);
+    int tot_h, tot_s, tot_k;
+    int ph = hole_base + block_scan<kCompactThreads>(nh, sh_warp, &tot_h) - nh;
+    int ps = src_base + block_scan<kCompactThreads>(ns, sh_warp, &tot_s) - ns;
+    block_scan<kCompactThreads>(nk, sh_warp, &tot_k);
+    for (uint32_t m = hole_bits; m; m &= m - 1) {
+      const int t = t0 + __ffs(m) - 1;
+      holes[ph++] = (bt[t / kPage] * hkv + h) * kPage + (t % kPage);
+    }
+    for (uint32_t m = src_bits; m; m &= m - 1) {
+      const int t = t0 + __ffs(m) - 1;
+      srcs[ps++] = (bt[t / kPage] * hkv + h) * kPage + (t % kPage);
+    }
+    hole_base += tot_h;
+    src_base += tot_s;
+    kept_total += tot_k;
   }
-  int tot_h, tot_k;
-  int pos_h = block_scan<kCompactThreads>(my_holes, sh_warp, &tot_h) - my_holes;
-  block_scan<kCompactThreads>(my_kept, sh_warp, &tot_k);
-  if (tot_k != np) {
+  if (kept_total != np || hole_base != src_base) {
     if (threadIdx.x == 0) atomicOr(&s.counters[kCtrStatus], kDevBadKeepMask);
     return;
   }
-  for (int t = t0; t < min(t1, np); ++t)
-    if (mrow[t] == 0) holes[pos_h++] = t;
   __syncthreads();
 
-  // pass 2: kept slots at or above n', in ascending order, fill the holes
-  const int a0 = max(t0, np);
-  int my_src = 0;
-  for (int t = a0; t < t1; ++t) my_src += mrow[t] != 0;
-  int tot_s;
-  int rank = block_scan<kCompactThreads>(my_src, sh_warp, &tot_s) - my_src;
-  const int rb = s.row_bytes;
-  for (int t = a0; t < t1; ++t) {
-    if (mrow[t] == 0) continue;
-    const int dst = holes[rank++];
-    bool ok1, ok2;
-    const size_t si = slot_index(s, bt, h, t, ok1);
-    const size_t di = slot_index(s, bt, h, dst, ok2);
-    if (!(ok1 && ok2)) {
-      atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
-      continue;
+  // phase 2: moves.  A row of codes is row_bytes / 4 words; lanes split it.
+  const int n_moves = hole_base;
+  const int words = s.row_bytes / 4;            // 32 (INT8) or 16 (INT4)
+  const int per_pass = 32 / words;              // moves covered by one warp instruction
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sub = lane / words, wl = lane % words;
+  constexpr int U = 4;
+  const int nwarps = kCompactThreads / 32;
+  const uint32_t nslots = (uint32_t)s.num_blocks * hkv * kPage;
+  const uint32_t* kc = reinterpret_cast<const uint32_t*>(s.k_codes);
+  const uint32_t* vc = reinterpret_cast<const uint32_t*>(s.v_codes);
+  for (int base = warp * per_pass * U; base < n_moves; base += nwarps * per_pass * U) {
+    uint32_t kw[U], vw[U], si[U], di[U];
+    float sc[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int mi = base + u * per_pass + sub;
+      si[u] = mi < n_moves ? (uint32_t)srcs[mi] : 0xFFFFFFFFu;
+      di[u] = mi < n_moves ? (uint32_t)holes[mi] : 0xFFFFFFFFu;
+      const bool ok = si[u] < nslots && di[u] < nslots;
+      if (!ok) si[u] = di[u] = 0xFFFFFFFFu;
+      kw[u] = ok ? kc[(size_t)si[u] * words + wl] : 0u;
+      vw[u] = ok ? vc[(size_t)si[u] * words + wl] : 0u;
+      sc[u] = 0.0f;
+      if (ok && wl < 4) {
+        const uint32_t* scal = wl == 0 ? reinterpret_cast<const uint32_t*>(s.k_scale)
+                             : wl == 1 ? reinterpret_cast<const uint32_t*>(s.v_scale)
+                             : wl == 2 ? reinterpret_cast<const uint32_t*>(s.slot_pos)
+                                       : reinterpret_cast<const uint32_t*>(s.score);
+        sc[u] = __uint_as_float(scal[si[u]]);
+      }
     }
-    const uint4* ks = reinterpret_cast<const uint4*>(s.k_codes + si * rb);
-    const uint4* vs = reinterpret_cast<const uint4*>(s.v_codes + si * rb);
-    uint4* kd = reinterpret_cast<uint4*>(s.k_codes + di * rb);
-    uint4* vd = reinterpret_cast<uint4*>(s.v_codes + di * rb);
-    for (int i = 0; i < rb / 16; ++i) {
-      kd[i] = ks[i];
-      vd[i] = vs[i];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (di[u] == 0xFFFFFFFFu) continue;
+      reinterpret_cast<uint32_t*>(s.k_codes)[(size_t)di[u] * words + wl] = kw[u];
+      reinterpret_cast<uint32_t*>(s.v_codes)[(size_t)di[u] * words + wl] = vw[u];
+      if (wl < 4) {
+        uint32_t* scal = wl == 0 ? reinterpret_cast<uint32_t*>(s.k_scale)
+                       : wl == 1 ? reinterpret_cast<uint32_t*>(s.v_scale)
+                       : wl == 2 ? reinterpret_cast<uint32_t*>(s.slot_pos)
+                                 : reinterpret_cast<uint32_t*>(s.score);
+        scal[di[u]] = __float_as_uint(sc[u]);
+      }
     }
-    s.k_scale[di] = s.k_scale[si];
-    s.v_scale[di] = s.v_scale[si];
-    s.slot_pos[di] = s.slot_pos[si];
-    s.score[di] = s.score[si];
   }
-
   // release the emptied pages (all KV heads share the page structure)
   if (h == 0) {
     const int keep_pages = (np + kPage - 1) / kPage;
@@ -322,10 +393,25 @@ cudaError_t launch_select(const DevState& s, int seq_begin, int batch, const Sel
   return cudaGetLastError();
 }
 
+int compact_max_smem_moves() { return (96 * 1024) / 8; }
+
 cudaError_t launch_compact(const DevState& s, int seq_begin, int batch, const uint8_t* keep_mask, int s_cap,
-                           int32_t* g_scratch, cudaStream_t st) {
+                           int32_t* g_holes, int32_t* g_srcs, int smem_moves, cudaStream_t st) {
+  const int smem = smem_moves > 0 ? smem_moves * 8 : 0;
+  if (smem > 48 * 1024) {
+    static int done[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 64 || !done[dev]) {
+      e = cudaFuncSetAttribute(compact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               compact_max_smem_moves() * 8);
+      if (e != cudaSuccess) return e;
+      if (dev < 64) done[dev] = 1;
+    }
+  }
   dim3 grid(s.hkv, batch);
-  compact_kernel<<<grid, kCompactThreads, 0, st>>>(s, seq_begin, keep_mask, s_cap, g_scratch);
+  compact_kernel<<<grid, kCompactThreads, smem, st>>>(s, seq_begin, keep_mask, s_cap, g_holes, g_srcs, smem_moves);
   return cudaGetLastError();
 }
 
