@@ -71,25 +71,44 @@ __device__ __forceinline__ void cp_async8(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(smem_u32(dst)), "l"(src));
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+__device__ __forceinline__ void cp_async16_s(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src));
+}
+// All code chunks of one page for this lane (see the lane offsets in the
+// split kernel): K then V, at fixed immediate distances from the lane bases.
+template <int BITS>
+__device__ __forceinline__ void copy_page(uint32_t sK, const uint8_t* kg, uint32_t sV, const uint8_t* vg) {
+  if (BITS == 8) {
+    asm volatile(
+        "cp.async.cg.shared.global [%0], [%1], 16;\n"
+        "cp.async.cg.shared.global [%0+512], [%1+16], 16;\n"
+        "cp.async.cg.shared.global [%0+1024], [%1+128], 16;\n"
+        "cp.async.cg.shared.global [%0+1536], [%1+144], 16;\n"
+        "cp.async.cg.shared.global [%2], [%3], 16;\n"
+        "cp.async.cg.shared.global [%2+512], [%3+128], 16;\n"
+        "cp.async.cg.shared.global [%2+1024], [%3+256], 16;\n"
+        "cp.async.cg.shared.global [%2+1536], [%3+384], 16;\n" ::"r"(sK), "l"(kg), "r"(sV), "l"(vg));
+  } else {
+    asm volatile(
+        "cp.async.cg.shared.global [%0], [%1], 16;\n"
+        "cp.async.cg.shared.global [%0+512], [%1+64], 16;\n"
+        "cp.async.ca.shared.global [%2], [%3], 8;\n"
+        "cp.async.ca.shared.global [%2+256], [%3+64], 8;\n"
+        "cp.async.ca.shared.global [%2+512], [%3+128], 8;\n"
+        "cp.async.ca.shared.global [%2+768], [%3+192], 8;\n" ::"r"(sK), "l"(kg), "r"(sV), "l"(vg));
+  }
+}
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
 
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t d;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-  return d;
-}
-__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) { return __byte_perm(a, b, sel); }
+__device__ __forceinline__ uint32_t as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) { return as_u32(__hsub2(as_h2(a), as_h2(b))); }
 __device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
+  return as_u32(__hfma2(as_h2(a), as_h2(b), as_h2(c)));
 }
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
@@ -133,6 +152,9 @@ __device__ __forceinline__ uint32_t i4_hi_to_h2(uint32_t v) {
 }
 
 __device__ __forceinline__ float bf16f(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+
+// 2^e as a float, for -126 <= e <= 127 (exact).
+__device__ __forceinline__ float pow2i(int e) { return __int_as_float((e + 127) << 23); }
 
 // Unbiased exponent of a positive normal float (floor(log2 x)).
 __device__ __forceinline__ int exponent_of(float x) {
@@ -193,15 +215,16 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
   extern __shared__ __align__(16) uint8_t smem[];
   uint8_t* ring = smem + warp * STAGES * Gm::kStage;
 
-  // per-lane offsets, within a head-page, of the chunks this lane copies and reads
-  uint32_t k_src[Gm::kKChunks], v_src[4];
-#pragma unroll
-  for (int j = 0; j < Gm::kKChunks; ++j)
-    k_src[j] = BITS == 8 ? (2 * r + (j >> 1)) * 128 + 32 * c + 16 * (j & 1) : (2 * r + j) * 64 + 16 * c;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) v_src[j] = BITS == 8 ? (4 * c + j) * 128 + 16 * r : (4 * c + j) * 64 + 8 * r;
-  const float* sc_src_base = lane < 4 ? s.k_scale : s.v_scale;
-  const uint32_t sc_off = 4 * (lane & 3);
+  // per-lane byte offsets of the chunks this lane copies: within a head-page
+  // (global) and within a stage (shared); the chunks of one page sit at fixed
+  // distances from these, so one asm block copies a page with immediates
+  const uint32_t ring_s = smem_u32(smem) + warp * STAGES * Gm::kStage;
+  const uint32_t k_goff = BITS == 8 ? (2 * r) * 128 + 32 * c : (2 * r) * 64 + 16 * c;
+  const uint32_t v_goff = BITS == 8 ? (4 * c) * 128 + 16 * r : (4 * c) * 64 + 8 * r;
+  const uint32_t k_soff = lane * 16;
+  const uint32_t v_soff = Gm::kKBytes + (BITS == 8 ? lane * 16 : lane * 8);
+  const uint32_t sc_soff = Gm::kKBytes + Gm::kVBytes + 16 * lane;
+  const float* sc_gbase = (lane < 4 ? s.k_scale : s.v_scale) + 4 * (lane & 3);
 
   while (F < F1) {
     // ---- the (sequence, KV head) pair of page F and this CTA's run of its pages
@@ -251,8 +274,9 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
       int e = 0;
       if (amax > 0.0f) e = min(max(14 - exponent_of(amax), -100), 100);
+      const float f2e = pow2i(e);  // multiplying by a power of two is exact here
 #pragma unroll
-      for (int i = 0; i < 32; ++i) qv[i] = ldexpf(qv[i], e);
+      for (int i = 0; i < 32; ++i) qv[i] *= f2e;
       if (BITS == 8) {
 #pragma unroll
         for (int st = 0; st < 8; ++st) {
@@ -270,8 +294,8 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
       }
       const int e0 = __shfl_sync(0xffffffffu, e, (2 * c) * 4);
       const int e1 = __shfl_sync(0xffffffffu, e, (2 * c + 1) * 4);
-      cq0 = ldexpf(qk_scale_log2, -e0);
-      cq1 = ldexpf(qk_scale_log2, -e1);
+      cq0 = qk_scale_log2 * pow2i(-e0);
+      cq1 = qk_scale_log2 * pow2i(-e1);
     }
 
     // ---- page pipeline: this warp takes pages pg_a + warp, + kWarps, ...
@@ -288,20 +312,10 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
         const bool ok = (unsigned)blk < (unsigned)s.num_blocks;
         stage_ok = ok ? (stage_ok | (1u << st_issue)) : (stage_ok & ~(1u << st_issue));
         if (ok) {
-          uint8_t* st = ring + st_issue * Gm::kStage;
+          const uint32_t sb = ring_s + st_issue * Gm::kStage;
           const size_t hp = ((size_t)blk * hkv + h) * kPage;
-          const uint8_t* kb = s.k_codes + hp * RB;
-          const uint8_t* vb = s.v_codes + hp * RB;
-#pragma unroll
-          for (int j = 0; j < Gm::kKChunks; ++j) cp_async16(st + j * 512 + lane * 16, kb + k_src[j]);
-          if (BITS == 8) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) cp_async16(st + Gm::kKBytes + j * 512 + lane * 16, vb + v_src[j]);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) cp_async8(st + Gm::kKBytes + j * 256 + lane * 8, vb + v_src[j]);
-          }
-          if (lane < 8) cp_async16(st + Gm::kKBytes + Gm::kVBytes + 16 * lane, sc_src_base + hp + sc_off);
+          copy_page<BITS>(sb + k_soff, s.k_codes + hp * RB + k_goff, sb + v_soff, s.v_codes + hp * RB + v_goff);
+          if (lane < 8) cp_async16_s(sb + sc_soff, sc_gbase + hp);
         }
       }
       cp_async_commit();
@@ -395,7 +409,8 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
         const bool rescale_e = svm > sv_hi || (!e_set && svm > 0.0f);
         int nE = E;
         if (rescale_e) nE = min(max(exponent_of(svm), -126), 126);
-        const float f = ldexpf(1.0f, E - nE);
+        const int dE = E - nE;  // <= 0 once E is set; up to +126 on the first page (O is 0 then)
+        const float f = dE >= -126 ? pow2i(min(dE, 127)) : 0.0f;
         const float f0 = al0 * f, f1 = al1 * f;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -411,8 +426,8 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
         if (rescale_e) {
           E = nE;
           e_set = true;
-          sv_hi = ldexpf(1.0f, E + 4);
-          inv2E = ldexpf(1.0f, -E);
+          sv_hi = pow2i(min(E + 4, 127));
+          inv2E = pow2i(-E);
         }
       }
       const float sn0 = v0 ? svv.x * inv2E : 0.0f;
@@ -482,7 +497,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
       l0 += __shfl_xor_sync(0xffffffffu, l0, o);
       l1 += __shfl_xor_sync(0xffffffffu, l1, o);
     }
-    const float f2E = ldexpf(1.0f, E);
+    const float f2E = pow2i(E);
     __syncthreads();  // every warp is done with its ring: reuse shared memory
     float* sm_m = reinterpret_cast<float*>(smem);  // [kWarps][8]
     float* sm_l = sm_m + kWarps * kMaxGroup;       // [kWarps][8]

@@ -24,7 +24,7 @@ namespace kvc {
 namespace {
 
 constexpr int kSelThreads = 1024;
-constexpr int kCompactThreads = 1024;
+constexpr int kCompactThreads = 512;
 constexpr int kSelBtStage = 2048;  // block-table entries staged in shared memory
 
 __device__ __forceinline__ size_t slot_index(const DevState& s, const int32_t* bt, int h, int t, bool& ok) {
@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(DevState s, in
   const int per_pass = 32 / words;              // moves covered by one warp instruction
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sub = lane / words, wl = lane % words;
-  constexpr int U = 4;
+  constexpr int U = 8;
   const int nwarps = kCompactThreads / 32;
   const uint32_t nslots = (uint32_t)s.num_blocks * hkv * kPage;
   const uint32_t* kc = reinterpret_cast<const uint32_t*>(s.k_codes);
