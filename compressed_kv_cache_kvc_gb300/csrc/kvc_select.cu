@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(DevState s, int seq
 // i-th hole and of the i-th source go to two lists.  Phase 2: each warp moves
 // several (source -> hole) rows at once, lanes splitting a row 4 bytes each,
 // all loads of a batch issued before its stores.
-__global__ void __launch_bounds__(kCompactThreads) compact_kernel(DevState s, int seq_begin,
+__global__ void __launch_bounds__(kCompactThreads, 2) compact_kernel(DevState s, int seq_begin,
                                                                  const uint8_t* __restrict__ mask, int s_cap,
                                                                  int32_t* __restrict__ g_holes,
                                                                  int32_t* __restrict__ g_srcs, int smem_moves) {
@@ -255,8 +255,17 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(DevState s, in
   int32_t* srcs = smem_moves > 0 ? dyn_lists + smem_moves : g_srcs + pair * s_cap;
   const int32_t* bt = s.block_table + (size_t)b * s.max_bps;
   const int hkv = s.hkv;
+  // the sequence's block-table row, staged in shared memory when it fits
+  __shared__ int32_t sh_bt[kSelBtStage];
+  const int npages = (S + kPage - 1) / kPage;
+  const int32_t* btp = bt;
+  if (npages <= kSelBtStage) {
+    for (int i = threadIdx.x; i < npages; i += blockDim.x) sh_bt[i] = bt[i];
+    btp = sh_bt;
+  }
+  __syncthreads();
 
-  int hole_base = 0, src_base = 0, kept_total = 0;
+  int hole_base = 0, src_base = 0;
   for (int tile0 = 0; tile0 < S; tile0 += kCompactThreads * 16) {
     const int t0 = tile0 + threadIdx.x * 16;
     uint32_t kept_bits = 0;
@@ -274,75 +283,70 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(DevState s, in
     const uint32_t valid = nv >= 16 ? 0xFFFFu : ((1u << nv) - 1u);
     const uint32_t hole_bits = ~kept_bits & below & valid;
     const uint32_t src_bits = kept_bits & ~below;
-    const int nh = __popc(hole_bits), ns = __popc(src_bits), nk = __popc(kept_bits);
-    int tot_h, tot_s, tot_k;
-    int ph = hole_base + block_scan<kCompactThreads>(nh, sh_warp, &tot_h) - nh;
-    int ps = src_base + block_scan<kCompactThreads>(ns, sh_warp, &tot_s) - ns;
-    block_scan<kCompactThreads>(nk, sh_warp, &tot_k);
+    // one scan of both counts (each <= 16 per thread, <= 8192 per tile)
+    const int nh = __popc(hole_bits), ns = __popc(src_bits);
+    int tot_packed;
+    const int incl = block_scan<kCompactThreads>(nh | (ns << 16), sh_warp, &tot_packed);
+    int ph = hole_base + (incl & 0xFFFF) - nh;
+    int ps = src_base + (incl >> 16) - ns;
     for (uint32_t m = hole_bits; m; m &= m - 1) {
       const int t = t0 + __ffs(m) - 1;
-      holes[ph++] = (bt[t / kPage] * hkv + h) * kPage + (t % kPage);
+      holes[ph++] = (btp[t / kPage] * hkv + h) * kPage + (t % kPage);
     }
     for (uint32_t m = src_bits; m; m &= m - 1) {
       const int t = t0 + __ffs(m) - 1;
-      srcs[ps++] = (bt[t / kPage] * hkv + h) * kPage + (t % kPage);
+      srcs[ps++] = (btp[t / kPage] * hkv + h) * kPage + (t % kPage);
     }
-    hole_base += tot_h;
-    src_base += tot_s;
-    kept_total += tot_k;
+    hole_base += tot_packed & 0xFFFF;
+    src_base += tot_packed >> 16;
   }
-  if (kept_total != np || hole_base != src_base) {
+  // kept slots = (n' - holes) below n' plus the sources above it; the mask
+  // holds exactly n' kept slots iff holes and sources pair up
+  if (hole_base != src_base) {
     if (threadIdx.x == 0) atomicOr(&s.counters[kCtrStatus], kDevBadKeepMask);
     return;
   }
   __syncthreads();
 
-  // phase 2: moves.  A row of codes is row_bytes / 4 words; lanes split it.
+  // phase 2: moves, one thread per (source -> hole) pair: the K and V rows
+  // move as 16-byte vectors (all loads of a row pair in flight before the
+  // stores), then the four per-slot values
   const int n_moves = hole_base;
-  const int words = s.row_bytes / 4;            // 32 (INT8) or 16 (INT4)
-  const int per_pass = 32 / words;              // moves covered by one warp instruction
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int sub = lane / words, wl = lane % words;
-  constexpr int U = 8;
-  const int nwarps = kCompactThreads / 32;
   const uint32_t nslots = (uint32_t)s.num_blocks * hkv * kPage;
-  const uint32_t* kc = reinterpret_cast<const uint32_t*>(s.k_codes);
-  const uint32_t* vc = reinterpret_cast<const uint32_t*>(s.v_codes);
-  for (int base = warp * per_pass * U; base < n_moves; base += nwarps * per_pass * U) {
-    uint32_t kw[U], vw[U], si[U], di[U];
-    float sc[U];
+  const int vecs = s.row_bytes / 16;  // 8 (INT8) or 4 (INT4)
+  for (int mi = threadIdx.x; mi < n_moves; mi += kCompactThreads) {
+    const uint32_t si = (uint32_t)srcs[mi];
+    const uint32_t di = (uint32_t)holes[mi];
+    if (si >= nslots || di >= nslots) {
+      atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
+      continue;
+    }
+    const uint4* kp = reinterpret_cast<const uint4*>(s.k_codes + (size_t)si * s.row_bytes);
+    const uint4* vp = reinterpret_cast<const uint4*>(s.v_codes + (size_t)si * s.row_bytes);
+    uint4* kd = reinterpret_cast<uint4*>(s.k_codes + (size_t)di * s.row_bytes);
+    uint4* vd = reinterpret_cast<uint4*>(s.v_codes + (size_t)di * s.row_bytes);
+    const float ks = s.k_scale[si], vs = s.v_scale[si], sc = s.score[si];
+    const int ps = s.slot_pos[si];
+    // 64-byte halves of the K and V rows: 8 vectors in flight, then stored
+    for (int h0 = 0; h0 < vecs; h0 += 4) {
+      uint4 kv[4], vv[4];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int mi = base + u * per_pass + sub;
-      si[u] = mi < n_moves ? (uint32_t)srcs[mi] : 0xFFFFFFFFu;
-      di[u] = mi < n_moves ? (uint32_t)holes[mi] : 0xFFFFFFFFu;
-      const bool ok = si[u] < nslots && di[u] < nslots;
-      if (!ok) si[u] = di[u] = 0xFFFFFFFFu;
-      kw[u] = ok ? kc[(size_t)si[u] * words + wl] : 0u;
-      vw[u] = ok ? vc[(size_t)si[u] * words + wl] : 0u;
-      sc[u] = 0.0f;
-      if (ok && wl < 4) {
-        const uint32_t* scal = wl == 0 ? reinterpret_cast<const uint32_t*>(s.k_scale)
-                             : wl == 1 ? reinterpret_cast<const uint32_t*>(s.v_scale)
-                             : wl == 2 ? reinterpret_cast<const uint32_t*>(s.slot_pos)
-                                       : reinterpret_cast<const uint32_t*>(s.score);
-        sc[u] = __uint_as_float(scal[si[u]]);
+      for (int i = 0; i < 4; ++i) {
+        kv[i] = kp[h0 + i];
+        vv[i] = vp[h0 + i];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        kd[h0 + i] = kv[i];
+        vd[h0 + i] = vv[i];
       }
     }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      if (di[u] == 0xFFFFFFFFu) continue;
-      reinterpret_cast<uint32_t*>(s.k_codes)[(size_t)di[u] * words + wl] = kw[u];
-      reinterpret_cast<uint32_t*>(s.v_codes)[(size_t)di[u] * words + wl] = vw[u];
-      if (wl < 4) {
-        uint32_t* scal = wl == 0 ? reinterpret_cast<uint32_t*>(s.k_scale)
-                       : wl == 1 ? reinterpret_cast<uint32_t*>(s.v_scale)
-                       : wl == 2 ? reinterpret_cast<uint32_t*>(s.slot_pos)
-                                 : reinterpret_cast<uint32_t*>(s.score);
-        scal[di[u]] = __float_as_uint(sc[u]);
-      }
-    }
+    s.k_scale[di] = ks;
+    s.v_scale[di] = vs;
+    s.slot_pos[di] = ps;
+    s.score[di] = sc;
   }
+
   // release the emptied pages (all KV heads share the page structure)
   if (h == 0) {
     const int keep_pages = (np + kPage - 1) / kPage;
