@@ -187,13 +187,13 @@ def reference_arm(args):
         return
     from compressed_kv_cache_kvc_gb300 import workloads as W
     w = W.WORKLOADS[WORKLOAD]
-    n_seq = 1
+    n_seq, reps = 1, 4
     for _ in range(args.warmup):
         run_oracle_child(n_seq, 1)
     secs, nbytes = 0.0, 0
     desc = ""
     for _ in range(args.steps):
-        r = run_oracle_child(n_seq, 1)
+        r = run_oracle_child(n_seq, reps)
         secs += r["seconds"]
         nbytes += r["bytes"]
         desc = r["desc"]
@@ -383,7 +383,7 @@ def gpu_arm(args):
         return
     cpu = None
     if not args.no_cpu_baseline and ws == 1:
-        r = run_oracle_child(1, 1)
+        r = run_oracle_child(4, 60)
         cpu = {"value": r["bytes"] / r["seconds"] / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": r["desc"], "seconds": r["seconds"]}
     traffic = None
