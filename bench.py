@@ -257,17 +257,13 @@ def gpu_arm(args):
             c.state_view.copy_(s, non_blocking=True)
 
     def step(stream=None):
+        # one library call per layer: append, split-K attention, and the fused
+        # merge + H2O scores + selection + compaction kernel
         n = 0
         for l, c in enumerate(caches):
             q, kn, vn = inputs[l]
-            c.quantize_append(kn, vn, stream=stream)
-            n += c.last_launch_count()
-            c.decode_attention(q, out=outs[l], workspace=ws_buf, stream=stream)
-            n += c.last_launch_count()
-            c.h2o_select_evict(B, "h2o", budget=w.budget, recent=w.recent, keep_mask=mask, workspace=ws_buf,
-                               stream=stream)
-            n += c.last_launch_count()
-            c.compact_blocks(mask, B, workspace=ws_buf, stream=stream)
+            c.decode_step(q, kn, vn, mode="h2o", budget=w.budget, recent=w.recent, out=outs[l], workspace=ws_buf,
+                          stream=stream)
             n += c.last_launch_count()
         return n
 
@@ -367,7 +363,7 @@ def gpu_arm(args):
                 for dst, src in zip(d_in[l], h_in[l]):
                     dst.copy_(src, non_blocking=True)
                 q, kn, vn = d_in[l]
-                c.step(q, kn, vn, mode="h2o", budget=w.budget, recent=w.recent, out=outs[l], keep_mask=mask)
+                c.decode_step(q, kn, vn, mode="h2o", budget=w.budget, recent=w.recent, out=outs[l], workspace=ws_buf)
                 h_out[l].copy_(outs[l], non_blocking=True)
             ev1.record(stream)
             ev1.synchronize()
@@ -410,7 +406,7 @@ def gpu_arm(args):
                      "avg_launch_ms": attn_avg_ms, "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)"},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_step, "path": "KVCache.step per layer, eager, pinned host buffers"},
+                "ms_per_step": e2e_step, "path": "KVCache.decode_step per layer, eager, pinned host buffers"},
         "gpu_launches": launches * args.steps,
         "clocks": clocks,
     }

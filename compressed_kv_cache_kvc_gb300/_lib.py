@@ -64,6 +64,7 @@ _SIGS = {
     "kvc_decode_attention": (_I, [_P, _I, _I, _P, _P, ctypes.c_float, _I, _P, _SZ, _P]),
     "kvc_h2o_select_evict": (_I, [_P, _I, _I, ctypes.POINTER(KvcEvictParams), _P, _P, _SZ, _P]),
     "kvc_compact_blocks": (_I, [_P, _I, _I, _P, _P, _SZ, _P]),
+    "kvc_decode_step": (_I, [_P, _I, _I, _P, _P, _P, _P, ctypes.c_float, ctypes.POINTER(KvcEvictParams), _P, _SZ, _P]),
     "kvc_decode_attention_noalloc": (_I, [_P, _I, _I, _P, _P, ctypes.c_float, _I, _P]),
     "kvc_read_status": (_I, [_P, ctypes.POINTER(_I), _P]),
     "kvc_set_trace_events": (_I, [_P, _P, _P]),

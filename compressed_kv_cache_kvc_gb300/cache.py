@@ -173,6 +173,33 @@ class KVCache:
                                             ctypes.c_void_p(ws.data_ptr()), ws.numel(),
                                             ctypes.c_void_p(_stream_ptr(stream))), "kvc_compact_blocks")
 
+    def decode_step(self, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, mode: str = "h2o",
+                    budget: int = 0, recent: int = 0, window: int = 0, seq_begin: int = 0, out=None,
+                    sm_scale: float | None = None, workspace=None, stream=None) -> torch.Tensor:
+        """The whole decode step of this layer in one library call (append one
+        token, attention, selection, compaction); same results as `step`."""
+        _need(q, torch.bfloat16, "q")
+        _need(k_new, torch.bfloat16, "k_new")
+        _need(v_new, torch.bfloat16, "v_new")
+        batch = q.shape[0]
+        if q.dim() != 3 or q.shape[1] != self.num_q_heads or q.shape[2] != HEAD_DIM:
+            raise ValueError("q must be [batch, num_q_heads, 128]")
+        if tuple(k_new.shape) != (batch, self.num_kv_heads, 1, HEAD_DIM) or k_new.shape != v_new.shape:
+            raise ValueError("k_new, v_new must be [batch, num_kv_heads, 1, 128]")
+        if out is None:
+            out = torch.empty_like(q)
+        _need(out, torch.bfloat16, "out")
+        ws = self.workspace(batch) if workspace is None else workspace
+        scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
+        m = {"h2o": L.KVC_EVICT_H2O, "streaming": L.KVC_EVICT_STREAMING}[mode]
+        params = L.KvcEvictParams(m, budget, recent, window)
+        L.check(self.lib.kvc_decode_step(self.handle, seq_begin, batch, ctypes.c_void_p(q.data_ptr()),
+                                         ctypes.c_void_p(k_new.data_ptr()), ctypes.c_void_p(v_new.data_ptr()),
+                                         ctypes.c_void_p(out.data_ptr()), ctypes.c_float(scale), ctypes.byref(params),
+                                         ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                                         ctypes.c_void_p(_stream_ptr(stream))), "kvc_decode_step")
+        return out
+
     def step(self, q, k_new, v_new, mode="h2o", budget=0, recent=0, window=0, seq_begin=0, out=None,
              keep_mask=None, stream=None):
         """One decode step of this layer: append -> attention (+H2O) -> select -> compact."""

@@ -39,16 +39,18 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "kvc_device.h"
 #include "kvc_internal.h"
 
 namespace kvc {
 namespace {
 
+using namespace dev;
+
 constexpr int kWarps = 4;
-constexpr float kNegBig = -1.0e30f;
-constexpr float kLazy = 4.0f;  // log2 units the running max may lag
-constexpr int kMergeBtStage = 2048;
-constexpr int kMergeThreads = 512;  // block-table entries staged in shared memory (32768 slots)
+constexpr float kLazy = 4.0f;        // log2 units the running max may lag
+constexpr int kMergeBtStage = 2048;  // block-table entries staged in shared memory (32768 slots)
+constexpr int kMergeThreads = 512;
 
 template <int BITS>
 struct Geom {
@@ -56,19 +58,12 @@ struct Geom {
   static constexpr int kKBytes = BITS == 8 ? 2048 : 1024;
   static constexpr int kVBytes = BITS == 8 ? 2048 : 1024;
   static constexpr int kStage = kKBytes + kVBytes + 128;  // + 16 K scales + 16 V scales
-  static constexpr int kKChunks = BITS == 8 ? 4 : 2;    // 16-byte K chunks per lane per page
   static constexpr int kStages = BITS == 8 ? 3 : 4;
   static constexpr int kSmem = kWarps * kStages * kStage;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(src));
-}
-__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(smem_u32(dst)), "l"(src));
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
 __device__ __forceinline__ void cp_async16_s(uint32_t dst, const void* src) {
@@ -119,11 +114,6 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
   return d;
 }
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -151,7 +141,6 @@ __device__ __forceinline__ uint32_t i4_hi_to_h2(uint32_t v) {
   return hfma2((v & 0x00F000F0u) ^ 0x64806480u, 0x2C002C00u /* 1/16 */, 0xD480D480u /* -72 */);
 }
 
-__device__ __forceinline__ float bf16f(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 
 // 2^e as a float, for -126 <= e <= 127 (exact).
 __device__ __forceinline__ float pow2i(int e) { return __int_as_float((e + 127) << 23); }
@@ -159,34 +148,6 @@ __device__ __forceinline__ float pow2i(int e) { return __int_as_float((e + 127) 
 // Unbiased exponent of a positive normal float (floor(log2 x)).
 __device__ __forceinline__ int exponent_of(float x) {
   return (int)((__float_as_uint(x) >> 23) & 0xFF) - 127;
-}
-
-// Pages per sequence of the slice, as an exclusive prefix in shared memory:
-// cum[i] = pages of local sequences 0..i-1 (each KV head of a sequence has the
-// same pages).  Warp 0 computes it; every thread returns after the barrier.
-__device__ __forceinline__ void pages_prefix(const DevState& s, int seq_begin, int batch, int* cum) {
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    int carry = 0;
-    if (lane == 0) cum[0] = 0;
-    for (int base = 0; base < batch; base += 32) {
-      const int i = base + lane;
-      int v = i < batch ? (s.seq_slots[seq_begin + i] + kPage - 1) / kPage : 0;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += y;
-      }
-      if (i < batch) cum[i + 1] = carry + v;
-      carry += __shfl_sync(0xffffffffu, v, 31);
-    }
-  }
-  __syncthreads();
-}
-
-// CTA of the stream-K split that holds flattened page F (see AttnWork).
-__device__ __forceinline__ int cta_of_page(long long F, long long T, int N) {
-  return (int)(((F + 1) * (long long)N - 1) / T);
 }
 
 template <int BITS>
@@ -199,6 +160,13 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
   constexpr int RB = Gm::kRowBytes;
   __shared__ int cum[kMaxCallBatch + 1];
   pages_prefix(s, seq_begin, batch, cum);
+  if (blockIdx.x == 0) {
+    // the page prefix and zeroed tickets for the kernel that follows the split
+    for (int i = threadIdx.x; i <= batch; i += blockDim.x) {
+      w.cum[i] = cum[i];
+      if (i < batch) w.seq_ticket[i] = 0;
+    }
+  }
 
   const int G = s.group;
   const int hkv = s.hkv;
@@ -548,100 +516,24 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
 // write the bf16 outputs of its G query heads; with H2O on, add this step's
 // probabilities to the sink scores and to every pool slot's score.
 __global__ void __launch_bounds__(kMergeThreads, 2) attn_merge_kernel(DevState s, int seq_begin, int batch,
-                                                             const uint16_t* __restrict__ q,
-                                                             uint16_t* __restrict__ out, float qk_scale_log2,
-                                                             AttnWork w, int accumulate) {
+                                                                     const uint16_t* __restrict__ q,
+                                                                     uint16_t* __restrict__ out,
+                                                                     float qk_scale_log2, AttnWork w, int accumulate) {
   __shared__ int cum[kMaxCallBatch + 1];
-  __shared__ float sh_sl[kMaxGroup][kSinks];
-  __shared__ float sh_M[kMaxGroup], sh_invL[kMaxGroup];
+  __shared__ MergeShared ms;
+  __shared__ int32_t sh_bt[kMergeBtStage];
   pages_prefix(s, seq_begin, batch, cum);
   const int h = blockIdx.x;
   const int bl = blockIdx.y;
+  merge_phase(s, seq_begin, batch, cum, h, bl, q, out, qk_scale_log2, w, accumulate != 0, ms);
+  if (!accumulate) return;
+  // score pass: the sequence's block-table row is staged in shared memory
+  // (when it fits) and each thread handles 4 slots with all loads issued first
   const int b = seq_begin + bl;
   const int G = s.group;
   const int hkv = s.hkv;
   const int S = s.seq_slots[b];
-  const int P = s.seq_pos[b];
-  const int ns = min(P, kSinks);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int pair = bl * hkv + h;
-  const int npg = cum[bl + 1] - cum[bl];
-  int i_first = 0, i_last = -1;
-  if (npg > 0) {
-    const long long T = (long long)hkv * cum[batch];
-    const long long Pf = (long long)hkv * cum[bl] + (long long)h * npg;
-    i_first = cta_of_page(Pf, T, w.ncta);
-    i_last = cta_of_page(Pf + npg - 1, T, w.ncta);
-  }
-  const uint16_t* sk = s.sink_k + ((size_t)b * hkv + h) * kSinks * kHeadDim;
-  const uint16_t* sv = s.sink_v + ((size_t)b * hkv + h) * kSinks * kHeadDim;
-
-  // sink logits: warp task (g, j) = (task / 4, task % 4)
-  for (int task = warp; task < kMaxGroup * kSinks; task += kMergeThreads / 32) {
-    const int g = task >> 2, j = task & 3;
-    if (g < G) {
-      float part = 0.0f;
-      if (j < ns) {
-        const uint16_t* qr = q + ((size_t)bl * s.hq + h * G + g) * kHeadDim;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) part += bf16f(qr[lane * 4 + e]) * bf16f(sk[j * kHeadDim + lane * 4 + e]);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-      if (lane == 0) sh_sl[g][j] = j < ns ? part * qk_scale_log2 : -INFINITY;
-    }
-  }
-  __syncthreads();
-  // global max and sum per query head: warp g
-  if (warp < G) {
-    const int g = warp;
-    float M = kNegBig;
-    for (int i = i_first + lane; i <= i_last; i += 32) M = fmaxf(M, w.part_ml[(((size_t)pair + i) * G + g) * 2]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-#pragma unroll
-    for (int j = 0; j < kSinks; ++j) M = fmaxf(M, sh_sl[g][j]);
-    float L = 0.0f;
-    for (int i = i_first + lane; i <= i_last; i += 32) {
-      const size_t pi = ((size_t)pair + i) * G + g;
-      L += fast_exp2(w.part_ml[pi * 2] - M) * w.part_ml[pi * 2 + 1];
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-    if (lane == 0) {
-#pragma unroll
-      for (int j = 0; j < kSinks; ++j)
-        if (j < ns) L += fast_exp2(sh_sl[g][j] - M);
-      sh_M[g] = M;
-      sh_invL[g] = L > 0.0f ? 1.0f / L : 0.0f;
-      w.stats[((size_t)bl * s.hq + h * G + g) * 2 + 0] = M;
-      w.stats[((size_t)bl * s.hq + h * G + g) * 2 + 1] = L;
-    }
-  }
-  __syncthreads();
-  // outputs: thread (g, d)
-  for (int gd = threadIdx.x; gd < G * kHeadDim; gd += kMergeThreads) {
-    const int g = gd >> 7, d = gd & (kHeadDim - 1);
-    const float M = sh_M[g];
-    float o = 0.0f;
-#pragma unroll
-    for (int j = 0; j < kSinks; ++j)
-      if (j < ns) o += fast_exp2(sh_sl[g][j] - M) * bf16f(sv[j * kHeadDim + d]);
-    for (int i = i_first; i <= i_last; ++i) {
-      const size_t pi = ((size_t)pair + i) * G + g;
-      o += fast_exp2(w.part_ml[pi * 2] - M) * w.part_o[pi * kHeadDim + d];
-    }
-    out[((size_t)bl * s.hq + h * G + g) * kHeadDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(o * sh_invL[g]));
-  }
-  if (!accumulate) return;
-  if ((int)threadIdx.x < ns) {
-    float inc = 0.0f;
-    for (int g = 0; g < G; ++g) inc += fast_exp2(sh_sl[g][threadIdx.x] - sh_M[g]) * sh_invL[g];
-    s.sink_score[((size_t)b * hkv + h) * kSinks + threadIdx.x] += inc;
-  }
-  // score pass: the sequence's block-table row is staged in shared memory
-  // (when it fits) and each thread handles 4 slots with all loads issued first
-  __shared__ int32_t sh_bt[kMergeBtStage];
   const int32_t* bt = s.block_table + (size_t)b * s.max_bps;
   const int npages = (S + kPage - 1) / kPage;
   const int32_t* btp = bt;
@@ -659,16 +551,7 @@ __global__ void __launch_bounds__(kMergeThreads, 2) attn_merge_kernel(DevState s
     for (int u = 0; u < 4; ++u) {
       const int t = t0 + u * nt;
       blk[u] = t < S ? btp[t / kPage] : -1;
-      inc[u] = 0.0f;
-    }
-    for (int g = 0; g < G; ++g) {
-      const float* lrow = lgr + (size_t)g * w.s_cap;
-      const float M = sh_M[g], iL = sh_invL[g];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int t = t0 + u * nt;
-        if (t < S) inc[u] += fast_exp2(lrow[t] - M) * iL;
-      }
+      inc[u] = t < S ? h2o_increment(lgr, w.s_cap, t, G, ms) : 0.0f;
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {

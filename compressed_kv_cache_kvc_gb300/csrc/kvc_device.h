@@ -1,0 +1,250 @@
+// Device helpers shared by the kernels of the compressed-KV library: the
+// exp2 and bf16 primitives, the page prefix of a batch slice and the stream-K
+// CTA lookup of the split attention, block scans and the radix select of the
+// kept-set selection, and the merge of the split-K partials with the sinks.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "kvc_internal.h"
+
+namespace kvc {
+namespace dev {
+
+constexpr float kNegBig = -1.0e30f;
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float bf16f(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+
+// Pages per sequence of the slice, as an exclusive prefix in shared memory:
+// cum[i] = pages of local sequences 0..i-1 (each KV head of a sequence has the
+// same pages).  Warp 0 computes it; every thread returns after the barrier.
+__device__ __forceinline__ void pages_prefix(const DevState& s, int seq_begin, int batch, int* cum) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int carry = 0;
+    if (lane == 0) cum[0] = 0;
+    for (int base = 0; base < batch; base += 32) {
+      const int i = base + lane;
+      int v = i < batch ? (s.seq_slots[seq_begin + i] + kPage - 1) / kPage : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+      }
+      if (i < batch) cum[i + 1] = carry + v;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+  }
+  __syncthreads();
+}
+
+// CTA of the stream-K split that holds flattened page F (see AttnWork).
+__device__ __forceinline__ int cta_of_page(long long F, long long T, int N) {
+  return (int)(((F + 1) * (long long)N - 1) / T);
+}
+
+// Block-wide inclusive sum of one int per thread; returns the thread's
+// inclusive prefix and writes the block total to *total.  All threads call it.
+template <int NT>
+__device__ int block_scan(int v, int* sh_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sh_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < NT / 32 ? sh_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < NT / 32) sh_warp[lane] = w;  // inclusive warp prefix
+  }
+  __syncthreads();
+  const int before = warp > 0 ? sh_warp[warp - 1] : 0;
+  *total = sh_warp[NT / 32 - 1];
+  __syncthreads();
+  return before + x;
+}
+
+// Radix select over `n` entries: among the entries with active(i) true, find
+// the `want`-th in the requested order (largest-first when `descending`) of
+// value(i); returns the value and, in *remaining, how many entries equal to it
+// are still wanted (1 <= *remaining).  MSB-first, 8-bit digits, shared-memory
+// histograms, warp 0 scans the 256 bins.
+template <typename ActiveF, typename ValueF>
+__device__ uint32_t radix_select(int n, int want, bool descending, ActiveF active, ValueF value, int* hist,
+                                 int* sh_sel, int* remaining) {
+  uint32_t prefix = 0, pmask = 0;
+  int rem = want;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      if (!active(i)) continue;
+      const uint32_t v = value(i);
+      if ((v & pmask) == prefix) atomicAdd(&hist[(v >> shift) & 0xFF], 1);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      int cnt[8];
+      int sum = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int bin = descending ? 255 - (lane * 8 + k) : lane * 8 + k;
+        cnt[k] = hist[bin];
+        sum += cnt[k];
+      }
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int excl = incl - sum;
+      if (excl < rem && incl >= rem) {
+        int run = excl;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (run + cnt[k] >= rem) {
+            const int bin = descending ? 255 - (lane * 8 + k) : lane * 8 + k;
+            sh_sel[0] = bin;
+            sh_sel[1] = rem - run;
+            break;
+          }
+          run += cnt[k];
+        }
+      }
+    }
+    __syncthreads();
+    prefix |= (uint32_t)sh_sel[0] << shift;
+    pmask |= 0xFFu << shift;
+    rem = sh_sel[1];
+    __syncthreads();
+  }
+  *remaining = rem;
+  return prefix;
+}
+
+// Shared state of the merge phase.
+struct MergeShared {
+  float sl[kMaxGroup][kSinks];  // sink logits (log2 domain)
+  float M[kMaxGroup];           // global max per query head
+  float invL[kMaxGroup];        // 1 / global sum per query head
+};
+
+// Merge, for one (sequence bl, KV head h), the stream-K partials of its pages
+// and its bf16 sinks: global (M, L) per query head of the group, bf16 output
+// o = (sum of rescaled partials + sinks) / L, and, with `accumulate`, the sink
+// scores' H2O increments.  `cum` is the page prefix of the slice.  Any block
+// size that is a multiple of 32; ends after a barrier with ms filled.
+__device__ __forceinline__ void merge_phase(const DevState& s, int seq_begin, int batch, const int* cum, int h,
+                                            int bl, const uint16_t* __restrict__ q, uint16_t* __restrict__ out,
+                                            float qk_scale_log2, const AttnWork& w, bool accumulate,
+                                            MergeShared& ms) {
+  const int b = seq_begin + bl;
+  const int G = s.group;
+  const int hkv = s.hkv;
+  const int P = s.seq_pos[b];
+  const int ns = min(P, kSinks);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int pair = bl * hkv + h;
+  const int npg = cum[bl + 1] - cum[bl];
+  int i_first = 0, i_last = -1;
+  if (npg > 0) {
+    const long long T = (long long)hkv * cum[batch];
+    const long long Pf = (long long)hkv * cum[bl] + (long long)h * npg;
+    i_first = cta_of_page(Pf, T, w.ncta);
+    i_last = cta_of_page(Pf + npg - 1, T, w.ncta);
+  }
+  const uint16_t* sk = s.sink_k + ((size_t)b * hkv + h) * kSinks * kHeadDim;
+  const uint16_t* sv = s.sink_v + ((size_t)b * hkv + h) * kSinks * kHeadDim;
+
+  // sink logits: warp task (g, j) = (task / 4, task % 4)
+  for (int task = warp; task < kMaxGroup * kSinks; task += nwarps) {
+    const int g = task >> 2, j = task & 3;
+    if (g < G) {
+      float part = 0.0f;
+      if (j < ns) {
+        const uint16_t* qr = q + ((size_t)bl * s.hq + h * G + g) * kHeadDim;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) part += bf16f(qr[lane * 4 + e]) * bf16f(sk[j * kHeadDim + lane * 4 + e]);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+      if (lane == 0) ms.sl[g][j] = j < ns ? part * qk_scale_log2 : -INFINITY;
+    }
+  }
+  __syncthreads();
+  // global max and sum per query head: warp g
+  if (warp < G) {
+    const int g = warp;
+    float M = kNegBig;
+    for (int i = i_first + lane; i <= i_last; i += 32) M = fmaxf(M, w.part_ml[(((size_t)pair + i) * G + g) * 2]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+#pragma unroll
+    for (int j = 0; j < kSinks; ++j) M = fmaxf(M, ms.sl[g][j]);
+    float L = 0.0f;
+    for (int i = i_first + lane; i <= i_last; i += 32) {
+      const size_t pi = ((size_t)pair + i) * G + g;
+      L += fast_exp2(w.part_ml[pi * 2] - M) * w.part_ml[pi * 2 + 1];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    if (lane == 0) {
+#pragma unroll
+      for (int j = 0; j < kSinks; ++j)
+        if (j < ns) L += fast_exp2(ms.sl[g][j] - M);
+      ms.M[g] = M;
+      ms.invL[g] = L > 0.0f ? 1.0f / L : 0.0f;
+      w.stats[((size_t)bl * s.hq + h * G + g) * 2 + 0] = M;
+      w.stats[((size_t)bl * s.hq + h * G + g) * 2 + 1] = L;
+    }
+  }
+  __syncthreads();
+  // outputs: thread (g, d)
+  for (int gd = threadIdx.x; gd < G * kHeadDim; gd += blockDim.x) {
+    const int g = gd >> 7, d = gd & (kHeadDim - 1);
+    const float M = ms.M[g];
+    float o = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kSinks; ++j)
+      if (j < ns) o += fast_exp2(ms.sl[g][j] - M) * bf16f(sv[j * kHeadDim + d]);
+    for (int i = i_first; i <= i_last; ++i) {
+      const size_t pi = ((size_t)pair + i) * G + g;
+      o += fast_exp2(w.part_ml[pi * 2] - M) * w.part_o[pi * kHeadDim + d];
+    }
+    out[((size_t)bl * s.hq + h * G + g) * kHeadDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(o * ms.invL[g]));
+  }
+  if (accumulate && (int)threadIdx.x < ns) {
+    float inc = 0.0f;
+    for (int g = 0; g < G; ++g) inc += fast_exp2(ms.sl[g][threadIdx.x] - ms.M[g]) * ms.invL[g];
+    s.sink_score[((size_t)b * hkv + h) * kSinks + threadIdx.x] += inc;
+  }
+}
+
+// H2O increment of one pool slot: sum over the G query heads of its softmax
+// probability, from the spilled log2-domain logits ([g][slot] rows).
+__device__ __forceinline__ float h2o_increment(const float* lgr, int s_cap, int t, int G, const MergeShared& ms) {
+  float inc = 0.0f;
+  for (int g = 0; g < G; ++g) inc = __fmaf_rn(fast_exp2(lgr[(size_t)g * s_cap + t] - ms.M[g]), ms.invL[g], inc);
+  return inc;
+}
+
+}  // namespace dev
+}  // namespace kvc

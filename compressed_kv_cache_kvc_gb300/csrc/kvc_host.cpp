@@ -112,7 +112,7 @@ int s_cap(const kvc_cache* c) { return c->cfg.max_blocks_per_seq * kvc::kPage; }
 
 // Workspace carving (all regions 256-byte aligned).
 struct WsLayout {
-  size_t part_o, part_ml, logits, stats, keys, pos, total;
+  size_t part_o, part_ml, logits, stats, cum, ticket, keys, pos, total;
 };
 
 WsLayout ws_layout(const kvc_cache* c, int batch) {
@@ -130,6 +130,10 @@ WsLayout ws_layout(const kvc_cache* c, int batch) {
   o = align_up(o + pairs * cap * G * 4);
   w.stats = o;
   o = align_up(o + (size_t)batch * c->cfg.num_q_heads * 2 * 4);
+  w.cum = o;
+  o = align_up(o + ((size_t)batch + 1) * 4);
+  w.ticket = o;
+  o = align_up(o + (size_t)batch * 4);
   w.keys = o;
   o = align_up(o + pairs * cap * 4);
   w.pos = o;
@@ -151,6 +155,94 @@ int sm_count(kvc_cache* c) {
 }
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// Checks shared by kvc_decode_attention and kvc_decode_step (everything the
+// host can see before a launch).  `appended` tokens are about to be added to
+// every sequence of the slice before the attention runs.
+kvc_status attention_check(const kvc_cache* c, int32_t seq_begin, int32_t batch, const void* d_q, const void* d_out,
+                           float sm_scale, const void* d_workspace, size_t workspace_bytes, int appended) {
+  if (!range_ok(c, seq_begin, batch)) return KVC_ERR_INVALID_ARG;
+  if (!d_q || !d_out || !aligned(d_q, 16) || !aligned(d_out, 16)) return KVC_ERR_INVALID_ARG;
+  if (!(sm_scale > 0.0f) || !std::isfinite(sm_scale)) return KVC_ERR_INVALID_ARG;
+  const WsLayout wl = ws_layout(c, batch);
+  if (!d_workspace || !aligned(d_workspace, kAlign) || workspace_bytes < wl.total) return KVC_ERR_INVALID_ARG;
+  if (batch > kvc::kMaxCallBatch) return KVC_ERR_UNSUPPORTED;
+  for (int i = 0; i < batch; ++i)
+    if (c->pos[seq_begin + i] + appended <= 0) return KVC_ERR_INVALID_ARG;  // nothing to attend to
+  return KVC_OK;
+}
+
+// Stream-K grid and workspace carving of one attention call (host mirror
+// lengths as they are now).
+void attention_plan(kvc_cache* c, int32_t seq_begin, int32_t batch, void* d_workspace, kvc::AttnWork* w,
+                    long long* total_pages) {
+  const WsLayout wl = ws_layout(c, batch);
+  long long tp = 0;
+  for (int i = 0; i < batch; ++i) tp += (long long)pages_of(c->slots[seq_begin + i]) * c->cfg.num_kv_heads;
+  // one wave of resident CTAs, each with at least kMinPagesPerCta pages of the
+  // current lengths (any grid size is correct for any lengths, so a graph
+  // replayed at other lengths stays correct)
+  int ncta = 1;
+  if (tp > 0) {
+    ncta = sm_count(c) * kvc::attention_ctas_per_sm(c->cfg.bits);
+    ncta = (int)std::min<long long>(ncta, std::max<long long>(1, tp / kMinPagesPerCta));
+    ncta = std::max(1, std::min(ncta, kvc::kMaxSplitCtas));
+  }
+  uint8_t* ws = static_cast<uint8_t*>(d_workspace);
+  *w = kvc::AttnWork{};
+  w->part_o = reinterpret_cast<float*>(ws + wl.part_o);
+  w->part_ml = reinterpret_cast<float*>(ws + wl.part_ml);
+  w->logits = reinterpret_cast<float*>(ws + wl.logits);
+  w->stats = reinterpret_cast<float*>(ws + wl.stats);
+  w->cum = reinterpret_cast<int*>(ws + wl.cum);
+  w->seq_ticket = reinterpret_cast<int*>(ws + wl.ticket);
+  w->ncta = ncta;
+  w->s_cap = s_cap(c);
+  *total_pages = tp;
+}
+
+// The split-K attention launch, bracketed by the trace events when set (under
+// stream capture they become event-record nodes of the graph).
+kvc_status launch_split_traced(kvc_cache* c, int32_t seq_begin, int32_t batch, const void* d_q, float qk_scale_log2,
+                               const kvc::AttnWork& w, bool h2o, long long total_pages, cudaStream_t st,
+                               int* launches) {
+  if (total_pages <= 0) return KVC_OK;
+  const bool trace = c->trace_start && c->trace_stop;
+  unsigned rec_flags = cudaEventRecordDefault;
+  if (trace) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return KVC_ERR_CUDA;
+    if (cs == cudaStreamCaptureStatusActive) rec_flags = cudaEventRecordExternal;
+  }
+  if (trace && cudaEventRecordWithFlags(static_cast<cudaEvent_t>(c->trace_start), st, rec_flags) != cudaSuccess)
+    return KVC_ERR_CUDA;
+  if (kvc::launch_attention_split(c->dev, seq_begin, batch, static_cast<const uint16_t*>(d_q), qk_scale_log2, w, h2o,
+                                  st) != cudaSuccess)
+    return KVC_ERR_CUDA;
+  ++*launches;
+  if (trace && cudaEventRecordWithFlags(static_cast<cudaEvent_t>(c->trace_stop), st, rec_flags) != cudaSuccess)
+    return KVC_ERR_CUDA;
+  return KVC_OK;
+}
+
+// Kept slots per sequence after a selection (the host mirror's plan).
+kvc_status evict_check(const kvc_evict_params* p) {
+  if (!p) return KVC_ERR_INVALID_ARG;
+  if (p->mode == KVC_EVICT_H2O) {
+    if (p->recent < 0 || p->budget < kvc::kSinks + p->recent) return KVC_ERR_INVALID_ARG;
+  } else if (p->mode == KVC_EVICT_STREAMING) {
+    if (p->window < 1) return KVC_ERR_INVALID_ARG;
+  } else {
+    return KVC_ERR_INVALID_ARG;
+  }
+  return KVC_OK;
+}
+
+int plan_keep(const kvc_evict_params* p, int S, int P) {
+  const int ns = std::min(P, kvc::kSinks);
+  if (p->mode == KVC_EVICT_H2O) return (ns + S <= p->budget) ? S : p->budget - kvc::kSinks;
+  return (S <= p->window) ? S : p->window;
+}
 
 }  // namespace
 
@@ -324,57 +416,18 @@ kvc_status kvc_decode_attention(kvc_cache* c, int32_t seq_begin, int32_t batch, 
                                 void* stream) {
   if (!c) return KVC_ERR_INVALID_ARG;
   c->last_launches = 0;
-  if (!range_ok(c, seq_begin, batch)) return KVC_ERR_INVALID_ARG;
-  if (!d_q || !d_out || !aligned(d_q, 16) || !aligned(d_out, 16)) return KVC_ERR_INVALID_ARG;
-  if (!(sm_scale > 0.0f) || !std::isfinite(sm_scale) || (flags & ~KVC_ATTN_ACCUM_H2O)) return KVC_ERR_INVALID_ARG;
-  const WsLayout wl = ws_layout(c, batch);
-  if (!d_workspace || !aligned(d_workspace, kAlign) || workspace_bytes < wl.total) return KVC_ERR_INVALID_ARG;
-  if (batch > kvc::kMaxCallBatch) return KVC_ERR_UNSUPPORTED;
+  if (flags & ~KVC_ATTN_ACCUM_H2O) return KVC_ERR_INVALID_ARG;
+  kvc_status st0 = attention_check(c, seq_begin, batch, d_q, d_out, sm_scale, d_workspace, workspace_bytes, 0);
+  if (st0 != KVC_OK) return st0;
+  kvc::AttnWork w;
   long long total_pages = 0;
-  for (int i = 0; i < batch; ++i) {
-    const int b = seq_begin + i;
-    if (c->pos[b] <= 0) return KVC_ERR_INVALID_ARG;  // nothing to attend to
-    total_pages += (long long)pages_of(c->slots[b]) * c->cfg.num_kv_heads;
-  }
-  // stream-K grid: one wave of resident CTAs, each with at least
-  // kMinPagesPerCta pages of the current lengths (any grid size is correct
-  // for any lengths, so a graph replayed at other lengths stays correct)
-  int ncta = 1;
-  if (total_pages > 0) {
-    ncta = sm_count(c) * kvc::attention_ctas_per_sm(c->cfg.bits);
-    ncta = (int)std::min<long long>(ncta, std::max<long long>(1, total_pages / kMinPagesPerCta));
-    ncta = std::max(1, std::min(ncta, kvc::kMaxSplitCtas));
-  }
-  uint8_t* ws = static_cast<uint8_t*>(d_workspace);
-  kvc::AttnWork w{};
-  w.part_o = reinterpret_cast<float*>(ws + wl.part_o);
-  w.part_ml = reinterpret_cast<float*>(ws + wl.part_ml);
-  w.logits = reinterpret_cast<float*>(ws + wl.logits);
-  w.stats = reinterpret_cast<float*>(ws + wl.stats);
-  w.ncta = ncta;
-  w.s_cap = s_cap(c);
+  attention_plan(c, seq_begin, batch, d_workspace, &w, &total_pages);
   const float qk_scale_log2 = sm_scale * 1.4426950408889634f;
   const bool h2o = (flags & KVC_ATTN_ACCUM_H2O) != 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const bool trace = c->trace_start && c->trace_stop;
   int launches = 0;
-  // under stream capture the trace events become event-record nodes of the graph
-  unsigned rec_flags = cudaEventRecordDefault;
-  if (trace) {
-    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return KVC_ERR_CUDA;
-    if (cs == cudaStreamCaptureStatusActive) rec_flags = cudaEventRecordExternal;
-  }
-  if (total_pages > 0) {
-    if (trace && cudaEventRecordWithFlags(static_cast<cudaEvent_t>(c->trace_start), st, rec_flags) != cudaSuccess)
-      return KVC_ERR_CUDA;
-    if (kvc::launch_attention_split(c->dev, seq_begin, batch, static_cast<const uint16_t*>(d_q), qk_scale_log2, w,
-                                    h2o, st) != cudaSuccess)
-      return KVC_ERR_CUDA;
-    ++launches;
-    if (trace && cudaEventRecordWithFlags(static_cast<cudaEvent_t>(c->trace_stop), st, rec_flags) != cudaSuccess)
-      return KVC_ERR_CUDA;
-  }
+  st0 = launch_split_traced(c, seq_begin, batch, d_q, qk_scale_log2, w, h2o, total_pages, st, &launches);
+  if (st0 != KVC_OK) return st0;
   if (kvc::launch_attention_merge(c->dev, seq_begin, batch, static_cast<const uint16_t*>(d_q),
                                   static_cast<uint16_t*>(d_out), qk_scale_log2, w, h2o, st) != cudaSuccess)
     return KVC_ERR_CUDA;
@@ -388,26 +441,15 @@ kvc_status kvc_h2o_select_evict(kvc_cache* c, int32_t seq_begin, int32_t batch, 
   if (!c) return KVC_ERR_INVALID_ARG;
   c->last_launches = 0;
   if (!range_ok(c, seq_begin, batch) || !p || !d_keep_mask) return KVC_ERR_INVALID_ARG;
-  if (p->mode == KVC_EVICT_H2O) {
-    if (p->recent < 0 || p->budget < kvc::kSinks + p->recent) return KVC_ERR_INVALID_ARG;
-  } else if (p->mode == KVC_EVICT_STREAMING) {
-    if (p->window < 1) return KVC_ERR_INVALID_ARG;
-  } else {
-    return KVC_ERR_INVALID_ARG;
-  }
+  if (evict_check(p) != KVC_OK) return KVC_ERR_INVALID_ARG;
   const WsLayout wl = ws_layout(c, batch);
   if (!d_workspace || !aligned(d_workspace, kAlign) || workspace_bytes < wl.total) return KVC_ERR_INVALID_ARG;
   std::vector<int32_t> plan(batch);
   int max_s = 0;
   for (int i = 0; i < batch; ++i) {
     const int b = seq_begin + i;
-    const int S = c->slots[b], ns = std::min(c->pos[b], kvc::kSinks);
-    int keep;
-    if (p->mode == KVC_EVICT_H2O)
-      keep = (ns + S <= p->budget) ? S : p->budget - kvc::kSinks;
-    else
-      keep = (S <= p->window) ? S : p->window;
-    plan[i] = keep;
+    const int S = c->slots[b];
+    plan[i] = plan_keep(p, S, c->pos[b]);
     max_s = std::max(max_s, S);
   }
   uint8_t* ws = static_cast<uint8_t*>(d_workspace);
@@ -455,6 +497,55 @@ kvc_status kvc_compact_blocks(kvc_cache* c, int32_t seq_begin, int32_t batch, co
   c->last_launches = 1;
   for (int i = 0; i < batch; ++i) c->slots[seq_begin + i] = c->plan_new[i];
   c->plan_pending = false;
+  return KVC_OK;
+}
+
+kvc_status kvc_decode_step(kvc_cache* c, int32_t seq_begin, int32_t batch, const void* d_q, const void* d_k_new,
+                           const void* d_v_new, void* d_out, float sm_scale, const kvc_evict_params* params,
+                           void* d_workspace, size_t workspace_bytes, void* stream) {
+  if (!c) return KVC_ERR_INVALID_ARG;
+  c->last_launches = 0;
+  if (evict_check(params) != KVC_OK) return KVC_ERR_INVALID_ARG;
+  kvc_status st0 =
+      attention_check(c, seq_begin, batch, d_q, d_out, sm_scale, d_workspace, workspace_bytes, /*appended=*/1);
+  if (st0 != KVC_OK) return st0;
+  // append one token to each sequence (checks capacity before anything runs)
+  st0 = kvc_quantize_append(c, seq_begin, batch, 1, d_k_new, d_v_new, stream);
+  if (st0 != KVC_OK) return st0;
+  int launches = c->last_launches;
+  kvc::AttnWork w;
+  long long total_pages = 0;
+  attention_plan(c, seq_begin, batch, d_workspace, &w, &total_pages);
+  const float qk_scale_log2 = sm_scale * 1.4426950408889634f;
+  const bool h2o = params->mode == KVC_EVICT_H2O;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  st0 = launch_split_traced(c, seq_begin, batch, d_q, qk_scale_log2, w, h2o, total_pages, st, &launches);
+  if (st0 != KVC_OK) return st0;
+  std::vector<int32_t> plan(batch);
+  int max_s = 0;
+  for (int i = 0; i < batch; ++i) {
+    const int b = seq_begin + i;
+    plan[i] = plan_keep(params, c->slots[b], c->pos[b]);
+    max_s = std::max(max_s, c->slots[b]);
+  }
+  const WsLayout wl = ws_layout(c, batch);
+  uint8_t* ws = static_cast<uint8_t*>(d_workspace);
+  kvc::StepArgs a{};
+  a.mode = params->mode;
+  a.budget = params->budget;
+  a.recent = params->recent;
+  a.window = params->window;
+  a.s_cap = s_cap(c);
+  a.smem_slots = max_s <= kvc::step_max_smem_slots() ? std::max(max_s, 1) : 0;
+  a.g_keys = reinterpret_cast<uint32_t*>(ws + wl.keys);
+  a.g_pos = reinterpret_cast<int32_t*>(ws + wl.pos);
+  if (kvc::launch_step_post(c->dev, seq_begin, batch, static_cast<const uint16_t*>(d_q),
+                            static_cast<uint16_t*>(d_out), qk_scale_log2, w, a, st) != cudaSuccess)
+    return KVC_ERR_CUDA;
+  ++launches;
+  for (int i = 0; i < batch; ++i) c->slots[seq_begin + i] = plan[i];
+  c->plan_pending = false;
+  c->last_launches = launches;
   return KVC_OK;
 }
 

@@ -56,6 +56,8 @@ struct AttnWork {
   float* part_ml;   // [pairs + ncta][group][2]
   float* logits;    // [batch][hkv][group][s_cap]  (log2 domain)
   float* stats;     // [batch][hq][2]  global (M, L) per query head
+  int* cum;         // [batch + 1] page prefix of the slice (written by split CTA 0)
+  int* seq_ticket;  // [batch] per-sequence completion tickets (zeroed by split CTA 0)
   int ncta;         // grid size of the split kernel
   int s_cap;
 };
@@ -90,6 +92,18 @@ cudaError_t launch_select(const DevState& s, int seq_begin, int batch, const Sel
 cudaError_t launch_compact(const DevState& s, int seq_begin, int batch, const uint8_t* keep_mask,
                            int s_cap, int32_t* g_holes, int32_t* g_srcs, int smem_moves, cudaStream_t st);
 int compact_max_smem_moves();
+
+// Fused merge + H2O scores + selection + compaction (kvc_decode_step).
+struct StepArgs {
+  int mode, budget, recent, window;
+  int s_cap;            // row stride of the workspace key/position arrays
+  int smem_slots;       // > 0: keys/positions in shared memory (capacity in slots)
+  uint32_t* g_keys;     // global fallback [batch][hkv][s_cap]
+  int32_t* g_pos;
+};
+cudaError_t launch_step_post(const DevState& s, int seq_begin, int batch, const uint16_t* q, uint16_t* out,
+                             float qk_scale_log2, const AttnWork& w, const StepArgs& a, cudaStream_t st);
+int step_max_smem_slots();
 
 int attention_smem_bytes(int bits);
 int attention_ctas_per_sm(int bits);  // resident split CTAs per SM (occupancy API, cached)

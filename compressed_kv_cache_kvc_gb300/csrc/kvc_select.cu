@@ -18,110 +18,18 @@
 // filled in ascending order by the kept slots at or above n' (ascending).
 // Sources all lie at or above n' and destinations below it, so the moves never
 // overlap.  The pages past ceil(n'/16) go back to the free-block stack.
+#include "kvc_device.h"
 #include "kvc_internal.h"
 
 namespace kvc {
 namespace {
 
+using namespace dev;
+
 constexpr int kSelThreads = 1024;
 constexpr int kCompactThreads = 512;
 constexpr int kSelBtStage = 2048;  // block-table entries staged in shared memory
 
-__device__ __forceinline__ size_t slot_index(const DevState& s, const int32_t* bt, int h, int t, bool& ok) {
-  const int blk = bt[t / kPage];
-  ok = (unsigned)blk < (unsigned)s.num_blocks;
-  return ((size_t)(ok ? blk : 0) * s.hkv + h) * kPage + (t % kPage);
-}
-
-// Block-wide inclusive sum of one int per thread; returns the thread's
-// inclusive prefix and writes the block total to *total.  All threads call it.
-template <int NT>
-__device__ int block_scan(int v, int* sh_warp, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) sh_warp[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < NT / 32 ? sh_warp[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
-    }
-    if (lane < NT / 32) sh_warp[lane] = w;  // inclusive warp prefix
-  }
-  __syncthreads();
-  const int before = warp > 0 ? sh_warp[warp - 1] : 0;
-  *total = sh_warp[NT / 32 - 1];
-  __syncthreads();
-  return before + x;
-}
-
-// Radix select over `n` entries: among the entries with active(i) true, find
-// the `want`-th in the requested order (largest-first when `descending`) of
-// value(i); returns the value and, in *remaining, how many entries equal to it
-// are still wanted (1 <= *remaining).
-template <typename ActiveF, typename ValueF>
-__device__ uint32_t radix_select(int n, int want, bool descending, ActiveF active, ValueF value,
-                                 int* hist, int* sh_sel, int* remaining) {
-  uint32_t prefix = 0, pmask = 0;
-  int rem = want;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
-    __syncthreads();
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-      if (!active(i)) continue;
-      const uint32_t v = value(i);
-      if ((v & pmask) == prefix) atomicAdd(&hist[(v >> shift) & 0xFF], 1);
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      // warp 0: scan the 256 bins in the requested order, 8 bins per lane
-      const int lane = threadIdx.x;
-      int cnt[8];
-      int sum = 0;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int bin = descending ? 255 - (lane * 8 + k) : lane * 8 + k;
-        cnt[k] = hist[bin];
-        sum += cnt[k];
-      }
-      int incl = sum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const int excl = incl - sum;
-      if (excl < rem && incl >= rem) {
-        int run = excl;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          if (run + cnt[k] >= rem) {
-            const int bin = descending ? 255 - (lane * 8 + k) : lane * 8 + k;
-            sh_sel[0] = bin;
-            sh_sel[1] = rem - run;
-            break;
-          }
-          run += cnt[k];
-        }
-      }
-    }
-    __syncthreads();
-    prefix |= (uint32_t)sh_sel[0] << shift;
-    pmask |= 0xFFu << shift;
-    rem = sh_sel[1];
-    __syncthreads();
-  }
-  *remaining = rem;
-  return prefix;
-}
 
 __global__ void __launch_bounds__(kSelThreads) select_kernel(DevState s, int seq_begin, SelectArgs a,
                                                             uint8_t* __restrict__ mask) {

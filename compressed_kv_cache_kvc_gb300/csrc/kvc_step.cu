@@ -1,0 +1,306 @@
+// One kernel for everything of a decode step that follows the split-K
+// attention: merge of the partials with the sinks (bf16 outputs), H2O score
+// accumulation, kept-set selection and compaction, for one (KV head,
+// sequence) per CTA.
+//
+// It computes exactly what attn_merge_kernel + select_kernel +
+// compact_kernel compute, in the same order, but the scores, selection keys,
+// positions, keep decisions and move lists stay in shared memory between the
+// phases instead of making round trips through global memory and three
+// launches.  The page prefix of the slice comes from the split kernel, so no
+// CTA reads another sequence's length; the last of a sequence's KV-head CTAs
+// to finish (an atomic ticket: no CTA waits for another) applies its new
+// length and releases its pages.  (Technical Report: KV Cache Compression for
+// Text-Only LLMs, sections 3.3 and 3.4; "KV Cache optimization techniques"
+// sections 2.2, 2.4 and 3.2.)
+#include "kvc_device.h"
+#include "kvc_internal.h"
+
+namespace kvc {
+namespace {
+
+using namespace dev;
+
+constexpr int kStepThreads = 512;
+constexpr int kStepBtStage = 2048;
+
+__global__ void __launch_bounds__(kStepThreads, 2) step_post_kernel(DevState s, int seq_begin, int batch,
+                                                                const uint16_t* __restrict__ q,
+                                                                uint16_t* __restrict__ out, float qk_scale_log2,
+                                                                AttnWork w, StepArgs a) {
+  __shared__ MergeShared ms;
+  __shared__ int32_t sh_bt[kStepBtStage];
+  __shared__ int hist[256];
+  __shared__ int sh_sel[2];
+  __shared__ int sh_warp[32];
+  extern __shared__ __align__(16) uint32_t dyn[];
+
+  const int h = blockIdx.x;
+  const int bl = blockIdx.y;
+  const int b = seq_begin + bl;
+  const bool h2o = a.mode == 0;
+  merge_phase(s, seq_begin, batch, w.cum, h, bl, q, out, qk_scale_log2, w, h2o, ms);
+
+  const int hkv = s.hkv;
+  const int G = s.group;
+  const int S = s.seq_slots[b];
+  const int P = s.seq_pos[b];
+  const int ns = min(P, kSinks);
+  const size_t pair = (size_t)bl * hkv + h;
+  bool keep_all;
+  int n_keep, thr;
+  if (h2o) {
+    keep_all = ns + S <= a.budget;
+    n_keep = a.budget - kSinks;
+    thr = P - a.recent;
+  } else {
+    keep_all = S <= a.window;
+    n_keep = a.window;
+    thr = P - a.window;
+  }
+  if (keep_all) n_keep = S;
+  if (h == 0 && threadIdx.x == 0) {
+    s.plan[2 * b] = S;
+    s.plan[2 * b + 1] = n_keep;
+  }
+
+  uint32_t* keys;
+  int32_t* pos;
+  if (a.smem_slots > 0) {
+    keys = dyn;
+    pos = reinterpret_cast<int32_t*>(dyn + a.smem_slots);
+  } else {
+    keys = a.g_keys + pair * a.s_cap;
+    pos = a.g_pos + pair * a.s_cap;
+  }
+  const int32_t* bt = s.block_table + (size_t)b * s.max_bps;
+  const int npages = (S + kPage - 1) / kPage;
+  const int32_t* btp = bt;
+  if (npages <= kStepBtStage) {
+    for (int i = threadIdx.x; i < npages; i += blockDim.x) sh_bt[i] = bt[i];
+    btp = sh_bt;
+  }
+  __syncthreads();
+
+  // ---- scores (H2O) and selection keys.  Keys: 0xFFFFFFFF for the recent
+  // window (always kept), else the fp32 score bits (H2O) or 0 (StreamingLLM).
+  // Two slots per thread and round, every load of the round (G logits, the
+  // slot's position and score) issued before the first use.
+  const float* lgr = w.logits + pair * G * w.s_cap;
+  const int nt = blockDim.x;
+  for (int t0 = threadIdx.x; t0 < S; t0 += 2 * nt) {
+    float lg[2][kMaxGroup];
+    int p[2];
+    float sc[2];
+    size_t idx[2];
+    bool ok[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int t = t0 + u * nt;
+      const int blk = t < S ? btp[t / kPage] : 0;
+      ok[u] = t < S && (unsigned)blk < (unsigned)s.num_blocks;
+      idx[u] = ((size_t)(ok[u] ? blk : 0) * hkv + h) * kPage + (t % kPage);
+#pragma unroll
+      for (int g = 0; g < kMaxGroup; ++g) lg[u][g] = (h2o && t < S && g < G) ? lgr[(size_t)g * w.s_cap + t] : 0.0f;
+      p[u] = ok[u] ? s.slot_pos[idx[u]] : -1;
+      sc[u] = (ok[u] && h2o) ? s.score[idx[u]] : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int t = t0 + u * nt;
+      if (t >= S) continue;
+      uint32_t key = 0;
+      if (!ok[u]) {
+        atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
+      } else if (h2o) {
+        // the H2O increment: sum over the group of the slot's probability,
+        // in query-head order (as h2o_increment)
+        float inc = 0.0f;
+#pragma unroll
+        for (int g = 0; g < kMaxGroup; ++g)
+          if (g < G) inc = __fmaf_rn(fast_exp2(lg[u][g] - ms.M[g]), ms.invL[g], inc);
+        const float v = sc[u] + inc;
+        s.score[idx[u]] = v;
+        key = p[u] >= thr ? 0xFFFFFFFFu : __float_as_uint(fmaxf(v, 0.0f));
+      } else {
+        key = p[u] >= thr ? 0xFFFFFFFFu : 0u;
+      }
+      keys[t] = key;
+      pos[t] = p[u];
+    }
+  }
+  __syncthreads();
+  bool lists_ok = true;
+  if (!keep_all) {
+
+  // ---- selection: the n_keep largest keys, ties at the threshold to the
+  // lower positions
+  uint32_t theta = 0xFFFFFFFFu, pos_cut = 0xFFFFFFFFu;
+  if (n_keep > 0) {
+    int need;
+    theta = radix_select(
+        S, n_keep, true, [&](int) { return true; }, [&](int i) { return keys[i]; }, hist, sh_sel, &need);
+    int my_ties = 0;
+    for (int t = threadIdx.x; t < S; t += blockDim.x) my_ties += keys[t] == theta;
+    int ties;
+    block_scan<kStepThreads>(my_ties, sh_warp, &ties);
+    if (ties > need) {
+      int rem2;
+      pos_cut = radix_select(
+          S, need, false, [&](int i) { return keys[i] == theta; }, [&](int i) { return (uint32_t)pos[i]; },
+          hist, sh_sel, &rem2);
+    }
+  }
+  const int np = n_keep;
+
+  // ---- compaction lists.  A tile is 16 x 32 consecutive slots per warp;
+  // lane l of warp w decides slots tile0 + 512 w + 32 i + l.  Holes and
+  // sources are ranked in slot order (warp totals, then ballots), and the
+  // lists overwrite the key/position arrays: the i-th hole (or source) lies
+  // at a slot >= i, and every read of a tile precedes its writes.
+  int32_t* holes = reinterpret_cast<int32_t*>(keys);
+  int32_t* srcs = pos;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t lt = (1u << lane) - 1u;
+  int hole_base = 0, src_base = 0;
+  for (int tile0 = 0; tile0 < S; tile0 += kStepThreads * 16) {
+    const int wbase = tile0 + warp * 512 + lane;
+    uint32_t hole_bits = 0, src_bits = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int t = wbase + 32 * i;
+      if (t < S) {
+        const uint32_t k = keys[t];
+        const bool kept = n_keep > 0 && (k > theta || (k == theta && (uint32_t)pos[t] <= pos_cut));
+        if (kept && t >= np) src_bits |= 1u << i;
+        if (!kept && t < np) hole_bits |= 1u << i;
+      }
+    }
+    const uint32_t packed = __reduce_add_sync(0xffffffffu, __popc(hole_bits) | (__popc(src_bits) << 16));
+    if (lane == 0) sh_warp[warp] = (int)packed;
+    __syncthreads();
+    int before = 0, tot = 0;
+#pragma unroll
+    for (int j = 0; j < kStepThreads / 32; ++j) {
+      const int v = sh_warp[j];
+      before += j < warp ? v : 0;
+      tot += v;
+    }
+    int ph = hole_base + (before & 0xFFFF), ps = src_base + (before >> 16);
+#pragma unroll 4
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t mh = __ballot_sync(0xffffffffu, (hole_bits >> i) & 1u);
+      const uint32_t msk = __ballot_sync(0xffffffffu, (src_bits >> i) & 1u);
+      if ((mh | msk) == 0u) continue;
+      const int t = wbase + 32 * i;
+      if ((hole_bits >> i) & 1u) holes[ph + __popc(mh & lt)] = (btp[t / kPage] * hkv + h) * kPage + (t % kPage);
+      if ((src_bits >> i) & 1u) srcs[ps + __popc(msk & lt)] = (btp[t / kPage] * hkv + h) * kPage + (t % kPage);
+      ph += __popc(mh);
+      ps += __popc(msk);
+    }
+    hole_base += tot & 0xFFFF;
+    src_base += tot >> 16;
+    __syncthreads();
+  }
+  if (hole_base != src_base) {
+    if (threadIdx.x == 0) atomicOr(&s.counters[kCtrStatus], kDevBadKeepMask);
+    lists_ok = false;
+  }
+
+  // ---- moves: one thread per (source -> hole), rows as 16-byte vectors
+  const int n_moves = hole_base;
+  const uint32_t nslots = (uint32_t)s.num_blocks * hkv * kPage;
+  const int vecs = s.row_bytes / 16;
+  for (int mi = threadIdx.x; lists_ok && mi < n_moves; mi += blockDim.x) {
+    const uint32_t si = (uint32_t)srcs[mi];
+    const uint32_t di = (uint32_t)holes[mi];
+    if (si >= nslots || di >= nslots) {
+      atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
+      continue;
+    }
+    const uint4* kp = reinterpret_cast<const uint4*>(s.k_codes + (size_t)si * s.row_bytes);
+    const uint4* vp = reinterpret_cast<const uint4*>(s.v_codes + (size_t)si * s.row_bytes);
+    uint4* kd = reinterpret_cast<uint4*>(s.k_codes + (size_t)di * s.row_bytes);
+    uint4* vd = reinterpret_cast<uint4*>(s.v_codes + (size_t)di * s.row_bytes);
+    const float ks = s.k_scale[si], vs = s.v_scale[si], sc = s.score[si];
+    const int ps = s.slot_pos[si];
+    for (int h0 = 0; h0 < vecs; h0 += 4) {
+      uint4 kv[4], vv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        kv[i] = kp[h0 + i];
+        vv[i] = vp[h0 + i];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        kd[h0 + i] = kv[i];
+        vd[h0 + i] = vv[i];
+      }
+    }
+    s.k_scale[di] = ks;
+    s.v_scale[di] = vs;
+    s.slot_pos[di] = ps;
+    s.score[di] = sc;
+  }
+
+  }  // !keep_all
+
+  // ---- the last of the sequence's KV-head CTAs to finish applies its new
+  // length and releases its pages past ceil(n'/16) (every CTA of the
+  // sequence has the same S and n_keep)
+  __shared__ int sh_last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    sh_last = atomicAdd(&w.seq_ticket[bl], 1) == hkv - 1;
+  }
+  __syncthreads();
+  if (!sh_last) return;
+  __threadfence();
+  const int keep_pages = (n_keep + kPage - 1) / kPage;
+  const int nfree = npages - keep_pages;
+  if (threadIdx.x == 0) {
+    int fbase = -1;
+    if (nfree > 0) {
+      fbase = atomicAdd(&s.counters[kCtrFreeTop], nfree);
+      if (fbase + nfree > s.num_blocks) {
+        atomicSub(&s.counters[kCtrFreeTop], nfree);
+        atomicOr(&s.counters[kCtrStatus], kDevStackOverflow);
+        fbase = -1;
+      }
+    }
+    sh_sel[0] = fbase;
+    if (n_keep < S) s.seq_slots[b] = n_keep;
+    w.seq_ticket[bl] = 0;
+  }
+  __syncthreads();
+  const int fbase = sh_sel[0];
+  if (fbase >= 0)
+    for (int j = threadIdx.x; j < nfree; j += blockDim.x) s.free_stack[fbase + j] = btp[keep_pages + j];
+}
+
+}  // namespace
+
+int step_max_smem_slots() { return (160 * 1024) / 8; }
+
+cudaError_t launch_step_post(const DevState& s, int seq_begin, int batch, const uint16_t* q, uint16_t* out,
+                             float qk_scale_log2, const AttnWork& w, const StepArgs& a, cudaStream_t st) {
+  const int smem = a.smem_slots > 0 ? a.smem_slots * 8 : 0;
+  if (smem > 48 * 1024) {
+    static int done[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 64 || !done[dev]) {
+      e = cudaFuncSetAttribute(step_post_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               step_max_smem_slots() * 8);
+      if (e != cudaSuccess) return e;
+      if (dev < 64) done[dev] = 1;
+    }
+  }
+  dim3 grid(s.hkv, batch);
+  step_post_kernel<<<grid, kStepThreads, smem, st>>>(s, seq_begin, batch, q, out, qk_scale_log2, w, a);
+  return cudaGetLastError();
+}
+
+}  // namespace kvc

@@ -239,6 +239,22 @@ kvc_status kvc_decode_attention_noalloc(kvc_cache* cache, int32_t seq_begin, int
                                         const void* d_q, void* d_out, float sm_scale, int32_t flags,
                                         void* stream);
 
+/* One whole decode step of a layer in one call: append one token per
+ * sequence (as kvc_quantize_append with n_new = 1), then decode attention
+ * (H2O accumulation on in H2O mode, off in StreamingLLM mode), selection and
+ * compaction with `params`, exactly as the four calls above compute them.
+ * After the split-K attention, the merge, the score update, the selection and
+ * the compaction of each (sequence, KV head) run in one kernel that keeps the
+ * scores, keys and move lists on chip; three launches in all.
+ *   d_q: bf16 [batch][Hq][128]; d_k_new, d_v_new: bf16 [batch][Hkv][1][128];
+ *   d_out: bf16 [batch][Hq][128]; workspace as for kvc_decode_attention.
+ * Host-visible errors (arguments, capacity) are returned before anything is
+ * enqueued.  No keep mask is written. */
+kvc_status kvc_decode_step(kvc_cache* cache, int32_t seq_begin, int32_t batch, const void* d_q,
+                           const void* d_k_new, const void* d_v_new, void* d_out, float sm_scale,
+                           const kvc_evict_params* params, void* d_workspace, size_t workspace_bytes,
+                           void* stream);
+
 /* ---------------------------------------------------------------- misc ---- */
 
 /* Synchronise `stream`, copy the device status word to *h_status and clear

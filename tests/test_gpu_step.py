@@ -1,0 +1,109 @@
+"""kvc_decode_step (one call per layer, fused merge/select/compaction) must
+leave exactly the device state and outputs that the four separate calls leave,
+step after step; plus one direct check against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import kvc_oracle as O
+from tests import kvc_testlib as T
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from compressed_kv_cache_kvc_gb300.build import build_library
+    build_library()
+
+
+def _bits(rng, shape):
+    from compressed_kv_cache_kvc_gb300.workloads import bf16_bits
+    return bf16_bits(rng.standard_normal(shape).astype(np.float32))
+
+
+def _same_state(a, b):
+    """Same logical cache: per (sequence, KV head) the slots in slot order
+    (positions, codes, scales, scores), the sinks and their scores, the
+    lengths and the number of free blocks.  Physical block ids may differ:
+    the two paths push released blocks in different orders."""
+    sa, sb = T.StateView(a), T.StateView(b)
+    assert np.array_equal(sa.slots, sb.slots) and np.array_equal(sa.seen, sb.seen)
+    for seq in range(a.max_batch):
+        for h in range(a.num_kv_heads):
+            for x, y in zip(sa.head(seq, h), sb.head(seq, h)):
+                assert np.array_equal(np.asarray(x).view(np.uint8), np.asarray(y).view(np.uint8)), (seq, h)
+    assert np.array_equal(sa.sink_k, sb.sink_k) and np.array_equal(sa.sink_v, sb.sink_v)
+    assert np.array_equal(sa.sink_score.view(np.uint32), sb.sink_score.view(np.uint32))
+    assert np.array_equal(sa.counters[:3], sb.counters[:3])  # free-stack top, status, ticket
+
+
+CASES = [
+    # bits, hq, hkv, lengths, mode, budget, recent, window, steps
+    (8, 8, 8, [512], "h2o", 128, 32, 0, 4),
+    (4, 40, 8, [600, 433, 70], "h2o", 180, 40, 0, 3),
+    (8, 32, 8, [700, 100, 257, 260], "streaming", 0, 0, 256, 3),
+    (8, 8, 2, [150], "h2o", 4 + 160, 8, 0, 2),        # budget covers the context: nothing evicted
+    (4, 4, 2, [90], "h2o", 4, 0, 0, 2),               # only the sinks are kept
+    (8, 16, 4, [1000, 1000], "h2o", 300, 64, 0, 2),
+]
+
+
+@pytest.mark.parametrize("bits,hq,hkv,lengths,mode,budget,recent,window,steps", CASES)
+def test_step_equals_separate_calls(bits, hq, hkv, lengths, mode, budget, recent, window, steps):
+    from compressed_kv_cache_kvc_gb300.cache import KVCache
+    rng = np.random.default_rng(bits * 7 + hq + len(lengths))
+    B, T_ = len(lengths), max(lengths)
+    mbps = (T_ + steps + 15) // 16 + 2
+    order = np.random.default_rng(1).permutation(B * mbps).astype(np.int32)
+    ca = KVCache(hq, hkv, bits, B * mbps, B, mbps, block_order=order)
+    cb = KVCache(hq, hkv, bits, B * mbps, B, mbps, block_order=order)
+    k = _bits(rng, (B, hkv, T_, 128))
+    v = _bits(rng, (B, hkv, T_, 128))
+    for c in (ca, cb):
+        for b, n in enumerate(lengths):
+            c.quantize_append(T.to_dev_bf16(np.ascontiguousarray(k[b:b + 1, :, :n])),
+                              T.to_dev_bf16(np.ascontiguousarray(v[b:b + 1, :, :n])), seq_begin=b)
+    _same_state(ca, cb)
+    for _ in range(steps):
+        q = T.to_dev_bf16(_bits(rng, (B, hq, 128)))
+        kn = T.to_dev_bf16(_bits(rng, (B, hkv, 1, 128)))
+        vn = T.to_dev_bf16(_bits(rng, (B, hkv, 1, 128)))
+        oa = ca.step(q, kn, vn, mode=mode, budget=budget, recent=recent, window=window)
+        ob = cb.decode_step(q, kn, vn, mode=mode, budget=budget, recent=recent, window=window)
+        assert cb.last_launch_count() == 3
+        torch.cuda.synchronize()
+        assert torch.equal(oa, ob)
+        _same_state(ca, cb)
+        for b in range(B):
+            assert ca.lengths(b) == cb.lengths(b)
+    assert ca.read_status() == 0 and cb.read_status() == 0
+
+
+def test_step_against_oracle_tiny_workload():
+    from compressed_kv_cache_kvc_gb300 import workloads as W
+    from compressed_kv_cache_kvc_gb300.cache import KVCache
+    w = W.WORKLOADS["tiny_b1_h8_t512_int8_h2o"]
+    d = W.gen_layer(w, 0)
+    mbps = (w.context + 16) // 16 + 1
+    c = KVCache(w.num_q_heads, w.num_kv_heads, w.bits, mbps, 1, mbps)
+    c.quantize_append(T.to_dev_bf16(d["k"]), T.to_dev_bf16(d["v"]))
+    out = c.decode_step(T.to_dev_bf16(d["q"]), T.to_dev_bf16(d["k_new"]), T.to_dev_bf16(d["v_new"]),
+                        mode="h2o", budget=w.budget, recent=w.recent)
+    ora = O.OracleCache(1, w.num_q_heads, w.num_kv_heads, w.bits)
+    f = O.bf16_bits_to_f32
+    ora.append(0, f(d["k"][0]), f(d["v"][0]))
+    ora.append(0, f(d["k_new"][0]), f(d["v_new"][0]))
+    ref = ora.attend(0, f(d["q"][0]), T.sm_scale())
+    T.assert_attention_close(T.bf16_tensor_to_f32(out)[0], ref, "decode_step")
+    masks = ora.keep_masks(0, "h2o", budget=w.budget, recent=w.recent)
+    st = T.StateView(c)
+    for h in range(w.num_kv_heads):
+        hs = ora.seqs[0].heads[h]
+        kept_ora = set(hs.pos[masks[h]].tolist())
+        kept_gpu = set(st.head(0, h)[0].tolist())
+        assert T.kept_sets_agree(kept_gpu, kept_ora, hs.pos, hs.score, w.budget - 4 - w.recent,
+                                 w.context + 1 - w.recent)
+    assert c.lengths(0) == (w.budget - 4, w.context + 1)
