@@ -566,14 +566,7 @@ __global__ void __launch_bounds__(kMergeThreads, 2) attn_merge_kernel(DevState s
 template <int BITS>
 cudaError_t ensure_split_smem() {
   static int done[64] = {0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 64 && done[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(attn_split_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Geom<BITS>::kSmem);
-  if (e == cudaSuccess && dev < 64) done[dev] = 1;
-  return e;
+  return opt_in_smem(reinterpret_cast<const void*>(attn_split_kernel<BITS>), Geom<BITS>::kSmem, done);
 }
 
 template <int BITS>

@@ -81,57 +81,64 @@ __device__ int block_scan(int v, int* sh_warp, int* total) {
 // Radix select over `n` entries: among the entries with active(i) true, find
 // the `want`-th in the requested order (largest-first when `descending`) of
 // value(i); returns the value and, in *remaining, how many entries equal to it
-// are still wanted (1 <= *remaining).  MSB-first, 8-bit digits, shared-memory
-// histograms, warp 0 scans the 256 bins.
-template <typename ActiveF, typename ValueF>
+// are still wanted (1 <= *remaining).  MSB-first in three passes of 11, 11
+// and 10 bits: wide digits spread values that share their top bits (scores
+// of one magnitude share sign and exponent) over many histogram bins, so the
+// shared-memory atomics seldom meet on one address.  `hist` holds
+// kRadixBins ints; the NT threads scan the bins, each owning nb / NT
+// consecutive ones in the requested order.
+constexpr int kRadixBins = 2048;
+
+template <int NT, typename ActiveF, typename ValueF>
 __device__ uint32_t radix_select(int n, int want, bool descending, ActiveF active, ValueF value, int* hist,
-                                 int* sh_sel, int* remaining) {
+                                 int* sh_warp, int* sh_sel, int* remaining) {
+  static_assert(NT >= 32 && NT <= 1024 && (1024 % NT) == 0, "block size");
   uint32_t prefix = 0, pmask = 0;
   int rem = want;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+#pragma unroll 1
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+    const int nb = pass == 2 ? 1024 : kRadixBins;
+    for (int i = threadIdx.x; i < nb; i += NT) hist[i] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    for (int i = threadIdx.x; i < n; i += NT) {
       if (!active(i)) continue;
       const uint32_t v = value(i);
-      if ((v & pmask) == prefix) atomicAdd(&hist[(v >> shift) & 0xFF], 1);
+      if ((v & pmask) == prefix) atomicAdd(&hist[(v >> shift) & (nb - 1)], 1);
     }
     __syncthreads();
-    if (threadIdx.x < 32) {
-      const int lane = threadIdx.x;
-      int cnt[8];
-      int sum = 0;
+    constexpr int kMaxPer = kRadixBins / NT;
+    const int per = nb / NT;
+    int cnt[kMaxPer];
+    int sum = 0;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int bin = descending ? 255 - (lane * 8 + k) : lane * 8 + k;
-        cnt[k] = hist[bin];
+    for (int k = 0; k < kMaxPer; ++k) {
+      cnt[k] = 0;
+      if (k < per) {
+        const int j = (int)threadIdx.x * per + k;
+        cnt[k] = hist[descending ? nb - 1 - j : j];
         sum += cnt[k];
       }
-      int incl = sum;
+    }
+    int total;
+    const int incl = block_scan<NT>(sum, sh_warp, &total);
+    const int excl = incl - sum;
+    if (excl < rem && incl >= rem) {
+      int run = excl;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const int excl = incl - sum;
-      if (excl < rem && incl >= rem) {
-        int run = excl;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          if (run + cnt[k] >= rem) {
-            const int bin = descending ? 255 - (lane * 8 + k) : lane * 8 + k;
-            sh_sel[0] = bin;
-            sh_sel[1] = rem - run;
-            break;
-          }
-          run += cnt[k];
+      for (int k = 0; k < kMaxPer; ++k) {
+        if (k < per && run + cnt[k] >= rem) {
+          const int j = (int)threadIdx.x * per + k;
+          sh_sel[0] = descending ? nb - 1 - j : j;
+          sh_sel[1] = rem - run;
+          break;
         }
+        run += cnt[k];
       }
     }
     __syncthreads();
     prefix |= (uint32_t)sh_sel[0] << shift;
-    pmask |= 0xFFu << shift;
+    pmask |= (uint32_t)(nb - 1) << shift;
     rem = sh_sel[1];
     __syncthreads();
   }

@@ -112,7 +112,7 @@ int s_cap(const kvc_cache* c) { return c->cfg.max_blocks_per_seq * kvc::kPage; }
 
 // Workspace carving (all regions 256-byte aligned).
 struct WsLayout {
-  size_t part_o, part_ml, logits, stats, cum, ticket, keys, pos, total;
+  size_t part_o, part_ml, logits, stats, cum, ticket, moves, keys, pos, total;
 };
 
 WsLayout ws_layout(const kvc_cache* c, int batch) {
@@ -134,6 +134,8 @@ WsLayout ws_layout(const kvc_cache* c, int batch) {
   o = align_up(o + ((size_t)batch + 1) * 4);
   w.ticket = o;
   o = align_up(o + (size_t)batch * 4);
+  w.moves = o;
+  o = align_up(o + pairs * 4);
   w.keys = o;
   o = align_up(o + pairs * cap * 4);
   w.pos = o;
@@ -536,13 +538,16 @@ kvc_status kvc_decode_step(kvc_cache* c, int32_t seq_begin, int32_t batch, const
   a.recent = params->recent;
   a.window = params->window;
   a.s_cap = s_cap(c);
-  a.smem_slots = max_s <= kvc::step_max_smem_slots() ? std::max(max_s, 1) : 0;
+  const int slots4 = (max_s + 3) & ~3;  // the score pass writes whole quarter pages of keys
+  a.smem_slots = slots4 <= kvc::step_max_smem_slots() ? std::max(slots4, 4) : 0;
   a.g_keys = reinterpret_cast<uint32_t*>(ws + wl.keys);
   a.g_pos = reinterpret_cast<int32_t*>(ws + wl.pos);
+  a.n_moves = reinterpret_cast<int*>(ws + wl.moves);
   if (kvc::launch_step_post(c->dev, seq_begin, batch, static_cast<const uint16_t*>(d_q),
                             static_cast<uint16_t*>(d_out), qk_scale_log2, w, a, st) != cudaSuccess)
     return KVC_ERR_CUDA;
-  ++launches;
+  if (kvc::launch_step_moves(c->dev, batch, a, st) != cudaSuccess) return KVC_ERR_CUDA;
+  launches += 2;
   for (int i = 0; i < batch; ++i) c->slots[seq_begin + i] = plan[i];
   c->plan_pending = false;
   c->last_launches = launches;

@@ -65,6 +65,19 @@ struct AttnWork {
 constexpr int kMaxCallBatch = 1024;  // sequences per attention call (prefix table in shared memory)
 constexpr int kMaxSplitCtas = 2048;
 
+// Raise a kernel's dynamic shared-memory limit to `bytes`, once per device
+// (`done` holds one flag per device ordinal below 64).  Needed whenever the
+// kernel's static plus dynamic shared memory passes the 48 KB default.
+inline cudaError_t opt_in_smem(const void* fn, int bytes, int* done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev < 64) done[dev] = 1;
+  return e;
+}
+
 // ---- launchers (return cudaGetLastError of the launch) -------------------
 cudaError_t launch_append(const DevState& s, int seq_begin, int batch, int n_new,
                           const uint16_t* k, const uint16_t* v, cudaStream_t st);
@@ -81,8 +94,9 @@ struct SelectArgs {
   int mode, budget, recent, window;
   int s_cap;            // mask row stride
   int smem_slots;       // > 0: keys/pos staged in shared memory (capacity in slots)
-  uint32_t* g_keys;     // global fallback [batch][hkv][s_cap]
-  int32_t* g_pos;
+  uint32_t* g_keys;     // global fallback [batch][hkv][s_cap]; then the hole list
+  int32_t* g_pos;       // likewise; then the source list
+  int* n_moves;         // [batch][hkv] list lengths (post kernel -> move kernel)
 };
 cudaError_t launch_select(const DevState& s, int seq_begin, int batch, const SelectArgs& a,
                           uint8_t* keep_mask, cudaStream_t st);
@@ -98,12 +112,14 @@ struct StepArgs {
   int mode, budget, recent, window;
   int s_cap;            // row stride of the workspace key/position arrays
   int smem_slots;       // > 0: keys/positions in shared memory (capacity in slots)
-  uint32_t* g_keys;     // global fallback [batch][hkv][s_cap]
-  int32_t* g_pos;
+  uint32_t* g_keys;     // global fallback [batch][hkv][s_cap]; then the hole list
+  int32_t* g_pos;       // likewise; then the source list
+  int* n_moves;         // [batch][hkv] list lengths (post kernel -> move kernel)
 };
 cudaError_t launch_step_post(const DevState& s, int seq_begin, int batch, const uint16_t* q, uint16_t* out,
                              float qk_scale_log2, const AttnWork& w, const StepArgs& a, cudaStream_t st);
-int step_max_smem_slots();
+cudaError_t launch_step_moves(const DevState& s, int batch, const StepArgs& a, cudaStream_t st);
+int step_max_smem_slots();  // a multiple of 4
 
 int attention_smem_bytes(int bits);
 int attention_ctas_per_sm(int bits);  // resident split CTAs per SM (occupancy API, cached)

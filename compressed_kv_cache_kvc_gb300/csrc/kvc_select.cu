@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(DevState s, int seq
   }
 
   extern __shared__ __align__(16) uint32_t dyn[];
-  __shared__ int hist[256];
+  __shared__ int hist[kRadixBins];
   __shared__ int sh_sel[2];
   __shared__ int sh_warp[32];
   uint32_t* keys;
@@ -118,8 +118,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(DevState s, int seq
   __syncthreads();
 
   int need;
-  const uint32_t theta = radix_select(
-      S, n_keep, true, [&](int) { return true; }, [&](int i) { return keys[i]; }, hist, sh_sel, &need);
+  const uint32_t theta = radix_select<kSelThreads>(
+      S, n_keep, true, [&](int) { return true; }, [&](int i) { return keys[i]; }, hist, sh_warp, sh_sel, &need);
   // ties at theta: how many are there?
   int my_ties = 0;
   for (int t = threadIdx.x; t < S; t += blockDim.x) my_ties += keys[t] == theta;
@@ -128,9 +128,9 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(DevState s, int seq
   uint32_t pos_cut = 0xFFFFFFFFu;
   if (ties > need) {
     int rem2;
-    pos_cut = radix_select(
+    pos_cut = radix_select<kSelThreads>(
         S, need, false, [&](int i) { return keys[i] == theta; }, [&](int i) { return (uint32_t)pos[i]; }, hist,
-        sh_sel, &rem2);
+        sh_warp, sh_sel, &rem2);
   }
   for (int t = threadIdx.x; t < S; t += blockDim.x) {
     const uint32_t k = keys[t];
@@ -287,18 +287,10 @@ int select_max_smem_slots() { return (200 * 1024) / 8; }
 cudaError_t launch_select(const DevState& s, int seq_begin, int batch, const SelectArgs& a, uint8_t* keep_mask,
                           cudaStream_t st) {
   const int smem = a.smem_slots > 0 ? a.smem_slots * 8 : 0;
-  if (smem > 48 * 1024) {
-    // raise the kernel's dynamic shared-memory limit once per device
+  if (smem > 0) {
     static int done[64] = {0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(select_kernel), select_max_smem_slots() * 8, done);
     if (e != cudaSuccess) return e;
-    if (dev >= 64 || !done[dev]) {
-      e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               select_max_smem_slots() * 8);
-      if (e != cudaSuccess) return e;
-      if (dev < 64) done[dev] = 1;
-    }
   }
   dim3 grid(s.hkv, batch);
   select_kernel<<<grid, kSelThreads, smem, st>>>(s, seq_begin, a, keep_mask);
@@ -310,17 +302,10 @@ int compact_max_smem_moves() { return (96 * 1024) / 8; }
 cudaError_t launch_compact(const DevState& s, int seq_begin, int batch, const uint8_t* keep_mask, int s_cap,
                            int32_t* g_holes, int32_t* g_srcs, int smem_moves, cudaStream_t st) {
   const int smem = smem_moves > 0 ? smem_moves * 8 : 0;
-  if (smem > 48 * 1024) {
+  if (smem > 0) {
     static int done[64] = {0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(compact_kernel), compact_max_smem_moves() * 8, done);
     if (e != cudaSuccess) return e;
-    if (dev >= 64 || !done[dev]) {
-      e = cudaFuncSetAttribute(compact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               compact_max_smem_moves() * 8);
-      if (e != cudaSuccess) return e;
-      if (dev < 64) done[dev] = 1;
-    }
   }
   dim3 grid(s.hkv, batch);
   compact_kernel<<<grid, kCompactThreads, smem, st>>>(s, seq_begin, keep_mask, s_cap, g_holes, g_srcs, smem_moves);

@@ -1,18 +1,23 @@
-// One kernel for everything of a decode step that follows the split-K
-// attention: merge of the partials with the sinks (bf16 outputs), H2O score
-// accumulation, kept-set selection and compaction, for one (KV head,
-// sequence) per CTA.
+// The decode-step work that follows the split-K attention, in two kernels.
 //
-// It computes exactly what attn_merge_kernel + select_kernel +
-// compact_kernel compute, in the same order, but the scores, selection keys,
-// positions, keep decisions and move lists stay in shared memory between the
-// phases instead of making round trips through global memory and three
-// launches.  The page prefix of the slice comes from the split kernel, so no
-// CTA reads another sequence's length; the last of a sequence's KV-head CTAs
-// to finish (an atomic ticket: no CTA waits for another) applies its new
-// length and releases its pages.  (Technical Report: KV Cache Compression for
-// Text-Only LLMs, sections 3.3 and 3.4; "KV Cache optimization techniques"
-// sections 2.2, 2.4 and 3.2.)
+// step_post_kernel, one CTA per (KV head, sequence): merge of the partials
+// with the sinks (bf16 outputs), H2O score accumulation, kept-set selection
+// and the compaction move lists.  It computes exactly what attn_merge_kernel
+// + select_kernel + the list phase of compact_kernel compute, in the same
+// order, but the scores, keys, positions and keep decisions stay in shared
+// memory between the phases.  The page prefix of the slice comes from the
+// split kernel, so no CTA reads another sequence's length; the last of a
+// sequence's KV-head CTAs to finish (an atomic ticket: no CTA waits for
+// another) applies its new length and releases its pages.  Released pages
+// are only taken by later calls, after step_moves_kernel has read them.
+//
+// step_moves_kernel, one CTA per (KV head, sequence): the row moves of the
+// lists.  Moves run in a launch of their own because, sharing an SM with
+// another CTA's selection phase, their global-memory traffic stalls that
+// phase's shared-memory work.
+//
+// (Technical Report: KV Cache Compression for Text-Only LLMs, sections 3.3
+// and 3.4; "KV Cache optimization techniques" sections 2.2, 2.4 and 3.2.)
 #include "kvc_device.h"
 #include "kvc_internal.h"
 
@@ -30,7 +35,7 @@ __global__ void __launch_bounds__(kStepThreads, 2) step_post_kernel(DevState s, 
                                                                 AttnWork w, StepArgs a) {
   __shared__ MergeShared ms;
   __shared__ int32_t sh_bt[kStepBtStage];
-  __shared__ int hist[256];
+  __shared__ int hist[kRadixBins];
   __shared__ int sh_sel[2];
   __shared__ int sh_warp[32];
   extern __shared__ __align__(16) uint32_t dyn[];
@@ -84,50 +89,62 @@ __global__ void __launch_bounds__(kStepThreads, 2) step_post_kernel(DevState s, 
 
   // ---- scores (H2O) and selection keys.  Keys: 0xFFFFFFFF for the recent
   // window (always kept), else the fp32 score bits (H2O) or 0 (StreamingLLM).
-  // Two slots per thread and round, every load of the round (G logits, the
-  // slot's position and score) issued before the first use.
+  // Four consecutive slots (a quarter page) per thread and round, moved as
+  // 16-byte vectors; every load of a round (G logit vectors, the positions
+  // and scores) is issued before the first use.
   const float* lgr = w.logits + pair * G * w.s_cap;
-  const int nt = blockDim.x;
-  for (int t0 = threadIdx.x; t0 < S; t0 += 2 * nt) {
-    float lg[2][kMaxGroup];
-    int p[2];
-    float sc[2];
-    size_t idx[2];
-    bool ok[2];
+  const int nq = (S + 3) >> 2;
+  for (int j = threadIdx.x; j < nq; j += blockDim.x) {
+    const int t = 4 * j;
+    const int blk = btp[t / kPage];
+    const bool ok = (unsigned)blk < (unsigned)s.num_blocks;
+    const size_t idx = ((size_t)(ok ? blk : 0) * hkv + h) * kPage + (t % kPage);
+    float4 lg[kMaxGroup];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int t = t0 + u * nt;
-      const int blk = t < S ? btp[t / kPage] : 0;
-      ok[u] = t < S && (unsigned)blk < (unsigned)s.num_blocks;
-      idx[u] = ((size_t)(ok[u] ? blk : 0) * hkv + h) * kPage + (t % kPage);
-#pragma unroll
-      for (int g = 0; g < kMaxGroup; ++g) lg[u][g] = (h2o && t < S && g < G) ? lgr[(size_t)g * w.s_cap + t] : 0.0f;
-      p[u] = ok[u] ? s.slot_pos[idx[u]] : -1;
-      sc[u] = (ok[u] && h2o) ? s.score[idx[u]] : 0.0f;
+    for (int g = 0; g < kMaxGroup; ++g)
+      lg[g] = (h2o && g < G) ? *reinterpret_cast<const float4*>(lgr + (size_t)g * w.s_cap + t)
+                             : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    int4 p4 = make_int4(-1, -1, -1, -1);
+    float4 sc4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (ok) {
+      p4 = *reinterpret_cast<const int4*>(s.slot_pos + idx);
+      if (h2o) sc4 = *reinterpret_cast<const float4*>(s.score + idx);
+    } else {
+      atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
     }
+    const int pp[4] = {p4.x, p4.y, p4.z, p4.w};
+    float vv[4] = {sc4.x, sc4.y, sc4.z, sc4.w};
+    uint32_t kk[4];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int t = t0 + u * nt;
-      if (t >= S) continue;
-      uint32_t key = 0;
-      if (!ok[u]) {
-        atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
-      } else if (h2o) {
+    for (int c = 0; c < 4; ++c) {
+      if (h2o) {
         // the H2O increment: sum over the group of the slot's probability,
         // in query-head order (as h2o_increment)
         float inc = 0.0f;
 #pragma unroll
-        for (int g = 0; g < kMaxGroup; ++g)
-          if (g < G) inc = __fmaf_rn(fast_exp2(lg[u][g] - ms.M[g]), ms.invL[g], inc);
-        const float v = sc[u] + inc;
-        s.score[idx[u]] = v;
-        key = p[u] >= thr ? 0xFFFFFFFFu : __float_as_uint(fmaxf(v, 0.0f));
+        for (int g = 0; g < kMaxGroup; ++g) {
+          const float l = c == 0 ? lg[g].x : c == 1 ? lg[g].y : c == 2 ? lg[g].z : lg[g].w;
+          if (g < G) inc = __fmaf_rn(fast_exp2(l - ms.M[g]), ms.invL[g], inc);
+        }
+        vv[c] += inc;
+        kk[c] = pp[c] >= thr ? 0xFFFFFFFFu : __float_as_uint(fmaxf(vv[c], 0.0f));
       } else {
-        key = p[u] >= thr ? 0xFFFFFFFFu : 0u;
+        kk[c] = pp[c] >= thr ? 0xFFFFFFFFu : 0u;
       }
-      keys[t] = key;
-      pos[t] = p[u];
+      if (!ok) kk[c] = 0u;
     }
+    if (ok && h2o) {
+      if (t + 4 <= S) {
+        *reinterpret_cast<float4*>(s.score + idx) = make_float4(vv[0], vv[1], vv[2], vv[3]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if (t + c < S) s.score[idx + c] = vv[c];
+      }
+    }
+    // slots past S in the last quarter page get keys too: nothing reads them
+    *reinterpret_cast<uint4*>(keys + t) = make_uint4(kk[0], kk[1], kk[2], kk[3]);
+    *reinterpret_cast<int4*>(pos + t) = p4;
   }
   __syncthreads();
   bool lists_ok = true;
@@ -138,28 +155,30 @@ __global__ void __launch_bounds__(kStepThreads, 2) step_post_kernel(DevState s, 
   uint32_t theta = 0xFFFFFFFFu, pos_cut = 0xFFFFFFFFu;
   if (n_keep > 0) {
     int need;
-    theta = radix_select(
-        S, n_keep, true, [&](int) { return true; }, [&](int i) { return keys[i]; }, hist, sh_sel, &need);
+    theta = radix_select<kStepThreads>(
+        S, n_keep, true, [&](int) { return true; }, [&](int i) { return keys[i]; }, hist, sh_warp, sh_sel, &need);
     int my_ties = 0;
     for (int t = threadIdx.x; t < S; t += blockDim.x) my_ties += keys[t] == theta;
     int ties;
     block_scan<kStepThreads>(my_ties, sh_warp, &ties);
     if (ties > need) {
       int rem2;
-      pos_cut = radix_select(
+      pos_cut = radix_select<kStepThreads>(
           S, need, false, [&](int i) { return keys[i] == theta; }, [&](int i) { return (uint32_t)pos[i]; },
-          hist, sh_sel, &rem2);
+          hist, sh_warp, sh_sel, &rem2);
     }
   }
   const int np = n_keep;
 
   // ---- compaction lists.  A tile is 16 x 32 consecutive slots per warp;
   // lane l of warp w decides slots tile0 + 512 w + 32 i + l.  Holes and
-  // sources are ranked in slot order (warp totals, then ballots), and the
-  // lists overwrite the key/position arrays: the i-th hole (or source) lies
-  // at a slot >= i, and every read of a tile precedes its writes.
-  int32_t* holes = reinterpret_cast<int32_t*>(keys);
-  int32_t* srcs = pos;
+  // sources are ranked in slot order (warp totals, then ballots) and go to
+  // the pair's rows of the workspace key/position arrays.  Where the keys
+  // and positions themselves live there, the lists overwrite them in place:
+  // the i-th hole (or source) lies at a slot >= i, and every read of a tile
+  // precedes its writes.
+  int32_t* holes = reinterpret_cast<int32_t*>(a.g_keys + pair * a.s_cap);
+  int32_t* srcs = a.g_pos + pair * a.s_cap;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t lt = (1u << lane) - 1u;
   int hole_base = 0, src_base = 0;
@@ -207,43 +226,11 @@ __global__ void __launch_bounds__(kStepThreads, 2) step_post_kernel(DevState s, 
     lists_ok = false;
   }
 
-  // ---- moves: one thread per (source -> hole), rows as 16-byte vectors
-  const int n_moves = hole_base;
-  const uint32_t nslots = (uint32_t)s.num_blocks * hkv * kPage;
-  const int vecs = s.row_bytes / 16;
-  for (int mi = threadIdx.x; lists_ok && mi < n_moves; mi += blockDim.x) {
-    const uint32_t si = (uint32_t)srcs[mi];
-    const uint32_t di = (uint32_t)holes[mi];
-    if (si >= nslots || di >= nslots) {
-      atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
-      continue;
-    }
-    const uint4* kp = reinterpret_cast<const uint4*>(s.k_codes + (size_t)si * s.row_bytes);
-    const uint4* vp = reinterpret_cast<const uint4*>(s.v_codes + (size_t)si * s.row_bytes);
-    uint4* kd = reinterpret_cast<uint4*>(s.k_codes + (size_t)di * s.row_bytes);
-    uint4* vd = reinterpret_cast<uint4*>(s.v_codes + (size_t)di * s.row_bytes);
-    const float ks = s.k_scale[si], vs = s.v_scale[si], sc = s.score[si];
-    const int ps = s.slot_pos[si];
-    for (int h0 = 0; h0 < vecs; h0 += 4) {
-      uint4 kv[4], vv[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        kv[i] = kp[h0 + i];
-        vv[i] = vp[h0 + i];
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        kd[h0 + i] = kv[i];
-        vd[h0 + i] = vv[i];
-      }
-    }
-    s.k_scale[di] = ks;
-    s.v_scale[di] = vs;
-    s.slot_pos[di] = ps;
-    s.score[di] = sc;
-  }
+  if (threadIdx.x == 0) a.n_moves[pair] = lists_ok ? hole_base : 0;
 
-  }  // !keep_all
+  } else if (threadIdx.x == 0) {
+    a.n_moves[pair] = 0;
+  }
 
   // ---- the last of the sequence's KV-head CTAs to finish applies its new
   // length and releases its pages past ceil(n'/16) (every CTA of the
@@ -279,6 +266,48 @@ __global__ void __launch_bounds__(kStepThreads, 2) step_post_kernel(DevState s, 
     for (int j = threadIdx.x; j < nfree; j += blockDim.x) s.free_stack[fbase + j] = btp[keep_pages + j];
 }
 
+// Row moves of one (KV head, sequence): one thread per (source -> hole),
+// rows as 16-byte vectors, the slot's scales, position and score with it.
+__global__ void __launch_bounds__(kStepThreads) step_moves_kernel(DevState s, StepArgs a) {
+  const size_t pair = (size_t)blockIdx.y * s.hkv + blockIdx.x;
+  const int n_moves = a.n_moves[pair];
+  const int32_t* holes = reinterpret_cast<const int32_t*>(a.g_keys + pair * a.s_cap);
+  const int32_t* srcs = a.g_pos + pair * a.s_cap;
+  const uint32_t nslots = (uint32_t)s.num_blocks * s.hkv * kPage;
+  const int vecs = s.row_bytes / 16;
+  for (int mi = threadIdx.x; mi < n_moves; mi += blockDim.x) {
+    const uint32_t si = (uint32_t)srcs[mi];
+    const uint32_t di = (uint32_t)holes[mi];
+    if (si >= nslots || di >= nslots) {
+      atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
+      continue;
+    }
+    const uint4* kp = reinterpret_cast<const uint4*>(s.k_codes + (size_t)si * s.row_bytes);
+    const uint4* vp = reinterpret_cast<const uint4*>(s.v_codes + (size_t)si * s.row_bytes);
+    uint4* kd = reinterpret_cast<uint4*>(s.k_codes + (size_t)di * s.row_bytes);
+    uint4* vd = reinterpret_cast<uint4*>(s.v_codes + (size_t)di * s.row_bytes);
+    const float ks = s.k_scale[si], vs = s.v_scale[si], sc = s.score[si];
+    const int ps = s.slot_pos[si];
+    for (int h0 = 0; h0 < vecs; h0 += 4) {
+      uint4 kv[4], vv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        kv[i] = kp[h0 + i];
+        vv[i] = vp[h0 + i];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        kd[h0 + i] = kv[i];
+        vd[h0 + i] = vv[i];
+      }
+    }
+    s.k_scale[di] = ks;
+    s.v_scale[di] = vs;
+    s.slot_pos[di] = ps;
+    s.score[di] = sc;
+  }
+}
+
 }  // namespace
 
 int step_max_smem_slots() { return (160 * 1024) / 8; }
@@ -286,20 +315,19 @@ int step_max_smem_slots() { return (160 * 1024) / 8; }
 cudaError_t launch_step_post(const DevState& s, int seq_begin, int batch, const uint16_t* q, uint16_t* out,
                              float qk_scale_log2, const AttnWork& w, const StepArgs& a, cudaStream_t st) {
   const int smem = a.smem_slots > 0 ? a.smem_slots * 8 : 0;
-  if (smem > 48 * 1024) {
+  if (smem > 0) {
     static int done[64] = {0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(step_post_kernel), step_max_smem_slots() * 8, done);
     if (e != cudaSuccess) return e;
-    if (dev >= 64 || !done[dev]) {
-      e = cudaFuncSetAttribute(step_post_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               step_max_smem_slots() * 8);
-      if (e != cudaSuccess) return e;
-      if (dev < 64) done[dev] = 1;
-    }
   }
   dim3 grid(s.hkv, batch);
   step_post_kernel<<<grid, kStepThreads, smem, st>>>(s, seq_begin, batch, q, out, qk_scale_log2, w, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_step_moves(const DevState& s, int batch, const StepArgs& a, cudaStream_t st) {
+  dim3 grid(s.hkv, batch);
+  step_moves_kernel<<<grid, kStepThreads, 0, st>>>(s, a);
   return cudaGetLastError();
 }
 

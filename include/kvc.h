@@ -244,8 +244,9 @@ kvc_status kvc_decode_attention_noalloc(kvc_cache* cache, int32_t seq_begin, int
  * (H2O accumulation on in H2O mode, off in StreamingLLM mode), selection and
  * compaction with `params`, exactly as the four calls above compute them.
  * After the split-K attention, the merge, the score update, the selection and
- * the compaction of each (sequence, KV head) run in one kernel that keeps the
- * scores, keys and move lists on chip; three launches in all.
+ * the compaction lists of each (sequence, KV head) run in one kernel that
+ * keeps the scores, keys and keep decisions on chip; the row moves follow in
+ * a launch of their own.  Four launches in all.
  *   d_q: bf16 [batch][Hq][128]; d_k_new, d_v_new: bf16 [batch][Hkv][1][128];
  *   d_out: bf16 [batch][Hq][128]; workspace as for kvc_decode_attention.
  * Host-visible errors (arguments, capacity) are returned before anything is

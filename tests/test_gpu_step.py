@@ -1,4 +1,5 @@
-"""kvc_decode_step (one call per layer, fused merge/select/compaction) must
+"""kvc_decode_step (one call per layer: append, split attention, the fused
+merge/score/select/list kernel, the move kernel) must
 leave exactly the device state and outputs that the four separate calls leave,
 step after step; plus one direct check against the oracle."""
 import numpy as np
@@ -73,7 +74,7 @@ def test_step_equals_separate_calls(bits, hq, hkv, lengths, mode, budget, recent
         vn = T.to_dev_bf16(_bits(rng, (B, hkv, 1, 128)))
         oa = ca.step(q, kn, vn, mode=mode, budget=budget, recent=recent, window=window)
         ob = cb.decode_step(q, kn, vn, mode=mode, budget=budget, recent=recent, window=window)
-        assert cb.last_launch_count() == 3
+        assert cb.last_launch_count() == 4
         torch.cuda.synchronize()
         assert torch.equal(oa, ob)
         _same_state(ca, cb)
