@@ -1,7 +1,8 @@
 // Device helpers shared by the kernels of the compressed-KV library: the
 // exp2 and bf16 primitives, the page prefix of a batch slice and the stream-K
 // CTA lookup of the split attention, block scans and the radix select of the
-// kept-set selection, and the merge of the split-K partials with the sinks.
+// kept-set selection, the merge of the split-K partials with the sinks, and
+// the compaction's row moves.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -251,6 +252,67 @@ __device__ __forceinline__ float h2o_increment(const float* lgr, int s_cap, int 
   float inc = 0.0f;
   for (int g = 0; g < G; ++g) inc = __fmaf_rn(fast_exp2(lgr[(size_t)g * s_cap + t] - ms.M[g]), ms.invL[g], inc);
   return inc;
+}
+
+// Row moves of one (KV head, sequence): entry i of `srcs` (a physical pool
+// slot) goes to entry i of `holes`, with its K and V code rows, scales,
+// position and score.  The row_bytes / 16 lanes of a row move its 16-byte
+// chunks in one instruction, so every store covers whole 32-byte sectors (a
+// store of half a sector makes L2 fetch the sector from DRAM first); a warp
+// moves 32 / (row_bytes / 16) consecutive entries per instruction, three such
+// groups in flight.  The lane holding chunk 0 of a row also moves the slot's
+// four scalars.  Entries outside the pool set kDevBadBlockId and are skipped.
+__device__ __forceinline__ void move_rows(const DevState& s, const int32_t* holes, const int32_t* srcs,
+                                          int n_moves) {
+  constexpr int U = 3;
+  const uint32_t nslots = (uint32_t)s.num_blocks * s.hkv * kPage;
+  const int lpr = s.row_bytes / 16;  // lanes per row
+  const int rpw = 32 / lpr;          // rows per warp instruction
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int r = lane / lpr, c = lane % lpr;
+  for (int base = warp * rpw * U; base < n_moves; base += nwarps * rpw * U) {
+    uint4 kv[U], vv[U];
+    uint32_t si[U], di[U];
+    bool on[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int mi = base + u * rpw + r;
+      on[u] = mi < n_moves;
+      si[u] = on[u] ? (uint32_t)srcs[mi] : 0u;
+      di[u] = on[u] ? (uint32_t)holes[mi] : 0u;
+      if (on[u] && (si[u] >= nslots || di[u] >= nslots)) {
+        if (c == 0) atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
+        on[u] = false;
+      }
+      if (on[u]) {
+        kv[u] = reinterpret_cast<const uint4*>(s.k_codes + (size_t)si[u] * s.row_bytes)[c];
+        vv[u] = reinterpret_cast<const uint4*>(s.v_codes + (size_t)si[u] * s.row_bytes)[c];
+      }
+    }
+    float ks[U], vs[U], sc[U];
+    int ps[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (on[u] && c == 0) {
+        ks[u] = s.k_scale[si[u]];
+        vs[u] = s.v_scale[si[u]];
+        sc[u] = s.score[si[u]];
+        ps[u] = s.slot_pos[si[u]];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (!on[u]) continue;
+      reinterpret_cast<uint4*>(s.k_codes + (size_t)di[u] * s.row_bytes)[c] = kv[u];
+      reinterpret_cast<uint4*>(s.v_codes + (size_t)di[u] * s.row_bytes)[c] = vv[u];
+      if (c == 0) {
+        s.k_scale[di[u]] = ks[u];
+        s.v_scale[di[u]] = vs[u];
+        s.score[di[u]] = sc[u];
+        s.slot_pos[di[u]] = ps[u];
+      }
+    }
+  }
 }
 
 }  // namespace dev

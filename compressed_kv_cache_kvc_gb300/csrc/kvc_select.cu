@@ -142,9 +142,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(DevState s, int seq
 // thread): the keep-mask bytes of a thread's 16 slots come in one 16-byte
 // load; block scans give every hole (evicted slot below n') and every source
 // (kept slot at or above n') its rank, and the physical pool index of the
-// i-th hole and of the i-th source go to two lists.  Phase 2: each warp moves
-// several (source -> hole) rows at once, lanes splitting a row 4 bytes each,
-// all loads of a batch issued before its stores.
+// i-th hole and of the i-th source go to two lists.  Phase 2: the row moves
+// (move_rows: the lanes of a row store its 16-byte chunks together).
 __global__ void __launch_bounds__(kCompactThreads, 2) compact_kernel(DevState s, int seq_begin,
                                                                  const uint8_t* __restrict__ mask, int s_cap,
                                                                  int32_t* __restrict__ g_holes,
@@ -216,44 +215,9 @@ __global__ void __launch_bounds__(kCompactThreads, 2) compact_kernel(DevState s,
   }
   __syncthreads();
 
-  // phase 2: moves, one thread per (source -> hole) pair: the K and V rows
-  // move as 16-byte vectors (all loads of a row pair in flight before the
-  // stores), then the four per-slot values
+  // phase 2: the row moves
   const int n_moves = hole_base;
-  const uint32_t nslots = (uint32_t)s.num_blocks * hkv * kPage;
-  const int vecs = s.row_bytes / 16;  // 8 (INT8) or 4 (INT4)
-  for (int mi = threadIdx.x; mi < n_moves; mi += kCompactThreads) {
-    const uint32_t si = (uint32_t)srcs[mi];
-    const uint32_t di = (uint32_t)holes[mi];
-    if (si >= nslots || di >= nslots) {
-      atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
-      continue;
-    }
-    const uint4* kp = reinterpret_cast<const uint4*>(s.k_codes + (size_t)si * s.row_bytes);
-    const uint4* vp = reinterpret_cast<const uint4*>(s.v_codes + (size_t)si * s.row_bytes);
-    uint4* kd = reinterpret_cast<uint4*>(s.k_codes + (size_t)di * s.row_bytes);
-    uint4* vd = reinterpret_cast<uint4*>(s.v_codes + (size_t)di * s.row_bytes);
-    const float ks = s.k_scale[si], vs = s.v_scale[si], sc = s.score[si];
-    const int ps = s.slot_pos[si];
-    // 64-byte halves of the K and V rows: 8 vectors in flight, then stored
-    for (int h0 = 0; h0 < vecs; h0 += 4) {
-      uint4 kv[4], vv[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        kv[i] = kp[h0 + i];
-        vv[i] = vp[h0 + i];
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        kd[h0 + i] = kv[i];
-        vd[h0 + i] = vv[i];
-      }
-    }
-    s.k_scale[di] = ks;
-    s.v_scale[di] = vs;
-    s.slot_pos[di] = ps;
-    s.score[di] = sc;
-  }
+  move_rows(s, holes, srcs, n_moves);
 
   // release the emptied pages (all KV heads share the page structure)
   if (h == 0) {

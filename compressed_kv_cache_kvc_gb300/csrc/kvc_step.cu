@@ -266,66 +266,11 @@ __global__ void __launch_bounds__(kStepThreads, 2) step_post_kernel(DevState s, 
     for (int j = threadIdx.x; j < nfree; j += blockDim.x) s.free_stack[fbase + j] = btp[keep_pages + j];
 }
 
-// Row moves of one (KV head, sequence).  The row_bytes / 16 lanes of a row
-// move its 16-byte chunks in one instruction, so every store covers whole
-// 32-byte sectors (a half-sector store makes L2 fetch the sector from DRAM
-// first); a warp moves 32 / (row_bytes / 16) consecutive list entries per
-// instruction, three such groups in flight.  The lane holding chunk 0 of a
-// row also moves the slot's scales, position and score.
+// Row moves of one (KV head, sequence) per CTA (see move_rows).
 __global__ void __launch_bounds__(kStepThreads, 2) step_moves_kernel(DevState s, StepArgs a) {
-  constexpr int U = 3;
   const size_t pair = (size_t)blockIdx.y * s.hkv + blockIdx.x;
-  const int n_moves = a.n_moves[pair];
-  const int32_t* holes = reinterpret_cast<const int32_t*>(a.g_keys + pair * a.s_cap);
-  const int32_t* srcs = a.g_pos + pair * a.s_cap;
-  const uint32_t nslots = (uint32_t)s.num_blocks * s.hkv * kPage;
-  const int lpr = s.row_bytes / 16;  // lanes per row
-  const int rpw = 32 / lpr;          // rows per warp instruction
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  const int r = lane / lpr, c = lane % lpr;
-  for (int base = warp * rpw * U; base < n_moves; base += nwarps * rpw * U) {
-    uint4 kv[U], vv[U];
-    uint32_t si[U], di[U];
-    bool on[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int mi = base + u * rpw + r;
-      on[u] = mi < n_moves;
-      si[u] = on[u] ? (uint32_t)srcs[mi] : 0u;
-      di[u] = on[u] ? (uint32_t)holes[mi] : 0u;
-      if (on[u] && (si[u] >= nslots || di[u] >= nslots)) {
-        if (c == 0) atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
-        on[u] = false;
-      }
-      if (on[u]) {
-        kv[u] = reinterpret_cast<const uint4*>(s.k_codes + (size_t)si[u] * s.row_bytes)[c];
-        vv[u] = reinterpret_cast<const uint4*>(s.v_codes + (size_t)si[u] * s.row_bytes)[c];
-      }
-    }
-    float ks[U], vs[U], sc[U];
-    int ps[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      if (on[u] && c == 0) {
-        ks[u] = s.k_scale[si[u]];
-        vs[u] = s.v_scale[si[u]];
-        sc[u] = s.score[si[u]];
-        ps[u] = s.slot_pos[si[u]];
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      if (!on[u]) continue;
-      reinterpret_cast<uint4*>(s.k_codes + (size_t)di[u] * s.row_bytes)[c] = kv[u];
-      reinterpret_cast<uint4*>(s.v_codes + (size_t)di[u] * s.row_bytes)[c] = vv[u];
-      if (c == 0) {
-        s.k_scale[di[u]] = ks[u];
-        s.v_scale[di[u]] = vs[u];
-        s.score[di[u]] = sc[u];
-        s.slot_pos[di[u]] = ps[u];
-      }
-    }
-  }
+  move_rows(s, reinterpret_cast<const int32_t*>(a.g_keys + pair * a.s_cap), a.g_pos + pair * a.s_cap,
+            a.n_moves[pair]);
 }
 
 }  // namespace
