@@ -181,6 +181,28 @@ __device__ __forceinline__ void merge_phase(const DevState& s, int seq_begin, in
   }
   const uint16_t* sk = s.sink_k + ((size_t)b * hkv + h) * kSinks * kHeadDim;
   const uint16_t* sv = s.sink_v + ((size_t)b * hkv + h) * kSinks * kHeadDim;
+  {
+    // Everything the merge reads lies in a few contiguous runs: the pair's
+    // partials (consecutive slots pair + i_first .. pair + i_last), its
+    // query rows and sink rows.  Prefetch them into L1 now, so the phases
+    // after each barrier below find them there instead of in L2.
+    const int npart = i_last - i_first + 1;
+    const char* po = reinterpret_cast<const char*>(w.part_o + ((size_t)pair + i_first) * G * kHeadDim);
+    const char* pm = reinterpret_cast<const char*>(w.part_ml + ((size_t)pair + i_first) * G * 2);
+    const char* qr = reinterpret_cast<const char*>(q + ((size_t)bl * s.hq + h * G) * kHeadDim);
+    const int lo = npart * G * kHeadDim * 4 / 128;             // part_o lines
+    const int lm = (npart * G * 2 * 4 + 127) / 128;            // part_ml lines
+    const int lq = G * kHeadDim * 2 / 128;                     // query lines
+    const int ls = kSinks * kHeadDim * 2 / 128;                // lines per sink tensor
+    for (int i = threadIdx.x; i < lo + lm + lq + 2 * ls; i += blockDim.x) {
+      const char* a = i < lo ? po + 128 * i
+                    : i < lo + lm ? pm + 128 * (i - lo)
+                    : i < lo + lm + lq ? qr + 128 * (i - lo - lm)
+                    : i < lo + lm + lq + ls ? reinterpret_cast<const char*>(sk) + 128 * (i - lo - lm - lq)
+                                            : reinterpret_cast<const char*>(sv) + 128 * (i - lo - lm - lq - ls);
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(a));
+    }
+  }
 
   // sink logits: warp task (g, j) = (task / 4, task % 4)
   for (int task = warp; task < kMaxGroup * kSinks; task += nwarps) {
