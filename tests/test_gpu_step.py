@@ -108,3 +108,40 @@ def test_step_against_oracle_tiny_workload():
         assert T.kept_sets_agree(kept_gpu, kept_ora, hs.pos, hs.score, w.budget - 4 - w.recent,
                                  w.context + 1 - w.recent)
     assert c.lengths(0) == (w.budget - 4, w.context + 1)
+
+
+@pytest.mark.parametrize("bits,hq,hkv", [(8, 16, 4), (4, 40, 8)])
+def test_step_on_batch_slices(bits, hq, hkv):
+    """Slices of the batch (seq_begin > 0, batch < max_batch) step exactly as
+    the separate calls on the same slices do, and leave the other sequences
+    untouched."""
+    from compressed_kv_cache_kvc_gb300.cache import KVCache
+    rng = np.random.default_rng(bits + hq)
+    lengths = [300, 530, 47, 1000, 260]
+    B, T_ = len(lengths), max(lengths)
+    mbps = (T_ + 16 + 15) // 16 + 2
+    ca = KVCache(hq, hkv, bits, B * mbps, B, mbps)
+    cb = KVCache(hq, hkv, bits, B * mbps, B, mbps)
+    k = _bits(rng, (B, hkv, T_, 128))
+    v = _bits(rng, (B, hkv, T_, 128))
+    for c in (ca, cb):
+        for b, n in enumerate(lengths):
+            c.quantize_append(T.to_dev_bf16(np.ascontiguousarray(k[b:b + 1, :, :n])),
+                              T.to_dev_bf16(np.ascontiguousarray(v[b:b + 1, :, :n])), seq_begin=b)
+    for seq_begin, batch in [(1, 3), (0, 2), (3, 2)]:
+        before = T.StateView(cb)
+        q = T.to_dev_bf16(_bits(rng, (batch, hq, 128)))
+        kn = T.to_dev_bf16(_bits(rng, (batch, hkv, 1, 128)))
+        vn = T.to_dev_bf16(_bits(rng, (batch, hkv, 1, 128)))
+        oa = ca.step(q, kn, vn, mode="h2o", budget=200, recent=32, seq_begin=seq_begin)
+        ob = cb.decode_step(q, kn, vn, mode="h2o", budget=200, recent=32, seq_begin=seq_begin)
+        torch.cuda.synchronize()
+        assert torch.equal(oa, ob)
+        _same_state(ca, cb)
+        after = T.StateView(cb)
+        for b in list(range(seq_begin)) + list(range(seq_begin + batch, B)):
+            assert after.slots[b] == before.slots[b] and after.seen[b] == before.seen[b]
+            for h in range(hkv):
+                for x, y in zip(before.head(b, h), after.head(b, h)):
+                    assert np.array_equal(np.asarray(x).view(np.uint8), np.asarray(y).view(np.uint8)), (b, h)
+    assert ca.read_status() == 0 and cb.read_status() == 0
