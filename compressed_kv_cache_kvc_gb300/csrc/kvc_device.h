@@ -147,6 +147,31 @@ __device__ uint32_t radix_select(int n, int want, bool descending, ActiveF activ
   return prefix;
 }
 
+// Compaction target: the kept slots of a (sequence, KV head) with S slots
+// and n' < S kept end up in the window [w, w + n'), w = the start of the
+// last page-aligned window of n' slots inside [0, S).  Evicted slots inside
+// the window are the holes, kept slots outside it the sources; afterwards
+// the block-table row drops its first w / 16 pages, so the window becomes
+// slots [0, n').  After a long prefill the always-kept recent tokens sit at
+// the end of the sequence, inside the window, and stay where they are; at
+// steady state (S = n' + 1) w = 0.  A function of (S, n') only, so every KV
+// head of a sequence uses the same window.
+__device__ __forceinline__ int keep_window(int S, int np) { return np < S ? ((S - np) / kPage) * kPage : 0; }
+
+// row[i] = row[p0 + i] for i < n, in place, by the whole block (reads of a
+// chunk before its writes; later chunks read only entries past this chunk).
+// Starts and ends with a barrier.
+__device__ __forceinline__ void shift_row(int32_t* row, int p0, int n) {
+  for (int c0 = 0; c0 < n; c0 += blockDim.x) {
+    const int i = c0 + (int)threadIdx.x;
+    __syncthreads();
+    const int32_t v = i < n ? row[p0 + i] : 0;
+    __syncthreads();
+    if (i < n) row[i] = v;
+  }
+  __syncthreads();
+}
+
 // Shared state of the merge phase.
 struct MergeShared {
   float sl[kMaxGroup][kSinks];  // sink logits (log2 domain)

@@ -496,7 +496,7 @@ kvc_status kvc_compact_blocks(kvc_cache* c, int32_t seq_begin, int32_t batch, co
                           reinterpret_cast<int32_t*>(ws + wl.pos), smem_moves,
                           static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return KVC_ERR_CUDA;
-  c->last_launches = 1;
+  c->last_launches = 2;  // compaction, then the release of the emptied pages
   for (int i = 0; i < batch; ++i) c->slots[seq_begin + i] = c->plan_new[i];
   c->plan_pending = false;
   return KVC_OK;

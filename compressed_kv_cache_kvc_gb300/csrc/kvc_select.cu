@@ -140,9 +140,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(DevState s, int seq
 
 // Compaction of one (KV head, sequence).  Phase 1 (tiles of 16 slots per
 // thread): the keep-mask bytes of a thread's 16 slots come in one 16-byte
-// load; block scans give every hole (evicted slot below n') and every source
-// (kept slot at or above n') its rank, and the physical pool index of the
-// i-th hole and of the i-th source go to two lists.  Phase 2: the row moves
+// load; block scans give every hole (evicted slot inside the keep window,
+// see keep_window) and every source (kept slot outside it) its rank, and the
+// physical pool index of the i-th hole and of the i-th source go to two
+// lists.  Phase 2: the row moves
 // (move_rows: the lanes of a row store its 16-byte chunks together).
 __global__ void __launch_bounds__(kCompactThreads, 2) compact_kernel(DevState s, int seq_begin,
                                                                  const uint8_t* __restrict__ mask, int s_cap,
@@ -172,6 +173,7 @@ __global__ void __launch_bounds__(kCompactThreads, 2) compact_kernel(DevState s,
   }
   __syncthreads();
 
+  const int wlo = keep_window(S, np);
   int hole_base = 0, src_base = 0;
   for (int tile0 = 0; tile0 < S; tile0 += kCompactThreads * 16) {
     const int t0 = tile0 + threadIdx.x * 16;
@@ -183,13 +185,13 @@ __global__ void __launch_bounds__(kCompactThreads, 2) compact_kernel(DevState s,
       for (int i = 0; i < 16; ++i)
         if (((wv[i >> 2] >> (8 * (i & 3))) & 0xFFu) != 0 && t0 + i < S) kept_bits |= 1u << i;
     }
-    // bit i of `below` is set when slot t0 + i < n'
-    const int nb = min(max(np - t0, 0), 16);
-    const uint32_t below = nb >= 16 ? 0xFFFFu : ((1u << nb) - 1u);
+    // bit i of `inwin` is set when slot t0 + i lies in the window [wlo, wlo + n')
+    const int lo = min(max(wlo - t0, 0), 16), hi = min(max(wlo + np - t0, 0), 16);
+    const uint32_t inwin = ((1u << hi) - 1u) & ~((1u << lo) - 1u);
     const int nv = min(max(S - t0, 0), 16);
     const uint32_t valid = nv >= 16 ? 0xFFFFu : ((1u << nv) - 1u);
-    const uint32_t hole_bits = ~kept_bits & below & valid;
-    const uint32_t src_bits = kept_bits & ~below;
+    const uint32_t hole_bits = ~kept_bits & inwin & valid;
+    const uint32_t src_bits = kept_bits & ~inwin;
     // one scan of both counts (each <= 16 per thread, <= 8192 per tile)
     const int nh = __popc(hole_bits), ns = __popc(src_bits);
     int tot_packed;
@@ -218,30 +220,40 @@ __global__ void __launch_bounds__(kCompactThreads, 2) compact_kernel(DevState s,
   // phase 2: the row moves
   const int n_moves = hole_base;
   move_rows(s, holes, srcs, n_moves);
+}
 
-  // release the emptied pages (all KV heads share the page structure)
-  if (h == 0) {
-    const int keep_pages = (np + kPage - 1) / kPage;
-    const int old_pages = (S + kPage - 1) / kPage;
-    const int nfree = old_pages - keep_pages;
-    __shared__ int sh_base;
-    if (threadIdx.x == 0) {
-      int base = 0;
-      if (nfree > 0) {
-        base = atomicAdd(&s.counters[kCtrFreeTop], nfree);
-        if (base + nfree > s.num_blocks) {
-          atomicSub(&s.counters[kCtrFreeTop], nfree);
-          atomicOr(&s.counters[kCtrStatus], kDevStackOverflow);
-          base = -1;
-        }
+// Release of one sequence's pages after its compaction (one CTA per
+// sequence, after every KV head's compact CTA): pages [0, p0) and
+// [p0 + ceil(n'/16), ceil(S/16)) go to the free stack, the row drops its
+// first p0 = w / 16 pages (see keep_window) and the sequence holds n' slots.
+__global__ void __launch_bounds__(256) release_kernel(DevState s, int seq_begin) {
+  const int b = seq_begin + blockIdx.x;
+  const int S = s.plan[2 * b];
+  const int np = s.plan[2 * b + 1];
+  if (np >= S) return;
+  const int keep_pages = (np + kPage - 1) / kPage;
+  const int old_pages = (S + kPage - 1) / kPage;
+  const int nfree = old_pages - keep_pages;
+  const int p0 = keep_window(S, np) / kPage;
+  int32_t* row = s.block_table + (size_t)b * s.max_bps;
+  __shared__ int sh_base;
+  if (threadIdx.x == 0) {
+    int base = -1;
+    if (nfree > 0) {
+      base = atomicAdd(&s.counters[kCtrFreeTop], nfree);
+      if (base + nfree > s.num_blocks) {
+        atomicSub(&s.counters[kCtrFreeTop], nfree);
+        atomicOr(&s.counters[kCtrStatus], kDevStackOverflow);
+        base = -1;
       }
-      sh_base = base;
-      s.seq_slots[b] = np;
     }
-    __syncthreads();
-    if (sh_base >= 0)
-      for (int i = threadIdx.x; i < nfree; i += blockDim.x) s.free_stack[sh_base + i] = bt[keep_pages + i];
+    sh_base = base;
+    s.seq_slots[b] = np;
   }
+  __syncthreads();
+  if (sh_base >= 0)
+    for (int j = threadIdx.x; j < nfree; j += blockDim.x) s.free_stack[sh_base + j] = row[j < p0 ? j : keep_pages + j];
+  if (p0 > 0) shift_row(row, p0, keep_pages);
 }
 
 }  // namespace
@@ -273,6 +285,9 @@ cudaError_t launch_compact(const DevState& s, int seq_begin, int batch, const ui
   }
   dim3 grid(s.hkv, batch);
   compact_kernel<<<grid, kCompactThreads, smem, st>>>(s, seq_begin, keep_mask, s_cap, g_holes, g_srcs, smem_moves);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  release_kernel<<<batch, 256, 0, st>>>(s, seq_begin);
   return cudaGetLastError();
 }
 

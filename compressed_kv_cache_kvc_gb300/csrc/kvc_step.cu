@@ -181,6 +181,7 @@ __global__ void __launch_bounds__(kStepThreads, 2) step_post_kernel(DevState s, 
   int32_t* srcs = a.g_pos + pair * a.s_cap;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t lt = (1u << lane) - 1u;
+  const int wlo = keep_window(S, np);
   int hole_base = 0, src_base = 0;
   for (int tile0 = 0; tile0 < S; tile0 += kStepThreads * 16) {
     const int wbase = tile0 + warp * 512 + lane;
@@ -191,8 +192,9 @@ __global__ void __launch_bounds__(kStepThreads, 2) step_post_kernel(DevState s, 
       if (t < S) {
         const uint32_t k = keys[t];
         const bool kept = n_keep > 0 && (k > theta || (k == theta && (uint32_t)pos[t] <= pos_cut));
-        if (kept && t >= np) src_bits |= 1u << i;
-        if (!kept && t < np) hole_bits |= 1u << i;
+        const bool inwin = (unsigned)(t - wlo) < (unsigned)max(np, 0);
+        if (kept && !inwin) src_bits |= 1u << i;
+        if (!kept && inwin) hole_bits |= 1u << i;
       }
     }
     const uint32_t packed = __reduce_add_sync(0xffffffffu, __popc(hole_bits) | (__popc(src_bits) << 16));
@@ -246,6 +248,7 @@ __global__ void __launch_bounds__(kStepThreads, 2) step_post_kernel(DevState s, 
   __threadfence();
   const int keep_pages = (n_keep + kPage - 1) / kPage;
   const int nfree = npages - keep_pages;
+  const int p0 = keep_window(S, n_keep) / kPage;  // first page of the window
   if (threadIdx.x == 0) {
     int fbase = -1;
     if (nfree > 0) {
@@ -262,8 +265,10 @@ __global__ void __launch_bounds__(kStepThreads, 2) step_post_kernel(DevState s, 
   }
   __syncthreads();
   const int fbase = sh_sel[0];
+  // released: pages [0, p0) and [p0 + keep_pages, npages) of the old row
   if (fbase >= 0)
-    for (int j = threadIdx.x; j < nfree; j += blockDim.x) s.free_stack[fbase + j] = btp[keep_pages + j];
+    for (int j = threadIdx.x; j < nfree; j += blockDim.x) s.free_stack[fbase + j] = btp[j < p0 ? j : keep_pages + j];
+  if (p0 > 0) shift_row(s.block_table + (size_t)b * s.max_bps, p0, keep_pages);
 }
 
 // Row moves of one (KV head, sequence) per CTA (see move_rows).

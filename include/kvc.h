@@ -203,12 +203,17 @@ kvc_status kvc_h2o_select_evict(kvc_cache* cache, int32_t seq_begin, int32_t bat
                                 void* d_workspace, size_t workspace_bytes, void* stream);
 
 /* Compaction ("KV Cache optimization techniques" 2.2: gather the kept tokens;
- * 3.2: release blocks).  With n' kept slots, every evicted slot below n' is
- * filled, in ascending order, by the kept slots at or above n', in ascending
- * order (codes, scales, position, score move together); the sequence then
- * holds n' slots and the pages past ceil(n'/16) return to the free stack.
- * Attention is invariant under the order of the attended tokens, so the
- * result attends to exactly the kept set.
+ * 3.2: release blocks).  With S slots and n' < S kept, the kept slots are
+ * gathered into the window [w, w + n'), w = 16 * floor((S - n') / 16), the
+ * last page-aligned window of n' slots: every evicted slot inside the window
+ * is filled, in ascending order, by the kept slots outside it, in ascending
+ * order (codes, scales, position, score move together).  The block-table row
+ * then drops its first w / 16 pages, so the window becomes slots [0, n'), and
+ * the pages before and after the window return to the free stack.  After a
+ * long context the always-kept recent tokens lie at the end, inside the
+ * window, and do not move; at steady state (S = n' + 1) w = 0.  Attention is
+ * invariant under the order of the attended tokens, so the result attends to
+ * exactly the kept set.  Two launches (compaction, page release).
  *   d_keep_mask: the mask kvc_h2o_select_evict wrote for the same slice.
  * Errors: KVC_ERR_STATE if the slice has no pending selection. */
 kvc_status kvc_compact_blocks(kvc_cache* cache, int32_t seq_begin, int32_t batch,
