@@ -82,30 +82,35 @@ __device__ int block_scan(int v, int* sh_warp, int* total) {
 // Radix select over `n` entries: among the entries with active(i) true, find
 // the `want`-th in the requested order (largest-first when `descending`) of
 // value(i); returns the value and, in *remaining, how many entries equal to it
-// are still wanted (1 <= *remaining).  MSB-first in three passes of 11, 11
-// and 10 bits: wide digits spread values that share their top bits (scores
-// of one magnitude share sign and exponent) over many histogram bins, so the
-// shared-memory atomics seldom meet on one address.  `hist` holds
-// kRadixBins ints; the NT threads scan the bins, each owning nb / NT
-// consecutive ones in the requested order.
+// are still wanted (1 <= *remaining) and, in *ties, how many active entries
+// equal it.  MSB-first in three passes of 11, 11 and 10 bits: wide digits
+// spread values that share their top bits (scores of one magnitude share
+// sign and exponent) over many histogram bins, so the shared-memory atomics
+// seldom meet on one address.  `hist` holds kRadixBins ints; with
+// pass0_ready it already holds the first pass's histogram (bits 31..21 of
+// every active value), built by the caller.  The NT threads scan the bins,
+// each owning nb / NT consecutive ones in the requested order.  sh_sel holds
+// three ints.
 constexpr int kRadixBins = 2048;
 
 template <int NT, typename ActiveF, typename ValueF>
 __device__ uint32_t radix_select(int n, int want, bool descending, ActiveF active, ValueF value, int* hist,
-                                 int* sh_warp, int* sh_sel, int* remaining) {
+                                 int* sh_warp, int* sh_sel, int* remaining, int* ties, bool pass0_ready = false) {
   static_assert(NT >= 32 && NT <= 1024 && (1024 % NT) == 0, "block size");
   uint32_t prefix = 0, pmask = 0;
-  int rem = want;
+  int rem = want, equal = 0;
 #pragma unroll 1
   for (int pass = 0; pass < 3; ++pass) {
     const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
     const int nb = pass == 2 ? 1024 : kRadixBins;
-    for (int i = threadIdx.x; i < nb; i += NT) hist[i] = 0;
-    __syncthreads();
-    for (int i = threadIdx.x; i < n; i += NT) {
-      if (!active(i)) continue;
-      const uint32_t v = value(i);
-      if ((v & pmask) == prefix) atomicAdd(&hist[(v >> shift) & (nb - 1)], 1);
+    if (pass > 0 || !pass0_ready) {
+      for (int i = threadIdx.x; i < nb; i += NT) hist[i] = 0;
+      __syncthreads();
+      for (int i = threadIdx.x; i < n; i += NT) {
+        if (!active(i)) continue;
+        const uint32_t v = value(i);
+        if ((v & pmask) == prefix) atomicAdd(&hist[(v >> shift) & (nb - 1)], 1);
+      }
     }
     __syncthreads();
     constexpr int kMaxPer = kRadixBins / NT;
@@ -132,6 +137,7 @@ __device__ uint32_t radix_select(int n, int want, bool descending, ActiveF activ
           const int j = (int)threadIdx.x * per + k;
           sh_sel[0] = descending ? nb - 1 - j : j;
           sh_sel[1] = rem - run;
+          sh_sel[2] = cnt[k];  // entries matching the prefix so far
           break;
         }
         run += cnt[k];
@@ -141,9 +147,11 @@ __device__ uint32_t radix_select(int n, int want, bool descending, ActiveF activ
     prefix |= (uint32_t)sh_sel[0] << shift;
     pmask |= (uint32_t)(nb - 1) << shift;
     rem = sh_sel[1];
+    equal = sh_sel[2];
     __syncthreads();
   }
   *remaining = rem;
+  *ties = equal;  // after the last pass: the entries equal to the result
   return prefix;
 }
 

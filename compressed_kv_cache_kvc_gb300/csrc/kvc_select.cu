@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(DevState s, int seq
 
   extern __shared__ __align__(16) uint32_t dyn[];
   __shared__ int hist[kRadixBins];
-  __shared__ int sh_sel[2];
+  __shared__ int sh_sel[3];
   __shared__ int sh_warp[32];
   uint32_t* keys;
   int32_t* pos;
@@ -117,20 +117,16 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(DevState s, int seq
   }
   __syncthreads();
 
-  int need;
+  int need, ties;
   const uint32_t theta = radix_select<kSelThreads>(
-      S, n_keep, true, [&](int) { return true; }, [&](int i) { return keys[i]; }, hist, sh_warp, sh_sel, &need);
-  // ties at theta: how many are there?
-  int my_ties = 0;
-  for (int t = threadIdx.x; t < S; t += blockDim.x) my_ties += keys[t] == theta;
-  int ties;
-  block_scan<kSelThreads>(my_ties, sh_warp, &ties);
+      S, n_keep, true, [&](int) { return true; }, [&](int i) { return keys[i]; }, hist, sh_warp, sh_sel, &need,
+      &ties);
   uint32_t pos_cut = 0xFFFFFFFFu;
-  if (ties > need) {
-    int rem2;
+  if (ties > need) {  // ties at theta: the lowest positions win
+    int rem2, t2;
     pos_cut = radix_select<kSelThreads>(
         S, need, false, [&](int i) { return keys[i] == theta; }, [&](int i) { return (uint32_t)pos[i]; }, hist,
-        sh_warp, sh_sel, &rem2);
+        sh_warp, sh_sel, &rem2, &t2);
   }
   for (int t = threadIdx.x; t < S; t += blockDim.x) {
     const uint32_t k = keys[t];

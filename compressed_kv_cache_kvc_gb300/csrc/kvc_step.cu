@@ -36,7 +36,7 @@ __global__ void __launch_bounds__(kStepThreads, 2) step_post_kernel(DevState s, 
   __shared__ MergeShared ms;
   __shared__ int32_t sh_bt[kStepBtStage];
   __shared__ int hist[kRadixBins];
-  __shared__ int sh_sel[2];
+  __shared__ int sh_sel[3];
   __shared__ int sh_warp[32];
   extern __shared__ __align__(16) uint32_t dyn[];
 
@@ -44,6 +44,8 @@ __global__ void __launch_bounds__(kStepThreads, 2) step_post_kernel(DevState s, 
   const int bl = blockIdx.y;
   const int b = seq_begin + bl;
   const bool h2o = a.mode == 0;
+  // the selection's first radix histogram is built by the score pass
+  for (int i = threadIdx.x; i < kRadixBins; i += blockDim.x) hist[i] = 0;
   merge_phase(s, seq_begin, batch, w.cum, h, bl, q, out, qk_scale_log2, w, h2o, ms);
 
   const int hkv = s.hkv;
@@ -145,6 +147,18 @@ __global__ void __launch_bounds__(kStepThreads, 2) step_post_kernel(DevState s, 
     // slots past S in the last quarter page get keys too: nothing reads them
     *reinterpret_cast<uint4*>(keys + t) = make_uint4(kk[0], kk[1], kk[2], kk[3]);
     *reinterpret_cast<int4*>(pos + t) = p4;
+    // first-pass histogram (bits 31..21) of the selection; the recent
+    // window's keys all fall in the top bin and are counted per warp
+    int n_top = 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      if (t + c >= S) continue;
+      if (kk[c] == 0xFFFFFFFFu) ++n_top;
+      else atomicAdd(&hist[kk[c] >> 21], 1);
+    }
+    const unsigned am = __activemask();
+    n_top = __reduce_add_sync(am, n_top);
+    if ((threadIdx.x & 31) == __ffs(am) - 1 && n_top > 0) atomicAdd(&hist[kRadixBins - 1], n_top);
   }
   __syncthreads();
   bool lists_ok = true;
@@ -154,18 +168,15 @@ __global__ void __launch_bounds__(kStepThreads, 2) step_post_kernel(DevState s, 
   // lower positions
   uint32_t theta = 0xFFFFFFFFu, pos_cut = 0xFFFFFFFFu;
   if (n_keep > 0) {
-    int need;
+    int need, ties;
     theta = radix_select<kStepThreads>(
-        S, n_keep, true, [&](int) { return true; }, [&](int i) { return keys[i]; }, hist, sh_warp, sh_sel, &need);
-    int my_ties = 0;
-    for (int t = threadIdx.x; t < S; t += blockDim.x) my_ties += keys[t] == theta;
-    int ties;
-    block_scan<kStepThreads>(my_ties, sh_warp, &ties);
-    if (ties > need) {
-      int rem2;
+        S, n_keep, true, [&](int) { return true; }, [&](int i) { return keys[i]; }, hist, sh_warp, sh_sel, &need,
+        &ties, /*pass0_ready=*/true);
+    if (ties > need) {  // ties at theta: the lowest positions win
+      int rem2, t2;
       pos_cut = radix_select<kStepThreads>(
           S, need, false, [&](int i) { return keys[i] == theta; }, [&](int i) { return (uint32_t)pos[i]; },
-          hist, sh_warp, sh_sel, &rem2);
+          hist, sh_warp, sh_sel, &rem2, &t2);
     }
   }
   const int np = n_keep;
