@@ -468,6 +468,146 @@ def gpu_arm(args):
     print(json.dumps(line))
 
 
+# ---------------------------------------------------------------------------
+# per-workload report (not the bench line): every synthetic workload through
+# the same one-call step, as absolute numbers and fractions of the HBM peak
+# ---------------------------------------------------------------------------
+
+def workload_report(args, name: str):
+    """Time the decode step of workload `name` on one GPU: all its layers,
+    one `decode_step` per layer, replayed from a CUDA graph; the state is
+    restored before every timed step (first step after the prefill), and for
+    multi-step workloads the consecutive steps are also timed without
+    restoring.  Prints one JSON line."""
+    import numpy as np
+    import torch
+
+    from compressed_kv_cache_kvc_gb300 import workloads as W
+    from compressed_kv_cache_kvc_gb300.build import build_library
+    build_library()
+    from compressed_kv_cache_kvc_gb300.cache import KVCache
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = W.WORKLOADS[name]
+    layers = args.layers or w.layers
+    B, Hq, Hkv, T = w.batch, w.num_q_heads, w.num_kv_heads, w.context
+    mbps = (T + w.steps + 15) // 16 + 1
+    nblocks = B * mbps
+    lengths = W.context_lengths(w)
+    order = W.block_order(w, nblocks) if w.shuffled_blocks else None
+    per_slot = 2 * (128 * w.bits // 8) + 2 * 4
+    caches, inputs = [], []
+    for l in range(layers):
+        c = KVCache(Hq, Hkv, w.bits, nblocks, B, mbps, block_order=order, device=dev)
+        q, k, v, kn, vn = W.gen_layer_torch(w, l, dev)
+        if np.all(lengths == T):
+            c.quantize_append(k, v)
+        else:
+            for b in range(B):
+                n = int(lengths[b])
+                c.quantize_append(k[b:b + 1, :, :n].contiguous(), v[b:b + 1, :, :n].contiguous(), seq_begin=b)
+        del k, v
+        caches.append(c)
+        inputs.append((q, kn, vn))
+    torch.cuda.synchronize()  # the prefill ran on the default stream; the steps run on their own
+    ws_buf = caches[0].workspace(B)
+    outs = [torch.empty(B, Hq, 128, dtype=torch.bfloat16, device=dev) for _ in range(layers)]
+
+    def step(stream=None):
+        for l, c in enumerate(caches):
+            q, kn, vn = inputs[l]
+            c.decode_step(q, kn, vn, mode=w.mode, budget=w.budget, recent=w.recent, window=w.window,
+                          out=outs[l], workspace=ws_buf, stream=stream)
+
+    stream = torch.cuda.Stream(device=dev)
+    if w.mode == "streaming":
+        # one untimed step: the timed steps see the steady window
+        with torch.cuda.stream(stream):
+            step()
+        torch.cuda.synchronize()
+    snaps = [c.state_view.clone() for c in caches]
+    slots = np.array([[c.lengths(b)[0] for b in range(B)] for c in caches])  # before the step's append
+    kv_bytes = int(((slots + 1) * per_slot).sum()) * Hkv + layers * B * Hkv * 4 * 2 * 128 * 2
+
+    def restore():
+        for c, sn in zip(caches, snaps):
+            c.state_view.copy_(sn, non_blocking=True)
+        torch.cuda.synchronize()
+        for c in caches:
+            c.sync_host()
+
+    tr = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(layers)]
+    for c, (a, b) in zip(caches, tr):
+        a.record()
+        b.record()
+        c.set_trace_events(a, b)
+    for _ in range(max(1, args.warmup)):
+        restore()
+        with torch.cuda.stream(stream):
+            step()
+        torch.cuda.synchronize()
+    restore()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step_ms, attn_ms = [], []
+    for _ in range(args.steps):
+        restore()
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            graph.replay()
+            ev1.record(stream)
+        ev1.synchronize()
+        step_ms.append(ev0.elapsed_time(ev1))
+        attn_ms.extend(a.elapsed_time(b) for a, b in tr)
+    for c in caches:
+        st = c.read_status()
+        if st:
+            raise RuntimeError(f"device status {st:#x}")
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        pass
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    ms = float(np.median(step_ms))
+    attn = float(np.median(attn_ms))
+    line = {"workload": name, "layers": layers, "batch": B, "bits": w.bits, "mode": w.mode,
+            "first_step": {"ms": ms, "kv_bytes": kv_bytes, "step_gbs": kv_bytes / (ms * 1e-3) / 1e9,
+                           "step_frac_of_peak": kv_bytes / (ms * 1e-3) / 1e9 / peak,
+                           "seq_steps_per_s": B / (ms * 1e-3),
+                           "split_us_per_layer": attn * 1e3,
+                           "split_gbs": kv_bytes / layers / (attn * 1e-3) / 1e9,
+                           "split_frac_of_peak": kv_bytes / layers / (attn * 1e-3) / 1e9 / peak},
+            "peak_gbs": peak, "steps_timed": args.steps}
+    if w.steps > 1:
+        # the workload's consecutive steps from the prefill, without restoring
+        restore()
+        per_step = []
+        total_bytes = 0
+        for _ in range(w.steps):
+            lens = np.array([[c.lengths(b)[0] for b in range(B)] for c in caches])
+            total_bytes += int(((lens + 1) * per_slot).sum()) * Hkv + layers * B * Hkv * 4 * 2 * 128 * 2
+            with torch.cuda.stream(stream):
+                ev0.record(stream)
+                step()
+                ev1.record(stream)
+            ev1.synchronize()
+            per_step.append(ev0.elapsed_time(ev1))
+        tot = sum(per_step)
+        line["consecutive_steps"] = {"steps": w.steps, "launch": "eager", "ms_total": tot,
+                                     "kv_bytes": total_bytes, "gbs": total_bytes / (tot * 1e-3) / 1e9,
+                                     "ms_first": per_step[0], "ms_median_later": float(np.median(per_step[1:])),
+                                     "seq_steps_per_s": B * w.steps / (tot * 1e-3)}
+        for c in caches:
+            st = c.read_status()
+            if st:
+                raise RuntimeError(f"device status {st:#x}")
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -477,6 +617,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling only)")
     ap.add_argument("--eager", action="store_true", help="launch each call instead of replaying a CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=None,
+                    help="report mode: time this workload (or 'all') instead of printing the bench line")
     ap.add_argument("--oracle-child", nargs=2, type=int, default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.oracle_child is not None:
@@ -485,6 +627,11 @@ def main():
         return
     if args.impl == "reference":
         reference_arm(args)
+        return
+    if args.workload:
+        from compressed_kv_cache_kvc_gb300 import workloads as W
+        for name in (list(W.WORKLOADS) if args.workload == "all" else [args.workload]):
+            workload_report(args, name)
         return
     gpu_arm(args)
 
