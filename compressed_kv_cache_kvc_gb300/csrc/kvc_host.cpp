@@ -538,15 +538,26 @@ kvc_status kvc_decode_step(kvc_cache* c, int32_t seq_begin, int32_t batch, const
   a.recent = params->recent;
   a.window = params->window;
   a.s_cap = s_cap(c);
-  const int slots4 = (max_s + 3) & ~3;  // the score pass writes whole quarter pages of keys
-  a.smem_slots = slots4 <= kvc::step_max_smem_slots() ? std::max(slots4, 4) : 0;
+  // the score pass writes whole quarter pages of keys; keys and positions in
+  // shared memory when both fit, else the keys alone, else neither
+  const int slots4 = std::max((max_s + 3) & ~3, 4);
+  if (slots4 * 8 <= kvc::step_max_smem_bytes()) {
+    a.smem_slots = slots4;
+    a.pos_smem = 1;
+  } else if (slots4 * 4 <= kvc::step_max_smem_bytes()) {
+    a.smem_slots = slots4;
+    a.pos_smem = 0;
+  } else {
+    a.smem_slots = 0;
+    a.pos_smem = 0;
+  }
   a.g_keys = reinterpret_cast<uint32_t*>(ws + wl.keys);
   a.g_pos = reinterpret_cast<int32_t*>(ws + wl.pos);
   a.n_moves = reinterpret_cast<int*>(ws + wl.moves);
   if (kvc::launch_step_post(c->dev, seq_begin, batch, static_cast<const uint16_t*>(d_q),
                             static_cast<uint16_t*>(d_out), qk_scale_log2, w, a, st) != cudaSuccess)
     return KVC_ERR_CUDA;
-  if (kvc::launch_step_moves(c->dev, batch, a, st) != cudaSuccess) return KVC_ERR_CUDA;
+  if (kvc::launch_step_moves(c->dev, batch, a, sm_count(c), st) != cudaSuccess) return KVC_ERR_CUDA;
   launches += 2;
   for (int i = 0; i < batch; ++i) c->slots[seq_begin + i] = plan[i];
   c->plan_pending = false;

@@ -111,15 +111,16 @@ int compact_max_smem_moves();
 struct StepArgs {
   int mode, budget, recent, window;
   int s_cap;            // row stride of the workspace key/position arrays
-  int smem_slots;       // > 0: keys/positions in shared memory (capacity in slots)
+  int smem_slots;       // > 0: keys (and, with pos_smem, positions) in shared memory (capacity in slots)
+  int pos_smem;         // positions in shared memory too (else in g_pos)
   uint32_t* g_keys;     // global fallback [batch][hkv][s_cap]; then the hole list
   int32_t* g_pos;       // likewise; then the source list
   int* n_moves;         // [batch][hkv] list lengths (post kernel -> move kernel)
 };
 cudaError_t launch_step_post(const DevState& s, int seq_begin, int batch, const uint16_t* q, uint16_t* out,
                              float qk_scale_log2, const AttnWork& w, const StepArgs& a, cudaStream_t st);
-cudaError_t launch_step_moves(const DevState& s, int batch, const StepArgs& a, cudaStream_t st);
-int step_max_smem_slots();  // a multiple of 4
+cudaError_t launch_step_moves(const DevState& s, int batch, const StepArgs& a, int sm_count, cudaStream_t st);
+int step_max_smem_bytes();  // dynamic shared memory of the post kernel (a multiple of 16)
 
 int attention_smem_bytes(int bits);
 int attention_ctas_per_sm(int bits);  // resident split CTAs per SM (occupancy API, cached)

@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(kStepThreads, 2) step_post_kernel(DevState s, 
   int32_t* pos;
   if (a.smem_slots > 0) {
     keys = dyn;
-    pos = reinterpret_cast<int32_t*>(dyn + a.smem_slots);
+    pos = a.pos_smem ? reinterpret_cast<int32_t*>(dyn + a.smem_slots) : a.g_pos + pair * a.s_cap;
   } else {
     keys = a.g_keys + pair * a.s_cap;
     pos = a.g_pos + pair * a.s_cap;
@@ -283,22 +283,27 @@ __global__ void __launch_bounds__(kStepThreads, 2) step_post_kernel(DevState s, 
 }
 
 // Row moves of one (KV head, sequence) per CTA (see move_rows).
+// With fewer pairs than SMs, gridDim.z CTAs share a pair's lists, each a
+// contiguous share.
 __global__ void __launch_bounds__(kStepThreads, 2) step_moves_kernel(DevState s, StepArgs a) {
   const size_t pair = (size_t)blockIdx.y * s.hkv + blockIdx.x;
-  move_rows(s, reinterpret_cast<const int32_t*>(a.g_keys + pair * a.s_cap), a.g_pos + pair * a.s_cap,
-            a.n_moves[pair]);
+  const int n = a.n_moves[pair];
+  const int lo = (int)((long long)n * blockIdx.z / gridDim.z);
+  const int hi = (int)((long long)n * (blockIdx.z + 1) / gridDim.z);
+  move_rows(s, reinterpret_cast<const int32_t*>(a.g_keys + pair * a.s_cap) + lo, a.g_pos + pair * a.s_cap + lo,
+            hi - lo);
 }
 
 }  // namespace
 
-int step_max_smem_slots() { return (160 * 1024) / 8; }
+int step_max_smem_bytes() { return 160 * 1024; }
 
 cudaError_t launch_step_post(const DevState& s, int seq_begin, int batch, const uint16_t* q, uint16_t* out,
                              float qk_scale_log2, const AttnWork& w, const StepArgs& a, cudaStream_t st) {
-  const int smem = a.smem_slots > 0 ? a.smem_slots * 8 : 0;
+  const int smem = a.smem_slots > 0 ? a.smem_slots * (a.pos_smem ? 8 : 4) : 0;
   if (smem > 0) {
     static int done[64] = {0};
-    const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(step_post_kernel), step_max_smem_slots() * 8, done);
+    const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(step_post_kernel), step_max_smem_bytes(), done);
     if (e != cudaSuccess) return e;
   }
   dim3 grid(s.hkv, batch);
@@ -306,8 +311,10 @@ cudaError_t launch_step_post(const DevState& s, int seq_begin, int batch, const 
   return cudaGetLastError();
 }
 
-cudaError_t launch_step_moves(const DevState& s, int batch, const StepArgs& a, cudaStream_t st) {
-  dim3 grid(s.hkv, batch);
+cudaError_t launch_step_moves(const DevState& s, int batch, const StepArgs& a, int sm_count, cudaStream_t st) {
+  const int pairs = batch * s.hkv;
+  const int z = pairs < sm_count ? (2 * sm_count + pairs - 1) / pairs : 1;
+  dim3 grid(s.hkv, batch, z);
   step_moves_kernel<<<grid, kStepThreads, 0, st>>>(s, a);
   return cudaGetLastError();
 }

@@ -49,6 +49,8 @@ CASES = [
     (8, 8, 2, [150], "h2o", 4 + 160, 8, 0, 2),        # budget covers the context: nothing evicted
     (4, 4, 2, [90], "h2o", 4, 0, 0, 2),               # only the sinks are kept
     (8, 16, 4, [1000, 1000], "h2o", 300, 64, 0, 2),
+    (8, 8, 2, [21000, 300], "h2o", 2100, 256, 0, 2),  # keys in shared memory, positions in the workspace
+    (4, 8, 2, [41000], "h2o", 4100, 512, 0, 2),       # keys and positions in the workspace
 ]
 
 
