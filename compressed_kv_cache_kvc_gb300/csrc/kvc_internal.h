@@ -118,8 +118,11 @@ struct StepArgs {
   int* n_moves;         // [batch][hkv] list lengths (post kernel -> move kernel)
 };
 cudaError_t launch_step_post(const DevState& s, int seq_begin, int batch, const uint16_t* q, uint16_t* out,
-                             float qk_scale_log2, const AttnWork& w, const StepArgs& a, cudaStream_t st);
-cudaError_t launch_step_moves(const DevState& s, int batch, const StepArgs& a, int sm_count, cudaStream_t st);
+                             float qk_scale_log2, const AttnWork& w, const StepArgs& a, int sm_count,
+                             cudaStream_t st);
+// max_moves: an upper bound of any pair's move count (sizes the grid only)
+cudaError_t launch_step_moves(const DevState& s, int batch, const StepArgs& a, int sm_count, int max_moves,
+                              cudaStream_t st);
 int step_max_smem_bytes();  // dynamic shared memory of the post kernel (a multiple of 16)
 
 int attention_smem_bytes(int bits);

@@ -18,6 +18,8 @@
 //
 // (Technical Report: KV Cache Compression for Text-Only LLMs, sections 3.3
 // and 3.4; "KV Cache optimization techniques" sections 2.2, 2.4 and 3.2.)
+#include <algorithm>
+
 #include "kvc_device.h"
 #include "kvc_internal.h"
 
@@ -29,7 +31,10 @@ using namespace dev;
 constexpr int kStepThreads = 512;
 constexpr int kStepBtStage = 2048;
 
-__global__ void __launch_bounds__(kStepThreads, 2) step_post_kernel(DevState s, int seq_begin, int batch,
+// NT threads: 512 (two CTAs per SM) or, when the pairs are no more than the
+// SMs, 1024 (one pair per SM, twice the threads on its slots).
+template <int NT>
+__global__ void __launch_bounds__(NT, 1024 / NT) step_post_kernel(DevState s, int seq_begin, int batch,
                                                                 const uint16_t* __restrict__ q,
                                                                 uint16_t* __restrict__ out, float qk_scale_log2,
                                                                 AttnWork w, StepArgs a) {
@@ -167,14 +172,36 @@ __global__ void __launch_bounds__(kStepThreads, 2) step_post_kernel(DevState s, 
   // ---- selection: the n_keep largest keys, ties at the threshold to the
   // lower positions
   uint32_t theta = 0xFFFFFFFFu, pos_cut = 0xFFFFFFFFu;
-  if (n_keep > 0) {
+  if (n_keep > 0 && S - n_keep == 1) {
+    // one slot goes (the steady state): the least key, and among equal least
+    // keys the highest position, is the one the rule below evicts.  One
+    // block-wide minimum of (key, ~position); pool positions are >= 4.
+    __shared__ unsigned long long sh_min[32];
+    unsigned long long best = ~0ull;
+    for (int t = threadIdx.x; t < S; t += NT) {
+      const unsigned long long v = ((unsigned long long)keys[t] << 32) | (uint32_t)~(uint32_t)pos[t];
+      best = v < best ? v : best;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
+      best = y < best ? y : best;
+    }
+    if ((threadIdx.x & 31) == 0) sh_min[threadIdx.x >> 5] = best;
+    __syncthreads();
+    best = ~0ull;
+#pragma unroll
+    for (int j = 0; j < NT / 32; ++j) best = sh_min[j] < best ? sh_min[j] : best;
+    theta = (uint32_t)(best >> 32);
+    pos_cut = ~(uint32_t)best - 1u;  // every other slot with key theta sits lower
+  } else if (n_keep > 0) {
     int need, ties;
-    theta = radix_select<kStepThreads>(
+    theta = radix_select<NT>(
         S, n_keep, true, [&](int) { return true; }, [&](int i) { return keys[i]; }, hist, sh_warp, sh_sel, &need,
         &ties, /*pass0_ready=*/true);
     if (ties > need) {  // ties at theta: the lowest positions win
       int rem2, t2;
-      pos_cut = radix_select<kStepThreads>(
+      pos_cut = radix_select<NT>(
           S, need, false, [&](int i) { return keys[i] == theta; }, [&](int i) { return (uint32_t)pos[i]; },
           hist, sh_warp, sh_sel, &rem2, &t2);
     }
@@ -194,7 +221,7 @@ __global__ void __launch_bounds__(kStepThreads, 2) step_post_kernel(DevState s, 
   const uint32_t lt = (1u << lane) - 1u;
   const int wlo = keep_window(S, np);
   int hole_base = 0, src_base = 0;
-  for (int tile0 = 0; tile0 < S; tile0 += kStepThreads * 16) {
+  for (int tile0 = 0; tile0 < S; tile0 += NT * 16) {
     const int wbase = tile0 + warp * 512 + lane;
     uint32_t hole_bits = 0, src_bits = 0;
 #pragma unroll
@@ -213,7 +240,7 @@ __global__ void __launch_bounds__(kStepThreads, 2) step_post_kernel(DevState s, 
     __syncthreads();
     int before = 0, tot = 0;
 #pragma unroll
-    for (int j = 0; j < kStepThreads / 32; ++j) {
+    for (int j = 0; j < NT / 32; ++j) {
       const int v = sh_warp[j];
       before += j < warp ? v : 0;
       tot += v;
@@ -298,22 +325,35 @@ __global__ void __launch_bounds__(kStepThreads, 2) step_moves_kernel(DevState s,
 
 int step_max_smem_bytes() { return 160 * 1024; }
 
-cudaError_t launch_step_post(const DevState& s, int seq_begin, int batch, const uint16_t* q, uint16_t* out,
-                             float qk_scale_log2, const AttnWork& w, const StepArgs& a, cudaStream_t st) {
+template <int NT>
+cudaError_t launch_step_post_nt(const DevState& s, int seq_begin, int batch, const uint16_t* q, uint16_t* out,
+                                float qk_scale_log2, const AttnWork& w, const StepArgs& a, cudaStream_t st) {
   const int smem = a.smem_slots > 0 ? a.smem_slots * (a.pos_smem ? 8 : 4) : 0;
   if (smem > 0) {
     static int done[64] = {0};
-    const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(step_post_kernel), step_max_smem_bytes(), done);
+    const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(step_post_kernel<NT>), step_max_smem_bytes(), done);
     if (e != cudaSuccess) return e;
   }
   dim3 grid(s.hkv, batch);
-  step_post_kernel<<<grid, kStepThreads, smem, st>>>(s, seq_begin, batch, q, out, qk_scale_log2, w, a);
+  step_post_kernel<NT><<<grid, NT, smem, st>>>(s, seq_begin, batch, q, out, qk_scale_log2, w, a);
   return cudaGetLastError();
 }
 
-cudaError_t launch_step_moves(const DevState& s, int batch, const StepArgs& a, int sm_count, cudaStream_t st) {
+cudaError_t launch_step_post(const DevState& s, int seq_begin, int batch, const uint16_t* q, uint16_t* out,
+                             float qk_scale_log2, const AttnWork& w, const StepArgs& a, int sm_count,
+                             cudaStream_t st) {
+  if (batch * s.hkv <= sm_count)
+    return launch_step_post_nt<1024>(s, seq_begin, batch, q, out, qk_scale_log2, w, a, st);
+  return launch_step_post_nt<kStepThreads>(s, seq_begin, batch, q, out, qk_scale_log2, w, a, st);
+}
+
+cudaError_t launch_step_moves(const DevState& s, int batch, const StepArgs& a, int sm_count, int max_moves,
+                              cudaStream_t st) {
+  // with fewer pairs than SMs, up to two CTAs per SM in all, but no CTA with
+  // fewer than ~256 moves (at steady state a pair moves one row)
   const int pairs = batch * s.hkv;
-  const int z = pairs < sm_count ? (2 * sm_count + pairs - 1) / pairs : 1;
+  int z = pairs < sm_count ? (2 * sm_count + pairs - 1) / pairs : 1;
+  z = std::max(1, std::min(z, (max_moves + 255) / 256));
   dim3 grid(s.hkv, batch, z);
   step_moves_kernel<<<grid, kStepThreads, 0, st>>>(s, a);
   return cudaGetLastError();
