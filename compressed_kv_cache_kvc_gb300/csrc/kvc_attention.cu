@@ -76,9 +76,9 @@ __device__ __forceinline__ void copy_page(uint32_t sK, const uint8_t* kg, uint32
   if (BITS == 8) {
     asm volatile(
         "cp.async.cg.shared.global [%0], [%1], 16;\n"
-        "cp.async.cg.shared.global [%0+512], [%1+16], 16;\n"
+        "cp.async.cg.shared.global [%0+512], [%1+64], 16;\n"
         "cp.async.cg.shared.global [%0+1024], [%1+128], 16;\n"
-        "cp.async.cg.shared.global [%0+1536], [%1+144], 16;\n"
+        "cp.async.cg.shared.global [%0+1536], [%1+192], 16;\n"
         "cp.async.cg.shared.global [%2], [%3], 16;\n"
         "cp.async.cg.shared.global [%2+512], [%3+128], 16;\n"
         "cp.async.cg.shared.global [%2+1024], [%3+256], 16;\n"
@@ -187,7 +187,9 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
   // (global) and within a stage (shared); the chunks of one page sit at fixed
   // distances from these, so one asm block copies a page with immediates
   const uint32_t ring_s = smem_u32(smem) + warp * STAGES * Gm::kStage;
-  const uint32_t k_goff = BITS == 8 ? (2 * r) * 128 + 32 * c : (2 * r) * 64 + 16 * c;
+  // INT8: bytes 16c and 64 + 16c of rows 2r and 2r+1, so the 4 lanes of a
+  // row read whole 32-byte sectors in each copy instruction
+  const uint32_t k_goff = BITS == 8 ? (2 * r) * 128 + 16 * c : (2 * r) * 64 + 16 * c;
   const uint32_t v_goff = BITS == 8 ? (4 * c) * 128 + 16 * r : (4 * c) * 64 + 8 * r;
   const uint32_t k_soff = lane * 16;
   const uint32_t v_soff = Gm::kKBytes + (BITS == 8 ? lane * 16 : lane * 8);
@@ -219,11 +221,14 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
       float qv[32];
       const int g = r;
       if (g < G) {
-        const uint4* src =
-            reinterpret_cast<const uint4*>(q + ((size_t)bl * s.hq + h * G + g) * kHeadDim + 32 * c);
+        // the lane's 32 dims, in the order of its K codes: INT8 dims
+        // 16c..16c+15 and 64+16c..64+16c+15, INT4 dims 32c..32c+31
+        const uint16_t* qrow = q + ((size_t)bl * s.hq + h * G + g) * kHeadDim;
+        const uint4* src_a = reinterpret_cast<const uint4*>(qrow + (BITS == 8 ? 16 * c : 32 * c));
+        const uint4* src_b = reinterpret_cast<const uint4*>(qrow + (BITS == 8 ? 64 + 16 * c : 32 * c + 16));
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const uint4 u = src[i];
+          const uint4 u = i < 2 ? src_a[i] : src_b[i - 2];
           const uint32_t ws[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
