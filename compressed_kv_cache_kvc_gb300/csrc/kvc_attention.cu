@@ -58,7 +58,7 @@ struct Geom {
   static constexpr int kKBytes = BITS == 8 ? 2048 : 1024;
   static constexpr int kVBytes = BITS == 8 ? 2048 : 1024;
   static constexpr int kStage = kKBytes + kVBytes + 128;  // + 16 K scales + 16 V scales
-  static constexpr int kStages = BITS == 8 ? 3 : 4;
+  static constexpr int kStages = 4;  // INT8: 3 CTAs/SM by shared memory, INT4: 4
   static constexpr int kSmem = kWarps * kStages * kStage;
 };
 
