@@ -394,32 +394,73 @@ def gpu_arm(args):
     peak = float(peaks.get("hbm_gbs", 6800.0))
     achieved = attn_bytes / (attn_avg_ms * 1e-3) / 1e9
 
-    # e2e through the public API with host buffers: per step, H2D of every
-    # layer's query and new K/V from pinned memory, the step, D2H of outputs
-    h_in = [tuple(t.cpu().pin_memory() for t in inp) for inp in inputs]
-    h_out = [torch.empty(B, Hq, 128, dtype=torch.bfloat16).pin_memory() for _ in range(layers)]
-    d_in = [tuple(torch.empty_like(t) for t in inp) for inp in inputs]
-    h2d = sum(t.numel() * t.element_size() for inp in h_in for t in inp)
-    d2h = sum(t.numel() * t.element_size() for t in h_out)
-    e2e_ms = []
+    # e2e through the public API with host buffers: per step, the H2D copy of
+    # every layer's query and new K/V from pinned memory (all layers' inputs
+    # in one buffer, one copy), the step, the D2H copy of all outputs
+    shapes = [tuple(t.shape) for t in inputs[0]]
+    sizes = [math.prod(sh) for sh in shapes]
+    per_layer = sum(sizes)
+    h_in_all = torch.empty(layers * per_layer, dtype=torch.bfloat16).pin_memory()
+    d_in_all = torch.empty(layers * per_layer, dtype=torch.bfloat16, device=dev)
+    d_in = []
+    for l in range(layers):
+        off, views = l * per_layer, []
+        for t, sh, n in zip(inputs[l], shapes, sizes):
+            h_in_all[off:off + n].copy_(t.reshape(-1).cpu())
+            views.append(d_in_all[off:off + n].view(sh))
+            off += n
+        d_in.append(tuple(views))
+    d_out_all = torch.empty(layers, B, Hq, 128, dtype=torch.bfloat16, device=dev)
+    h_out_all = torch.empty(layers, B, Hq, 128, dtype=torch.bfloat16).pin_memory()
+    h2d = h_in_all.numel() * h_in_all.element_size()
+    d2h = h_out_all.numel() * h_out_all.element_size()
+
+    def e2e_step_calls():
+        d_in_all.copy_(h_in_all, non_blocking=True)
+        for l, c in enumerate(caches):
+            q, kn, vn = d_in[l]
+            c.decode_step(q, kn, vn, mode="h2o", budget=w.budget, recent=w.recent, out=d_out_all[l],
+                          workspace=ws_buf)
+        h_out_all.copy_(d_out_all, non_blocking=True)
+
     e_steps = max(1, min(args.steps, 10))
+    # (a) each call launched as the user makes it
+    e2e_eager_ms = []
     with torch.cuda.stream(stream):
         for _ in range(e_steps):
             restore()
             torch.cuda.synchronize()
             resync()
             ev0.record(stream)
-            for l, c in enumerate(caches):
-                for dst, src in zip(d_in[l], h_in[l]):
-                    dst.copy_(src, non_blocking=True)
-                q, kn, vn = d_in[l]
-                c.decode_step(q, kn, vn, mode="h2o", budget=w.budget, recent=w.recent, out=outs[l], workspace=ws_buf)
-                h_out[l].copy_(outs[l], non_blocking=True)
+            e2e_step_calls()
             ev1.record(stream)
             ev1.synchronize()
-            e2e_ms.append(ev0.elapsed_time(ev1))
+            e2e_eager_ms.append(ev0.elapsed_time(ev1))
+    # (b) the same calls captured once into a CUDA graph, as a serving loop
+    # would: every replay copies the pinned host inputs in and the outputs out
+    e2e_ms = []
+    if graph is not None:
+        restore()
+        torch.cuda.synchronize()
+        resync()
+        e2e_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(e2e_graph, stream=stream):
+            e2e_step_calls()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for _ in range(e_steps):
+                restore()
+                torch.cuda.synchronize()
+                ev0.record(stream)
+                e2e_graph.replay()
+                ev1.record(stream)
+                ev1.synchronize()
+                e2e_ms.append(ev0.elapsed_time(ev1))
+    else:
+        e2e_ms = e2e_eager_ms
     e2e_step = reduce_max(sum(e2e_ms), ws, dev) / e_steps
     e2e_value = kv_bytes * ws / (e2e_step * 1e-3) / 1e9
+    e2e_eager_step = reduce_max(sum(e2e_eager_ms), ws, dev) / e_steps
     for c in caches:
         st = c.read_status()
         if st:
@@ -461,7 +502,14 @@ def gpu_arm(args):
                      "avg_launch_ms": attn_avg_ms, "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)"},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_step, "path": "KVCache.decode_step per layer, eager, pinned host buffers"},
+                "ms_per_step": e2e_step,
+                "path": ("one H2D copy of all layers' inputs from pinned host memory, KVCache.decode_step "
+                         "per layer, one D2H copy of all outputs; captured once into a CUDA graph and "
+                         "replayed every step" if graph is not None else
+                         "one H2D copy of all layers' inputs, KVCache.decode_step per layer, one D2H "
+                         "copy of all outputs, eager"),
+                "eager": {"value": kv_bytes * ws / (e2e_eager_step * 1e-3) / 1e9, "ms_per_step": e2e_eager_step,
+                          "path": "the same calls launched one by one"}},
         "gpu_launches": launches * args.steps,
         "clocks": clocks,
     }
