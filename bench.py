@@ -560,11 +560,19 @@ def workload_report(args, name: str):
     torch.cuda.synchronize()  # the prefill ran on the default stream; the steps run on their own
     ws_buf = caches[0].workspace(B)
     outs = [torch.empty(B, Hq, 128, dtype=torch.bfloat16, device=dev) for _ in range(layers)]
+    budgets = [w.budget] * layers
+    if args.schedule and w.mode == "h2o":
+        from compressed_kv_cache_kvc_gb300.budgets import pyramid_budgets
+        if args.schedule == "linear":
+            budgets = pyramid_budgets(layers, "linear", recent=w.recent, base=w.budget)
+        else:
+            budgets = pyramid_budgets(layers, "quadratic", recent=w.recent, context=w.context,
+                                      base_ratio=w.budget / w.context)
 
     def step(stream=None):
         for l, c in enumerate(caches):
             q, kn, vn = inputs[l]
-            c.decode_step(q, kn, vn, mode=w.mode, budget=w.budget, recent=w.recent, window=w.window,
+            c.decode_step(q, kn, vn, mode=w.mode, budget=budgets[l], recent=w.recent, window=w.window,
                           out=outs[l], workspace=ws_buf, stream=stream)
 
     stream = torch.cuda.Stream(device=dev)
@@ -623,6 +631,8 @@ def workload_report(args, name: str):
     ms = float(np.median(step_ms))
     attn = float(np.median(attn_ms))
     line = {"workload": name, "layers": layers, "batch": B, "bits": w.bits, "mode": w.mode,
+            "budgets": ({"schedule": args.schedule, "first": budgets[0], "middle": budgets[layers // 2],
+                         "last": budgets[-1]} if args.schedule and w.mode == "h2o" else budgets[0]),
             "first_step": {"ms": ms, "kv_bytes": kv_bytes, "step_gbs": kv_bytes / (ms * 1e-3) / 1e9,
                            "step_frac_of_peak": kv_bytes / (ms * 1e-3) / 1e9 / peak,
                            "seq_steps_per_s": B / (ms * 1e-3),
@@ -667,6 +677,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=None,
                     help="report mode: time this workload (or 'all') instead of printing the bench line")
+    ap.add_argument("--schedule", default=None, choices=["linear", "quadratic"],
+                    help="report mode: per-layer H2O budgets (PyramidKV-style schedule)")
     ap.add_argument("--oracle-child", nargs=2, type=int, default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.oracle_child is not None:

@@ -147,3 +147,44 @@ def test_step_on_batch_slices(bits, hq, hkv):
                 for x, y in zip(before.head(b, h), after.head(b, h)):
                     assert np.array_equal(np.asarray(x).view(np.uint8), np.asarray(y).view(np.uint8)), (b, h)
     assert ca.read_status() == 0 and cb.read_status() == 0
+
+
+def test_step_with_pyramid_budgets():
+    """Per-layer budgets (the linear PyramidKV schedule) through the one-call
+    step: every layer keeps exactly its budget, the kept set the oracle's rule
+    gives for that budget."""
+    from compressed_kv_cache_kvc_gb300.budgets import pyramid_budgets
+    from compressed_kv_cache_kvc_gb300.cache import KVCache
+    rng = np.random.default_rng(5)
+    L, B, hq, hkv, T_, recent = 4, 2, 16, 4, 600, 32
+    budgets = pyramid_budgets(L, "linear", recent=recent, base=300)
+    assert budgets == [300, 240, 180, 119]  # 300 * (1 - 0.8 * 3/4) = 119.99999999999997 in floating point
+    mbps = (T_ + 1 + 15) // 16 + 2
+    f = O.bf16_bits_to_f32
+    for budget in budgets:
+        c = KVCache(hq, hkv, 8, B * mbps, B, mbps)
+        k = _bits(rng, (B, hkv, T_, 128))
+        v = _bits(rng, (B, hkv, T_, 128))
+        q = _bits(rng, (B, hq, 128))
+        kn = _bits(rng, (B, hkv, 1, 128))
+        vn = _bits(rng, (B, hkv, 1, 128))
+        c.quantize_append(T.to_dev_bf16(k), T.to_dev_bf16(v))
+        out = c.decode_step(T.to_dev_bf16(q), T.to_dev_bf16(kn), T.to_dev_bf16(vn), mode="h2o", budget=budget,
+                            recent=recent)
+        gpu = T.bf16_tensor_to_f32(out)
+        st = T.StateView(c)
+        for b in range(B):
+            ora = O.OracleCache(1, hq, hkv, 8)
+            ora.append(0, f(k[b]), f(v[b]))
+            ora.append(0, f(kn[b]), f(vn[b]))
+            ref = ora.attend(0, f(q[b]), T.sm_scale())
+            T.assert_attention_close(gpu[b], ref, f"budget {budget} b={b}")
+            masks = ora.keep_masks(0, "h2o", budget=budget, recent=recent)
+            for h in range(hkv):
+                hs = ora.seqs[0].heads[h]
+                kept_gpu = set(st.head(b, h)[0].tolist())
+                assert len(kept_gpu) == budget - 4
+                assert T.kept_sets_agree(kept_gpu, set(hs.pos[masks[h]].tolist()), hs.pos, hs.score,
+                                         budget - 4 - recent, T_ + 1 - recent), (budget, b, h)
+            assert c.lengths(b) == (budget - 4, T_ + 1)
+        assert c.read_status() == 0
