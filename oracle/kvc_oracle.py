@@ -28,6 +28,9 @@ What it computes, step by step, each citing the page passage it restates:
   the recent window, and the top-k of the remaining tokens by accumulated
   score, ties to the lower position (Technical Report sections 3.3-3.4,
   "KV Cache optimization techniques" sections 2.2 and 2.4).
+* ``select_blocks`` -- block-granular eviction (the eviction-and-reuse survey
+  page, section 4, the block manager's eviction by attention): blocks sorted
+  by their mean attention score, the lowest int(n * (1 - ratio)) evicted.
 
 Readings where the pages are silent or disagree are listed in the design doc; the
 ones that change arithmetic are restated beside the function they affect.
@@ -45,6 +48,7 @@ import numpy as np
 
 HEAD_DIM = 128
 NUM_SINK = 4
+PAGE = 16  # tokens per block of the paged pool
 
 
 # ---------------------------------------------------------------------------
@@ -242,6 +246,38 @@ def select_streaming(pos: np.ndarray, pos_total: int, window: int,
     return pos >= pos_total - window
 
 
+def select_blocks(scores: list, n_slots: int, recent: int, retention: float) -> np.ndarray:
+    """Block-granular eviction (the eviction-and-reuse survey page, section 4:
+    the block manager's eviction by attention sorts the blocks by the mean
+    attention score of their tokens and evicts the first int(len * (1 -
+    ratio)) of them).
+
+    The pool of one sequence, in slot order, is cut into blocks of PAGE slots;
+    all KV heads share a block, so a block's score covers its PAGE slots of
+    every head.  Readings: the candidates are the full blocks that lie before
+    the last ``recent`` slots (the recent window and the unfilled last block
+    always stay; the sinks are not in the pool); a block is ordered by the
+    sum of its PAGE x Hkv scores, accumulated in fp64 head by head and slot by
+    slot (the sum orders blocks exactly as the mean does); ties go to the
+    earlier block, as a stable sort leaves them.  ``scores`` holds one score
+    array per KV head, in slot order.  Returns the keep mask over the
+    ``n_slots`` slots, the same for every head."""
+    n_cand = max(0, n_slots - recent) // PAGE
+    n_evict = int(n_cand * (1.0 - retention))
+    sums = []
+    for p in range(n_cand):
+        acc = 0.0
+        for sc in scores:
+            for t in range(p * PAGE, (p + 1) * PAGE):
+                acc += float(sc[t])
+        sums.append(acc)
+    order = sorted(range(n_cand), key=lambda p: (sums[p], p))
+    keep = np.ones(n_slots, dtype=bool)
+    for p in order[:n_evict]:
+        keep[p * PAGE:(p + 1) * PAGE] = False
+    return keep
+
+
 # ---------------------------------------------------------------------------
 # Dense per-(sequence, KV head) cache that runs the decode step
 # ---------------------------------------------------------------------------
@@ -353,8 +389,12 @@ class OracleCache:
 
     # -- eviction -----------------------------------------------------------
     def keep_masks(self, b: int, mode: str, budget: int = 0, recent: int = 0,
-                   window: int = 0) -> list:
+                   window: int = 0, retention: float = 1.0) -> list:
         s = self.seqs[b]
+        if mode == "block":
+            # slot order is insertion order while only whole blocks are evicted
+            keep = select_blocks([hs.score for hs in s.heads], s.heads[0].pos.shape[0], recent, retention)
+            return [keep.copy() for _ in range(self.hkv)]
         masks = []
         for h in range(self.hkv):
             hs = s.heads[h]

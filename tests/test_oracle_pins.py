@@ -374,3 +374,60 @@ def test_planted_heavy_hitters_kept_tiny_workload():
         assert len(kept) == w.budget - 4
         planted = set(np.nonzero(d["planted"][0, h])[0].tolist())
         assert planted and planted <= kept | set(range(p_total - w.recent, p_total))
+
+
+# ---------------------------------------------------------------------------
+# block-granular eviction (the survey page's block manager)
+# ---------------------------------------------------------------------------
+
+def _block_scores(block_sums, hkv=2, extra=0):
+    """Per-head score arrays whose block sums (over heads and slots) are the
+    given values: the whole sum sits on slot 0 of head 0."""
+    n = len(block_sums) * 16 + extra
+    sc = [np.zeros(n) for _ in range(hkv)]
+    for p, v in enumerate(block_sums):
+        sc[0][16 * p] = v
+    return sc
+
+
+def test_blocks_worked_example_with_a_tie():
+    # 100 slots, recent 20: candidates are the 5 full blocks before slot 80;
+    # retention 0.4 evicts int(5 * 0.6) = 3 of them: sums 5, 1, 4, 1, 9 ->
+    # blocks 1 and 3 (tie at 1, earlier first), then block 2
+    sc = _block_scores([5.0, 1.0, 4.0, 1.0, 9.0], extra=20)
+    keep = O.select_blocks(sc, 100, recent=20, retention=0.4)
+    want = np.ones(100, dtype=bool)
+    want[16:64] = False
+    assert np.array_equal(keep, want)
+
+
+def test_blocks_edges():
+    sc = _block_scores([3.0, 2.0, 1.0], extra=7)  # 55 slots
+    assert O.select_blocks(sc, 55, recent=7, retention=1.0).all()          # keep everything
+    assert O.select_blocks(sc, 55, recent=60, retention=0.1).all()         # no candidate
+    keep = O.select_blocks(sc, 55, recent=7, retention=1e-9)                # int(3 * (1 - 1e-9)) = 2
+    assert np.array_equal(np.nonzero(~keep)[0], np.arange(16, 48))         # blocks 2 and 1 go
+    keep = O.select_blocks(sc, 55, recent=8, retention=0.5)                 # 47 slots -> 2 candidates, evict 1
+    assert np.array_equal(np.nonzero(~keep)[0], np.arange(16, 32))
+
+
+def test_blocks_against_numpy_means():
+    rng = np.random.default_rng(8)
+    for trial in range(20):
+        hkv = int(rng.integers(1, 5))
+        n_slots = int(rng.integers(1, 300))
+        recent = int(rng.integers(0, 80))
+        retention = float(rng.uniform(0.05, 1.0))
+        sc = [rng.random(n_slots) for _ in range(hkv)]
+        keep = O.select_blocks(sc, n_slots, recent, retention)
+        n_cand = max(0, n_slots - recent) // 16
+        n_evict = int(n_cand * (1.0 - retention))
+        means = np.array([np.mean([s[16 * p:16 * p + 16] for s in sc]) for p in range(n_cand)])
+        lowest = np.argsort(means, kind="stable")[:n_evict]
+        want = np.ones(n_slots, dtype=bool)
+        for p in lowest:
+            want[16 * p:16 * p + 16] = False
+        assert np.array_equal(keep, want), trial
+        # whole blocks only, never the recent window or the unfilled last block
+        assert (~keep).sum() == 16 * n_evict
+        assert keep[16 * n_cand:].all()
