@@ -19,6 +19,7 @@ KVC_ERR_STATE = 6
 KVC_ATTN_ACCUM_H2O = 0x1
 KVC_EVICT_H2O = 0
 KVC_EVICT_STREAMING = 1
+KVC_EVICT_BLOCK = 2
 KVC_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 BUF = dict(K_CODES=0, V_CODES=1, K_SCALE=2, V_SCALE=3, SLOT_POS=4, SCORE=5, SINK_K=6, SINK_V=7,
@@ -34,7 +35,7 @@ class KvcConfig(ctypes.Structure):
 
 class KvcEvictParams(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int32), ("budget", ctypes.c_int32), ("recent", ctypes.c_int32),
-                ("window", ctypes.c_int32)]
+                ("window", ctypes.c_int32), ("retention", ctypes.c_double)]
 
 
 class KvcError(RuntimeError):

@@ -153,9 +153,11 @@ class KVCache:
 
     def h2o_select_evict(self, batch: int, mode: str = "h2o", budget: int = 0, recent: int = 0,
                          window: int = 0, seq_begin: int = 0, keep_mask=None, workspace=None,
-                         stream=None) -> torch.Tensor:
-        m = {"h2o": L.KVC_EVICT_H2O, "streaming": L.KVC_EVICT_STREAMING}[mode]
-        params = L.KvcEvictParams(m, budget, recent, window)
+                         stream=None, retention: float = 1.0) -> torch.Tensor:
+        """mode "h2o", "streaming" or "block" (whole pages by mean H2O score;
+        `retention` = fraction of the candidate pages kept)."""
+        m = {"h2o": L.KVC_EVICT_H2O, "streaming": L.KVC_EVICT_STREAMING, "block": L.KVC_EVICT_BLOCK}[mode]
+        params = L.KvcEvictParams(m, budget, recent, window, retention)
         mask = self.new_keep_mask(batch) if keep_mask is None else keep_mask
         _need(mask, torch.uint8, "keep_mask")
         ws = self.workspace(batch) if workspace is None else workspace
@@ -192,7 +194,7 @@ class KVCache:
         ws = self.workspace(batch) if workspace is None else workspace
         scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
         m = {"h2o": L.KVC_EVICT_H2O, "streaming": L.KVC_EVICT_STREAMING}[mode]
-        params = L.KvcEvictParams(m, budget, recent, window)
+        params = L.KvcEvictParams(m, budget, recent, window, 1.0)
         L.check(self.lib.kvc_decode_step(self.handle, seq_begin, batch, ctypes.c_void_p(q.data_ptr()),
                                          ctypes.c_void_p(k_new.data_ptr()), ctypes.c_void_p(v_new.data_ptr()),
                                          ctypes.c_void_p(out.data_ptr()), ctypes.c_float(scale), ctypes.byref(params),

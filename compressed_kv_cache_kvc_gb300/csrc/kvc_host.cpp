@@ -88,6 +88,7 @@ struct kvc_cache {
   std::vector<int32_t> pos;    // host mirror: positions seen per sequence
   // pending selection (kvc_h2o_select_evict -> kvc_compact_blocks)
   bool plan_pending = false;
+  bool plan_block = false;  // the pending plan drops whole pages
   int32_t plan_begin = 0, plan_batch = 0;
   std::vector<int32_t> plan_new;
   void* trace_start = nullptr;
@@ -234,6 +235,8 @@ kvc_status evict_check(const kvc_evict_params* p) {
     if (p->recent < 0 || p->budget < kvc::kSinks + p->recent) return KVC_ERR_INVALID_ARG;
   } else if (p->mode == KVC_EVICT_STREAMING) {
     if (p->window < 1) return KVC_ERR_INVALID_ARG;
+  } else if (p->mode == KVC_EVICT_BLOCK) {
+    if (p->recent < 0 || !(p->retention > 0.0 && p->retention <= 1.0)) return KVC_ERR_INVALID_ARG;
   } else {
     return KVC_ERR_INVALID_ARG;
   }
@@ -243,6 +246,12 @@ kvc_status evict_check(const kvc_evict_params* p) {
 int plan_keep(const kvc_evict_params* p, int S, int P) {
   const int ns = std::min(P, kvc::kSinks);
   if (p->mode == KVC_EVICT_H2O) return (ns + S <= p->budget) ? S : p->budget - kvc::kSinks;
+  if (p->mode == KVC_EVICT_BLOCK) {
+    // the device computes the same double expression
+    const int n_cand = std::max(0, S - p->recent) / kvc::kPage;
+    const int n_evict = (int)((double)n_cand * (1.0 - p->retention));
+    return S - kvc::kPage * n_evict;
+  }
   return (S <= p->window) ? S : p->window;
 }
 
@@ -454,6 +463,19 @@ kvc_status kvc_h2o_select_evict(kvc_cache* c, int32_t seq_begin, int32_t batch, 
     plan[i] = plan_keep(p, S, c->pos[b]);
     max_s = std::max(max_s, S);
   }
+  if (p->mode == KVC_EVICT_BLOCK) {
+    if (c->cfg.max_blocks_per_seq > kvc::kMaxBlockPages) return KVC_ERR_UNSUPPORTED;
+    if (kvc::launch_select_blocks(c->dev, seq_begin, batch, p->recent, p->retention, d_keep_mask, s_cap(c),
+                                  static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return KVC_ERR_CUDA;
+    c->last_launches = 1;
+    c->plan_pending = true;
+    c->plan_block = true;
+    c->plan_begin = seq_begin;
+    c->plan_batch = batch;
+    c->plan_new = plan;
+    return KVC_OK;
+  }
   uint8_t* ws = static_cast<uint8_t*>(d_workspace);
   kvc::SelectArgs a{};
   a.mode = p->mode;
@@ -469,6 +491,7 @@ kvc_status kvc_h2o_select_evict(kvc_cache* c, int32_t seq_begin, int32_t batch, 
     return KVC_ERR_CUDA;
   c->last_launches = 1;
   c->plan_pending = true;
+  c->plan_block = false;
   c->plan_begin = seq_begin;
   c->plan_batch = batch;
   c->plan_new = plan;
@@ -484,6 +507,16 @@ kvc_status kvc_compact_blocks(kvc_cache* c, int32_t seq_begin, int32_t batch, co
   const WsLayout wl = ws_layout(c, batch);
   if (!d_workspace || !aligned(d_workspace, kAlign) || workspace_bytes < wl.total) return KVC_ERR_INVALID_ARG;
   if (!aligned(d_keep_mask, 16)) return KVC_ERR_INVALID_ARG;
+  if (c->plan_block) {
+    // block-granular plan: the row drops the pages, nothing moves
+    if (kvc::launch_release_blocks(c->dev, seq_begin, batch, d_keep_mask, s_cap(c),
+                                   static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return KVC_ERR_CUDA;
+    c->last_launches = 1;
+    for (int i = 0; i < batch; ++i) c->slots[seq_begin + i] = c->plan_new[i];
+    c->plan_pending = false;
+    return KVC_OK;
+  }
   uint8_t* ws = static_cast<uint8_t*>(d_workspace);
   // largest move count of the slice: min(kept, evicted) per sequence
   int max_moves = 0;
@@ -508,6 +541,7 @@ kvc_status kvc_decode_step(kvc_cache* c, int32_t seq_begin, int32_t batch, const
   if (!c) return KVC_ERR_INVALID_ARG;
   c->last_launches = 0;
   if (evict_check(params) != KVC_OK) return KVC_ERR_INVALID_ARG;
+  if (params->mode == KVC_EVICT_BLOCK) return KVC_ERR_UNSUPPORTED;  // separate calls only
   kvc_status st0 =
       attention_check(c, seq_begin, batch, d_q, d_out, sm_scale, d_workspace, workspace_bytes, /*appended=*/1);
   if (st0 != KVC_OK) return st0;

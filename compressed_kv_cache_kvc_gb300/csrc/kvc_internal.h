@@ -94,12 +94,20 @@ struct SelectArgs {
   int mode, budget, recent, window;
   int s_cap;            // mask row stride
   int smem_slots;       // > 0: keys/pos staged in shared memory (capacity in slots)
-  uint32_t* g_keys;     // global fallback [batch][hkv][s_cap]; then the hole list
-  int32_t* g_pos;       // likewise; then the source list
-  int* n_moves;         // [batch][hkv] list lengths (post kernel -> move kernel)
+  uint32_t* g_keys;     // global fallback [batch][hkv][s_cap]
+  int32_t* g_pos;
 };
 cudaError_t launch_select(const DevState& s, int seq_begin, int batch, const SelectArgs& a,
                           uint8_t* keep_mask, cudaStream_t st);
+
+// Block-granular eviction: the keep mask and plan of whole pages (select), and
+// the block-table rewrite that drops them (release).  At most
+// kMaxBlockPages pages per sequence.
+constexpr int kMaxBlockPages = 4096;
+cudaError_t launch_select_blocks(const DevState& s, int seq_begin, int batch, int recent, double retention,
+                                 uint8_t* keep_mask, int s_cap, cudaStream_t st);
+cudaError_t launch_release_blocks(const DevState& s, int seq_begin, int batch, const uint8_t* keep_mask,
+                                  int s_cap, cudaStream_t st);
 // g_holes / g_srcs: [batch][hkv][s_cap] move lists in the workspace, used when
 // smem_moves == 0; otherwise both lists (smem_moves entries each) live in
 // shared memory.

@@ -252,6 +252,136 @@ __global__ void __launch_bounds__(256) release_kernel(DevState s, int seq_begin)
   if (p0 > 0) shift_row(row, p0, keep_pages);
 }
 
+// Block-granular eviction (the eviction-and-reuse survey page, section 4:
+// the block manager's eviction by attention sorts blocks by the mean
+// attention score of their tokens and evicts the first int(n * (1 - ratio))).
+// A block is one page of the sequence, shared by every KV head; the
+// candidates are the full pages before the last `recent` slots; a page is
+// ordered by the fp64 sum of its 16 x Hkv scores, added head by head and slot
+// by slot (the sum orders pages as the mean does); ties go to the earlier
+// page.  One CTA per sequence: the plan, then the keep mask of every head
+// (all heads the same).  The lowest pages are found by radix select on the
+// sum's bit pattern (sums are >= 0, so their bits order like their values):
+// the high word, then the low word among equal high words, then the page
+// index among equal sums.
+constexpr int kBlockThreads = 256;
+
+__global__ void __launch_bounds__(kBlockThreads) block_select_kernel(DevState s, int seq_begin, int recent,
+                                                                     double retention, uint8_t* __restrict__ mask,
+                                                                     int s_cap) {
+  __shared__ unsigned long long key[kMaxBlockPages];
+  __shared__ int hist[kRadixBins];
+  __shared__ int sh_sel[3];
+  __shared__ int sh_warp[32];
+  const int bl = blockIdx.x;
+  const int b = seq_begin + bl;
+  const int S = s.seq_slots[b];
+  const int hkv = s.hkv;
+  const int n_cand = max(0, S - recent) / kPage;
+  const int n_evict = (int)((double)n_cand * (1.0 - retention));
+  if (threadIdx.x == 0) {
+    s.plan[2 * b] = S;
+    s.plan[2 * b + 1] = S - kPage * n_evict;
+  }
+  const int32_t* bt = s.block_table + (size_t)b * s.max_bps;
+  for (int p = threadIdx.x; p < n_cand; p += blockDim.x) {
+    const int blk = bt[p];
+    double acc = 0.0;
+    if ((unsigned)blk < (unsigned)s.num_blocks) {
+      const float* sc = s.score + (size_t)blk * hkv * kPage;
+      for (int i = 0; i < hkv * kPage; ++i) acc += (double)sc[i];  // head by head, slot by slot
+    } else {
+      atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
+    }
+    key[p] = (unsigned long long)__double_as_longlong(acc);
+  }
+  __syncthreads();
+  unsigned long long theta = 0;
+  uint32_t idx_cut = 0;
+  bool any = n_evict > 0;
+  if (any) {
+    int need, ties;
+    const uint32_t hi = radix_select<kBlockThreads>(
+        n_cand, n_evict, false, [&](int) { return true; }, [&](int i) { return (uint32_t)(key[i] >> 32); },
+        hist, sh_warp, sh_sel, &need, &ties);
+    int need2, ties2;
+    const uint32_t lo = radix_select<kBlockThreads>(
+        n_cand, need, false, [&](int i) { return (uint32_t)(key[i] >> 32) == hi; },
+        [&](int i) { return (uint32_t)key[i]; }, hist, sh_warp, sh_sel, &need2, &ties2);
+    theta = ((unsigned long long)hi << 32) | lo;
+    int r3, t3;
+    idx_cut = radix_select<kBlockThreads>(
+        n_cand, need2, false, [&](int i) { return key[i] == theta; }, [&](int i) { return (uint32_t)i; }, hist,
+        sh_warp, sh_sel, &r3, &t3);
+  }
+  // keep mask of every head: a slot goes when its page goes
+  for (int h = 0; h < hkv; ++h) {
+    uint8_t* mrow = mask + ((size_t)bl * hkv + h) * s_cap;
+    for (int t = threadIdx.x; t < S; t += blockDim.x) {
+      const int p = t / kPage;
+      bool gone = false;
+      if (any && p < n_cand) gone = key[p] < theta || (key[p] == theta && (uint32_t)p <= idx_cut);
+      mrow[t] = gone ? 0 : 1;
+    }
+  }
+}
+
+// The block-table rewrite of block-granular eviction (one CTA per sequence):
+// the pages whose slots the mask drops (head 0's row; every head's is the
+// same) leave the row, the others keep their order, the dropped pages go to
+// the free stack and the sequence holds S - 16 * dropped slots.  Nothing
+// moves in the pool.
+__global__ void __launch_bounds__(kBlockThreads) block_release_kernel(DevState s, int seq_begin,
+                                                                      const uint8_t* __restrict__ mask,
+                                                                      int s_cap) {
+  __shared__ int32_t row_in[kMaxBlockPages];
+  __shared__ int sh_warp[32];
+  __shared__ int sh_base;
+  const int bl = blockIdx.x;
+  const int b = seq_begin + bl;
+  const int S = s.plan[2 * b];
+  const int np = s.plan[2 * b + 1];
+  if (np >= S) return;
+  const int npages = (S + kPage - 1) / kPage;
+  int32_t* row = s.block_table + (size_t)b * s.max_bps;
+  const uint8_t* m0 = mask + (size_t)bl * s.hkv * s_cap;  // head 0
+  for (int p = threadIdx.x; p < npages; p += blockDim.x) row_in[p] = row[p];
+  __syncthreads();
+  // ranks of kept and dropped pages, chunk by chunk
+  int kept_base = 0, drop_base = 0;
+  const int n_drop = (S - np) / kPage;
+  if (threadIdx.x == 0) {
+    int base = -1;
+    if (n_drop > 0) {
+      base = atomicAdd(&s.counters[kCtrFreeTop], n_drop);
+      if (base + n_drop > s.num_blocks) {
+        atomicSub(&s.counters[kCtrFreeTop], n_drop);
+        atomicOr(&s.counters[kCtrStatus], kDevStackOverflow);
+        base = -1;
+      }
+    }
+    sh_base = base;
+  }
+  for (int c0 = 0; c0 < npages; c0 += kBlockThreads) {
+    const int p = c0 + (int)threadIdx.x;
+    const bool valid = p < npages;
+    const bool keep = valid && m0[p * kPage] != 0;
+    const bool drop = valid && !keep;
+    int tot;
+    const int incl = block_scan<kBlockThreads>((keep ? 1 : 0) | (drop ? 1 << 16 : 0), sh_warp, &tot);
+    const int k_rank = kept_base + (incl & 0xFFFF) - (keep ? 1 : 0);
+    const int d_rank = drop_base + (incl >> 16) - (drop ? 1 : 0);
+    if (keep) row[k_rank] = row_in[p];
+    if (drop && sh_base >= 0 && d_rank < n_drop) s.free_stack[sh_base + d_rank] = row_in[p];
+    kept_base += tot & 0xFFFF;
+    drop_base += tot >> 16;
+  }
+  if (threadIdx.x == 0) {
+    if (drop_base != n_drop) atomicOr(&s.counters[kCtrStatus], kDevBadKeepMask);
+    s.seq_slots[b] = np;
+  }
+}
+
 }  // namespace
 
 int select_max_smem_slots() { return (200 * 1024) / 8; }
@@ -284,6 +414,18 @@ cudaError_t launch_compact(const DevState& s, int seq_begin, int batch, const ui
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   release_kernel<<<batch, 256, 0, st>>>(s, seq_begin);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_select_blocks(const DevState& s, int seq_begin, int batch, int recent, double retention,
+                                 uint8_t* keep_mask, int s_cap, cudaStream_t st) {
+  block_select_kernel<<<batch, kBlockThreads, 0, st>>>(s, seq_begin, recent, retention, keep_mask, s_cap);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_release_blocks(const DevState& s, int seq_begin, int batch, const uint8_t* keep_mask,
+                                  int s_cap, cudaStream_t st) {
+  block_release_kernel<<<batch, kBlockThreads, 0, st>>>(s, seq_begin, keep_mask, s_cap);
   return cudaGetLastError();
 }
 

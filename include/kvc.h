@@ -113,12 +113,15 @@ typedef enum {
 /* Eviction modes of kvc_h2o_select_evict. */
 #define KVC_EVICT_H2O       0
 #define KVC_EVICT_STREAMING 1
+#define KVC_EVICT_BLOCK     2  /* whole pages by mean H2O score (separate calls only) */
 
 typedef struct {
-  int32_t mode;    /* KVC_EVICT_H2O or KVC_EVICT_STREAMING                      */
-  int32_t budget;  /* H2O: tokens kept including the 4 sinks; >= 4 + recent    */
-  int32_t recent;  /* H2O: recent window kept unconditionally                  */
-  int32_t window;  /* StreamingLLM: recent window (sinks kept besides it)      */
+  int32_t mode;      /* KVC_EVICT_H2O, KVC_EVICT_STREAMING or KVC_EVICT_BLOCK   */
+  int32_t budget;    /* H2O: tokens kept including the 4 sinks; >= 4 + recent  */
+  int32_t recent;    /* H2O: recent window kept unconditionally; BLOCK: the    */
+                     /* last `recent` pool slots are never evicted             */
+  int32_t window;    /* StreamingLLM: recent window (sinks kept besides it)    */
+  double retention;  /* BLOCK: fraction of candidate pages kept, (0, 1]        */
 } kvc_evict_params;
 
 /* ---------------------------------------------------------------- set-up -- */
@@ -201,6 +204,22 @@ kvc_status kvc_decode_attention(kvc_cache* cache, int32_t seq_begin, int32_t bat
 kvc_status kvc_h2o_select_evict(kvc_cache* cache, int32_t seq_begin, int32_t batch,
                                 const kvc_evict_params* params, uint8_t* d_keep_mask,
                                 void* d_workspace, size_t workspace_bytes, void* stream);
+
+/* Block-granular eviction, KVC_EVICT_BLOCK (the eviction-and-reuse survey
+ * page, section 4: blocks sorted by the mean attention score of their tokens,
+ * the lowest int(n * (1 - ratio)) evicted).  A block is one page (16 slots)
+ * of the sequence, shared by all KV heads.  The candidates are the n full
+ * pages before the last `recent` pool slots; they are ordered by the sum, in
+ * fp64 head by head and slot by slot, of their 16 x Hkv H2O scores (the sum
+ * orders pages as the mean does), ties to the earlier page; the first
+ * int(n * (1 - retention)) go.  kvc_h2o_select_evict writes the keep mask
+ * (a page's slots all alike, every head alike) and the plan
+ * S - 16 * evicted; kvc_compact_blocks then drops those pages from the
+ * sequence's block-table row (the others keep their order), returns them to
+ * the free stack and moves nothing in the pool.  The scores are what the
+ * attention with KVC_ATTN_ACCUM_H2O accumulated.  At most 4096 pages per
+ * sequence (max_blocks_per_seq), else KVC_ERR_UNSUPPORTED; kvc_decode_step
+ * returns KVC_ERR_UNSUPPORTED for this mode. */
 
 /* Compaction ("KV Cache optimization techniques" 2.2: gather the kept tokens;
  * 3.2: release blocks).  With S slots and n' < S kept, the kept slots are

@@ -139,11 +139,18 @@ def test_call_validation_before_any_launch(lib):
     # eviction parameters
     mask = dummy
     bad = [lib.KvcEvictParams(0, 10, 8, 0), lib.KvcEvictParams(0, 10, -1, 0), lib.KvcEvictParams(1, 0, 0, 0),
-           lib.KvcEvictParams(7, 100, 0, 0)]
+           lib.KvcEvictParams(7, 100, 0, 0),
+           # block-granular: retention in (0, 1], recent >= 0
+           lib.KvcEvictParams(2, 0, 8, 0, 0.0), lib.KvcEvictParams(2, 0, 8, 0, 1.5),
+           lib.KvcEvictParams(2, 0, -1, 0, 0.5), lib.KvcEvictParams(2, 0, 8, 0, float("nan"))]
     for prm in bad:
         assert L.kvc_h2o_select_evict(h, 0, 1, ctypes.byref(prm), mask, wsp, ws, None) == lib.KVC_ERR_INVALID_ARG
     # compaction needs a pending selection
     assert L.kvc_compact_blocks(h, 0, 1, mask, wsp, ws, None) == lib.KVC_ERR_STATE
+    # block-granular eviction is for the separate calls only
+    blk = lib.KvcEvictParams(2, 0, 8, 0, 0.5)
+    assert L.kvc_decode_step(h, 0, 1, dummy, dummy, dummy, dummy, ctypes.c_float(0.088), ctypes.byref(blk), wsp, ws,
+                             None) == lib.KVC_ERR_UNSUPPORTED
     # tracing events come in pairs
     assert L.kvc_set_trace_events(h, dummy, None) == lib.KVC_ERR_INVALID_ARG
     assert L.kvc_set_trace_events(h, None, None) == lib.KVC_OK
