@@ -572,8 +572,12 @@ def workload_report(args, name: str):
     def step(stream=None):
         for l, c in enumerate(caches):
             q, kn, vn = inputs[l]
-            c.decode_step(q, kn, vn, mode=w.mode, budget=budgets[l], recent=w.recent, window=w.window,
-                          out=outs[l], workspace=ws_buf, stream=stream)
+            if args.evict == "block":
+                c.decode_step(q, kn, vn, mode="block", recent=w.recent, retention=args.retention,
+                              out=outs[l], workspace=ws_buf, stream=stream)
+            else:
+                c.decode_step(q, kn, vn, mode=w.mode, budget=budgets[l], recent=w.recent, window=w.window,
+                              out=outs[l], workspace=ws_buf, stream=stream)
 
     stream = torch.cuda.Stream(device=dev)
     if w.mode == "streaming":
@@ -630,7 +634,8 @@ def workload_report(args, name: str):
     peak = float(peaks.get("hbm_gbs", 6800.0))
     ms = float(np.median(step_ms))
     attn = float(np.median(attn_ms))
-    line = {"workload": name, "layers": layers, "batch": B, "bits": w.bits, "mode": w.mode,
+    line = {"workload": name, "layers": layers, "batch": B, "bits": w.bits,
+            "mode": ("block, retention %g" % args.retention) if args.evict == "block" else w.mode,
             "budgets": ({"schedule": args.schedule, "first": budgets[0], "middle": budgets[layers // 2],
                          "last": budgets[-1]} if args.schedule and w.mode == "h2o" else budgets[0]),
             "first_step": {"ms": ms, "kv_bytes": kv_bytes, "step_gbs": kv_bytes / (ms * 1e-3) / 1e9,
@@ -679,6 +684,9 @@ def main():
                     help="report mode: time this workload (or 'all') instead of printing the bench line")
     ap.add_argument("--schedule", default=None, choices=["linear", "quadratic"],
                     help="report mode: per-layer H2O budgets (PyramidKV-style schedule)")
+    ap.add_argument("--evict", default=None, choices=["block"],
+                    help="report mode: block-granular eviction instead of the workload's mode")
+    ap.add_argument("--retention", type=float, default=0.25, help="report mode, --evict block: pages kept")
     ap.add_argument("--oracle-child", nargs=2, type=int, default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.oracle_child is not None:

@@ -177,9 +177,11 @@ class KVCache:
 
     def decode_step(self, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, mode: str = "h2o",
                     budget: int = 0, recent: int = 0, window: int = 0, seq_begin: int = 0, out=None,
-                    sm_scale: float | None = None, workspace=None, stream=None) -> torch.Tensor:
+                    sm_scale: float | None = None, workspace=None, stream=None,
+                    retention: float = 1.0) -> torch.Tensor:
         """The whole decode step of this layer in one library call (append one
-        token, attention, selection, compaction); same results as `step`."""
+        token, attention, selection, compaction); same results as `step`.
+        mode "h2o", "streaming" or "block" (see `h2o_select_evict`)."""
         _need(q, torch.bfloat16, "q")
         _need(k_new, torch.bfloat16, "k_new")
         _need(v_new, torch.bfloat16, "v_new")
@@ -193,8 +195,8 @@ class KVCache:
         _need(out, torch.bfloat16, "out")
         ws = self.workspace(batch) if workspace is None else workspace
         scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
-        m = {"h2o": L.KVC_EVICT_H2O, "streaming": L.KVC_EVICT_STREAMING}[mode]
-        params = L.KvcEvictParams(m, budget, recent, window, 1.0)
+        m = {"h2o": L.KVC_EVICT_H2O, "streaming": L.KVC_EVICT_STREAMING, "block": L.KVC_EVICT_BLOCK}[mode]
+        params = L.KvcEvictParams(m, budget, recent, window, retention)
         L.check(self.lib.kvc_decode_step(self.handle, seq_begin, batch, ctypes.c_void_p(q.data_ptr()),
                                          ctypes.c_void_p(k_new.data_ptr()), ctypes.c_void_p(v_new.data_ptr()),
                                          ctypes.c_void_p(out.data_ptr()), ctypes.c_float(scale), ctypes.byref(params),
@@ -203,12 +205,13 @@ class KVCache:
         return out
 
     def step(self, q, k_new, v_new, mode="h2o", budget=0, recent=0, window=0, seq_begin=0, out=None,
-             keep_mask=None, stream=None):
+             keep_mask=None, stream=None, retention=1.0):
         """One decode step of this layer: append -> attention (+H2O) -> select -> compact."""
         batch = q.shape[0]
         self.quantize_append(k_new, v_new, seq_begin=seq_begin, stream=stream)
-        out = self.decode_attention(q, out=out, seq_begin=seq_begin, accumulate_h2o=(mode == "h2o"), stream=stream)
+        out = self.decode_attention(q, out=out, seq_begin=seq_begin, accumulate_h2o=(mode != "streaming"),
+                                    stream=stream)
         mask = self.h2o_select_evict(batch, mode=mode, budget=budget, recent=recent, window=window,
-                                     seq_begin=seq_begin, keep_mask=keep_mask, stream=stream)
+                                     seq_begin=seq_begin, keep_mask=keep_mask, stream=stream, retention=retention)
         self.compact_blocks(mask, batch, seq_begin=seq_begin, stream=stream)
         return out

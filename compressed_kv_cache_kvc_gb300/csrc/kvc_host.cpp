@@ -243,6 +243,14 @@ kvc_status evict_check(const kvc_evict_params* p) {
   return KVC_OK;
 }
 
+// Candidate pages of block-granular eviction, the most of any sequence of
+// the slice (sizes the page-key grid only).
+int max_block_cand(const kvc_cache* c, int32_t seq_begin, int32_t batch, int recent) {
+  int m = 0;
+  for (int i = 0; i < batch; ++i) m = std::max(m, std::max(0, c->slots[seq_begin + i] - recent) / kvc::kPage);
+  return m;
+}
+
 int plan_keep(const kvc_evict_params* p, int S, int P) {
   const int ns = std::min(P, kvc::kSinks);
   if (p->mode == KVC_EVICT_H2O) return (ns + S <= p->budget) ? S : p->budget - kvc::kSinks;
@@ -465,10 +473,14 @@ kvc_status kvc_h2o_select_evict(kvc_cache* c, int32_t seq_begin, int32_t batch, 
   }
   if (p->mode == KVC_EVICT_BLOCK) {
     if (c->cfg.max_blocks_per_seq > kvc::kMaxBlockPages) return KVC_ERR_UNSUPPORTED;
-    if (kvc::launch_select_blocks(c->dev, seq_begin, batch, p->recent, p->retention, d_keep_mask, s_cap(c),
-                                  static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    auto* keys = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(d_workspace) + wl.keys);
+    if (kvc::launch_block_keys(c->dev, seq_begin, batch, p->recent, max_block_cand(c, seq_begin, batch, p->recent),
+                               sm_count(c), keys, st) != cudaSuccess ||
+        kvc::launch_select_blocks(c->dev, seq_begin, batch, p->recent, p->retention, keys, d_keep_mask, s_cap(c),
+                                  st) != cudaSuccess)
       return KVC_ERR_CUDA;
-    c->last_launches = 1;
+    c->last_launches = 2;
     c->plan_pending = true;
     c->plan_block = true;
     c->plan_begin = seq_begin;
@@ -541,7 +553,8 @@ kvc_status kvc_decode_step(kvc_cache* c, int32_t seq_begin, int32_t batch, const
   if (!c) return KVC_ERR_INVALID_ARG;
   c->last_launches = 0;
   if (evict_check(params) != KVC_OK) return KVC_ERR_INVALID_ARG;
-  if (params->mode == KVC_EVICT_BLOCK) return KVC_ERR_UNSUPPORTED;  // separate calls only
+  const bool block = params->mode == KVC_EVICT_BLOCK;
+  if (block && c->cfg.max_blocks_per_seq > kvc::kMaxBlockPages) return KVC_ERR_UNSUPPORTED;
   kvc_status st0 =
       attention_check(c, seq_begin, batch, d_q, d_out, sm_scale, d_workspace, workspace_bytes, /*appended=*/1);
   if (st0 != KVC_OK) return st0;
@@ -553,7 +566,7 @@ kvc_status kvc_decode_step(kvc_cache* c, int32_t seq_begin, int32_t batch, const
   long long total_pages = 0;
   attention_plan(c, seq_begin, batch, d_workspace, &w, &total_pages);
   const float qk_scale_log2 = sm_scale * 1.4426950408889634f;
-  const bool h2o = params->mode == KVC_EVICT_H2O;
+  const bool h2o = params->mode != KVC_EVICT_STREAMING;  // H2O scores (token or block selection)
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   st0 = launch_split_traced(c, seq_begin, batch, d_q, qk_scale_log2, w, h2o, total_pages, st, &launches);
   if (st0 != KVC_OK) return st0;
@@ -575,7 +588,10 @@ kvc_status kvc_decode_step(kvc_cache* c, int32_t seq_begin, int32_t batch, const
   // the score pass writes whole quarter pages of keys; keys and positions in
   // shared memory when both fit, else the keys alone, else neither
   const int slots4 = std::max((max_s + 3) & ~3, 4);
-  if (slots4 * 8 <= kvc::step_max_smem_bytes()) {
+  if (block) {  // no slot keys: the page selection follows
+    a.smem_slots = 0;
+    a.pos_smem = 0;
+  } else if (slots4 * 8 <= kvc::step_max_smem_bytes()) {
     a.smem_slots = slots4;
     a.pos_smem = 1;
   } else if (slots4 * 4 <= kvc::step_max_smem_bytes()) {
@@ -591,6 +607,22 @@ kvc_status kvc_decode_step(kvc_cache* c, int32_t seq_begin, int32_t batch, const
   if (kvc::launch_step_post(c->dev, seq_begin, batch, static_cast<const uint16_t*>(d_q),
                             static_cast<uint16_t*>(d_out), qk_scale_log2, w, a, sm_count(c), st) != cudaSuccess)
     return KVC_ERR_CUDA;
+  if (block) {
+    // page keys over the whole GPU, then one CTA per sequence selects and
+    // drops its pages (no rows move)
+    auto* keys = reinterpret_cast<unsigned long long*>(ws + wl.keys);
+    if (kvc::launch_block_keys(c->dev, seq_begin, batch, params->recent,
+                               max_block_cand(c, seq_begin, batch, params->recent), sm_count(c), keys,
+                               st) != cudaSuccess ||
+        kvc::launch_evict_blocks(c->dev, seq_begin, batch, params->recent, params->retention, keys, st) !=
+            cudaSuccess)
+      return KVC_ERR_CUDA;
+    launches += 3;
+    for (int i = 0; i < batch; ++i) c->slots[seq_begin + i] = plan[i];
+    c->plan_pending = false;
+    c->last_launches = launches;
+    return KVC_OK;
+  }
   int max_moves = 0;  // a pair moves at most min(n', S - n') rows
   for (int i = 0; i < batch; ++i)
     max_moves = std::max(max_moves, std::min(plan[i], c->slots[seq_begin + i] - plan[i]));

@@ -100,12 +100,17 @@ struct SelectArgs {
 cudaError_t launch_select(const DevState& s, int seq_begin, int batch, const SelectArgs& a,
                           uint8_t* keep_mask, cudaStream_t st);
 
-// Block-granular eviction: the keep mask and plan of whole pages (select), and
-// the block-table rewrite that drops them (release).  At most
-// kMaxBlockPages pages per sequence.
+// Block-granular eviction.  keys: [batch][max_bps] page keys in the
+// workspace (block_keys writes them); select writes the plan and the keep
+// mask, release applies a keep mask, evict selects and applies in one launch.
+// At most kMaxBlockPages pages per sequence.
 constexpr int kMaxBlockPages = 4096;
+cudaError_t launch_block_keys(const DevState& s, int seq_begin, int batch, int recent, int max_cand,
+                              int sm_count, unsigned long long* keys, cudaStream_t st);
 cudaError_t launch_select_blocks(const DevState& s, int seq_begin, int batch, int recent, double retention,
-                                 uint8_t* keep_mask, int s_cap, cudaStream_t st);
+                                 const unsigned long long* keys, uint8_t* keep_mask, int s_cap, cudaStream_t st);
+cudaError_t launch_evict_blocks(const DevState& s, int seq_begin, int batch, int recent, double retention,
+                                const unsigned long long* keys, cudaStream_t st);
 cudaError_t launch_release_blocks(const DevState& s, int seq_begin, int batch, const uint8_t* keep_mask,
                                   int s_cap, cudaStream_t st);
 // g_holes / g_srcs: [batch][hkv][s_cap] move lists in the workspace, used when

@@ -10,7 +10,7 @@
 // 0xFFFFFFFF for the recent window (always kept) and the fp32 score's bit
 // pattern otherwise (scores are >= 0, so the bit patterns order like the
 // values).  The n_keep-th largest key is found by an MSB-first radix select
-// (four 8-bit passes, shared-memory histograms); ties at the threshold key are
+// (passes of 11, 11 and 10 bits, shared-memory histograms); ties at the threshold key are
 // resolved by a second radix select on the positions (smallest first).  Keys
 // and positions sit in shared memory when they fit, else in the workspace.
 //
@@ -18,6 +18,8 @@
 // filled in ascending order by the kept slots at or above n' (ascending).
 // Sources all lie at or above n' and destinations below it, so the moves never
 // overlap.  The pages past ceil(n'/16) go back to the free-block stack.
+#include <algorithm>
+
 #include "kvc_device.h"
 #include "kvc_internal.h"
 
@@ -259,78 +261,212 @@ __global__ void __launch_bounds__(256) release_kernel(DevState s, int seq_begin)
 // candidates are the full pages before the last `recent` slots; a page is
 // ordered by the fp64 sum of its 16 x Hkv scores, added head by head and slot
 // by slot (the sum orders pages as the mean does); ties go to the earlier
-// page.  One CTA per sequence: the plan, then the keep mask of every head
-// (all heads the same).  The lowest pages are found by radix select on the
-// sum's bit pattern (sums are >= 0, so their bits order like their values):
-// the high word, then the low word among equal high words, then the page
-// index among equal sums.
+// page.
+//
+// block_key_kernel: one thread per candidate page (grid-stride over the
+// sequence's pages, so any grid is correct for any lengths) writes the sum's
+// bit pattern to the workspace.  The sum is one chain of 16 x Hkv dependent
+// fp64 additions; spreading the pages over the whole GPU keeps the chains'
+// fp64 work off any single SM.
+//
+// block_evict_kernel: one CTA per sequence.  The lowest n_evict keys (sums are
+// >= 0, so their bit patterns order like their values) by an MSB-first radix
+// select over the 64-bit keys, eight 8-bit passes; among the pages equal to
+// the threshold on the selected bits the earliest go first (a block scan in
+// page order).  kRelease = false writes the plan and the keep mask of every
+// head (all heads the same); kRelease = true applies the eviction at once:
+// the dropped pages leave the row (the others keep their order) and go to the
+// free stack, and the sequence holds S - 16 * n_evict slots.  Nothing moves in
+// the pool.
 constexpr int kBlockThreads = 256;
+constexpr int kKeyThreads = 128;
+constexpr int kEvictThreads = 512;
 
-__global__ void __launch_bounds__(kBlockThreads) block_select_kernel(DevState s, int seq_begin, int recent,
-                                                                     double retention, uint8_t* __restrict__ mask,
-                                                                     int s_cap) {
-  __shared__ unsigned long long key[kMaxBlockPages];
-  __shared__ int hist[kRadixBins];
-  __shared__ int sh_sel[3];
+__global__ void __launch_bounds__(kKeyThreads) block_key_kernel(DevState s, int seq_begin, int recent,
+                                                                unsigned long long* __restrict__ keys) {
+  const int bl = blockIdx.y;
+  const int b = seq_begin + bl;
+  const int S = s.seq_slots[b];
+  const int n_cand = max(0, S - recent) / kPage;
+  const int hkv = s.hkv;
+  const int32_t* bt = s.block_table + (size_t)b * s.max_bps;
+  unsigned long long* krow = keys + (size_t)bl * s.max_bps;
+  for (int p = blockIdx.x * kKeyThreads + threadIdx.x; p < n_cand; p += gridDim.x * kKeyThreads) {
+    const int blk = bt[p];
+    double acc = 0.0;
+    if ((unsigned)blk < (unsigned)s.num_blocks) {
+      // the page's scores are contiguous: [head][slot]
+      const float4* sc = reinterpret_cast<const float4*>(s.score + (size_t)blk * hkv * kPage);
+      const int n4 = hkv * (kPage / 4);
+#pragma unroll 4
+      for (int i = 0; i < n4; ++i) {
+        const float4 v = sc[i];
+        acc += (double)v.x;
+        acc += (double)v.y;
+        acc += (double)v.z;
+        acc += (double)v.w;
+      }
+    } else {
+      atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
+    }
+    krow[p] = (unsigned long long)__double_as_longlong(acc);
+  }
+}
+
+template <bool kRelease>
+__global__ void __launch_bounds__(kEvictThreads) block_evict_kernel(DevState s, int seq_begin, int recent,
+                                                                    double retention,
+                                                                    const unsigned long long* __restrict__ keys,
+                                                                    uint8_t* __restrict__ mask, int s_cap) {
+  __shared__ __align__(16) unsigned long long buf[kMaxBlockPages];  // the keys, then (release) the old row
+  __shared__ uint8_t gone[kMaxBlockPages];
+  __shared__ int hist[256];
   __shared__ int sh_warp[32];
+  __shared__ int sh_sel[3];
   const int bl = blockIdx.x;
   const int b = seq_begin + bl;
   const int S = s.seq_slots[b];
   const int hkv = s.hkv;
   const int n_cand = max(0, S - recent) / kPage;
   const int n_evict = (int)((double)n_cand * (1.0 - retention));
+  const int np = S - kPage * n_evict;
   if (threadIdx.x == 0) {
     s.plan[2 * b] = S;
-    s.plan[2 * b + 1] = S - kPage * n_evict;
+    s.plan[2 * b + 1] = np;
   }
-  const int32_t* bt = s.block_table + (size_t)b * s.max_bps;
-  for (int p = threadIdx.x; p < n_cand; p += blockDim.x) {
-    const int blk = bt[p];
-    double acc = 0.0;
-    if ((unsigned)blk < (unsigned)s.num_blocks) {
-      const float* sc = s.score + (size_t)blk * hkv * kPage;
-      for (int i = 0; i < hkv * kPage; ++i) acc += (double)sc[i];  // head by head, slot by slot
-    } else {
-      atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
+  if (kRelease && n_evict == 0) return;
+  const unsigned long long* krow = keys + (size_t)bl * s.max_bps;
+  for (int p = threadIdx.x; p < n_cand; p += kEvictThreads) buf[p] = krow[p];
+  __syncthreads();
+
+  // ---- the n_evict-th smallest key on the selected bits (prefix / pmask);
+  // rem = how many of the keys equal to it there go
+  unsigned long long prefix = 0, pmask = 0;
+  int rem = n_evict;
+  if (n_evict > 0) {
+#pragma unroll 1
+    for (int pass = 0; pass < 8; ++pass) {
+      const int shift = 56 - 8 * pass;
+      if (threadIdx.x < 256) hist[threadIdx.x] = 0;
+      __syncthreads();
+      for (int p = threadIdx.x; p < n_cand; p += kEvictThreads) {
+        const unsigned long long k = buf[p];
+        if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & 0xFF], 1);
+      }
+      __syncthreads();
+      if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        int c[8], sum = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          c[j] = hist[8 * lane + j];
+          sum += c[j];
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const int excl = incl - sum;
+        if (excl < rem && incl >= rem) {
+          int run = excl;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (run + c[j] >= rem) {
+              sh_sel[0] = 8 * lane + j;
+              sh_sel[1] = rem - run;
+              sh_sel[2] = c[j];
+              break;
+            }
+            run += c[j];
+          }
+        }
+      }
+      __syncthreads();
+      prefix |= (unsigned long long)sh_sel[0] << shift;
+      pmask |= 0xFFull << shift;
+      rem = sh_sel[1];
+      const bool all_of_bin = sh_sel[2] == rem;
+      __syncthreads();
+      if (all_of_bin) break;  // every key on this prefix goes: the lower bits decide nothing
     }
-    key[p] = (unsigned long long)__double_as_longlong(acc);
+  }
+  // ---- per page: gone = below the prefix, or on it and among the first rem
+  // in page order
+  int eq_base = 0;
+  const int npages = (S + kPage - 1) / kPage;
+  for (int c0 = 0; c0 < npages; c0 += kEvictThreads) {
+    const int p = c0 + (int)threadIdx.x;
+    const bool cand = n_evict > 0 && p < n_cand;
+    const unsigned long long km = cand ? (buf[p] & pmask) : 0;
+    const bool on = cand && km == prefix;
+    int tot;
+    const int incl = block_scan<kEvictThreads>(on ? 1 : 0, sh_warp, &tot);
+    if (p < npages) gone[p] = (cand && km < prefix) || (on && eq_base + incl - 1 < rem);
+    eq_base += tot;
   }
   __syncthreads();
-  unsigned long long theta = 0;
-  uint32_t idx_cut = 0;
-  bool any = n_evict > 0;
-  if (any) {
-    int need, ties;
-    const uint32_t hi = radix_select<kBlockThreads>(
-        n_cand, n_evict, false, [&](int) { return true; }, [&](int i) { return (uint32_t)(key[i] >> 32); },
-        hist, sh_warp, sh_sel, &need, &ties);
-    int need2, ties2;
-    const uint32_t lo = radix_select<kBlockThreads>(
-        n_cand, need, false, [&](int i) { return (uint32_t)(key[i] >> 32) == hi; },
-        [&](int i) { return (uint32_t)key[i]; }, hist, sh_warp, sh_sel, &need2, &ties2);
-    theta = ((unsigned long long)hi << 32) | lo;
-    int r3, t3;
-    idx_cut = radix_select<kBlockThreads>(
-        n_cand, need2, false, [&](int i) { return key[i] == theta; }, [&](int i) { return (uint32_t)i; }, hist,
-        sh_warp, sh_sel, &r3, &t3);
-  }
-  // keep mask of every head: a slot goes when its page goes
-  for (int h = 0; h < hkv; ++h) {
-    uint8_t* mrow = mask + ((size_t)bl * hkv + h) * s_cap;
-    for (int t = threadIdx.x; t < S; t += blockDim.x) {
-      const int p = t / kPage;
-      bool gone = false;
-      if (any && p < n_cand) gone = key[p] < theta || (key[p] == theta && (uint32_t)p <= idx_cut);
-      mrow[t] = gone ? 0 : 1;
+
+  if (!kRelease) {
+    // keep mask of every head: a slot goes when its page goes
+    const bool vec = ((reinterpret_cast<uintptr_t>(mask) | (uintptr_t)s_cap) & 15) == 0;
+    for (int i = threadIdx.x; i < hkv * npages; i += kEvictThreads) {
+      const int h = i / npages, p = i - h * npages;
+      uint8_t* m = mask + ((size_t)bl * hkv + h) * s_cap + (size_t)p * kPage;
+      const uint8_t v = gone[p] ? 0 : 1;
+      if (vec && (p + 1) * kPage <= S) {
+        const uint32_t w4 = v * 0x01010101u;
+        *reinterpret_cast<uint4*>(m) = make_uint4(w4, w4, w4, w4);
+      } else {
+        for (int t = 0; t < kPage && p * kPage + t < S; ++t) m[t] = v;
+      }
     }
+    return;
+  }
+
+  // ---- release: the kept pages in order, the dropped ones to the free stack
+  int32_t* row = s.block_table + (size_t)b * s.max_bps;
+  int32_t* row_in = reinterpret_cast<int32_t*>(buf);
+  for (int p = threadIdx.x; p < npages; p += kEvictThreads) row_in[p] = row[p];
+  if (threadIdx.x == 0) {
+    int base = -1;
+    if (n_evict > 0) {
+      base = atomicAdd(&s.counters[kCtrFreeTop], n_evict);
+      if (base + n_evict > s.num_blocks) {
+        atomicSub(&s.counters[kCtrFreeTop], n_evict);
+        atomicOr(&s.counters[kCtrStatus], kDevStackOverflow);
+        base = -1;
+      }
+    }
+    sh_sel[0] = base;
+  }
+  __syncthreads();
+  const int fbase = sh_sel[0];
+  int kept_base = 0, drop_base = 0;
+  for (int c0 = 0; c0 < npages; c0 += kEvictThreads) {
+    const int p = c0 + (int)threadIdx.x;
+    const bool valid = p < npages;
+    const bool drop = valid && gone[p];
+    const bool keep = valid && !drop;
+    int tot;
+    const int incl = block_scan<kEvictThreads>((keep ? 1 : 0) | (drop ? 1 << 16 : 0), sh_warp, &tot);
+    if (keep) row[kept_base + (incl & 0xFFFF) - 1] = row_in[p];
+    const int d_rank = drop_base + (incl >> 16) - 1;
+    if (drop && fbase >= 0 && d_rank < n_evict) s.free_stack[fbase + d_rank] = row_in[p];
+    kept_base += tot & 0xFFFF;
+    drop_base += tot >> 16;
+  }
+  if (threadIdx.x == 0) {
+    if (drop_base != n_evict) atomicOr(&s.counters[kCtrStatus], kDevBadKeepMask);
+    if (n_evict > 0) s.seq_slots[b] = np;
   }
 }
 
-// The block-table rewrite of block-granular eviction (one CTA per sequence):
-// the pages whose slots the mask drops (head 0's row; every head's is the
-// same) leave the row, the others keep their order, the dropped pages go to
-// the free stack and the sequence holds S - 16 * dropped slots.  Nothing
-// moves in the pool.
+// The block-table rewrite of a block-granular eviction's keep mask (one CTA
+// per sequence): the pages whose slots the mask drops (head 0's row; every
+// head's is the same) leave the row, the others keep their order, the dropped
+// pages go to the free stack and the sequence holds S - 16 * dropped slots.
 __global__ void __launch_bounds__(kBlockThreads) block_release_kernel(DevState s, int seq_begin,
                                                                       const uint8_t* __restrict__ mask,
                                                                       int s_cap) {
@@ -347,7 +483,6 @@ __global__ void __launch_bounds__(kBlockThreads) block_release_kernel(DevState s
   const uint8_t* m0 = mask + (size_t)bl * s.hkv * s_cap;  // head 0
   for (int p = threadIdx.x; p < npages; p += blockDim.x) row_in[p] = row[p];
   __syncthreads();
-  // ranks of kept and dropped pages, chunk by chunk
   int kept_base = 0, drop_base = 0;
   const int n_drop = (S - np) / kPage;
   if (threadIdx.x == 0) {
@@ -417,9 +552,25 @@ cudaError_t launch_compact(const DevState& s, int seq_begin, int batch, const ui
   return cudaGetLastError();
 }
 
+cudaError_t launch_block_keys(const DevState& s, int seq_begin, int batch, int recent, int max_cand,
+                              int sm_count, unsigned long long* keys, cudaStream_t st) {
+  // about two CTAs per SM over the slice (any grid is correct: grid-stride)
+  int gx = (2 * sm_count + batch - 1) / batch;
+  gx = std::max(1, std::min(gx, (max_cand + 31) / 32));
+  dim3 grid(gx, batch);
+  block_key_kernel<<<grid, kKeyThreads, 0, st>>>(s, seq_begin, recent, keys);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_select_blocks(const DevState& s, int seq_begin, int batch, int recent, double retention,
-                                 uint8_t* keep_mask, int s_cap, cudaStream_t st) {
-  block_select_kernel<<<batch, kBlockThreads, 0, st>>>(s, seq_begin, recent, retention, keep_mask, s_cap);
+                                 const unsigned long long* keys, uint8_t* keep_mask, int s_cap, cudaStream_t st) {
+  block_evict_kernel<false><<<batch, kEvictThreads, 0, st>>>(s, seq_begin, recent, retention, keys, keep_mask, s_cap);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_evict_blocks(const DevState& s, int seq_begin, int batch, int recent, double retention,
+                                const unsigned long long* keys, cudaStream_t st) {
+  block_evict_kernel<true><<<batch, kEvictThreads, 0, st>>>(s, seq_begin, recent, retention, keys, nullptr, 0);
   return cudaGetLastError();
 }
 

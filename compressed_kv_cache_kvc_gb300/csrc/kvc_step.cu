@@ -11,6 +11,9 @@
 // another) applies its new length and releases its pages.  Released pages
 // are only taken by later calls, after step_moves_kernel has read them.
 //
+// With block-granular eviction the post kernel stops after the scores; the
+// page keys and the eviction follow as launches of their own (kvc_select.cu).
+//
 // step_moves_kernel, one CTA per (KV head, sequence): the row moves of the
 // lists.  Moves run in a launch of their own because, sharing an SM with
 // another CTA's selection phase, their global-memory traffic stalls that
@@ -48,7 +51,10 @@ __global__ void __launch_bounds__(NT, 1024 / NT) step_post_kernel(DevState s, in
   const int h = blockIdx.x;
   const int bl = blockIdx.y;
   const int b = seq_begin + bl;
-  const bool h2o = a.mode == 0;
+  // mode 0: H2O; 1: StreamingLLM (no scores); 2: block-granular eviction
+  // (scores only: the page selection runs in launches of its own)
+  const bool block = a.mode == 2;
+  const bool h2o = a.mode != 1;
   // the selection's first radix histogram is built by the score pass
   for (int i = threadIdx.x; i < kRadixBins; i += blockDim.x) hist[i] = 0;
   merge_phase(s, seq_begin, batch, w.cum, h, bl, q, out, qk_scale_log2, w, h2o, ms);
@@ -61,7 +67,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) step_post_kernel(DevState s, in
   const size_t pair = (size_t)bl * hkv + h;
   bool keep_all;
   int n_keep, thr;
-  if (h2o) {
+  if (a.mode == 0) {
     keep_all = ns + S <= a.budget;
     n_keep = a.budget - kSinks;
     thr = P - a.recent;
@@ -71,7 +77,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) step_post_kernel(DevState s, in
     thr = P - a.window;
   }
   if (keep_all) n_keep = S;
-  if (h == 0 && threadIdx.x == 0) {
+  if (h == 0 && threadIdx.x == 0 && !block) {
     s.plan[2 * b] = S;
     s.plan[2 * b + 1] = n_keep;
   }
@@ -149,6 +155,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) step_post_kernel(DevState s, in
           if (t + c < S) s.score[idx + c] = vv[c];
       }
     }
+    if (block) continue;
     // slots past S in the last quarter page get keys too: nothing reads them
     *reinterpret_cast<uint4*>(keys + t) = make_uint4(kk[0], kk[1], kk[2], kk[3]);
     *reinterpret_cast<int4*>(pos + t) = p4;
@@ -165,6 +172,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) step_post_kernel(DevState s, in
     n_top = __reduce_add_sync(am, n_top);
     if ((threadIdx.x & 31) == __ffs(am) - 1 && n_top > 0) atomicAdd(&hist[kRadixBins - 1], n_top);
   }
+  if (block) return;
   __syncthreads();
   bool lists_ok = true;
   if (!keep_all) {

@@ -113,7 +113,7 @@ typedef enum {
 /* Eviction modes of kvc_h2o_select_evict. */
 #define KVC_EVICT_H2O       0
 #define KVC_EVICT_STREAMING 1
-#define KVC_EVICT_BLOCK     2  /* whole pages by mean H2O score (separate calls only) */
+#define KVC_EVICT_BLOCK     2  /* whole pages by mean H2O score                        */
 
 typedef struct {
   int32_t mode;      /* KVC_EVICT_H2O, KVC_EVICT_STREAMING or KVC_EVICT_BLOCK   */
@@ -218,8 +218,10 @@ kvc_status kvc_h2o_select_evict(kvc_cache* cache, int32_t seq_begin, int32_t bat
  * sequence's block-table row (the others keep their order), returns them to
  * the free stack and moves nothing in the pool.  The scores are what the
  * attention with KVC_ATTN_ACCUM_H2O accumulated.  At most 4096 pages per
- * sequence (max_blocks_per_seq), else KVC_ERR_UNSUPPORTED; kvc_decode_step
- * returns KVC_ERR_UNSUPPORTED for this mode. */
+ * sequence (max_blocks_per_seq), else KVC_ERR_UNSUPPORTED, before anything
+ * is enqueued.  The selection takes two launches (the page sums over the
+ * whole GPU, then one CTA per sequence selects and writes the mask; the page
+ * sums use the workspace), the compaction one (the row rewrite). */
 
 /* Compaction ("KV Cache optimization techniques" 2.2: gather the kept tokens;
  * 3.2: release blocks).  With S slots and n' < S kept, the kept slots are
@@ -265,12 +267,15 @@ kvc_status kvc_decode_attention_noalloc(kvc_cache* cache, int32_t seq_begin, int
 
 /* One whole decode step of a layer in one call: append one token per
  * sequence (as kvc_quantize_append with n_new = 1), then decode attention
- * (H2O accumulation on in H2O mode, off in StreamingLLM mode), selection and
- * compaction with `params`, exactly as the four calls above compute them.
- * After the split-K attention, the merge, the score update, the selection and
- * the compaction lists of each (sequence, KV head) run in one kernel that
- * keeps the scores, keys and keep decisions on chip; the row moves follow in
- * a launch of their own.  Four launches in all.
+ * (H2O accumulation on in H2O and block mode, off in StreamingLLM mode),
+ * selection and compaction with `params`, exactly as the four calls above
+ * compute them.  After the split-K attention, the merge, the score update,
+ * the selection and the compaction lists of each (sequence, KV head) run in
+ * one kernel that keeps the scores, keys and keep decisions on chip; the row
+ * moves follow in a launch of their own.  Four launches in all.  In block
+ * mode (KVC_EVICT_BLOCK) that kernel stops after the scores; the page sums
+ * and then the page selection and the row rewrite of each sequence follow
+ * (five launches).
  *   d_q: bf16 [batch][Hq][128]; d_k_new, d_v_new: bf16 [batch][Hkv][1][128];
  *   d_out: bf16 [batch][Hq][128]; workspace as for kvc_decode_attention.
  * Host-visible errors (arguments, capacity) are returned before anything is

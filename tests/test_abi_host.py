@@ -147,13 +147,28 @@ def test_call_validation_before_any_launch(lib):
         assert L.kvc_h2o_select_evict(h, 0, 1, ctypes.byref(prm), mask, wsp, ws, None) == lib.KVC_ERR_INVALID_ARG
     # compaction needs a pending selection
     assert L.kvc_compact_blocks(h, 0, 1, mask, wsp, ws, None) == lib.KVC_ERR_STATE
-    # block-granular eviction is for the separate calls only
-    blk = lib.KvcEvictParams(2, 0, 8, 0, 0.5)
-    assert L.kvc_decode_step(h, 0, 1, dummy, dummy, dummy, dummy, ctypes.c_float(0.088), ctypes.byref(blk), wsp, ws,
-                             None) == lib.KVC_ERR_UNSUPPORTED
     # tracing events come in pairs
     assert L.kvc_set_trace_events(h, dummy, None) == lib.KVC_ERR_INVALID_ARG
     assert L.kvc_set_trace_events(h, None, None) == lib.KVC_OK
+    L.kvc_cache_destroy(h)
+
+
+def test_block_eviction_page_limit(lib):
+    """Block-granular eviction keeps a sequence's page keys in one CTA's
+    shared memory: more than 4096 pages per sequence is refused before any
+    launch, by the selection and by the one-call step."""
+    L = lib.lib()
+    st, h, fs = _create(lib, _cfg(lib, num_blocks=3, max_blocks_per_seq=4097))
+    assert st == lib.KVC_OK
+    dummy = ctypes.c_void_p(fs.ptr.value)
+    ws = L.kvc_workspace_bytes(h, 1)
+    wsbuf = ctypes.create_string_buffer(ws + 512)
+    wsp = ctypes.c_void_p(ctypes.addressof(wsbuf) + (-ctypes.addressof(wsbuf)) % 256)
+    blk = lib.KvcEvictParams(2, 0, 8, 0, 0.5)
+    assert L.kvc_h2o_select_evict(h, 0, 1, ctypes.byref(blk), dummy, wsp, ws, None) == lib.KVC_ERR_UNSUPPORTED
+    assert L.kvc_decode_step(h, 0, 1, dummy, dummy, dummy, dummy, ctypes.c_float(0.088), ctypes.byref(blk), wsp, ws,
+                             None) == lib.KVC_ERR_UNSUPPORTED
+    assert L.kvc_last_launch_count(h) == 0
     L.kvc_cache_destroy(h)
 
 

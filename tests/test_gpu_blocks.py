@@ -33,6 +33,7 @@ CASES = [
     (8, 32, 8, [700, 1300], 128, 0.05, 2),
     (8, 8, 8, [200], 0, 1.0, 2),      # keep everything
     (8, 8, 2, [300], 400, 0.2, 2),    # the recent window covers the pool: no candidate
+    (8, 8, 2, [9000, 4100], 100, 0.4, 2),  # more pages than the selection CTA has threads
 ]
 
 
@@ -55,7 +56,7 @@ def test_block_eviction(bits, hq, hkv, lengths, recent, retention, steps):
         cache.decode_attention(T.to_dev_bf16(_bits(rng, (B, hq, 128))), accumulate_h2o=True)
         pre = T.StateView(cache)
         mask = cache.h2o_select_evict(B, mode="block", recent=recent, retention=retention)
-        assert cache.last_launch_count() == 1
+        assert cache.last_launch_count() == 2  # page sums, then the selection
         mask_h = mask.cpu().numpy()
         cache.compact_blocks(mask, B)
         assert cache.last_launch_count() == 1
@@ -78,3 +79,26 @@ def test_block_eviction(bits, hq, hkv, lengths, recent, retention, steps):
         assert cache.read_status() == 0
     if retention < 1.0 and recent < min(lengths) - 32:
         assert evicted_any
+
+
+def test_block_eviction_ties_to_the_earlier_page():
+    """With no attention run every score is 0, so every page sum ties: the
+    earliest candidate pages go."""
+    from compressed_kv_cache_kvc_gb300.cache import KVCache
+    rng = np.random.default_rng(11)
+    hq, hkv, n, recent, retention = 8, 2, 900, 32, 0.35
+    mbps = (n + 15) // 16 + 1
+    cache = KVCache(hq, hkv, 8, mbps, 1, mbps)
+    cache.quantize_append(T.to_dev_bf16(_bits(rng, (1, hkv, n, 128))), T.to_dev_bf16(_bits(rng, (1, hkv, n, 128))))
+    S = cache.lengths(0)[0]
+    mask = cache.h2o_select_evict(1, mode="block", recent=recent, retention=retention).cpu().numpy()
+    n_cand = (S - recent) // 16
+    n_evict = int(n_cand * (1.0 - retention))
+    want = np.ones(S, dtype=bool)
+    want[:16 * n_evict] = False
+    assert np.array_equal(want, O.select_blocks([np.zeros(S)] * hkv, S, recent, retention))
+    for h in range(hkv):
+        assert np.array_equal(mask[0, h, :S] == 1, want)
+    cache.compact_blocks(torch.from_numpy(mask).cuda(), 1)
+    assert cache.lengths(0)[0] == S - 16 * n_evict
+    assert cache.read_status() == 0

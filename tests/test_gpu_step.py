@@ -85,6 +85,47 @@ def test_step_equals_separate_calls(bits, hq, hkv, lengths, mode, budget, recent
     assert ca.read_status() == 0 and cb.read_status() == 0
 
 
+BLOCK_CASES = [
+    # bits, hq, hkv, lengths, recent, retention, steps
+    (8, 16, 4, [600, 333], 40, 0.5, 3),
+    (4, 40, 8, [1000, 257, 64], 64, 0.3, 3),
+    (8, 8, 2, [9000, 70], 100, 0.6, 2),
+    (4, 8, 8, [200], 0, 1.0, 2),  # keep everything
+]
+
+
+@pytest.mark.parametrize("bits,hq,hkv,lengths,recent,retention,steps", BLOCK_CASES)
+def test_block_step_equals_separate_calls(bits, hq, hkv, lengths, recent, retention, steps):
+    """Block-granular eviction through the one-call step (five launches):
+    the same outputs and logical state as the separate calls."""
+    from compressed_kv_cache_kvc_gb300.cache import KVCache
+    rng = np.random.default_rng(bits * 5 + hq + len(lengths))
+    B, T_ = len(lengths), max(lengths)
+    mbps = (T_ + steps + 15) // 16 + 2
+    order = np.random.default_rng(3).permutation(B * mbps).astype(np.int32)
+    ca = KVCache(hq, hkv, bits, B * mbps, B, mbps, block_order=order)
+    cb = KVCache(hq, hkv, bits, B * mbps, B, mbps, block_order=order)
+    k = _bits(rng, (B, hkv, T_, 128))
+    v = _bits(rng, (B, hkv, T_, 128))
+    for c in (ca, cb):
+        for b, n in enumerate(lengths):
+            c.quantize_append(T.to_dev_bf16(np.ascontiguousarray(k[b:b + 1, :, :n])),
+                              T.to_dev_bf16(np.ascontiguousarray(v[b:b + 1, :, :n])), seq_begin=b)
+    for _ in range(steps):
+        q = T.to_dev_bf16(_bits(rng, (B, hq, 128)))
+        kn = T.to_dev_bf16(_bits(rng, (B, hkv, 1, 128)))
+        vn = T.to_dev_bf16(_bits(rng, (B, hkv, 1, 128)))
+        oa = ca.step(q, kn, vn, mode="block", recent=recent, retention=retention)
+        ob = cb.decode_step(q, kn, vn, mode="block", recent=recent, retention=retention)
+        assert cb.last_launch_count() == 5
+        torch.cuda.synchronize()
+        assert torch.equal(oa, ob)
+        _same_state(ca, cb)
+        for b in range(B):
+            assert ca.lengths(b) == cb.lengths(b)
+    assert ca.read_status() == 0 and cb.read_status() == 0
+
+
 def test_step_against_oracle_tiny_workload():
     from compressed_kv_cache_kvc_gb300 import workloads as W
     from compressed_kv_cache_kvc_gb300.cache import KVCache
