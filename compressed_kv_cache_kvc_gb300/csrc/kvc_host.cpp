@@ -475,8 +475,8 @@ kvc_status kvc_h2o_select_evict(kvc_cache* c, int32_t seq_begin, int32_t batch, 
     if (c->cfg.max_blocks_per_seq > kvc::kMaxBlockPages) return KVC_ERR_UNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     auto* keys = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(d_workspace) + wl.keys);
-    if (kvc::launch_block_keys(c->dev, seq_begin, batch, p->recent, max_block_cand(c, seq_begin, batch, p->recent),
-                               sm_count(c), keys, st) != cudaSuccess ||
+    if (kvc::launch_block_keys(c->dev, seq_begin, batch, p->recent, max_block_cand(c, seq_begin, batch, p->recent), keys,
+                               st) != cudaSuccess ||
         kvc::launch_select_blocks(c->dev, seq_begin, batch, p->recent, p->retention, keys, d_keep_mask, s_cap(c),
                                   st) != cudaSuccess)
       return KVC_ERR_CUDA;
@@ -612,8 +612,7 @@ kvc_status kvc_decode_step(kvc_cache* c, int32_t seq_begin, int32_t batch, const
     // drops its pages (no rows move)
     auto* keys = reinterpret_cast<unsigned long long*>(ws + wl.keys);
     if (kvc::launch_block_keys(c->dev, seq_begin, batch, params->recent,
-                               max_block_cand(c, seq_begin, batch, params->recent), sm_count(c), keys,
-                               st) != cudaSuccess ||
+                               max_block_cand(c, seq_begin, batch, params->recent), keys, st) != cudaSuccess ||
         kvc::launch_evict_blocks(c->dev, seq_begin, batch, params->recent, params->retention, keys, st) !=
             cudaSuccess)
       return KVC_ERR_CUDA;

@@ -106,7 +106,7 @@ cudaError_t launch_select(const DevState& s, int seq_begin, int batch, const Sel
 // At most kMaxBlockPages pages per sequence.
 constexpr int kMaxBlockPages = 4096;
 cudaError_t launch_block_keys(const DevState& s, int seq_begin, int batch, int recent, int max_cand,
-                              int sm_count, unsigned long long* keys, cudaStream_t st);
+                              unsigned long long* keys, cudaStream_t st);
 cudaError_t launch_select_blocks(const DevState& s, int seq_begin, int batch, int recent, double retention,
                                  const unsigned long long* keys, uint8_t* keep_mask, int s_cap, cudaStream_t st);
 cudaError_t launch_evict_blocks(const DevState& s, int seq_begin, int batch, int recent, double retention,

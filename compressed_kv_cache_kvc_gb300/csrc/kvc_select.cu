@@ -266,8 +266,11 @@ __global__ void __launch_bounds__(256) release_kernel(DevState s, int seq_begin)
 // block_key_kernel: one thread per candidate page (grid-stride over the
 // sequence's pages, so any grid is correct for any lengths) writes the sum's
 // bit pattern to the workspace.  The sum is one chain of 16 x Hkv dependent
-// fp64 additions; spreading the pages over the whole GPU keeps the chains'
-// fp64 work off any single SM.
+// fp64 additions, each after an fp32 -> fp64 conversion, and both run on
+// GB300's narrow fp64 pipe (measured: about 1.6 additions per clock per SM
+// at best), so this kernel is bound by that pipe, not by its 512 bytes of
+// loads per page; the pages go one per thread in 64-thread CTAs, spread
+// over every SM.
 //
 // block_evict_kernel: one CTA per sequence.  The lowest n_evict keys (sums are
 // >= 0, so their bit patterns order like their values) by an MSB-first radix
@@ -279,7 +282,7 @@ __global__ void __launch_bounds__(256) release_kernel(DevState s, int seq_begin)
 // free stack, and the sequence holds S - 16 * n_evict slots.  Nothing moves in
 // the pool.
 constexpr int kBlockThreads = 256;
-constexpr int kKeyThreads = 128;
+constexpr int kKeyThreads = 64;
 constexpr int kEvictThreads = 512;
 
 __global__ void __launch_bounds__(kKeyThreads) block_key_kernel(DevState s, int seq_begin, int recent,
@@ -298,7 +301,6 @@ __global__ void __launch_bounds__(kKeyThreads) block_key_kernel(DevState s, int 
       // the page's scores are contiguous: [head][slot]
       const float4* sc = reinterpret_cast<const float4*>(s.score + (size_t)blk * hkv * kPage);
       const int n4 = hkv * (kPage / 4);
-#pragma unroll 4
       for (int i = 0; i < n4; ++i) {
         const float4 v = sc[i];
         acc += (double)v.x;
@@ -349,9 +351,15 @@ __global__ void __launch_bounds__(kEvictThreads) block_evict_kernel(DevState s, 
       const int shift = 56 - 8 * pass;
       if (threadIdx.x < 256) hist[threadIdx.x] = 0;
       __syncthreads();
-      for (int p = threadIdx.x; p < n_cand; p += kEvictThreads) {
-        const unsigned long long k = buf[p];
-        if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & 0xFF], 1);
+      // lanes of a warp that fall in the same bin add once (the high bytes,
+      // mostly the sums' exponents, put most pages in a few bins)
+      for (int p0 = 0; p0 < n_cand; p0 += kEvictThreads) {
+        const int p = p0 + (int)threadIdx.x;
+        const unsigned long long k = p < n_cand ? buf[p] : 0ull;
+        const bool on = p < n_cand && (k & pmask) == prefix;
+        const int bin = on ? (int)((k >> shift) & 0xFF) : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, bin);
+        if (on && (threadIdx.x & 31) == (unsigned)(__ffs(peers) - 1)) atomicAdd(&hist[bin], __popc(peers));
       }
       __syncthreads();
       if (threadIdx.x < 32) {
@@ -553,10 +561,10 @@ cudaError_t launch_compact(const DevState& s, int seq_begin, int batch, const ui
 }
 
 cudaError_t launch_block_keys(const DevState& s, int seq_begin, int batch, int recent, int max_cand,
-                              int sm_count, unsigned long long* keys, cudaStream_t st) {
-  // about two CTAs per SM over the slice (any grid is correct: grid-stride)
-  int gx = (2 * sm_count + batch - 1) / batch;
-  gx = std::max(1, std::min(gx, (max_cand + 31) / 32));
+                              unsigned long long* keys, cudaStream_t st) {
+  // one thread per candidate page of the longest sequence, in small CTAs so
+  // the fp64 chains spread over every SM (any grid is correct: grid-stride)
+  const int gx = std::max(1, (max_cand + kKeyThreads - 1) / kKeyThreads);
   dim3 grid(gx, batch);
   block_key_kernel<<<grid, kKeyThreads, 0, st>>>(s, seq_begin, recent, keys);
   return cudaGetLastError();

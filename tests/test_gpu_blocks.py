@@ -102,3 +102,35 @@ def test_block_eviction_ties_to_the_earlier_page():
     cache.compact_blocks(torch.from_numpy(mask).cuda(), 1)
     assert cache.lengths(0)[0] == S - 16 * n_evict
     assert cache.read_status() == 0
+
+
+def test_block_sums_exact_on_planted_scores():
+    """Scores planted directly in the pool: subnormals, zeros, tiny and huge
+    normals side by side, so the fp64 page sums round at many steps.  The
+    mask must still be the oracle's (its sums are exact conversions of the
+    fp32 scores added in the same order)."""
+    from compressed_kv_cache_kvc_gb300.cache import KVCache
+    rng = np.random.default_rng(21)
+    hq, hkv, n, recent = 16, 4, 2000, 48
+    mbps = (n + 15) // 16 + 1
+    cache = KVCache(hq, hkv, 8, mbps, 1, mbps)
+    cache.quantize_append(T.to_dev_bf16(_bits(rng, (1, hkv, n, 128))), T.to_dev_bf16(_bits(rng, (1, hkv, n, 128))))
+    sc = cache.buffer("SCORE").view(torch.int32)
+    kind = rng.integers(0, 5, sc.numel())
+    bits = np.where(kind == 0, rng.integers(1, 1 << 23, sc.numel()),                  # subnormal
+           np.where(kind == 1, 0,                                                     # zero
+           np.where(kind == 2, rng.integers(1 << 23, 20 << 23, sc.numel()),           # tiny normal
+           np.where(kind == 3, rng.integers(190 << 23, 230 << 23, sc.numel()),        # huge normal
+                    rng.integers(100 << 23, 130 << 23, sc.numel())))))                # ordinary
+    planted = bits.astype(np.int64).astype(np.int32)
+    sc.copy_(torch.from_numpy(planted).to(sc.device))
+    st = T.StateView(cache)
+    S = int(st.slots[0])
+    heads = [st.head(0, h)[5].astype(np.float64) for h in range(hkv)]
+    for retention in (0.7, 0.2):
+        mask = cache.h2o_select_evict(1, mode="block", recent=recent, retention=retention).cpu().numpy()
+        want = O.select_blocks(heads, S, recent, retention)
+        assert not want.all()
+        for h in range(hkv):
+            assert np.array_equal(mask[0, h, :S] == 1, want), (retention, h)
+    assert cache.read_status() == 0
