@@ -31,6 +31,10 @@ What it computes, step by step, each citing the page passage it restates:
 * ``select_blocks`` -- block-granular eviction (the eviction-and-reuse survey
   page, section 4, the block manager's eviction by attention): blocks sorted
   by their mean attention score, the lowest int(n * (1 - ratio)) evicted.
+* ``OracleCache(bf16_window=W)`` -- hybrid precision ("KV Cache optimization
+  techniques" section 1.3, HybridPrecisionKVCache: recent tokens at 16 bits,
+  older ones at INT4/INT8): the tokens at the last W positions attend with
+  their unquantised bf16 values, older ones with their codes.
 
 Readings where the pages are silent or disagree are listed in the design doc; the
 ones that change arithmetic are restated beside the function they affect.
@@ -296,6 +300,8 @@ class HeadState:
 @dataclass
 class SeqState:
     pos_total: int = 0
+    raw_k: list = field(default_factory=list)    # per head: fp32 [pos_total, D], every token's bf16 values
+    raw_v: list = field(default_factory=list)
     sink_k: list = field(default_factory=list)   # per head: fp32 [ns, D]
     sink_v: list = field(default_factory=list)
     sink_score: list = field(default_factory=list)  # per head: fp64 [ns]
@@ -317,11 +323,14 @@ class OracleCache:
     """
 
     def __init__(self, batch: int, num_q_heads: int, num_kv_heads: int, bits: int,
-                 head_dim: int = HEAD_DIM):
+                 head_dim: int = HEAD_DIM, bf16_window: int = 0):
         if num_q_heads % num_kv_heads:
             raise ValueError("num_q_heads must be a multiple of num_kv_heads")
+        if bf16_window < 0:
+            raise ValueError("bf16_window must be >= 0")
         qmax_for_bits(bits)
         self.batch, self.hq, self.hkv, self.bits, self.d = batch, num_q_heads, num_kv_heads, bits, head_dim
+        self.bf16_window = bf16_window
         self.group = num_q_heads // num_kv_heads
         self.seqs = []
         for _ in range(batch):
@@ -331,6 +340,8 @@ class OracleCache:
                 s.sink_v.append(np.zeros((0, head_dim), np.float32))
                 s.sink_score.append(np.zeros(0, np.float64))
                 s.heads.append(_empty_head(head_dim))
+                s.raw_k.append(np.zeros((0, head_dim), np.float32))
+                s.raw_v.append(np.zeros((0, head_dim), np.float32))
             self.seqs.append(s)
 
     # -- write path ---------------------------------------------------------
@@ -341,6 +352,9 @@ class OracleCache:
         once, at write time."""
         s = self.seqs[b]
         n = k.shape[1]
+        for h in range(self.hkv):
+            s.raw_k[h] = np.concatenate([s.raw_k[h], k[h].astype(np.float32)])
+            s.raw_v[h] = np.concatenate([s.raw_v[h], v[h].astype(np.float32)])
         for i in range(n):
             p = s.pos_total + i
             for h in range(self.hkv):
@@ -370,13 +384,26 @@ class OracleCache:
         [Hq, D].  Query head j reads KV head j // G (consecutive query heads
         share a KV head).  With ``accumulate`` the H2O scores of every attended
         token (sinks included) grow by the column sums of this step's
-        probabilities."""
+        probabilities.
+
+        Hybrid precision (bf16_window = W > 0; "KV Cache optimization
+        techniques" section 1.3): a held token whose position is one of the
+        last W (>= pos_total - W) attends with its unquantised bf16 values,
+        every older one with its codes.  Reading: the page's "recent" slice
+        is the most recent tokens (its code slices the oldest, a bug), over a
+        window of fixed length that slides with the sequence."""
         s = self.seqs[b]
         out = np.zeros((self.hq, self.d), np.float64)
         for h in range(self.hkv):
             hs = s.heads[h]
-            keys = np.vstack([s.sink_k[h].astype(np.float64), dequantize(hs.kcodes, hs.kscale)])
-            vals = np.vstack([s.sink_v[h].astype(np.float64), dequantize(hs.vcodes, hs.vscale)])
+            kq = dequantize(hs.kcodes, hs.kscale)
+            vq = dequantize(hs.vcodes, hs.vscale)
+            if self.bf16_window > 0:
+                recent = hs.pos >= s.pos_total - self.bf16_window
+                kq[recent] = s.raw_k[h][hs.pos[recent]].astype(np.float64)
+                vq[recent] = s.raw_v[h][hs.pos[recent]].astype(np.float64)
+            keys = np.vstack([s.sink_k[h].astype(np.float64), kq])
+            vals = np.vstack([s.sink_v[h].astype(np.float64), vq])
             qg = q[h * self.group:(h + 1) * self.group]
             o, p = attention(qg, keys, vals, sm_scale)
             out[h * self.group:(h + 1) * self.group] = o

@@ -431,3 +431,88 @@ def test_blocks_against_numpy_means():
         # whole blocks only, never the recent window or the unfilled last block
         assert (~keep).sum() == 16 * n_evict
         assert keep[16 * n_cand:].all()
+
+
+# ---------------------------------------------------------------------------
+# Hybrid precision (the last W positions attend in bf16)
+# ---------------------------------------------------------------------------
+
+def _bf16_round(x):
+    b = np.asarray(x, np.float32).view(np.uint32)
+    b = ((b + np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)).astype(np.uint16)
+    return O.bf16_bits_to_f32(b)
+
+
+def test_hybrid_window_covering_the_context_is_bf16_attention():
+    """A window longer than the sequence keeps every token unquantised: the
+    output is plain fp64 attention over the bf16 inputs (torch SDPA witness
+    with the KV heads repeated for GQA)."""
+    rng = np.random.default_rng(40)
+    Hq, Hkv, n = 8, 2, 45
+    k = _bf16_round(rng.standard_normal((Hkv, n, 128)) * 2.0)
+    v = _bf16_round(rng.standard_normal((Hkv, n, 128)))
+    q = _bf16_round(rng.standard_normal((Hq, 128)))
+    c = O.OracleCache(1, Hq, Hkv, 4, bf16_window=1000)
+    c.append(0, k, v)
+    out = c.attend(0, q)
+    K = torch.from_numpy(k).double().repeat_interleave(Hq // Hkv, dim=0)
+    V = torch.from_numpy(v).double().repeat_interleave(Hq // Hkv, dim=0)
+    ref = torch.nn.functional.scaled_dot_product_attention(torch.from_numpy(q).double()[:, None, :], K, V)[:, 0, :]
+    np.testing.assert_allclose(out, ref.numpy(), rtol=0, atol=1e-12)
+    # and it differs from the INT4 cache: the window matters
+    plain = O.OracleCache(1, Hq, Hkv, 4)
+    plain.append(0, k, v)
+    assert np.abs(plain.attend(0, q) - out).max() > 1e-3
+
+
+def test_hybrid_window_zero_is_the_quantised_cache():
+    rng = np.random.default_rng(41)
+    k = _bf16_round(rng.standard_normal((2, 30, 128)))
+    v = _bf16_round(rng.standard_normal((2, 30, 128)))
+    q = _bf16_round(rng.standard_normal((4, 128)))
+    a, b = O.OracleCache(1, 4, 2, 8), O.OracleCache(1, 4, 2, 8, bf16_window=0)
+    a.append(0, k, v)
+    b.append(0, k, v)
+    assert np.array_equal(a.attend(0, q), b.attend(0, q))
+    for h in range(2):
+        assert np.array_equal(a.seqs[0].heads[h].score, b.seqs[0].heads[h].score)
+
+
+def test_hybrid_window_boundary_brute_force():
+    """One KV head, one query, INT4, window 3: every key row has one large
+    outlier, so INT4 rounds its other entries to 0 and the choice of
+    precision per token is visible.  Brute force in plain Python: positions
+    0-3 are sinks (bf16), positions >= P - 3 use the bf16 values, the rest
+    code * scale; checked before and after one more token moves position
+    P - 3 out of the window."""
+    rng = np.random.default_rng(42)
+    n = 10
+    base = rng.uniform(0.2, 0.6, (1, n + 1, 128))
+    base[..., 0] = 60.0
+    k = _bf16_round(base)
+    v = _bf16_round(rng.uniform(-1.0, 1.0, (1, n + 1, 128)))
+    q = _bf16_round(rng.uniform(-1.0, 1.0, (1, 128)))
+    q[0, 0] = 0.0  # the outlier column does not decide the logits
+
+    def brute(ntok, window):
+        kc, ks = O.quantize_rows(k[0, :ntok], 4)
+        vc, vs = O.quantize_rows(v[0, :ntok], 4)
+        logits, rows = [], []
+        for p in range(ntok):
+            exact = p < 4 or p >= ntok - window
+            kr = [float(x) for x in k[0, p]] if exact else [float(kc[p, d]) * float(ks[p]) for d in range(128)]
+            vr = [float(x) for x in v[0, p]] if exact else [float(vc[p, d]) * float(vs[p]) for d in range(128)]
+            logits.append(sum(float(q[0, d]) * kr[d] for d in range(128)) / math.sqrt(128))
+            rows.append(vr)
+        m = max(logits)
+        e = [math.exp(x - m) for x in logits]
+        z = sum(e)
+        return np.array([sum(e[p] / z * rows[p][d] for p in range(ntok)) for d in range(128)])
+
+    c = O.OracleCache(1, 1, 1, 4, bf16_window=3)
+    c.append(0, k[:, :n], v[:, :n])
+    got = c.attend(0, q, accumulate=False)[0]
+    np.testing.assert_allclose(got, brute(n, 3), rtol=0, atol=1e-12)
+    assert np.abs(got - brute(n, 0)).max() > 1e-4 and np.abs(got - brute(n, n)).max() > 1e-4
+    c.append(0, k[:, n:n + 1], v[:, n:n + 1])
+    np.testing.assert_allclose(c.attend(0, q, accumulate=False)[0], brute(n + 1, 3), rtol=0, atol=1e-12)
