@@ -23,14 +23,15 @@ KVC_EVICT_BLOCK = 2
 KVC_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 BUF = dict(K_CODES=0, V_CODES=1, K_SCALE=2, V_SCALE=3, SLOT_POS=4, SCORE=5, SINK_K=6, SINK_V=7,
-           SINK_SCORE=8, BLOCK_TABLE=9, SEQ_SLOTS=10, SEQ_POS=11, FREE_STACK=12, COUNTERS=13, PLAN=14)
+           SINK_SCORE=8, BLOCK_TABLE=9, SEQ_SLOTS=10, SEQ_POS=11, FREE_STACK=12, COUNTERS=13, PLAN=14,
+           RING_K=15, RING_V=16, RING_SCORE=17)
 
 
 class KvcConfig(ctypes.Structure):
     _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32), ("bits", ctypes.c_int32),
                 ("num_blocks", ctypes.c_int32), ("max_batch", ctypes.c_int32),
-                ("max_blocks_per_seq", ctypes.c_int32)]
+                ("max_blocks_per_seq", ctypes.c_int32), ("bf16_window", ctypes.c_int32)]
 
 
 class KvcEvictParams(ctypes.Structure):

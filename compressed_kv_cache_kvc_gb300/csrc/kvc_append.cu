@@ -9,6 +9,11 @@
 // One CTA per sequence: thread 0 takes the pages the new tokens need from the
 // device free-block stack and advances the sequence lengths; after a barrier
 // every warp quantises rows (one warp per 128-value row, 4 values per lane).
+//
+// Hybrid precision ("KV Cache optimization techniques" section 1.3): with a
+// window of W positions, a new token goes to the bf16 ring of its (sequence,
+// KV head), slot (position - 4) mod W, and enters the pool, quantised from
+// the ring, only when a later append pushes it out of the window.
 #include "kvc_internal.h"
 
 namespace kvc {
@@ -18,18 +23,71 @@ __device__ __forceinline__ float bf16_to_f32(uint32_t bits16) {
   return __uint_as_float(bits16 << 16);
 }
 
+// Quantise one 128-value row (4 values per lane, one warp) into pool slot
+// `slot` of (sequence b, KV head h): codes, scale, and for K the position and
+// the initial score.
+template <int BITS>
+__device__ __forceinline__ void quantize_row(const DevState& s, int b, int h, int kv, int slot, int p, float score,
+                                             uint2 raw, int lane) {
+  constexpr float kQmax = BITS == 8 ? 127.0f : 7.0f;
+  constexpr int kLo = BITS == 8 ? -127 : -8;
+  constexpr int kHi = BITS == 8 ? 127 : 7;
+  float x[4];
+  x[0] = bf16_to_f32(raw.x & 0xFFFFu);
+  x[1] = bf16_to_f32(raw.x >> 16);
+  x[2] = bf16_to_f32(raw.y & 0xFFFFu);
+  x[3] = bf16_to_f32(raw.y >> 16);
+  float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float scale = __fdiv_rn(amax, kQmax);
+  int c[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    int q = 0;
+    if (scale > 0.0f) q = __float2int_rn(__fdiv_rn(x[e], scale));
+    c[e] = min(max(q, kLo), kHi);
+  }
+  const int page = slot / kPage;
+  const int off = slot % kPage;
+  const int blk = s.block_table[(size_t)b * s.max_bps + page];
+  if ((unsigned)blk >= (unsigned)s.num_blocks) {
+    if (lane == 0) atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
+    return;
+  }
+  const size_t sidx = ((size_t)blk * s.hkv + h) * kPage + off;
+  uint8_t* codes = (kv ? s.v_codes : s.k_codes) + sidx * s.row_bytes;
+  if (BITS == 8) {
+    const uint32_t packed = (uint32_t)(c[0] & 0xFF) | ((uint32_t)(c[1] & 0xFF) << 8) |
+                            ((uint32_t)(c[2] & 0xFF) << 16) | ((uint32_t)(c[3] & 0xFF) << 24);
+    *reinterpret_cast<uint32_t*>(codes + lane * 4) = packed;
+  } else {
+    const uint32_t packed = (uint32_t)(c[0] & 0xF) | ((uint32_t)(c[1] & 0xF) << 4) |
+                            ((uint32_t)(c[2] & 0xF) << 8) | ((uint32_t)(c[3] & 0xF) << 12);
+    *reinterpret_cast<uint16_t*>(codes + lane * 2) = (uint16_t)packed;
+  }
+  if (lane == 0) {
+    (kv ? s.v_scale : s.k_scale)[sidx] = scale;
+    if (kv == 0) {
+      s.slot_pos[sidx] = p;
+      s.score[sidx] = score;
+    }
+  }
+}
+
 template <int BITS>
 __global__ void __launch_bounds__(512) append_kernel(DevState s, int seq_begin, int n_new,
                                                      const uint16_t* __restrict__ kin,
                                                      const uint16_t* __restrict__ vin) {
   const int bl = blockIdx.x;
   const int b = seq_begin + bl;
-  __shared__ int sh_slots, sh_pos, sh_ok;
+  __shared__ int sh_slots, sh_pos, sh_ok, sh_lo, sh_hi;
   if (threadIdx.x == 0) {
     const int slots = s.seq_slots[b];
     const int pos = s.seq_pos[b];
-    const int n_sink_new = min(n_new, max(0, kSinks - pos));
-    const int new_slots = slots + (n_new - n_sink_new);
+    int lo, hi;  // positions that enter the pool
+    pool_range(pos, n_new, s.ring, &lo, &hi);
+    const int new_slots = slots + (hi - lo);
     const int old_pages = (slots + kPage - 1) / kPage;
     const int new_pages = (new_slots + kPage - 1) / kPage;
     const int need = new_pages - old_pages;
@@ -55,6 +113,8 @@ __global__ void __launch_bounds__(512) append_kernel(DevState s, int seq_begin, 
     sh_slots = slots;
     sh_pos = pos;
     sh_ok = ok;
+    sh_lo = lo;
+    sh_hi = hi;
   }
   __syncthreads();
   if (!sh_ok) return;
@@ -63,13 +123,27 @@ __global__ void __launch_bounds__(512) append_kernel(DevState s, int seq_begin, 
   const int warp = threadIdx.x >> 5;
   const int nwarps = blockDim.x >> 5;
   const int hkv = s.hkv;
-  const int total_rows = n_new * hkv * 2;
-  const int first_quant_pos = max(sh_pos, kSinks);
-  constexpr float kQmax = BITS == 8 ? 127.0f : 7.0f;
-  constexpr int kLo = BITS == 8 ? -127 : -8;
-  constexpr int kHi = BITS == 8 ? 127 : 7;
+  const int W = s.ring;
 
-  for (int row = warp; row < total_rows; row += nwarps) {
+  // ---- hybrid precision: the window tokens this append pushes out (positions
+  // [lo, min(pos, hi)), all in the ring) are quantised into the pool with the
+  // score they gathered there, before any new token overwrites their slots
+  if (W > 0) {
+    const int n_aged = max(0, min(sh_pos, sh_hi) - sh_lo);
+    for (int row = warp; row < n_aged * hkv * 2; row += nwarps) {
+      const int kv = row & 1;
+      const int h = (row >> 1) % hkv;
+      const int a = sh_lo + (row >> 1) / hkv;
+      const size_t ridx = ((size_t)b * hkv + h) * W + (a - kSinks) % W;
+      const uint16_t* src = (kv ? s.ring_v : s.ring_k) + ridx * kHeadDim;
+      const uint2 raw = *reinterpret_cast<const uint2*>(src + lane * 4);
+      quantize_row<BITS>(s, b, h, kv, sh_slots + (a - sh_lo), a, s.ring_score[ridx], raw, lane);
+    }
+    __syncthreads();
+  }
+
+  // ---- the new tokens: sinks, pool (quantised), or the window ring (bf16)
+  for (int row = warp; row < n_new * hkv * 2; row += nwarps) {
     const int kv = row & 1;
     const int h = (row >> 1) % hkv;
     const int i = (row >> 1) / hkv;
@@ -80,49 +154,13 @@ __global__ void __launch_bounds__(512) append_kernel(DevState s, int seq_begin, 
       uint16_t* dst = (kv ? s.sink_v : s.sink_k) + (((size_t)b * hkv + h) * kSinks + p) * kHeadDim;
       *reinterpret_cast<uint2*>(dst + lane * 4) = raw;
       if (kv == 0 && lane == 0) s.sink_score[((size_t)b * hkv + h) * kSinks + p] = 0.0f;
-      continue;
-    }
-    float x[4];
-    x[0] = bf16_to_f32(raw.x & 0xFFFFu);
-    x[1] = bf16_to_f32(raw.x >> 16);
-    x[2] = bf16_to_f32(raw.y & 0xFFFFu);
-    x[3] = bf16_to_f32(raw.y >> 16);
-    float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float scale = __fdiv_rn(amax, kQmax);
-    int c[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      int q = 0;
-      if (scale > 0.0f) q = __float2int_rn(__fdiv_rn(x[e], scale));
-      c[e] = min(max(q, kLo), kHi);
-    }
-    const int slot = sh_slots + (p - first_quant_pos);
-    const int page = slot / kPage;
-    const int off = slot % kPage;
-    const int blk = s.block_table[(size_t)b * s.max_bps + page];
-    if ((unsigned)blk >= (unsigned)s.num_blocks) {
-      if (lane == 0) atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
-      continue;
-    }
-    const size_t sidx = ((size_t)blk * hkv + h) * kPage + off;
-    uint8_t* codes = (kv ? s.v_codes : s.k_codes) + sidx * s.row_bytes;
-    if (BITS == 8) {
-      const uint32_t packed = (uint32_t)(c[0] & 0xFF) | ((uint32_t)(c[1] & 0xFF) << 8) |
-                              ((uint32_t)(c[2] & 0xFF) << 16) | ((uint32_t)(c[3] & 0xFF) << 24);
-      *reinterpret_cast<uint32_t*>(codes + lane * 4) = packed;
+    } else if (p < sh_hi) {
+      quantize_row<BITS>(s, b, h, kv, sh_slots + (p - sh_lo), p, 0.0f, raw, lane);
     } else {
-      const uint32_t packed = (uint32_t)(c[0] & 0xF) | ((uint32_t)(c[1] & 0xF) << 4) |
-                              ((uint32_t)(c[2] & 0xF) << 8) | ((uint32_t)(c[3] & 0xF) << 12);
-      *reinterpret_cast<uint16_t*>(codes + lane * 2) = (uint16_t)packed;
-    }
-    if (lane == 0) {
-      (kv ? s.v_scale : s.k_scale)[sidx] = scale;
-      if (kv == 0) {
-        s.slot_pos[sidx] = p;
-        s.score[sidx] = 0.0f;
-      }
+      const size_t ridx = ((size_t)b * hkv + h) * W + (p - kSinks) % W;
+      uint16_t* dst = (kv ? s.ring_v : s.ring_k) + ridx * kHeadDim;
+      *reinterpret_cast<uint2*>(dst + lane * 4) = raw;
+      if (kv == 0 && lane == 0) s.ring_score[ridx] = 0.0f;
     }
   }
 }

@@ -532,6 +532,7 @@ __global__ void __launch_bounds__(kMergeThreads, 2) attn_merge_kernel(DevState s
   const int bl = blockIdx.y;
   merge_phase(s, seq_begin, batch, cum, h, bl, q, out, qk_scale_log2, w, accumulate != 0, ms);
   if (!accumulate) return;
+  ring_score_pass(s, w, seq_begin + bl, bl, h, ms);
   // score pass: the sequence's block-table row is staged in shared memory
   // (when it fits) and each thread handles 4 slots with all loads issued first
   const int b = seq_begin + bl;

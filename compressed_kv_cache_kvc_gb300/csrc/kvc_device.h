@@ -187,11 +187,13 @@ struct MergeShared {
   float invL[kMaxGroup];        // 1 / global sum per query head
 };
 
-// Merge, for one (sequence bl, KV head h), the stream-K partials of its pages
-// and its bf16 sinks: global (M, L) per query head of the group, bf16 output
-// o = (sum of rescaled partials + sinks) / L, and, with `accumulate`, the sink
-// scores' H2O increments.  `cum` is the page prefix of the slice.  Any block
-// size that is a multiple of 32; ends after a barrier with ms filled.
+// Merge, for one (sequence bl, KV head h), the stream-K partials of its pages,
+// the partials of its bf16 window (hybrid precision, one per chunk that holds
+// tokens) and its bf16 sinks: global (M, L) per query head of the group, bf16
+// output o = (sum of rescaled partials + sinks) / L, and, with `accumulate`,
+// the sink scores' H2O increments.  `cum` is the page prefix of the slice.
+// Any block size that is a multiple of 32; ends after a barrier with ms
+// filled.
 __device__ __forceinline__ void merge_phase(const DevState& s, int seq_begin, int batch, const int* cum, int h,
                                             int bl, const uint16_t* __restrict__ q, uint16_t* __restrict__ out,
                                             float qk_scale_log2, const AttnWork& w, bool accumulate,
@@ -205,6 +207,9 @@ __device__ __forceinline__ void merge_phase(const DevState& s, int seq_begin, in
   const int nwarps = blockDim.x >> 5;
   const int pair = bl * hkv + h;
   const int npg = cum[bl + 1] - cum[bl];
+  const int nrc = (ring_count(P, s.ring) + kRingChunk - 1) / kRingChunk;  // window chunks with tokens
+  const float* rpo = w.ring_po + (size_t)pair * w.ring_chunks * G * kHeadDim;
+  const float* rpml = w.ring_pml + (size_t)pair * w.ring_chunks * G * 2;
   int i_first = 0, i_last = -1;
   if (npg > 0) {
     const long long T = (long long)hkv * cum[batch];
@@ -258,6 +263,7 @@ __device__ __forceinline__ void merge_phase(const DevState& s, int seq_begin, in
     const int g = warp;
     float M = kNegBig;
     for (int i = i_first + lane; i <= i_last; i += 32) M = fmaxf(M, w.part_ml[(((size_t)pair + i) * G + g) * 2]);
+    for (int i = lane; i < nrc; i += 32) M = fmaxf(M, rpml[((size_t)i * G + g) * 2]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
 #pragma unroll
@@ -266,6 +272,10 @@ __device__ __forceinline__ void merge_phase(const DevState& s, int seq_begin, in
     for (int i = i_first + lane; i <= i_last; i += 32) {
       const size_t pi = ((size_t)pair + i) * G + g;
       L += fast_exp2(w.part_ml[pi * 2] - M) * w.part_ml[pi * 2 + 1];
+    }
+    for (int i = lane; i < nrc; i += 32) {
+      const size_t pi = (size_t)i * G + g;
+      L += fast_exp2(rpml[pi * 2] - M) * rpml[pi * 2 + 1];
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
@@ -292,12 +302,34 @@ __device__ __forceinline__ void merge_phase(const DevState& s, int seq_begin, in
       const size_t pi = ((size_t)pair + i) * G + g;
       o += fast_exp2(w.part_ml[pi * 2] - M) * w.part_o[pi * kHeadDim + d];
     }
+    for (int i = 0; i < nrc; ++i) {
+      const size_t pi = (size_t)i * G + g;
+      o += fast_exp2(rpml[pi * 2] - M) * rpo[pi * kHeadDim + d];
+    }
     out[((size_t)bl * s.hq + h * G + g) * kHeadDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(o * ms.invL[g]));
   }
   if (accumulate && (int)threadIdx.x < ns) {
     float inc = 0.0f;
     for (int g = 0; g < G; ++g) inc += fast_exp2(ms.sl[g][threadIdx.x] - ms.M[g]) * ms.invL[g];
     s.sink_score[((size_t)b * hkv + h) * kSinks + threadIdx.x] += inc;
+  }
+}
+
+// H2O increments of the bf16 window's tokens (hybrid precision), from the
+// logits the window attention spilled; same arithmetic and order as
+// h2o_increment.  After merge_phase (ms filled); any block size.
+__device__ __forceinline__ void ring_score_pass(const DevState& s, const AttnWork& w, int b, int bl, int h,
+                                                const MergeShared& ms) {
+  const int W = s.ring;
+  if (W <= 0) return;
+  const int G = s.group;
+  const int nr = ring_count(s.seq_pos[b], W);
+  const float* lg = w.ring_lg + ((size_t)bl * s.hkv + h) * G * W;
+  float* sc = s.ring_score + ((size_t)b * s.hkv + h) * W;
+  for (int r = threadIdx.x; r < nr; r += blockDim.x) {
+    float inc = 0.0f;
+    for (int g = 0; g < G; ++g) inc = __fmaf_rn(fast_exp2(lg[(size_t)g * W + r] - ms.M[g]), ms.invL[g], inc);
+    sc[r] += inc;
   }
 }
 

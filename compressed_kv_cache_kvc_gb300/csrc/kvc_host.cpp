@@ -39,6 +39,8 @@ kvc_status config_check(const kvc_config* c) {
   if (c->head_dim != kvc::kHeadDim || c->page_size != kvc::kPage || (c->bits != 8 && c->bits != 4) ||
       c->num_q_heads / c->num_kv_heads > kvc::kMaxGroup)
     return KVC_ERR_UNSUPPORTED;
+  if (c->bf16_window < 0) return KVC_ERR_INVALID_ARG;
+  if (c->bf16_window > kvc::kMaxRing) return KVC_ERR_UNSUPPORTED;
   // 32-bit slot arithmetic inside the kernels
   if ((double)c->num_blocks * c->num_kv_heads * kvc::kPage >= 2147483647.0 ||
       (double)c->max_blocks_per_seq * kvc::kPage > 2.0e9)
@@ -66,6 +68,10 @@ Layout make_layout(const kvc_config* c) {
   L.size[KVC_BUF_FREE_STACK] = (size_t)c->num_blocks * 4;
   L.size[KVC_BUF_COUNTERS] = (size_t)kvc::kCounters * 4;
   L.size[KVC_BUF_PLAN] = (size_t)c->max_batch * 2 * 4;
+  const size_t ring = (size_t)c->max_batch * c->num_kv_heads * c->bf16_window;
+  L.size[KVC_BUF_RING_K] = ring * kvc::kHeadDim * 2;
+  L.size[KVC_BUF_RING_V] = ring * kvc::kHeadDim * 2;
+  L.size[KVC_BUF_RING_SCORE] = ring * 4;
   size_t o = 0;
   for (int i = 0; i < KVC_BUF_COUNT; ++i) {
     L.off[i] = o;
@@ -113,8 +119,10 @@ int s_cap(const kvc_cache* c) { return c->cfg.max_blocks_per_seq * kvc::kPage; }
 
 // Workspace carving (all regions 256-byte aligned).
 struct WsLayout {
-  size_t part_o, part_ml, logits, stats, cum, ticket, moves, keys, pos, total;
+  size_t part_o, part_ml, logits, stats, cum, ticket, moves, keys, pos, ring_po, ring_pml, ring_lg, total;
 };
+
+int ring_chunks(const kvc_cache* c);
 
 WsLayout ws_layout(const kvc_cache* c, int batch) {
   const size_t G = c->cfg.num_q_heads / c->cfg.num_kv_heads;
@@ -141,8 +149,19 @@ WsLayout ws_layout(const kvc_cache* c, int batch) {
   o = align_up(o + pairs * cap * 4);
   w.pos = o;
   o = align_up(o + pairs * cap * 4);
+  const size_t rc = ring_chunks(c);
+  w.ring_po = o;
+  o = align_up(o + pairs * rc * G * kvc::kHeadDim * 4);
+  w.ring_pml = o;
+  o = align_up(o + pairs * rc * G * 2 * 4);
+  w.ring_lg = o;
+  o = align_up(o + pairs * G * (size_t)c->cfg.bf16_window * 4);
   w.total = o;
   return w;
+}
+
+int ring_chunks(const kvc_cache* c) {
+  return (c->cfg.bf16_window + kvc::kRingChunk - 1) / kvc::kRingChunk;
 }
 
 int sm_count(kvc_cache* c) {
@@ -199,6 +218,10 @@ void attention_plan(kvc_cache* c, int32_t seq_begin, int32_t batch, void* d_work
   w->stats = reinterpret_cast<float*>(ws + wl.stats);
   w->cum = reinterpret_cast<int*>(ws + wl.cum);
   w->seq_ticket = reinterpret_cast<int*>(ws + wl.ticket);
+  w->ring_po = reinterpret_cast<float*>(ws + wl.ring_po);
+  w->ring_pml = reinterpret_cast<float*>(ws + wl.ring_pml);
+  w->ring_lg = reinterpret_cast<float*>(ws + wl.ring_lg);
+  w->ring_chunks = ring_chunks(c);
   w->ncta = ncta;
   w->s_cap = s_cap(c);
   *total_pages = tp;
@@ -206,10 +229,13 @@ void attention_plan(kvc_cache* c, int32_t seq_begin, int32_t batch, void* d_work
 
 // The split-K attention launch, bracketed by the trace events when set (under
 // stream capture they become event-record nodes of the graph).
+// With no pages the launch is skipped unless `always` (kvc_decode_step: the
+// post kernel reads the page prefix and tickets that the split's first CTA
+// publishes, and a grid of one CTA with no pages does only that).
 kvc_status launch_split_traced(kvc_cache* c, int32_t seq_begin, int32_t batch, const void* d_q, float qk_scale_log2,
                                const kvc::AttnWork& w, bool h2o, long long total_pages, cudaStream_t st,
-                               int* launches) {
-  if (total_pages <= 0) return KVC_OK;
+                               int* launches, bool always = false) {
+  if (total_pages <= 0 && !always) return KVC_OK;
   const bool trace = c->trace_start && c->trace_stop;
   unsigned rec_flags = cudaEventRecordDefault;
   if (trace) {
@@ -228,15 +254,30 @@ kvc_status launch_split_traced(kvc_cache* c, int32_t seq_begin, int32_t batch, c
   return KVC_OK;
 }
 
+// The attention over the bf16 window (hybrid precision), when there is one.
+kvc_status launch_ring(kvc_cache* c, int32_t seq_begin, int32_t batch, const void* d_q, float qk_scale_log2,
+                       const kvc::AttnWork& w, cudaStream_t st, int* launches) {
+  if (c->cfg.bf16_window <= 0) return KVC_OK;
+  if (kvc::launch_attention_ring(c->dev, seq_begin, batch, static_cast<const uint16_t*>(d_q), qk_scale_log2, w,
+                                 st) != cudaSuccess)
+    return KVC_ERR_CUDA;
+  ++*launches;
+  return KVC_OK;
+}
+
 // Kept slots per sequence after a selection (the host mirror's plan).
-kvc_status evict_check(const kvc_evict_params* p) {
+// The window W of hybrid precision is always kept: the recent window (H2O)
+// or the StreamingLLM window must cover it.
+kvc_status evict_check(const kvc_cache* c, const kvc_evict_params* p) {
   if (!p) return KVC_ERR_INVALID_ARG;
+  const int W = c->cfg.bf16_window;
   if (p->mode == KVC_EVICT_H2O) {
-    if (p->recent < 0 || p->budget < kvc::kSinks + p->recent) return KVC_ERR_INVALID_ARG;
+    if (p->recent < W || p->budget < kvc::kSinks + p->recent) return KVC_ERR_INVALID_ARG;
   } else if (p->mode == KVC_EVICT_STREAMING) {
-    if (p->window < 1) return KVC_ERR_INVALID_ARG;
+    if (p->window < 1 || p->window < W) return KVC_ERR_INVALID_ARG;
   } else if (p->mode == KVC_EVICT_BLOCK) {
     if (p->recent < 0 || !(p->retention > 0.0 && p->retention <= 1.0)) return KVC_ERR_INVALID_ARG;
+    if (W > 0) return KVC_ERR_UNSUPPORTED;
   } else {
     return KVC_ERR_INVALID_ARG;
   }
@@ -251,16 +292,19 @@ int max_block_cand(const kvc_cache* c, int32_t seq_begin, int32_t batch, int rec
   return m;
 }
 
-int plan_keep(const kvc_evict_params* p, int S, int P) {
+// Pool slots kept out of S; the nr window tokens count inside the budget or
+// window.
+int plan_keep(const kvc_evict_params* p, int S, int P, int W) {
   const int ns = std::min(P, kvc::kSinks);
-  if (p->mode == KVC_EVICT_H2O) return (ns + S <= p->budget) ? S : p->budget - kvc::kSinks;
+  const int nr = kvc::ring_count(P, W);
+  if (p->mode == KVC_EVICT_H2O) return (ns + nr + S <= p->budget) ? S : p->budget - kvc::kSinks - nr;
   if (p->mode == KVC_EVICT_BLOCK) {
     // the device computes the same double expression
     const int n_cand = std::max(0, S - p->recent) / kvc::kPage;
     const int n_evict = (int)((double)n_cand * (1.0 - p->retention));
     return S - kvc::kPage * n_evict;
   }
-  return (S <= p->window) ? S : p->window;
+  return (nr + S <= p->window) ? S : p->window - nr;
 }
 
 }  // namespace
@@ -316,6 +360,10 @@ kvc_status kvc_cache_create(const kvc_config* cfg, void* d_state, size_t state_b
   d.free_stack = reinterpret_cast<int32_t*>(b + L.off[KVC_BUF_FREE_STACK]);
   d.counters = reinterpret_cast<int32_t*>(b + L.off[KVC_BUF_COUNTERS]);
   d.plan = reinterpret_cast<int32_t*>(b + L.off[KVC_BUF_PLAN]);
+  d.ring_k = reinterpret_cast<uint16_t*>(b + L.off[KVC_BUF_RING_K]);
+  d.ring_v = reinterpret_cast<uint16_t*>(b + L.off[KVC_BUF_RING_V]);
+  d.ring_score = reinterpret_cast<float*>(b + L.off[KVC_BUF_RING_SCORE]);
+  d.ring = cfg->bf16_window;
   d.hq = cfg->num_q_heads;
   d.hkv = cfg->num_kv_heads;
   d.group = cfg->num_q_heads / cfg->num_kv_heads;
@@ -410,9 +458,10 @@ kvc_status kvc_quantize_append(kvc_cache* c, int32_t seq_begin, int32_t batch, i
   std::vector<int32_t> new_slots(batch);
   for (int i = 0; i < batch; ++i) {
     const int b = seq_begin + i;
-    const long long n_sink_new = std::min<long long>(n_new, std::max(0, kvc::kSinks - c->pos[b]));
-    const long long ns = c->slots[b] + (n_new - n_sink_new);
     if ((long long)c->pos[b] + n_new > 2000000000LL) return KVC_ERR_CAPACITY;
+    int lo, hi;  // positions entering the pool (the device computes the same)
+    kvc::pool_range(c->pos[b], n_new, c->cfg.bf16_window, &lo, &hi);
+    const long long ns = (long long)c->slots[b] + (hi - lo);
     if ((ns + kvc::kPage - 1) / kvc::kPage > c->cfg.max_blocks_per_seq) return KVC_ERR_CAPACITY;
     need += pages_of((int)ns) - pages_of(c->slots[b]);
     new_slots[i] = (int32_t)ns;
@@ -447,6 +496,8 @@ kvc_status kvc_decode_attention(kvc_cache* c, int32_t seq_begin, int32_t batch, 
   int launches = 0;
   st0 = launch_split_traced(c, seq_begin, batch, d_q, qk_scale_log2, w, h2o, total_pages, st, &launches);
   if (st0 != KVC_OK) return st0;
+  st0 = launch_ring(c, seq_begin, batch, d_q, qk_scale_log2, w, st, &launches);
+  if (st0 != KVC_OK) return st0;
   if (kvc::launch_attention_merge(c->dev, seq_begin, batch, static_cast<const uint16_t*>(d_q),
                                   static_cast<uint16_t*>(d_out), qk_scale_log2, w, h2o, st) != cudaSuccess)
     return KVC_ERR_CUDA;
@@ -460,7 +511,10 @@ kvc_status kvc_h2o_select_evict(kvc_cache* c, int32_t seq_begin, int32_t batch, 
   if (!c) return KVC_ERR_INVALID_ARG;
   c->last_launches = 0;
   if (!range_ok(c, seq_begin, batch) || !p || !d_keep_mask) return KVC_ERR_INVALID_ARG;
-  if (evict_check(p) != KVC_OK) return KVC_ERR_INVALID_ARG;
+  {
+    const kvc_status e = evict_check(c, p);
+    if (e != KVC_OK) return e;
+  }
   const WsLayout wl = ws_layout(c, batch);
   if (!d_workspace || !aligned(d_workspace, kAlign) || workspace_bytes < wl.total) return KVC_ERR_INVALID_ARG;
   std::vector<int32_t> plan(batch);
@@ -468,7 +522,7 @@ kvc_status kvc_h2o_select_evict(kvc_cache* c, int32_t seq_begin, int32_t batch, 
   for (int i = 0; i < batch; ++i) {
     const int b = seq_begin + i;
     const int S = c->slots[b];
-    plan[i] = plan_keep(p, S, c->pos[b]);
+    plan[i] = plan_keep(p, S, c->pos[b], c->cfg.bf16_window);
     max_s = std::max(max_s, S);
   }
   if (p->mode == KVC_EVICT_BLOCK) {
@@ -552,7 +606,10 @@ kvc_status kvc_decode_step(kvc_cache* c, int32_t seq_begin, int32_t batch, const
                            void* d_workspace, size_t workspace_bytes, void* stream) {
   if (!c) return KVC_ERR_INVALID_ARG;
   c->last_launches = 0;
-  if (evict_check(params) != KVC_OK) return KVC_ERR_INVALID_ARG;
+  {
+    const kvc_status e = evict_check(c, params);
+    if (e != KVC_OK) return e;
+  }
   const bool block = params->mode == KVC_EVICT_BLOCK;
   if (block && c->cfg.max_blocks_per_seq > kvc::kMaxBlockPages) return KVC_ERR_UNSUPPORTED;
   kvc_status st0 =
@@ -568,13 +625,16 @@ kvc_status kvc_decode_step(kvc_cache* c, int32_t seq_begin, int32_t batch, const
   const float qk_scale_log2 = sm_scale * 1.4426950408889634f;
   const bool h2o = params->mode != KVC_EVICT_STREAMING;  // H2O scores (token or block selection)
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  st0 = launch_split_traced(c, seq_begin, batch, d_q, qk_scale_log2, w, h2o, total_pages, st, &launches);
+  st0 = launch_split_traced(c, seq_begin, batch, d_q, qk_scale_log2, w, h2o, total_pages, st, &launches,
+                            /*always=*/true);
+  if (st0 != KVC_OK) return st0;
+  st0 = launch_ring(c, seq_begin, batch, d_q, qk_scale_log2, w, st, &launches);
   if (st0 != KVC_OK) return st0;
   std::vector<int32_t> plan(batch);
   int max_s = 0;
   for (int i = 0; i < batch; ++i) {
     const int b = seq_begin + i;
-    plan[i] = plan_keep(params, c->slots[b], c->pos[b]);
+    plan[i] = plan_keep(params, c->slots[b], c->pos[b], c->cfg.bf16_window);
     max_s = std::max(max_s, c->slots[b]);
   }
   const WsLayout wl = ws_layout(c, batch);

@@ -31,8 +31,28 @@ struct DevState {
   int32_t* free_stack;  // [num_blocks]
   int32_t* counters;    // [0] free top, [1] status
   int32_t* plan;        // [max_batch][2]
+  uint16_t* ring_k;     // [max_batch][hkv][ring][128] bf16 (hybrid precision window)
+  uint16_t* ring_v;
+  float* ring_score;    // [max_batch][hkv][ring]
   int32_t hq, hkv, group, bits, row_bytes, num_blocks, max_batch, max_bps;
+  int32_t ring;         // hybrid window W (0: off); ring slot of position p >= 4 is (p - 4) % W
 };
+
+// Tokens held in the bf16 window of a sequence with P positions.
+__host__ __device__ inline int ring_count(int P, int W) {
+  if (W <= 0 || P <= kSinks) return 0;
+  return P - kSinks < W ? P - kSinks : W;
+}
+
+// Positions [pool_lo, pool_hi) enter the pool when n_new tokens are appended
+// to a sequence that has seen P: with a window, the tokens that leave it
+// (from the ring, then straight from the input), else every non-sink token.
+__host__ __device__ inline void pool_range(int P, int n_new, int W, int* lo, int* hi) {
+  const int a = P - W > kSinks ? P - W : kSinks;
+  const int e = P + n_new - W;
+  *lo = a;
+  *hi = e > a ? e : a;
+}
 
 enum { kCtrFreeTop = 0, kCtrStatus = 1 };
 
@@ -58,11 +78,17 @@ struct AttnWork {
   float* stats;     // [batch][hq][2]  global (M, L) per query head
   int* cum;         // [batch + 1] page prefix of the slice (written by split CTA 0)
   int* seq_ticket;  // [batch] per-sequence completion tickets (zeroed by split CTA 0)
+  float* ring_po;   // [batch][hkv][ring_chunks][group][128] partials of the bf16 window
+  float* ring_pml;  // [batch][hkv][ring_chunks][group][2]
+  float* ring_lg;   // [batch][hkv][group][ring] window logits (log2 domain)
+  int ring_chunks;  // ceil(W / kRingChunk), 0 without a window
   int ncta;         // grid size of the split kernel
   int s_cap;
 };
 
 constexpr int kMaxCallBatch = 1024;  // sequences per attention call (prefix table in shared memory)
+constexpr int kRingChunk = 64;       // window slots per CTA of the window attention
+constexpr int kMaxRing = 4096;
 constexpr int kMaxSplitCtas = 2048;
 
 // Raise a kernel's dynamic shared-memory limit to `bytes`, once per device
@@ -86,6 +112,10 @@ cudaError_t launch_fill_free_stack(const DevState& s, cudaStream_t st);
 cudaError_t launch_attention_split(const DevState& s, int seq_begin, int batch, const uint16_t* q,
                                    float qk_scale_log2, const AttnWork& w, bool spill_logits,
                                    cudaStream_t st);
+// Attention over the bf16 window (hybrid precision): one partial per
+// (sequence, KV head, chunk of kRingChunk slots), logits to w.ring_lg.
+cudaError_t launch_attention_ring(const DevState& s, int seq_begin, int batch, const uint16_t* q,
+                                  float qk_scale_log2, const AttnWork& w, cudaStream_t st);
 cudaError_t launch_attention_merge(const DevState& s, int seq_begin, int batch, const uint16_t* q,
                                    uint16_t* out, float qk_scale_log2, const AttnWork& w,
                                    bool accumulate_h2o, cudaStream_t st);

@@ -44,13 +44,16 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(DevState s, int seq
   uint8_t* mrow = mask + ((size_t)bl * s.hkv + h) * a.s_cap;
   bool keep_all;
   int n_keep, thr;
+  // the nr tokens of the bf16 window (hybrid precision) are kept and count
+  // inside the budget or window; the choice is among the pool slots
+  const int nr = ring_count(P, s.ring);
   if (a.mode == 0) {
-    keep_all = ns + S <= a.budget;
-    n_keep = a.budget - kSinks;
+    keep_all = ns + nr + S <= a.budget;
+    n_keep = a.budget - kSinks - nr;
     thr = P - a.recent;
   } else {
-    keep_all = S <= a.window;
-    n_keep = a.window;
+    keep_all = nr + S <= a.window;
+    n_keep = a.window - nr;
     thr = P - a.window;
   }
   if (keep_all) n_keep = S;

@@ -58,6 +58,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) step_post_kernel(DevState s, in
   // the selection's first radix histogram is built by the score pass
   for (int i = threadIdx.x; i < kRadixBins; i += blockDim.x) hist[i] = 0;
   merge_phase(s, seq_begin, batch, w.cum, h, bl, q, out, qk_scale_log2, w, h2o, ms);
+  if (h2o) ring_score_pass(s, w, seq_begin + bl, bl, h, ms);
 
   const int hkv = s.hkv;
   const int G = s.group;
@@ -67,13 +68,16 @@ __global__ void __launch_bounds__(NT, 1024 / NT) step_post_kernel(DevState s, in
   const size_t pair = (size_t)bl * hkv + h;
   bool keep_all;
   int n_keep, thr;
+  // the nr tokens of the bf16 window (hybrid precision) are kept and count
+  // inside the budget or window; the choice is among the pool slots
+  const int nr = ring_count(P, s.ring);
   if (a.mode == 0) {
-    keep_all = ns + S <= a.budget;
-    n_keep = a.budget - kSinks;
+    keep_all = ns + nr + S <= a.budget;
+    n_keep = a.budget - kSinks - nr;
     thr = P - a.recent;
   } else {
-    keep_all = S <= a.window;
-    n_keep = a.window;
+    keep_all = nr + S <= a.window;
+    n_keep = a.window - nr;
     thr = P - a.window;
   }
   if (keep_all) n_keep = S;

@@ -78,7 +78,23 @@ typedef struct {
   int32_t num_blocks;         /* physical blocks in the pool                    */
   int32_t max_batch;          /* sequences the cache holds                      */
   int32_t max_blocks_per_seq; /* block-table row length                         */
+  int32_t bf16_window;        /* hybrid precision: the last W positions of each
+                                 sequence are kept in bf16 (0 = off, W <= 4096);
+                                 see "Hybrid precision" below                   */
 } kvc_config;
+
+/* Hybrid precision (bf16_window = W > 0; "KV Cache optimization techniques"
+ * section 1.3, HybridPrecisionKVCache: recent tokens at 16 bits, older ones
+ * quantised).  The tokens at the last W positions of a sequence (after the
+ * sinks) live in a bf16 ring per (sequence, KV head), slot (position - 4)
+ * mod W, and attend with their exact bf16 values; a token enters the paged
+ * pool, quantised as kvc_quantize_append quantises, only when it leaves the
+ * window (the append that pushes it out quantises it from the ring, with the
+ * H2O score it gathered there).  Pool slots therefore hold only positions
+ * < P - W.  The ring tokens are always kept, so the selection requires
+ * recent >= W (H2O) or window >= W (StreamingLLM), counts them inside the
+ * budget or window, and chooses among the pool slots only; block-granular
+ * eviction is not available with a window (KVC_ERR_UNSUPPORTED). */
 
 /* Opaque host handle of one layer's cache (host mirror of the sequence
  * lengths, buffer offsets, launch policy). */
@@ -104,7 +120,11 @@ typedef enum {
                              [2..] plan scratch                                */
   KVC_BUF_PLAN = 14,      /* i32 [max_batch][2] (slots before, slots after) of
                              the last selection                                */
-  KVC_BUF_COUNT = 15
+  KVC_BUF_RING_K = 15,    /* bf16 [max_batch][Hkv][W][128] hybrid window;
+                             slot (position - 4) mod W; empty when W = 0       */
+  KVC_BUF_RING_V = 16,    /* bf16 [max_batch][Hkv][W][128]                      */
+  KVC_BUF_RING_SCORE = 17,/* f32 [max_batch][Hkv][W] H2O scores of the window   */
+  KVC_BUF_COUNT = 18
 } kvc_buffer_id;
 
 /* Flags of kvc_decode_attention. */

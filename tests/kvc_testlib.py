@@ -51,6 +51,21 @@ class StateView:
         self.free_stack = get("FREE_STACK", np.int32)
         self.counters = get("COUNTERS", np.int32)
         self.num_blocks = nb
+        self.W = getattr(cache, "bf16_window", 0)
+        if self.W > 0:
+            self.ring_k = get("RING_K", np.uint16).reshape(cache.max_batch, hkv, self.W, 128)
+            self.ring_v = get("RING_V", np.uint16).reshape(cache.max_batch, hkv, self.W, 128)
+            self.ring_score = get("RING_SCORE", np.float32).reshape(cache.max_batch, hkv, self.W)
+
+    def ring_head(self, b, h):
+        """(positions, K bf16 bits, V bf16 bits, scores) of the bf16 window of
+        (b, h), in position order: positions P - n .. P - 1 at ring slot
+        (position - 4) mod W."""
+        P = int(self.seen[b])
+        n = min(self.W, max(0, P - 4))
+        p = np.arange(P - n, P)
+        r = (p - 4) % self.W
+        return p, self.ring_k[b, h, r], self.ring_v[b, h, r], self.ring_score[b, h, r]
 
     def codes(self, raw):
         if self.bits == 8:

@@ -178,3 +178,35 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(L, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError):
         L.lib()
+
+
+def test_hybrid_window_validation(lib):
+    """bf16_window: negative is invalid, above 4096 unsupported; the ring
+    buffers take max_batch x Hkv x W rows of 128 bf16 for K and for V; the
+    selection needs the recent window (H2O) or the StreamingLLM window to
+    cover W, and block-granular eviction is unsupported with a window; the
+    host capacity check counts only the tokens that leave the window."""
+    L = lib.lib()
+    assert L.kvc_state_bytes(ctypes.byref(_cfg(lib, bf16_window=-1))) == 0
+    assert L.kvc_state_bytes(ctypes.byref(_cfg(lib, bf16_window=4097))) == 0
+    cfg = _cfg(lib, bf16_window=16, num_blocks=3, max_blocks_per_seq=2)
+    st, h, fs = _create(lib, cfg)
+    assert st == lib.KVC_OK
+    ptr, nb = ctypes.c_void_p(), ctypes.c_size_t()
+    assert L.kvc_cache_buffer(h, lib.BUF["RING_K"], ctypes.byref(ptr), ctypes.byref(nb)) == lib.KVC_OK
+    assert nb.value == 2 * 2 * 16 * 128 * 2
+    assert L.kvc_cache_buffer(h, lib.BUF["RING_SCORE"], ctypes.byref(ptr), ctypes.byref(nb)) == lib.KVC_OK
+    assert nb.value == 2 * 2 * 16 * 4
+    dummy = ctypes.c_void_p(fs.ptr.value)
+    ws = L.kvc_workspace_bytes(h, 1)
+    wsbuf = ctypes.create_string_buffer(ws + 512)
+    wsp = ctypes.c_void_p(ctypes.addressof(wsbuf) + (-ctypes.addressof(wsbuf)) % 256)
+    for prm, want in [(lib.KvcEvictParams(0, 100, 8, 0), lib.KVC_ERR_INVALID_ARG),      # recent < W
+                      (lib.KvcEvictParams(1, 0, 0, 8), lib.KVC_ERR_INVALID_ARG),        # window < W
+                      (lib.KvcEvictParams(2, 0, 8, 0, 0.5), lib.KVC_ERR_UNSUPPORTED)]:  # block + window
+        assert L.kvc_h2o_select_evict(h, 0, 1, ctypes.byref(prm), dummy, wsp, ws, None) == want
+        assert L.kvc_decode_step(h, 0, 1, dummy, dummy, dummy, dummy, ctypes.c_float(0.088), ctypes.byref(prm),
+                                 wsp, ws, None) == want
+    # 4 sinks + 16 window + 33 pool slots need 3 pages > 2
+    assert L.kvc_quantize_append(h, 0, 1, 53, dummy, dummy, None) == lib.KVC_ERR_CAPACITY
+    L.kvc_cache_destroy(h)
