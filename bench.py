@@ -546,7 +546,8 @@ def workload_report(args, name: str):
     per_slot = 2 * (128 * w.bits // 8) + 2 * 4
     caches, inputs = [], []
     for l in range(layers):
-        c = KVCache(Hq, Hkv, w.bits, nblocks, B, mbps, block_order=order, device=dev)
+        c = KVCache(Hq, Hkv, w.bits, nblocks, B, mbps, block_order=order, device=dev,
+                    bf16_window=args.bf16_window)
         q, k, v, kn, vn = W.gen_layer_torch(w, l, dev)
         if np.all(lengths == T):
             c.quantize_append(k, v)
@@ -586,8 +587,22 @@ def workload_report(args, name: str):
             step()
         torch.cuda.synchronize()
     snaps = [c.state_view.clone() for c in caches]
-    slots = np.array([[c.lengths(b)[0] for b in range(B)] for c in caches])  # before the step's append
-    kv_bytes = int(((slots + 1) * per_slot).sum()) * Hkv + layers * B * Hkv * 4 * 2 * 128 * 2
+    def step_kv_bytes(pool_only=False):
+        """What the step's attention reads: the pool after the append (one
+        more slot per sequence: the new token, or with a bf16 window the
+        token leaving it), the bf16 sinks and the bf16 window (the split-K
+        kernel reads the pool and the sinks, the window kernel the window)."""
+        tot = 0
+        for c in caches:
+            for b in range(B):
+                S, P = c.lengths(b)
+                pool = S + (1 if P + 1 - args.bf16_window > 4 else 0) if args.bf16_window else S + 1
+                ring = 0 if pool_only else min(args.bf16_window, max(0, P + 1 - 4))
+                tot += (pool * per_slot + (ring + 4) * 2 * 128 * 2) * Hkv
+        return tot
+
+    kv_bytes = step_kv_bytes()
+    split_bytes = step_kv_bytes(pool_only=True)
 
     def restore():
         for c, sn in zip(caches, snaps):
@@ -636,14 +651,15 @@ def workload_report(args, name: str):
     attn = float(np.median(attn_ms))
     line = {"workload": name, "layers": layers, "batch": B, "bits": w.bits,
             "mode": ("block, retention %g" % args.retention) if args.evict == "block" else w.mode,
+            "bf16_window": args.bf16_window,
             "budgets": ({"schedule": args.schedule, "first": budgets[0], "middle": budgets[layers // 2],
                          "last": budgets[-1]} if args.schedule and w.mode == "h2o" else budgets[0]),
             "first_step": {"ms": ms, "kv_bytes": kv_bytes, "step_gbs": kv_bytes / (ms * 1e-3) / 1e9,
                            "step_frac_of_peak": kv_bytes / (ms * 1e-3) / 1e9 / peak,
                            "seq_steps_per_s": B / (ms * 1e-3),
                            "split_us_per_layer": attn * 1e3,
-                           "split_gbs": kv_bytes / layers / (attn * 1e-3) / 1e9,
-                           "split_frac_of_peak": kv_bytes / layers / (attn * 1e-3) / 1e9 / peak},
+                           "split_gbs": split_bytes / layers / (attn * 1e-3) / 1e9,
+                           "split_frac_of_peak": split_bytes / layers / (attn * 1e-3) / 1e9 / peak},
             "peak_gbs": peak, "steps_timed": args.steps}
     if w.steps > 1:
         # the workload's consecutive steps from the prefill, without restoring
@@ -651,8 +667,7 @@ def workload_report(args, name: str):
         per_step = []
         total_bytes = 0
         for _ in range(w.steps):
-            lens = np.array([[c.lengths(b)[0] for b in range(B)] for c in caches])
-            total_bytes += int(((lens + 1) * per_slot).sum()) * Hkv + layers * B * Hkv * 4 * 2 * 128 * 2
+            total_bytes += step_kv_bytes()
             with torch.cuda.stream(stream):
                 ev0.record(stream)
                 step()
@@ -687,6 +702,8 @@ def main():
     ap.add_argument("--evict", default=None, choices=["block"],
                     help="report mode: block-granular eviction instead of the workload's mode")
     ap.add_argument("--retention", type=float, default=0.25, help="report mode, --evict block: pages kept")
+    ap.add_argument("--bf16-window", type=int, default=0,
+                    help="report mode: hybrid precision, the last W positions kept in bf16 (W <= recent)")
     ap.add_argument("--oracle-child", nargs=2, type=int, default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.oracle_child is not None:

@@ -12,10 +12,9 @@
 // ldmatrix row addresses fall in different banks).  QK^T: each warp takes 16
 // slots and runs mma.sync m16n8k16 with bf16 operands (slots on M, query
 // heads on N, padded to 8): the query's own bf16 bits and the stored bf16
-// keys multiply exactly, the sums accumulate in fp32.  PV: thread d owns head
-// dimension d for every query head and accumulates the probabilities times
-// V[., d] in fp32 (the probabilities, one small tile, are read from shared
-// memory as broadcasts).
+// keys multiply exactly, the sums accumulate in fp32.  PV: mma.sync again,
+// head dimensions on M (32 per warp), query heads on N, slots on K, with the
+// probabilities split into two bf16 parts (16 significant bits in all).
 #include <cuda_bf16.h>
 
 #include "kvc_device.h"
@@ -58,11 +57,16 @@ __global__ void __launch_bounds__(kRingThreads) attn_ring_kernel(DevState s, int
   const int pair = bl * hkv + h;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
-  // ---- stage the chunk's rows
+  // ---- stage the chunk's rows: K, then V as a second group that lands
+  // while QK^T and the softmax run
   const size_t row0 = ((size_t)b * hkv + h) * W + slot0;
   for (int i = threadIdx.x; i < n_here * (kHeadDim / 8); i += kRingThreads) {
     const int row = i / (kHeadDim / 8), ch = i % (kHeadDim / 8);
     cp_async16(smem_addr(&sk[row][ch * 8]), s.ring_k + (row0 + row) * kHeadDim + ch * 8);
+  }
+  asm volatile("cp.async.commit_group;\n" ::);
+  for (int i = threadIdx.x; i < n_here * (kHeadDim / 8); i += kRingThreads) {
+    const int row = i / (kHeadDim / 8), ch = i % (kHeadDim / 8);
     cp_async16(smem_addr(&sv[row][ch * 8]), s.ring_v + (row0 + row) * kHeadDim + ch * 8);
   }
   asm volatile("cp.async.commit_group;\n" ::);
@@ -79,7 +83,7 @@ __global__ void __launch_bounds__(kRingThreads) attn_ring_kernel(DevState s, int
       bq[kk][1] = n < G ? qr[8 * kk + 4 + c] : 0u;
     }
   }
-  asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+  asm volatile("cp.async.wait_group 1;\n" ::: "memory");  // K is in
   __syncthreads();
 
   // ---- logits of 16 slots per warp
@@ -128,34 +132,70 @@ __global__ void __launch_bounds__(kRingThreads) attn_ring_kernel(DevState s, int
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < n_here * kMaxGroup; i += kRingThreads) {
+  // probabilities of the k-steps' slots (0 past n_here) and zero V rows past
+  // n_here in the last k-step: their probability is 0, but 0 times stale
+  // shared memory could be NaN
+  const int kt = (n_here + 15) >> 4;  // 16-slot k-steps of PV
+  for (int i = threadIdx.x; i < 16 * kt * kMaxGroup; i += kRingThreads) {
     const int t = i / kMaxGroup, g = i % kMaxGroup;
-    sp[t][g] = g < G ? fast_exp2(sp[t][g] - sm_m[g]) : 0.0f;
+    sp[t][g] = (t < n_here && g < G) ? fast_exp2(sp[t][g] - sm_m[g]) : 0.0f;
   }
+  for (int i = threadIdx.x; i < (16 * kt - n_here) * (kHeadDim / 8); i += kRingThreads)
+    *reinterpret_cast<uint4*>(&sv[n_here + i / (kHeadDim / 8)][(i % (kHeadDim / 8)) * 8]) = make_uint4(0u, 0u, 0u, 0u);
+  asm volatile("cp.async.wait_group 0;\n" ::: "memory");  // V is in
   __syncthreads();
 
-  // ---- o[g][d] = sum over the chunk's slots of p[t][g] * V[t][d]
-  const int d = threadIdx.x;
-  float o[kMaxGroup];
+  // ---- O^T (head dims x query heads) = V^T . P on the tensor cores: warp w
+  // takes dims 32w .. 32w + 31 (two M tiles), the slots are K.  V^T comes
+  // from the staged rows by ldmatrix.trans; P enters as two bf16 parts, hi =
+  // bf16(p) and lo = bf16(p - hi) (p - hi is exact in fp32), so the operand
+  // carries 16 significant bits and the products are exact.
+  float oc[2][4];
 #pragma unroll
-  for (int g = 0; g < kMaxGroup; ++g) o[g] = 0.0f;
-  for (int t = 0; t < n_here; ++t) {
-    const float v = bf16f(sv[t][d]);
-    const float4 p0 = *reinterpret_cast<const float4*>(&sp[t][0]);
-    const float4 p1 = *reinterpret_cast<const float4*>(&sp[t][4]);
-    o[0] = fmaf(p0.x, v, o[0]);
-    o[1] = fmaf(p0.y, v, o[1]);
-    o[2] = fmaf(p0.z, v, o[2]);
-    o[3] = fmaf(p0.w, v, o[3]);
-    o[4] = fmaf(p1.x, v, o[4]);
-    o[5] = fmaf(p1.y, v, o[5]);
-    o[6] = fmaf(p1.z, v, o[6]);
-    o[7] = fmaf(p1.w, v, o[7]);
+  for (int m = 0; m < 2; ++m) oc[m][0] = oc[m][1] = oc[m][2] = oc[m][3] = 0.0f;
+  const int tr = (lane & 7) + ((lane >> 4) << 3);  // ldmatrix.trans row (slot) of this lane
+  const int tc = ((lane >> 3) & 1) * 8;            // and column (dim) offset
+  for (int kk = 0; kk < kt; ++kk) {
+    uint32_t bh[2], bl[2];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int t = 16 * kk + 8 * half + 2 * c;
+      const float p0 = sp[t][n], p1 = sp[t + 1][n];
+      const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - __low2float(hi), p1 - __high2float(hi));
+      bh[half] = *reinterpret_cast<const uint32_t*>(&hi);
+      bl[half] = *reinterpret_cast<const uint32_t*>(&lo);
+    }
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      uint32_t a0, a1, a2, a3;
+      asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+                   : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                   : "r"(smem_addr(&sv[16 * kk + tr][32 * warp + 16 * m + tc])));
+      asm volatile(
+          "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+          "{%0, %1, %2, %3};\n"
+          : "+f"(oc[m][0]), "+f"(oc[m][1]), "+f"(oc[m][2]), "+f"(oc[m][3])
+          : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(bh[0]), "r"(bh[1]));
+      asm volatile(
+          "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+          "{%0, %1, %2, %3};\n"
+          : "+f"(oc[m][0]), "+f"(oc[m][1]), "+f"(oc[m][2]), "+f"(oc[m][3])
+          : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(bl[0]), "r"(bl[1]));
+    }
   }
+  // C fragment: dims 32w + 16m + lane / 4 (+ 8), query heads 2 (lane % 4) + {0, 1}
   const size_t pidx = (size_t)pair * w.ring_chunks + chunk;
 #pragma unroll
-  for (int g = 0; g < kMaxGroup; ++g)
-    if (g < G) w.ring_po[(pidx * G + g) * kHeadDim + d] = o[g];
+  for (int m = 0; m < 2; ++m) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int d = 32 * warp + 16 * m + (lane >> 2) + (e >= 2 ? 8 : 0);
+      const int g = 2 * c + (e & 1);
+      if (g < G) w.ring_po[(pidx * G + g) * kHeadDim + d] = oc[m][e];
+    }
+  }
+  const int d = threadIdx.x;
   if (d < G) {
     w.ring_pml[(pidx * G + d) * 2 + 0] = sm_m[d];
     w.ring_pml[(pidx * G + d) * 2 + 1] = sm_l[d];
