@@ -31,6 +31,11 @@ What it computes, step by step, each citing the page passage it restates:
 * ``select_blocks`` -- block-granular eviction (the eviction-and-reuse survey
   page, section 4, the block manager's eviction by attention): blocks sorted
   by their mean attention score, the lowest int(n * (1 - ratio)) evicted.
+* ``prefill_attention`` -- the prompt's causal attention over itself and the
+  H2O scores it gives (Technical Report section 3.4: the score is the sum of
+  the attention matrix over its query rows; the survey page's section 3.3:
+  a token's cumulative attention from all later tokens), in fp64 on the exact
+  bf16 inputs.
 * ``OracleCache(bf16_window=W)`` -- hybrid precision ("KV Cache optimization
   techniques" section 1.3, HybridPrecisionKVCache: recent tokens at 16 bits,
   older ones at INT4/INT8): the tokens at the last W positions attend with
@@ -211,6 +216,40 @@ def h2o_increments(probs: np.ndarray) -> np.ndarray:
 # Selection
 # ---------------------------------------------------------------------------
 
+def prefill_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray,
+                      sm_scale: float | None = None) -> tuple[np.ndarray, np.ndarray]:
+    """Causal attention of a prompt over itself, and the H2O scores it gives.
+
+    q: [Hq, n, D]; k, v: [Hkv, n, D] (exact bf16 values, fp32).  Query head j
+    reads KV head j // G; query i attends keys 0..i.  Returns, in fp64,
+    (out [Hq, n, D], scores [Hkv, n]) where scores[h, t] is the sum, over the
+    G query heads of KV head h and over every query, of the probability that
+    query gives key t: the column sums of the attention matrix (Technical
+    Report section 3.4, ``attention_scores.sum(dim=0)``).  Reading: the prompt
+    attends with its exact values; the compressed cache is what the decode
+    steps read."""
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    hq, n, d = q.shape
+    hkv = k.shape[0]
+    g = hq // hkv
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(d)
+    future = np.triu(np.ones((n, n), dtype=bool), 1)  # key index > query index
+    out = np.zeros((hq, n, d), np.float64)
+    scores = np.zeros((hkv, n), np.float64)
+    for j in range(hq):
+        h = j // g
+        logits = (q[j] @ k[h].T) * sm_scale
+        logits[future] = -np.inf
+        e = np.exp(logits - logits.max(axis=-1, keepdims=True))
+        probs = e / e.sum(axis=-1, keepdims=True)
+        out[j] = probs @ v[h]
+        scores[h] += probs.sum(axis=0)
+    return out, scores
+
+
 def select_h2o(pos: np.ndarray, score: np.ndarray, pos_total: int, budget: int,
                recent: int, n_sink_present: int = NUM_SINK) -> np.ndarray:
     """Keep-mask over the non-sink tokens of one (sequence, KV head).
@@ -376,6 +415,23 @@ class OracleCache:
                 hs.vscale = np.concatenate([hs.vscale, vs[h]])
                 hs.score = np.concatenate([hs.score, np.zeros(n - first_q)])
         s.pos_total += n
+
+    def prefill(self, b: int, q: np.ndarray, k: np.ndarray, v: np.ndarray,
+                sm_scale: float | None = None) -> np.ndarray:
+        """The prompt of a fresh sequence b: append its n tokens (k, v: fp32
+        [Hkv, n, D]), run ``prefill_attention`` with q (fp32 [Hq, n, D]) and
+        set every prompt token's H2O score (sinks included) to its column
+        sum.  Returns the attention output fp64 [Hq, n, D]."""
+        s = self.seqs[b]
+        if s.pos_total != 0:
+            raise ValueError("prefill needs a fresh sequence")
+        self.append(b, k, v)
+        out, sc = prefill_attention(q, k, v, sm_scale)
+        for h in range(self.hkv):
+            ns = s.sink_k[h].shape[0]
+            s.sink_score[h] = sc[h, :ns].copy()
+            s.heads[h].score = sc[h, s.heads[h].pos].copy()
+        return out
 
     # -- read path ----------------------------------------------------------
     def attend(self, b: int, q: np.ndarray, sm_scale: float | None = None,

@@ -516,3 +516,65 @@ def test_hybrid_window_boundary_brute_force():
     assert np.abs(got - brute(n, 0)).max() > 1e-4 and np.abs(got - brute(n, n)).max() > 1e-4
     c.append(0, k[:, n:n + 1], v[:, n:n + 1])
     np.testing.assert_allclose(c.attend(0, q, accumulate=False)[0], brute(n + 1, 3), rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Prefill: causal attention of the prompt and the H2O scores it gives
+# ---------------------------------------------------------------------------
+
+def test_prefill_attention_against_causal_sdpa():
+    rng = np.random.default_rng(50)
+    Hq, Hkv, n = 8, 2, 37
+    q = _bf16_round(rng.standard_normal((Hq, n, 128)))
+    k = _bf16_round(rng.standard_normal((Hkv, n, 128)))
+    v = _bf16_round(rng.standard_normal((Hkv, n, 128)))
+    out, sc = O.prefill_attention(q, k, v)
+    K = torch.from_numpy(k).double().repeat_interleave(Hq // Hkv, dim=0)
+    V = torch.from_numpy(v).double().repeat_interleave(Hq // Hkv, dim=0)
+    ref = torch.nn.functional.scaled_dot_product_attention(torch.from_numpy(q).double(), K, V, is_causal=True)
+    np.testing.assert_allclose(out, ref.numpy(), rtol=0, atol=1e-12)
+    # every query's probabilities sum to 1: a KV head's scores sum to G * n
+    np.testing.assert_allclose(sc.sum(axis=1), [Hq // Hkv * n] * Hkv, rtol=1e-12)
+
+
+def test_prefill_scores_brute_force():
+    """Column sums written out in plain Python on a tiny prompt (head dim 8):
+    key t collects, from every query i >= t of the two query heads, that
+    query's softmax probability on t."""
+    rng = np.random.default_rng(51)
+    Hq, Hkv, n, d = 2, 1, 6, 8
+    q = rng.standard_normal((Hq, n, d))
+    k = rng.standard_normal((Hkv, n, d))
+    v = rng.standard_normal((Hkv, n, d))
+    out, sc = O.prefill_attention(q, k, v)
+    want = [0.0] * n
+    for j in range(Hq):
+        for i in range(n):
+            lg = [sum(q[j, i, e] * k[0, t, e] for e in range(d)) / math.sqrt(d) for t in range(i + 1)]
+            m = max(lg)
+            ex = [math.exp(x - m) for x in lg]
+            z = sum(ex)
+            for t in range(i + 1):
+                want[t] += ex[t] / z
+            o = [sum(ex[t] / z * v[0, t, e] for t in range(i + 1)) for e in range(d)]
+            np.testing.assert_allclose(out[j, i], o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(sc[0], want, rtol=0, atol=1e-12)
+    # the last key is seen by the last query only
+    assert sc[0, -1] < Hq and sc[0, 0] > sc[0, -1]
+
+
+def test_oracle_cache_prefill_sets_the_scores():
+    rng = np.random.default_rng(52)
+    Hq, Hkv, n = 4, 2, 30
+    q = _bf16_round(rng.standard_normal((Hq, n, 128)))
+    k = _bf16_round(rng.standard_normal((Hkv, n, 128)))
+    v = _bf16_round(rng.standard_normal((Hkv, n, 128)))
+    c = O.OracleCache(1, Hq, Hkv, 8)
+    out = c.prefill(0, q, k, v)
+    _, sc = O.prefill_attention(q, k, v)
+    np.testing.assert_array_equal(out, O.prefill_attention(q, k, v)[0])
+    for h in range(Hkv):
+        assert np.array_equal(c.seqs[0].sink_score[h], sc[h, :4])
+        assert np.array_equal(c.seqs[0].heads[h].score, sc[h, 4:])
+    with pytest.raises(ValueError):
+        c.prefill(0, q, k, v)
