@@ -179,6 +179,37 @@ class KVCache:
                                             ctypes.c_void_p(ws.data_ptr()), ws.numel(),
                                             ctypes.c_void_p(_stream_ptr(stream))), "kvc_compact_blocks")
 
+    def prefill(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seq_begin: int = 0, out=None,
+                sm_scale: float | None = None, accumulate_h2o: bool = True, workspace=None, stream=None):
+        """Prompt of fresh sequences: q bf16 [batch, Hq, n, 128], k/v bf16
+        [batch, Hkv, n, 128] -> causal attention output bf16 [batch, Hq, n,
+        128]; the tokens are appended and (accumulate_h2o) their H2O scores
+        set to the prompt attention's column sums."""
+        _need(q, torch.bfloat16, "q")
+        _need(k, torch.bfloat16, "k")
+        _need(v, torch.bfloat16, "v")
+        batch, n = q.shape[0], q.shape[2]
+        if q.dim() != 4 or q.shape[1] != self.num_q_heads or q.shape[3] != HEAD_DIM:
+            raise ValueError("q must be [batch, num_q_heads, n, 128]")
+        if tuple(k.shape) != (batch, self.num_kv_heads, n, HEAD_DIM) or k.shape != v.shape:
+            raise ValueError("k, v must be [batch, num_kv_heads, n, 128]")
+        if out is None:
+            out = torch.empty_like(q)
+        _need(out, torch.bfloat16, "out")
+        nbytes = self.lib.kvc_prefill_workspace_bytes(self.handle, batch, n)
+        if workspace is None:
+            raw = torch.empty(nbytes + 256, dtype=torch.uint8, device=self.device)
+            off = (-raw.data_ptr()) % 256
+            workspace = raw[off:off + nbytes]
+        scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
+        L.check(self.lib.kvc_prefill_attention(self.handle, seq_begin, batch, n, ctypes.c_void_p(q.data_ptr()),
+                                               ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()),
+                                               ctypes.c_void_p(out.data_ptr()), ctypes.c_float(scale),
+                                               L.KVC_ATTN_ACCUM_H2O if accumulate_h2o else 0,
+                                               ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                                               ctypes.c_void_p(_stream_ptr(stream))), "kvc_prefill_attention")
+        return out
+
     def decode_step(self, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, mode: str = "h2o",
                     budget: int = 0, recent: int = 0, window: int = 0, seq_begin: int = 0, out=None,
                     sm_scale: float | None = None, workspace=None, stream=None,

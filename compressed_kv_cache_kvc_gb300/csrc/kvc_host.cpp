@@ -693,6 +693,39 @@ kvc_status kvc_decode_step(kvc_cache* c, int32_t seq_begin, int32_t batch, const
   return KVC_OK;
 }
 
+size_t kvc_prefill_workspace_bytes(const kvc_cache* c, int32_t batch, int32_t n) {
+  if (!c || batch <= 0 || n <= 0) return 0;
+  return align_up((size_t)batch * c->cfg.num_q_heads * n * 2 * 4);
+}
+
+kvc_status kvc_prefill_attention(kvc_cache* c, int32_t seq_begin, int32_t batch, int32_t n, const void* d_q,
+                                 const void* d_k, const void* d_v, void* d_out, float sm_scale, int32_t flags,
+                                 void* d_workspace, size_t workspace_bytes, void* stream) {
+  if (!c) return KVC_ERR_INVALID_ARG;
+  c->last_launches = 0;
+  if (!range_ok(c, seq_begin, batch) || n <= 0 || (flags & ~KVC_ATTN_ACCUM_H2O)) return KVC_ERR_INVALID_ARG;
+  if (!d_q || !d_out || !aligned(d_q, 16) || !aligned(d_out, 16) || !d_k || !d_v || !aligned(d_k, 16) ||
+      !aligned(d_v, 16))
+    return KVC_ERR_INVALID_ARG;
+  if (!(sm_scale > 0.0f) || !std::isfinite(sm_scale)) return KVC_ERR_INVALID_ARG;
+  if (!d_workspace || !aligned(d_workspace, kAlign) ||
+      workspace_bytes < kvc_prefill_workspace_bytes(c, batch, n))
+    return KVC_ERR_INVALID_ARG;
+  if ((long long)n * kvc::kHeadDim * c->cfg.num_q_heads * batch > 2000000000000LL) return KVC_ERR_UNSUPPORTED;
+  for (int i = 0; i < batch; ++i)
+    if (c->pos[seq_begin + i] != 0) return KVC_ERR_STATE;  // a prompt starts a sequence
+  kvc_status st0 = kvc_quantize_append(c, seq_begin, batch, n, d_k, d_v, stream);
+  if (st0 != KVC_OK) return st0;
+  const bool h2o = (flags & KVC_ATTN_ACCUM_H2O) != 0;
+  if (kvc::launch_prefill(c->dev, seq_begin, batch, n, static_cast<const uint16_t*>(d_q),
+                          static_cast<const uint16_t*>(d_k), static_cast<const uint16_t*>(d_v),
+                          static_cast<uint16_t*>(d_out), static_cast<float*>(d_workspace),
+                          sm_scale * 1.4426950408889634f, h2o, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return KVC_ERR_CUDA;
+  c->last_launches = 1 + 1 + (h2o ? 1 : 0);
+  return KVC_OK;
+}
+
 kvc_status kvc_read_status(kvc_cache* c, int32_t* h_status, void* stream) {
   if (!c || !h_status) return KVC_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

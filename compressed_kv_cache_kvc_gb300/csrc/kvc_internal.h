@@ -150,6 +150,13 @@ cudaError_t launch_compact(const DevState& s, int seq_begin, int batch, const ui
                            int s_cap, int32_t* g_holes, int32_t* g_srcs, int smem_moves, cudaStream_t st);
 int compact_max_smem_moves();
 
+// Prefill of fresh sequences: causal attention over the prompt's bf16 K/V
+// (output bf16 [batch][hq][n][128], row statistics to `stats`
+// [batch][hq][n][2]) and, with `scores`, the H2O scores of its tokens.
+cudaError_t launch_prefill(const DevState& s, int seq_begin, int batch, int n, const uint16_t* q, const uint16_t* k,
+                           const uint16_t* v, uint16_t* out, float* stats, float qk_scale_log2, bool scores,
+                           cudaStream_t st);
+
 // Fused merge + H2O scores + selection + compaction (kvc_decode_step).
 struct StepArgs {
   int mode, budget, recent, window;

@@ -305,6 +305,29 @@ kvc_status kvc_decode_step(kvc_cache* cache, int32_t seq_begin, int32_t batch, c
                            const kvc_evict_params* params, void* d_workspace, size_t workspace_bytes,
                            void* stream);
 
+/* Prefill of fresh sequences (the step before the decode path): append the
+ * n prompt tokens of every sequence of the slice (exactly as
+ * kvc_quantize_append), run the causal attention of the n queries over the
+ * prompt's exact bf16 keys and values (query i attends keys 0..i; query head
+ * j reads KV head j / G), and, with KVC_ATTN_ACCUM_H2O, set every prompt
+ * token's H2O score (sinks, pool slots, bf16 window) to the sum over all n
+ * queries and the G query heads of its KV head of the probability they give
+ * it: the column sums of the prompt's attention matrix (Technical Report 3.4:
+ * scores = attention_scores.sum(dim=0); the eviction-and-reuse survey page
+ * 3.3: a token's cumulative attention from the later tokens).
+ *   d_q:   bf16 [batch][Hq][n][128];  d_k, d_v: bf16 [batch][Hkv][n][128];
+ *   d_out: bf16 [batch][Hq][n][128];  all 16-byte aligned;
+ *   d_workspace: kvc_prefill_workspace_bytes(cache, batch, n) bytes, 256-byte
+ *   aligned (the row statistics the score pass reads).
+ * Two or three launches (append, attention, scores), tensor cores (bf16
+ * operands, fp32 accumulation).  Errors: KVC_ERR_STATE unless every sequence
+ * of the slice is empty (no token appended since the last reset);
+ * KVC_ERR_CAPACITY as kvc_quantize_append. */
+size_t kvc_prefill_workspace_bytes(const kvc_cache* cache, int32_t batch, int32_t n);
+kvc_status kvc_prefill_attention(kvc_cache* cache, int32_t seq_begin, int32_t batch, int32_t n, const void* d_q,
+                                 const void* d_k, const void* d_v, void* d_out, float sm_scale, int32_t flags,
+                                 void* d_workspace, size_t workspace_bytes, void* stream);
+
 /* ---------------------------------------------------------------- misc ---- */
 
 /* Synchronise `stream`, copy the device status word to *h_status and clear
