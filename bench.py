@@ -521,6 +521,75 @@ def gpu_arm(args):
 # the same one-call step, as absolute numbers and fractions of the HBM peak
 # ---------------------------------------------------------------------------
 
+def prefill_report(args, name: str):
+    """Time one layer's prefill (kvc_prefill_attention: append, causal
+    attention, H2O scores) on workload `name`'s shape, every sequence a fresh
+    prompt of the workload's context length; inputs seeded, resident on the
+    device.  Prints one JSON line with the attention's algorithmic TFLOP/s
+    against the measured bf16 tensor peak."""
+    import numpy as np
+    import torch
+
+    from compressed_kv_cache_kvc_gb300 import workloads as W
+    from compressed_kv_cache_kvc_gb300.build import build_library
+    build_library()
+    from compressed_kv_cache_kvc_gb300.cache import KVCache
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = W.WORKLOADS[name]
+    B, Hq, Hkv, n = w.batch, w.num_q_heads, w.num_kv_heads, w.context
+    mbps = (n + 15) // 16 + 1
+    c = KVCache(Hq, Hkv, w.bits, B * mbps, B, mbps, device=dev, bf16_window=args.bf16_window)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1234)
+    q = torch.randn(B, Hq, n, 128, device=dev, generator=g).to(torch.bfloat16)
+    k = torch.randn(B, Hkv, n, 128, device=dev, generator=g).to(torch.bfloat16)
+    v = torch.randn(B, Hkv, n, 128, device=dev, generator=g).to(torch.bfloat16)
+    out = torch.empty_like(q)
+    nbytes = c.lib.kvc_prefill_workspace_bytes(c.handle, B, n)
+    raw = torch.empty(nbytes + 256, dtype=torch.uint8, device=dev)
+    ws = raw[(-raw.data_ptr()) % 256:][:nbytes]
+    stream = torch.cuda.Stream(device=dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def run(scores):
+        ms = []
+        for i in range(max(1, args.warmup) + args.steps):
+            c.reset(stream=stream)
+            with torch.cuda.stream(stream):
+                ev0.record(stream)
+                c.prefill(q, k, v, out=out, workspace=ws, accumulate_h2o=scores, stream=stream)
+                ev1.record(stream)
+            ev1.synchronize()
+            if i >= max(1, args.warmup):
+                ms.append(ev0.elapsed_time(ev1))
+        return float(np.median(ms))
+
+    ms_all = run(True)
+    ms_attn = run(False)
+    st = c.read_status()
+    if st:
+        raise RuntimeError(f"device status {st:#x}")
+    pairs = n * (n + 1) / 2  # (query, key <= query) pairs per query head
+    attn_flop = 4.0 * 128 * pairs * Hq * B  # QK^T and PV
+    score_flop = 2.0 * 128 * pairs * Hq * B  # QK^T again, for the column sums
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        pass
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    line = {"workload": name, "prefill": True, "batch": B, "n": n, "q_heads": Hq, "kv_heads": Hkv,
+            "bits": w.bits, "bf16_window": args.bf16_window,
+            "ms_with_scores": ms_all, "ms_without_scores": ms_attn,
+            "attention_tflops": attn_flop / (ms_attn * 1e-3) / 1e12,
+            "attention_frac_of_bf16_peak": attn_flop / (ms_attn * 1e-3) / 1e12 / peak,
+            "scores_tflops": score_flop / ((ms_all - ms_attn) * 1e-3) / 1e12 if ms_all > ms_attn else None,
+            "prompt_tokens_per_s": B * n / (ms_all * 1e-3), "peak_bf16_tflops": peak, "steps_timed": args.steps,
+            "note": "times include the append of the prompt (quantisation into the pool)"}
+    print(json.dumps(line), flush=True)
+
+
 def workload_report(args, name: str):
     """Time the decode step of workload `name` on one GPU: all its layers,
     one `decode_step` per layer, replayed from a CUDA graph; the state is
@@ -702,6 +771,8 @@ def main():
     ap.add_argument("--evict", default=None, choices=["block"],
                     help="report mode: block-granular eviction instead of the workload's mode")
     ap.add_argument("--retention", type=float, default=0.25, help="report mode, --evict block: pages kept")
+    ap.add_argument("--prefill", action="store_true",
+                    help="report mode: time one layer's prefill (fresh prompts of the workload's context)")
     ap.add_argument("--bf16-window", type=int, default=0,
                     help="report mode: hybrid precision, the last W positions kept in bf16 (W <= recent)")
     ap.add_argument("--oracle-child", nargs=2, type=int, default=None, help=argparse.SUPPRESS)
@@ -716,7 +787,7 @@ def main():
     if args.workload:
         from compressed_kv_cache_kvc_gb300 import workloads as W
         for name in (list(W.WORKLOADS) if args.workload == "all" else [args.workload]):
-            workload_report(args, name)
+            (prefill_report if args.prefill else workload_report)(args, name)
         return
     gpu_arm(args)
 

@@ -165,11 +165,107 @@ __global__ void __launch_bounds__(512) append_kernel(DevState s, int seq_begin, 
   }
 }
 
+// Bulk appends (a prompt) run as two launches: append_alloc_kernel, one
+// thread per sequence, takes the pages and advances the lengths exactly as
+// append_kernel's first thread does and leaves the old lengths in the plan
+// scratch (slots -1 when it failed); append_rows_kernel then spreads the
+// rows over (token chunk, sequence) CTAs.  Only for appends that push no
+// window token into the pool, so no row reads what another CTA writes.
+constexpr int kBulkTokens = 64;  // tokens per CTA of append_rows_kernel
+
+__global__ void append_alloc_kernel(DevState s, int seq_begin, int batch, int n_new) {
+  const int bl = blockIdx.x * blockDim.x + threadIdx.x;
+  if (bl >= batch) return;
+  const int b = seq_begin + bl;
+  const int slots = s.seq_slots[b];
+  const int pos = s.seq_pos[b];
+  int lo, hi;
+  pool_range(pos, n_new, s.ring, &lo, &hi);
+  const int new_slots = slots + (hi - lo);
+  const int old_pages = (slots + kPage - 1) / kPage;
+  const int new_pages = (new_slots + kPage - 1) / kPage;
+  const int need = new_pages - old_pages;
+  int ok = 1;
+  if (new_pages > s.max_bps) {
+    atomicOr(&s.counters[kCtrStatus], kDevTableOverflow);
+    ok = 0;
+  } else if (need > 0) {
+    const int top = atomicSub(&s.counters[kCtrFreeTop], need);
+    if (top - need < 0 || top > s.num_blocks) {
+      atomicAdd(&s.counters[kCtrFreeTop], need);
+      atomicOr(&s.counters[kCtrStatus], kDevOutOfBlocks);
+      ok = 0;
+    } else {
+      int32_t* row = s.block_table + (size_t)b * s.max_bps;
+      for (int j = 0; j < need; ++j) row[old_pages + j] = s.free_stack[top - 1 - j];
+    }
+  }
+  if (ok) {
+    s.seq_slots[b] = new_slots;
+    s.seq_pos[b] = pos + n_new;
+  }
+  s.plan[2 * b] = ok ? slots : -1;
+  s.plan[2 * b + 1] = pos;
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(512) append_rows_kernel(DevState s, int seq_begin, int n_new,
+                                                          const uint16_t* __restrict__ kin,
+                                                          const uint16_t* __restrict__ vin) {
+  const int bl = blockIdx.y;
+  const int b = seq_begin + bl;
+  const int slots = s.plan[2 * b];
+  if (slots < 0) return;
+  const int pos = s.plan[2 * b + 1];
+  int lo, hi;
+  pool_range(pos, n_new, s.ring, &lo, &hi);
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int hkv = s.hkv;
+  const int W = s.ring;
+  const int t0 = blockIdx.x * kBulkTokens;
+  const int nt = min(kBulkTokens, n_new - t0);
+  for (int row = warp; row < nt * hkv * 2; row += nwarps) {
+    const int kv = row & 1;
+    const int h = (row >> 1) % hkv;
+    const int i = t0 + (row >> 1) / hkv;
+    const uint16_t* src = (kv ? vin : kin) + (((size_t)bl * hkv + h) * n_new + i) * kHeadDim;
+    const uint2 raw = *reinterpret_cast<const uint2*>(src + lane * 4);
+    const int p = pos + i;
+    if (p < kSinks) {
+      uint16_t* dst = (kv ? s.sink_v : s.sink_k) + (((size_t)b * hkv + h) * kSinks + p) * kHeadDim;
+      *reinterpret_cast<uint2*>(dst + lane * 4) = raw;
+      if (kv == 0 && lane == 0) s.sink_score[((size_t)b * hkv + h) * kSinks + p] = 0.0f;
+    } else if (p < hi) {
+      quantize_row<BITS>(s, b, h, kv, slots + (p - lo), p, 0.0f, raw, lane);
+    } else {
+      const size_t ridx = ((size_t)b * hkv + h) * W + (p - kSinks) % W;
+      uint16_t* dst = (kv ? s.ring_v : s.ring_k) + ridx * kHeadDim;
+      *reinterpret_cast<uint2*>(dst + lane * 4) = raw;
+      if (kv == 0 && lane == 0) s.ring_score[ridx] = 0.0f;
+    }
+  }
+}
+
 __global__ void fill_free_stack_kernel(int32_t* stack, int n) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) stack[i] = n - 1 - i;
 }
 
 }  // namespace
+
+cudaError_t launch_append_bulk(const DevState& s, int seq_begin, int batch, int n_new, const uint16_t* k,
+                               const uint16_t* v, cudaStream_t st) {
+  append_alloc_kernel<<<(batch + 127) / 128, 128, 0, st>>>(s, seq_begin, batch, n_new);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const dim3 grid((n_new + kBulkTokens - 1) / kBulkTokens, batch);
+  if (s.bits == 8)
+    append_rows_kernel<8><<<grid, 512, 0, st>>>(s, seq_begin, n_new, k, v);
+  else
+    append_rows_kernel<4><<<grid, 512, 0, st>>>(s, seq_begin, n_new, k, v);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_append(const DevState& s, int seq_begin, int batch, int n_new, const uint16_t* k,
                           const uint16_t* v, cudaStream_t st) {

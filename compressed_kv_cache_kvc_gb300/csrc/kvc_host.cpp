@@ -467,10 +467,21 @@ kvc_status kvc_quantize_append(kvc_cache* c, int32_t seq_begin, int32_t batch, i
     new_slots[i] = (int32_t)ns;
   }
   if (need > (long long)c->cfg.num_blocks - used_pages(c)) return KVC_ERR_CAPACITY;
-  const cudaError_t e = kvc::launch_append(c->dev, seq_begin, batch, n_new, static_cast<const uint16_t*>(d_k),
-                                           static_cast<const uint16_t*>(d_v), static_cast<cudaStream_t>(stream));
+  // long appends that move no window token into the pool: rows spread over
+  // (token chunk, sequence) CTAs
+  bool bulk = n_new >= kvc::kBulkAppendMin;
+  for (int i = 0; i < batch && bulk; ++i) {
+    int lo, hi;
+    kvc::pool_range(c->pos[seq_begin + i], n_new, c->cfg.bf16_window, &lo, &hi);
+    if (c->cfg.bf16_window > 0 && std::min(c->pos[seq_begin + i], hi) > lo) bulk = false;
+  }
+  const cudaError_t e =
+      bulk ? kvc::launch_append_bulk(c->dev, seq_begin, batch, n_new, static_cast<const uint16_t*>(d_k),
+                                     static_cast<const uint16_t*>(d_v), static_cast<cudaStream_t>(stream))
+           : kvc::launch_append(c->dev, seq_begin, batch, n_new, static_cast<const uint16_t*>(d_k),
+                                static_cast<const uint16_t*>(d_v), static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return KVC_ERR_CUDA;
-  c->last_launches = 1;
+  c->last_launches = bulk ? 2 : 1;
   for (int i = 0; i < batch; ++i) {
     c->slots[seq_begin + i] = new_slots[i];
     c->pos[seq_begin + i] += n_new;
@@ -722,7 +733,7 @@ kvc_status kvc_prefill_attention(kvc_cache* c, int32_t seq_begin, int32_t batch,
                           static_cast<uint16_t*>(d_out), static_cast<float*>(d_workspace),
                           sm_scale * 1.4426950408889634f, h2o, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return KVC_ERR_CUDA;
-  c->last_launches = 1 + 1 + (h2o ? 1 : 0);
+  c->last_launches += 1 + (h2o ? 1 : 0);
   return KVC_OK;
 }
 

@@ -107,6 +107,11 @@ inline cudaError_t opt_in_smem(const void* fn, int bytes, int* done) {
 // ---- launchers (return cudaGetLastError of the launch) -------------------
 cudaError_t launch_append(const DevState& s, int seq_begin, int batch, int n_new,
                           const uint16_t* k, const uint16_t* v, cudaStream_t st);
+// Two launches (page allocation, then the rows over token chunks) for long
+// appends that push no bf16-window token into the pool.
+cudaError_t launch_append_bulk(const DevState& s, int seq_begin, int batch, int n_new, const uint16_t* k,
+                               const uint16_t* v, cudaStream_t st);
+constexpr int kBulkAppendMin = 64;  // tokens per sequence from which the bulk path pays
 cudaError_t launch_fill_free_stack(const DevState& s, cudaStream_t st);
 
 cudaError_t launch_attention_split(const DevState& s, int seq_begin, int batch, const uint16_t* q,

@@ -353,6 +353,8 @@ def test_launch_counts():
     cache = _cache(8, 2, 8, 1, 100)
     k = _rand_bits(rng, (1, 2, 80, 128))
     cache.quantize_append(T.to_dev_bf16(k), T.to_dev_bf16(k))
+    assert cache.last_launch_count() == 2  # a long append: page allocation, then rows over token chunks
+    cache.quantize_append(T.to_dev_bf16(k[:, :, :10]), T.to_dev_bf16(k[:, :, :10]))
     assert cache.last_launch_count() == 1
     q = _rand_bits(rng, (1, 8, 128))
     cache.decode_attention(T.to_dev_bf16(q))
@@ -361,3 +363,38 @@ def test_launch_counts():
     assert cache.last_launch_count() == 1
     cache.compact_blocks(m, 1)
     assert cache.last_launch_count() == 2  # compaction, page release
+
+
+@pytest.mark.parametrize("bits,W", [(8, 0), (4, 0), (8, 40)])
+def test_bulk_append_equals_token_by_token(bits, W):
+    """A long append (page allocation, then rows spread over token chunks)
+    leaves the same device state, byte for byte, as the same tokens appended
+    one at a time (one CTA per sequence)."""
+    from compressed_kv_cache_kvc_gb300.cache import KVCache
+    rng = np.random.default_rng(bits + W)
+    lengths = [300, 77, 129]
+    B, hkv, n = 3, 4, max(lengths)
+    mbps = (n + 15) // 16 + 1
+    ca = KVCache(16, hkv, bits, B * mbps, B, mbps, bf16_window=W)
+    cb = KVCache(16, hkv, bits, B * mbps, B, mbps, bf16_window=W)
+    k = _rand_bits(rng, (B, hkv, n, 128))
+    v = _rand_bits(rng, (B, hkv, n, 128))
+    for b, nb in enumerate(lengths):
+        ca.quantize_append(T.to_dev_bf16(np.ascontiguousarray(k[b:b + 1, :, :nb])),
+                           T.to_dev_bf16(np.ascontiguousarray(v[b:b + 1, :, :nb])), seq_begin=b)
+        assert ca.last_launch_count() == 2
+        for t in range(nb):
+            cb.quantize_append(T.to_dev_bf16(np.ascontiguousarray(k[b:b + 1, :, t:t + 1])),
+                               T.to_dev_bf16(np.ascontiguousarray(v[b:b + 1, :, t:t + 1])), seq_begin=b)
+    torch.cuda.synchronize()
+    sa, sb = T.StateView(ca), T.StateView(cb)
+    for b, nb in enumerate(lengths):
+        for h in range(hkv):
+            for x, y in zip(sa.head(b, h), sb.head(b, h)):
+                assert np.array_equal(np.asarray(x).view(np.uint8), np.asarray(y).view(np.uint8)), (b, h)
+            if W:
+                for x, y in zip(sa.ring_head(b, h), sb.ring_head(b, h)):
+                    assert np.array_equal(np.asarray(x).view(np.uint8), np.asarray(y).view(np.uint8)), (b, h)
+    for name in ["BLOCK_TABLE", "SEQ_SLOTS", "SEQ_POS", "SINK_K", "SINK_V"]:
+        assert torch.equal(ca.buffer(name), cb.buffer(name)), name
+    assert ca.read_status() == 0 and cb.read_status() == 0

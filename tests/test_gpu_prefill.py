@@ -47,7 +47,7 @@ def test_prefill_against_oracle(bits, hq, hkv, batch, n, W):
     k = _bits(rng, (batch, hkv, n, 128))
     v = _bits(rng, (batch, hkv, n, 128))
     out = cache.prefill(T.to_dev_bf16(q), T.to_dev_bf16(k), T.to_dev_bf16(v))
-    assert cache.last_launch_count() == 3
+    assert cache.last_launch_count() == (4 if n >= 64 else 3)  # append (1 or 2), attention, scores
     gpu = T.bf16_tensor_to_f32(out)
     st = T.StateView(cache)
     f = O.bf16_bits_to_f32
