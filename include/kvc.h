@@ -292,10 +292,12 @@ kvc_status kvc_decode_attention_noalloc(kvc_cache* cache, int32_t seq_begin, int
  * compute them.  After the split-K attention, the merge, the score update,
  * the selection and the compaction lists of each (sequence, KV head) run in
  * one kernel that keeps the scores, keys and keep decisions on chip; the row
- * moves follow in a launch of their own.  Four launches in all.  In block
- * mode (KVC_EVICT_BLOCK) that kernel stops after the scores; the page sums
- * and then the page selection and the row rewrite of each sequence follow
- * (five launches).
+ * moves follow in a launch of their own.  Four launches in all (the split
+ * kernel runs even when every pool is empty: its first CTA publishes the
+ * page prefix the next kernel reads); five with a bf16 window (its attention
+ * follows the split).  In block mode (KVC_EVICT_BLOCK) that kernel stops
+ * after the scores; the page sums and then the page selection and the row
+ * rewrite of each sequence follow (five launches).
  *   d_q: bf16 [batch][Hq][128]; d_k_new, d_v_new: bf16 [batch][Hkv][1][128];
  *   d_out: bf16 [batch][Hq][128]; workspace as for kvc_decode_attention.
  * Host-visible errors (arguments, capacity) are returned before anything is
