@@ -15,6 +15,12 @@ What it computes, step by step, each citing the page passage it restates:
   (token, head) = amax over head_dim / (2^(bits-1) - 1), code = round-half-even
   of x / scale, clamped.  Computed in IEEE fp32 exactly as the pages' fp32
   tensors would be (division, not reciprocal multiplication).
+* ``quantize_rows_e4m3`` -- FP8 codes (the techniques page lists FP8 among
+  its quantisation strategies, section 1.1; the Technical Report's section 2
+  lists INT8/FP8/INT4): the same per-token symmetric scale with the E4M3
+  range (amax / 448), and each x / scale rounded to E4M3, ties to even,
+  saturating at 448 (``e4m3_encode``, written from the OCP 8-bit floating
+  point format: 4 exponent bits with bias 7, 3 fraction bits, subnormals).
 * ``attention`` -- the dense definition softmax(Q K^T / sqrt(d)) V of the
   Technical Report section 1.1, evaluated in fp64 on the dequantised keys and
   values (code * scale, section 3.2) and on the bf16 sink tokens (section 3.2:
@@ -151,6 +157,60 @@ def quantize_rows(x: np.ndarray, bits: int) -> tuple[np.ndarray, np.ndarray]:
     lo, hi = code_range(bits)
     codes = np.clip(codes, lo, hi)
     codes = np.where(scale[..., None] > 0, codes, 0).astype(np.int8)
+    return codes, scale
+
+
+E4M3_MAX = 448.0  # largest finite FP8 E4M3 value: 1.75 * 2^8
+
+
+def e4m3_encode(y: np.ndarray) -> np.ndarray:
+    """FP8 E4M3 codes (uint8) of fp32 values: round to nearest, ties to even,
+    saturating to +-448 (no infinities in E4M3).
+
+    Format (OCP 8-bit floating point, E4M3): sign bit, 4 exponent bits with
+    bias 7, 3 fraction bits; exponent field 0 holds the subnormals m * 2^-9
+    (m = 0..7); the largest finite value is 1.75 * 2^8 = 448.  Rounding:
+    the representable values near |y| are spaced 2^(e-3) apart, e =
+    max(floor(log2 |y|), -6); |y| / 2^(e-3) rounded half to even, times
+    2^(e-3), is the nearest value (exact in fp64: power-of-two scaling)."""
+    y = np.asarray(y, dtype=np.float32).astype(np.float64)
+    sign = np.signbit(y).astype(np.uint8)
+    a = np.minimum(np.abs(y), E4M3_MAX)  # saturation (values above 448 round to 448 or beyond)
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))  # a = f * 2^ex, f in [0.5, 1): floor(log2 a) = ex - 1
+    e = np.maximum(ex - 1, -6)
+    quantum = np.ldexp(1.0, e - 3)
+    v = np.rint(a / quantum) * quantum  # rounded magnitude, <= 448
+    sub = v < 2.0 ** -6
+    fm, fe = np.frexp(np.where(v > 0, v, 1.0))  # v = (2 fm) * 2^(fe - 1)
+    exp_field = np.where(sub, 0, fe - 1 + 7)
+    frac = np.where(sub, v / 2.0 ** -9, (2.0 * fm - 1.0) * 8.0)
+    code = (exp_field.astype(np.int64) << 3) | np.rint(frac).astype(np.int64)
+    return ((sign.astype(np.int64) << 7) | code).astype(np.uint8)
+
+
+def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+    """Exact fp64 values of FP8 E4M3 codes (the NaN codes 0x7F / 0xFF are
+    never produced by ``e4m3_encode``)."""
+    c = np.asarray(codes).astype(np.uint8).astype(np.int64)
+    sign = np.where(c >> 7, -1.0, 1.0)
+    ef = (c >> 3) & 0xF
+    m = c & 7
+    mag = np.where(ef == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.ldexp(1.0, ef - 7))
+    return sign * mag
+
+
+def quantize_rows_e4m3(x: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """FP8 (E4M3) per-token quantisation of each row (last axis): amax over
+    the row, scale = amax / 448 (one IEEE fp32 division), code =
+    e4m3_encode(x / scale) with an IEEE fp32 division; a zero row has scale 0
+    and codes 0.  Returns (uint8 codes, fp32 scales)."""
+    x = np.asarray(x, dtype=np.float32)
+    amax = np.max(np.abs(x), axis=-1)
+    scale = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+    safe = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)
+    ratio = (x / safe[..., None]).astype(np.float32)
+    codes = e4m3_encode(ratio)
+    codes = np.where(scale[..., None] > 0, codes, 0).astype(np.uint8)
     return codes, scale
 
 
@@ -362,14 +422,17 @@ class OracleCache:
     """
 
     def __init__(self, batch: int, num_q_heads: int, num_kv_heads: int, bits: int,
-                 head_dim: int = HEAD_DIM, bf16_window: int = 0):
+                 head_dim: int = HEAD_DIM, bf16_window: int = 0, codes: str = "int"):
         if num_q_heads % num_kv_heads:
             raise ValueError("num_q_heads must be a multiple of num_kv_heads")
         if bf16_window < 0:
             raise ValueError("bf16_window must be >= 0")
         qmax_for_bits(bits)
+        if codes not in ("int", "e4m3") or (codes == "e4m3" and bits != 8):
+            raise ValueError("codes: 'int', or 'e4m3' with bits = 8")
         self.batch, self.hq, self.hkv, self.bits, self.d = batch, num_q_heads, num_kv_heads, bits, head_dim
         self.bf16_window = bf16_window
+        self.codes = codes
         self.group = num_q_heads // num_kv_heads
         self.seqs = []
         for _ in range(batch):
@@ -403,8 +466,13 @@ class OracleCache:
                     s.sink_score[h] = np.append(s.sink_score[h], 0.0)
         first_q = max(0, NUM_SINK - s.pos_total)
         if first_q < n:
-            kc, ks = quantize_rows(k[:, first_q:], self.bits)
-            vc, vs = quantize_rows(v[:, first_q:], self.bits)
+            if self.codes == "e4m3":  # byte codes kept in the int8 arrays
+                kc, ks = quantize_rows_e4m3(k[:, first_q:])
+                vc, vs = quantize_rows_e4m3(v[:, first_q:])
+                kc, vc = kc.view(np.int8), vc.view(np.int8)
+            else:
+                kc, ks = quantize_rows(k[:, first_q:], self.bits)
+                vc, vs = quantize_rows(v[:, first_q:], self.bits)
             newpos = np.arange(s.pos_total + first_q, s.pos_total + n, dtype=np.int64)
             for h in range(self.hkv):
                 hs = s.heads[h]
@@ -433,6 +501,12 @@ class OracleCache:
             s.heads[h].score = sc[h, s.heads[h].pos].copy()
         return out
 
+    def dequantize(self, codes: np.ndarray, scale: np.ndarray) -> np.ndarray:
+        """code value * scale in fp64 (INT codes, or E4M3 codes decoded)."""
+        if self.codes == "e4m3":
+            return e4m3_decode(np.asarray(codes).view(np.uint8)) * np.asarray(scale, np.float64)[..., None]
+        return dequantize(codes, scale)
+
     # -- read path ----------------------------------------------------------
     def attend(self, b: int, q: np.ndarray, sm_scale: float | None = None,
                accumulate: bool = True) -> np.ndarray:
@@ -452,8 +526,8 @@ class OracleCache:
         out = np.zeros((self.hq, self.d), np.float64)
         for h in range(self.hkv):
             hs = s.heads[h]
-            kq = dequantize(hs.kcodes, hs.kscale)
-            vq = dequantize(hs.vcodes, hs.vscale)
+            kq = self.dequantize(hs.kcodes, hs.kscale)
+            vq = self.dequantize(hs.vcodes, hs.vscale)
             if self.bf16_window > 0:
                 recent = hs.pos >= s.pos_total - self.bf16_window
                 kq[recent] = s.raw_k[h][hs.pos[recent]].astype(np.float64)

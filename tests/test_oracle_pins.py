@@ -578,3 +578,56 @@ def test_oracle_cache_prefill_sets_the_scores():
         assert np.array_equal(c.seqs[0].heads[h].score, sc[h, 4:])
     with pytest.raises(ValueError):
         c.prefill(0, q, k, v)
+
+
+# ---------------------------------------------------------------------------
+# FP8 E4M3 codes
+# ---------------------------------------------------------------------------
+
+def test_e4m3_against_torch_float8():
+    """Library witness: torch's float8_e4m3fn conversion (round to nearest
+    even) on values within the finite range, and its decoding of every
+    finite code."""
+    rng = np.random.default_rng(70)
+    y = (rng.standard_normal(100000) * np.exp(rng.uniform(-12, 7, 100000))).astype(np.float32)
+    y = np.clip(y, -448, 448).astype(np.float32)
+    want = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.e4m3_encode(y), want)
+    codes = np.arange(256, dtype=np.uint8)
+    codes = codes[(codes & 0x7F) != 0x7F]  # the NaN codes
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(O.e4m3_decode(codes), ref)
+    assert np.array_equal(O.e4m3_encode(O.e4m3_decode(codes).astype(np.float32)), codes)
+
+
+@pytest.mark.parametrize("y,code", [
+    (1.0, 0x38), (448.0, 0x7E), (-2.5, 0xC2),
+    (2.0 ** -9, 0x01),                  # smallest subnormal
+    (2.0 ** -10, 0x00),                 # half of it: tie to the even code 0
+    (0.75 * 2.0 ** -9, 0x01),
+    (2.0 ** -6, 0x08),                  # smallest normal
+    (17.0, 0x58), (19.0, 0x5A),         # ties between 16/18 and 18/20 go to the even fraction
+    (460.0, 0x7E),                      # nearest is 448
+    (1.0e6, 0x7E), (-1.0e6, 0xFE),      # saturation to the largest finite value
+])
+def test_e4m3_worked_values(y, code):
+    assert int(O.e4m3_encode(np.array([y], np.float32))[0]) == code
+
+
+def test_e4m3_row_quantiser_invariants():
+    rng = np.random.default_rng(71)
+    x = (rng.standard_normal((64, 128)) * np.exp(rng.uniform(-4, 4, (64, 1)))).astype(np.float32)
+    x[3] = 0.0
+    codes, scale = O.quantize_rows_e4m3(x)
+    amax = np.abs(x).max(axis=1)
+    np.testing.assert_array_equal(scale, (amax / np.float32(448.0)).astype(np.float32))
+    assert scale[3] == 0 and not codes[3].any()
+    rows = np.arange(64) != 3
+    # the amax element maps to +-448 (code 0x7E / 0xFE)
+    j = np.abs(x).argmax(axis=1)
+    assert np.all((codes[rows, j[rows]] & 0x7F) == 0x7E)
+    # within half a quantum: 2^-4 relative for normals, 2^-10 * scale for subnormals
+    dec = O.e4m3_decode(codes) * scale[:, None].astype(np.float64)
+    err = np.abs(dec - x.astype(np.float64))
+    bound = np.abs(x) * 2.0 ** -4 * (1 + 1e-6) + scale[:, None] * 2.0 ** -10 * (1 + 1e-6)
+    assert np.all(err <= bound)
