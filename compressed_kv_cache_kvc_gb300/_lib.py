@@ -17,6 +17,8 @@ KVC_ERR_DEVICE = 5
 KVC_ERR_STATE = 6
 
 KVC_ATTN_ACCUM_H2O = 0x1
+KVC_CODES_INT = 0
+KVC_CODES_E4M3 = 1
 KVC_EVICT_H2O = 0
 KVC_EVICT_STREAMING = 1
 KVC_EVICT_BLOCK = 2
@@ -31,7 +33,7 @@ class KvcConfig(ctypes.Structure):
     _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32), ("bits", ctypes.c_int32),
                 ("num_blocks", ctypes.c_int32), ("max_batch", ctypes.c_int32),
-                ("max_blocks_per_seq", ctypes.c_int32), ("bf16_window", ctypes.c_int32)]
+                ("max_blocks_per_seq", ctypes.c_int32), ("bf16_window", ctypes.c_int32), ("codes", ctypes.c_int32)]
 
 
 class KvcEvictParams(ctypes.Structure):

@@ -33,14 +33,17 @@ class KVCache:
     """One layer's compressed, paged KV cache on the current CUDA device."""
 
     def __init__(self, num_q_heads: int, num_kv_heads: int, bits: int, num_blocks: int,
-                 max_batch: int, max_blocks_per_seq: int, block_order=None, device=None, bf16_window: int = 0):
+                 max_batch: int, max_blocks_per_seq: int, block_order=None, device=None, bf16_window: int = 0,
+                 codes: str = "int"):
         """bf16_window = W > 0: hybrid precision, the last W positions of each
         sequence kept in bf16 (they enter the quantised pool when they leave
-        the window)."""
+        the window).  codes = "int" (INT8/INT4) or "e4m3" (FP8, bits = 8)."""
         self.lib = L.lib()
         self.cfg = L.KvcConfig(num_q_heads, num_kv_heads, HEAD_DIM, PAGE, bits, num_blocks, max_batch,
-                               max_blocks_per_seq, bf16_window)
+                               max_blocks_per_seq, bf16_window,
+                               {"int": L.KVC_CODES_INT, "e4m3": L.KVC_CODES_E4M3}[codes])
         self.bf16_window = bf16_window
+        self.codes = codes
         self.num_q_heads, self.num_kv_heads, self.bits = num_q_heads, num_kv_heads, bits
         self.group = num_q_heads // num_kv_heads
         self.num_blocks, self.max_batch, self.max_blocks_per_seq = num_blocks, max_batch, max_blocks_per_seq

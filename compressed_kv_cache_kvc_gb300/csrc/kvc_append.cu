@@ -25,7 +25,22 @@ __device__ __forceinline__ float bf16_to_f32(uint32_t bits16) {
 
 // Quantise one 128-value row (4 values per lane, one warp) into pool slot
 // `slot` of (sequence b, KV head h): codes, scale, and for K the position and
-// the initial score.
+// the initial score.  Integer codes, or with E4M3 codes (s.fp8) scale =
+// amax / 448 and each x / scale converted to FP8.
+// Four fp32 values -> four FP8 E4M3 codes (byte i = value i), rounded to
+// nearest even and saturated to +-448 by the conversion instruction (which
+// packs its first source into the upper byte).
+__device__ __forceinline__ uint32_t e4m3x4(float y0, float y1, float y2, float y3) {
+  uint32_t w;
+  asm("{\n .reg .b16 l, h;\n"
+      " cvt.rn.satfinite.e4m3x2.f32 l, %2, %1;\n"
+      " cvt.rn.satfinite.e4m3x2.f32 h, %4, %3;\n"
+      " mov.b32 %0, {l, h};\n}"
+      : "=r"(w)
+      : "f"(y0), "f"(y1), "f"(y2), "f"(y3));
+  return w;
+}
+
 template <int BITS>
 __device__ __forceinline__ void quantize_row(const DevState& s, int b, int h, int kv, int slot, int p, float score,
                                              uint2 raw, int lane) {
@@ -40,13 +55,16 @@ __device__ __forceinline__ void quantize_row(const DevState& s, int b, int h, in
   float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  const float scale = __fdiv_rn(amax, kQmax);
-  int c[4];
+  const bool fp8 = BITS == 8 && s.fp8;
+  const float scale = __fdiv_rn(amax, fp8 ? 448.0f : kQmax);
+  int c[4] = {0, 0, 0, 0};
+  if (!fp8) {
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    int q = 0;
-    if (scale > 0.0f) q = __float2int_rn(__fdiv_rn(x[e], scale));
-    c[e] = min(max(q, kLo), kHi);
+    for (int e = 0; e < 4; ++e) {
+      int q = 0;
+      if (scale > 0.0f) q = __float2int_rn(__fdiv_rn(x[e], scale));
+      c[e] = min(max(q, kLo), kHi);
+    }
   }
   const int page = slot / kPage;
   const int off = slot % kPage;
@@ -57,7 +75,12 @@ __device__ __forceinline__ void quantize_row(const DevState& s, int b, int h, in
   }
   const size_t sidx = ((size_t)blk * s.hkv + h) * kPage + off;
   uint8_t* codes = (kv ? s.v_codes : s.k_codes) + sidx * s.row_bytes;
-  if (BITS == 8) {
+  if (fp8) {
+    float y[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) y[e] = scale > 0.0f ? __fdiv_rn(x[e], scale) : 0.0f;
+    *reinterpret_cast<uint32_t*>(codes + lane * 4) = e4m3x4(y[0], y[1], y[2], y[3]);
+  } else if (BITS == 8) {
     const uint32_t packed = (uint32_t)(c[0] & 0xFF) | ((uint32_t)(c[1] & 0xFF) << 8) |
                             ((uint32_t)(c[2] & 0xFF) << 16) | ((uint32_t)(c[3] & 0xFF) << 24);
     *reinterpret_cast<uint32_t*>(codes + lane * 4) = packed;

@@ -132,6 +132,27 @@ __device__ __forceinline__ void i8x4_to_h2(uint32_t wx, uint32_t& lo, uint32_t& 
 __device__ __forceinline__ uint32_t i8_pair_to_h2(uint32_t x, uint32_t y, uint32_t sel) {
   return hsub2((prmt(x, y, sel) & 0x00FF00FFu) ^ 0x64806480u, 0x64806480u);
 }
+// FP8 E4M3 codes -> fp16 (every E4M3 value is exact in fp16), by the
+// conversion instruction: 4 codes (bytes b0..b3 of w) -> (b0, b1) and (b2, b3).
+__device__ __forceinline__ void e4m3x4_to_h2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n .reg .b16 l, h;\n"
+      " mov.b32 {l, h}, %2;\n"
+      " cvt.rn.f16x2.e4m3x2 %0, l;\n"
+      " cvt.rn.f16x2.e4m3x2 %1, h;\n}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+// Byte k of x and byte k of y (E4M3 codes) -> fp16x2 (x_k, y_k).
+__device__ __forceinline__ uint32_t e4m3_pair_to_h2(uint32_t x, uint32_t y, int k) {
+  const uint32_t pr = prmt(x, y, (uint32_t)k | ((uint32_t)(4 + k) << 4));
+  uint32_t d;
+  asm("{\n .reg .b16 l, h;\n"
+      " mov.b32 {l, h}, %1;\n"
+      " cvt.rn.f16x2.e4m3x2 %0, l;\n}"
+      : "=r"(d)
+      : "r"(pr));
+  return d;
+}
 // Low nibbles of the two 16-bit halves (INT4 codes) -> fp16x2.
 __device__ __forceinline__ uint32_t i4_lo_to_h2(uint32_t v) {
   return hsub2((v & 0x000F000Fu) ^ 0x64086408u, 0x64086408u);
@@ -150,7 +171,9 @@ __device__ __forceinline__ int exponent_of(float x) {
   return (int)((__float_as_uint(x) >> 23) & 0xFF) - 127;
 }
 
-template <int BITS>
+// FP8: the 8-bit codes are FP8 E4M3 instead of INT8 (same layout, same
+// scales; only the code -> fp16 conversion differs).
+template <int BITS, bool FP8 = false>
 __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int seq_begin, int batch,
                                                                  const uint16_t* __restrict__ q,
                                                                  float qk_scale_log2, AttnWork w,
@@ -338,8 +361,13 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
 #pragma unroll
         for (int stp = 0; stp < 8; ++stp) {
           uint32_t a0, a1, a2, a3;
-          i8x4_to_h2(w0[stp] ^ 0x80808080u, a0, a2);
-          i8x4_to_h2(w1[stp] ^ 0x80808080u, a1, a3);
+          if (FP8) {
+            e4m3x4_to_h2(w0[stp], a0, a2);
+            e4m3x4_to_h2(w1[stp], a1, a3);
+          } else {
+            i8x4_to_h2(w0[stp] ^ 0x80808080u, a0, a2);
+            i8x4_to_h2(w1[stp] ^ 0x80808080u, a1, a3);
+          }
           mma16816(acc, a0, a1, a2, a3, bq[stp][0], bq[stp][1]);
         }
       } else {
@@ -427,13 +455,21 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             const int j = 2 * wd + half;
-            const uint32_t sa = (2 * half) | ((2 * half) << 4) | ((4 + 2 * half) << 8) | ((4 + 2 * half) << 12);
-            const uint32_t sb =
-                (2 * half + 1) | ((2 * half + 1) << 4) | ((5 + 2 * half) << 8) | ((5 + 2 * half) << 12);
-            const uint32_t a0 = i8_pair_to_h2(x0[wd], x2[wd], sa);
-            const uint32_t a1 = i8_pair_to_h2(x0[wd], x2[wd], sb);
-            const uint32_t a2 = i8_pair_to_h2(x1[wd], x3[wd], sa);
-            const uint32_t a3 = i8_pair_to_h2(x1[wd], x3[wd], sb);
+            uint32_t a0, a1, a2, a3;
+            if (FP8) {
+              a0 = e4m3_pair_to_h2(x0[wd], x2[wd], 2 * half);
+              a1 = e4m3_pair_to_h2(x0[wd], x2[wd], 2 * half + 1);
+              a2 = e4m3_pair_to_h2(x1[wd], x3[wd], 2 * half);
+              a3 = e4m3_pair_to_h2(x1[wd], x3[wd], 2 * half + 1);
+            } else {
+              const uint32_t sa = (2 * half) | ((2 * half) << 4) | ((4 + 2 * half) << 8) | ((4 + 2 * half) << 12);
+              const uint32_t sb =
+                  (2 * half + 1) | ((2 * half + 1) << 4) | ((5 + 2 * half) << 8) | ((5 + 2 * half) << 12);
+              a0 = i8_pair_to_h2(x0[wd], x2[wd], sa);
+              a1 = i8_pair_to_h2(x0[wd], x2[wd], sb);
+              a2 = i8_pair_to_h2(x1[wd], x3[wd], sa);
+              a3 = i8_pair_to_h2(x1[wd], x3[wd], sb);
+            }
             mma16816(oacc[j], a0, a1, a2, a3, pb0, pb1);
           }
         }
@@ -569,21 +605,22 @@ __global__ void __launch_bounds__(kMergeThreads, 2) attn_merge_kernel(DevState s
 }
 
 // cudaFuncSetAttribute is per device and per kernel: one flag per (BITS, device).
-template <int BITS>
+template <int BITS, bool FP8 = false>
 cudaError_t ensure_split_smem() {
   static int done[64] = {0};
-  return opt_in_smem(reinterpret_cast<const void*>(attn_split_kernel<BITS>), Geom<BITS>::kSmem, done);
+  return opt_in_smem(reinterpret_cast<const void*>(attn_split_kernel<BITS, FP8>), Geom<BITS>::kSmem, done);
 }
 
-template <int BITS>
+template <int BITS, bool FP8 = false>
 int split_ctas_per_sm() {
   static int cached[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 1;
   if (dev < 64 && cached[dev] > 0) return cached[dev];
-  if (ensure_split_smem<BITS>() != cudaSuccess) return 1;
+  if (ensure_split_smem<BITS, FP8>() != cudaSuccess) return 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_split_kernel<BITS>, kWarps * 32, Geom<BITS>::kSmem) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_split_kernel<BITS, FP8>, kWarps * 32,
+                                                    Geom<BITS>::kSmem) !=
           cudaSuccess ||
       n < 1)
     n = 1;
@@ -595,23 +632,27 @@ int split_ctas_per_sm() {
 
 int attention_smem_bytes(int bits) { return bits == 8 ? Geom<8>::kSmem : Geom<4>::kSmem; }
 
-int attention_ctas_per_sm(int bits) { return bits == 8 ? split_ctas_per_sm<8>() : split_ctas_per_sm<4>(); }
+int attention_ctas_per_sm(int bits, bool fp8) {
+  if (bits == 8) return fp8 ? split_ctas_per_sm<8, true>() : split_ctas_per_sm<8>();
+  return split_ctas_per_sm<4>();
+}
+
+template <int BITS, bool FP8>
+cudaError_t launch_split_t(const DevState& s, int seq_begin, int batch, const uint16_t* q, float qk_scale_log2,
+                           const AttnWork& w, bool spill, cudaStream_t st) {
+  const cudaError_t e = ensure_split_smem<BITS, FP8>();
+  if (e != cudaSuccess) return e;
+  attn_split_kernel<BITS, FP8><<<w.ncta, kWarps * 32, Geom<BITS>::kSmem, st>>>(s, seq_begin, batch, q,
+                                                                               qk_scale_log2, w, spill);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_attention_split(const DevState& s, int seq_begin, int batch, const uint16_t* q,
                                    float qk_scale_log2, const AttnWork& w, bool spill, cudaStream_t st) {
-  cudaError_t e;
-  if (s.bits == 8) {
-    e = ensure_split_smem<8>();
-    if (e != cudaSuccess) return e;
-    attn_split_kernel<8><<<w.ncta, kWarps * 32, Geom<8>::kSmem, st>>>(s, seq_begin, batch, q, qk_scale_log2, w,
-                                                                      spill);
-  } else {
-    e = ensure_split_smem<4>();
-    if (e != cudaSuccess) return e;
-    attn_split_kernel<4><<<w.ncta, kWarps * 32, Geom<4>::kSmem, st>>>(s, seq_begin, batch, q, qk_scale_log2, w,
-                                                                      spill);
-  }
-  return cudaGetLastError();
+  if (s.bits == 8)
+    return s.fp8 ? launch_split_t<8, true>(s, seq_begin, batch, q, qk_scale_log2, w, spill, st)
+                 : launch_split_t<8, false>(s, seq_begin, batch, q, qk_scale_log2, w, spill, st);
+  return launch_split_t<4, false>(s, seq_begin, batch, q, qk_scale_log2, w, spill, st);
 }
 
 cudaError_t launch_attention_merge(const DevState& s, int seq_begin, int batch, const uint16_t* q, uint16_t* out,

@@ -40,6 +40,8 @@ kvc_status config_check(const kvc_config* c) {
       c->num_q_heads / c->num_kv_heads > kvc::kMaxGroup)
     return KVC_ERR_UNSUPPORTED;
   if (c->bf16_window < 0) return KVC_ERR_INVALID_ARG;
+  if (c->codes != KVC_CODES_INT && c->codes != KVC_CODES_E4M3) return KVC_ERR_INVALID_ARG;
+  if (c->codes == KVC_CODES_E4M3 && c->bits != 8) return KVC_ERR_UNSUPPORTED;
   if (c->bf16_window > kvc::kMaxRing) return KVC_ERR_UNSUPPORTED;
   // 32-bit slot arithmetic inside the kernels
   if ((double)c->num_blocks * c->num_kv_heads * kvc::kPage >= 2147483647.0 ||
@@ -206,7 +208,7 @@ void attention_plan(kvc_cache* c, int32_t seq_begin, int32_t batch, void* d_work
   // replayed at other lengths stays correct)
   int ncta = 1;
   if (tp > 0) {
-    ncta = sm_count(c) * kvc::attention_ctas_per_sm(c->cfg.bits);
+    ncta = sm_count(c) * kvc::attention_ctas_per_sm(c->cfg.bits, c->cfg.codes == KVC_CODES_E4M3);
     ncta = (int)std::min<long long>(ncta, std::max<long long>(1, tp / kMinPagesPerCta));
     ncta = std::max(1, std::min(ncta, kvc::kMaxSplitCtas));
   }
@@ -364,6 +366,7 @@ kvc_status kvc_cache_create(const kvc_config* cfg, void* d_state, size_t state_b
   d.ring_v = reinterpret_cast<uint16_t*>(b + L.off[KVC_BUF_RING_V]);
   d.ring_score = reinterpret_cast<float*>(b + L.off[KVC_BUF_RING_SCORE]);
   d.ring = cfg->bf16_window;
+  d.fp8 = cfg->codes == KVC_CODES_E4M3 ? 1 : 0;
   d.hq = cfg->num_q_heads;
   d.hkv = cfg->num_kv_heads;
   d.group = cfg->num_q_heads / cfg->num_kv_heads;

@@ -36,6 +36,7 @@ struct DevState {
   float* ring_score;    // [max_batch][hkv][ring]
   int32_t hq, hkv, group, bits, row_bytes, num_blocks, max_batch, max_bps;
   int32_t ring;         // hybrid window W (0: off); ring slot of position p >= 4 is (p - 4) % W
+  int32_t fp8;          // 1: FP8 E4M3 codes (bits = 8), 0: integer codes
 };
 
 // Tokens held in the bf16 window of a sequence with P positions.
@@ -181,7 +182,7 @@ cudaError_t launch_step_moves(const DevState& s, int batch, const StepArgs& a, i
 int step_max_smem_bytes();  // dynamic shared memory of the post kernel (a multiple of 16)
 
 int attention_smem_bytes(int bits);
-int attention_ctas_per_sm(int bits);  // resident split CTAs per SM (occupancy API, cached)
+int attention_ctas_per_sm(int bits, bool fp8);  // resident split CTAs per SM (occupancy API, cached)
 int select_max_smem_slots();
 
 }  // namespace kvc

@@ -53,7 +53,8 @@ typedef enum {
   KVC_OK = 0,
   KVC_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, out-of-range value      */
   KVC_ERR_UNSUPPORTED = 2,  /* head_dim != 128, page_size != 16, bits not 4|8,
-                               more than 8 query heads per KV head             */
+                               E4M3 codes with bits != 8, more than 8 query
+                               heads per KV head                               */
   KVC_ERR_CAPACITY = 3,     /* pool or per-sequence block table would overflow
                                (the page's allocate_sequence returning False)  */
   KVC_ERR_CUDA = 4,         /* a CUDA runtime call failed                      */
@@ -81,7 +82,16 @@ typedef struct {
   int32_t bf16_window;        /* hybrid precision: the last W positions of each
                                  sequence are kept in bf16 (0 = off, W <= 4096);
                                  see "Hybrid precision" below                   */
+  int32_t codes;              /* KVC_CODES_INT, or KVC_CODES_E4M3 (bits = 8)     */
 } kvc_config;
+
+/* Code formats.  KVC_CODES_INT: scale = amax / (2^(bits-1) - 1), integer
+ * codes.  KVC_CODES_E4M3 (FP8; the pages list FP8 among their quantisation
+ * strategies): scale = amax / 448 (IEEE fp32 division), code = x / scale
+ * (IEEE fp32 division) rounded to FP8 E4M3, ties to even, saturating at
+ * +-448; one byte per code, same layout as INT8. */
+#define KVC_CODES_INT  0
+#define KVC_CODES_E4M3 1
 
 /* Hybrid precision (bf16_window = W > 0; "KV Cache optimization techniques"
  * section 1.3, HybridPrecisionKVCache: recent tokens at 16 bits, older ones

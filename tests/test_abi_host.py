@@ -210,3 +210,14 @@ def test_hybrid_window_validation(lib):
     # 4 sinks + 16 window + 33 pool slots need 3 pages > 2
     assert L.kvc_quantize_append(h, 0, 1, 53, dummy, dummy, None) == lib.KVC_ERR_CAPACITY
     L.kvc_cache_destroy(h)
+
+
+def test_code_format_validation(lib):
+    L = lib.lib()
+    assert L.kvc_state_bytes(ctypes.byref(_cfg(lib, codes=2))) == 0
+    assert L.kvc_state_bytes(ctypes.byref(_cfg(lib, codes=-1))) == 0
+    assert L.kvc_state_bytes(ctypes.byref(_cfg(lib, codes=lib.KVC_CODES_E4M3, bits=4))) == 0
+    st, h, fs = _create(lib, _cfg(lib, codes=lib.KVC_CODES_E4M3, bits=4))
+    assert st == lib.KVC_ERR_UNSUPPORTED
+    a = L.kvc_state_bytes(ctypes.byref(_cfg(lib, codes=lib.KVC_CODES_E4M3)))
+    assert a > 0 and a == L.kvc_state_bytes(ctypes.byref(_cfg(lib)))  # same layout as INT8
