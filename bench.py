@@ -616,7 +616,7 @@ def workload_report(args, name: str):
     caches, inputs = [], []
     for l in range(layers):
         c = KVCache(Hq, Hkv, w.bits, nblocks, B, mbps, block_order=order, device=dev,
-                    bf16_window=args.bf16_window)
+                    bf16_window=args.bf16_window, codes=args.codes)
         q, k, v, kn, vn = W.gen_layer_torch(w, l, dev)
         if np.all(lengths == T):
             c.quantize_append(k, v)
@@ -720,7 +720,7 @@ def workload_report(args, name: str):
     attn = float(np.median(attn_ms))
     line = {"workload": name, "layers": layers, "batch": B, "bits": w.bits,
             "mode": ("block, retention %g" % args.retention) if args.evict == "block" else w.mode,
-            "bf16_window": args.bf16_window,
+            "bf16_window": args.bf16_window, "codes": args.codes,
             "budgets": ({"schedule": args.schedule, "first": budgets[0], "middle": budgets[layers // 2],
                          "last": budgets[-1]} if args.schedule and w.mode == "h2o" else budgets[0]),
             "first_step": {"ms": ms, "kv_bytes": kv_bytes, "step_gbs": kv_bytes / (ms * 1e-3) / 1e9,
@@ -771,6 +771,8 @@ def main():
     ap.add_argument("--evict", default=None, choices=["block"],
                     help="report mode: block-granular eviction instead of the workload's mode")
     ap.add_argument("--retention", type=float, default=0.25, help="report mode, --evict block: pages kept")
+    ap.add_argument("--codes", default="int", choices=["int", "e4m3"],
+                    help="report mode: code format (e4m3: FP8 codes, 8-bit workloads)")
     ap.add_argument("--prefill", action="store_true",
                     help="report mode: time one layer's prefill (fresh prompts of the workload's context)")
     ap.add_argument("--bf16-window", type=int, default=0,
