@@ -63,6 +63,7 @@ _SIGS = {
     "kvc_cache_buffer": (_I, [_P, _I, ctypes.POINTER(_P), ctypes.POINTER(_SZ)]),
     "kvc_cache_lengths": (_I, [_P, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "kvc_cache_sync_host": (_I, [_P, _P]),
+    "kvc_release_sequences": (_I, [_P, _I, _I, _P]),
     "kvc_workspace_bytes": (_SZ, [_P, _I]),
     "kvc_quantize_append": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "kvc_decode_attention": (_I, [_P, _I, _I, _P, _P, ctypes.c_float, _I, _P, _SZ, _P]),

@@ -80,6 +80,12 @@ class KVCache:
             arr = (ctypes.c_int32 * len(vals))(*vals)
         L.check(self.lib.kvc_cache_reset(self.handle, arr, ctypes.c_void_p(_stream_ptr(stream))), "kvc_cache_reset")
 
+    def release(self, seq_begin: int = 0, batch: int = 1, stream=None):
+        """Free the sequences [seq_begin, seq_begin + batch): pages back to the
+        pool, lengths to 0 (idempotent)."""
+        L.check(self.lib.kvc_release_sequences(self.handle, seq_begin, batch, ctypes.c_void_p(_stream_ptr(stream))),
+                "kvc_release_sequences")
+
     def buffer(self, name: str) -> torch.Tensor:
         """Device view of one state buffer (uint8, reinterpret with .view)."""
         ptr, nb = ctypes.c_void_p(), ctypes.c_size_t()

@@ -429,6 +429,24 @@ kvc_status kvc_cache_reset(kvc_cache* c, const int32_t* h_block_order, void* str
   return KVC_OK;
 }
 
+kvc_status kvc_release_sequences(kvc_cache* c, int32_t seq_begin, int32_t batch, void* stream) {
+  if (!c) return KVC_ERR_INVALID_ARG;
+  c->last_launches = 0;
+  if (!range_ok(c, seq_begin, batch)) return KVC_ERR_INVALID_ARG;
+  bool any = false;
+  for (int i = 0; i < batch; ++i) any |= c->pos[seq_begin + i] != 0;
+  c->plan_pending = false;
+  if (!any) return KVC_OK;
+  if (kvc::launch_release_sequences(c->dev, seq_begin, batch, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return KVC_ERR_CUDA;
+  c->last_launches = 1;
+  for (int i = 0; i < batch; ++i) {
+    c->slots[seq_begin + i] = 0;
+    c->pos[seq_begin + i] = 0;
+  }
+  return KVC_OK;
+}
+
 kvc_status kvc_cache_sync_host(kvc_cache* c, void* stream) {
   if (!c) return KVC_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

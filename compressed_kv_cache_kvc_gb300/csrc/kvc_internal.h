@@ -149,6 +149,8 @@ cudaError_t launch_evict_blocks(const DevState& s, int seq_begin, int batch, int
                                 const unsigned long long* keys, cudaStream_t st);
 cudaError_t launch_release_blocks(const DevState& s, int seq_begin, int batch, const uint8_t* keep_mask,
                                   int s_cap, cudaStream_t st);
+// Whole sequences back to the pool (kvc_release_sequences).
+cudaError_t launch_release_sequences(const DevState& s, int seq_begin, int batch, cudaStream_t st);
 // g_holes / g_srcs: [batch][hkv][s_cap] move lists in the workspace, used when
 // smem_moves == 0; otherwise both lists (smem_moves entries each) live in
 // shared memory.

@@ -528,7 +528,41 @@ __global__ void __launch_bounds__(kBlockThreads) block_release_kernel(DevState s
   }
 }
 
+// Release whole sequences (one CTA each): every page of the row back to the
+// free stack, lengths to 0.
+__global__ void __launch_bounds__(kBlockThreads) release_seq_kernel(DevState s, int seq_begin) {
+  __shared__ int sh_base;
+  const int b = seq_begin + blockIdx.x;
+  const int S = s.seq_slots[b];
+  const int np = (S + kPage - 1) / kPage;
+  if (threadIdx.x == 0) {
+    int base = -1;
+    if (np > 0) {
+      base = atomicAdd(&s.counters[kCtrFreeTop], np);
+      if (base + np > s.num_blocks) {
+        atomicSub(&s.counters[kCtrFreeTop], np);
+        atomicOr(&s.counters[kCtrStatus], kDevStackOverflow);
+        base = -1;
+      }
+    }
+    sh_base = base;
+  }
+  __syncthreads();
+  const int32_t* row = s.block_table + (size_t)b * s.max_bps;
+  if (sh_base >= 0)
+    for (int j = threadIdx.x; j < np; j += blockDim.x) s.free_stack[sh_base + j] = row[j];
+  if (threadIdx.x == 0) {
+    s.seq_slots[b] = 0;
+    s.seq_pos[b] = 0;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_release_sequences(const DevState& s, int seq_begin, int batch, cudaStream_t st) {
+  release_seq_kernel<<<batch, kBlockThreads, 0, st>>>(s, seq_begin);
+  return cudaGetLastError();
+}
 
 int select_max_smem_slots() { return (200 * 1024) / 8; }
 

@@ -172,6 +172,14 @@ void kvc_cache_destroy(kvc_cache* cache);
  * NULL = ascending ids) and zero the host mirror.  Synchronises `stream`. */
 kvc_status kvc_cache_reset(kvc_cache* cache, const int32_t* h_block_order, void* stream);
 
+/* Release the sequences [seq_begin, seq_begin + batch) (the paged cache's
+ * free_sequence, "KV Cache optimization techniques" section 3.2): their
+ * pages return to the free-block stack and their lengths become 0, so the
+ * slots take a new prompt.  Idempotent: an empty sequence is left as it is.
+ * One launch (none when every sequence of the slice is empty); a pending
+ * selection is dropped. */
+kvc_status kvc_release_sequences(kvc_cache* cache, int32_t seq_begin, int32_t batch, void* stream);
+
 /* Device pointer and size of one buffer of the state (for inspection). */
 kvc_status kvc_cache_buffer(const kvc_cache* cache, int32_t which, void** d_ptr, size_t* bytes);
 

@@ -221,3 +221,14 @@ def test_code_format_validation(lib):
     assert st == lib.KVC_ERR_UNSUPPORTED
     a = L.kvc_state_bytes(ctypes.byref(_cfg(lib, codes=lib.KVC_CODES_E4M3)))
     assert a > 0 and a == L.kvc_state_bytes(ctypes.byref(_cfg(lib)))  # same layout as INT8
+
+
+def test_release_validation(lib):
+    L = lib.lib()
+    st, h, fs = _create(lib, _cfg(lib))
+    assert st == lib.KVC_OK
+    assert L.kvc_release_sequences(h, 1, 2, None) == lib.KVC_ERR_INVALID_ARG
+    assert L.kvc_release_sequences(h, -1, 1, None) == lib.KVC_ERR_INVALID_ARG
+    assert L.kvc_release_sequences(h, 0, 2, None) == lib.KVC_OK  # empty: nothing to launch
+    assert L.kvc_last_launch_count(h) == 0
+    L.kvc_cache_destroy(h)

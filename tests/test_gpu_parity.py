@@ -398,3 +398,47 @@ def test_bulk_append_equals_token_by_token(bits, W):
     for name in ["BLOCK_TABLE", "SEQ_SLOTS", "SEQ_POS", "SINK_K", "SINK_V"]:
         assert torch.equal(ca.buffer(name), cb.buffer(name)), name
     assert ca.read_status() == 0 and cb.read_status() == 0
+
+
+def test_release_sequences():
+    """Releasing a sequence returns its pages (no block lost or duplicated),
+    empties it, leaves the others alone, is idempotent, and the freed slot
+    takes a new prompt that leaves the state a fresh cache would hold."""
+    from compressed_kv_cache_kvc_gb300.cache import KVCache
+    rng = np.random.default_rng(90)
+    lengths = [300, 170, 90]
+    B, hkv, hq = 3, 2, 8
+    mbps = 24
+    cache = KVCache(hq, hkv, 8, B * mbps, B, mbps)
+    k = _rand_bits(rng, (B, hkv, 300, 128))
+    for b, n in enumerate(lengths):
+        cache.quantize_append(T.to_dev_bf16(np.ascontiguousarray(k[b:b + 1, :, :n])),
+                              T.to_dev_bf16(np.ascontiguousarray(k[b:b + 1, :, :n])), seq_begin=b)
+    q = T.to_dev_bf16(_rand_bits(rng, (B, hq, 128)))
+    kn = T.to_dev_bf16(_rand_bits(rng, (B, hkv, 1, 128)))
+    cache.decode_step(q, kn, kn, mode="h2o", budget=120, recent=16)
+    before = T.StateView(cache)
+    cache.release(1, 1)
+    assert cache.last_launch_count() == 1
+    after = T.StateView(cache)
+    assert cache.lengths(1) == (0, 0) and int(after.slots[1]) == 0 and int(after.seen[1]) == 0
+    for b in (0, 2):
+        assert cache.lengths(b) == (int(before.slots[b]), int(before.seen[b]))
+        for h in range(hkv):
+            for x, y in zip(before.head(b, h), after.head(b, h)):
+                assert np.array_equal(np.asarray(x).view(np.uint8), np.asarray(y).view(np.uint8))
+    used = np.concatenate([after.used_blocks(b) for b in (0, 2)])
+    free = after.free_stack[:int(after.counters[0])]
+    assert np.unique(np.concatenate([used, free])).size == B * mbps == used.size + free.size
+    cache.release(1, 1)  # idempotent
+    assert cache.last_launch_count() == 0
+    # a new prompt in the freed slot equals the same prompt in a fresh cache
+    k2 = _rand_bits(rng, (1, hkv, 200, 128))
+    cache.quantize_append(T.to_dev_bf16(k2), T.to_dev_bf16(k2), seq_begin=1)
+    fresh = KVCache(hq, hkv, 8, B * mbps, B, mbps)
+    fresh.quantize_append(T.to_dev_bf16(k2), T.to_dev_bf16(k2), seq_begin=1)
+    sa, sb = T.StateView(cache), T.StateView(fresh)
+    for h in range(hkv):
+        for x, y in zip(sa.head(1, h), sb.head(1, h)):
+            assert np.array_equal(np.asarray(x).view(np.uint8), np.asarray(y).view(np.uint8))
+    assert cache.read_status() == 0
