@@ -32,14 +32,15 @@ def _bf16(rng, shape):
     return x.to(torch.bfloat16).cuda()
 
 
-@pytest.mark.parametrize("bits,hq,hkv,lengths", [(8, 8, 2, [300, 47]), (4, 40, 8, [700, 130, 9])])
-def test_noalloc_matches_workspace_entry_point(bits, hq, hkv, lengths):
+@pytest.mark.parametrize("bits,hq,hkv,lengths,window", [(8, 8, 2, [300, 47], 0), (4, 40, 8, [700, 130, 9], 0),
+                                                         (8, 16, 4, [400, 30], 64)])  # with a bf16 window
+def test_noalloc_matches_workspace_entry_point(bits, hq, hkv, lengths, window):
     from compressed_kv_cache_kvc_gb300 import _lib as L
     from compressed_kv_cache_kvc_gb300.cache import KVCache
     rng = np.random.default_rng(bits + hq)
     B = len(lengths)
     mbps = (max(lengths) + 15) // 16 + 2
-    cache = KVCache(hq, hkv, bits, B * mbps, B, mbps)
+    cache = KVCache(hq, hkv, bits, B * mbps, B, mbps, bf16_window=window)
     for b, n in enumerate(lengths):
         cache.quantize_append(_bf16(rng, (1, hkv, n, 128)), _bf16(rng, (1, hkv, n, 128)), seq_begin=b)
     lib = L.lib()
