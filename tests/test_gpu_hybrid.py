@@ -180,3 +180,67 @@ def test_hybrid_h2o_selection_against_oracle(bits, W, recent):
                                      budget - 4 - recent, P - recent), (b, h)
         assert cache.lengths(b) == (budget - 4 - W, P)
     assert cache.read_status() == 0
+
+
+@pytest.mark.parametrize("bits,W,recent,budget", [(8, 48, 64, 200), (4, 32, 32, 150)])
+def test_hybrid_h2o_steps_lock_step(bits, W, recent, budget):
+    """Twelve one-call steps with a bf16 window and H2O eviction, in lock-step
+    with the oracle: each step's attention within tolerance, the window the
+    last W positions, the kept set (pool and window) the oracle's rule on its
+    scores up to near-ties, the kept tokens' scores close to the oracle's;
+    then the oracle takes the GPU's state (pool and window)."""
+    from compressed_kv_cache_kvc_gb300.cache import KVCache
+    rng = np.random.default_rng(bits * 13 + W)
+    hq, hkv, lengths, steps = 16, 4, [400, 211, 60], 12
+    B, T_ = len(lengths), max(lengths)
+    mbps = (T_ + steps + 15) // 16 + 2
+    cache = KVCache(hq, hkv, bits, B * mbps, B, mbps, bf16_window=W)
+    ora = O.OracleCache(B, hq, hkv, bits, bf16_window=W)
+    f = O.bf16_bits_to_f32
+    k = _bits(rng, (B, hkv, T_, 128))
+    v = _bits(rng, (B, hkv, T_, 128))
+    for b, n in enumerate(lengths):
+        cache.quantize_append(T.to_dev_bf16(np.ascontiguousarray(k[b:b + 1, :, :n])),
+                              T.to_dev_bf16(np.ascontiguousarray(v[b:b + 1, :, :n])), seq_begin=b)
+        ora.append(b, f(k[b, :, :n]), f(v[b, :, :n]))
+    for step in range(steps):
+        kn = _bits(rng, (B, hkv, 1, 128))
+        vn = _bits(rng, (B, hkv, 1, 128))
+        q = _bits(rng, (B, hq, 128))
+        out = T.bf16_tensor_to_f32(cache.decode_step(T.to_dev_bf16(q), T.to_dev_bf16(kn), T.to_dev_bf16(vn),
+                                                     mode="h2o", budget=budget, recent=recent))
+        st = T.StateView(cache)
+        for b in range(B):
+            ora.append(b, f(kn[b]), f(vn[b]))
+            T.assert_attention_close(out[b], ora.attend(b, f(q[b]), T.sm_scale()), f"step {step} b={b}")
+            s = ora.seqs[b]
+            P = s.pos_total
+            ns = min(P, 4)
+            for h in range(hkv):
+                hs = s.heads[h]
+                pos, kc, ks, vc, vs, sc = st.head(b, h)
+                rpos, _, _, rsc = st.ring_head(b, h)
+                assert np.array_equal(rpos, np.arange(max(4, P - W), P))
+                kept = set(pos.tolist()) | set(rpos.tolist())
+                by_pos = dict(zip(hs.pos.tolist(), hs.score.tolist()))
+                exact = O.select_h2o(hs.pos, hs.score, P, budget, recent, ns)
+                ora_kept = set(hs.pos[exact].tolist())
+                if kept != ora_kept:
+                    assert T.kept_sets_agree(kept, ora_kept, hs.pos, hs.score, budget - 4 - recent, P - recent), \
+                        (step, b, h)
+                assert len(kept) == min(len(hs.pos), budget - 4)
+                np.testing.assert_allclose(sc, [by_pos[p] for p in pos.tolist()], rtol=2e-3, atol=1e-5)
+                np.testing.assert_allclose(rsc, [by_pos[p] for p in rpos.tolist()], rtol=2e-3, atol=1e-5)
+                # lock-step: the oracle takes the GPU's kept tokens; the window
+                # tokens' codes are the oracle's own (the ageing reproduces them)
+                idx = {p: i for i, p in enumerate(hs.pos.tolist())}
+                ri = np.array([idx[p] for p in rpos.tolist()], dtype=np.int64)
+                ora.load_head(b, h, np.concatenate([pos, rpos]),
+                              np.concatenate([kc, hs.kcodes[ri]]), np.concatenate([ks, hs.kscale[ri]]),
+                              np.concatenate([vc, hs.vcodes[ri]]), np.concatenate([vs, hs.vscale[ri]]),
+                              np.concatenate([sc, rsc]).astype(np.float64))
+                s.sink_score[h] = st.sink_score[b, h, :ns].astype(np.float64)
+        used = np.concatenate([st.used_blocks(b) for b in range(B)])
+        free = st.free_stack[:int(st.counters[0])]
+        assert np.unique(np.concatenate([used, free])).size == B * mbps == used.size + free.size
+    assert cache.read_status() == 0
