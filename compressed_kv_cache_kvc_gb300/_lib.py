@@ -16,6 +16,7 @@ KVC_ERR_CUDA = 4
 KVC_ERR_DEVICE = 5
 KVC_ERR_STATE = 6
 
+KVC_VERSION = 200  # the header this binding's structures follow
 KVC_ATTN_ACCUM_H2O = 0x1
 KVC_CODES_INT = 0
 KVC_CODES_E4M3 = 1
@@ -91,6 +92,8 @@ def lib() -> ctypes.CDLL:
             fn = getattr(L, name)
             fn.restype = res
             fn.argtypes = args
+        if L.kvc_version() != KVC_VERSION:
+            raise RuntimeError(f"{LIB_PATH} is version {L.kvc_version()}, the binding expects {KVC_VERSION}: rebuild it")
         _lib = L
     return _lib
 

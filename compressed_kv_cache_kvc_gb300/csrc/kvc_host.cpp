@@ -313,7 +313,7 @@ int plan_keep(const kvc_evict_params* p, int S, int P, int W) {
 
 extern "C" {
 
-int32_t kvc_version(void) { return 100; }
+int32_t kvc_version(void) { return KVC_VERSION; }
 
 const char* kvc_status_string(kvc_status s) {
   switch (s) {

@@ -364,7 +364,10 @@ int32_t kvc_last_launch_count(const kvc_cache* cache);
 
 const char* kvc_status_string(kvc_status status);
 
-/* Library version: major * 10000 + minor * 100 + patch. */
+/* Library version: major * 10000 + minor * 100 + patch.  A caller built
+ * against this header checks kvc_version() == KVC_VERSION before passing
+ * structures (kvc_config grew in 0.2: bf16_window, codes). */
+#define KVC_VERSION 200
 int32_t kvc_version(void);
 
 #ifdef __cplusplus

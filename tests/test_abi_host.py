@@ -36,7 +36,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_version_and_strings(lib):
     L = lib.lib()
-    assert L.kvc_version() == 100
+    assert L.kvc_version() == lib.KVC_VERSION == 200
     assert L.kvc_status_string(lib.KVC_ERR_CAPACITY) == b"out of cache capacity"
 
 
