@@ -34,6 +34,8 @@ CASES = [
     (8, 8, 8, 2, 3, 0),        # sinks only
     (8, 32, 8, 1, 257, 0),
     (4, 16, 4, 2, 150, 50),    # with a bf16 window: the last 50 tokens in the ring
+    (8, 64, 8, 1, 130, 0),     # the largest query group (G = 8)
+    (4, 8, 1, 2, 1, 0),        # a one-token prompt, one KV head
 ]
 
 

@@ -229,3 +229,39 @@ def test_step_with_pyramid_budgets():
                                          budget - 4 - recent, T_ + 1 - recent), (budget, b, h)
             assert c.lengths(b) == (budget - 4, T_ + 1)
         assert c.read_status() == 0
+
+
+@pytest.mark.parametrize("bits,hq,hkv", [(8, 64, 8), (4, 64, 8), (8, 8, 1), (4, 12, 4), (8, 42, 7), (8, 14, 2)])
+def test_step_head_layouts_against_oracle(bits, hq, hkv):
+    """The one-call step at the largest query group (G = 8: every MMA column
+    used), multi-query attention (one KV head) and odd groups (G = 3, 6, 7):
+    outputs within tolerance and kept sets the oracle's rule."""
+    from compressed_kv_cache_kvc_gb300.cache import KVCache
+    rng = np.random.default_rng(bits * 100 + hq * 10 + hkv)
+    B, n, budget, recent = 2, 300, 100, 24
+    lengths = [300, 137]
+    mbps = (n + 1 + 15) // 16 + 2
+    cache = KVCache(hq, hkv, bits, B * mbps, B, mbps)
+    k = _bits(rng, (B, hkv, n, 128))
+    v = _bits(rng, (B, hkv, n, 128))
+    for b, nb in enumerate(lengths):
+        cache.quantize_append(T.to_dev_bf16(np.ascontiguousarray(k[b:b + 1, :, :nb])),
+                              T.to_dev_bf16(np.ascontiguousarray(v[b:b + 1, :, :nb])), seq_begin=b)
+    q = _bits(rng, (B, hq, 128))
+    kn = _bits(rng, (B, hkv, 1, 128))
+    vn = _bits(rng, (B, hkv, 1, 128))
+    out = T.bf16_tensor_to_f32(cache.decode_step(T.to_dev_bf16(q), T.to_dev_bf16(kn), T.to_dev_bf16(vn),
+                                                 mode="h2o", budget=budget, recent=recent))
+    st = T.StateView(cache)
+    f = O.bf16_bits_to_f32
+    for b, nb in enumerate(lengths):
+        ora = O.OracleCache(1, hq, hkv, bits)
+        ora.append(0, f(k[b, :, :nb]), f(v[b, :, :nb]))
+        ora.append(0, f(kn[b]), f(vn[b]))
+        T.assert_attention_close(out[b], ora.attend(0, f(q[b]), T.sm_scale()), f"G={hq // hkv} b={b}")
+        masks = ora.keep_masks(0, "h2o", budget=budget, recent=recent)
+        for h in range(hkv):
+            hs = ora.seqs[0].heads[h]
+            assert T.kept_sets_agree(set(st.head(b, h)[0].tolist()), set(hs.pos[masks[h]].tolist()), hs.pos,
+                                     hs.score, budget - 4 - recent, nb + 1 - recent), (b, h)
+    assert cache.read_status() == 0
