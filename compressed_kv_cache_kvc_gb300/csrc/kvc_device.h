@@ -333,6 +333,13 @@ __device__ __forceinline__ void ring_score_pass(const DevState& s, const AttnWor
   }
 }
 
+// Pool slot index of slot t of a sequence's row for KV head h, or -1 (which
+// move_rows rejects) when the row's block id is outside the pool.
+__device__ __forceinline__ int32_t slot_index(const DevState& s, const int32_t* row, int t, int h) {
+  const int blk = row[t / kPage];
+  return (unsigned)blk < (unsigned)s.num_blocks ? (blk * s.hkv + h) * kPage + (t % kPage) : -1;
+}
+
 // H2O increment of one pool slot: sum over the G query heads of its softmax
 // probability, from the spilled log2-domain logits ([g][slot] rows).
 __device__ __forceinline__ float h2o_increment(const float* lgr, int s_cap, int t, int G, const MergeShared& ms) {

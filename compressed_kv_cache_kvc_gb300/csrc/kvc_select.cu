@@ -201,11 +201,11 @@ __global__ void __launch_bounds__(kCompactThreads, 2) compact_kernel(DevState s,
     int ps = src_base + (incl >> 16) - ns;
     for (uint32_t m = hole_bits; m; m &= m - 1) {
       const int t = t0 + __ffs(m) - 1;
-      holes[ph++] = (btp[t / kPage] * hkv + h) * kPage + (t % kPage);
+      holes[ph++] = slot_index(s, btp, t, h);
     }
     for (uint32_t m = src_bits; m; m &= m - 1) {
       const int t = t0 + __ffs(m) - 1;
-      srcs[ps++] = (btp[t / kPage] * hkv + h) * kPage + (t % kPage);
+      srcs[ps++] = slot_index(s, btp, t, h);
     }
     hole_base += tot_packed & 0xFFFF;
     src_base += tot_packed >> 16;

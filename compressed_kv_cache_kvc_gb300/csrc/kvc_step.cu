@@ -264,8 +264,8 @@ __global__ void __launch_bounds__(NT, 1024 / NT) step_post_kernel(DevState s, in
       const uint32_t msk = __ballot_sync(0xffffffffu, (src_bits >> i) & 1u);
       if ((mh | msk) == 0u) continue;
       const int t = wbase + 32 * i;
-      if ((hole_bits >> i) & 1u) holes[ph + __popc(mh & lt)] = (btp[t / kPage] * hkv + h) * kPage + (t % kPage);
-      if ((src_bits >> i) & 1u) srcs[ps + __popc(msk & lt)] = (btp[t / kPage] * hkv + h) * kPage + (t % kPage);
+      if ((hole_bits >> i) & 1u) holes[ph + __popc(mh & lt)] = slot_index(s, btp, t, h);
+      if ((src_bits >> i) & 1u) srcs[ps + __popc(msk & lt)] = slot_index(s, btp, t, h);
       ph += __popc(mh);
       ps += __popc(msk);
     }
