@@ -137,3 +137,83 @@ class _single:
 
     def head(self, _b, h):
         return self.sv.head(self.b, h)
+
+
+FEATURES = [
+    ("hybrid", "qwen14b_b32_gqa5_t8192_int4_h2o_48l"),   # bf16 window of the recent 512 positions
+    ("fp8", "llama7b_b16_h32_t4096_int8_h2o"),          # FP8 E4M3 codes
+    ("block", "qwen14b_b32_gqa5_t8192_int4_h2o_48l"),    # block-granular eviction, 25 % of the pages kept
+]
+
+
+@pytest.mark.parametrize("feature,name", FEATURES)
+def test_full_size_features_sampled(feature, name):
+    """One full-size layer per feature at the bench's launch configuration:
+    two sampled sequences against the oracle (outputs; FP8 codes bit for bit;
+    kept sets), and on every (sequence, KV head) the kept counts and block
+    conservation; block eviction's mask is the oracle's rule on the GPU's own
+    scores for every sequence."""
+    from compressed_kv_cache_kvc_gb300 import workloads as W
+    from compressed_kv_cache_kvc_gb300.cache import KVCache
+    w = W.WORKLOADS[name]
+    d = W.gen_layer(w, 0)
+    B, hq, hkv, n = w.batch, w.num_q_heads, w.num_kv_heads, w.context
+    window = w.recent if feature == "hybrid" else 0
+    codes = "e4m3" if feature == "fp8" else "int"
+    mbps = (n + 1 + 15) // 16 + 1
+    cache = KVCache(hq, hkv, w.bits, B * mbps, B, mbps, bf16_window=window, codes=codes)
+    cache.quantize_append(T.to_dev_bf16(d["k"]), T.to_dev_bf16(d["v"]))
+    f = O.bf16_bits_to_f32
+    sample = sorted(np.random.default_rng(98).choice(B, size=2, replace=False).tolist())
+    oras = {}
+    for b in sample:
+        oras[b] = O.OracleCache(1, hq, hkv, w.bits, bf16_window=window, codes=codes)
+        oras[b].append(0, f(d["k"][b]), f(d["v"][b]))
+    if feature == "fp8":
+        st = T.StateView(cache)
+        for b in sample:
+            for h in range(hkv):
+                T.check_codes(_single(st, b), oras[b], 0, h)
+    del d["k"], d["v"]
+    q, kn, vn = T.to_dev_bf16(d["q"]), T.to_dev_bf16(d["k_new"]), T.to_dev_bf16(d["v_new"])
+    if feature == "block":
+        retention = 0.25
+        cache.quantize_append(kn, vn)
+        out = cache.decode_attention(q)
+        pre = T.StateView(cache)
+        mask = cache.h2o_select_evict(B, mode="block", recent=w.recent, retention=retention).cpu().numpy()
+        cache.compact_blocks(torch.from_numpy(mask).cuda(), B)
+        for b in range(B):
+            S = int(pre.slots[b])
+            want = O.select_blocks([pre.head(b, h)[5].astype(np.float64) for h in range(hkv)], S, w.recent,
+                                   retention)
+            for h in range(hkv):
+                assert np.array_equal(mask[b, h, :S] == 1, want), (b, h)
+            assert cache.lengths(b)[0] == int(want.sum())
+    else:
+        out = cache.decode_step(q, kn, vn, mode="h2o", budget=w.budget, recent=w.recent)
+    gpu = T.bf16_tensor_to_f32(out)
+    post = T.StateView(cache)
+    for b in sample:
+        ora = oras[b]
+        ora.append(0, f(d["k_new"][b]), f(d["v_new"][b]))
+        T.assert_attention_close(gpu[b], ora.attend(0, f(d["q"][b]), T.sm_scale()), f"{feature} b={b}")
+        if feature == "block":
+            continue
+        P = n + 1
+        masks = ora.keep_masks(0, "h2o", budget=w.budget, recent=w.recent)
+        for h in range(hkv):
+            hs = ora.seqs[0].heads[h]
+            kept = set(post.head(b, h)[0].tolist())
+            if window:
+                kept |= set(post.ring_head(b, h)[0].tolist())
+            assert T.kept_sets_agree(kept, set(hs.pos[masks[h]].tolist()), hs.pos, hs.score,
+                                     w.budget - 4 - w.recent, P - w.recent), (b, h)
+    if feature != "block":
+        nr = min(window, n + 1 - 4) if window else 0
+        for b in range(B):
+            assert cache.lengths(b) == (w.budget - 4 - nr, n + 1)
+    used = np.concatenate([post.used_blocks(b) for b in range(B)])
+    free = post.free_stack[:int(post.counters[0])]
+    assert np.unique(np.concatenate([used, free])).size == B * mbps == used.size + free.size
+    assert cache.read_status() == 0
