@@ -53,23 +53,24 @@ def _check_state(cache, ora, B):
 
 
 ATTN_CASES = [
-    # bits, hq, hkv, lengths, W, steps
-    (8, 8, 2, [300, 41, 130], 64, 4),
-    (4, 40, 8, [500, 90], 50, 3),
-    (8, 16, 4, [20, 70], 100, 3),     # the first sequence stays inside the window: empty pool
-    (4, 8, 8, [1000], 16, 2),
-    (8, 32, 8, [260], 200, 2),        # more than one window chunk
+    # bits, hq, hkv, lengths, W, steps, codes
+    (8, 8, 2, [300, 41, 130], 64, 4, "int"),
+    (4, 40, 8, [500, 90], 50, 3, "int"),
+    (8, 16, 4, [20, 70], 100, 3, "int"),     # the first sequence stays inside the window: empty pool
+    (4, 8, 8, [1000], 16, 2, "int"),
+    (8, 32, 8, [260], 200, 2, "int"),        # more than one window chunk
+    (8, 16, 4, [300, 77], 48, 3, "e4m3"),    # FP8 codes for the tokens that leave the window
 ]
 
 
-@pytest.mark.parametrize("bits,hq,hkv,lengths,W,steps", ATTN_CASES)
-def test_hybrid_attention_and_state_against_oracle(bits, hq, hkv, lengths, W, steps):
+@pytest.mark.parametrize("bits,hq,hkv,lengths,W,steps,codes", ATTN_CASES)
+def test_hybrid_attention_and_state_against_oracle(bits, hq, hkv, lengths, W, steps, codes):
     from compressed_kv_cache_kvc_gb300.cache import KVCache
     rng = np.random.default_rng(bits + hq + W)
     B, T_ = len(lengths), max(lengths)
     mbps = (T_ + steps + 15) // 16 + 2
-    cache = KVCache(hq, hkv, bits, B * mbps, B, mbps, bf16_window=W)
-    ora = O.OracleCache(B, hq, hkv, bits, bf16_window=W)
+    cache = KVCache(hq, hkv, bits, B * mbps, B, mbps, bf16_window=W, codes=codes)
+    ora = O.OracleCache(B, hq, hkv, bits, bf16_window=W, codes=codes)
     f = O.bf16_bits_to_f32
     k = _bits(rng, (B, hkv, T_, 128))
     v = _bits(rng, (B, hkv, T_, 128))
