@@ -14,6 +14,13 @@
  *   kvc_compact_blocks    move the kept tokens into the evicted slots and give
  *                         the emptied pages back to the pool.
  *
+ * kvc_decode_step runs those four for one layer in one call.  Around them:
+ * kvc_prefill_attention (a fresh prompt's causal attention and the H2O scores
+ * it gives), kvc_release_sequences (free finished sequences), and the
+ * options of the cache geometry: FP8 E4M3 codes and hybrid precision (the
+ * last W positions kept in bf16).  Eviction modes: H2O, StreamingLLM and
+ * block-granular (whole pages by mean score).
+ *
  * Sources (page title, section):
  *   - "KV Cache optimization techniques" (metaphor-xennon): 1.2 per-token
  *     quantisation, 2.2 H2O, 2.4 StreamingLLM cache, 3.2 PagedAttention cache;
@@ -21,7 +28,10 @@
  *     Models": 1.1 attention, 3.2 INT8 quantisation with dequantisation fused
  *     into the attention kernel and sinks kept in half precision, 3.3 sliding
  *     window, 3.4 H2O eviction;
- *   - "KV cache eviction and reuse survey" (tbxsx.cn): 3.3 H2O objective.
+ *   - "KV cache eviction and reuse survey" (tbxsx.cn): 3.3 H2O objective,
+ *     4 block manager (block-granular eviction by mean attention score);
+ *   - "KV Cache optimization techniques" also: 1.3 hybrid precision, 2.3
+ *     PyramidKV budgets (host side: compressed_kv_cache_kvc_gb300/budgets.py).
  *
  * Conventions shared by every call
  *   - The caller owns all device memory and the stream.  The library never
