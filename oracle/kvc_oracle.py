@@ -42,6 +42,9 @@ What it computes, step by step, each citing the page passage it restates:
   the attention matrix over its query rows; the survey page's section 3.3:
   a token's cumulative attention from all later tokens), in fp64 on the exact
   bf16 inputs.
+* ``OracleCache.prefill_chunk`` -- a prompt appended to a sequence that may
+  already hold context, each query attending causally to the compressed
+  cache as the decode step does (no GPU counterpart yet).
 * ``OracleCache(bf16_window=W)`` -- hybrid precision ("KV Cache optimization
   techniques" section 1.3, HybridPrecisionKVCache: recent tokens at 16 bits,
   older ones at INT4/INT8): the tokens at the last W positions attend with
@@ -506,6 +509,48 @@ class OracleCache:
         if self.codes == "e4m3":
             return e4m3_decode(np.asarray(codes).view(np.uint8)) * np.asarray(scale, np.float64)[..., None]
         return dequantize(codes, scale)
+
+    def prefill_chunk(self, b: int, q: np.ndarray, k: np.ndarray, v: np.ndarray,
+                      sm_scale: float | None = None, accumulate: bool = True) -> np.ndarray:
+        """A prompt of n tokens appended to sequence b, which may already
+        hold context (a later turn; the survey's prefill over the compressed
+        pool): append the tokens (quantised as on every append), then query
+        i (position P_old + i) attends, as the decode step does, to every
+        held token at a position <= P_old + i in its stored form (sinks and
+        bf16-window tokens exact, pool tokens dequantised).  With
+        ``accumulate`` every held token's score grows by the probabilities all
+        n queries (and the G query heads of its KV head) give it.  q: fp32
+        [Hq, n, D]; k, v: fp32 [Hkv, n, D].  Returns fp64 [Hq, n, D]."""
+        s = self.seqs[b]
+        p_old = s.pos_total
+        n = q.shape[1]
+        self.append(b, k, v)
+        d = self.d
+        if sm_scale is None:
+            sm_scale = 1.0 / math.sqrt(d)
+        out = np.zeros((self.hq, n, d), np.float64)
+        for h in range(self.hkv):
+            hs = s.heads[h]
+            ns = s.sink_k[h].shape[0]
+            kq = self.dequantize(hs.kcodes, hs.kscale)
+            vq = self.dequantize(hs.vcodes, hs.vscale)
+            if self.bf16_window > 0:
+                recent = hs.pos >= s.pos_total - self.bf16_window
+                kq[recent] = s.raw_k[h][hs.pos[recent]].astype(np.float64)
+                vq[recent] = s.raw_v[h][hs.pos[recent]].astype(np.float64)
+            keys = np.vstack([s.sink_k[h].astype(np.float64), kq])
+            vals = np.vstack([s.sink_v[h].astype(np.float64), vq])
+            kpos = np.concatenate([np.arange(ns), hs.pos])
+            inc = np.zeros(keys.shape[0], np.float64)
+            for i in range(n):
+                seen = kpos <= p_old + i
+                o, pr = attention(q[h * self.group:(h + 1) * self.group, i], keys[seen], vals[seen], sm_scale)
+                out[h * self.group:(h + 1) * self.group, i] = o
+                inc[seen] += h2o_increments(pr)
+            if accumulate:
+                s.sink_score[h] = s.sink_score[h] + inc[:ns]
+                hs.score = hs.score + inc[ns:]
+        return out
 
     # -- read path ----------------------------------------------------------
     def attend(self, b: int, q: np.ndarray, sm_scale: float | None = None,

@@ -631,3 +631,73 @@ def test_e4m3_row_quantiser_invariants():
     err = np.abs(dec - x.astype(np.float64))
     bound = np.abs(x) * 2.0 ** -4 * (1 + 1e-6) + scale[:, None] * 2.0 ** -10 * (1 + 1e-6)
     assert np.all(err <= bound)
+
+
+# ---------------------------------------------------------------------------
+# Prefill over the compressed cache (a prompt on a sequence with context)
+# ---------------------------------------------------------------------------
+
+def test_prefill_chunk_of_one_token_is_the_decode_step():
+    rng = np.random.default_rng(53)
+    Hq, Hkv, n = 8, 2, 60
+    k = _bf16_round(rng.standard_normal((Hkv, n + 1, 128)))
+    v = _bf16_round(rng.standard_normal((Hkv, n + 1, 128)))
+    q = _bf16_round(rng.standard_normal((Hq, 128)))
+    a, c = O.OracleCache(1, Hq, Hkv, 4), O.OracleCache(1, Hq, Hkv, 4)
+    for o in (a, c):
+        o.append(0, k[:, :n], v[:, :n])
+    a.append(0, k[:, n:], v[:, n:])
+    want = a.attend(0, q)
+    got = c.prefill_chunk(0, q[:, None, :], k[:, n:], v[:, n:])[:, 0]
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-13)
+    for h in range(Hkv):
+        np.testing.assert_allclose(c.seqs[0].heads[h].score, a.seqs[0].heads[h].score, rtol=0, atol=1e-13)
+
+
+def test_prefill_chunk_with_an_all_covering_window_is_the_exact_prefill():
+    """On a fresh sequence whose bf16 window covers every token, the chunk's
+    attention is the exact causal prefill, scores included."""
+    rng = np.random.default_rng(54)
+    Hq, Hkv, n = 4, 2, 40
+    q = _bf16_round(rng.standard_normal((Hq, n, 128)))
+    k = _bf16_round(rng.standard_normal((Hkv, n, 128)))
+    v = _bf16_round(rng.standard_normal((Hkv, n, 128)))
+    c = O.OracleCache(1, Hq, Hkv, 8, bf16_window=1000)
+    got = c.prefill_chunk(0, q, k, v)
+    want, sc = O.prefill_attention(q, k, v)
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+    for h in range(Hkv):
+        np.testing.assert_allclose(c.seqs[0].sink_score[h], sc[h, :4], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(c.seqs[0].heads[h].score, sc[h, 4:], rtol=0, atol=1e-12)
+
+
+def test_prefill_chunk_brute_force_after_eviction():
+    """A context with evicted tokens, then a 3-token chunk: plain-Python
+    causal attention over the held tokens in their stored form."""
+    rng = np.random.default_rng(55)
+    Hq, Hkv, n0, n, d = 2, 1, 12, 3, 128
+    k = _bf16_round(rng.standard_normal((Hkv, n0 + n, d)))
+    v = _bf16_round(rng.standard_normal((Hkv, n0 + n, d)))
+    q = _bf16_round(rng.standard_normal((Hq, n, d)))
+    c = O.OracleCache(1, Hq, Hkv, 4)
+    c.append(0, k[:, :n0], v[:, :n0])
+    c.evict(0, [np.array([True, False, True, True, False, True, False, True])])  # pool positions 4..11
+    got = c.prefill_chunk(0, q, k[:, n0:], v[:, n0:], accumulate=False)
+    hs = c.seqs[0].heads[0]
+    kept_pos = [0, 1, 2, 3] + hs.pos.tolist()
+    rows_k = {p: (k[0, p].astype(np.float64) if p < 4 else None) for p in kept_pos}
+    rows_v = {p: (v[0, p].astype(np.float64) if p < 4 else None) for p in kept_pos}
+    kq = O.dequantize(hs.kcodes, hs.kscale)
+    vq = O.dequantize(hs.vcodes, hs.vscale)
+    for j, p in enumerate(hs.pos.tolist()):
+        rows_k[p], rows_v[p] = kq[j], vq[j]
+    for g in range(Hq):
+        for i in range(n):
+            lim = n0 + i
+            ps = [p for p in kept_pos if p <= lim]
+            lg = [sum(float(q[g, i, e]) * float(rows_k[p][e]) for e in range(d)) / math.sqrt(d) for p in ps]
+            m = max(lg)
+            ex = [math.exp(x - m) for x in lg]
+            z = sum(ex)
+            want = [sum(ex[t] / z * float(rows_v[p][e]) for t, p in enumerate(ps)) for e in range(d)]
+            np.testing.assert_allclose(got[g, i], want, rtol=0, atol=1e-12)
