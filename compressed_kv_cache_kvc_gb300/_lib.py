@@ -74,6 +74,8 @@ _SIGS = {
     "kvc_decode_attention_noalloc": (_I, [_P, _I, _I, _P, _P, ctypes.c_float, _I, _P]),
     "kvc_prefill_workspace_bytes": (_SZ, [_P, _I, _I]),
     "kvc_prefill_attention": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, ctypes.c_float, _I, _P, _SZ, _P]),
+    "kvc_prefill_context_workspace_bytes": (_SZ, [_P, _I]),
+    "kvc_prefill_context": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, ctypes.c_float, _I, _P, _SZ, _P]),
     "kvc_read_status": (_I, [_P, ctypes.POINTER(_I), _P]),
     "kvc_set_trace_events": (_I, [_P, _P, _P]),
     "kvc_last_launch_count": (_I, [_P]),

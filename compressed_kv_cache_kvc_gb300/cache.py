@@ -219,6 +219,34 @@ class KVCache:
                                                ctypes.c_void_p(_stream_ptr(stream))), "kvc_prefill_attention")
         return out
 
+    def prefill_context(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seq_begin: int = 0, out=None,
+                        sm_scale: float | None = None, accumulate_h2o: bool = True, stream=None):
+        """A prompt on sequences that may hold context: q bf16 [batch, Hq, n,
+        128], k/v bf16 [batch, Hkv, n, 128] -> bf16 [batch, Hq, n, 128]; each
+        prompt query attends causally to the compressed cache."""
+        _need(q, torch.bfloat16, "q")
+        _need(k, torch.bfloat16, "k")
+        _need(v, torch.bfloat16, "v")
+        batch, n = q.shape[0], q.shape[2]
+        if q.dim() != 4 or q.shape[1] != self.num_q_heads or q.shape[3] != HEAD_DIM:
+            raise ValueError("q must be [batch, num_q_heads, n, 128]")
+        if tuple(k.shape) != (batch, self.num_kv_heads, n, HEAD_DIM) or k.shape != v.shape:
+            raise ValueError("k, v must be [batch, num_kv_heads, n, 128]")
+        if out is None:
+            out = torch.empty_like(q)
+        _need(out, torch.bfloat16, "out")
+        nbytes = self.lib.kvc_prefill_context_workspace_bytes(self.handle, batch)
+        raw = torch.empty(nbytes + 256, dtype=torch.uint8, device=self.device)
+        ws = raw[(-raw.data_ptr()) % 256:][:nbytes]
+        scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
+        L.check(self.lib.kvc_prefill_context(self.handle, seq_begin, batch, n, ctypes.c_void_p(q.data_ptr()),
+                                             ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()),
+                                             ctypes.c_void_p(out.data_ptr()), ctypes.c_float(scale),
+                                             L.KVC_ATTN_ACCUM_H2O if accumulate_h2o else 0,
+                                             ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                                             ctypes.c_void_p(_stream_ptr(stream))), "kvc_prefill_context")
+        return out
+
     def decode_step(self, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, mode: str = "h2o",
                     budget: int = 0, recent: int = 0, window: int = 0, seq_begin: int = 0, out=None,
                     sm_scale: float | None = None, workspace=None, stream=None,

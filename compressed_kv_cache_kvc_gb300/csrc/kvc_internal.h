@@ -165,6 +165,13 @@ cudaError_t launch_prefill(const DevState& s, int seq_begin, int batch, int n, c
                            const uint16_t* v, uint16_t* out, float* stats, float qk_scale_log2, bool scores,
                            cudaStream_t st);
 
+// A prompt on sequences with context (kvc_prefill_context), after its
+// append: per prompt query i the lengths that query may see (pass 0 keeps the
+// lengths from before the prompt in base[batch][2]), query i gathered into
+// qbuf, the previous output scattered; pass n restores the appended lengths.
+cudaError_t launch_ctx_step(const DevState& s, int seq_begin, int batch, int n, int i, int32_t* base,
+                            const uint16_t* q, uint16_t* qbuf, const uint16_t* obuf, uint16_t* out, cudaStream_t st);
+
 // Fused merge + H2O scores + selection + compaction (kvc_decode_step).
 struct StepArgs {
   int mode, budget, recent, window;

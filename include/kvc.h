@@ -358,6 +358,23 @@ kvc_status kvc_prefill_attention(kvc_cache* cache, int32_t seq_begin, int32_t ba
                                  const void* d_k, const void* d_v, void* d_out, float sm_scale, int32_t flags,
                                  void* d_workspace, size_t workspace_bytes, void* stream);
 
+/* A prompt of n tokens appended to sequences that may already hold context
+ * (a later turn), attending to the compressed cache: append the tokens (as
+ * kvc_quantize_append), then prompt query i (position P + i, P the positions
+ * seen before) attends, as a decode step does, to every held token at a
+ * position <= P + i in its stored form (sinks bf16, pool tokens dequantised),
+ * and with KVC_ATTN_ACCUM_H2O adds its probabilities to their H2O scores (the
+ * survey's prefill over the compressed pool).  Runs as n passes of the decode
+ * attention (a small step kernel, the split kernel, the merge kernel each),
+ * so its cost grows with n times the context: for fresh prompts
+ * kvc_prefill_attention is the fast path.  Shapes as kvc_prefill_attention;
+ * d_workspace: kvc_prefill_context_workspace_bytes(cache, batch) bytes.
+ * KVC_ERR_UNSUPPORTED with a bf16 window (bf16_window > 0). */
+size_t kvc_prefill_context_workspace_bytes(const kvc_cache* cache, int32_t batch);
+kvc_status kvc_prefill_context(kvc_cache* cache, int32_t seq_begin, int32_t batch, int32_t n, const void* d_q,
+                               const void* d_k, const void* d_v, void* d_out, float sm_scale, int32_t flags,
+                               void* d_workspace, size_t workspace_bytes, void* stream);
+
 /* ---------------------------------------------------------------- misc ---- */
 
 /* Synchronise `stream`, copy the device status word to *h_status and clear

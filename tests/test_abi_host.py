@@ -172,6 +172,41 @@ def test_block_eviction_page_limit(lib):
     L.kvc_cache_destroy(h)
 
 
+def test_prefill_context_validation(lib):
+    """A prompt over a sequence with context: bad ranges, lengths, flags,
+    scales and workspaces are refused, the capacity is checked and a bf16
+    window is unsupported, all before any launch."""
+    L = lib.lib()
+    st, h, fs = _create(lib, _cfg(lib, num_blocks=3, max_blocks_per_seq=2))
+    assert st == lib.KVC_OK
+    dummy = ctypes.c_void_p(fs.ptr.value)
+    ws = L.kvc_prefill_context_workspace_bytes(h, 1)
+    assert ws > L.kvc_workspace_bytes(h, 1)
+    assert L.kvc_prefill_context_workspace_bytes(None, 1) == 0 and L.kvc_prefill_context_workspace_bytes(h, 0) == 0
+    wsbuf = ctypes.create_string_buffer(ws + 512)
+    wsp = ctypes.c_void_p(ctypes.addressof(wsbuf) + (-ctypes.addressof(wsbuf)) % 256)
+
+    def call(handle=h, seq_begin=0, batch=1, n=5, scale=0.088, flags=1, nbytes=ws):
+        return L.kvc_prefill_context(handle, seq_begin, batch, n, dummy, dummy, dummy, dummy, ctypes.c_float(scale),
+                                     flags, wsp, nbytes, None)
+
+    assert call(handle=None) == lib.KVC_ERR_INVALID_ARG
+    for kw in [dict(seq_begin=1, batch=2), dict(n=0), dict(flags=4), dict(scale=-1.0), dict(scale=float("inf")),
+               dict(nbytes=ws - 1)]:
+        assert call(**kw) == lib.KVC_ERR_INVALID_ARG, kw
+    assert call(n=37) == lib.KVC_ERR_CAPACITY  # 4 sinks + 33 slots need 3 pages > 2
+    assert L.kvc_last_launch_count(h) == 0
+    s, p = ctypes.c_int32(), ctypes.c_int32()
+    assert L.kvc_cache_lengths(h, 0, ctypes.byref(s), ctypes.byref(p)) == lib.KVC_OK
+    assert (s.value, p.value) == (0, 0)
+    L.kvc_cache_destroy(h)
+    st, h, fs = _create(lib, _cfg(lib, num_blocks=3, max_blocks_per_seq=2, bf16_window=16))
+    assert st == lib.KVC_OK
+    dummy = ctypes.c_void_p(fs.ptr.value)
+    assert call(handle=h, nbytes=L.kvc_prefill_context_workspace_bytes(h, 1)) == lib.KVC_ERR_UNSUPPORTED
+    L.kvc_cache_destroy(h)
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     from compressed_kv_cache_kvc_gb300 import _lib as L
     monkeypatch.setattr(L, "_lib", None)

@@ -1,0 +1,133 @@
+"""A prompt on sequences that already hold context (a later turn): every
+prompt query attends causally to the compressed cache (sinks bf16, pool
+tokens dequantised, earlier prompt tokens included) and adds its
+probabilities to the H2O scores, against the oracle's prefill_chunk; the
+context is empty, a few sink tokens, a fresh prefill, or a prefill followed
+by a StreamingLLM eviction (pool slots no longer follow positions)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import kvc_oracle as O
+from tests import kvc_testlib as T
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from compressed_kv_cache_kvc_gb300.build import build_library
+    build_library()
+
+
+def _bits(rng, shape):
+    from compressed_kv_cache_kvc_gb300.workloads import bf16_bits
+    return bf16_bits(rng.standard_normal(shape).astype(np.float32))
+
+
+CASES = [
+    # bits, codes, hq, hkv, batch, context, n1, streaming window (0: no eviction)
+    (8, "int", 8, 2, 2, 0, 20, 0),        # an empty sequence: the first queries see only sinks
+    (4, "int", 16, 4, 2, 2, 30, 0),       # two sink tokens of context, appended one call earlier
+    (4, "int", 32, 8, 2, 100, 17, 0),     # a prefill's context, a prompt ending mid-page
+    (8, "int", 40, 8, 1, 200, 40, 64),    # G = 5, after a StreamingLLM eviction
+    (8, "e4m3", 16, 4, 1, 50, 25, 0),     # FP8 codes
+]
+
+
+@pytest.mark.parametrize("bits,codes,hq,hkv,batch,ctx,n1,window", CASES)
+def test_prefill_context_against_oracle(bits, codes, hq, hkv, batch, ctx, n1, window):
+    from compressed_kv_cache_kvc_gb300.cache import KVCache
+    rng = np.random.default_rng(bits + hq + ctx + n1)
+    mbps = (ctx + n1 + 15) // 16 + 2
+    cache = KVCache(hq, hkv, bits, batch * mbps, batch, mbps, codes=codes)
+    f = O.bf16_bits_to_f32
+    ora = O.OracleCache(batch, hq, hkv, bits, codes=codes)
+    if ctx:
+        k0 = _bits(rng, (batch, hkv, ctx, 128))
+        v0 = _bits(rng, (batch, hkv, ctx, 128))
+        if ctx < 4:
+            cache.quantize_append(T.to_dev_bf16(k0), T.to_dev_bf16(v0))
+            for b in range(batch):
+                ora.append(b, f(k0[b]), f(v0[b]))
+        else:
+            q0 = _bits(rng, (batch, hq, ctx, 128))
+            cache.prefill(T.to_dev_bf16(q0), T.to_dev_bf16(k0), T.to_dev_bf16(v0))
+            for b in range(batch):
+                ora.prefill(b, f(q0[b]), f(k0[b]), f(v0[b]), T.sm_scale())
+    if window:
+        mask = cache.h2o_select_evict(batch, mode="streaming", window=window)
+        cache.compact_blocks(mask, batch)
+        for b in range(batch):
+            ora.evict(b, ora.keep_masks(b, "streaming", window=window))
+    q1 = _bits(rng, (batch, hq, n1, 128))
+    k1 = _bits(rng, (batch, hkv, n1, 128))
+    v1 = _bits(rng, (batch, hkv, n1, 128))
+    out = T.bf16_tensor_to_f32(cache.prefill_context(T.to_dev_bf16(q1), T.to_dev_bf16(k1), T.to_dev_bf16(v1)))
+    append_launches = 2 if n1 >= 64 else 1
+    no_pages = sum(1 for i in range(n1) if ctx + i + 1 <= 4)  # passes that see sinks only: no split launch
+    # append, n passes of (step, split, merge), the last output's scatter
+    assert cache.last_launch_count() == append_launches + 3 * n1 - no_pages + 1
+    st = T.StateView(cache)
+    for b in range(batch):
+        ref = ora.prefill_chunk(b, f(q1[b]), f(k1[b]), f(v1[b]), T.sm_scale())
+        T.assert_attention_close(out[b].reshape(hq * n1, 128), ref.reshape(hq * n1, 128), f"b={b}")
+        s = ora.seqs[b]
+        assert cache.lengths(b) == (s.heads[0].pos.shape[0], s.pos_total)
+        assert int(st.slots[b]) == s.heads[0].pos.shape[0] and int(st.seen[b]) == s.pos_total
+        for h in range(hkv):
+            T.check_codes(st, ora, b, h)
+            ns = s.sink_k[h].shape[0]
+            np.testing.assert_allclose(st.sink_score[b, h, :ns], s.sink_score[h], rtol=1e-3, atol=1e-5)
+            pos, *_, score = st.head(b, h)
+            hs = s.heads[h]
+            np.testing.assert_allclose(score[np.argsort(pos)], hs.score[np.argsort(hs.pos)], rtol=1e-3, atol=1e-5)
+    assert cache.read_status() == 0
+
+
+def test_prefill_context_then_decode_step():
+    """A decode step after the second turn's prompt evicts by the scores of
+    both turns and its own: the kept sets are the oracle's."""
+    from compressed_kv_cache_kvc_gb300.cache import KVCache
+    rng = np.random.default_rng(62)
+    hq, hkv, batch, n0, n1, budget, recent = 16, 4, 2, 150, 30, 100, 24
+    mbps = (n0 + n1 + 1 + 15) // 16 + 2
+    cache = KVCache(hq, hkv, 8, batch * mbps, batch, mbps)
+    f = O.bf16_bits_to_f32
+    q0, k0, v0 = (_bits(rng, (batch, x, n0, 128)) for x in (hq, hkv, hkv))
+    q1, k1, v1 = (_bits(rng, (batch, x, n1, 128)) for x in (hq, hkv, hkv))
+    qn = _bits(rng, (batch, hq, 128))
+    kn, vn = (_bits(rng, (batch, hkv, 1, 128)) for _ in range(2))
+    cache.prefill(T.to_dev_bf16(q0), T.to_dev_bf16(k0), T.to_dev_bf16(v0))
+    cache.prefill_context(T.to_dev_bf16(q1), T.to_dev_bf16(k1), T.to_dev_bf16(v1))
+    out = T.bf16_tensor_to_f32(cache.decode_step(T.to_dev_bf16(qn), T.to_dev_bf16(kn), T.to_dev_bf16(vn),
+                                                 mode="h2o", budget=budget, recent=recent))
+    st = T.StateView(cache)
+    for b in range(batch):
+        ora = O.OracleCache(1, hq, hkv, 8)
+        ora.prefill(0, f(q0[b]), f(k0[b]), f(v0[b]), T.sm_scale())
+        ora.prefill_chunk(0, f(q1[b]), f(k1[b]), f(v1[b]), T.sm_scale())
+        ora.append(0, f(kn[b]), f(vn[b]))
+        T.assert_attention_close(out[b], ora.attend(0, f(qn[b]), T.sm_scale()), f"b={b}")
+        masks = ora.keep_masks(0, "h2o", budget=budget, recent=recent)
+        for h in range(hkv):
+            hs = ora.seqs[0].heads[h]
+            kept = set(st.head(b, h)[0].tolist())
+            assert T.kept_sets_agree(kept, set(hs.pos[masks[h]].tolist()), hs.pos, hs.score,
+                                     budget - 4 - recent, n0 + n1 + 1 - recent), (b, h)
+    assert cache.read_status() == 0
+
+
+def test_prefill_context_refuses_a_bf16_window():
+    from compressed_kv_cache_kvc_gb300 import _lib as L
+    from compressed_kv_cache_kvc_gb300.cache import KVCache
+    rng = np.random.default_rng(63)
+    cache = KVCache(8, 2, 8, 16, 1, 8, bf16_window=16)
+    q = T.to_dev_bf16(_bits(rng, (1, 8, 5, 128)))
+    k = T.to_dev_bf16(_bits(rng, (1, 2, 5, 128)))
+    with pytest.raises(L.KvcError) as e:
+        cache.prefill_context(q, k, k)
+    assert e.value.status == L.KVC_ERR_UNSUPPORTED
+    assert cache.lengths(0) == (0, 0)
