@@ -591,6 +591,78 @@ def prefill_report(args, name: str):
     print(json.dumps(line), flush=True)
 
 
+def prefill_context_report(args, name: str):
+    """Time one layer's prompt of args.prefill_context tokens on sequences
+    that hold the workload's context in the compressed cache
+    (kvc_prefill_context: append, then per prompt query the decode attention
+    over the pool, with H2O scores); the state is restored before every
+    timed call; inputs seeded, resident on the device.  Prints one JSON line
+    with the pool bytes the attention passes read per second against the
+    measured HBM peak."""
+    import numpy as np
+    import torch
+
+    from compressed_kv_cache_kvc_gb300 import workloads as W
+    from compressed_kv_cache_kvc_gb300.build import build_library
+    build_library()
+    from compressed_kv_cache_kvc_gb300.cache import KVCache
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = W.WORKLOADS[name]
+    B, Hq, Hkv, ctx, n1 = w.batch, w.num_q_heads, w.num_kv_heads, w.context, args.prefill_context
+    mbps = (ctx + n1 + 15) // 16 + 2
+    c = KVCache(Hq, Hkv, w.bits, B * mbps, B, mbps, device=dev, codes=args.codes)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1234)
+    k0 = torch.randn(B, Hkv, ctx, 128, device=dev, generator=g).to(torch.bfloat16)
+    v0 = torch.randn(B, Hkv, ctx, 128, device=dev, generator=g).to(torch.bfloat16)
+    q1 = torch.randn(B, Hq, n1, 128, device=dev, generator=g).to(torch.bfloat16)
+    k1 = torch.randn(B, Hkv, n1, 128, device=dev, generator=g).to(torch.bfloat16)
+    v1 = torch.randn(B, Hkv, n1, 128, device=dev, generator=g).to(torch.bfloat16)
+    c.quantize_append(k0, v0)
+    torch.cuda.synchronize()
+    snap = c.state_view.clone()
+    out = torch.empty_like(q1)
+    ws = c.prefill_context_workspace(B)
+    stream = torch.cuda.Stream(device=dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ms = []
+    for i in range(max(1, args.warmup) + args.steps):
+        c.state_view.copy_(snap)
+        torch.cuda.synchronize()
+        c.sync_host()
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            c.prefill_context(q1, k1, v1, out=out, workspace=ws, stream=stream)
+            ev1.record(stream)
+        ev1.synchronize()
+        if i >= max(1, args.warmup):
+            ms.append(ev0.elapsed_time(ev1))
+    st = c.read_status()
+    if st:
+        raise RuntimeError(f"device status {st:#x}")
+    launches = c.last_launch_count()
+    t = float(np.median(ms))
+    per_slot = 2 * (128 * w.bits // 8) + 2 * 4
+    s0 = max(0, ctx - 4)
+    # pass i reads the pool slots query i may see, and the four bf16 sinks
+    nbytes = sum((s0 + max(0, ctx + i + 1 - max(ctx, 4))) * per_slot + 4 * 2 * 128 * 2
+                 for i in range(n1)) * Hkv * B
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        pass
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    gbs = nbytes / (t * 1e-3) / 1e9
+    line = {"workload": name, "prefill_context": n1, "batch": B, "context": ctx, "q_heads": Hq, "kv_heads": Hkv,
+            "bits": w.bits, "codes": args.codes, "ms_per_call": t, "ms_per_query_pass": t / n1,
+            "prompt_tokens_per_s": B * n1 / (t * 1e-3), "pool_gbs": gbs, "pool_frac_of_hbm_peak": gbs / peak,
+            "peak_hbm_gbs": peak, "launches_per_call": launches, "steps_timed": args.steps,
+            "note": "one decode attention pass per prompt query; the time includes the prompt's append"}
+    print(json.dumps(line), flush=True)
+
+
 def workload_report(args, name: str):
     """Time the decode step of workload `name` on one GPU: all its layers,
     one `decode_step` per layer, replayed from a CUDA graph; the state is
@@ -776,6 +848,8 @@ def main():
                     help="report mode: code format (e4m3: FP8 codes, 8-bit workloads)")
     ap.add_argument("--prefill", action="store_true",
                     help="report mode: time one layer's prefill (fresh prompts of the workload's context)")
+    ap.add_argument("--prefill-context", type=int, default=0,
+                    help="report mode: time a prompt of this many tokens over the workload's context")
     ap.add_argument("--bf16-window", type=int, default=0,
                     help="report mode: hybrid precision, the last W positions kept in bf16 (W <= recent)")
     ap.add_argument("--oracle-child", nargs=2, type=int, default=None, help=argparse.SUPPRESS)
@@ -790,7 +864,10 @@ def main():
     if args.workload:
         from compressed_kv_cache_kvc_gb300 import workloads as W
         for name in (list(W.WORKLOADS) if args.workload == "all" else [args.workload]):
-            (prefill_report if args.prefill else workload_report)(args, name)
+            if args.prefill_context:
+                prefill_context_report(args, name)
+            else:
+                (prefill_report if args.prefill else workload_report)(args, name)
         return
     gpu_arm(args)
 

@@ -219,8 +219,13 @@ class KVCache:
                                                ctypes.c_void_p(_stream_ptr(stream))), "kvc_prefill_attention")
         return out
 
+    def prefill_context_workspace(self, batch: int) -> torch.Tensor:
+        nbytes = self.lib.kvc_prefill_context_workspace_bytes(self.handle, batch)
+        raw = torch.empty(nbytes + 256, dtype=torch.uint8, device=self.device)
+        return raw[(-raw.data_ptr()) % 256:][:nbytes]
+
     def prefill_context(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seq_begin: int = 0, out=None,
-                        sm_scale: float | None = None, accumulate_h2o: bool = True, stream=None):
+                        sm_scale: float | None = None, accumulate_h2o: bool = True, workspace=None, stream=None):
         """A prompt on sequences that may hold context: q bf16 [batch, Hq, n,
         128], k/v bf16 [batch, Hkv, n, 128] -> bf16 [batch, Hq, n, 128]; each
         prompt query attends causally to the compressed cache."""
@@ -235,9 +240,7 @@ class KVCache:
         if out is None:
             out = torch.empty_like(q)
         _need(out, torch.bfloat16, "out")
-        nbytes = self.lib.kvc_prefill_context_workspace_bytes(self.handle, batch)
-        raw = torch.empty(nbytes + 256, dtype=torch.uint8, device=self.device)
-        ws = raw[(-raw.data_ptr()) % 256:][:nbytes]
+        ws = self.prefill_context_workspace(batch) if workspace is None else workspace
         scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
         L.check(self.lib.kvc_prefill_context(self.handle, seq_begin, batch, n, ctypes.c_void_p(q.data_ptr()),
                                              ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()),

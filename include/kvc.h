@@ -16,7 +16,9 @@
  *
  * kvc_decode_step runs those four for one layer in one call.  Around them:
  * kvc_prefill_attention (a fresh prompt's causal attention and the H2O scores
- * it gives), kvc_release_sequences (free finished sequences), and the
+ * it gives), kvc_prefill_context (a prompt over sequences that hold context,
+ * each query attending to the compressed cache), kvc_release_sequences (free
+ * finished sequences), and the
  * options of the cache geometry: FP8 E4M3 codes and hybrid precision (the
  * last W positions kept in bf16).  Eviction modes: H2O, StreamingLLM and
  * block-granular (whole pages by mean score).

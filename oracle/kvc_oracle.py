@@ -44,7 +44,7 @@ What it computes, step by step, each citing the page passage it restates:
   bf16 inputs.
 * ``OracleCache.prefill_chunk`` -- a prompt appended to a sequence that may
   already hold context, each query attending causally to the compressed
-  cache as the decode step does (no GPU counterpart yet).
+  cache as the decode step does.
 * ``OracleCache(bf16_window=W)`` -- hybrid precision ("KV Cache optimization
   techniques" section 1.3, HybridPrecisionKVCache: recent tokens at 16 bits,
   older ones at INT4/INT8): the tokens at the last W positions attend with
