@@ -369,9 +369,18 @@ kvc_status kvc_prefill_attention(kvc_cache* cache, int32_t seq_begin, int32_t ba
  * survey's prefill over the compressed pool).  Runs as n passes of the decode
  * attention (a small step kernel, the split kernel, the merge kernel each),
  * so its cost grows with n times the context: for fresh prompts
- * kvc_prefill_attention is the fast path.  Shapes as kvc_prefill_attention;
- * d_workspace: kvc_prefill_context_workspace_bytes(cache, batch) bytes.
- * KVC_ERR_UNSUPPORTED with a bf16 window (bf16_window > 0). */
+ * kvc_prefill_attention is the fast path.
+ *   d_q:   bf16 [batch][Hq][n][128];  d_k, d_v: bf16 [batch][Hkv][n][128];
+ *   d_out: bf16 [batch][Hq][n][128];  all device memory, 16-byte aligned,
+ *   owned by the caller; flags 0 or KVC_ATTN_ACCUM_H2O; d_workspace:
+ *   kvc_prefill_context_workspace_bytes(cache, batch) bytes, 256-byte
+ *   aligned (scratch for the duration of the call, stream-ordered).
+ * The trace events (kvc_set_trace_events) bracket each pass's split kernel.
+ * Errors, before any launch: KVC_ERR_INVALID_ARG (range, n <= 0, flags,
+ * sm_scale not positive and finite, pointers, workspace);
+ * KVC_ERR_CAPACITY as kvc_quantize_append; KVC_ERR_UNSUPPORTED with a bf16
+ * window (bf16_window > 0) or batch > 1024.  KVC_ERR_CUDA when a launch
+ * fails part-way: the slice's lengths on the device are then undefined. */
 size_t kvc_prefill_context_workspace_bytes(const kvc_cache* cache, int32_t batch);
 kvc_status kvc_prefill_context(kvc_cache* cache, int32_t seq_begin, int32_t batch, int32_t n, const void* d_q,
                                const void* d_k, const void* d_v, void* d_out, float sm_scale, int32_t flags,
@@ -385,7 +394,9 @@ kvc_status kvc_read_status(kvc_cache* cache, int32_t* h_status, void* stream);
 
 /* Tracing: when both are non-NULL, the next kvc_decode_attention calls record
  * `ev_start` (a cudaEvent_t) just before the split-K attention kernel and
- * `ev_stop` just after it, on the call's stream.  NULL, NULL turns it off. */
+ * `ev_stop` just after it, on the call's stream (kvc_decode_step and
+ * kvc_prefill_context likewise, around each split launch).  NULL, NULL
+ * turns it off. */
 kvc_status kvc_set_trace_events(kvc_cache* cache, void* ev_start, void* ev_stop);
 
 /* Number of kernels the last call on this handle enqueued. */
