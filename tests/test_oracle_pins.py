@@ -401,6 +401,15 @@ def test_blocks_worked_example_with_a_tie():
     assert np.array_equal(keep, want)
 
 
+def test_blocks_tie_at_the_eviction_boundary():
+    # sums 5, 1, 4, 1, 9 with retention 0.7: int(5 * 0.3) = 1 block goes, and
+    # blocks 1 and 3 tie for it: the earlier one goes (a stable sort, as the
+    # survey page's sorted() leaves equal keys)
+    sc = _block_scores([5.0, 1.0, 4.0, 1.0, 9.0], extra=20)
+    keep = O.select_blocks(sc, 100, recent=20, retention=0.7)
+    assert np.array_equal(np.nonzero(~keep)[0], np.arange(16, 32))
+
+
 def test_blocks_edges():
     sc = _block_scores([3.0, 2.0, 1.0], extra=7)  # 55 slots
     assert O.select_blocks(sc, 55, recent=7, retention=1.0).all()          # keep everything
