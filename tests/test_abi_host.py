@@ -4,6 +4,8 @@ before anything reaches a GPU (so these run without one)."""
 import ctypes
 import os
 import re
+import shutil
+import subprocess
 
 import pytest
 
@@ -205,6 +207,22 @@ def test_prefill_context_validation(lib):
     dummy = ctypes.c_void_p(fs.ptr.value)
     assert call(handle=h, nbytes=L.kvc_prefill_context_workspace_bytes(h, 1)) == lib.KVC_ERR_UNSUPPORTED
     L.kvc_cache_destroy(h)
+
+
+def test_header_is_c99_and_the_abi_works_from_c(lib, tmp_path):
+    """include/kvc.h compiles as plain C99 (-pedantic, warnings as errors) and
+    a C program linked against the library makes the host-side calls."""
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    libdir = os.path.dirname(lib.LIB_PATH)
+    exe = str(tmp_path / "kvc_abi_c99")
+    cmd = ["gcc", "-std=c99", "-pedantic", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+           os.path.join(ROOT, "tests", "c", "kvc_abi_c99.c"), "-o", exe, "-L", libdir, "-lkvc",
+           "-Wl,-rpath," + libdir]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stderr
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
