@@ -178,6 +178,52 @@ def _attend_without_window(orig):
     return attend
 
 
+def _evict_complement(orig):
+    def evict(self, b, masks):
+        return orig(self, b, [~np.asarray(m, dtype=bool) for m in masks])
+    return evict
+
+
+def _attend_modulo_heads(orig):
+    """Query head j reads KV head j % Hkv instead of j // G."""
+    def attend(self, b, q, sm_scale=None, accumulate=True):
+        g, hkv = self.group, self.hkv
+        perm = np.array([gi * hkv + h for h in range(hkv) for gi in range(g)])
+        out = np.empty((self.hq, self.d))
+        out[perm] = orig(self, b, np.asarray(q)[perm], sm_scale, accumulate)
+        return out
+    return attend
+
+
+def _dequantize_as_int(orig):
+    def dequantize(self, codes, scale):
+        return O.dequantize(codes, scale)
+    return dequantize
+
+
+def _prefill_without_scores(orig):
+    def prefill(self, b, q, k, v, sm_scale=None):
+        out = orig(self, b, q, k, v, sm_scale)
+        s = self.seqs[b]
+        for h in range(self.hkv):
+            s.sink_score[h] = np.zeros_like(s.sink_score[h])
+            s.heads[h].score = np.zeros_like(s.heads[h].score)
+        return out
+    return prefill
+
+
+def _keep_masks_without_recent(orig):
+    def keep_masks(self, b, mode, budget=0, recent=0, window=0, retention=1.0):
+        return orig(self, b, mode, budget, 0 if mode == "h2o" else recent, window, retention)
+    return keep_masks
+
+
+def _chunk_without_scores(orig):
+    def prefill_chunk(self, b, q, k, v, sm_scale=None, accumulate=True):
+        return orig(self, b, q, k, v, sm_scale, False)
+    return prefill_chunk
+
+
 # name -> list of (object, attribute, factory(original) -> replacement)
 MUTANTS = {
     "INT8 scale divides by 128": [(O, "qmax_for_bits", lambda f: lambda bits: 128 if bits == 8 else f(bits))],
@@ -203,6 +249,13 @@ MUTANTS = {
     "FP8 scale from the E4M3-FNUZ maximum 240": [(O, "quantize_rows_e4m3", lambda f: _quantize_e4m3(240.0))],
     "KV size counts K only": [(O, "kv_cache_bytes", lambda f: lambda *a, **k: f(*a, **k) // 2)],
     "bf16 window ignored by the decode attention": [(O.OracleCache, "attend", _attend_without_window)],
+    "eviction keeps the complement of the mask": [(O.OracleCache, "evict", _evict_complement)],
+    "three sink tokens": [(O, "NUM_SINK", lambda f: 3)],
+    "query head j reads KV head j mod Hkv": [(O.OracleCache, "attend", _attend_modulo_heads)],
+    "FP8 codes dequantised as integers": [(O.OracleCache, "dequantize", _dequantize_as_int)],
+    "prefill leaves the scores at zero": [(O.OracleCache, "prefill", _prefill_without_scores)],
+    "H2O keep masks drop the recent window": [(O.OracleCache, "keep_masks", _keep_masks_without_recent)],
+    "prompt over context adds no scores": [(O.OracleCache, "prefill_chunk", _chunk_without_scores)],
 }
 
 

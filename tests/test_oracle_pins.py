@@ -376,6 +376,22 @@ def test_planted_heavy_hitters_kept_tiny_workload():
         assert planted and planted <= kept | set(range(p_total - w.recent, p_total))
 
 
+def test_cache_keep_masks_brute_force():
+    """keep_masks("h2o") of a cache after a few decode steps keeps what the
+    plain-Python rule keeps on that cache's positions and scores."""
+    B, Hq, Hkv, T = 1, 4, 2, 60
+    c, _, _, rng = _fill_cache(8, B, Hq, Hkv, T, 15)
+    for _ in range(3):
+        c.attend(0, rng.standard_normal((Hq, 128)).astype(np.float32))
+    s = c.seqs[0]
+    for budget, recent in [(30, 8), (20, 0), (14, 10), (4 + T, 8)]:
+        masks = c.keep_masks(0, "h2o", budget=budget, recent=recent)
+        for h in range(Hkv):
+            hs = s.heads[h]
+            want = _brute_select(hs.pos.tolist(), hs.score.tolist(), s.pos_total, budget, recent)
+            assert set(hs.pos[masks[h]].tolist()) == want, (budget, recent, h)
+
+
 # ---------------------------------------------------------------------------
 # block-granular eviction (the survey page's block manager)
 # ---------------------------------------------------------------------------
@@ -640,6 +656,39 @@ def test_e4m3_row_quantiser_invariants():
     err = np.abs(dec - x.astype(np.float64))
     bound = np.abs(x) * 2.0 ** -4 * (1 + 1e-6) + scale[:, None] * 2.0 ** -10 * (1 + 1e-6)
     assert np.all(err <= bound)
+
+
+def test_fp8_cache_attends_with_torch_float8_values():
+    """Library witness: an E4M3 cache's decode attention is torch SDPA over
+    the bf16 sinks and torch's float8_e4m3fn reading of the stored codes
+    times their scales; the codes are torch's conversion of x / scale."""
+    rng = np.random.default_rng(72)
+    Hq, Hkv, T = 4, 2, 50
+    k = _bf16_round(rng.standard_normal((Hkv, T, 128)) * 3)
+    v = _bf16_round(rng.standard_normal((Hkv, T, 128)))
+    q = _bf16_round(rng.standard_normal((Hq, 128)))
+    c = O.OracleCache(1, Hq, Hkv, 8, codes="e4m3")
+    c.append(0, k, v)
+    out = c.attend(0, q, accumulate=False)
+    s = c.seqs[0]
+
+    def f8(codes, scale):
+        t = torch.from_numpy(np.ascontiguousarray(codes).view(np.uint8)).view(torch.float8_e4m3fn).double()
+        return t * torch.from_numpy(np.asarray(scale, np.float64))[:, None]
+
+    keys, vals = [], []
+    for h in range(Hkv):
+        hs = s.heads[h]
+        keys.append(torch.cat([torch.from_numpy(s.sink_k[h]).double(), f8(hs.kcodes, hs.kscale)]))
+        vals.append(torch.cat([torch.from_numpy(s.sink_v[h]).double(), f8(hs.vcodes, hs.vscale)]))
+        x = torch.from_numpy(k[h, 4:])
+        sc = x.abs().amax(dim=-1, keepdim=True) / 448.0
+        want = (x / sc).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(hs.kcodes.view(np.uint8), want)
+    K = torch.stack(keys).repeat_interleave(Hq // Hkv, dim=0)
+    V = torch.stack(vals).repeat_interleave(Hq // Hkv, dim=0)
+    ref = torch.nn.functional.scaled_dot_product_attention(torch.from_numpy(q).double()[:, None, :], K, V)[:, 0]
+    assert np.allclose(out, ref.numpy(), atol=1e-12)
 
 
 # ---------------------------------------------------------------------------
