@@ -224,6 +224,24 @@ def _chunk_without_scores(orig):
     return prefill_chunk
 
 
+def _attend_window_one_long(orig):
+    def attend(self, b, q, sm_scale=None, accumulate=True):
+        w = self.bf16_window
+        if w > 0:
+            self.bf16_window = w + 1
+        try:
+            return orig(self, b, q, sm_scale, accumulate)
+        finally:
+            self.bf16_window = w
+    return attend
+
+
+def _block_masks_without_recent(orig):
+    def keep_masks(self, b, mode, budget=0, recent=0, window=0, retention=1.0):
+        return orig(self, b, mode, budget, 0 if mode == "block" else recent, window, retention)
+    return keep_masks
+
+
 # name -> list of (object, attribute, factory(original) -> replacement)
 MUTANTS = {
     "INT8 scale divides by 128": [(O, "qmax_for_bits", lambda f: lambda bits: 128 if bits == 8 else f(bits))],
@@ -256,6 +274,8 @@ MUTANTS = {
     "prefill leaves the scores at zero": [(O.OracleCache, "prefill", _prefill_without_scores)],
     "H2O keep masks drop the recent window": [(O.OracleCache, "keep_masks", _keep_masks_without_recent)],
     "prompt over context adds no scores": [(O.OracleCache, "prefill_chunk", _chunk_without_scores)],
+    "bf16 window one position too long": [(O.OracleCache, "attend", _attend_window_one_long)],
+    "block keep masks drop the recent pages": [(O.OracleCache, "keep_masks", _block_masks_without_recent)],
 }
 
 

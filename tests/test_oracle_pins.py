@@ -458,6 +458,29 @@ def test_blocks_against_numpy_means():
         assert keep[16 * n_cand:].all()
 
 
+def test_cache_block_masks_against_numpy_means():
+    """keep_masks("block") of a cache after a few decode steps: whole pages
+    of the pool (slot order), the lowest mean scores over all heads go, the
+    last `recent` slots and the unfilled page stay; the same mask for every
+    head."""
+    B, Hq, Hkv, T = 1, 4, 2, 150
+    c, _, _, rng = _fill_cache(8, B, Hq, Hkv, T, 16)
+    for _ in range(3):
+        c.attend(0, rng.standard_normal((Hq, 128)).astype(np.float32))
+    s = c.seqs[0]
+    n_slots = T - 4
+    for recent, retention in [(20, 0.5), (0, 0.25), (40, 0.9)]:
+        masks = c.keep_masks(0, "block", recent=recent, retention=retention)
+        n_cand = (n_slots - recent) // 16
+        means = np.array([np.mean([s.heads[h].score[16 * p:16 * p + 16] for h in range(Hkv)])
+                          for p in range(n_cand)])
+        want = np.ones(n_slots, dtype=bool)
+        for p in np.argsort(means, kind="stable")[:int(n_cand * (1.0 - retention))]:
+            want[16 * p:16 * p + 16] = False
+        for h in range(Hkv):
+            assert np.array_equal(masks[h], want), (recent, retention, h)
+
+
 # ---------------------------------------------------------------------------
 # Hybrid precision (the last W positions attend in bf16)
 # ---------------------------------------------------------------------------
