@@ -24,9 +24,16 @@ def _stream_ptr(stream=None) -> int:
     return s.cuda_stream
 
 
-def _need(t: torch.Tensor, dtype, name: str):
+def _need(t: torch.Tensor, dtype, name: str, device=None, shape=None):
+    """Argument check before any pointer goes to the library: a contiguous
+    CUDA tensor of `dtype` (on `device`, of `shape`, when given), since the
+    kernels read and write exactly the extents the call's sizes imply."""
     if not isinstance(t, torch.Tensor) or t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous CUDA tensor of dtype {dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the cache on {device}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, not {tuple(t.shape)}")
 
 
 class KVCache:
@@ -52,6 +59,8 @@ class KVCache:
         if nbytes == 0:
             raise L.KvcError(L.KVC_ERR_UNSUPPORTED, "kvc_state_bytes")
         self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        if self.device.type == "cuda" and self.device.index is None:
+            self.device = torch.device("cuda", torch.cuda.current_device())
         self.state = torch.empty(nbytes + 256, dtype=torch.uint8, device=self.device)
         off = (-self.state.data_ptr()) % 256
         self.state_view = self.state[off:off + nbytes]
@@ -133,8 +142,8 @@ class KVCache:
     # -- the decode step -----------------------------------------------------
     def quantize_append(self, k: torch.Tensor, v: torch.Tensor, seq_begin: int = 0, stream=None):
         """k, v: bf16 [batch, Hkv, n_new, 128]."""
-        _need(k, torch.bfloat16, "k")
-        _need(v, torch.bfloat16, "v")
+        _need(k, torch.bfloat16, "k", self.device)
+        _need(v, torch.bfloat16, "v", self.device)
         if k.shape != v.shape or k.dim() != 4 or k.shape[1] != self.num_kv_heads or k.shape[3] != HEAD_DIM:
             raise ValueError("k, v must be [batch, num_kv_heads, n_new, 128]")
         L.check(self.lib.kvc_quantize_append(self.handle, seq_begin, k.shape[0], k.shape[2],
@@ -145,14 +154,15 @@ class KVCache:
                          sm_scale: float | None = None, accumulate_h2o: bool = True, workspace=None,
                          stream=None) -> torch.Tensor:
         """q: bf16 [batch, Hq, 128] -> bf16 [batch, Hq, 128]."""
-        _need(q, torch.bfloat16, "q")
+        _need(q, torch.bfloat16, "q", self.device)
         if q.dim() != 3 or q.shape[1] != self.num_q_heads or q.shape[2] != HEAD_DIM:
             raise ValueError("q must be [batch, num_q_heads, 128]")
         batch = q.shape[0]
         if out is None:
             out = torch.empty_like(q)
-        _need(out, torch.bfloat16, "out")
+        _need(out, torch.bfloat16, "out", self.device, q.shape)
         ws = self.workspace(batch) if workspace is None else workspace
+        _need(ws, torch.uint8, "workspace", self.device)
         scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
         flags = L.KVC_ATTN_ACCUM_H2O if accumulate_h2o else 0
         L.check(self.lib.kvc_decode_attention(self.handle, seq_begin, batch, ctypes.c_void_p(q.data_ptr()),
@@ -172,8 +182,9 @@ class KVCache:
         m = {"h2o": L.KVC_EVICT_H2O, "streaming": L.KVC_EVICT_STREAMING, "block": L.KVC_EVICT_BLOCK}[mode]
         params = L.KvcEvictParams(m, budget, recent, window, retention)
         mask = self.new_keep_mask(batch) if keep_mask is None else keep_mask
-        _need(mask, torch.uint8, "keep_mask")
+        _need(mask, torch.uint8, "keep_mask", self.device, (batch, self.num_kv_heads, self.s_cap))
         ws = self.workspace(batch) if workspace is None else workspace
+        _need(ws, torch.uint8, "workspace", self.device)
         L.check(self.lib.kvc_h2o_select_evict(self.handle, seq_begin, batch, ctypes.byref(params),
                                               ctypes.c_void_p(mask.data_ptr()), ctypes.c_void_p(ws.data_ptr()),
                                               ws.numel(), ctypes.c_void_p(_stream_ptr(stream))),
@@ -182,8 +193,9 @@ class KVCache:
 
     def compact_blocks(self, keep_mask: torch.Tensor, batch: int, seq_begin: int = 0, workspace=None,
                        stream=None):
-        _need(keep_mask, torch.uint8, "keep_mask")
+        _need(keep_mask, torch.uint8, "keep_mask", self.device, (batch, self.num_kv_heads, self.s_cap))
         ws = self.workspace(batch) if workspace is None else workspace
+        _need(ws, torch.uint8, "workspace", self.device)
         L.check(self.lib.kvc_compact_blocks(self.handle, seq_begin, batch, ctypes.c_void_p(keep_mask.data_ptr()),
                                             ctypes.c_void_p(ws.data_ptr()), ws.numel(),
                                             ctypes.c_void_p(_stream_ptr(stream))), "kvc_compact_blocks")
@@ -194,22 +206,23 @@ class KVCache:
         [batch, Hkv, n, 128] -> causal attention output bf16 [batch, Hq, n,
         128]; the tokens are appended and (accumulate_h2o) their H2O scores
         set to the prompt attention's column sums."""
-        _need(q, torch.bfloat16, "q")
-        _need(k, torch.bfloat16, "k")
-        _need(v, torch.bfloat16, "v")
-        batch, n = q.shape[0], q.shape[2]
+        _need(q, torch.bfloat16, "q", self.device)
+        _need(k, torch.bfloat16, "k", self.device)
+        _need(v, torch.bfloat16, "v", self.device)
         if q.dim() != 4 or q.shape[1] != self.num_q_heads or q.shape[3] != HEAD_DIM:
             raise ValueError("q must be [batch, num_q_heads, n, 128]")
+        batch, n = q.shape[0], q.shape[2]
         if tuple(k.shape) != (batch, self.num_kv_heads, n, HEAD_DIM) or k.shape != v.shape:
             raise ValueError("k, v must be [batch, num_kv_heads, n, 128]")
         if out is None:
             out = torch.empty_like(q)
-        _need(out, torch.bfloat16, "out")
+        _need(out, torch.bfloat16, "out", self.device, q.shape)
         nbytes = self.lib.kvc_prefill_workspace_bytes(self.handle, batch, n)
         if workspace is None:
             raw = torch.empty(nbytes + 256, dtype=torch.uint8, device=self.device)
             off = (-raw.data_ptr()) % 256
             workspace = raw[off:off + nbytes]
+        _need(workspace, torch.uint8, "workspace", self.device)
         scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
         L.check(self.lib.kvc_prefill_attention(self.handle, seq_begin, batch, n, ctypes.c_void_p(q.data_ptr()),
                                                ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()),
@@ -229,18 +242,19 @@ class KVCache:
         """A prompt on sequences that may hold context: q bf16 [batch, Hq, n,
         128], k/v bf16 [batch, Hkv, n, 128] -> bf16 [batch, Hq, n, 128]; each
         prompt query attends causally to the compressed cache."""
-        _need(q, torch.bfloat16, "q")
-        _need(k, torch.bfloat16, "k")
-        _need(v, torch.bfloat16, "v")
-        batch, n = q.shape[0], q.shape[2]
+        _need(q, torch.bfloat16, "q", self.device)
+        _need(k, torch.bfloat16, "k", self.device)
+        _need(v, torch.bfloat16, "v", self.device)
         if q.dim() != 4 or q.shape[1] != self.num_q_heads or q.shape[3] != HEAD_DIM:
             raise ValueError("q must be [batch, num_q_heads, n, 128]")
+        batch, n = q.shape[0], q.shape[2]
         if tuple(k.shape) != (batch, self.num_kv_heads, n, HEAD_DIM) or k.shape != v.shape:
             raise ValueError("k, v must be [batch, num_kv_heads, n, 128]")
         if out is None:
             out = torch.empty_like(q)
-        _need(out, torch.bfloat16, "out")
+        _need(out, torch.bfloat16, "out", self.device, q.shape)
         ws = self.prefill_context_workspace(batch) if workspace is None else workspace
+        _need(ws, torch.uint8, "workspace", self.device)
         scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
         L.check(self.lib.kvc_prefill_context(self.handle, seq_begin, batch, n, ctypes.c_void_p(q.data_ptr()),
                                              ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()),
@@ -257,9 +271,9 @@ class KVCache:
         """The whole decode step of this layer in one library call (append one
         token, attention, selection, compaction); same results as `step`.
         mode "h2o", "streaming" or "block" (see `h2o_select_evict`)."""
-        _need(q, torch.bfloat16, "q")
-        _need(k_new, torch.bfloat16, "k_new")
-        _need(v_new, torch.bfloat16, "v_new")
+        _need(q, torch.bfloat16, "q", self.device)
+        _need(k_new, torch.bfloat16, "k_new", self.device)
+        _need(v_new, torch.bfloat16, "v_new", self.device)
         batch = q.shape[0]
         if q.dim() != 3 or q.shape[1] != self.num_q_heads or q.shape[2] != HEAD_DIM:
             raise ValueError("q must be [batch, num_q_heads, 128]")
@@ -267,8 +281,9 @@ class KVCache:
             raise ValueError("k_new, v_new must be [batch, num_kv_heads, 1, 128]")
         if out is None:
             out = torch.empty_like(q)
-        _need(out, torch.bfloat16, "out")
+        _need(out, torch.bfloat16, "out", self.device, q.shape)
         ws = self.workspace(batch) if workspace is None else workspace
+        _need(ws, torch.uint8, "workspace", self.device)
         scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
         m = {"h2o": L.KVC_EVICT_H2O, "streaming": L.KVC_EVICT_STREAMING, "block": L.KVC_EVICT_BLOCK}[mode]
         params = L.KvcEvictParams(m, budget, recent, window, retention)
