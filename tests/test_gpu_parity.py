@@ -442,3 +442,33 @@ def test_release_sequences():
         for x, y in zip(sa.head(1, h), sb.head(1, h)):
             assert np.array_equal(np.asarray(x).view(np.uint8), np.asarray(y).view(np.uint8))
     assert cache.read_status() == 0
+
+
+def test_binding_refuses_mis_sized_buffers():
+    """The binding refuses, before any launch, an output, keep mask or
+    workspace whose shape, dtype or device differs from what the call's sizes
+    imply, and inputs that are not on the cache's device; the cache is left
+    usable."""
+    from compressed_kv_cache_kvc_gb300.cache import KVCache
+    c = KVCache(8, 2, 8, 16, 2, 8)
+    bf = dict(dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros(2, 8, 128, **bf)
+    k = torch.zeros(2, 2, 1, 128, **bf)
+    c.quantize_append(k, k)
+    bad = [
+        lambda: c.decode_attention(q, out=torch.empty(1, 8, 128, **bf)),
+        lambda: c.decode_attention(q, workspace=torch.empty(1 << 20, dtype=torch.float32, device="cuda")),
+        lambda: c.decode_attention(q.cpu()),
+        lambda: c.decode_step(q, k, k, out=torch.empty(2, 8, 64, **bf)),
+        lambda: c.h2o_select_evict(2, budget=8, recent=2, keep_mask=torch.empty(2, 2, 8, dtype=torch.uint8,
+                                                                                  device="cuda")),
+        lambda: c.compact_blocks(torch.zeros(1, 2, c.s_cap, dtype=torch.uint8, device="cuda"), 2),
+        lambda: c.prefill_context(torch.zeros(2, 8, 3, 128, **bf), torch.zeros(2, 2, 3, 128, **bf),
+                                  torch.zeros(2, 2, 3, 128, **bf), out=torch.empty(2, 8, 2, 128, **bf)),
+    ]
+    for f in bad:
+        with pytest.raises(ValueError):
+            f()
+    assert c.lengths(0) == (0, 1) and c.lengths(1) == (0, 1)
+    out = c.decode_attention(q)
+    assert out.shape == q.shape and c.read_status() == 0
