@@ -25,6 +25,11 @@
 // probabilities with the forward's row statistics, and sums them over the
 // query rows; the column sums land in the tokens' score slots (sinks, pool
 // or bf16 window).
+//
+// A prompt over sequences that already hold context (kvc_prefill_context)
+// attends to the compressed cache instead: each of its queries runs through
+// the decode attention kernels, and ctx_step_kernel, between the passes,
+// sets the lengths that query may see and moves its input and output.
 #include <cuda_bf16.h>
 
 #include "kvc_device.h"
