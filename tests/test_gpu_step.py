@@ -265,3 +265,46 @@ def test_step_head_layouts_against_oracle(bits, hq, hkv):
             assert T.kept_sets_agree(set(st.head(b, h)[0].tolist()), set(hs.pos[masks[h]].tolist()), hs.pos,
                                      hs.score, budget - 4 - recent, nb + 1 - recent), (b, h)
     assert cache.read_status() == 0
+
+
+def test_checkpoint_to_host_and_resume_in_another_arena():
+    """Checkpoint/resume: after a few steps the state arena is copied to host
+    memory and restored into a second cache of the same geometry (another
+    device allocation), whose host mirror is then reloaded
+    (kvc_cache_sync_host).  The state holds block ids, never addresses, so
+    the next steps give the same outputs and the same logical state in both
+    caches."""
+    from compressed_kv_cache_kvc_gb300.cache import KVCache
+    rng = np.random.default_rng(77)
+    hq, hkv, bits, lengths, budget, recent = 16, 4, 4, [300, 170], 120, 24
+    B = len(lengths)
+    mbps = (max(lengths) + 4 + 15) // 16 + 2
+    ca = KVCache(hq, hkv, bits, B * mbps, B, mbps)
+    k = _bits(rng, (B, hkv, max(lengths), 128))
+    v = _bits(rng, (B, hkv, max(lengths), 128))
+    for b, n in enumerate(lengths):
+        ca.quantize_append(T.to_dev_bf16(np.ascontiguousarray(k[b:b + 1, :, :n])),
+                           T.to_dev_bf16(np.ascontiguousarray(v[b:b + 1, :, :n])), seq_begin=b)
+
+    def inputs():
+        return (T.to_dev_bf16(_bits(rng, (B, hq, 128))), T.to_dev_bf16(_bits(rng, (B, hkv, 1, 128))),
+                T.to_dev_bf16(_bits(rng, (B, hkv, 1, 128))))
+
+    for _ in range(2):
+        ca.decode_step(*inputs(), mode="h2o", budget=budget, recent=recent)
+    torch.cuda.synchronize()
+    checkpoint = ca.state_view.cpu()
+    cb = KVCache(hq, hkv, bits, B * mbps, B, mbps)
+    assert cb.state_view.data_ptr() != ca.state_view.data_ptr()
+    cb.state_view.copy_(checkpoint.to(cb.device))
+    cb.sync_host()
+    for b in range(B):
+        assert cb.lengths(b) == ca.lengths(b)
+    for _ in range(2):
+        q, kn, vn = inputs()
+        oa = ca.decode_step(q, kn, vn, mode="h2o", budget=budget, recent=recent)
+        ob = cb.decode_step(q, kn, vn, mode="h2o", budget=budget, recent=recent)
+        torch.cuda.synchronize()
+        assert torch.equal(oa, ob)
+        _same_state(ca, cb)
+    assert ca.read_status() == 0 and cb.read_status() == 0
