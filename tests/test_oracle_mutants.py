@@ -152,6 +152,27 @@ def _prefill_not_causal():
     return prefill_attention
 
 
+def _prefill_variant(first_head_scores_only=False, mask_offset=1):
+    def prefill_attention(q, k, v, sm_scale=None):
+        q, k, v = (np.asarray(a, np.float64) for a in (q, k, v))
+        hq, n, d = q.shape
+        g = hq // k.shape[0]
+        s = 1.0 / math.sqrt(d) if sm_scale is None else sm_scale
+        future = np.triu(np.ones((n, n), dtype=bool), mask_offset)
+        out = np.zeros((hq, n, d))
+        scores = np.zeros((k.shape[0], n))
+        for j in range(hq):
+            logits = (q[j] @ k[j // g].T) * s
+            logits[future] = -np.inf
+            e = np.exp(logits - logits.max(axis=-1, keepdims=True))
+            probs = e / e.sum(axis=-1, keepdims=True)
+            out[j] = probs @ v[j // g]
+            if not first_head_scores_only or j % g == 0:
+                scores[j // g] += probs.sum(axis=0)
+        return out, scores
+    return prefill_attention
+
+
 def _pack_swapped(codes):
     c = np.asarray(codes, dtype=np.int8).astype(np.uint8) & np.uint8(0x0F)
     return (c[..., 1::2] | (c[..., 0::2] << np.uint8(4))).astype(np.uint8)
@@ -276,6 +297,15 @@ MUTANTS = {
     "prompt over context adds no scores": [(O.OracleCache, "prefill_chunk", _chunk_without_scores)],
     "bf16 window one position too long": [(O.OracleCache, "attend", _attend_window_one_long)],
     "block keep masks drop the recent pages": [(O.OracleCache, "keep_masks", _block_masks_without_recent)],
+    "prefill scores from one query head of the group": [(O, "prefill_attention",
+                                                         lambda f: _prefill_variant(first_head_scores_only=True))],
+    "prefill mask lets a query see the next key": [(O, "prefill_attention", lambda f: _prefill_variant(mask_offset=2))],
+    "E4M3 saturates at 240": [(O, "e4m3_encode", lambda f: lambda y: f(np.clip(np.asarray(y, np.float32), -240, 240)))],
+    "H2O increment from the first query head only": [(O, "h2o_increments",
+                                                      lambda f: lambda p: np.asarray(p, np.float64)[0])],
+    "StreamingLLM keeps the oldest window": [(O, "select_streaming", lambda f: lambda pos, pt, w, ns=O.NUM_SINK:
+                                             np.argsort(np.argsort(np.asarray(pos))) < w
+                                             if np.asarray(pos).shape[0] > w else np.ones(len(pos), bool))],
 }
 
 
