@@ -218,9 +218,15 @@ size_t kvc_workspace_bytes(const kvc_cache* cache, int32_t batch);
  * [-8, 7]; a zero row has scale 0 and codes 0.  Tokens at positions 0..3 are
  * attention sinks: stored unchanged in bf16 and never quantised (Technical
  * Report 3.2).  New pages come from the device free-block stack; their score
- * starts at 0.  n_new == 0 is a no-op.
- * Errors: KVC_ERR_CAPACITY when a sequence would exceed max_blocks_per_seq
- * pages or the pool has too few free blocks (nothing is written). */
+ * starts at 0.  n_new == 0 is a no-op.  With KVC_CODES_E4M3 the scale is
+ * amax / 448 and the codes FP8 E4M3 (see "Code formats"); with a bf16 window
+ * the newest tokens go to the ring and the tokens they push out of it are
+ * quantised into the pool (see "Hybrid precision").  Appends of 64 tokens or
+ * more that push no window token out take two launches, others one.
+ * Errors: KVC_ERR_INVALID_ARG for a slice outside [0, max_batch), n_new < 0
+ * or a null or misaligned pointer; KVC_ERR_CAPACITY when a sequence would
+ * exceed max_blocks_per_seq pages or the pool has too few free blocks
+ * (nothing is written). */
 kvc_status kvc_quantize_append(kvc_cache* cache, int32_t seq_begin, int32_t batch, int32_t n_new,
                                const void* d_k, const void* d_v, void* stream);
 
@@ -234,7 +240,12 @@ kvc_status kvc_quantize_append(kvc_cache* cache, int32_t seq_begin, int32_t batc
  * With KVC_ATTN_ACCUM_H2O, every attended token's score (sinks included) grows
  * by the sum over the query heads of its KV head of its softmax probability.
  * Every sequence of the slice must hold at least one token.
- * d_workspace: kvc_workspace_bytes(cache, batch) bytes, 256-byte aligned. */
+ * d_workspace: kvc_workspace_bytes(cache, batch) bytes, 256-byte aligned.
+ * Errors: KVC_ERR_INVALID_ARG for a slice outside the cache, a null or
+ * misaligned pointer, sm_scale not positive and finite, unknown flags, a
+ * short workspace or an empty sequence; KVC_ERR_UNSUPPORTED for batch >
+ * 1024.  Two launches (split-K, merge with the scores), three with a bf16
+ * window; the split launch is skipped when no sequence holds a pool page. */
 kvc_status kvc_decode_attention(kvc_cache* cache, int32_t seq_begin, int32_t batch,
                                 const void* d_q, void* d_out, float sm_scale, int32_t flags,
                                 void* d_workspace, size_t workspace_bytes, void* stream);
@@ -250,7 +261,14 @@ kvc_status kvc_decode_attention(kvc_cache* cache, int32_t seq_begin, int32_t bat
  * The sinks are always kept and are not part of the mask.
  *   d_keep_mask: u8 [batch][Hkv][max_blocks_per_seq*16], entry t = 1 if pool
  *   slot t is kept (entries >= S are left unspecified).
- * Records the plan (S, kept slots) that kvc_compact_blocks applies. */
+ * Records the plan (S, kept slots) that kvc_compact_blocks applies.
+ * Errors: KVC_ERR_INVALID_ARG for a slice outside the cache, a null mask or
+ * params, an unknown mode, a budget below 4 + recent, a negative recent
+ * window, a StreamingLLM window below 1, a retention outside (0, 1], a bf16
+ * window not covered by the recent window (H2O) or the StreamingLLM window,
+ * or a short workspace;
+ * KVC_ERR_UNSUPPORTED for block mode with a bf16 window or more than 4096
+ * pages per sequence.  One launch (two in block mode). */
 kvc_status kvc_h2o_select_evict(kvc_cache* cache, int32_t seq_begin, int32_t batch,
                                 const kvc_evict_params* params, uint8_t* d_keep_mask,
                                 void* d_workspace, size_t workspace_bytes, void* stream);
