@@ -14,10 +14,15 @@
 // resolved by a second radix select on the positions (smallest first).  Keys
 // and positions sit in shared memory when they fit, else in the workspace.
 //
-// Compaction: with n' kept slots, the evicted slots below n' ("holes") are
-// filled in ascending order by the kept slots at or above n' (ascending).
-// Sources all lie at or above n' and destinations below it, so the moves never
-// overlap.  The pages past ceil(n'/16) go back to the free-block stack.
+// Compaction into a keep window: with S slots and n' < S kept, the kept slots
+// end up in [w, w + n'), w = 16 * floor((S - n') / 16), the last page-aligned
+// window of n' slots.  The evicted slots inside the window ("holes") are
+// filled in ascending order by the kept slots outside it ("sources",
+// ascending); a hole and a source are never the same slot, so the moves never
+// overlap.  The w / 16 pages before the window go back to the free-block
+// stack and the block-table row drops them.  After a long context the always
+// kept recent tokens already sit inside the window and do not move; at steady
+// state (one slot evicted) w = 0 and at most one row moves.
 #include <algorithm>
 
 #include "kvc_device.h"

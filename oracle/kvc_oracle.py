@@ -50,8 +50,8 @@ What it computes, step by step, each citing the page passage it restates:
   older ones at INT4/INT8): the tokens at the last W positions attend with
   their unquantised bf16 values, older ones with their codes.
 
-Readings where the pages are silent or disagree are listed in the design doc; the
-ones that change arithmetic are restated beside the function they affect.
+Where the pages are silent or disagree, the reading taken is restated beside
+the function whose arithmetic it affects.
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (closed forms, worked examples with exact scales, library witnesses, invariants,
@@ -144,7 +144,8 @@ def quantize_rows(x: np.ndarray, bits: int) -> tuple[np.ndarray, np.ndarray]:
     Steps, in the order of "KV Cache optimization techniques" section 1.2:
       1. amax = max |x| over the row (exact in fp32);
       2. scale = amax / qmax, one IEEE fp32 division (no epsilon: the
-         Technical Report's quantize_kv adds none; see DESIGN.md);
+         Technical Report's quantize_kv adds none, and the techniques page's
+         +1e-8 would change the codes of tiny rows);
       3. code = round-half-to-even(x / scale) with an IEEE fp32 division,
          then clamp to ``code_range(bits)``.
     A row whose amax is 0 has scale 0 and all codes 0 (0/0 is avoided).

@@ -28,6 +28,22 @@ FULL = [
 ]
 
 
+def _same_logical_state(a, b):
+    """Two caches hold the same logical state: per (sequence, KV head) the
+    slots in slot order (positions, codes, scales, scores) bit for bit, the
+    sinks and their scores, the lengths and the free-block count."""
+    sa, sb = T.StateView(a), T.StateView(b)
+    assert np.array_equal(sa.slots, sb.slots) and np.array_equal(sa.seen, sb.seen)
+    for seq in range(a.max_batch):
+        for h in range(a.num_kv_heads):
+            for x, y in zip(sa.head(seq, h), sb.head(seq, h)):
+                assert np.array_equal(np.asarray(x).view(np.uint8), np.asarray(y).view(np.uint8)), (seq, h)
+    assert np.array_equal(sa.sink_k, sb.sink_k) and np.array_equal(sa.sink_v, sb.sink_v)
+    assert np.array_equal(sa.sink_score.view(np.uint32), sb.sink_score.view(np.uint32))
+    assert sa.counters[0] == sb.counters[0]
+    return sb
+
+
 @pytest.fixture(scope="module", autouse=True)
 def _lib():
     if not torch.cuda.is_available():
@@ -38,6 +54,34 @@ def _lib():
 
 @pytest.mark.parametrize("name,steps", FULL)
 def test_full_size_sampled(name, steps):
+    _full_size(name, steps, with_step=False)
+
+
+# The one-call step at the shapes the bench times: 256 (Qwen-shaped INT4) and
+# 512 (LLaMA-shaped INT8) (sequence, KV head) pairs, more than the SMs, so the
+# library runs the 512-thread post kernel beside the split and move kernels;
+# the 32k-context stack has 32 pairs (the 1024-thread post kernel).
+STEP_FULL = [
+    ("qwen14b_b32_gqa5_t8192_int4_h2o_48l", 2),
+    ("llama7b_b16_h32_t4096_int8_h2o", 2),
+    ("longctx_b4_gqa4_t32768_int8_h2o_32l_64s", 3),
+]
+
+
+@pytest.mark.parametrize("name,steps", STEP_FULL)
+def test_full_size_decode_step(name, steps):
+    """The benchmarked path itself: kvc_decode_step on a full-size layer,
+    step after step.  A second cache runs the separate calls on the same
+    inputs and gets every check of the sampled test (oracle outputs, codes,
+    scores and kept sets on sampled sequences; on every pair the kept set the
+    oracle's rule gives on the GPU's own scores, the score-sum invariant,
+    block conservation); the one-call step must give the same outputs bit for
+    bit and the same logical state after every step, so every check carries
+    over to it.  Its own outputs are also checked against the oracle."""
+    _full_size(name, steps, with_step=True)
+
+
+def _full_size(name, steps, with_step):
     from compressed_kv_cache_kvc_gb300 import workloads as W
     from compressed_kv_cache_kvc_gb300.cache import KVCache
     w = W.WORKLOADS[name]
@@ -48,12 +92,17 @@ def test_full_size_sampled(name, steps):
     nb = B * mbps
     order = W.block_order(w, nb) if w.shuffled_blocks else None
     cache = KVCache(hq, hkv, w.bits, nb, B, mbps, block_order=order)
-    if np.all(lengths == lengths[0]):
-        cache.quantize_append(T.to_dev_bf16(d["k"]), T.to_dev_bf16(d["v"]))
-    else:
-        for b in range(B):
-            n = int(lengths[b])
-            cache.quantize_append(T.to_dev_bf16(np.ascontiguousarray(d["k"][b:b + 1, :, :n])),
+    caches = [cache]
+    if with_step:
+        stepper = KVCache(hq, hkv, w.bits, nb, B, mbps, block_order=order)
+        caches.append(stepper)
+    for c in caches:
+        if np.all(lengths == lengths[0]):
+            c.quantize_append(T.to_dev_bf16(d["k"]), T.to_dev_bf16(d["v"]))
+        else:
+            for b in range(B):
+                n = int(lengths[b])
+                c.quantize_append(T.to_dev_bf16(np.ascontiguousarray(d["k"][b:b + 1, :, :n])),
                                   T.to_dev_bf16(np.ascontiguousarray(d["v"][b:b + 1, :, :n])), seq_begin=b)
     rng = np.random.default_rng(99)
     sample = sorted(rng.choice(B, size=min(2, B), replace=False).tolist())
@@ -68,6 +117,10 @@ def test_full_size_sampled(name, steps):
     prev_sum = np.zeros((B, hkv))
     for step in range(steps):
         s = d if step == 0 else W.gen_step(w, 0, step)
+        if with_step:
+            sout = stepper.decode_step(T.to_dev_bf16(s["q"]), T.to_dev_bf16(s["k_new"]), T.to_dev_bf16(s["v_new"]),
+                                       mode=w.mode, budget=w.budget, recent=w.recent, window=w.window)
+            assert stepper.last_launch_count() == 4
         cache.quantize_append(T.to_dev_bf16(s["k_new"]), T.to_dev_bf16(s["v_new"]))
         out = cache.decode_attention(T.to_dev_bf16(s["q"]), accumulate_h2o=h2o)
         gpu = T.bf16_tensor_to_f32(out)
@@ -98,11 +151,19 @@ def test_full_size_sampled(name, steps):
                 assert np.array_equal(np.sort(ppos), np.sort(pos[kept])), (step, b, h)
                 prev_sum[b, h] = float(post.head(b, h)[5].astype(np.float64).sum() +
                                        post.sink_score[b, h, :min(P, 4)].sum())
+        if with_step:
+            torch.cuda.synchronize()
+            assert torch.equal(sout, out), f"{name} step {step}: one-call step output differs"
+            _same_logical_state(cache, stepper)
+            for b in range(B):
+                assert stepper.lengths(b) == cache.lengths(b)
         for b in sample:
             ora = oras[b]
             ora.append(0, O.bf16_bits_to_f32(s["k_new"][b]), O.bf16_bits_to_f32(s["v_new"][b]))
             ref = ora.attend(0, O.bf16_bits_to_f32(s["q"][b]), T.sm_scale(), accumulate=h2o)
             T.assert_attention_close(gpu[b], ref, f"{name} step {step} b={b}")
+            if with_step:
+                T.assert_attention_close(T.bf16_tensor_to_f32(sout)[b], ref, f"{name} one-call step {step} b={b}")
             for h in range(hkv):
                 # codes/scales/positions of the sampled sequence, bit for bit
                 sv = _single(pre, b)
@@ -123,6 +184,8 @@ def test_full_size_sampled(name, steps):
         allb = np.concatenate([used, free])
         assert allb.size == nb and np.unique(allb).size == nb
         assert cache.read_status() == 0
+    if with_step:
+        assert stepper.read_status() == 0
 
 
 class _single:

@@ -127,7 +127,8 @@ def test_quant_zero_row():
 @pytest.mark.parametrize("bits", [8, 4])
 def test_quant_torch_witness(bits):
     # Library witness: the page's per-token quantiser written with torch ops in
-    # fp32 (without the 1e-8 epsilon).
+    # fp32, without the techniques page's 1e-8 epsilon (the Technical Report's
+    # quantize_kv has none).
     rng = np.random.default_rng(2)
     x = rng.standard_normal((300, 128)).astype(np.float32)
     x[:, 7] *= 10
