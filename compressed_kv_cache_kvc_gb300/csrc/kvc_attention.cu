@@ -15,16 +15,26 @@
 //     (which may span a pair boundary: one partial per pair touched).  Inside
 //     a CTA the 4 warps take the run's pages round-robin.
 //   * Each warp streams its pages through a private ring of shared-memory
-//     stages with cp.async (16-byte, coalesced: a K or V page of one head is
-//     one contiguous 2 KB (INT8) / 1 KB (INT4) run of the pool).
-//   * Codes are exact small integers, so they are converted to fp16 exactly
-//     (byte-permute + magic-number subtraction, the integer-to-float trick of
-//     Kim et al., "Who Says Elephants Can't Run", 2022) and fed straight from
-//     registers to mma.sync m16n8k16 (fp16 in, fp32 accumulate).  QK^T puts the
-//     16 tokens of a page on M and the G <= 8 query heads on N; PV puts 16
+//     stages with cp.async: a K or V page of one head is one contiguous
+//     2 KB (8-bit) / 1 KB (INT4) run of the pool, copied by the 32 lanes in
+//     512-byte instructions; rows 8..15 land 64 bytes after rows 0..7, which
+//     puts the rows the lanes read together on all 32 banks.  The block ids
+//     of a warp's pages are held 32 at a time across its lanes.
+//   * Integer codes enter the tensor cores without an arithmetic conversion:
+//     one logic instruction per register moves two codes, offset to unsigned
+//     (INT8 c + 128, INT4 c + 8), into the mantissa of two fp16 subnormals,
+//     which are exactly (c + offset) * 2^-24; mma.sync m16n8k16 (fp16 in,
+//     fp32 accumulate) then sums exact products.  The offset comes back out
+//     once per dot product for K (offset * sum of the query) and once per
+//     output for V (offset * sum of the PV operand, which one more MMA with
+//     an all-ones A operand accumulates alongside O).  FP8 E4M3 codes are
+//     converted by cvt.rn.f16x2.e4m3x2 (exact, no offset).  QK^T puts the 16
+//     tokens of a page on M and the G <= 8 query heads on N; PV puts 16
 //     head-dim rows on M and the query heads on N, with P transposed in
 //     registers by movmatrix.  The head-dim order inside a lane is permuted
 //     consistently for Q and K (a dot product does not depend on it).
+//   * Pages whose 16 slots are all valid (all but a sequence's last) take a
+//     path without per-slot masks.
 //   * The per-token scales stay out of the inner products: logit =
 //     (q' . c) * scale_k * (sm_scale * log2 e * 2^-e_q), and the PV operand is
 //     p * scale_v * 2^-E.  q' = q * 2^e_q and the warp-wide power of two 2^-E
@@ -39,6 +49,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "kvc_device.h"
 #include "kvc_internal.h"
 
@@ -48,66 +60,74 @@ namespace {
 using namespace dev;
 
 constexpr int kWarps = 4;
+constexpr int kPagesPerIter = 1;     // pages of a warp processed together in the split kernel
 constexpr float kLazy = 4.0f;        // log2 units the running max may lag
 constexpr int kMergeBtStage = 2048;  // block-table entries staged in shared memory (32768 slots)
 constexpr int kMergeThreads = 512;
 
+// One stage of a warp's ring holds one head-page: its K and V code rows and
+// its 16 K and 16 V scales (a head-page is a contiguous run of 16 rows in the
+// pool).  Rows 8..15 of K and of V sit 64 bytes after rows 0..7, so the row
+// groups the lanes read in one instruction fall on all 32 shared-memory banks.
 template <int BITS>
 struct Geom {
-  static constexpr int kRowBytes = BITS * 16;           // 128 (INT8) or 64 (INT4)
-  static constexpr int kKBytes = BITS == 8 ? 2048 : 1024;
-  static constexpr int kVBytes = BITS == 8 ? 2048 : 1024;
-  static constexpr int kStage = kKBytes + kVBytes + 128;  // + 16 K scales + 16 V scales
-  static constexpr int kStages = 4;  // INT8: 3 CTAs/SM by shared memory, INT4: 4
+  static constexpr int kRowBytes = BITS * 16;            // 128 (8-bit codes) or 64 (INT4)
+  static constexpr int kHalf = 8 * kRowBytes;            // rows 0..7 of a head-page
+  static constexpr int kK = 0;                           // K rows 0..7 | 64 | K rows 8..15
+  static constexpr int kV = 2 * kHalf + 64;              // V rows 0..7 | 64 | V rows 8..15
+  static constexpr int kKS = 2 * (2 * kHalf + 64);       // 16 fp32 K scales
+  static constexpr int kVS = kKS + 64;                   // 16 fp32 V scales
+  static constexpr int kStage = kVS + 64;
+  static constexpr int kStages = 4;
   static constexpr int kSmem = kWarps * kStages * kStage;
+  // offset of code row t within its K or V block of a stage
+  static __host__ __device__ constexpr int row_off(int t) { return t * kRowBytes + (t >= 8 ? 64 : 0); }
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-__device__ __forceinline__ void cp_async16_s(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src));
-}
-// All code chunks of one page for this lane (see the lane offsets in the
-// split kernel): K then V, at fixed immediate distances from the lane bases.
-template <int BITS>
-__device__ __forceinline__ void copy_page(uint32_t sK, const uint8_t* kg, uint32_t sV, const uint8_t* vg) {
-  if (BITS == 8) {
-    asm volatile(
-        "cp.async.cg.shared.global [%0], [%1], 16;\n"
-        "cp.async.cg.shared.global [%0+512], [%1+64], 16;\n"
-        "cp.async.cg.shared.global [%0+1024], [%1+128], 16;\n"
-        "cp.async.cg.shared.global [%0+1536], [%1+192], 16;\n"
-        "cp.async.cg.shared.global [%2], [%3], 16;\n"
-        "cp.async.cg.shared.global [%2+512], [%3+128], 16;\n"
-        "cp.async.cg.shared.global [%2+1024], [%3+256], 16;\n"
-        "cp.async.cg.shared.global [%2+1536], [%3+384], 16;\n" ::"r"(sK), "l"(kg), "r"(sV), "l"(vg));
-  } else {
-    asm volatile(
-        "cp.async.cg.shared.global [%0], [%1], 16;\n"
-        "cp.async.cg.shared.global [%0+512], [%1+64], 16;\n"
-        "cp.async.ca.shared.global [%2], [%3], 8;\n"
-        "cp.async.ca.shared.global [%2+256], [%3+64], 8;\n"
-        "cp.async.ca.shared.global [%2+512], [%3+128], 8;\n"
-        "cp.async.ca.shared.global [%2+768], [%3+192], 8;\n" ::"r"(sK), "l"(kg), "r"(sV), "l"(vg));
-  }
-}
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
+// The code rows of one page of one head into a stage: lane L copies the
+// 16-byte chunks L + 32 i of the K run and of the V run (every instruction
+// reads 512 contiguous bytes), to their place in the stage (rows 8..15 64
+// bytes further).  The offsets are immediates from the two lane bases.
+template <int BITS>
+__device__ __forceinline__ void copy_codes(uint32_t sK, const uint8_t* gK, uint32_t sV, const uint8_t* gV) {
+  if (BITS == 8) {
+    asm volatile(
+        "cp.async.cg.shared.global [%0], [%1], 16;\n"
+        "cp.async.cg.shared.global [%0+512], [%1+512], 16;\n"
+        "cp.async.cg.shared.global [%0+1088], [%1+1024], 16;\n"
+        "cp.async.cg.shared.global [%0+1600], [%1+1536], 16;\n"
+        "cp.async.cg.shared.global [%2], [%3], 16;\n"
+        "cp.async.cg.shared.global [%2+512], [%3+512], 16;\n"
+        "cp.async.cg.shared.global [%2+1088], [%3+1024], 16;\n"
+        "cp.async.cg.shared.global [%2+1600], [%3+1536], 16;\n" ::"r"(sK), "l"(gK), "r"(sV), "l"(gV));
+  } else {
+    asm volatile(
+        "cp.async.cg.shared.global [%0], [%1], 16;\n"
+        "cp.async.cg.shared.global [%0+576], [%1+512], 16;\n"
+        "cp.async.cg.shared.global [%2], [%3], 16;\n"
+        "cp.async.cg.shared.global [%2+576], [%3+512], 16;\n" ::"r"(sK), "l"(gK), "r"(sV), "l"(gV));
+  }
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src));
+}
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) { return __byte_perm(a, b, sel); }
-__device__ __forceinline__ uint32_t as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
-__device__ __forceinline__ __half2 as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
-__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) { return as_u32(__hsub2(as_h2(a), as_h2(b))); }
-__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
-  return as_u32(__hfma2(as_h2(a), as_h2(b), as_h2(c)));
-}
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ float2 unpack_half2(uint32_t u) {
+  return __half22float2(*reinterpret_cast<__half2*>(&u));
 }
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
   uint32_t d;
@@ -123,15 +143,26 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// 4 INT8 codes (bytes b0..b3 of w, already XOR 0x80) -> fp16x2 (b0, b1) and (b2, b3).
-__device__ __forceinline__ void i8x4_to_h2(uint32_t wx, uint32_t& lo, uint32_t& hi) {
-  lo = hsub2(prmt(wx, 0x64646464u, 0x4140u), 0x64806480u);
-  hi = hsub2(prmt(wx, 0x64646464u, 0x4342u), 0x64806480u);
+// Integer codes enter the MMA as fp16 subnormals: a field of u < 1024 in the
+// low mantissa bits of an fp16 (exponent bits zero) is exactly u * 2^-24.
+// The codes are offset to unsigned first (INT8: c + 128, INT4: c + 8, by
+// flipping the field's top bit), so every product and partial sum is exact
+// or rounded as an fp16 x fp16 -> fp32 MMA rounds it; the offsets come back
+// out once per dot product (K) or once per output (V), see the kernel.
+// INT8: bytes 0 and 2 of w -> (b0 + 128, b2 + 128) * 2^-24.
+// One logic instruction each: (w & mask) ^ flip, written as lop3 so that the
+// mask and the flip are not split into two.
+__device__ __forceinline__ uint32_t and_xor(uint32_t w, uint32_t mask, uint32_t flip) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(w), "r"(mask), "r"(flip));
+  return d;
 }
-// Byte k of x and byte k of y (INT8 codes) -> fp16x2 (x_k, y_k).
-__device__ __forceinline__ uint32_t i8_pair_to_h2(uint32_t x, uint32_t y, uint32_t sel) {
-  return hsub2((prmt(x, y, sel) & 0x00FF00FFu) ^ 0x64806480u, 0x64806480u);
-}
+__device__ __forceinline__ uint32_t u8_even(uint32_t w) { return and_xor(w, 0x00FF00FFu, 0x00800080u); }
+// INT4: the low nibble of each 16-bit half -> (n + 8) * 2^-24.
+__device__ __forceinline__ uint32_t u4_lo(uint32_t w) { return and_xor(w, 0x000F000Fu, 0x00080008u); }
+// INT4: bits 4..7 of each 16-bit half -> 16 (n + 8) * 2^-24.
+__device__ __forceinline__ uint32_t u4_hi(uint32_t w) { return and_xor(w, 0x00F000F0u, 0x00800080u); }
+
 // FP8 E4M3 codes -> fp16 (every E4M3 value is exact in fp16), by the
 // conversion instruction: 4 codes (bytes b0..b3 of w) -> (b0, b1) and (b2, b3).
 __device__ __forceinline__ void e4m3x4_to_h2(uint32_t w, uint32_t& lo, uint32_t& hi) {
@@ -153,15 +184,6 @@ __device__ __forceinline__ uint32_t e4m3_pair_to_h2(uint32_t x, uint32_t y, int 
       : "r"(pr));
   return d;
 }
-// Low nibbles of the two 16-bit halves (INT4 codes) -> fp16x2.
-__device__ __forceinline__ uint32_t i4_lo_to_h2(uint32_t v) {
-  return hsub2((v & 0x000F000Fu) ^ 0x64086408u, 0x64086408u);
-}
-// Bits 4..7 of the two 16-bit halves (INT4 codes) -> fp16x2.
-__device__ __forceinline__ uint32_t i4_hi_to_h2(uint32_t v) {
-  return hfma2((v & 0x00F000F0u) ^ 0x64806480u, 0x2C002C00u /* 1/16 */, 0xD480D480u /* -72 */);
-}
-
 
 // 2^e as a float, for -126 <= e <= 127 (exact).
 __device__ __forceinline__ float pow2i(int e) { return __int_as_float((e + 127) << 23); }
@@ -172,7 +194,7 @@ __device__ __forceinline__ int exponent_of(float x) {
 }
 
 // FP8: the 8-bit codes are FP8 E4M3 instead of INT8 (same layout, same
-// scales; only the code -> fp16 conversion differs).
+// scales; only the code -> fp16 conversion differs, and no offset).
 template <int BITS, bool FP8 = false>
 __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int seq_begin, int batch,
                                                                  const uint16_t* __restrict__ q,
@@ -181,7 +203,16 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
   using Gm = Geom<BITS>;
   constexpr int STAGES = Gm::kStages;
   constexpr int RB = Gm::kRowBytes;
+  static_assert((STAGES & (STAGES - 1)) == 0, "ring positions are page index & (STAGES - 1)");
+  constexpr bool kOffset = !FP8;  // integer codes as offset subnormals
+  // the code offset times 2^-24 (K: subtracted from each dot product in units
+  // of the query's sum) and the scale that brings the subnormal sums back
+  constexpr float kOffK = BITS == 8 ? 128.0f * 0x1p-24f : 8.0f * 0x1p-24f;
+  constexpr float kOffV = BITS == 8 ? 128.0f : 8.0f;
   __shared__ int cum[kMaxCallBatch + 1];
+
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
   pages_prefix(s, seq_begin, batch, cum);
   if (blockIdx.x == 0) {
     // the page prefix and zeroed tickets for the kernel that follows the split
@@ -193,8 +224,6 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
 
   const int G = s.group;
   const int hkv = s.hkv;
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
   const int r = lane >> 2;
   const int c = lane & 3;
   const long long T = (long long)hkv * cum[batch];
@@ -203,21 +232,23 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
   long long F = (long long)cta * T / N;
   const long long F1 = (long long)(cta + 1) * T / N;
 
-  extern __shared__ __align__(16) uint8_t smem[];
-  uint8_t* ring = smem + warp * STAGES * Gm::kStage;
-
-  // per-lane byte offsets of the chunks this lane copies: within a head-page
-  // (global) and within a stage (shared); the chunks of one page sit at fixed
-  // distances from these, so one asm block copies a page with immediates
+  extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t ring_s = smem_u32(smem) + warp * STAGES * Gm::kStage;
-  // INT8: bytes 16c and 64 + 16c of rows 2r and 2r+1, so the 4 lanes of a
-  // row read whole 32-byte sectors in each copy instruction
-  const uint32_t k_goff = BITS == 8 ? (2 * r) * 128 + 16 * c : (2 * r) * 64 + 16 * c;
-  const uint32_t v_goff = BITS == 8 ? (4 * c) * 128 + 16 * r : (4 * c) * 64 + 8 * r;
-  const uint32_t k_soff = lane * 16;
-  const uint32_t v_soff = Gm::kKBytes + (BITS == 8 ? lane * 16 : lane * 8);
-  const uint32_t sc_soff = Gm::kKBytes + Gm::kVBytes + 16 * lane;
+  const uint8_t* ring = smem + warp * STAGES * Gm::kStage;
+
+  // what this lane copies of a page: chunks lane + 32 i of the K and V runs,
+  // and (lanes 0..7) one 16-byte chunk of the 16 K or 16 V scales
+  const uint32_t k_soff = Gm::kK + 16 * lane;
+  const uint32_t v_soff = Gm::kV + 16 * lane;
+  const uint32_t sc_soff = Gm::kKS + 16 * lane;  // K scales, then V scales (kVS = kKS + 64)
   const float* sc_gbase = (lane < 4 ? s.k_scale : s.v_scale) + 4 * (lane & 3);
+  // what this lane reads of a stage: K rows 2r and 2r+1 from byte 16c (INT8
+  // also from 64 + 16c), V rows 4c..4c+3 from byte 8r (INT4) or 16r, the
+  // scales of slots 2r and 2r+1
+  const int k_off = Gm::row_off(2 * r) + 16 * c;
+  const int v_off = Gm::kV + Gm::row_off(4 * c) + (BITS == 8 ? 16 * r : 8 * r);
+  const int s_off = Gm::kKS + 8 * r;
+
 
   while (F < F1) {
     // ---- the (sequence, KV head) pair of page F and this CTA's run of its pages
@@ -237,14 +268,58 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
     const int S = s.seq_slots[b];
     const int pair = bl * hkv + h;
 
-    // ---- query fragments (B operand of QK^T), scaled by 2^e_g into fp16 range
+    // ---- page pipeline: this warp takes pages pg_a + warp, + kWarps, ...
+    const int n_range = pg_e - pg_a;
+    const int n_my = n_range > warp ? (n_range - warp + kWarps - 1) / kWarps : 0;
+    const int32_t* bt = s.block_table + (size_t)b * s.max_bps;
+    // block ids of this warp's pages, 32 at a time across the lanes (the
+    // next 32 loaded while the current ones are used)
+    auto bt_load = [&](int chunk) -> int {
+      const int kk = chunk * 32 + lane;
+      return kk < n_my ? bt[pg_a + warp + kWarps * kk] : -1;
+    };
+    int bt_cur = bt_load(0);
+    int bt_nxt = n_my > 32 ? bt_load(1) : -1;
+    uint32_t stage_ok = 0;  // bit k: the page in stage k has a valid block id
+
+    auto issue = [&](int k) {
+      if (k < n_my) {
+        if ((k & 31) == 0 && k > 0) {
+          bt_cur = bt_nxt;
+          bt_nxt = bt_load((k >> 5) + 1);
+        }
+        const int blk = __shfl_sync(0xffffffffu, bt_cur, k & 31);
+        const bool ok = (unsigned)blk < (unsigned)s.num_blocks;
+        const int slot_issue = k & (STAGES - 1);
+        stage_ok = ok ? (stage_ok | (1u << slot_issue)) : (stage_ok & ~(1u << slot_issue));
+        if (ok) {
+          const uint32_t sb = ring_s + slot_issue * Gm::kStage;
+          const size_t hp = (size_t)blk * hkv + h;
+          copy_codes<BITS>(sb + k_soff, s.k_codes + hp * (16 * RB) + 16 * lane, sb + v_soff,
+                           s.v_codes + hp * (16 * RB) + 16 * lane);
+          if (lane < 8) cp_async16(sb + sc_soff, sc_gbase + hp * kPage);
+        }
+      }
+      cp_async_commit();
+    };
+
+    // pages [0, nxt) are issued, one commit group each (empty past n_my)
+    int nxt = 0;
+    auto issue_upto = [&](int n) {
+#pragma unroll 1
+      for (; nxt < n; ++nxt) issue(nxt);
+    };
+    issue_upto(STAGES - 1);
+
+    // ---- query fragments (B operand of QK^T), scaled by 2^e_g into fp16 range;
+    // with offset codes, the sum of each head's query values as the MMA sees them
     uint32_t bq[8][2];
-    float cq0, cq1;
+    float cq0, cq1, ch0 = 0.0f, ch1 = 0.0f;
     {
       float qv[32];
       const int g = r;
       if (g < G) {
-        // the lane's 32 dims, in the order of its K codes: INT8 dims
+        // the lane's 32 dims, in the order of its K codes: 8-bit dims
         // 16c..16c+15 and 64+16c..64+16c+15, INT4 dims 32c..32c+31
         const uint16_t* qrow = q + ((size_t)bl * s.hq + h * G + g) * kHeadDim;
         const uint4* src_a = reinterpret_cast<const uint4*>(qrow + (BITS == 8 ? 16 * c : 32 * c));
@@ -273,54 +348,57 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
       const float f2e = pow2i(e);  // multiplying by a power of two is exact here
 #pragma unroll
       for (int i = 0; i < 32; ++i) qv[i] *= f2e;
+      // the B fragment pairs each A register's two codes: 8-bit offset codes
+      // give (b0, b2) and (b1, b3) of a word, E4M3 (b0, b1) and (b2, b3); INT4
+      // gives the low nibbles of bytes 0 and 2, then their high nibbles (16x:
+      // the query's matching values are divided by 16, exactly)
       if (BITS == 8) {
 #pragma unroll
         for (int st = 0; st < 8; ++st) {
-          bq[st][0] = pack_half2(qv[4 * st + 0], qv[4 * st + 1]);
-          bq[st][1] = pack_half2(qv[4 * st + 2], qv[4 * st + 3]);
+          if (FP8) {
+            bq[st][0] = pack_half2(qv[4 * st + 0], qv[4 * st + 1]);
+            bq[st][1] = pack_half2(qv[4 * st + 2], qv[4 * st + 3]);
+          } else {
+            bq[st][0] = pack_half2(qv[4 * st + 0], qv[4 * st + 2]);
+            bq[st][1] = pack_half2(qv[4 * st + 1], qv[4 * st + 3]);
+          }
         }
       } else {
+        constexpr float k16 = 0.0625f;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           bq[2 * i][0] = pack_half2(qv[8 * i + 0], qv[8 * i + 4]);
-          bq[2 * i][1] = pack_half2(qv[8 * i + 1], qv[8 * i + 5]);
+          bq[2 * i][1] = pack_half2(qv[8 * i + 1] * k16, qv[8 * i + 5] * k16);
           bq[2 * i + 1][0] = pack_half2(qv[8 * i + 2], qv[8 * i + 6]);
-          bq[2 * i + 1][1] = pack_half2(qv[8 * i + 3], qv[8 * i + 7]);
+          bq[2 * i + 1][1] = pack_half2(qv[8 * i + 3] * k16, qv[8 * i + 7] * k16);
         }
+      }
+      if (kOffset) {
+        // sum of q' over the head's 128 dims, from the fp16 values fed to the MMA
+        float qs = 0.0f;
+#pragma unroll
+        for (int st = 0; st < 8; ++st) {
+          const float2 a = unpack_half2(bq[st][0]);
+          const float2 bb = unpack_half2(bq[st][1]);
+          const float fb = BITS == 4 ? 16.0f : 1.0f;
+          qs += (a.x + a.y) + fb * (bb.x + bb.y);
+        }
+        qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+        qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+        ch0 = kOffK * __shfl_sync(0xffffffffu, qs, (2 * c) * 4);
+        ch1 = kOffK * __shfl_sync(0xffffffffu, qs, (2 * c + 1) * 4);
       }
       const int e0 = __shfl_sync(0xffffffffu, e, (2 * c) * 4);
       const int e1 = __shfl_sync(0xffffffffu, e, (2 * c + 1) * 4);
-      cq0 = qk_scale_log2 * pow2i(-e0);
-      cq1 = qk_scale_log2 * pow2i(-e1);
+      // offset codes carry 2^-24: scale the dot products back by 2^24
+      cq0 = qk_scale_log2 * pow2i((kOffset ? 24 : 0) - e0);
+      cq1 = qk_scale_log2 * pow2i((kOffset ? 24 : 0) - e1);
     }
-
-    // ---- page pipeline: this warp takes pages pg_a + warp, + kWarps, ...
-    const int n_range = pg_e - pg_a;
-    const int n_my = n_range > warp ? (n_range - warp + kWarps - 1) / kWarps : 0;
-    const int32_t* bt = s.block_table + (size_t)b * s.max_bps;
-    uint32_t stage_ok = 0;  // bit k: the page in stage k has a valid block id
-    int st_issue = 0;
-
-    auto issue = [&](int k) {
-      if (k < n_my) {
-        const int page = pg_a + warp + kWarps * k;
-        const int blk = bt[page];
-        const bool ok = (unsigned)blk < (unsigned)s.num_blocks;
-        stage_ok = ok ? (stage_ok | (1u << st_issue)) : (stage_ok & ~(1u << st_issue));
-        if (ok) {
-          const uint32_t sb = ring_s + st_issue * Gm::kStage;
-          const size_t hp = ((size_t)blk * hkv + h) * kPage;
-          copy_page<BITS>(sb + k_soff, s.k_codes + hp * RB + k_goff, sb + v_soff, s.v_codes + hp * RB + v_goff);
-          if (lane < 8) cp_async16_s(sb + sc_soff, sc_gbase + hp);
-        }
-      }
-      cp_async_commit();
-      st_issue = st_issue + 1 == STAGES ? 0 : st_issue + 1;
-    };
 
     float oacc[8][4];
 #pragma unroll
     for (int j = 0; j < 8; ++j) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.0f;
+    float osum[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // offset codes: sum over slots of the PV operand
     float m0 = kNegBig, m1 = kNegBig, l0 = 0.0f, l1 = 0.0f;
     int E = 0;
     bool e_set = false;
@@ -330,75 +408,105 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
     float* lg0p = spill && 2 * c < G ? w.logits + ((size_t)pair * G + 2 * c) * w.s_cap + 2 * r : nullptr;
     float* lg1p = spill && 2 * c + 1 < G ? w.logits + ((size_t)pair * G + 2 * c + 1) * w.s_cap + 2 * r : nullptr;
 
-#pragma unroll 1
-    for (int k = 0; k < STAGES - 1; ++k) issue(k);
-
-    int st_comp = 0;
-#pragma unroll 1
-    for (int k = 0; k < n_my; ++k) {
-      issue(k + STAGES - 1);
-      cp_async_wait<STAGES - 1>();
-      __syncwarp();
-      const uint8_t* st = ring + st_comp * Gm::kStage;
-      const int page = pg_a + warp + kWarps * k;
-      const bool blk_ok = (stage_ok >> st_comp) & 1u;
-      if (!blk_ok && lane == 0) atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
-      const int slot0 = page * kPage;
-      const bool v0 = blk_ok && (slot0 + 2 * r < S);
-      const bool v1 = blk_ok && (slot0 + 2 * r + 1 < S);
-      const float2 skv = *reinterpret_cast<const float2*>(st + Gm::kKBytes + Gm::kVBytes + 8 * r);
-      const float2 svv = *reinterpret_cast<const float2*>(st + Gm::kKBytes + Gm::kVBytes + 64 + 8 * r);
+    // NP consecutive pages of this warp (k .. k + NP - 1), their instructions
+    // interleaved; FULL: every slot valid (the common case), no per-slot masks
+    auto pages_body = [&](auto np_tag, auto full_tag, int k) {
+      constexpr int NP = decltype(np_tag)::value;
+      constexpr bool FULL = decltype(full_tag)::value;
+      const uint8_t* st[NP];
+      int slot0[NP];
+      bool v0[NP], v1[NP];
+      float2 skv[NP], svv[NP];
+#pragma unroll
+      for (int pp = 0; pp < NP; ++pp) {
+        const int sc = (k + pp) & (STAGES - 1);
+        const bool blk_ok = (stage_ok >> sc) & 1u;
+        st[pp] = ring + sc * Gm::kStage;
+        slot0[pp] = (pg_a + warp + kWarps * (k + pp)) * kPage;
+        v0[pp] = FULL || (blk_ok && (slot0[pp] + 2 * r < S));
+        v1[pp] = FULL || (blk_ok && (slot0[pp] + 2 * r + 1 < S));
+        skv[pp] = *reinterpret_cast<const float2*>(st[pp] + s_off);
+        svv[pp] = *reinterpret_cast<const float2*>(st[pp] + s_off + 64);
+      }
 
       // ---- S = K_codes . q'  (rows: slots 2r and 2r+1, cols: query heads 2c, 2c+1)
-      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      float acc[NP][4];
+#pragma unroll
+      for (int pp = 0; pp < NP; ++pp) acc[pp][0] = acc[pp][1] = acc[pp][2] = acc[pp][3] = 0.0f;
       if (BITS == 8) {
-        const uint4 ka = *reinterpret_cast<const uint4*>(st + 0 * 512 + lane * 16);
-        const uint4 kb2 = *reinterpret_cast<const uint4*>(st + 1 * 512 + lane * 16);
-        const uint4 kc = *reinterpret_cast<const uint4*>(st + 2 * 512 + lane * 16);
-        const uint4 kd = *reinterpret_cast<const uint4*>(st + 3 * 512 + lane * 16);
-        const uint32_t w0[8] = {ka.x, ka.y, ka.z, ka.w, kb2.x, kb2.y, kb2.z, kb2.w};
-        const uint32_t w1[8] = {kc.x, kc.y, kc.z, kc.w, kd.x, kd.y, kd.z, kd.w};
+        uint32_t w0[NP][8], w1[NP][8];
+#pragma unroll
+        for (int pp = 0; pp < NP; ++pp) {
+          const uint4 ka = *reinterpret_cast<const uint4*>(st[pp] + k_off);
+          const uint4 kb2 = *reinterpret_cast<const uint4*>(st[pp] + k_off + 64);
+          const uint4 kc = *reinterpret_cast<const uint4*>(st[pp] + k_off + RB);
+          const uint4 kd = *reinterpret_cast<const uint4*>(st[pp] + k_off + RB + 64);
+          w0[pp][0] = ka.x; w0[pp][1] = ka.y; w0[pp][2] = ka.z; w0[pp][3] = ka.w;
+          w0[pp][4] = kb2.x; w0[pp][5] = kb2.y; w0[pp][6] = kb2.z; w0[pp][7] = kb2.w;
+          w1[pp][0] = kc.x; w1[pp][1] = kc.y; w1[pp][2] = kc.z; w1[pp][3] = kc.w;
+          w1[pp][4] = kd.x; w1[pp][5] = kd.y; w1[pp][6] = kd.z; w1[pp][7] = kd.w;
+        }
 #pragma unroll
         for (int stp = 0; stp < 8; ++stp) {
-          uint32_t a0, a1, a2, a3;
-          if (FP8) {
-            e4m3x4_to_h2(w0[stp], a0, a2);
-            e4m3x4_to_h2(w1[stp], a1, a3);
-          } else {
-            i8x4_to_h2(w0[stp] ^ 0x80808080u, a0, a2);
-            i8x4_to_h2(w1[stp] ^ 0x80808080u, a1, a3);
+#pragma unroll
+          for (int pp = 0; pp < NP; ++pp) {
+            uint32_t a0, a1, a2, a3;
+            if (FP8) {
+              e4m3x4_to_h2(w0[pp][stp], a0, a2);
+              e4m3x4_to_h2(w1[pp][stp], a1, a3);
+            } else {
+              a0 = u8_even(w0[pp][stp]);
+              a1 = u8_even(w1[pp][stp]);
+              a2 = u8_even(w0[pp][stp] >> 8);
+              a3 = u8_even(w1[pp][stp] >> 8);
+            }
+            mma16816(acc[pp], a0, a1, a2, a3, bq[stp][0], bq[stp][1]);
           }
-          mma16816(acc, a0, a1, a2, a3, bq[stp][0], bq[stp][1]);
         }
       } else {
-        const uint4 ka = *reinterpret_cast<const uint4*>(st + 0 * 512 + lane * 16);
-        const uint4 kb2 = *reinterpret_cast<const uint4*>(st + 1 * 512 + lane * 16);
-        const uint32_t w0[4] = {ka.x, ka.y, ka.z, ka.w};
-        const uint32_t w1[4] = {kb2.x, kb2.y, kb2.z, kb2.w};
+        uint32_t w0[NP][4], w1[NP][4];
+#pragma unroll
+        for (int pp = 0; pp < NP; ++pp) {
+          const uint4 ka = *reinterpret_cast<const uint4*>(st[pp] + k_off);
+          const uint4 kb2 = *reinterpret_cast<const uint4*>(st[pp] + k_off + RB);
+          w0[pp][0] = ka.x; w0[pp][1] = ka.y; w0[pp][2] = ka.z; w0[pp][3] = ka.w;
+          w1[pp][0] = kb2.x; w1[pp][1] = kb2.y; w1[pp][2] = kb2.z; w1[pp][3] = kb2.w;
+        }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const uint32_t x0 = w0[i], x1 = w1[i];
-          const uint32_t x0s = x0 >> 8, x1s = x1 >> 8;
-          mma16816(acc, i4_lo_to_h2(x0), i4_lo_to_h2(x1), i4_hi_to_h2(x0), i4_hi_to_h2(x1), bq[2 * i][0],
-                   bq[2 * i][1]);
-          mma16816(acc, i4_lo_to_h2(x0s), i4_lo_to_h2(x1s), i4_hi_to_h2(x0s), i4_hi_to_h2(x1s),
-                   bq[2 * i + 1][0], bq[2 * i + 1][1]);
+#pragma unroll
+          for (int pp = 0; pp < NP; ++pp) {
+            const uint32_t x0 = w0[pp][i], x1 = w1[pp][i];
+            const uint32_t x0s = x0 >> 8, x1s = x1 >> 8;
+            mma16816(acc[pp], u4_lo(x0), u4_lo(x1), u4_hi(x0), u4_hi(x1), bq[2 * i][0], bq[2 * i][1]);
+            mma16816(acc[pp], u4_lo(x0s), u4_lo(x1s), u4_hi(x0s), u4_hi(x1s), bq[2 * i + 1][0],
+                     bq[2 * i + 1][1]);
+          }
         }
       }
-      const float lg0 = v0 ? acc[0] * skv.x * cq0 : -INFINITY;  // slot 2r,   head 2c
-      const float lg1 = v0 ? acc[1] * skv.x * cq1 : -INFINITY;  // slot 2r,   head 2c+1
-      const float lg2 = v1 ? acc[2] * skv.y * cq0 : -INFINITY;  // slot 2r+1, head 2c
-      const float lg3 = v1 ? acc[3] * skv.y * cq1 : -INFINITY;  // slot 2r+1, head 2c+1
-      if (lg0p) *reinterpret_cast<float2*>(lg0p + slot0) = make_float2(lg0, lg2);
-      if (lg1p) *reinterpret_cast<float2*>(lg1p + slot0) = make_float2(lg1, lg3);
+      float lg[NP][4];
+#pragma unroll
+      for (int pp = 0; pp < NP; ++pp) {
+        lg[pp][0] = v0[pp] ? (acc[pp][0] - ch0) * (skv[pp].x * cq0) : -INFINITY;  // slot 2r,   head 2c
+        lg[pp][1] = v0[pp] ? (acc[pp][1] - ch1) * (skv[pp].x * cq1) : -INFINITY;  // slot 2r,   head 2c+1
+        lg[pp][2] = v1[pp] ? (acc[pp][2] - ch0) * (skv[pp].y * cq0) : -INFINITY;  // slot 2r+1, head 2c
+        lg[pp][3] = v1[pp] ? (acc[pp][3] - ch1) * (skv[pp].y * cq1) : -INFINITY;  // slot 2r+1, head 2c+1
+        if (lg0p) *reinterpret_cast<float2*>(lg0p + slot0[pp]) = make_float2(lg[pp][0], lg[pp][2]);
+        if (lg1p) *reinterpret_cast<float2*>(lg1p + slot0[pp]) = make_float2(lg[pp][1], lg[pp][3]);
+      }
 
       // ---- lazy online softmax: reduce and rescale only when some lane's
       // logit exceeds the running max by kLazy, or a V scale outgrows 2^(E+4)
-      const float svl = fmaxf(v0 ? svv.x : 0.0f, v1 ? svv.y : 0.0f);
-      const bool need = fmaxf(lg0, lg2) > m0 + kLazy || fmaxf(lg1, lg3) > m1 + kLazy || svl > sv_hi ||
-                        (!e_set && svl > 0.0f);
+      float tm0 = -INFINITY, tm1 = -INFINITY, svl = 0.0f;
+#pragma unroll
+      for (int pp = 0; pp < NP; ++pp) {
+        tm0 = fmaxf(tm0, fmaxf(lg[pp][0], lg[pp][2]));
+        tm1 = fmaxf(tm1, fmaxf(lg[pp][1], lg[pp][3]));
+        svl = fmaxf(svl, fmaxf(v0[pp] ? svv[pp].x : 0.0f, v1[pp] ? svv[pp].y : 0.0f));
+      }
+      const bool need = tm0 > m0 + kLazy || tm1 > m1 + kLazy || svl > sv_hi || (!e_set && svl > 0.0f);
       if (__any_sync(0xffffffffu, need)) {
-        float tm0 = fmaxf(lg0, lg2), tm1 = fmaxf(lg1, lg3), svm = svl;
+        float svm = svl;
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) {
           tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, o));
@@ -420,6 +528,10 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
           oacc[j][1] *= f1;
           oacc[j][3] *= f1;
         }
+        osum[0] *= f0;
+        osum[2] *= f0;
+        osum[1] *= f1;
+        osum[3] *= f1;
         l0 *= al0;
         l1 *= al1;
         m0 = nm0;
@@ -431,72 +543,132 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
           inv2E = pow2i(-E);
         }
       }
-      const float sn0 = v0 ? svv.x * inv2E : 0.0f;
-      const float sn1 = v1 ? svv.y * inv2E : 0.0f;
-      const float p0 = fast_exp2(lg0 - m0), p1 = fast_exp2(lg1 - m1);
-      const float p2 = fast_exp2(lg2 - m0), p3 = fast_exp2(lg3 - m1);
-      l0 += p0 + p2;
-      l1 += p1 + p3;
-      const uint32_t pb0 = movmatrix_t(pack_half2(p0 * sn0, p1 * sn0));
-      const uint32_t pb1 = movmatrix_t(pack_half2(p2 * sn1, p3 * sn1));
+      uint32_t pb0[NP], pb1[NP];
+#pragma unroll
+      for (int pp = 0; pp < NP; ++pp) {
+        const float sn0 = v0[pp] ? svv[pp].x * inv2E : 0.0f;
+        const float sn1 = v1[pp] ? svv[pp].y * inv2E : 0.0f;
+        const float p0 = fast_exp2(lg[pp][0] - m0), p1 = fast_exp2(lg[pp][1] - m1);
+        const float p2 = fast_exp2(lg[pp][2] - m0), p3 = fast_exp2(lg[pp][3] - m1);
+        l0 += p0 + p2;
+        l1 += p1 + p3;
+        pb0[pp] = movmatrix_t(pack_half2(p0 * sn0, p1 * sn0));
+        pb1[pp] = movmatrix_t(pack_half2(p2 * sn1, p3 * sn1));
+      }
 
       // ---- O^T += V_codes^T . P~^T   (rows: head-dim 16r + 2j (+1), cols: query heads)
-      if (BITS == 8) {
-        const uint4 r0 = *reinterpret_cast<const uint4*>(st + Gm::kKBytes + 0 * 512 + lane * 16);
-        const uint4 r1 = *reinterpret_cast<const uint4*>(st + Gm::kKBytes + 1 * 512 + lane * 16);
-        const uint4 r2 = *reinterpret_cast<const uint4*>(st + Gm::kKBytes + 2 * 512 + lane * 16);
-        const uint4 r3 = *reinterpret_cast<const uint4*>(st + Gm::kKBytes + 3 * 512 + lane * 16);
-        const uint32_t x0[4] = {r0.x, r0.y, r0.z, r0.w};  // slot 4c
-        const uint32_t x1[4] = {r1.x, r1.y, r1.z, r1.w};  // slot 4c+1
-        const uint32_t x2[4] = {r2.x, r2.y, r2.z, r2.w};  // slot 4c+2
-        const uint32_t x3[4] = {r3.x, r3.y, r3.z, r3.w};  // slot 4c+3
 #pragma unroll
-        for (int wd = 0; wd < 4; ++wd) {
+      for (int pp = 0; pp < NP; ++pp) {
+        if (BITS == 8) {
+          const uint4 r0 = *reinterpret_cast<const uint4*>(st[pp] + v_off + 0 * RB);
+          const uint4 r1 = *reinterpret_cast<const uint4*>(st[pp] + v_off + 1 * RB);
+          const uint4 r2 = *reinterpret_cast<const uint4*>(st[pp] + v_off + 2 * RB);
+          const uint4 r3 = *reinterpret_cast<const uint4*>(st[pp] + v_off + 3 * RB);
+          const uint32_t x0[4] = {r0.x, r0.y, r0.z, r0.w};  // slot 4c
+          const uint32_t x1[4] = {r1.x, r1.y, r1.z, r1.w};  // slot 4c+1
+          const uint32_t x2[4] = {r2.x, r2.y, r2.z, r2.w};  // slot 4c+2
+          const uint32_t x3[4] = {r3.x, r3.y, r3.z, r3.w};  // slot 4c+3
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const int j = 2 * wd + half;
-            uint32_t a0, a1, a2, a3;
-            if (FP8) {
-              a0 = e4m3_pair_to_h2(x0[wd], x2[wd], 2 * half);
-              a1 = e4m3_pair_to_h2(x0[wd], x2[wd], 2 * half + 1);
-              a2 = e4m3_pair_to_h2(x1[wd], x3[wd], 2 * half);
-              a3 = e4m3_pair_to_h2(x1[wd], x3[wd], 2 * half + 1);
-            } else {
-              const uint32_t sa = (2 * half) | ((2 * half) << 4) | ((4 + 2 * half) << 8) | ((4 + 2 * half) << 12);
-              const uint32_t sb =
-                  (2 * half + 1) | ((2 * half + 1) << 4) | ((5 + 2 * half) << 8) | ((5 + 2 * half) << 12);
-              a0 = i8_pair_to_h2(x0[wd], x2[wd], sa);
-              a1 = i8_pair_to_h2(x0[wd], x2[wd], sb);
-              a2 = i8_pair_to_h2(x1[wd], x3[wd], sa);
-              a3 = i8_pair_to_h2(x1[wd], x3[wd], sb);
+          for (int wd = 0; wd < 4; ++wd) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              const int j = 2 * wd + half;
+              // byte k of x and of y in bytes 0 and 2: pairs slots (4c, 4c+2) or (4c+1, 4c+3)
+              const uint32_t sa = (2 * half) | ((4 + 2 * half) << 8);
+              const uint32_t sb = (2 * half + 1) | ((5 + 2 * half) << 8);
+              uint32_t a0, a1, a2, a3;
+              if (FP8) {
+                a0 = e4m3_pair_to_h2(x0[wd], x2[wd], 2 * half);
+                a1 = e4m3_pair_to_h2(x0[wd], x2[wd], 2 * half + 1);
+                a2 = e4m3_pair_to_h2(x1[wd], x3[wd], 2 * half);
+                a3 = e4m3_pair_to_h2(x1[wd], x3[wd], 2 * half + 1);
+              } else {
+                a0 = u8_even(prmt(x0[wd], x2[wd], sa));
+                a1 = u8_even(prmt(x0[wd], x2[wd], sb));
+                a2 = u8_even(prmt(x1[wd], x3[wd], sa));
+                a3 = u8_even(prmt(x1[wd], x3[wd], sb));
+              }
+              mma16816(oacc[j], a0, a1, a2, a3, pb0[pp], pb1[pp]);
             }
-            mma16816(oacc[j], a0, a1, a2, a3, pb0, pb1);
+          }
+        } else {
+          const uint2 r0 = *reinterpret_cast<const uint2*>(st[pp] + v_off + 0 * RB);
+          const uint2 r1 = *reinterpret_cast<const uint2*>(st[pp] + v_off + 1 * RB);
+          const uint2 r2 = *reinterpret_cast<const uint2*>(st[pp] + v_off + 2 * RB);
+          const uint2 r3 = *reinterpret_cast<const uint2*>(st[pp] + v_off + 3 * RB);
+          const uint32_t x0[2] = {r0.x, r0.y};
+          const uint32_t x1[2] = {r1.x, r1.y};
+          const uint32_t x2[2] = {r2.x, r2.y};
+          const uint32_t x3[2] = {r3.x, r3.y};
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+              // bytes 2m, 2m+1 of slots (4c, 4c+2) and of (4c+1, 4c+3), one pair per 16-bit half
+              const uint32_t sel = m == 0 ? 0x5410u : 0x7632u;
+              const uint32_t v02 = prmt(x0[u], x2[u], sel);
+              const uint32_t v13 = prmt(x1[u], x3[u], sel);
+              const uint32_t v02s = v02 >> 8, v13s = v13 >> 8;
+              mma16816(oacc[4 * u + 2 * m], u4_lo(v02), u4_hi(v02), u4_lo(v13), u4_hi(v13), pb0[pp], pb1[pp]);
+              mma16816(oacc[4 * u + 2 * m + 1], u4_lo(v02s), u4_hi(v02s), u4_lo(v13s), u4_hi(v13s), pb0[pp],
+                       pb1[pp]);
+            }
           }
         }
-      } else {
-        const uint2 r0 = *reinterpret_cast<const uint2*>(st + Gm::kKBytes + 0 * 256 + lane * 8);
-        const uint2 r1 = *reinterpret_cast<const uint2*>(st + Gm::kKBytes + 1 * 256 + lane * 8);
-        const uint2 r2 = *reinterpret_cast<const uint2*>(st + Gm::kKBytes + 2 * 256 + lane * 8);
-        const uint2 r3 = *reinterpret_cast<const uint2*>(st + Gm::kKBytes + 3 * 256 + lane * 8);
-        const uint32_t x0[2] = {r0.x, r0.y};
-        const uint32_t x1[2] = {r1.x, r1.y};
-        const uint32_t x2[2] = {r2.x, r2.y};
-        const uint32_t x3[2] = {r3.x, r3.y};
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const int j = 4 * u + kk;
-            const uint32_t sel = kk | (kk << 4) | ((4 + kk) << 8) | ((4 + kk) << 12);
-            const uint32_t v02 = prmt(x0[u], x2[u], sel);
-            const uint32_t v13 = prmt(x1[u], x3[u], sel);
-            mma16816(oacc[j], i4_lo_to_h2(v02), i4_hi_to_h2(v02), i4_lo_to_h2(v13), i4_hi_to_h2(v13), pb0,
-                     pb1);
-          }
+        if (kOffset) {
+          constexpr uint32_t kOne = 0x3C003C00u;  // fp16 (1, 1)
+          mma16816(osum, kOne, kOne, kOne, kOne, pb0[pp], pb1[pp]);
         }
       }
-      st_comp = st_comp + 1 == STAGES ? 0 : st_comp + 1;
-      __syncwarp();
+    };
+    // a page is FULL when its block id is valid and all 16 slots are below S
+    auto full_page = [&](int k) {
+      return ((stage_ok >> (k & (STAGES - 1))) & 1u) && (pg_a + warp + kWarps * k + 1) * kPage <= S;
+    };
+    auto flag_bad = [&](int k) {
+      if (!((stage_ok >> (k & (STAGES - 1))) & 1u) && lane == 0) atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
+    };
+
+    // at page k the pages through k + STAGES - 1 are issued (into the stages
+    // of pages already consumed) and page k (and k + 1) waited for
+    int k = 0;
+    if (kPagesPerIter == 2) {
+      // two pages per iteration while both are FULL
+#pragma unroll 1
+      for (; k + 1 < n_my; k += 2) {
+        issue_upto(k + STAGES);
+        cp_async_wait<STAGES - 2>();
+        __syncwarp();
+        if (!(full_page(k) && full_page(k + 1))) break;
+        pages_body(std::integral_constant<int, 2>{}, std::true_type{}, k);
+        __syncwarp();
+      }
+      // the rest one page at a time
+#pragma unroll 1
+      for (; k < n_my; ++k) {
+        issue_upto(k + STAGES);
+        cp_async_wait<STAGES - 1>();
+        __syncwarp();
+        flag_bad(k);
+        if (full_page(k))
+          pages_body(std::integral_constant<int, 1>{}, std::true_type{}, k);
+        else
+          pages_body(std::integral_constant<int, 1>{}, std::false_type{}, k);
+        __syncwarp();
+      }
+    } else {
+#pragma unroll 1
+      for (; k < n_my; ++k) {
+        issue_upto(k + STAGES);
+        cp_async_wait<STAGES - 1>();
+        __syncwarp();
+        flag_bad(k);
+        if (full_page(k))
+          pages_body(std::integral_constant<int, 1>{}, std::true_type{}, k);
+        else
+          pages_body(std::integral_constant<int, 1>{}, std::false_type{}, k);
+        __syncwarp();
+      }
     }
     cp_async_wait<0>();
 
@@ -518,14 +690,20 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
       sm_l[warp * kMaxGroup + 2 * c + 1] = l1;
     }
     {
+      // offset codes: o = (2^24 acc - offset x sum of the PV operand) 2^E,
+      // with 2^20 for the rows of INT4 high nibbles (16x)
+      const float sA = kOffset ? 0x1p24f : 1.0f;
+      const float sB = kOffset ? (BITS == 4 ? 0x1p20f : 0x1p24f) : 1.0f;
+      const float b0 = kOffset ? kOffV * osum[0] : 0.0f;
+      const float b1 = kOffset ? kOffV * osum[1] : 0.0f;
       float* o0 = sm_o + ((size_t)warp * kMaxGroup + 2 * c) * kHeadDim + 16 * r;
       float* o1 = o0 + kHeadDim;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        o0[2 * j] = oacc[j][0] * f2E;
-        o0[2 * j + 1] = oacc[j][2] * f2E;
-        o1[2 * j] = oacc[j][1] * f2E;
-        o1[2 * j + 1] = oacc[j][3] * f2E;
+        o0[2 * j] = (oacc[j][0] * sA - b0) * f2E;
+        o0[2 * j + 1] = (oacc[j][2] * sB - b0) * f2E;
+        o1[2 * j] = (oacc[j][1] * sA - b1) * f2E;
+        o1[2 * j + 1] = (oacc[j][3] * sB - b1) * f2E;
       }
     }
     __syncthreads();

@@ -80,6 +80,9 @@ typedef enum {
 #define KVC_DEV_BAD_KEEP_MASK   0x4  /* keep mask count differs from the plan     */
 #define KVC_DEV_TABLE_OVERFLOW  0x8  /* per-sequence block table overflow         */
 #define KVC_DEV_STACK_OVERFLOW  0x10 /* free-block stack overflow on release      */
+#define KVC_DEV_WAIT_TIMEOUT    0x20 /* a page copy into shared memory did not
+                                        complete within 2 s; the pages not yet
+                                        read were skipped (outputs invalid)    */
 
 /* Geometry of one layer's cache. */
 typedef struct {
