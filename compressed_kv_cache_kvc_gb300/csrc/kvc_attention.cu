@@ -60,24 +60,25 @@ namespace {
 using namespace dev;
 
 constexpr int kWarps = 4;
-constexpr int kPagesPerIter = 1;     // pages of a warp processed together in the split kernel
+constexpr int kPagesPerIter = 2;     // pages of a warp processed together in the split kernel
 constexpr float kLazy = 4.0f;        // log2 units the running max may lag
 constexpr int kMergeBtStage = 2048;  // block-table entries staged in shared memory (32768 slots)
 constexpr int kMergeThreads = 512;
 
 // One stage of a warp's ring holds one head-page: its K and V code rows and
 // its 16 K and 16 V scales (a head-page is a contiguous run of 16 rows in the
-// pool).  Rows 8..15 of K and of V sit 64 bytes after rows 0..7, so the row
-// groups the lanes read in one instruction fall on all 32 shared-memory banks.
+// pool).  Order: K rows 0..7 | 16 K scales | K rows 8..15 | V rows 0..7 | 16
+// V scales | V rows 8..15: the 64 bytes of scales between the two row groups
+// put the rows the lanes read together on all 32 shared-memory banks.
 template <int BITS>
 struct Geom {
   static constexpr int kRowBytes = BITS * 16;            // 128 (8-bit codes) or 64 (INT4)
   static constexpr int kHalf = 8 * kRowBytes;            // rows 0..7 of a head-page
-  static constexpr int kK = 0;                           // K rows 0..7 | 64 | K rows 8..15
-  static constexpr int kV = 2 * kHalf + 64;              // V rows 0..7 | 64 | V rows 8..15
-  static constexpr int kKS = 2 * (2 * kHalf + 64);       // 16 fp32 K scales
-  static constexpr int kVS = kKS + 64;                   // 16 fp32 V scales
-  static constexpr int kStage = kVS + 64;
+  static constexpr int kK = 0;
+  static constexpr int kKS = kHalf;
+  static constexpr int kV = 2 * kHalf + 64;
+  static constexpr int kVS = 3 * kHalf + 64;
+  static constexpr int kStage = 4 * kHalf + 128;
   static constexpr int kStages = 4;
   static constexpr int kSmem = kWarps * kStages * kStage;
   // offset of code row t within its K or V block of a stage
@@ -117,8 +118,20 @@ __device__ __forceinline__ void copy_codes(uint32_t sK, const uint8_t* gK, uint3
         "cp.async.cg.shared.global [%2+576], [%3+512], 16;\n" ::"r"(sK), "l"(gK), "r"(sV), "l"(gV));
   }
 }
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src));
+// A 16-byte cp.async done only when `pred` (no branch).
+__device__ __forceinline__ void cp_async16_if(bool pred, uint32_t dst, const void* src) {
+  asm volatile(
+      "{\n .reg .pred q;\n setp.ne.u32 q, %0, 0;\n"
+      " @q cp.async.cg.shared.global [%1], [%2], 16;\n}\n" ::"r"((uint32_t)pred),
+      "r"(dst), "l"(src));
+}
+// Two floats to global memory only when `pred` (no branch).
+__device__ __forceinline__ void st2_if(bool pred, float* dst, float a, float b) {
+  asm volatile(
+      "{\n .reg .pred q;\n setp.ne.u32 q, %0, 0;\n"
+      " @q st.global.v2.f32 [%1], {%2, %3};\n}\n" ::"r"((uint32_t)pred),
+      "l"(dst), "f"(a), "f"(b)
+      : "memory");
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) { return __byte_perm(a, b, sel); }
@@ -240,7 +253,8 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
   // and (lanes 0..7) one 16-byte chunk of the 16 K or 16 V scales
   const uint32_t k_soff = Gm::kK + 16 * lane;
   const uint32_t v_soff = Gm::kV + 16 * lane;
-  const uint32_t sc_soff = Gm::kKS + 16 * lane;  // K scales, then V scales (kVS = kKS + 64)
+  const uint32_t sc_soff = lane < 4 ? Gm::kKS + 16 * lane : Gm::kVS + 16 * (lane - 4);
+  // (lanes 8..31 get an address inside the scales too, never used)
   const float* sc_gbase = (lane < 4 ? s.k_scale : s.v_scale) + 4 * (lane & 3);
   // what this lane reads of a stage: K rows 2r and 2r+1 from byte 16c (INT8
   // also from 64 + 16c), V rows 4c..4c+3 from byte 8r (INT4) or 16r, the
@@ -297,7 +311,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
           const size_t hp = (size_t)blk * hkv + h;
           copy_codes<BITS>(sb + k_soff, s.k_codes + hp * (16 * RB) + 16 * lane, sb + v_soff,
                            s.v_codes + hp * (16 * RB) + 16 * lane);
-          if (lane < 8) cp_async16(sb + sc_soff, sc_gbase + hp * kPage);
+          cp_async16_if(lane < 8, sb + sc_soff, sc_gbase + hp * kPage);
         }
       }
       cp_async_commit();
@@ -309,7 +323,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
 #pragma unroll 1
       for (; nxt < n; ++nxt) issue(nxt);
     };
-    issue_upto(STAGES - 1);
+    issue_upto(kPagesPerIter == 2 ? 2 : STAGES - 1);
 
     // ---- query fragments (B operand of QK^T), scaled by 2^e_g into fp16 range;
     // with offset codes, the sum of each head's query values as the MMA sees them
@@ -404,9 +418,11 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
     bool e_set = false;
     float sv_hi = 0.0f;
     float inv2E = 1.0f;
-    // logits of this pair, [g][slot]; the lane writes slots (2r, 2r+1) of heads 2c and 2c+1
-    float* lg0p = spill && 2 * c < G ? w.logits + ((size_t)pair * G + 2 * c) * w.s_cap + 2 * r : nullptr;
-    float* lg1p = spill && 2 * c + 1 < G ? w.logits + ((size_t)pair * G + 2 * c + 1) * w.s_cap + 2 * r : nullptr;
+    // logits of this pair, [g][slot]; the lane writes slots (2r, 2r+1) of heads
+    // 2c and 2c+1 (lanes of padding heads write nothing)
+    const bool sp0 = spill && 2 * c < G, sp1 = spill && 2 * c + 1 < G;
+    float* lg0p = w.logits + ((size_t)pair * G + (sp0 ? 2 * c : 0)) * w.s_cap + 2 * r;
+    float* lg1p = w.logits + ((size_t)pair * G + (sp1 ? 2 * c + 1 : 0)) * w.s_cap + 2 * r;
 
     // NP consecutive pages of this warp (k .. k + NP - 1), their instructions
     // interleaved; FULL: every slot valid (the common case), no per-slot masks
@@ -426,13 +442,18 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
         v0[pp] = FULL || (blk_ok && (slot0[pp] + 2 * r < S));
         v1[pp] = FULL || (blk_ok && (slot0[pp] + 2 * r + 1 < S));
         skv[pp] = *reinterpret_cast<const float2*>(st[pp] + s_off);
-        svv[pp] = *reinterpret_cast<const float2*>(st[pp] + s_off + 64);
+        svv[pp] = *reinterpret_cast<const float2*>(st[pp] + s_off + (Gm::kVS - Gm::kKS));
       }
 
       // ---- S = K_codes . q'  (rows: slots 2r and 2r+1, cols: query heads 2c, 2c+1)
+      // the accumulators start at -(code offset x query sum), so they end at
+      // the dot products of the query with the signed codes
       float acc[NP][4];
 #pragma unroll
-      for (int pp = 0; pp < NP; ++pp) acc[pp][0] = acc[pp][1] = acc[pp][2] = acc[pp][3] = 0.0f;
+      for (int pp = 0; pp < NP; ++pp) {
+        acc[pp][0] = acc[pp][2] = -ch0;
+        acc[pp][1] = acc[pp][3] = -ch1;
+      }
       if (BITS == 8) {
         uint32_t w0[NP][8], w1[NP][8];
 #pragma unroll
@@ -487,12 +508,12 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
       float lg[NP][4];
 #pragma unroll
       for (int pp = 0; pp < NP; ++pp) {
-        lg[pp][0] = v0[pp] ? (acc[pp][0] - ch0) * (skv[pp].x * cq0) : -INFINITY;  // slot 2r,   head 2c
-        lg[pp][1] = v0[pp] ? (acc[pp][1] - ch1) * (skv[pp].x * cq1) : -INFINITY;  // slot 2r,   head 2c+1
-        lg[pp][2] = v1[pp] ? (acc[pp][2] - ch0) * (skv[pp].y * cq0) : -INFINITY;  // slot 2r+1, head 2c
-        lg[pp][3] = v1[pp] ? (acc[pp][3] - ch1) * (skv[pp].y * cq1) : -INFINITY;  // slot 2r+1, head 2c+1
-        if (lg0p) *reinterpret_cast<float2*>(lg0p + slot0[pp]) = make_float2(lg[pp][0], lg[pp][2]);
-        if (lg1p) *reinterpret_cast<float2*>(lg1p + slot0[pp]) = make_float2(lg[pp][1], lg[pp][3]);
+        lg[pp][0] = v0[pp] ? acc[pp][0] * (skv[pp].x * cq0) : -INFINITY;  // slot 2r,   head 2c
+        lg[pp][1] = v0[pp] ? acc[pp][1] * (skv[pp].x * cq1) : -INFINITY;  // slot 2r,   head 2c+1
+        lg[pp][2] = v1[pp] ? acc[pp][2] * (skv[pp].y * cq0) : -INFINITY;  // slot 2r+1, head 2c
+        lg[pp][3] = v1[pp] ? acc[pp][3] * (skv[pp].y * cq1) : -INFINITY;  // slot 2r+1, head 2c+1
+        st2_if(sp0, lg0p + slot0[pp], lg[pp][0], lg[pp][2]);
+        st2_if(sp1, lg1p + slot0[pp], lg[pp][1], lg[pp][3]);
       }
 
       // ---- lazy online softmax: reduce and rescale only when some lane's
@@ -621,54 +642,39 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
         }
       }
     };
-    // a page is FULL when its block id is valid and all 16 slots are below S
-    auto full_page = [&](int k) {
-      return ((stage_ok >> (k & (STAGES - 1))) & 1u) && (pg_a + warp + kWarps * k + 1) * kPage <= S;
-    };
-    auto flag_bad = [&](int k) {
-      if (!((stage_ok >> (k & (STAGES - 1))) & 1u) && lane == 0) atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
-    };
-
-    // at page k the pages through k + STAGES - 1 are issued (into the stages
-    // of pages already consumed) and page k (and k + 1) waited for
+    // this warp's pages k < k_full have all 16 slots below S
+    const int full_pages = S / kPage;
+    const int k_full = full_pages > pg_a + warp ? min(n_my, (full_pages - pg_a - warp + kWarps - 1) / kWarps) : 0;
     int k = 0;
     if (kPagesPerIter == 2) {
-      // two pages per iteration while both are FULL
+      // two full pages per iteration, the copies of the next two in flight;
+      // on entry pages [0, k + 2) are issued
 #pragma unroll 1
-      for (; k + 1 < n_my; k += 2) {
-        issue_upto(k + STAGES);
-        cp_async_wait<STAGES - 2>();
+      for (; k + 1 < k_full; k += 2) {
+        if (((stage_ok >> (k & (STAGES - 1))) & 3u) != 3u) break;  // a bad block id: the slow path
+        issue(k + 2);
+        issue(k + 3);
+        nxt = k + 4;
+        cp_async_wait<2>();
         __syncwarp();
-        if (!(full_page(k) && full_page(k + 1))) break;
         pages_body(std::integral_constant<int, 2>{}, std::true_type{}, k);
         __syncwarp();
       }
-      // the rest one page at a time
+    }
+    // one page at a time: the pages through k + STAGES - 1 issued (into the
+    // stages of pages already consumed), page k waited for
 #pragma unroll 1
-      for (; k < n_my; ++k) {
-        issue_upto(k + STAGES);
-        cp_async_wait<STAGES - 1>();
-        __syncwarp();
-        flag_bad(k);
-        if (full_page(k))
-          pages_body(std::integral_constant<int, 1>{}, std::true_type{}, k);
-        else
-          pages_body(std::integral_constant<int, 1>{}, std::false_type{}, k);
-        __syncwarp();
-      }
-    } else {
-#pragma unroll 1
-      for (; k < n_my; ++k) {
-        issue_upto(k + STAGES);
-        cp_async_wait<STAGES - 1>();
-        __syncwarp();
-        flag_bad(k);
-        if (full_page(k))
-          pages_body(std::integral_constant<int, 1>{}, std::true_type{}, k);
-        else
-          pages_body(std::integral_constant<int, 1>{}, std::false_type{}, k);
-        __syncwarp();
-      }
+    for (; k < n_my; ++k) {
+      issue_upto(k + STAGES);
+      cp_async_wait<STAGES - 1>();
+      __syncwarp();
+      const bool ok = (stage_ok >> (k & (STAGES - 1))) & 1u;
+      if (!ok && lane == 0) atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
+      if (ok && k < k_full)
+        pages_body(std::integral_constant<int, 1>{}, std::true_type{}, k);
+      else
+        pages_body(std::integral_constant<int, 1>{}, std::false_type{}, k);
+      __syncwarp();
     }
     cp_async_wait<0>();
 
