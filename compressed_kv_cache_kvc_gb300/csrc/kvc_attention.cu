@@ -65,24 +65,30 @@ constexpr float kLazy = 4.0f;        // log2 units the running max may lag
 constexpr int kMergeBtStage = 2048;  // block-table entries staged in shared memory (32768 slots)
 constexpr int kMergeThreads = 512;
 
-// One stage of a warp's ring holds one head-page: its K and V code rows and
-// its 16 K and 16 V scales (a head-page is a contiguous run of 16 rows in the
-// pool).  Order: K rows 0..7 | 16 K scales | K rows 8..15 | V rows 0..7 | 16
-// V scales | V rows 8..15: the 64 bytes of scales between the two row groups
-// put the rows the lanes read together on all 32 shared-memory banks.
+// One stage of a warp's ring holds one head-page: its K code rows, its V code
+// rows, 16 K scales and 16 V scales (a K or V head-page is one contiguous run
+// of 16 rows in the pool).  The 16-byte chunks of the code rows are placed by
+// a fixed permutation (chunk_off) chosen so that every copy instruction and
+// every read instruction of the kernel touches each shared-memory bank at most
+// once per 128 bytes: chunk j of row t goes to
+//   INT4 (4 chunks a row): 16 (8 (t >> 1) + 4 ((t ^ t >> 1 ^ t >> 2) & 1) + ((j + 2 (t >> 3)) & 3)),
+//   8-bit (8 chunks a row): 128 t + 16 (j ^ (2 ((t >> 2) & 3) ^ 4 ((t >> 1) & 1))).
 template <int BITS>
 struct Geom {
   static constexpr int kRowBytes = BITS * 16;            // 128 (8-bit codes) or 64 (INT4)
-  static constexpr int kHalf = 8 * kRowBytes;            // rows 0..7 of a head-page
   static constexpr int kK = 0;
-  static constexpr int kKS = kHalf;
-  static constexpr int kV = 2 * kHalf + 64;
-  static constexpr int kVS = 3 * kHalf + 64;
-  static constexpr int kStage = 4 * kHalf + 128;
+  static constexpr int kV = 16 * kRowBytes;
+  static constexpr int kKS = 32 * kRowBytes;
+  static constexpr int kVS = kKS + 64;
+  static constexpr int kStage = kVS + 64;
   static constexpr int kStages = 4;
   static constexpr int kSmem = kWarps * kStages * kStage;
-  // offset of code row t within its K or V block of a stage
-  static __host__ __device__ constexpr int row_off(int t) { return t * kRowBytes + (t >= 8 ? 64 : 0); }
+  static constexpr int kChunksPerRow = kRowBytes / 16;
+  static constexpr int kCopies = 16 * kRowBytes / 512;   // 16-byte copies per lane per K (or V) run
+  static __host__ __device__ constexpr int chunk_off(int t, int j) {
+    return BITS == 4 ? 16 * (8 * (t >> 1) + 4 * ((t ^ (t >> 1) ^ (t >> 2)) & 1) + ((j + 2 * (t >> 3)) & 3))
+                     : 128 * t + 16 * (j ^ ((2 * ((t >> 2) & 3)) ^ (4 * ((t >> 1) & 1))));
+  }
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -94,28 +100,35 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
-// The code rows of one page of one head into a stage: lane L copies the
-// 16-byte chunks L + 32 i of the K run and of the V run (every instruction
-// reads 512 contiguous bytes), to their place in the stage (rows 8..15 64
-// bytes further).  The offsets are immediates from the two lane bases.
+// The code rows of one page of one head into a stage, when `pred`: lane L
+// copies the 16-byte chunks L + 32 i of the K run and of the V run (every
+// instruction reads 512 contiguous bytes) to their permuted places d[i]
+// (V: + kV).
 template <int BITS>
-__device__ __forceinline__ void copy_codes(uint32_t sK, const uint8_t* gK, uint32_t sV, const uint8_t* gV) {
+__device__ __forceinline__ void copy_codes(bool pred, uint32_t sb, const uint32_t (&d)[Geom<BITS>::kCopies],
+                                           const uint8_t* gK, const uint8_t* gV) {
+  constexpr int kV = Geom<BITS>::kV;
   if (BITS == 8) {
     asm volatile(
-        "cp.async.cg.shared.global [%0], [%1], 16;\n"
-        "cp.async.cg.shared.global [%0+512], [%1+512], 16;\n"
-        "cp.async.cg.shared.global [%0+1088], [%1+1024], 16;\n"
-        "cp.async.cg.shared.global [%0+1600], [%1+1536], 16;\n"
-        "cp.async.cg.shared.global [%2], [%3], 16;\n"
-        "cp.async.cg.shared.global [%2+512], [%3+512], 16;\n"
-        "cp.async.cg.shared.global [%2+1088], [%3+1024], 16;\n"
-        "cp.async.cg.shared.global [%2+1600], [%3+1536], 16;\n" ::"r"(sK), "l"(gK), "r"(sV), "l"(gV));
+        "{\n .reg .pred q;\n setp.ne.u32 q, %7, 0;\n"
+        " @q cp.async.cg.shared.global [%0], [%4], 16;\n"
+        " @q cp.async.cg.shared.global [%1], [%4+512], 16;\n"
+        " @q cp.async.cg.shared.global [%2], [%4+1024], 16;\n"
+        " @q cp.async.cg.shared.global [%3], [%4+1536], 16;\n"
+        " @q cp.async.cg.shared.global [%0+%6], [%5], 16;\n"
+        " @q cp.async.cg.shared.global [%1+%6], [%5+512], 16;\n"
+        " @q cp.async.cg.shared.global [%2+%6], [%5+1024], 16;\n"
+        " @q cp.async.cg.shared.global [%3+%6], [%5+1536], 16;\n}\n" ::"r"(sb + d[0]),
+        "r"(sb + d[1 % Geom<BITS>::kCopies]), "r"(sb + d[2 % Geom<BITS>::kCopies]),
+        "r"(sb + d[3 % Geom<BITS>::kCopies]), "l"(gK), "l"(gV), "n"(kV), "r"((uint32_t)pred));
   } else {
     asm volatile(
-        "cp.async.cg.shared.global [%0], [%1], 16;\n"
-        "cp.async.cg.shared.global [%0+576], [%1+512], 16;\n"
-        "cp.async.cg.shared.global [%2], [%3], 16;\n"
-        "cp.async.cg.shared.global [%2+576], [%3+512], 16;\n" ::"r"(sK), "l"(gK), "r"(sV), "l"(gV));
+        "{\n .reg .pred q;\n setp.ne.u32 q, %5, 0;\n"
+        " @q cp.async.cg.shared.global [%0], [%2], 16;\n"
+        " @q cp.async.cg.shared.global [%1], [%2+512], 16;\n"
+        " @q cp.async.cg.shared.global [%0+%4], [%3], 16;\n"
+        " @q cp.async.cg.shared.global [%1+%4], [%3+512], 16;\n}\n" ::"r"(sb + d[0]),
+        "r"(sb + d[1]), "l"(gK), "l"(gV), "n"(kV), "r"((uint32_t)pred));
   }
 }
 // A 16-byte cp.async done only when `pred` (no branch).
@@ -251,18 +264,30 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
 
   // what this lane copies of a page: chunks lane + 32 i of the K and V runs,
   // and (lanes 0..7) one 16-byte chunk of the 16 K or 16 V scales
-  const uint32_t k_soff = Gm::kK + 16 * lane;
-  const uint32_t v_soff = Gm::kV + 16 * lane;
+  uint32_t cp_d[Gm::kCopies];
+#pragma unroll
+  for (int i = 0; i < Gm::kCopies; ++i)
+    cp_d[i] = Gm::chunk_off((lane + 32 * i) / Gm::kChunksPerRow, (lane + 32 * i) % Gm::kChunksPerRow);
   const uint32_t sc_soff = lane < 4 ? Gm::kKS + 16 * lane : Gm::kVS + 16 * (lane - 4);
   // (lanes 8..31 get an address inside the scales too, never used)
   const float* sc_gbase = (lane < 4 ? s.k_scale : s.v_scale) + 4 * (lane & 3);
-  // what this lane reads of a stage: K rows 2r and 2r+1 from byte 16c (INT8
-  // also from 64 + 16c), V rows 4c..4c+3 from byte 8r (INT4) or 16r, the
-  // scales of slots 2r and 2r+1
-  const int k_off = Gm::row_off(2 * r) + 16 * c;
-  const int v_off = Gm::kV + Gm::row_off(4 * c) + (BITS == 8 ? 16 * r : 8 * r);
+  // what this lane reads of a stage: the chunks of K rows 2r and 2r+1 holding
+  // dims 32c.. (INT4) or 16c.. and 64+16c.. (8-bit); of V rows 4c..4c+3 the
+  // 8 bytes at 8r (INT4) or 16 bytes at 16r; the scales of slots 2r and 2r+1
+  int k_off[BITS == 8 ? 4 : 2], v_off[4];
+  if (BITS == 8) {
+    k_off[0] = Gm::chunk_off(2 * r, c);
+    k_off[1] = Gm::chunk_off(2 * r, c + 4);
+    k_off[2] = Gm::chunk_off(2 * r + 1, c);
+    k_off[3 % (BITS == 8 ? 4 : 2)] = Gm::chunk_off(2 * r + 1, c + 4);
+  } else {
+    k_off[0] = Gm::chunk_off(2 * r, c);
+    k_off[1] = Gm::chunk_off(2 * r + 1, c);
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    v_off[k] = Gm::kV + (BITS == 8 ? Gm::chunk_off(4 * c + k, r) : Gm::chunk_off(4 * c + k, r >> 1) + 8 * (r & 1));
   const int s_off = Gm::kKS + 8 * r;
-
 
   while (F < F1) {
     // ---- the (sequence, KV head) pair of page F and this CTA's run of its pages
@@ -295,25 +320,27 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
     int bt_cur = bt_load(0);
     int bt_nxt = n_my > 32 ? bt_load(1) : -1;
     uint32_t stage_ok = 0;  // bit k: the page in stage k has a valid block id
+    // this lane's source bases for head h (a block's head-page = base + block x stride)
+    const uint8_t* kb = s.k_codes + (size_t)h * (16 * RB) + 16 * lane;
+    const uint8_t* vb = s.v_codes + (size_t)h * (16 * RB) + 16 * lane;
+    const float* scb = sc_gbase + (size_t)h * kPage;
+    const uint32_t code_stride = (uint32_t)hkv * (16 * RB), sc_stride = (uint32_t)hkv * kPage;
 
+    // page k of this warp into stage k & (STAGES - 1), one commit group (empty
+    // past n_my: the block ids there are -1)
     auto issue = [&](int k) {
-      if (k < n_my) {
-        if ((k & 31) == 0 && k > 0) {
-          bt_cur = bt_nxt;
-          bt_nxt = bt_load((k >> 5) + 1);
-        }
-        const int blk = __shfl_sync(0xffffffffu, bt_cur, k & 31);
-        const bool ok = (unsigned)blk < (unsigned)s.num_blocks;
-        const int slot_issue = k & (STAGES - 1);
-        stage_ok = ok ? (stage_ok | (1u << slot_issue)) : (stage_ok & ~(1u << slot_issue));
-        if (ok) {
-          const uint32_t sb = ring_s + slot_issue * Gm::kStage;
-          const size_t hp = (size_t)blk * hkv + h;
-          copy_codes<BITS>(sb + k_soff, s.k_codes + hp * (16 * RB) + 16 * lane, sb + v_soff,
-                           s.v_codes + hp * (16 * RB) + 16 * lane);
-          cp_async16_if(lane < 8, sb + sc_soff, sc_gbase + hp * kPage);
-        }
+      if ((k & 31) == 0 && k > 0) {
+        bt_cur = bt_nxt;
+        bt_nxt = bt_load((k >> 5) + 1);
       }
+      const int blk = __shfl_sync(0xffffffffu, bt_cur, k & 31);
+      const bool ok = (unsigned)blk < (unsigned)s.num_blocks;
+      const int slot_issue = k & (STAGES - 1);
+      stage_ok = (stage_ok & ~(1u << slot_issue)) | ((uint32_t)ok << slot_issue);
+      const uint32_t sb = ring_s + slot_issue * Gm::kStage;
+      const size_t off = (size_t)(uint32_t)blk * code_stride;
+      copy_codes<BITS>(ok, sb, cp_d, kb + off, vb + off);
+      cp_async16_if(ok && lane < 8, sb + sc_soff, scb + (size_t)(uint32_t)blk * sc_stride);
       cp_async_commit();
     };
 
@@ -442,7 +469,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
         v0[pp] = FULL || (blk_ok && (slot0[pp] + 2 * r < S));
         v1[pp] = FULL || (blk_ok && (slot0[pp] + 2 * r + 1 < S));
         skv[pp] = *reinterpret_cast<const float2*>(st[pp] + s_off);
-        svv[pp] = *reinterpret_cast<const float2*>(st[pp] + s_off + (Gm::kVS - Gm::kKS));
+        svv[pp] = *reinterpret_cast<const float2*>(st[pp] + s_off + 64);
       }
 
       // ---- S = K_codes . q'  (rows: slots 2r and 2r+1, cols: query heads 2c, 2c+1)
@@ -458,10 +485,10 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
         uint32_t w0[NP][8], w1[NP][8];
 #pragma unroll
         for (int pp = 0; pp < NP; ++pp) {
-          const uint4 ka = *reinterpret_cast<const uint4*>(st[pp] + k_off);
-          const uint4 kb2 = *reinterpret_cast<const uint4*>(st[pp] + k_off + 64);
-          const uint4 kc = *reinterpret_cast<const uint4*>(st[pp] + k_off + RB);
-          const uint4 kd = *reinterpret_cast<const uint4*>(st[pp] + k_off + RB + 64);
+          const uint4 ka = *reinterpret_cast<const uint4*>(st[pp] + k_off[0]);
+          const uint4 kb2 = *reinterpret_cast<const uint4*>(st[pp] + k_off[1]);
+          const uint4 kc = *reinterpret_cast<const uint4*>(st[pp] + k_off[2 % (BITS == 8 ? 4 : 2)]);
+          const uint4 kd = *reinterpret_cast<const uint4*>(st[pp] + k_off[3 % (BITS == 8 ? 4 : 2)]);
           w0[pp][0] = ka.x; w0[pp][1] = ka.y; w0[pp][2] = ka.z; w0[pp][3] = ka.w;
           w0[pp][4] = kb2.x; w0[pp][5] = kb2.y; w0[pp][6] = kb2.z; w0[pp][7] = kb2.w;
           w1[pp][0] = kc.x; w1[pp][1] = kc.y; w1[pp][2] = kc.z; w1[pp][3] = kc.w;
@@ -488,8 +515,8 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
         uint32_t w0[NP][4], w1[NP][4];
 #pragma unroll
         for (int pp = 0; pp < NP; ++pp) {
-          const uint4 ka = *reinterpret_cast<const uint4*>(st[pp] + k_off);
-          const uint4 kb2 = *reinterpret_cast<const uint4*>(st[pp] + k_off + RB);
+          const uint4 ka = *reinterpret_cast<const uint4*>(st[pp] + k_off[0]);
+          const uint4 kb2 = *reinterpret_cast<const uint4*>(st[pp] + k_off[1]);
           w0[pp][0] = ka.x; w0[pp][1] = ka.y; w0[pp][2] = ka.z; w0[pp][3] = ka.w;
           w1[pp][0] = kb2.x; w1[pp][1] = kb2.y; w1[pp][2] = kb2.z; w1[pp][3] = kb2.w;
         }
@@ -581,10 +608,10 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
 #pragma unroll
       for (int pp = 0; pp < NP; ++pp) {
         if (BITS == 8) {
-          const uint4 r0 = *reinterpret_cast<const uint4*>(st[pp] + v_off + 0 * RB);
-          const uint4 r1 = *reinterpret_cast<const uint4*>(st[pp] + v_off + 1 * RB);
-          const uint4 r2 = *reinterpret_cast<const uint4*>(st[pp] + v_off + 2 * RB);
-          const uint4 r3 = *reinterpret_cast<const uint4*>(st[pp] + v_off + 3 * RB);
+          const uint4 r0 = *reinterpret_cast<const uint4*>(st[pp] + v_off[0]);
+          const uint4 r1 = *reinterpret_cast<const uint4*>(st[pp] + v_off[1]);
+          const uint4 r2 = *reinterpret_cast<const uint4*>(st[pp] + v_off[2]);
+          const uint4 r3 = *reinterpret_cast<const uint4*>(st[pp] + v_off[3]);
           const uint32_t x0[4] = {r0.x, r0.y, r0.z, r0.w};  // slot 4c
           const uint32_t x1[4] = {r1.x, r1.y, r1.z, r1.w};  // slot 4c+1
           const uint32_t x2[4] = {r2.x, r2.y, r2.z, r2.w};  // slot 4c+2
@@ -613,10 +640,10 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
             }
           }
         } else {
-          const uint2 r0 = *reinterpret_cast<const uint2*>(st[pp] + v_off + 0 * RB);
-          const uint2 r1 = *reinterpret_cast<const uint2*>(st[pp] + v_off + 1 * RB);
-          const uint2 r2 = *reinterpret_cast<const uint2*>(st[pp] + v_off + 2 * RB);
-          const uint2 r3 = *reinterpret_cast<const uint2*>(st[pp] + v_off + 3 * RB);
+          const uint2 r0 = *reinterpret_cast<const uint2*>(st[pp] + v_off[0]);
+          const uint2 r1 = *reinterpret_cast<const uint2*>(st[pp] + v_off[1]);
+          const uint2 r2 = *reinterpret_cast<const uint2*>(st[pp] + v_off[2]);
+          const uint2 r3 = *reinterpret_cast<const uint2*>(st[pp] + v_off[3]);
           const uint32_t x0[2] = {r0.x, r0.y};
           const uint32_t x1[2] = {r1.x, r1.y};
           const uint32_t x2[2] = {r2.x, r2.y};
