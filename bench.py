@@ -623,7 +623,7 @@ def prefill_context_report(args, name: str):
     torch.cuda.synchronize()
     snap = c.state_view.clone()
     out = torch.empty_like(q1)
-    ws = c.prefill_context_workspace(B)
+    ws = c.prefill_context_workspace(B, n1)
     stream = torch.cuda.Stream(device=dev)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ms = []

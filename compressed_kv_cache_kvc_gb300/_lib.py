@@ -16,7 +16,7 @@ KVC_ERR_CUDA = 4
 KVC_ERR_DEVICE = 5
 KVC_ERR_STATE = 6
 
-KVC_VERSION = 200  # the header this binding's structures follow
+KVC_VERSION = 300  # the header this binding's structures and signatures follow
 KVC_ATTN_ACCUM_H2O = 0x1
 KVC_CODES_INT = 0
 KVC_CODES_E4M3 = 1
@@ -74,7 +74,7 @@ _SIGS = {
     "kvc_decode_attention_noalloc": (_I, [_P, _I, _I, _P, _P, ctypes.c_float, _I, _P]),
     "kvc_prefill_workspace_bytes": (_SZ, [_P, _I, _I]),
     "kvc_prefill_attention": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, ctypes.c_float, _I, _P, _SZ, _P]),
-    "kvc_prefill_context_workspace_bytes": (_SZ, [_P, _I]),
+    "kvc_prefill_context_workspace_bytes": (_SZ, [_P, _I, _I]),
     "kvc_prefill_context": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, ctypes.c_float, _I, _P, _SZ, _P]),
     "kvc_read_status": (_I, [_P, ctypes.POINTER(_I), _P]),
     "kvc_set_trace_events": (_I, [_P, _P, _P]),

@@ -232,8 +232,8 @@ class KVCache:
                                                ctypes.c_void_p(_stream_ptr(stream))), "kvc_prefill_attention")
         return out
 
-    def prefill_context_workspace(self, batch: int) -> torch.Tensor:
-        nbytes = self.lib.kvc_prefill_context_workspace_bytes(self.handle, batch)
+    def prefill_context_workspace(self, batch: int, n: int) -> torch.Tensor:
+        nbytes = self.lib.kvc_prefill_context_workspace_bytes(self.handle, batch, n)
         raw = torch.empty(nbytes + 256, dtype=torch.uint8, device=self.device)
         return raw[(-raw.data_ptr()) % 256:][:nbytes]
 
@@ -241,7 +241,8 @@ class KVCache:
                         sm_scale: float | None = None, accumulate_h2o: bool = True, workspace=None, stream=None):
         """A prompt on sequences that may hold context: q bf16 [batch, Hq, n,
         128], k/v bf16 [batch, Hkv, n, 128] -> bf16 [batch, Hq, n, 128]; each
-        prompt query attends causally to the compressed cache."""
+        prompt query attends causally to the compressed cache (the workspace,
+        if given, from prefill_context_workspace(batch, n))."""
         _need(q, torch.bfloat16, "q", self.device)
         _need(k, torch.bfloat16, "k", self.device)
         _need(v, torch.bfloat16, "v", self.device)
@@ -253,7 +254,7 @@ class KVCache:
         if out is None:
             out = torch.empty_like(q)
         _need(out, torch.bfloat16, "out", self.device, q.shape)
-        ws = self.prefill_context_workspace(batch) if workspace is None else workspace
+        ws = self.prefill_context_workspace(batch, n) if workspace is None else workspace
         _need(ws, torch.uint8, "workspace", self.device)
         scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
         L.check(self.lib.kvc_prefill_context(self.handle, seq_begin, batch, n, ctypes.c_void_p(q.data_ptr()),

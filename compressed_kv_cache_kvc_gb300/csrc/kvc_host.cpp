@@ -758,10 +758,26 @@ kvc_status kvc_prefill_attention(kvc_cache* c, int32_t seq_begin, int32_t batch,
   return KVC_OK;
 }
 
-size_t kvc_prefill_context_workspace_bytes(const kvc_cache* c, int32_t batch) {
-  if (!c || batch <= 0) return 0;
-  const size_t qb = align_up((size_t)batch * c->cfg.num_q_heads * kvc::kHeadDim * 2);
-  return ws_layout(c, batch).total + align_up((size_t)batch * 8) + 2 * qb;
+// Workspace of kvc_prefill_context: per (sequence, KV head) the row
+// statistics of its n * G attention rows, one row of column sums per CTA of
+// the multi-query kernel (sinks first, then every pool slot), a ticket.
+struct CtxWs {
+  size_t stats, colsum, ticket, total;
+};
+CtxWs ctx_ws(const kvc_cache* c, int32_t batch, int32_t n) {
+  const size_t pairs = (size_t)batch * c->cfg.num_kv_heads;
+  const int G = c->cfg.num_q_heads / c->cfg.num_kv_heads;
+  CtxWs w;
+  w.stats = 0;
+  w.colsum = align_up(pairs * n * G * 2 * 4);
+  w.ticket = w.colsum + align_up(pairs * kvc::ctx_groups(n, G) * (kvc::kSinks + (size_t)s_cap(c)) * 4);
+  w.total = w.ticket + align_up(pairs * 4);
+  return w;
+}
+
+size_t kvc_prefill_context_workspace_bytes(const kvc_cache* c, int32_t batch, int32_t n) {
+  if (!c || batch <= 0 || n <= 0) return 0;
+  return ctx_ws(c, batch, n).total;
 }
 
 kvc_status kvc_prefill_context(kvc_cache* c, int32_t seq_begin, int32_t batch, int32_t n, const void* d_q,
@@ -775,58 +791,25 @@ kvc_status kvc_prefill_context(kvc_cache* c, int32_t seq_begin, int32_t batch, i
     return KVC_ERR_INVALID_ARG;
   if (!(sm_scale > 0.0f) || !std::isfinite(sm_scale)) return KVC_ERR_INVALID_ARG;
   if (!d_workspace || !aligned(d_workspace, kAlign) ||
-      workspace_bytes < kvc_prefill_context_workspace_bytes(c, batch))
+      workspace_bytes < kvc_prefill_context_workspace_bytes(c, batch, n))
     return KVC_ERR_INVALID_ARG;
-  if (batch > kvc::kMaxCallBatch) return KVC_ERR_UNSUPPORTED;
   if (c->cfg.bf16_window > 0) return KVC_ERR_UNSUPPORTED;  // the causal limit is a slot count only without a window
-  const WsLayout wl = ws_layout(c, batch);
-  uint8_t* ws = static_cast<uint8_t*>(d_workspace);
-  int32_t* base = reinterpret_cast<int32_t*>(ws + wl.total);
-  uint16_t* qbuf = reinterpret_cast<uint16_t*>(ws + wl.total + align_up((size_t)batch * 8));
-  uint16_t* obuf = qbuf + align_up((size_t)batch * c->cfg.num_q_heads * kvc::kHeadDim * 2) / 2;
-  std::vector<int32_t> s0(batch), p0(batch);
-  for (int i = 0; i < batch; ++i) {
-    s0[i] = c->slots[seq_begin + i];
-    p0[i] = c->pos[seq_begin + i];
-  }
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if ((long long)n * c->cfg.num_q_heads > (1LL << 30)) return KVC_ERR_UNSUPPORTED;
   kvc_status st0 = kvc_quantize_append(c, seq_begin, batch, n, d_k, d_v, stream);
   if (st0 != KVC_OK) return st0;
   int launches = c->last_launches;
-  std::vector<int32_t> sf(c->slots.begin() + seq_begin, c->slots.begin() + seq_begin + batch);
-  std::vector<int32_t> pf(c->pos.begin() + seq_begin, c->pos.begin() + seq_begin + batch);
-  const float qk_scale_log2 = sm_scale * 1.4426950408889634f;
-  const bool h2o = (flags & KVC_ATTN_ACCUM_H2O) != 0;
-  const uint16_t* q = static_cast<const uint16_t*>(d_q);
-  uint16_t* out = static_cast<uint16_t*>(d_out);
-  for (int i = 0; i <= n && st0 == KVC_OK; ++i) {
-    if (kvc::launch_ctx_step(c->dev, seq_begin, batch, n, i, base, q, qbuf, obuf, out, st) != cudaSuccess) {
-      st0 = KVC_ERR_CUDA;
-      break;
-    }
-    ++launches;
-    if (i == n) break;
-    // the host mirror follows the lengths query i sees (the attention's grid)
-    for (int j = 0; j < batch; ++j) {
-      c->slots[seq_begin + j] = s0[j] + std::max(0, p0[j] + i + 1 - std::max(p0[j], kvc::kSinks));
-      c->pos[seq_begin + j] = p0[j] + i + 1;
-    }
-    kvc::AttnWork w;
-    long long total_pages = 0;
-    attention_plan(c, seq_begin, batch, d_workspace, &w, &total_pages);
-    st0 = launch_split_traced(c, seq_begin, batch, qbuf, qk_scale_log2, w, h2o, total_pages, st, &launches);
-    if (st0 == KVC_OK &&
-        kvc::launch_attention_merge(c->dev, seq_begin, batch, qbuf, obuf, qk_scale_log2, w, h2o, st) != cudaSuccess)
-      st0 = KVC_ERR_CUDA;
-    ++launches;
+  const CtxWs wl = ctx_ws(c, batch, n);
+  uint8_t* ws = static_cast<uint8_t*>(d_workspace);
+  if (kvc::launch_ctx_attention(c->dev, seq_begin, batch, n, static_cast<const uint16_t*>(d_q),
+                                static_cast<uint16_t*>(d_out), reinterpret_cast<float*>(ws + wl.stats),
+                                reinterpret_cast<float*>(ws + wl.colsum), reinterpret_cast<int*>(ws + wl.ticket),
+                                s_cap(c), sm_scale * 1.4426950408889634f, (flags & KVC_ATTN_ACCUM_H2O) != 0,
+                                static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    c->last_launches = launches;
+    return KVC_ERR_CUDA;
   }
-  for (int j = 0; j < batch; ++j) {  // the last pass put the device lengths back where the append left them
-    c->slots[seq_begin + j] = sf[j];
-    c->pos[seq_begin + j] = pf[j];
-  }
-  c->plan_pending = false;
-  c->last_launches = launches;
-  return st0;
+  c->last_launches = launches + 2;
+  return KVC_OK;
 }
 
 kvc_status kvc_read_status(kvc_cache* c, int32_t* h_status, void* stream) {

@@ -167,11 +167,16 @@ cudaError_t launch_prefill(const DevState& s, int seq_begin, int batch, int n, c
                            cudaStream_t st);
 
 // A prompt on sequences with context (kvc_prefill_context), after its
-// append: per prompt query i the lengths that query may see (pass 0 keeps the
-// lengths from before the prompt in base[batch][2]), query i gathered into
-// qbuf, the previous output scattered; pass n restores the appended lengths.
-cudaError_t launch_ctx_step(const DevState& s, int seq_begin, int batch, int n, int i, int32_t* base,
-                            const uint16_t* q, uint16_t* qbuf, const uint16_t* obuf, uint16_t* out, cudaStream_t st);
+// append: the multi-query attention over the compressed cache in two
+// launches (row statistics; outputs, column sums and, with `accumulate`, the
+// scores).  stats: [batch * hkv][n * group][2] floats; colsum: [batch * hkv]
+// [ctx_groups][4 + s_cap] floats; ticket: [batch * hkv] ints.
+constexpr int kCtxBtStage = 2048;   // block-table entries staged in shared memory
+constexpr int kMaxCtxGroups = 64;   // CTAs per (sequence, KV head)
+int ctx_groups(int n, int group);
+cudaError_t launch_ctx_attention(const DevState& s, int seq_begin, int batch, int n, const uint16_t* q,
+                                 uint16_t* out, float* stats, float* colsum, int* ticket, int s_cap,
+                                 float qk_scale_log2, bool accumulate, cudaStream_t st);
 
 // Fused merge + H2O scores + selection + compaction (kvc_decode_step).
 struct StepArgs {

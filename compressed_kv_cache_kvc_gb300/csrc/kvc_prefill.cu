@@ -27,9 +27,7 @@
 // or bf16 window).
 //
 // A prompt over sequences that already hold context (kvc_prefill_context)
-// attends to the compressed cache instead: each of its queries runs through
-// the decode attention kernels, and ctx_step_kernel, between the passes,
-// sets the lengths that query may see and moves its input and output.
+// attends to the compressed cache instead (kvc_context.cu).
 #include <cuda_bf16.h>
 
 #include "kvc_device.h"
@@ -362,57 +360,7 @@ __global__ void __launch_bounds__(kPfThreads) prefill_scores_kernel(DevState s, 
   }
 }
 
-// A prompt appended to sequences that already hold context, one query at a
-// time through the decode attention.  Launched after the append, with
-// ctx_step_kernel(i) for i = 0..n: it sets each sequence's lengths to what
-// prompt query i may see (the context and prompt tokens 0..i: without a bf16
-// window the prompt's pool tokens are the pool's last slots, in order, so the
-// causal limit is a slot count), gathers query i into a contiguous
-// [batch][Hq][128] buffer and scatters the previous query's output; i == n
-// only scatters, and leaves the lengths where the append put them.  Pass 0
-// derives the lengths from before the prompt from those after the append and
-// keeps them in base[batch][2] for the later passes.
-__global__ void ctx_step_kernel(DevState s, int seq_begin, int n, int i, int32_t* __restrict__ base,
-                                const uint16_t* __restrict__ q, uint16_t* __restrict__ qbuf,
-                                const uint16_t* __restrict__ obuf, uint16_t* __restrict__ out) {
-  const int bl = blockIdx.x;
-  const int b = seq_begin + bl;
-  const int hq = s.hq;
-  if (threadIdx.x == 0) {
-    int S0, P0;
-    if (i == 0) {
-      const int Sf = s.seq_slots[b], Pf = s.seq_pos[b];
-      P0 = Pf - n;
-      S0 = Sf - max(0, Pf - max(P0, kSinks));
-      base[2 * bl] = S0;
-      base[2 * bl + 1] = P0;
-    } else {
-      S0 = base[2 * bl];
-      P0 = base[2 * bl + 1];
-    }
-    const int p = min(P0 + i + 1, P0 + n);
-    s.seq_slots[b] = S0 + max(0, p - max(P0, kSinks));
-    s.seq_pos[b] = p;
-  }
-  for (int c = threadIdx.x; c < hq * (kHeadDim / 8); c += blockDim.x) {
-    const size_t row = (size_t)bl * hq + c / (kHeadDim / 8);
-    const int ch = c % (kHeadDim / 8);
-    if (i < n)
-      reinterpret_cast<uint4*>(qbuf + row * kHeadDim)[ch] =
-          reinterpret_cast<const uint4*>(q + (row * n + i) * kHeadDim)[ch];
-    if (i > 0)
-      reinterpret_cast<uint4*>(out + (row * n + i - 1) * kHeadDim)[ch] =
-          reinterpret_cast<const uint4*>(obuf + row * kHeadDim)[ch];
-  }
-}
-
 }  // namespace
-
-cudaError_t launch_ctx_step(const DevState& s, int seq_begin, int batch, int n, int i, int32_t* base,
-                            const uint16_t* q, uint16_t* qbuf, const uint16_t* obuf, uint16_t* out, cudaStream_t st) {
-  ctx_step_kernel<<<batch, 256, 0, st>>>(s, seq_begin, n, i, base, q, qbuf, obuf, out);
-  return cudaGetLastError();
-}
 
 int prefill_fwd_smem_bytes() { return (int)sizeof(PfFwdSmem); }
 int prefill_scores_smem_bytes() { return (int)sizeof(PfScoreSmem); }

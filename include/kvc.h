@@ -387,22 +387,30 @@ kvc_status kvc_prefill_attention(kvc_cache* cache, int32_t seq_begin, int32_t ba
  * seen before) attends, as a decode step does, to every held token at a
  * position <= P + i in its stored form (sinks bf16, pool tokens dequantised),
  * and with KVC_ATTN_ACCUM_H2O adds its probabilities to their H2O scores (the
- * survey's prefill over the compressed pool).  Runs as n passes of the decode
- * attention (a small step kernel, the split kernel, the merge kernel each),
- * so its cost grows with n times the context: for fresh prompts
- * kvc_prefill_attention is the fast path.
+ * survey's prefill over the compressed pool: "KV cache eviction and reuse
+ * survey" 3.3, cumulative attention from the later tokens; Technical Report
+ * 3.4, column sums of the attention matrix).  Because the prompt's own pool
+ * tokens are the last pool slots, what query i sees is the sinks up to its
+ * position and a prefix of the pool: the causal mask shifted by the context.
+ * Three launches: the append, then a multi-query kernel in two passes (the
+ * row maxima and sums; the outputs and per-CTA column sums, the last CTA of
+ * each (sequence, KV head) adding them, in a fixed order, to the scores).
+ * Every pool page is read once per pass per tile of 64 attention rows (query
+ * x query head of the group); tensor cores, the codes entering the MMA as in
+ * kvc_decode_attention.
  *   d_q:   bf16 [batch][Hq][n][128];  d_k, d_v: bf16 [batch][Hkv][n][128];
  *   d_out: bf16 [batch][Hq][n][128];  all device memory, 16-byte aligned,
  *   owned by the caller; flags 0 or KVC_ATTN_ACCUM_H2O; d_workspace:
- *   kvc_prefill_context_workspace_bytes(cache, batch) bytes, 256-byte
- *   aligned (scratch for the duration of the call, stream-ordered).
- * The trace events (kvc_set_trace_events) bracket each pass's split kernel.
+ *   kvc_prefill_context_workspace_bytes(cache, batch, n) bytes, 256-byte
+ *   aligned (scratch for the duration of the call, stream-ordered: per
+ *   (sequence, KV head) the n * G row statistics and up to 64 rows of
+ *   column sums over 4 + max_blocks_per_seq * 16 tokens).
  * Errors, before any launch: KVC_ERR_INVALID_ARG (range, n <= 0, flags,
  * sm_scale not positive and finite, pointers, workspace);
  * KVC_ERR_CAPACITY as kvc_quantize_append; KVC_ERR_UNSUPPORTED with a bf16
- * window (bf16_window > 0) or batch > 1024.  KVC_ERR_CUDA when a launch
- * fails part-way: the slice's lengths on the device are then undefined. */
-size_t kvc_prefill_context_workspace_bytes(const kvc_cache* cache, int32_t batch);
+ * window (bf16_window > 0) or n * Hq > 2^30.  KVC_ERR_CUDA when a launch
+ * fails; the lengths then already include the appended prompt. */
+size_t kvc_prefill_context_workspace_bytes(const kvc_cache* cache, int32_t batch, int32_t n);
 kvc_status kvc_prefill_context(kvc_cache* cache, int32_t seq_begin, int32_t batch, int32_t n, const void* d_q,
                                const void* d_k, const void* d_v, void* d_out, float sm_scale, int32_t flags,
                                void* d_workspace, size_t workspace_bytes, void* stream);
@@ -427,8 +435,9 @@ const char* kvc_status_string(kvc_status status);
 
 /* Library version: major * 10000 + minor * 100 + patch.  A caller built
  * against this header checks kvc_version() == KVC_VERSION before passing
- * structures (kvc_config grew in 0.2: bf16_window, codes). */
-#define KVC_VERSION 200
+ * structures (kvc_config grew in 0.2: bf16_window, codes;
+ * kvc_prefill_context_workspace_bytes took the prompt length in 0.3). */
+#define KVC_VERSION 300
 int32_t kvc_version(void);
 
 #ifdef __cplusplus

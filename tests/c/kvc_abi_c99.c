@@ -55,7 +55,7 @@ int main(void) {
   CHECK(kvc_cache_lengths(cache, 0, &slots, &pos) == KVC_OK && slots == 0 && pos == 0);
   ws = kvc_workspace_bytes(cache, 1);
   CHECK(ws > 0);
-  CHECK(kvc_prefill_context_workspace_bytes(cache, 1) > ws);
+  CHECK(kvc_prefill_context_workspace_bytes(cache, 1, 8) > 0);
   /* validation before any launch (4 pages of 16 slots hold 68 tokens) */
   CHECK(kvc_quantize_append(cache, 1, 2, 1, state, state, NULL) == KVC_ERR_INVALID_ARG);
   CHECK(kvc_quantize_append(cache, 0, 1, 0, NULL, NULL, NULL) == KVC_OK);

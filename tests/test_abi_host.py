@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_version_and_strings(lib):
     L = lib.lib()
-    assert L.kvc_version() == lib.KVC_VERSION == 200
+    assert L.kvc_version() == lib.KVC_VERSION == 300
     assert L.kvc_status_string(lib.KVC_ERR_CAPACITY) == b"out of cache capacity"
 
 
@@ -182,19 +182,21 @@ def test_prefill_context_validation(lib):
     st, h, fs = _create(lib, _cfg(lib, num_blocks=3, max_blocks_per_seq=2))
     assert st == lib.KVC_OK
     dummy = ctypes.c_void_p(fs.ptr.value)
-    ws = L.kvc_prefill_context_workspace_bytes(h, 1)
-    assert ws > L.kvc_workspace_bytes(h, 1)
-    assert L.kvc_prefill_context_workspace_bytes(None, 1) == 0 and L.kvc_prefill_context_workspace_bytes(h, 0) == 0
-    wsbuf = ctypes.create_string_buffer(ws + 512)
+    ws = L.kvc_prefill_context_workspace_bytes(h, 1, 5)
+    ws37 = L.kvc_prefill_context_workspace_bytes(h, 1, 37)
+    assert 0 < ws < ws37  # the row statistics grow with the prompt
+    assert L.kvc_prefill_context_workspace_bytes(None, 1, 5) == 0
+    assert L.kvc_prefill_context_workspace_bytes(h, 0, 5) == 0 and L.kvc_prefill_context_workspace_bytes(h, 1, 0) == 0
+    wsbuf = ctypes.create_string_buffer(ws37 + 512)
     wsp = ctypes.c_void_p(ctypes.addressof(wsbuf) + (-ctypes.addressof(wsbuf)) % 256)
 
-    def call(handle=h, seq_begin=0, batch=1, n=5, scale=0.088, flags=1, nbytes=ws):
+    def call(handle=h, seq_begin=0, batch=1, n=5, scale=0.088, flags=1, nbytes=ws37):
         return L.kvc_prefill_context(handle, seq_begin, batch, n, dummy, dummy, dummy, dummy, ctypes.c_float(scale),
                                      flags, wsp, nbytes, None)
 
     assert call(handle=None) == lib.KVC_ERR_INVALID_ARG
     for kw in [dict(seq_begin=1, batch=2), dict(n=0), dict(flags=4), dict(scale=-1.0), dict(scale=float("inf")),
-               dict(nbytes=ws - 1)]:
+               dict(nbytes=ws - 1), dict(n=37, nbytes=ws37 - 1)]:
         assert call(**kw) == lib.KVC_ERR_INVALID_ARG, kw
     assert call(n=37) == lib.KVC_ERR_CAPACITY  # 4 sinks + 33 slots need 3 pages > 2
     assert L.kvc_last_launch_count(h) == 0
@@ -205,7 +207,7 @@ def test_prefill_context_validation(lib):
     st, h, fs = _create(lib, _cfg(lib, num_blocks=3, max_blocks_per_seq=2, bf16_window=16))
     assert st == lib.KVC_OK
     dummy = ctypes.c_void_p(fs.ptr.value)
-    assert call(handle=h, nbytes=L.kvc_prefill_context_workspace_bytes(h, 1)) == lib.KVC_ERR_UNSUPPORTED
+    assert call(handle=h, nbytes=L.kvc_prefill_context_workspace_bytes(h, 1, 5)) == lib.KVC_ERR_UNSUPPORTED
     L.kvc_cache_destroy(h)
 
 
