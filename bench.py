@@ -817,10 +817,49 @@ def workload_report(args, name: str):
             ev1.synchronize()
             per_step.append(ev0.elapsed_time(ev1))
         tot = sum(per_step)
-        line["consecutive_steps"] = {"steps": w.steps, "launch": "eager", "ms_total": tot,
-                                     "kv_bytes": total_bytes, "gbs": total_bytes / (tot * 1e-3) / 1e9,
-                                     "ms_first": per_step[0], "ms_median_later": float(np.median(per_step[1:])),
-                                     "seq_steps_per_s": B * w.steps / (tot * 1e-3)}
+        line["consecutive_steps_eager"] = {"steps": w.steps, "launch": "eager", "ms_total": tot,
+                                           "kv_bytes": total_bytes, "gbs": total_bytes / (tot * 1e-3) / 1e9,
+                                           "ms_first": per_step[0],
+                                           "ms_median_later": float(np.median(per_step[1:])),
+                                           "seq_steps_per_s": B * w.steps / (tot * 1e-3)}
+        # the same steps from CUDA graphs: the first step (hundreds of rows
+        # move per pair) replays the first-step graph, then one graph captured
+        # at the steady state (one token evicted and at most one row moved per
+        # pair: no move kernel) is replayed for the remaining steps, all
+        # back to back between two events
+        restore()
+        with torch.cuda.stream(stream):
+            step()  # step 1 eagerly, so the steady graph is captured at step-2 lengths
+        torch.cuda.synchronize()
+        steady = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(steady, stream=stream):
+            step()
+        torch.cuda.synchronize()
+        launches_steady = sum(c.last_launch_count() for c in caches)
+        reps = []
+        for _ in range(max(1, min(args.steps, 5))):
+            restore()
+            with torch.cuda.stream(stream):
+                ev0.record(stream)
+                graph.replay()
+                ev_mid = torch.cuda.Event(enable_timing=True)
+                ev_mid.record(stream)
+                for _ in range(w.steps - 1):
+                    steady.replay()
+                ev1.record(stream)
+            ev1.synchronize()
+            reps.append((ev0.elapsed_time(ev1), ev_mid.elapsed_time(ev1)))
+        for c in caches:
+            c.sync_host()
+        tot_g = float(np.median([r[0] for r in reps]))
+        later = float(np.median([r[1] for r in reps]))
+        line["consecutive_steps"] = {"steps": w.steps, "launch": "cuda graphs", "ms_total": tot_g,
+                                     "kv_bytes": total_bytes, "gbs": total_bytes / (tot_g * 1e-3) / 1e9,
+                                     "frac_of_peak": total_bytes / (tot_g * 1e-3) / 1e9 / peak,
+                                     "ms_later_steps": later,
+                                     "us_per_layer_steady": later * 1e3 / ((w.steps - 1) * layers),
+                                     "launches_per_layer_steady": launches_steady / layers,
+                                     "seq_steps_per_s": B * w.steps / (tot_g * 1e-3), "repetitions": len(reps)}
         for c in caches:
             st = c.read_status()
             if st:

@@ -696,6 +696,10 @@ kvc_status kvc_decode_step(kvc_cache* c, int32_t seq_begin, int32_t batch, const
   a.g_keys = reinterpret_cast<uint32_t*>(ws + wl.keys);
   a.g_pos = reinterpret_cast<int32_t*>(ws + wl.pos);
   a.n_moves = reinterpret_cast<int*>(ws + wl.moves);
+  int max_moves = 0;  // a pair moves at most min(n', S - n') rows
+  for (int i = 0; i < batch; ++i)
+    max_moves = std::max(max_moves, std::min(plan[i], c->slots[seq_begin + i] - plan[i]));
+  a.inline_moves = !block && max_moves <= kvc::kInlineMoves;
   if (kvc::launch_step_post(c->dev, seq_begin, batch, static_cast<const uint16_t*>(d_q),
                             static_cast<uint16_t*>(d_out), qk_scale_log2, w, a, sm_count(c), st) != cudaSuccess)
     return KVC_ERR_CUDA;
@@ -714,11 +718,11 @@ kvc_status kvc_decode_step(kvc_cache* c, int32_t seq_begin, int32_t batch, const
     c->last_launches = launches;
     return KVC_OK;
   }
-  int max_moves = 0;  // a pair moves at most min(n', S - n') rows
-  for (int i = 0; i < batch; ++i)
-    max_moves = std::max(max_moves, std::min(plan[i], c->slots[seq_begin + i] - plan[i]));
-  if (kvc::launch_step_moves(c->dev, batch, a, sm_count(c), max_moves, st) != cudaSuccess) return KVC_ERR_CUDA;
-  launches += 2;
+  if (!a.inline_moves) {
+    if (kvc::launch_step_moves(c->dev, batch, a, sm_count(c), max_moves, st) != cudaSuccess) return KVC_ERR_CUDA;
+    ++launches;
+  }
+  ++launches;
   for (int i = 0; i < batch; ++i) c->slots[seq_begin + i] = plan[i];
   c->plan_pending = false;
   c->last_launches = launches;

@@ -187,7 +187,11 @@ struct StepArgs {
   uint32_t* g_keys;     // global fallback [batch][hkv][s_cap]; then the hole list
   int32_t* g_pos;       // likewise; then the source list
   int* n_moves;         // [batch][hkv] list lengths (post kernel -> move kernel)
+  int inline_moves;     // the post kernel moves the rows itself (no move kernel follows)
 };
+// Pairs that move at most this many rows are moved inside the post kernel
+// (the steady state moves one row per pair).
+constexpr int kInlineMoves = 32;
 cudaError_t launch_step_post(const DevState& s, int seq_begin, int batch, const uint16_t* q, uint16_t* out,
                              float qk_scale_log2, const AttnWork& w, const StepArgs& a, int sm_count,
                              cudaStream_t st);

@@ -17,7 +17,9 @@
 // step_moves_kernel, one CTA per (KV head, sequence): the row moves of the
 // lists.  Moves run in a launch of their own because, sharing an SM with
 // another CTA's selection phase, their global-memory traffic stalls that
-// phase's shared-memory work.
+// phase's shared-memory work; when no pair moves more than kInlineMoves rows
+// (the steady state moves one), the post kernel moves them and the move
+// kernel is not launched.
 //
 // (Technical Report: KV Cache Compression for Text-Only LLMs, sections 3.3
 // and 3.4; "KV Cache optimization techniques" sections 2.2, 2.4 and 3.2.)
@@ -279,6 +281,12 @@ __global__ void __launch_bounds__(NT, 1024 / NT) step_post_kernel(DevState s, in
   }
 
   if (threadIdx.x == 0) a.n_moves[pair] = lists_ok ? hole_base : 0;
+  if (a.inline_moves && lists_ok && hole_base > 0) {
+    // few rows (no move kernel follows): this CTA moves them (the lists are
+    // this CTA's own writes, visible after the barrier)
+    __syncthreads();
+    move_rows(s, holes, srcs, hole_base);
+  }
 
   } else if (threadIdx.x == 0) {
     a.n_moves[pair] = 0;

@@ -120,7 +120,9 @@ def _full_size(name, steps, with_step):
         if with_step:
             sout = stepper.decode_step(T.to_dev_bf16(s["q"]), T.to_dev_bf16(s["k_new"]), T.to_dev_bf16(s["v_new"]),
                                        mode=w.mode, budget=w.budget, recent=w.recent, window=w.window)
-            assert stepper.last_launch_count() == 4
+            # the first step moves hundreds of rows per pair (a move kernel); later
+            # steps move one (inside the post kernel)
+            assert stepper.last_launch_count() == (4 if step == 0 else 3)
         cache.quantize_append(T.to_dev_bf16(s["k_new"]), T.to_dev_bf16(s["v_new"]))
         out = cache.decode_attention(T.to_dev_bf16(s["q"]), accumulate_h2o=h2o)
         gpu = T.bf16_tensor_to_f32(out)

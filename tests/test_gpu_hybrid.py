@@ -140,7 +140,7 @@ def test_hybrid_step_equals_separate_calls(bits, hq, hkv, lengths, W, mode, budg
         vn = T.to_dev_bf16(_bits(rng, (B, hkv, 1, 128)))
         oa = ca.step(q, kn, vn, mode=mode, budget=budget, recent=recent, window=window)
         ob = cb.decode_step(q, kn, vn, mode=mode, budget=budget, recent=recent, window=window)
-        assert cb.last_launch_count() == 5  # append, split, window, post, moves
+        assert cb.last_launch_count() in (4, 5)  # append, split, window, post (+ moves when > 32 rows)
         torch.cuda.synchronize()
         assert torch.equal(oa, ob)
         _same_hybrid_state(ca, cb)

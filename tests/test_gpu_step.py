@@ -76,7 +76,7 @@ def test_step_equals_separate_calls(bits, hq, hkv, lengths, mode, budget, recent
         vn = T.to_dev_bf16(_bits(rng, (B, hkv, 1, 128)))
         oa = ca.step(q, kn, vn, mode=mode, budget=budget, recent=recent, window=window)
         ob = cb.decode_step(q, kn, vn, mode=mode, budget=budget, recent=recent, window=window)
-        assert cb.last_launch_count() == 4
+        assert cb.last_launch_count() in (3, 4)  # the move kernel only when a pair moves > 32 rows
         torch.cuda.synchronize()
         assert torch.equal(oa, ob)
         _same_state(ca, cb)
@@ -304,6 +304,35 @@ def test_checkpoint_to_host_and_resume_in_another_arena():
         q, kn, vn = inputs()
         oa = ca.decode_step(q, kn, vn, mode="h2o", budget=budget, recent=recent)
         ob = cb.decode_step(q, kn, vn, mode="h2o", budget=budget, recent=recent)
+        torch.cuda.synchronize()
+        assert torch.equal(oa, ob)
+        _same_state(ca, cb)
+    assert ca.read_status() == 0 and cb.read_status() == 0
+
+
+@pytest.mark.parametrize("length,budget,first_launches", [(600, 180, 4), (200, 190, 3)])
+def test_step_moves_inline_or_in_their_own_kernel(length, budget, first_launches):
+    """Pairs that move at most 32 rows have them moved by the post kernel (no
+    move kernel: 3 launches), more take the move kernel (4 launches); either
+    way the outputs and the cache equal those of the separate calls, step
+    after step (the second step evicts one token: inline)."""
+    from compressed_kv_cache_kvc_gb300.cache import KVCache
+    rng = np.random.default_rng(length + budget)
+    hq, hkv, B = 16, 4, 2
+    mbps = (length + 3 + 15) // 16 + 2
+    ca = KVCache(hq, hkv, 8, B * mbps, B, mbps)
+    cb = KVCache(hq, hkv, 8, B * mbps, B, mbps)
+    k = _bits(rng, (B, hkv, length, 128))
+    v = _bits(rng, (B, hkv, length, 128))
+    for c in (ca, cb):
+        c.quantize_append(T.to_dev_bf16(k), T.to_dev_bf16(v))
+    for step in range(3):
+        q = T.to_dev_bf16(_bits(rng, (B, hq, 128)))
+        kn = T.to_dev_bf16(_bits(rng, (B, hkv, 1, 128)))
+        vn = T.to_dev_bf16(_bits(rng, (B, hkv, 1, 128)))
+        oa = ca.step(q, kn, vn, mode="h2o", budget=budget, recent=24)
+        ob = cb.decode_step(q, kn, vn, mode="h2o", budget=budget, recent=24)
+        assert cb.last_launch_count() == (first_launches if step == 0 else 3)
         torch.cuda.synchronize()
         assert torch.equal(oa, ob)
         _same_state(ca, cb)
