@@ -101,29 +101,31 @@ template <int BITS>
 __device__ __forceinline__ void copy_codes(bool pred, uint32_t sb, const uint32_t (&d)[Geom<BITS>::kCopies],
                                            const uint8_t* gK, const uint8_t* gV) {
   constexpr int kV = Geom<BITS>::kV;
+  const uint64_t pol = l2_evict_first();
   if (BITS == 8) {
     asm volatile(
         "{\n .reg .pred q;\n setp.ne.u32 q, %7, 0;\n"
-        " @q cp.async.cg.shared.global [%0], [%4], 16;\n"
-        " @q cp.async.cg.shared.global [%1], [%4+512], 16;\n"
-        " @q cp.async.cg.shared.global [%2], [%4+1024], 16;\n"
-        " @q cp.async.cg.shared.global [%3], [%4+1536], 16;\n"
-        " @q cp.async.cg.shared.global [%0+%6], [%5], 16;\n"
-        " @q cp.async.cg.shared.global [%1+%6], [%5+512], 16;\n"
-        " @q cp.async.cg.shared.global [%2+%6], [%5+1024], 16;\n"
-        " @q cp.async.cg.shared.global [%3+%6], [%5+1536], 16;\n}\n" ::"r"(sb + d[0]),
+        " @q cp.async.cg.shared.global.L2::cache_hint [%0], [%4], 16, %8;\n"
+        " @q cp.async.cg.shared.global.L2::cache_hint [%1], [%4+512], 16, %8;\n"
+        " @q cp.async.cg.shared.global.L2::cache_hint [%2], [%4+1024], 16, %8;\n"
+        " @q cp.async.cg.shared.global.L2::cache_hint [%3], [%4+1536], 16, %8;\n"
+        " @q cp.async.cg.shared.global.L2::cache_hint [%0+%6], [%5], 16, %8;\n"
+        " @q cp.async.cg.shared.global.L2::cache_hint [%1+%6], [%5+512], 16, %8;\n"
+        " @q cp.async.cg.shared.global.L2::cache_hint [%2+%6], [%5+1024], 16, %8;\n"
+        " @q cp.async.cg.shared.global.L2::cache_hint [%3+%6], [%5+1536], 16, %8;\n}\n" ::"r"(sb + d[0]),
         "r"(sb + d[1 % Geom<BITS>::kCopies]), "r"(sb + d[2 % Geom<BITS>::kCopies]),
-        "r"(sb + d[3 % Geom<BITS>::kCopies]), "l"(gK), "l"(gV), "n"(kV), "r"((uint32_t)pred));
+        "r"(sb + d[3 % Geom<BITS>::kCopies]), "l"(gK), "l"(gV), "n"(kV), "r"((uint32_t)pred), "l"(pol));
   } else {
     asm volatile(
         "{\n .reg .pred q;\n setp.ne.u32 q, %5, 0;\n"
-        " @q cp.async.cg.shared.global [%0], [%2], 16;\n"
-        " @q cp.async.cg.shared.global [%1], [%2+512], 16;\n"
-        " @q cp.async.cg.shared.global [%0+%4], [%3], 16;\n"
-        " @q cp.async.cg.shared.global [%1+%4], [%3+512], 16;\n}\n" ::"r"(sb + d[0]),
-        "r"(sb + d[1]), "l"(gK), "l"(gV), "n"(kV), "r"((uint32_t)pred));
+        " @q cp.async.cg.shared.global.L2::cache_hint [%0], [%2], 16, %6;\n"
+        " @q cp.async.cg.shared.global.L2::cache_hint [%1], [%2+512], 16, %6;\n"
+        " @q cp.async.cg.shared.global.L2::cache_hint [%0+%4], [%3], 16, %6;\n"
+        " @q cp.async.cg.shared.global.L2::cache_hint [%1+%4], [%3+512], 16, %6;\n}\n" ::"r"(sb + d[0]),
+        "r"(sb + d[1]), "l"(gK), "l"(gV), "n"(kV), "r"((uint32_t)pred), "l"(pol));
   }
 }
+
 // FP8: the 8-bit codes are FP8 E4M3 instead of INT8 (same layout, same
 // scales; only the code -> fp16 conversion differs, and no offset).
 template <int BITS, bool FP8 = false>
@@ -353,6 +355,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
     // logits of this pair, [g][slot]; the lane writes slots (2r, 2r+1) of heads
     // 2c and 2c+1 (lanes of padding heads write nothing)
     const bool sp0 = spill && 2 * c < G, sp1 = spill && 2 * c + 1 < G;
+    const uint64_t spill_pol = l2_evict_last();
     float* lg0p = w.logits + ((size_t)pair * G + (sp0 ? 2 * c : 0)) * w.s_cap + 2 * r;
     float* lg1p = w.logits + ((size_t)pair * G + (sp1 ? 2 * c + 1 : 0)) * w.s_cap + 2 * r;
 
@@ -444,8 +447,8 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
         lg[pp][1] = v0[pp] ? acc[pp][1] * (skv[pp].x * cq1) : -INFINITY;  // slot 2r,   head 2c+1
         lg[pp][2] = v1[pp] ? acc[pp][2] * (skv[pp].y * cq0) : -INFINITY;  // slot 2r+1, head 2c
         lg[pp][3] = v1[pp] ? acc[pp][3] * (skv[pp].y * cq1) : -INFINITY;  // slot 2r+1, head 2c+1
-        st2_if(sp0, lg0p + slot0[pp], lg[pp][0], lg[pp][2]);
-        st2_if(sp1, lg1p + slot0[pp], lg[pp][1], lg[pp][3]);
+        st2_if_hint(sp0, lg0p + slot0[pp], lg[pp][0], lg[pp][2], spill_pol);
+        st2_if_hint(sp1, lg1p + slot0[pp], lg[pp][1], lg[pp][3], spill_pol);
       }
 
       // ---- lazy online softmax: reduce and rescale only when some lane's

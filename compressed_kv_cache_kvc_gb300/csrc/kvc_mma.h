@@ -25,6 +25,24 @@ __device__ __forceinline__ void cp_async16_if(bool pred, uint32_t dst, const voi
       " @q cp.async.cg.shared.global [%1], [%2], 16;\n}\n" ::"r"((uint32_t)pred),
       "r"(dst), "l"(src));
 }
+__device__ __forceinline__ uint64_t l2_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// Two floats to global memory only when `pred`, kept in L2 by `policy`.
+__device__ __forceinline__ void st2_if_hint(bool pred, float* dst, float a, float b, uint64_t policy) {
+  asm volatile(
+      "{\n .reg .pred q;\n setp.ne.u32 q, %0, 0;\n"
+      " @q st.global.L2::cache_hint.v2.f32 [%1], {%2, %3}, %4;\n}\n" ::"r"((uint32_t)pred),
+      "l"(dst), "f"(a), "f"(b), "l"(policy)
+      : "memory");
+}
 // Two floats to global memory only when `pred` (no branch).
 __device__ __forceinline__ void st2_if(bool pred, float* dst, float a, float b) {
   asm volatile(

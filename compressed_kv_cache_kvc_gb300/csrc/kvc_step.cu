@@ -113,6 +113,8 @@ __global__ void __launch_bounds__(NT, 1024 / NT) step_post_kernel(DevState s, in
   // and scores) is issued before the first use.
   const float* lgr = w.logits + pair * G * w.s_cap;
   const int nq = (S + 3) >> 2;
+  // whole 128-byte lines of logits (rows 128-byte aligned) can be dropped
+  const bool discard_ok = (w.s_cap % 32) == 0 && ((uintptr_t)lgr % 128) == 0;
   for (int j = threadIdx.x; j < nq; j += blockDim.x) {
     const int t = 4 * j;
     const int blk = btp[t / kPage];
@@ -160,6 +162,14 @@ __global__ void __launch_bounds__(NT, 1024 / NT) step_post_kernel(DevState s, in
         for (int c = 0; c < 4; ++c)
           if (t + c < S) s.score[idx + c] = vv[c];
       }
+    }
+    if (h2o && discard_ok) {
+      // the logits of 32 slots are read once the 8 threads of their line have
+      // used them: drop those lines from L2 without writing them back
+      __syncwarp(__activemask());
+      if ((threadIdx.x & 7) == 0 && t + 32 <= S)
+        for (int g = 0; g < G; ++g)
+          asm volatile("discard.global.L2 [%0], 128;" ::"l"(lgr + (size_t)g * w.s_cap + t) : "memory");
     }
     if (block) continue;
     // slots past S in the last quarter page get keys too: nothing reads them
