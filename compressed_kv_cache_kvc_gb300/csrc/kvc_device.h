@@ -364,7 +364,20 @@ __device__ __forceinline__ void move_rows(const DevState& s, const int32_t* hole
   const int rpw = 32 / lpr;          // rows per warp instruction
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int r = lane / lpr, c = lane % lpr;
-  for (int base = warp * rpw * U; base < n_moves; base += nwarps * rpw * U) {
+  const int stride = nwarps * rpw * U;
+  // the list entries of the next round are loaded while this round's rows
+  // are in flight (one memory round trip per round instead of two)
+  uint32_t nsi[U], ndi[U];
+  auto load_lists = [&](int base) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int mi = base + u * rpw + r;
+      nsi[u] = mi < n_moves ? (uint32_t)srcs[mi] : 0xFFFFFFFFu;
+      ndi[u] = mi < n_moves ? (uint32_t)holes[mi] : 0xFFFFFFFFu;
+    }
+  };
+  load_lists(warp * rpw * U);
+  for (int base = warp * rpw * U; base < n_moves; base += stride) {
     uint4 kv[U], vv[U];
     uint32_t si[U], di[U];
     bool on[U];
@@ -372,8 +385,8 @@ __device__ __forceinline__ void move_rows(const DevState& s, const int32_t* hole
     for (int u = 0; u < U; ++u) {
       const int mi = base + u * rpw + r;
       on[u] = mi < n_moves;
-      si[u] = on[u] ? (uint32_t)srcs[mi] : 0u;
-      di[u] = on[u] ? (uint32_t)holes[mi] : 0u;
+      si[u] = nsi[u];
+      di[u] = ndi[u];
       if (on[u] && (si[u] >= nslots || di[u] >= nslots)) {
         if (c == 0) atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
         on[u] = false;
@@ -394,6 +407,7 @@ __device__ __forceinline__ void move_rows(const DevState& s, const int32_t* hole
         ps[u] = s.slot_pos[si[u]];
       }
     }
+    load_lists(base + stride);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       if (!on[u]) continue;
