@@ -99,9 +99,8 @@ struct Geom {
 // (V: + kV).
 template <int BITS>
 __device__ __forceinline__ void copy_codes(bool pred, uint32_t sb, const uint32_t (&d)[Geom<BITS>::kCopies],
-                                           const uint8_t* gK, const uint8_t* gV) {
+                                           const uint8_t* gK, const uint8_t* gV, uint64_t pol) {
   constexpr int kV = Geom<BITS>::kV;
-  const uint64_t pol = l2_evict_first();
   if (BITS == 8) {
     asm volatile(
         "{\n .reg .pred q;\n setp.ne.u32 q, %7, 0;\n"
@@ -195,6 +194,10 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
   for (int k = 0; k < 4; ++k)
     v_off[k] = Gm::kV + (BITS == 8 ? Gm::chunk_off(4 * c + k, r) : Gm::chunk_off(4 * c + k, r >> 1) + 8 * (r & 1));
   const int s_off = Gm::kKS + 8 * r;
+  // L2 policies: the KV stream is read once (evict first); the logit spill is
+  // read back by the next kernel (evict last)
+  const uint64_t kv_pol = l2_evict_first();
+  const uint64_t spill_pol = l2_evict_last();
 
   while (F < F1) {
     // ---- the (sequence, KV head) pair of page F and this CTA's run of its pages
@@ -246,7 +249,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
       stage_ok = (stage_ok & ~(1u << slot_issue)) | ((uint32_t)ok << slot_issue);
       const uint32_t sb = ring_s + slot_issue * Gm::kStage;
       const size_t off = (size_t)(uint32_t)blk * code_stride;
-      copy_codes<BITS>(ok, sb, cp_d, kb + off, vb + off);
+      copy_codes<BITS>(ok, sb, cp_d, kb + off, vb + off, kv_pol);
       cp_async16_if(ok && lane < 8, sb + sc_soff, scb + (size_t)(uint32_t)blk * sc_stride);
       cp_async_commit();
     };
@@ -355,7 +358,6 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
     // logits of this pair, [g][slot]; the lane writes slots (2r, 2r+1) of heads
     // 2c and 2c+1 (lanes of padding heads write nothing)
     const bool sp0 = spill && 2 * c < G, sp1 = spill && 2 * c + 1 < G;
-    const uint64_t spill_pol = l2_evict_last();
     float* lg0p = w.logits + ((size_t)pair * G + (sp0 ? 2 * c : 0)) * w.s_cap + 2 * r;
     float* lg1p = w.logits + ((size_t)pair * G + (sp1 ? 2 * c + 1 : 0)) * w.s_cap + 2 * r;
 

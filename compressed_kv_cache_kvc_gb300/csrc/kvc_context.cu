@@ -77,29 +77,46 @@ struct CtxArgs {
   float* colsum;      // [pairs][groups][4 + s_cap]  per-CTA column sums (sinks first)
   int* ticket;        // [pairs]
   int n, groups, s_cap;
+  int cs_row;         // 4 + s_cap + W: sinks, pool slots, window positions from rlo
   float qk_scale_log2;
   int accumulate;
 };
 
-// Lengths of sequence b after the prompt's append: the slots before it (S0),
-// the positions before it (P0), the slots now (S1).
+// Lengths of sequence b after the prompt's append: the positions before it
+// (P0) and now (P1), the pool slots now (S1).  The append moved positions
+// [a, rlo) into the pool, in position order, after the S0 slots it held
+// (a = max(4, P0 - W): with a bf16 window of W positions these are the
+// window's tokens that aged out and the prompt's own tokens that did; without
+// one, the prompt's non-sink tokens); the window holds [rlo, P1).
 struct CtxLens {
-  int S0, P0, S1;
+  int S0, P0, S1, P1, a, rlo;
 };
 __device__ __forceinline__ CtxLens ctx_lens(const DevState& s, int b, int n) {
   CtxLens l;
   l.S1 = s.seq_slots[b];
-  const int P1 = s.seq_pos[b];
-  l.P0 = P1 - n;
-  l.S0 = l.S1 - max(0, P1 - max(l.P0, kSinks));
+  l.P1 = s.seq_pos[b];
+  l.P0 = l.P1 - n;
+  l.a = max(kSinks, l.P0 - s.ring);
+  l.rlo = max(l.a, l.P1 - s.ring);
+  l.S0 = l.S1 - (l.rlo - l.a);
   return l;
 }
+// pool slots query i (position P0 + i) sees: the S0 older ones and the
+// appended ones at positions <= P0 + i
 __device__ __forceinline__ int ctx_vis(const CtxLens& l, int i) {
-  return l.S0 + max(0, l.P0 + i + 1 - max(l.P0, kSinks));
+  return l.S0 + min(max(l.P0 + i + 1 - l.a, 0), l.rlo - l.a);
 }
+// window positions query i sees: [rlo, ctx_ring_end)
+__device__ __forceinline__ int ctx_ring_end(const CtxLens& l, int i) { return min(l.P1, l.P0 + i + 1); }
+
+// One stage of the window tiles: 16 K rows and 16 V rows of 128 bf16, each
+// row padded to 272 bytes (ldmatrix reads them without bank conflicts).
+constexpr int kRingRow = 136;  // bf16 per staged row
+constexpr int kRingStage = 2 * 16 * kRingRow * 2;
 
 // PASS 0: row statistics; PASS 1: outputs and column sums.
-template <int BITS, bool FP8, int PASS>
+// WIN: the cache keeps a bf16 window (its tiles follow the pool's pages).
+template <int BITS, bool FP8, int PASS, bool WIN>
 __global__ void __launch_bounds__(kCtxThreads) ctx_attn_kernel(DevState s, int seq_begin, CtxArgs a) {
   using Gm = CtxGeom<BITS>;
   constexpr int RB = Gm::kRowBytes;
@@ -160,14 +177,16 @@ __global__ void __launch_bounds__(kCtxThreads) ctx_attn_kernel(DevState s, int s
 
   // block ids of the sequence's pages, staged once (the rounds reuse them)
   const int npages_all = (L.S1 + kPage - 1) / kPage;
-  int32_t* sbt = reinterpret_cast<int32_t*>(smem + ST * Gm::kStage);
+  constexpr int kRingBytes = WIN && 2 * kRingStage > ST * Gm::kStage ? 2 * kRingStage : ST * Gm::kStage;
+  int32_t* sbt = reinterpret_cast<int32_t*>(smem + kRingBytes);
   const int n_stage_bt = min(npages_all, kCtxBtStage);
   for (int i = threadIdx.x; i < n_stage_bt; i += kCtxThreads) sbt[i] = bt[i];
   if (PASS == 0 && mg == 0 && threadIdx.x == 0) a.ticket[pair] = 0;
   __syncthreads();
   auto blk_of = [&](int p) -> int { return p < kCtxBtStage ? sbt[p] : bt[p]; };
 
-  float* colsum = a.colsum + ((size_t)pair * a.groups + mg) * (kSinks + a.s_cap);
+  float* colsum = a.colsum + ((size_t)pair * a.groups + mg) * a.cs_row;
+  float* cs_ring = colsum + kSinks + a.s_cap;
   // sink keys and values of this (sequence, KV head)
   const uint16_t* sink_k = s.sink_k + ((size_t)b * hkv + h) * kSinks * kHeadDim;
   const uint16_t* sink_v = s.sink_v + ((size_t)b * hkv + h) * kSinks * kHeadDim;
@@ -192,12 +211,24 @@ __global__ void __launch_bounds__(kCtxThreads) ctx_attn_kernel(DevState s, int s
     const int wfirst = active ? ctx_vis(L, row0 / G) : 0;                       // every row sees these
     const int wlast = active ? ctx_vis(L, (min(R, row0 + 16) - 1) / G) : 0;     // some row sees these
     const int npages = (cta_lim + kPage - 1) / kPage;
+    // window tiles (16 positions from rlo) the CTA's rows see, and the window
+    // positions this warp's rows see
+    int nrt = 0, wring_end = 0;
+    if (WIN && s.ring > 0) {
+      const int last_row = min(R, 16 * ((round * a.groups + mg) * kCtxWarps + kCtxWarps)) - 1;
+      if (last_row >= 16 * (round * a.groups + mg) * kCtxWarps)
+        nrt = (max(0, ctx_ring_end(L, last_row / G) - L.rlo) + 15) / 16;
+      wring_end = active ? ctx_ring_end(L, (min(R, row0 + 16) - 1) / G) : 0;
+      if (PASS == 1 && round == 0)
+        for (int e2 = threadIdx.x; e2 < L.P1 - L.rlo; e2 += kCtxThreads) cs_ring[e2] = 0.0f;
+    }
 
     // ---- query fragments (A operand), rows r_lo / r_hi, scaled by 2^e into
     // fp16 range; the offset sum per row; the sink logits per row
     uint32_t qa[8][4];
     float ch_lo = 0.0f, ch_hi = 0.0f, cq_lo = 0.0f, cq_hi = 0.0f;
     float sk_lg[2][kSinks];
+    int e_row[2] = {0, 0};
     {
       float qv[2][32];
       float amax[2] = {0.0f, 0.0f};
@@ -229,7 +260,7 @@ __global__ void __launch_bounds__(kCtxThreads) ctx_attn_kernel(DevState s, int s
         amax[rr] = fmaxf(amax[rr], __shfl_xor_sync(0xffffffffu, amax[rr], 1));
         amax[rr] = fmaxf(amax[rr], __shfl_xor_sync(0xffffffffu, amax[rr], 2));
       }
-      int e[2];
+      int* e = e_row;
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
         e[rr] = amax[rr] > 0.0f ? min(max(14 - exponent_of(amax[rr]), -100), 100) : 0;
@@ -596,6 +627,188 @@ __global__ void __launch_bounds__(kCtxThreads) ctx_attn_kernel(DevState s, int s
       for (int sl = npages * kPage + threadIdx.x; sl < L.S1; sl += kCtxThreads) colsum[kSinks + sl] = 0.0f;
     }
 
+    // ---- the bf16 window (hybrid precision): tiles of 16 positions from
+    // rlo, K and V exact in bf16 (bf16 MMA; the query rows again as bf16 A
+    // fragments, q' = q 2^e being exact in bf16 too)
+    if (WIN && nrt > 0) {
+      const int W = s.ring;
+      uint32_t qb[8][4];
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const int row = rr ? r_hi : r_lo;
+        const bool ok = (rr ? ok_hi : ok_lo) && active;
+        const uint16_t* qrow =
+            a.q + (((size_t)bl * s.hq + h * G + (ok ? row % G : 0)) * n + (ok ? row / G : 0)) * kHeadDim;
+        const float f2e = pow2i(e_row[rr]);
+#pragma unroll
+        for (int st = 0; st < 8; ++st) {
+          const int d0 = 16 * st + 2 * tq, d1 = d0 + 8;
+          float x0 = 0.0f, x1 = 0.0f, x2 = 0.0f, x3 = 0.0f;
+          if (ok) {
+            const uint32_t w0 = *reinterpret_cast<const uint32_t*>(qrow + d0);
+            const uint32_t w1 = *reinterpret_cast<const uint32_t*>(qrow + d1);
+            x0 = bf16f(w0 & 0xFFFFu) * f2e;
+            x1 = bf16f(w0 >> 16) * f2e;
+            x2 = bf16f(w1 & 0xFFFFu) * f2e;
+            x3 = bf16f(w1 >> 16) * f2e;
+          }
+          qb[st][rr] = pack_bf16x2(x0, x1);
+          qb[st][2 + rr] = pack_bf16x2(x2, x3);
+        }
+      }
+      const float cr_lo = a.qk_scale_log2 * pow2i(-e_row[0]), cr_hi = a.qk_scale_log2 * pow2i(-e_row[1]);
+      const int re_lo = ok_lo ? ctx_ring_end(L, i_lo) : 0, re_hi = ok_hi ? ctx_ring_end(L, i_hi) : 0;
+      // the PV operand of window tokens: p in the units of the pool's
+      // accumulators (their sum is scaled by 2^24 (2^20) and 2^E at the end)
+      const float rscale = pow2i(max((kOffset ? -24 : 0) - E, -126));
+      const uint16_t* rk = s.ring_k + ((size_t)b * hkv + h) * W * kHeadDim;
+      const uint16_t* rv = s.ring_v + ((size_t)b * hkv + h) * W * kHeadDim;
+      auto ring_issue = [&](int u) {
+        if (u < nrt) {
+          const uint32_t sb = ring + (u & 1) * kRingStage;
+          for (int c = threadIdx.x; c < (kNeedV ? 512 : 256); c += kCtxThreads) {
+            const int kv = c >> 8, row = (c >> 4) & 15, ch = c & 15;
+            const int pos = L.rlo + 16 * u + row;
+            const uint32_t dst = sb + (uint32_t)((kv * 16 + row) * kRingRow * 2 + ch * 16);
+            if (pos < L.P1)
+              cp_async16_if(true, dst, (kv ? rv : rk) + (size_t)((pos - kSinks) % W) * kHeadDim + ch * 8);
+            else  // past the window's end: zeros (a zero probability times stale bits could be NaN)
+              asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0u) : "memory");
+          }
+        }
+        cp_async_commit();
+      };
+      ring_issue(0);
+#pragma unroll 1
+      for (int u = 0; u < nrt; ++u) {
+        ring_issue(u + 1);
+        cp_async_wait<1>();
+        __syncthreads();  // tile u is in; every warp is done with tile u - 1
+        if (PASS == 1 && u > 0 && threadIdx.x < 16) {
+          const int e2 = 16 * (u - 1) + threadIdx.x;
+          if (L.rlo + e2 < L.P1) {
+            const int pb = (u - 1) & 1;
+            float v = sh_cs[pb][0][threadIdx.x];
+#pragma unroll
+            for (int w2 = 1; w2 < kCtxWarps; ++w2) v += sh_cs[pb][w2][threadIdx.x];
+            cs_ring[e2] += v;
+          }
+        }
+        const int pos0 = L.rlo + 16 * u;
+        float cs_t[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (active && pos0 < wring_end) {
+          const uint32_t sb = ring + (u & 1) * kRingStage;
+          float acc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
+          // B fragments by ldmatrix: matrices (tokens 0..7 | 8..15) x (dims 16st.. | 16st+8..)
+          const int mtx = lane >> 3;
+          const uint32_t kaddr = sb + (uint32_t)((((mtx >> 1) * 8 + (lane & 7)) * kRingRow + ((mtx & 1) * 8)) * 2);
+#pragma unroll
+          for (int st = 0; st < 8; ++st) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(b0, b1, b2, b3, kaddr + 32 * st);
+            mma16816_bf16(acc[0], qb[st][0], qb[st][1], qb[st][2], qb[st][3], b0, b1);
+            mma16816_bf16(acc[1], qb[st][0], qb[st][1], qb[st][2], qb[st][3], b2, b3);
+          }
+          float lg[2][4];
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int ps = pos0 + 8 * t + 2 * tq;
+            lg[t][0] = ps < re_lo ? acc[t][0] * cr_lo : -INFINITY;
+            lg[t][1] = ps + 1 < re_lo ? acc[t][1] * cr_lo : -INFINITY;
+            lg[t][2] = ps < re_hi ? acc[t][2] * cr_hi : -INFINITY;
+            lg[t][3] = ps + 1 < re_hi ? acc[t][3] * cr_hi : -INFINITY;
+          }
+          if (PASS == 0) {
+            const float t_lo = fmaxf(fmaxf(lg[0][0], lg[0][1]), fmaxf(lg[1][0], lg[1][1]));
+            const float t_hi = fmaxf(fmaxf(lg[0][2], lg[0][3]), fmaxf(lg[1][2], lg[1][3]));
+            if (__any_sync(0xffffffffu, t_lo > m_lo + kCtxLazy || t_hi > m_hi + kCtxLazy)) {
+              float x_lo = t_lo, x_hi = t_hi;
+              x_lo = fmaxf(x_lo, __shfl_xor_sync(0xffffffffu, x_lo, 1));
+              x_lo = fmaxf(x_lo, __shfl_xor_sync(0xffffffffu, x_lo, 2));
+              x_hi = fmaxf(x_hi, __shfl_xor_sync(0xffffffffu, x_hi, 1));
+              x_hi = fmaxf(x_hi, __shfl_xor_sync(0xffffffffu, x_hi, 2));
+              const float n_lo = fmaxf(m_lo, x_lo), n_hi = fmaxf(m_hi, x_hi);
+              l_lo *= fast_exp2(m_lo - n_lo);
+              l_hi *= fast_exp2(m_hi - n_hi);
+              m_lo = n_lo;
+              m_hi = n_hi;
+            }
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              l_lo += fast_exp2(lg[t][0] - m_lo) + fast_exp2(lg[t][1] - m_lo);
+              l_hi += fast_exp2(lg[t][2] - m_hi) + fast_exp2(lg[t][3] - m_hi);
+            }
+          } else {
+            float pr[2][4];
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              pr[t][0] = fast_exp2(lg[t][0] - M_lo) * iL_lo;
+              pr[t][1] = fast_exp2(lg[t][1] - M_lo) * iL_lo;
+              pr[t][2] = fast_exp2(lg[t][2] - M_hi) * iL_hi;
+              pr[t][3] = fast_exp2(lg[t][3] - M_hi) * iL_hi;
+              cs_t[2 * t] = pr[t][0] + pr[t][2];
+              cs_t[2 * t + 1] = pr[t][1] + pr[t][3];
+            }
+            uint32_t ph[4], pl[4];
+            split_bf16x2(pr[0][0] * rscale, pr[0][1] * rscale, ph[0], pl[0]);
+            split_bf16x2(pr[0][2] * rscale, pr[0][3] * rscale, ph[1], pl[1]);
+            split_bf16x2(pr[1][0] * rscale, pr[1][1] * rscale, ph[2], pl[2]);
+            split_bf16x2(pr[1][2] * rscale, pr[1][3] * rscale, ph[3], pl[3]);
+            // V rows 2tq, 2tq+1, 2tq+8, 2tq+9 at head dims 16g .. 16g+15
+            uint32_t xr[4][8];
+            const int vr[4] = {2 * tq, 2 * tq + 1, 2 * tq + 8, 2 * tq + 9};
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const uint8_t* vp = smem + (u & 1) * kRingStage + ((16 + vr[q4]) * kRingRow + 16 * g) * 2;
+              const uint4 y0 = *reinterpret_cast<const uint4*>(vp);
+              const uint4 y1 = *reinterpret_cast<const uint4*>(vp + 16);
+              xr[q4][0] = y0.x; xr[q4][1] = y0.y; xr[q4][2] = y0.z; xr[q4][3] = y0.w;
+              xr[q4][4] = y1.x; xr[q4][5] = y1.y; xr[q4][6] = y1.z; xr[q4][7] = y1.w;
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
+              uint32_t b0 = prmt(xr[0][j >> 1], xr[1][j >> 1], sel);
+              uint32_t b1 = prmt(xr[2][j >> 1], xr[3][j >> 1], sel);
+              if (kOffset && BITS == 4 && (j & 1)) {  // these N-tiles hold 16x values (INT4 high nibbles)
+                b0 = bf16x2_times16(b0);
+                b1 = bf16x2_times16(b1);
+              }
+              mma16816_bf16(oacc[j], ph[0], ph[1], ph[2], ph[3], b0, b1);
+              mma16816_bf16(oacc[j], pl[0], pl[1], pl[2], pl[3], b0, b1);
+            }
+          }
+        }
+        if (PASS == 1) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            cs_t[q4] += __shfl_xor_sync(0xffffffffu, cs_t[q4], 4);
+            cs_t[q4] += __shfl_xor_sync(0xffffffffu, cs_t[q4], 8);
+            cs_t[q4] += __shfl_xor_sync(0xffffffffu, cs_t[q4], 16);
+          }
+          if (g == 0) {
+            float* cw = sh_cs[u & 1][warp];
+            cw[2 * tq] = cs_t[0];
+            cw[2 * tq + 1] = cs_t[1];
+            cw[8 + 2 * tq] = cs_t[2];
+            cw[9 + 2 * tq] = cs_t[3];
+          }
+        }
+      }
+      cp_async_wait<0>();
+      __syncthreads();
+      if (PASS == 1 && threadIdx.x < 16) {
+        const int e2 = 16 * (nrt - 1) + threadIdx.x;
+        if (L.rlo + e2 < L.P1) {
+          const int pb = (nrt - 1) & 1;
+          float v = sh_cs[pb][0][threadIdx.x];
+#pragma unroll
+          for (int w2 = 1; w2 < kCtxWarps; ++w2) v += sh_cs[pb][w2][threadIdx.x];
+          cs_ring[e2] += v;
+        }
+      }
+    }
+
     if (PASS == 0) {
       if (active) {
         l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
@@ -690,11 +903,18 @@ __global__ void __launch_bounds__(kCtxThreads) ctx_attn_kernel(DevState s, int s
     __syncthreads();
     if (sh_last) {
       __threadfence();
-      const float* base = a.colsum + (size_t)pair * a.groups * (kSinks + a.s_cap);
+      const float* base = a.colsum + (size_t)pair * a.groups * a.cs_row;
+      if (WIN && s.ring > 0) {
+        for (int e = threadIdx.x; e < L.P1 - L.rlo; e += kCtxThreads) {
+          float v = 0.0f;
+          for (int c = 0; c < a.groups; ++c) v += base[(size_t)c * a.cs_row + kSinks + a.s_cap + e];
+          s.ring_score[((size_t)b * hkv + h) * s.ring + (L.rlo + e - kSinks) % s.ring] += v;
+        }
+      }
       for (int sl = threadIdx.x; sl < kSinks + L.S1; sl += kCtxThreads) {
         if (sl < kSinks && sl >= n_sinks) continue;
         float v = 0.0f;
-        for (int c = 0; c < a.groups; ++c) v += base[(size_t)c * (kSinks + a.s_cap) + sl];
+        for (int c = 0; c < a.groups; ++c) v += base[(size_t)c * a.cs_row + sl];
         if (sl < kSinks) {
           s.sink_score[((size_t)b * hkv + h) * kSinks + sl] += v;
         } else {
@@ -707,16 +927,30 @@ __global__ void __launch_bounds__(kCtxThreads) ctx_attn_kernel(DevState s, int s
   }
 }
 
-template <int BITS, bool FP8, int PASS>
+template <int BITS, bool FP8, int PASS, bool WIN>
 cudaError_t launch_ctx_t(const DevState& s, int seq_begin, int batch, const CtxArgs& a, cudaStream_t st) {
   using Gm = CtxGeom<BITS>;
-  const int smem = kCtxStages * Gm::kStage + kCtxBtStage * 4;
+  const int ring_bytes = WIN && 2 * kRingStage > kCtxStages * Gm::kStage ? 2 * kRingStage : kCtxStages * Gm::kStage;
+  const int smem = ring_bytes + kCtxBtStage * 4;
   static int done[64] = {0};
-  const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(ctx_attn_kernel<BITS, FP8, PASS>), smem, done);
+  const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(ctx_attn_kernel<BITS, FP8, PASS, WIN>), smem, done);
   if (e != cudaSuccess) return e;
   dim3 grid(a.groups, batch * s.hkv);
-  ctx_attn_kernel<BITS, FP8, PASS><<<grid, kCtxThreads, smem, st>>>(s, seq_begin, a);
+  ctx_attn_kernel<BITS, FP8, PASS, WIN><<<grid, kCtxThreads, smem, st>>>(s, seq_begin, a);
   return cudaGetLastError();
+}
+
+template <int BITS, bool FP8, bool WIN>
+cudaError_t launch_ctx_passes(const DevState& s, int seq_begin, int batch, const CtxArgs& a, cudaStream_t st) {
+  cudaError_t e = launch_ctx_t<BITS, FP8, 0, WIN>(s, seq_begin, batch, a, st);
+  if (e == cudaSuccess) e = launch_ctx_t<BITS, FP8, 1, WIN>(s, seq_begin, batch, a, st);
+  return e;
+}
+
+template <int BITS, bool FP8>
+cudaError_t launch_ctx_codes(const DevState& s, int seq_begin, int batch, const CtxArgs& a, cudaStream_t st) {
+  return s.ring > 0 ? launch_ctx_passes<BITS, FP8, true>(s, seq_begin, batch, a, st)
+                    : launch_ctx_passes<BITS, FP8, false>(s, seq_begin, batch, a, st);
 }
 
 }  // namespace
@@ -739,19 +973,16 @@ cudaError_t launch_ctx_attention(const DevState& s, int seq_begin, int batch, in
   a.n = n;
   a.groups = ctx_groups(n, s.group);
   a.s_cap = s_cap;
+  a.cs_row = kSinks + s_cap + s.ring;
   a.qk_scale_log2 = qk_scale_log2;
   a.accumulate = accumulate ? 1 : 0;
   cudaError_t e;
-  if (s.bits == 8 && s.fp8) {
-    e = launch_ctx_t<8, true, 0>(s, seq_begin, batch, a, st);
-    if (e == cudaSuccess) e = launch_ctx_t<8, true, 1>(s, seq_begin, batch, a, st);
-  } else if (s.bits == 8) {
-    e = launch_ctx_t<8, false, 0>(s, seq_begin, batch, a, st);
-    if (e == cudaSuccess) e = launch_ctx_t<8, false, 1>(s, seq_begin, batch, a, st);
-  } else {
-    e = launch_ctx_t<4, false, 0>(s, seq_begin, batch, a, st);
-    if (e == cudaSuccess) e = launch_ctx_t<4, false, 1>(s, seq_begin, batch, a, st);
-  }
+  if (s.bits == 8 && s.fp8)
+    e = launch_ctx_codes<8, true>(s, seq_begin, batch, a, st);
+  else if (s.bits == 8)
+    e = launch_ctx_codes<8, false>(s, seq_begin, batch, a, st);
+  else
+    e = launch_ctx_codes<4, false>(s, seq_begin, batch, a, st);
   return e;
 }
 

@@ -764,7 +764,8 @@ kvc_status kvc_prefill_attention(kvc_cache* c, int32_t seq_begin, int32_t batch,
 
 // Workspace of kvc_prefill_context: per (sequence, KV head) the row
 // statistics of its n * G attention rows, one row of column sums per CTA of
-// the multi-query kernel (sinks first, then every pool slot), a ticket.
+// the multi-query kernel (sinks first, then every pool slot, then the bf16
+// window's positions), a ticket.
 struct CtxWs {
   size_t stats, colsum, ticket, total;
 };
@@ -774,7 +775,8 @@ CtxWs ctx_ws(const kvc_cache* c, int32_t batch, int32_t n) {
   CtxWs w;
   w.stats = 0;
   w.colsum = align_up(pairs * n * G * 2 * 4);
-  w.ticket = w.colsum + align_up(pairs * kvc::ctx_groups(n, G) * (kvc::kSinks + (size_t)s_cap(c)) * 4);
+  w.ticket = w.colsum + align_up(pairs * kvc::ctx_groups(n, G) *
+                                 (kvc::kSinks + (size_t)s_cap(c) + c->cfg.bf16_window) * 4);
   w.total = w.ticket + align_up(pairs * 4);
   return w;
 }
@@ -797,7 +799,6 @@ kvc_status kvc_prefill_context(kvc_cache* c, int32_t seq_begin, int32_t batch, i
   if (!d_workspace || !aligned(d_workspace, kAlign) ||
       workspace_bytes < kvc_prefill_context_workspace_bytes(c, batch, n))
     return KVC_ERR_INVALID_ARG;
-  if (c->cfg.bf16_window > 0) return KVC_ERR_UNSUPPORTED;  // the causal limit is a slot count only without a window
   if ((long long)n * c->cfg.num_q_heads > (1LL << 30)) return KVC_ERR_UNSUPPORTED;
   kvc_status st0 = kvc_quantize_append(c, seq_begin, batch, n, d_k, d_v, stream);
   if (st0 != KVC_OK) return st0;

@@ -125,14 +125,59 @@ def test_prefill_context_then_decode_step():
     assert cache.read_status() == 0
 
 
-def test_prefill_context_refuses_a_bf16_window():
-    from compressed_kv_cache_kvc_gb300 import _lib as L
+WINDOW_CASES = [
+    # bits, codes, hq, hkv, batch, context, n1, bf16 window W
+    (8, "int", 16, 4, 2, 100, 30, 32),    # a prompt shorter than the window: older window tokens age into the pool
+    (4, "int", 40, 8, 1, 200, 80, 48),    # a prompt longer than the window: its own first tokens age out too
+    (8, "e4m3", 8, 2, 1, 10, 40, 64),     # the window holds the whole context and prompt: an empty pool
+    (4, "int", 8, 2, 2, 0, 50, 16),       # an empty sequence
+    (8, "int", 16, 2, 1, 300, 200, 96),   # several window tiles, 400 attention rows per KV head
+]
+
+
+@pytest.mark.parametrize("bits,codes,hq,hkv,batch,ctx,n1,W", WINDOW_CASES)
+def test_prefill_context_with_bf16_window(bits, codes, hq, hkv, batch, ctx, n1, W):
+    """Hybrid precision: the last W positions stay bf16 (exact), older tokens
+    are quantised; each prompt query attends to the sinks, the pool and the
+    window tokens at positions up to its own.  Outputs, the pool and window
+    contents and every held token's score against the oracle."""
     from compressed_kv_cache_kvc_gb300.cache import KVCache
-    rng = np.random.default_rng(63)
-    cache = KVCache(8, 2, 8, 16, 1, 8, bf16_window=16)
-    q = T.to_dev_bf16(_bits(rng, (1, 8, 5, 128)))
-    k = T.to_dev_bf16(_bits(rng, (1, 2, 5, 128)))
-    with pytest.raises(L.KvcError) as e:
-        cache.prefill_context(q, k, k)
-    assert e.value.status == L.KVC_ERR_UNSUPPORTED
-    assert cache.lengths(0) == (0, 0)
+    rng = np.random.default_rng(bits + hq + ctx + n1 + W)
+    mbps = (ctx + n1 + 15) // 16 + 2
+    cache = KVCache(hq, hkv, bits, batch * mbps, batch, mbps, bf16_window=W, codes=codes)
+    f = O.bf16_bits_to_f32
+    ora = O.OracleCache(batch, hq, hkv, bits, bf16_window=W, codes=codes)
+    if ctx:
+        q0 = _bits(rng, (batch, hq, ctx, 128))
+        k0 = _bits(rng, (batch, hkv, ctx, 128))
+        v0 = _bits(rng, (batch, hkv, ctx, 128))
+        cache.prefill(T.to_dev_bf16(q0), T.to_dev_bf16(k0), T.to_dev_bf16(v0))
+        for b in range(batch):
+            ora.prefill(b, f(q0[b]), f(k0[b]), f(v0[b]), T.sm_scale())
+    q1 = _bits(rng, (batch, hq, n1, 128))
+    k1 = _bits(rng, (batch, hkv, n1, 128))
+    v1 = _bits(rng, (batch, hkv, n1, 128))
+    out = T.bf16_tensor_to_f32(cache.prefill_context(T.to_dev_bf16(q1), T.to_dev_bf16(k1), T.to_dev_bf16(v1)))
+    st = T.StateView(cache)
+    for b in range(batch):
+        ref = ora.prefill_chunk(b, f(q1[b]), f(k1[b]), f(v1[b]), T.sm_scale())
+        T.assert_attention_close(out[b].reshape(hq * n1, 128), ref.reshape(hq * n1, 128), f"b={b}")
+        s = ora.seqs[b]
+        P = s.pos_total
+        assert int(st.seen[b]) == P
+        for h in range(hkv):
+            hs = s.heads[h]
+            old = hs.pos < P - W
+            pos, kc, ks, vc, vs, sc = st.head(b, h)
+            o, oo = np.argsort(pos), np.argsort(hs.pos[old])
+            assert np.array_equal(pos[o], hs.pos[old][oo]), (b, h)
+            assert np.array_equal(kc[o], hs.kcodes[old][oo]) and np.array_equal(vc[o], hs.vcodes[old][oo]), (b, h)
+            np.testing.assert_allclose(sc[o], hs.score[old][oo], rtol=1e-3, atol=1e-5)
+            rpos, rk, rv, rsc = st.ring_head(b, h)
+            assert np.array_equal(rpos, np.sort(hs.pos[~old])), (b, h)
+            assert np.array_equal(f(rk), s.raw_k[h][rpos]) and np.array_equal(f(rv), s.raw_v[h][rpos])
+            by_pos = dict(zip(hs.pos.tolist(), hs.score.tolist()))
+            np.testing.assert_allclose(rsc, [by_pos[p] for p in rpos.tolist()], rtol=1e-3, atol=1e-5)
+            ns = s.sink_k[h].shape[0]
+            np.testing.assert_allclose(st.sink_score[b, h, :ns], s.sink_score[h], rtol=1e-3, atol=1e-5)
+    assert cache.read_status() == 0
