@@ -594,11 +594,12 @@ def prefill_report(args, name: str):
 def prefill_context_report(args, name: str):
     """Time one layer's prompt of args.prefill_context tokens on sequences
     that hold the workload's context in the compressed cache
-    (kvc_prefill_context: append, then per prompt query the decode attention
-    over the pool, with H2O scores); the state is restored before every
-    timed call; inputs seeded, resident on the device.  Prints one JSON line
-    with the pool bytes the attention passes read per second against the
-    measured HBM peak."""
+    (kvc_prefill_context: the append, then the multi-query attention over
+    the pool (and the bf16 window with --bf16-window) in two passes, with H2O
+    scores); the state is restored before every timed call; inputs seeded,
+    resident on the device.  Prints one JSON line with the attention's
+    algorithmic rate (4 x 128 flops per visible (query row, key) pair: QK and
+    PV) and the pool bytes one pass reads per second."""
     import numpy as np
     import torch
 
@@ -610,8 +611,9 @@ def prefill_context_report(args, name: str):
     dev = torch.device("cuda", torch.cuda.current_device())
     w = W.WORKLOADS[name]
     B, Hq, Hkv, ctx, n1 = w.batch, w.num_q_heads, w.num_kv_heads, w.context, args.prefill_context
+    G = Hq // Hkv
     mbps = (ctx + n1 + 15) // 16 + 2
-    c = KVCache(Hq, Hkv, w.bits, B * mbps, B, mbps, device=dev, codes=args.codes)
+    c = KVCache(Hq, Hkv, w.bits, B * mbps, B, mbps, device=dev, codes=args.codes, bf16_window=args.bf16_window)
     g = torch.Generator(device=dev)
     g.manual_seed(1234)
     k0 = torch.randn(B, Hkv, ctx, 128, device=dev, generator=g).to(torch.bfloat16)
@@ -643,23 +645,26 @@ def prefill_context_report(args, name: str):
         raise RuntimeError(f"device status {st:#x}")
     launches = c.last_launch_count()
     t = float(np.median(ms))
+    # query i (position ctx + i) sees ctx + i + 1 keys (sinks, pool, window)
+    pairs = sum(ctx + i + 1 for i in range(n1)) * G * Hkv * B
+    flops = 4 * 128 * pairs
     per_slot = 2 * (128 * w.bits // 8) + 2 * 4
-    s0 = max(0, ctx - 4)
-    # pass i reads the pool slots query i may see, and the four bf16 sinks
-    nbytes = sum((s0 + max(0, ctx + i + 1 - max(ctx, 4))) * per_slot + 4 * 2 * 128 * 2
-                 for i in range(n1)) * Hkv * B
+    pool_slots = max(0, ctx + n1 - 4 - args.bf16_window)
+    pool_bytes = pool_slots * per_slot * Hkv * B
     peaks = {}
     try:
         peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
     except (OSError, ValueError):
         pass
-    peak = float(peaks.get("hbm_gbs", 6800.0))
-    gbs = nbytes / (t * 1e-3) / 1e9
     line = {"workload": name, "prefill_context": n1, "batch": B, "context": ctx, "q_heads": Hq, "kv_heads": Hkv,
-            "bits": w.bits, "codes": args.codes, "ms_per_call": t, "ms_per_query_pass": t / n1,
-            "prompt_tokens_per_s": B * n1 / (t * 1e-3), "pool_gbs": gbs, "pool_frac_of_hbm_peak": gbs / peak,
-            "peak_hbm_gbs": peak, "launches_per_call": launches, "steps_timed": args.steps,
-            "note": "one decode attention pass per prompt query; the time includes the prompt's append"}
+            "bits": w.bits, "codes": args.codes, "bf16_window": args.bf16_window, "ms_per_call": t,
+            "prompt_tokens_per_s": B * n1 / (t * 1e-3),
+            "attention_tflops": flops / (t * 1e-3) / 1e12,
+            "attention_frac_of_bf16_peak": flops / (t * 1e-3) / 1e12 / float(peaks.get("bf16_tflops", 1900.0)),
+            "pool_bytes_one_pass": pool_bytes, "pool_gbs_one_pass": pool_bytes / (t * 1e-3) / 1e9,
+            "launches_per_call": launches, "steps_timed": args.steps,
+            "note": "append + two passes of the multi-query attention (row statistics; outputs and column sums); "
+                    "the time includes the append"}
     print(json.dumps(line), flush=True)
 
 
