@@ -36,13 +36,13 @@ WORKLOAD = "qwen14b_b32_gqa5_t8192_int4_h2o_48l"
 METRIC = "decode-attention KV bytes read GB/s (% of GB300 HBM peak); seq·steps/s"
 
 
-def kv_read_bytes_per_step(w, slots_per_head: int, layers: int) -> int:
+def kv_read_bytes_per_step(w, slots_per_head: int, layers: int, batch: int | None = None) -> int:
     """Algorithmic KV bytes the attention reads in one step: per (sequence, KV
     head) every pool slot's K and V codes and fp32 scales, plus the 4 bf16
     sinks' K and V."""
     per_slot = 2 * (128 * w.bits // 8) + 2 * 4
     sinks = 4 * 2 * 128 * 2
-    return layers * w.batch * w.num_kv_heads * (slots_per_head * per_slot + sinks)
+    return layers * (w.batch if batch is None else batch) * w.num_kv_heads * (slots_per_head * per_slot + sinks)
 
 
 # ---------------------------------------------------------------------------
@@ -281,13 +281,22 @@ def gpu_arm(args):
 
     w = W.WORKLOADS[WORKLOAD]
     layers = args.layers or w.layers
-    B, Hq, Hkv, T = w.batch, w.num_q_heads, w.num_kv_heads, w.context
+    Hq, Hkv, T = w.num_q_heads, w.num_kv_heads, w.context
+    # replicas: every rank runs the whole workload on its own draws (weak
+    # scaling); batch: the workload's sequences are divided over the ranks,
+    # each rank drawing the single-GPU workload and keeping its slice
+    # (strong scaling, the union of the ranks' work is the one-GPU job)
+    b0, b1 = shard_range(w.batch, ws, rank) if args.split == "batch" else (0, w.batch)
+    B = b1 - b0
     mbps = (T + 1 + 15) // 16 + 1
     nblocks = B * mbps
     caches, snaps, inputs = [], [], []
     for l in range(layers):
         c = KVCache(Hq, Hkv, w.bits, nblocks, B, mbps, device=dev)
-        q, k, v, kn, vn = W.gen_layer_torch(w, l + 1000 * rank, dev)
+        if args.split == "batch":
+            q, k, v, kn, vn = (x[b0:b1].contiguous() for x in W.gen_layer_torch(w, l, dev))
+        else:
+            q, k, v, kn, vn = W.gen_layer_torch(w, l + 1000 * rank, dev)
         c.quantize_append(k, v)
         del k, v
         torch.cuda.synchronize()
@@ -301,7 +310,7 @@ def gpu_arm(args):
     mask = caches[0].new_keep_mask(B)
     outs = [torch.empty(B, Hq, 128, dtype=torch.bfloat16, device=dev) for _ in range(layers)]
     slots0 = caches[0].lengths(0)[0]  # pool slots before the step's append
-    kv_bytes = kv_read_bytes_per_step(w, slots0 + 1, layers)
+    kv_bytes = kv_read_bytes_per_step(w, slots0 + 1, layers, batch=B)  # this rank's
 
     def restore():
         for c, s in zip(caches, snaps):
@@ -383,8 +392,11 @@ def gpu_arm(args):
     total_ms = sum(step_ms)
     total_ms_max = reduce_max(total_ms, ws, dev)
     ms_per_step = total_ms_max / args.steps
-    value = kv_bytes * ws / (ms_per_step * 1e-3) / 1e9
-    seq_steps = B * ws / (ms_per_step * 1e-3)
+    # bytes and sequences of all ranks (with a batch split the ranks' slices
+    # add up to the one-GPU workload)
+    kv_bytes_all = kv_read_bytes_per_step(w, slots0 + 1, layers) if args.split == "batch" else kv_bytes * ws
+    value = kv_bytes_all / (ms_per_step * 1e-3) / 1e9
+    seq_steps = (w.batch if args.split == "batch" else B * ws) / (ms_per_step * 1e-3)
     attn_avg_ms = sum(attn_ms) / len(attn_ms)
     attn_bytes = kv_bytes // layers
     peaks = {}
@@ -460,7 +472,7 @@ def gpu_arm(args):
     else:
         e2e_ms = e2e_eager_ms
     e2e_step = reduce_max(sum(e2e_ms), ws, dev) / e_steps
-    e2e_value = kv_bytes * ws / (e2e_step * 1e-3) / 1e9
+    e2e_value = kv_bytes_all / (e2e_step * 1e-3) / 1e9
     e2e_eager_step = reduce_max(sum(e2e_eager_ms), ws, dev) / e_steps
     for c in caches:
         st = c.read_status()
@@ -489,11 +501,13 @@ def gpu_arm(args):
             traffic = None
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "strong" if args.split == "batch" else "weak",
         "vs_baseline": None, "dtype": "int4-codes/f16-mma/f32-accum", "data": "synthetic",
         "config": {"workload": WORKLOAD, "batch": B, "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": 128,
                    "context": T, "layers": layers, "bits": w.bits, "budget": w.budget, "recent": w.recent,
-                   "parallelism": f"replicas{ws}", "l2": "state restore copy (>L2) between timed steps",
+                   "parallelism": f"batch-split{ws}" if args.split == "batch" else f"replicas{ws}",
+                   "l2": "state restore copy (>L2) between timed steps",
                    "cuda_graph": graph is not None},
         "seq_steps_per_s": seq_steps,
         "kv_bytes_per_step": kv_bytes,
@@ -896,6 +910,8 @@ def main():
                     help="report mode: time a prompt of this many tokens over the workload's context")
     ap.add_argument("--bf16-window", type=int, default=0,
                     help="report mode: hybrid precision, the last W positions kept in bf16 (W <= recent)")
+    ap.add_argument("--split", default="replicas", choices=["replicas", "batch"],
+                    help="N > 1: independent replicas (weak scaling) or the batch divided over the GPUs (strong)")
     ap.add_argument("--oracle-child", nargs=2, type=int, default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.oracle_child is not None:

@@ -59,3 +59,16 @@ def test_shard_range_partitions(total, world):
         assert 0 <= b <= e <= total
         seen.extend(range(b, e))
     assert seen == list(range(total))
+
+
+def test_batch_split_covers_the_workload():
+    """--split batch: the ranks' batch slices of the bench workload are
+    disjoint and add up to the one-GPU batch, and so do their KV bytes."""
+    from compressed_kv_cache_kvc_gb300 import workloads as W
+    w = W.WORKLOADS[bench.WORKLOAD]
+    for world in (1, 2, 4, 8):
+        slices = [bench.shard_range(w.batch, world, r) for r in range(world)]
+        assert slices[0][0] == 0 and slices[-1][1] == w.batch
+        assert all(a[1] == b[0] for a, b in zip(slices, slices[1:]))
+        per_rank = sum(bench.kv_read_bytes_per_step(w, 100, 3, batch=e - b) for b, e in slices)
+        assert per_rank == bench.kv_read_bytes_per_step(w, 100, 3)
