@@ -33,7 +33,8 @@ void* g_scratch_addr[kMaxDevices] = {nullptr};
 
 // Device address of the scratch on the current device.  The array's name in
 // host code is only a host-side handle, so the address is looked up once per
-// device (with that device current) and cached.
+// device (with that device current) and cached for the life of the process;
+// a device reset invalidates it (the header says so).
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

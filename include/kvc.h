@@ -326,8 +326,11 @@ kvc_status kvc_compact_blocks(kvc_cache* cache, int32_t seq_begin, int32_t batch
  *     needs more workspace than that (kvc_workspace_bytes(cache, batch) >
  *     KVC_NOALLOC_SCRATCH_BYTES); use kvc_decode_attention then.
  *   - The first call on a device looks up the array's device address (with
- *     that device current) and caches it; make that first call before any
- *     stream capture on the device.
+ *     that device current) and caches it for the life of the process; make
+ *     that first call before any stream capture on the device.  A device
+ *     reset (cudaDeviceReset, or the primary context torn down and created
+ *     again) unloads the library's module and invalidates the cached
+ *     address: do not call this entry point on that device after one.
  *   - All calls share the one array and leave their contents in it; calls
  *     that overlap on the GPU (other streams or host threads) race.  No part
  *     of it needs to start at zero. */
@@ -343,12 +346,17 @@ kvc_status kvc_decode_attention_noalloc(kvc_cache* cache, int32_t seq_begin, int
  * compute them.  After the split-K attention, the merge, the score update,
  * the selection and the compaction lists of each (sequence, KV head) run in
  * one kernel that keeps the scores, keys and keep decisions on chip; the row
- * moves follow in a launch of their own.  Four launches in all (the split
- * kernel runs even when every pool is empty: its first CTA publishes the
- * page prefix the next kernel reads); five with a bf16 window (its attention
- * follows the split).  In block mode (KVC_EVICT_BLOCK) that kernel stops
- * after the scores; the page sums and then the page selection and the row
- * rewrite of each sequence follow (five launches).
+ * moves follow in a launch of their own when some (sequence, KV head) moves
+ * more than 32 rows (the first step after a long prompt), else that kernel
+ * moves them itself (the steady state moves one row).  Three or four
+ * launches in all (the split kernel runs even when every pool is empty: its
+ * first CTA publishes the page prefix the next kernel reads); one more with
+ * a bf16 window (its attention follows the split).  In block mode
+ * (KVC_EVICT_BLOCK) that kernel stops after the scores; the page sums and
+ * then the page selection and the row rewrite of each sequence follow (five
+ * launches).  A CUDA graph captured at one state replays correctly at any
+ * other (every kernel reads the lengths from the device; a post kernel
+ * captured without a move kernel moves any number of rows itself).
  *   d_q: bf16 [batch][Hq][128]; d_k_new, d_v_new: bf16 [batch][Hkv][1][128];
  *   d_out: bf16 [batch][Hq][128]; workspace as for kvc_decode_attention.
  * Host-visible errors (arguments, capacity) are returned before anything is
