@@ -63,7 +63,7 @@ constexpr int kDevBadBlockId = 0x2;
 constexpr int kDevBadKeepMask = 0x4;
 constexpr int kDevTableOverflow = 0x8;
 constexpr int kDevStackOverflow = 0x10;
-constexpr int kDevWaitTimeout = 0x20;
+constexpr int kDevStaleHost = 0x20;
 
 // Scratch carved from the caller's workspace for one attention call.
 //

@@ -70,6 +70,14 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(DevState s, int seq
     for (int t = threadIdx.x; t < S; t += blockDim.x) mrow[t] = keep_all ? 1 : 0;
     return;
   }
+  if (a.smem_slots > 0 && S > a.smem_slots) {
+    // the shared key buffer was sized from the host's mirror of the lengths,
+    // which is behind the device (state restored without a host resync):
+    // flag it and keep every slot
+    for (int t = threadIdx.x; t < S; t += blockDim.x) mrow[t] = 1;
+    if (threadIdx.x == 0) atomicOr(&s.counters[kCtrStatus], kDevStaleHost);
+    return;
+  }
 
   extern __shared__ __align__(16) uint32_t dyn[];
   __shared__ int hist[kRadixBins];

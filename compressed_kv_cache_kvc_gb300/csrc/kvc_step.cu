@@ -83,6 +83,10 @@ __global__ void __launch_bounds__(NT, 1024 / NT) step_post_kernel(DevState s, in
     thr = P - a.window;
   }
   if (keep_all) n_keep = S;
+  // the host sized the shared key buffer from its mirror of the lengths; a
+  // longer sequence on the device (state restored without a host resync) is
+  // flagged and keeps its slots
+  const bool fits = a.smem_slots == 0 || S <= a.smem_slots;
   if (h == 0 && threadIdx.x == 0 && !block) {
     s.plan[2 * b] = S;
     s.plan[2 * b + 1] = n_keep;
@@ -171,7 +175,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) step_post_kernel(DevState s, in
         for (int g = 0; g < G; ++g)
           asm volatile("discard.global.L2 [%0], 128;" ::"l"(lgr + (size_t)g * w.s_cap + t) : "memory");
     }
-    if (block) continue;
+    if (block || !fits) continue;
     // slots past S in the last quarter page get keys too: nothing reads them
     *reinterpret_cast<uint4*>(keys + t) = make_uint4(kk[0], kk[1], kk[2], kk[3]);
     *reinterpret_cast<int4*>(pos + t) = p4;
@@ -189,6 +193,13 @@ __global__ void __launch_bounds__(NT, 1024 / NT) step_post_kernel(DevState s, in
     if ((threadIdx.x & 31) == __ffs(am) - 1 && n_top > 0) atomicAdd(&hist[kRadixBins - 1], n_top);
   }
   if (block) return;
+  if (!fits) {  // every CTA of the sequence takes this exit (same S)
+    if (threadIdx.x == 0) {
+      a.n_moves[pair] = 0;
+      atomicOr(&s.counters[kCtrStatus], kDevStaleHost);
+    }
+    return;
+  }
   __syncthreads();
   bool lists_ok = true;
   if (!keep_all) {

@@ -80,9 +80,11 @@ typedef enum {
 #define KVC_DEV_BAD_KEEP_MASK   0x4  /* keep mask count differs from the plan     */
 #define KVC_DEV_TABLE_OVERFLOW  0x8  /* per-sequence block table overflow         */
 #define KVC_DEV_STACK_OVERFLOW  0x10 /* free-block stack overflow on release      */
-#define KVC_DEV_WAIT_TIMEOUT    0x20 /* a page copy into shared memory did not
-                                        complete within 2 s; the pages not yet
-                                        read were skipped (outputs invalid)    */
+#define KVC_DEV_STALE_HOST      0x20 /* a sequence held more pool slots on the
+                                        device than the host mirror planned for
+                                        (state bytes restored without
+                                        kvc_cache_sync_host): its selection and
+                                        compaction were skipped                */
 
 /* Geometry of one layer's cache. */
 typedef struct {

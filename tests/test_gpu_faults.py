@@ -82,3 +82,44 @@ def test_bad_block_id_in_the_separate_calls():
     assert clean.read_status() == 0
     assert corrupt.read_status() & BAD_BLOCK_ID
     assert torch.equal(outs[0][1:], outs[1][1:])
+
+
+STALE_HOST = 0x20
+
+
+def test_state_restored_without_host_resync_is_flagged():
+    """The host sizes the selection's shared key buffer from its mirror of the
+    lengths.  Device state bytes restored from a snapshot without
+    kvc_cache_sync_host leave the device longer than that mirror: the step and
+    the separate selection must flag KVC_DEV_STALE_HOST and keep the slots
+    (never write past the buffer); the attention itself reads the device
+    lengths and is unaffected.  After a resync the step is exact again."""
+    (c, _), mbps, q, kn, vn = _pair()
+    snap = c.state_view.clone()
+    o1 = c.decode_step(q, kn, vn, mode="h2o", budget=120, recent=16)
+    torch.cuda.synchronize()
+    assert c.read_status() == 0
+    after = [c.lengths(b)[0] for b in range(q.shape[0])]
+    assert max(after) < 200
+    # restore without a resync: the host still plans for the evicted lengths
+    c.state_view.copy_(snap)
+    o2 = c.decode_step(q, kn, vn, mode="h2o", budget=120, recent=16)
+    torch.cuda.synchronize()
+    assert c.read_status() & STALE_HOST
+    assert torch.equal(o1, o2)
+    # the separate selection call takes the same guard
+    c.state_view.copy_(snap)
+    c.quantize_append(kn, vn)
+    o3 = c.decode_attention(q)
+    c.h2o_select_evict(q.shape[0], budget=120, recent=16)
+    torch.cuda.synchronize()
+    assert c.read_status() & STALE_HOST
+    assert torch.equal(o1, o3)
+    # resynchronised, the step is the first one again
+    c.state_view.copy_(snap)
+    c.sync_host()
+    o4 = c.decode_step(q, kn, vn, mode="h2o", budget=120, recent=16)
+    torch.cuda.synchronize()
+    assert c.read_status() == 0
+    assert torch.equal(o1, o4)
+    assert [c.lengths(b)[0] for b in range(q.shape[0])] == after
