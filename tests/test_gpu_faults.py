@@ -87,13 +87,19 @@ def test_bad_block_id_in_the_separate_calls():
 STALE_HOST = 0x20
 
 
+def _close(a, b):
+    a, b = a.float(), b.float()
+    assert bool(((a - b).abs() <= 2e-3 + 1e-2 * a.abs()).all())
+
+
 def test_state_restored_without_host_resync_is_flagged():
     """The host sizes the selection's shared key buffer from its mirror of the
     lengths.  Device state bytes restored from a snapshot without
     kvc_cache_sync_host leave the device longer than that mirror: the step and
     the separate selection must flag KVC_DEV_STALE_HOST and keep the slots
     (never write past the buffer); the attention itself reads the device
-    lengths and is unaffected.  After a resync the step is exact again."""
+    lengths and is unaffected (up to the summation order: the stream-K grid
+    follows the host's page count).  After a resync the step is exact again."""
     (c, _), mbps, q, kn, vn = _pair()
     snap = c.state_view.clone()
     o1 = c.decode_step(q, kn, vn, mode="h2o", budget=120, recent=16)
@@ -106,7 +112,7 @@ def test_state_restored_without_host_resync_is_flagged():
     o2 = c.decode_step(q, kn, vn, mode="h2o", budget=120, recent=16)
     torch.cuda.synchronize()
     assert c.read_status() & STALE_HOST
-    assert torch.equal(o1, o2)
+    _close(o1, o2)
     # the separate selection call takes the same guard
     c.state_view.copy_(snap)
     c.quantize_append(kn, vn)
@@ -114,7 +120,7 @@ def test_state_restored_without_host_resync_is_flagged():
     c.h2o_select_evict(q.shape[0], budget=120, recent=16)
     torch.cuda.synchronize()
     assert c.read_status() & STALE_HOST
-    assert torch.equal(o1, o3)
+    _close(o1, o3)
     # resynchronised, the step is the first one again
     c.state_view.copy_(snap)
     c.sync_host()
