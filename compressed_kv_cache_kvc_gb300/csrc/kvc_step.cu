@@ -24,9 +24,11 @@
 // (Technical Report: KV Cache Compression for Text-Only LLMs, sections 3.3
 // and 3.4; "KV Cache optimization techniques" sections 2.2, 2.4 and 3.2.)
 #include <algorithm>
+#include <type_traits>
 
 #include "kvc_device.h"
 #include "kvc_internal.h"
+#include "kvc_mma.h"  // codes::smem_u32
 
 namespace kvc {
 namespace {
@@ -36,9 +38,32 @@ using namespace dev;
 constexpr int kStepThreads = 512;
 constexpr int kStepBtStage = 2048;
 
+// Predicated stores and shared-memory adds (no branch).
+__device__ __forceinline__ void st4_if(bool pred, float* dst, float a, float b, float c, float d) {
+  asm volatile(
+      "{\n .reg .pred q;\n setp.ne.u32 q, %0, 0;\n"
+      " @q st.global.v4.f32 [%1], {%2, %3, %4, %5};\n}\n" ::"r"((uint32_t)pred),
+      "l"(dst), "f"(a), "f"(b), "f"(c), "f"(d)
+      : "memory");
+}
+__device__ __forceinline__ void st1_if(bool pred, float* dst, float a) {
+  asm volatile(
+      "{\n .reg .pred q;\n setp.ne.u32 q, %0, 0;\n"
+      " @q st.global.f32 [%1], %2;\n}\n" ::"r"((uint32_t)pred),
+      "l"(dst), "f"(a)
+      : "memory");
+}
+__device__ __forceinline__ void red_shared_add_if(bool pred, int* addr, int v) {
+  asm volatile(
+      "{\n .reg .pred q;\n setp.ne.u32 q, %0, 0;\n"
+      " @q red.shared.add.s32 [%1], %2;\n}\n" ::"r"((uint32_t)pred),
+      "r"(codes::smem_u32(addr)), "r"(v)
+      : "memory");
+}
+
 // NT threads: 512 (two CTAs per SM) or, when the pairs are no more than the
 // SMs, 1024 (one pair per SM, twice the threads on its slots).
-template <int NT>
+template <int NT, int GC>
 __global__ void __launch_bounds__(NT, 1024 / NT) step_post_kernel(DevState s, int seq_begin, int batch,
                                                                 const uint16_t* __restrict__ q,
                                                                 uint16_t* __restrict__ out, float qk_scale_log2,
@@ -57,17 +82,38 @@ __global__ void __launch_bounds__(NT, 1024 / NT) step_post_kernel(DevState s, in
   // (scores only: the page selection runs in launches of its own)
   const bool block = a.mode == 2;
   const bool h2o = a.mode != 1;
-  // the selection's first radix histogram is built by the score pass
-  for (int i = threadIdx.x; i < kRadixBins; i += blockDim.x) hist[i] = 0;
-  merge_phase(s, seq_begin, batch, w.cum, h, bl, q, out, qk_scale_log2, w, h2o, ms);
-  if (h2o) ring_score_pass(s, w, seq_begin + bl, bl, h, ms);
-
   const int hkv = s.hkv;
   const int G = s.group;
   const int S = s.seq_slots[b];
+  const size_t pair = (size_t)bl * hkv + h;
+  // the selection's first radix histogram is built by the score pass
+  for (int i = threadIdx.x; i < kRadixBins; i += blockDim.x) hist[i] = 0;
+  const int32_t* bt = s.block_table + (size_t)b * s.max_bps;
+  const int npages = (S + kPage - 1) / kPage;
+  const int32_t* btp = bt;
+  if (npages <= kStepBtStage) {
+    for (int i = threadIdx.x; i < npages; i += blockDim.x) sh_bt[i] = bt[i];
+    btp = sh_bt;
+  }
+  // the host sized the shared key buffer from its mirror of the lengths; a
+  // longer sequence on the device (state restored without a host resync) is
+  // flagged and keeps its slots
+  const bool fits = a.smem_slots == 0 || S <= a.smem_slots;
+  uint32_t* keys;
+  int32_t* pos;
+  if (a.smem_slots > 0) {
+    keys = dyn;
+    pos = a.pos_smem ? reinterpret_cast<int32_t*>(dyn + a.smem_slots) : a.g_pos + pair * a.s_cap;
+  } else {
+    keys = a.g_keys + pair * a.s_cap;
+    pos = a.g_pos + pair * a.s_cap;
+  }
+  // (the merge's barriers publish the block-table row)
+  merge_phase(s, seq_begin, batch, w.cum, h, bl, q, out, qk_scale_log2, w, h2o, ms);
+  if (h2o) ring_score_pass(s, w, seq_begin + bl, bl, h, ms);
+
   const int P = s.seq_pos[b];
   const int ns = min(P, kSinks);
-  const size_t pair = (size_t)bl * hkv + h;
   bool keep_all;
   int n_keep, thr;
   // the nr tokens of the bf16 window (hybrid precision) are kept and count
@@ -83,115 +129,130 @@ __global__ void __launch_bounds__(NT, 1024 / NT) step_post_kernel(DevState s, in
     thr = P - a.window;
   }
   if (keep_all) n_keep = S;
-  // the host sized the shared key buffer from its mirror of the lengths; a
-  // longer sequence on the device (state restored without a host resync) is
-  // flagged and keeps its slots
-  const bool fits = a.smem_slots == 0 || S <= a.smem_slots;
   if (h == 0 && threadIdx.x == 0 && !block) {
     s.plan[2 * b] = S;
     s.plan[2 * b + 1] = n_keep;
   }
 
-  uint32_t* keys;
-  int32_t* pos;
-  if (a.smem_slots > 0) {
-    keys = dyn;
-    pos = a.pos_smem ? reinterpret_cast<int32_t*>(dyn + a.smem_slots) : a.g_pos + pair * a.s_cap;
-  } else {
-    keys = a.g_keys + pair * a.s_cap;
-    pos = a.g_pos + pair * a.s_cap;
-  }
-  const int32_t* bt = s.block_table + (size_t)b * s.max_bps;
-  const int npages = (S + kPage - 1) / kPage;
-  const int32_t* btp = bt;
-  if (npages <= kStepBtStage) {
-    for (int i = threadIdx.x; i < npages; i += blockDim.x) sh_bt[i] = bt[i];
-    btp = sh_bt;
-  }
   __syncthreads();
 
   // ---- scores (H2O) and selection keys.  Keys: 0xFFFFFFFF for the recent
   // window (always kept), else the fp32 score bits (H2O) or 0 (StreamingLLM).
   // Four consecutive slots (a quarter page) per thread and round, moved as
-  // 16-byte vectors; every load of a round (G logit vectors, the positions
-  // and scores) is issued before the first use.
+  // 16-byte vectors; every load of a round (the group's logit vectors, the
+  // positions and scores) is issued before the first use.  The pass is bound
+  // by instruction issue, so the round is branch-free: a bad block id loads
+  // from block 0 and is masked, the stores and histogram adds are
+  // predicated, and the ragged last quarter page runs after the loop.
+  constexpr int GL = GC > 0 ? GC : kMaxGroup;  // logit rows held per round
+  const int Gr = GC > 0 ? GC : G;
   const float* lgr = w.logits + pair * G * w.s_cap;
-  const int nq = (S + 3) >> 2;
   // whole 128-byte lines of logits (rows 128-byte aligned) can be dropped
-  const bool discard_ok = (w.s_cap % 32) == 0 && ((uintptr_t)lgr % 128) == 0;
-  for (int j = threadIdx.x; j < nq; j += blockDim.x) {
+  const bool discard_ok = h2o && (w.s_cap % 32) == 0 && ((uintptr_t)lgr % 128) == 0;
+  const bool want_keys = !block && fits;
+  // the group's (M, 1/L) in registers when they fit beside the logit rows
+  constexpr bool kStatsInRegs = GL <= 5;
+  float Mg[GL], iLg[GL];
+#pragma unroll
+  for (int g = 0; g < GL; ++g) {
+    Mg[g] = g < Gr ? ms.M[g] : 0.0f;
+    iLg[g] = g < Gr ? ms.invL[g] : 0.0f;
+  }
+  int n_top = 0;   // recent-window keys of this thread (the histogram's top bin)
+  bool bad = false;
+  auto quad = [&](int j, auto tail_tag) {
+    constexpr bool kTail = decltype(tail_tag)::value;
     const int t = 4 * j;
     const int blk = btp[t / kPage];
     const bool ok = (unsigned)blk < (unsigned)s.num_blocks;
+    bad |= !ok;
     const size_t idx = ((size_t)(ok ? blk : 0) * hkv + h) * kPage + (t % kPage);
-    float4 lg[kMaxGroup];
+    // logit rows in chunks of at most 5 (wider groups would spill)
+    constexpr int CH = GL <= 5 ? GL : 4;
+    float4 lg[CH];
+    auto load_rows = [&](int g0) {
 #pragma unroll
-    for (int g = 0; g < kMaxGroup; ++g)
-      lg[g] = (h2o && g < G) ? *reinterpret_cast<const float4*>(lgr + (size_t)g * w.s_cap + t)
-                             : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    int4 p4 = make_int4(-1, -1, -1, -1);
+      for (int i = 0; i < CH; ++i)
+        lg[i] = g0 + i < Gr ? *reinterpret_cast<const float4*>(lgr + (size_t)(g0 + i) * w.s_cap + t)
+                            : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    };
+    if (h2o) load_rows(0);
+    int4 p4 = *reinterpret_cast<const int4*>(s.slot_pos + idx);
     float4 sc4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    if (ok) {
-      p4 = *reinterpret_cast<const int4*>(s.slot_pos + idx);
-      if (h2o) sc4 = *reinterpret_cast<const float4*>(s.score + idx);
-    } else {
-      atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
+    if (h2o) sc4 = *reinterpret_cast<const float4*>(s.score + idx);
+    if (!ok) {
+      p4 = make_int4(-1, -1, -1, -1);
+      sc4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     }
     const int pp[4] = {p4.x, p4.y, p4.z, p4.w};
     float vv[4] = {sc4.x, sc4.y, sc4.z, sc4.w};
     uint32_t kk[4];
+    if (h2o) {
+      // the H2O increment: sum over the group of the slot's probability, in
+      // query-head order (as h2o_increment)
+      float inc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int g0 = 0; g0 < GL; g0 += CH) {
+        if (g0 > 0) load_rows(g0);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+          for (int i = 0; i < CH; ++i) {
+            const int g = g0 + i;
+            const float l = c == 0 ? lg[i].x : c == 1 ? lg[i].y : c == 2 ? lg[i].z : lg[i].w;
+            const float Mv = kStatsInRegs ? Mg[g] : ms.M[g];
+            const float iLv = kStatsInRegs ? iLg[g] : ms.invL[g];
+            if (g < Gr) inc[c] = __fmaf_rn(fast_exp2(l - Mv), iLv, inc[c]);
+          }
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) vv[c] += inc[c];
+    }
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      if (h2o) {
-        // the H2O increment: sum over the group of the slot's probability,
-        // in query-head order (as h2o_increment)
-        float inc = 0.0f;
-#pragma unroll
-        for (int g = 0; g < kMaxGroup; ++g) {
-          const float l = c == 0 ? lg[g].x : c == 1 ? lg[g].y : c == 2 ? lg[g].z : lg[g].w;
-          if (g < G) inc = __fmaf_rn(fast_exp2(l - ms.M[g]), ms.invL[g], inc);
-        }
-        vv[c] += inc;
-        kk[c] = pp[c] >= thr ? 0xFFFFFFFFu : __float_as_uint(fmaxf(vv[c], 0.0f));
-      } else {
-        kk[c] = pp[c] >= thr ? 0xFFFFFFFFu : 0u;
-      }
-      if (!ok) kk[c] = 0u;
+      const uint32_t key = h2o ? __float_as_uint(fmaxf(vv[c], 0.0f)) : 0u;
+      kk[c] = ok ? (pp[c] >= thr ? 0xFFFFFFFFu : key) : 0u;
     }
-    if (ok && h2o) {
-      if (t + 4 <= S) {
-        *reinterpret_cast<float4*>(s.score + idx) = make_float4(vv[0], vv[1], vv[2], vv[3]);
-      } else {
+    if (h2o) {
+      if (kTail) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          if (t + c < S) s.score[idx + c] = vv[c];
+        for (int c = 0; c < 4; ++c) st1_if(ok && t + c < S, s.score + idx + c, vv[c]);
+      } else {
+        st4_if(ok, s.score + idx, vv[0], vv[1], vv[2], vv[3]);
       }
     }
-    if (h2o && discard_ok) {
+    if (discard_ok && !kTail) {
       // the logits of 32 slots are read once the 8 threads of their line have
       // used them: drop those lines from L2 without writing them back
       __syncwarp(__activemask());
       if ((threadIdx.x & 7) == 0 && t + 32 <= S)
-        for (int g = 0; g < G; ++g)
-          asm volatile("discard.global.L2 [%0], 128;" ::"l"(lgr + (size_t)g * w.s_cap + t) : "memory");
+#pragma unroll
+        for (int g = 0; g < GL; ++g)
+          if (g < Gr) asm volatile("discard.global.L2 [%0], 128;" ::"l"(lgr + (size_t)g * w.s_cap + t) : "memory");
     }
-    if (block || !fits) continue;
+    if (!want_keys) return;
     // slots past S in the last quarter page get keys too: nothing reads them
     *reinterpret_cast<uint4*>(keys + t) = make_uint4(kk[0], kk[1], kk[2], kk[3]);
     *reinterpret_cast<int4*>(pos + t) = p4;
     // first-pass histogram (bits 31..21) of the selection; the recent
-    // window's keys all fall in the top bin and are counted per warp
-    int n_top = 0;
+    // window's keys all fall in the top bin and are counted apart
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      if (t + c >= S) continue;
-      if (kk[c] == 0xFFFFFFFFu) ++n_top;
-      else atomicAdd(&hist[kk[c] >> 21], 1);
+      const bool in = !kTail || t + c < S;
+      const bool top = kk[c] == 0xFFFFFFFFu;
+      n_top += (in && top) ? 1 : 0;
+      red_shared_add_if(in && !top, &hist[kk[c] >> 21], 1);
     }
-    const unsigned am = __activemask();
-    n_top = __reduce_add_sync(am, n_top);
-    if ((threadIdx.x & 31) == __ffs(am) - 1 && n_top > 0) atomicAdd(&hist[kRadixBins - 1], n_top);
+  };
+  const int nq_full = S >> 2;
+  for (int j = threadIdx.x; j < nq_full; j += NT) quad(j, std::false_type());
+  if ((S & 3) != 0 && (int)threadIdx.x == nq_full % NT) quad(nq_full, std::true_type());
+  if (want_keys) {
+    n_top = __reduce_add_sync(0xffffffffu, n_top);
+    if ((threadIdx.x & 31) == 0 && n_top > 0) atomicAdd(&hist[kRadixBins - 1], n_top);
   }
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
   if (block) return;
   if (!fits) {  // every CTA of the sequence takes this exit (same S)
     if (threadIdx.x == 0) {
@@ -366,26 +427,39 @@ __global__ void __launch_bounds__(kStepThreads, 2) step_moves_kernel(DevState s,
 
 int step_max_smem_bytes() { return 160 * 1024; }
 
-template <int NT>
+template <int NT, int GC>
 cudaError_t launch_step_post_nt(const DevState& s, int seq_begin, int batch, const uint16_t* q, uint16_t* out,
                                 float qk_scale_log2, const AttnWork& w, const StepArgs& a, cudaStream_t st) {
   const int smem = a.smem_slots > 0 ? a.smem_slots * (a.pos_smem ? 8 : 4) : 0;
   if (smem > 0) {
     static int done[64] = {0};
-    const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(step_post_kernel<NT>), step_max_smem_bytes(), done);
+    const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(step_post_kernel<NT, GC>), step_max_smem_bytes(), done);
     if (e != cudaSuccess) return e;
   }
   dim3 grid(s.hkv, batch);
-  step_post_kernel<NT><<<grid, NT, smem, st>>>(s, seq_begin, batch, q, out, qk_scale_log2, w, a);
+  step_post_kernel<NT, GC><<<grid, NT, smem, st>>>(s, seq_begin, batch, q, out, qk_scale_log2, w, a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_step_post(const DevState& s, int seq_begin, int batch, const uint16_t* q, uint16_t* out,
                              float qk_scale_log2, const AttnWork& w, const StepArgs& a, int sm_count,
                              cudaStream_t st) {
-  if (batch * s.hkv <= sm_count)
-    return launch_step_post_nt<1024>(s, seq_begin, batch, q, out, qk_scale_log2, w, a, st);
-  return launch_step_post_nt<kStepThreads>(s, seq_begin, batch, q, out, qk_scale_log2, w, a, st);
+  // the group sizes of common layouts get a score pass of their own width
+  // (1: multi-head attention; 4 and 5: GQA); others take the general one
+  const bool wide = batch * s.hkv <= sm_count;
+  switch (s.group) {
+#define KVC_POST_CASE(GC)                                                                              \
+  case GC:                                                                                             \
+    return wide ? launch_step_post_nt<1024, GC>(s, seq_begin, batch, q, out, qk_scale_log2, w, a, st) \
+                : launch_step_post_nt<kStepThreads, GC>(s, seq_begin, batch, q, out, qk_scale_log2, w, a, st);
+    KVC_POST_CASE(1)
+    KVC_POST_CASE(4)
+    KVC_POST_CASE(5)
+#undef KVC_POST_CASE
+    default:
+      return wide ? launch_step_post_nt<1024, 0>(s, seq_begin, batch, q, out, qk_scale_log2, w, a, st)
+                  : launch_step_post_nt<kStepThreads, 0>(s, seq_begin, batch, q, out, qk_scale_log2, w, a, st);
+  }
 }
 
 cudaError_t launch_step_moves(const DevState& s, int batch, const StepArgs& a, int sm_count, int max_moves,
