@@ -333,10 +333,16 @@ def gpu_arm(args):
 
     # trace events around every layer's split-K attention kernel
     tr = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(layers)]
-    for c, (a, b) in zip(caches, tr):
+    for a, b in tr:
         a.record()
         b.record()  # creates the underlying CUDA events
-        c.set_trace_events(a, b)
+
+    def set_tracing(on: bool):
+        for c, (a, b) in zip(caches, tr):
+            if on:
+                c.set_trace_events(a, b)
+            else:
+                c.set_trace_events(None, None)
 
     stream = torch.cuda.Stream(device=dev)
     # eager warm-up (sets kernel attributes), then capture one step
@@ -348,20 +354,33 @@ def gpu_arm(args):
         with torch.cuda.stream(stream):
             launches = step()
         torch.cuda.synchronize()
-    graph = None
+    # two graphs of the same step: the plain one is what the step time is
+    # taken from; the traced one has an event pair around every layer's
+    # split-K launch (event nodes add gaps between the kernels, so its step
+    # time is not used) and gives the split kernel's launch durations
+    graph = traced = None
     if not args.eager:
-        restore()
-        torch.cuda.synchronize()
-        resync()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            step()
-        torch.cuda.synchronize()
-        for _ in range(args.warmup):
+        for on in (False, True):
+            set_tracing(on)
             restore()
             torch.cuda.synchronize()
-            graph.replay()
-        torch.cuda.synchronize()
+            resync()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step()
+            torch.cuda.synchronize()
+            for _ in range(args.warmup):
+                restore()
+                torch.cuda.synchronize()
+                g.replay()
+            torch.cuda.synchronize()
+            if on:
+                traced = g
+            else:
+                graph = g
+        set_tracing(False)
+    else:
+        set_tracing(True)
 
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
@@ -385,6 +404,14 @@ def gpu_arm(args):
             ev1.record(stream)
             ev1.synchronize()
             step_ms.append(ev0.elapsed_time(ev1))
+            if graph is None:
+                attn_ms.extend(a.elapsed_time(b) for a, b in tr)
+        # the split kernel's launches, timed by the event nodes of the traced
+        # graph over as many steps
+        for _ in range(args.steps if traced is not None else 0):
+            restore()
+            traced.replay()
+            torch.cuda.synchronize()
             attn_ms.extend(a.elapsed_time(b) for a, b in tr)
     torch.cuda.synchronize()
     barrier(ws)
@@ -525,7 +552,7 @@ def gpu_arm(args):
                          "copy of all outputs, eager"),
                 "eager": {"value": kv_bytes * ws / (e2e_eager_step * 1e-3) / 1e9, "ms_per_step": e2e_eager_step,
                           "path": "the same calls launched one by one"}},
-        "gpu_launches": launches * args.steps,
+        "gpu_launches": launches * args.steps * (2 if traced is not None else 1),
         "clocks": clocks,
     }
     print(json.dumps(line))
@@ -773,20 +800,35 @@ def workload_report(args, name: str):
             c.sync_host()
 
     tr = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(layers)]
-    for c, (a, b) in zip(caches, tr):
+    for a, b in tr:
         a.record()
         b.record()
-        c.set_trace_events(a, b)
+
+    def set_tracing(on: bool):
+        for c, (a, b) in zip(caches, tr):
+            if on:
+                c.set_trace_events(a, b)
+            else:
+                c.set_trace_events(None, None)
+
     for _ in range(max(1, args.warmup)):
         restore()
         with torch.cuda.stream(stream):
             step()
         torch.cuda.synchronize()
-    restore()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        step()
-    torch.cuda.synchronize()
+    # the step time from a plain graph, the split kernel's launch durations
+    # from a graph with event nodes around them (which add gaps to the step)
+    graphs = {}
+    for on in (False, True):
+        set_tracing(on)
+        restore()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step()
+        torch.cuda.synchronize()
+        graphs[on] = g
+    set_tracing(False)
+    graph = graphs[False]
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     step_ms, attn_ms = [], []
     for _ in range(args.steps):
@@ -797,6 +839,11 @@ def workload_report(args, name: str):
             ev1.record(stream)
         ev1.synchronize()
         step_ms.append(ev0.elapsed_time(ev1))
+    for _ in range(args.steps):
+        restore()
+        with torch.cuda.stream(stream):
+            graphs[True].replay()
+        torch.cuda.synchronize()
         attn_ms.extend(a.elapsed_time(b) for a, b in tr)
     for c in caches:
         st = c.read_status()
