@@ -16,7 +16,7 @@ KVC_ERR_CUDA = 4
 KVC_ERR_DEVICE = 5
 KVC_ERR_STATE = 6
 
-KVC_VERSION = 300  # the header this binding's structures and signatures follow
+KVC_VERSION = 400  # the header this binding's structures and signatures follow
 KVC_ATTN_ACCUM_H2O = 0x1
 KVC_CODES_INT = 0
 KVC_CODES_E4M3 = 1
@@ -71,6 +71,8 @@ _SIGS = {
     "kvc_h2o_select_evict": (_I, [_P, _I, _I, ctypes.POINTER(KvcEvictParams), _P, _P, _SZ, _P]),
     "kvc_compact_blocks": (_I, [_P, _I, _I, _P, _P, _SZ, _P]),
     "kvc_decode_step": (_I, [_P, _I, _I, _P, _P, _P, _P, ctypes.c_float, ctypes.POINTER(KvcEvictParams), _P, _SZ, _P]),
+    "kvc_decode_step_overlap": (_I, [_P, _I, _I, _P, _P, _P, _P, ctypes.c_float, ctypes.POINTER(KvcEvictParams), _P,
+                                     _SZ, _P, _P]),
     "kvc_decode_attention_noalloc": (_I, [_P, _I, _I, _P, _P, ctypes.c_float, _I, _P]),
     "kvc_prefill_workspace_bytes": (_SZ, [_P, _I, _I]),
     "kvc_prefill_attention": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, ctypes.c_float, _I, _P, _SZ, _P]),

@@ -295,6 +295,39 @@ class KVCache:
                                          ctypes.c_void_p(_stream_ptr(stream))), "kvc_decode_step")
         return out
 
+    def decode_step_overlap(self, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, evict_stream,
+                            mode: str = "h2o", budget: int = 0, recent: int = 0, window: int = 0,
+                            seq_begin: int = 0, out=None, sm_scale: float | None = None, workspace=None,
+                            stream=None, retention: float = 1.0) -> torch.Tensor:
+        """`decode_step` with the eviction (scores, selection, compaction) on
+        `evict_stream`, after the output is ready on `stream`.  The workspace
+        stays in use until the eviction has run (one per cache); later calls
+        on this cache order themselves after it.  Inside a stream capture the
+        caller joins `evict_stream` back into `stream` before the capture
+        ends."""
+        _need(q, torch.bfloat16, "q", self.device)
+        _need(k_new, torch.bfloat16, "k_new", self.device)
+        _need(v_new, torch.bfloat16, "v_new", self.device)
+        batch = q.shape[0]
+        if q.dim() != 3 or q.shape[1] != self.num_q_heads or q.shape[2] != HEAD_DIM:
+            raise ValueError("q must be [batch, num_q_heads, 128]")
+        if tuple(k_new.shape) != (batch, self.num_kv_heads, 1, HEAD_DIM) or k_new.shape != v_new.shape:
+            raise ValueError("k_new, v_new must be [batch, num_kv_heads, 1, 128]")
+        if out is None:
+            out = torch.empty_like(q)
+        _need(out, torch.bfloat16, "out", self.device, q.shape)
+        ws = self.workspace(batch) if workspace is None else workspace
+        _need(ws, torch.uint8, "workspace", self.device)
+        scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
+        m = {"h2o": L.KVC_EVICT_H2O, "streaming": L.KVC_EVICT_STREAMING, "block": L.KVC_EVICT_BLOCK}[mode]
+        params = L.KvcEvictParams(m, budget, recent, window, retention)
+        L.check(self.lib.kvc_decode_step_overlap(
+            self.handle, seq_begin, batch, ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k_new.data_ptr()),
+            ctypes.c_void_p(v_new.data_ptr()), ctypes.c_void_p(out.data_ptr()), ctypes.c_float(scale),
+            ctypes.byref(params), ctypes.c_void_p(ws.data_ptr()), ws.numel(), ctypes.c_void_p(_stream_ptr(stream)),
+            ctypes.c_void_p(_stream_ptr(evict_stream))), "kvc_decode_step_overlap")
+        return out
+
     def step(self, q, k_new, v_new, mode="h2o", budget=0, recent=0, window=0, seq_begin=0, out=None,
              keep_mask=None, stream=None, retention=1.0):
         """One decode step of this layer: append -> attention (+H2O) -> select -> compact."""

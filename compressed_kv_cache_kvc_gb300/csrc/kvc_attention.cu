@@ -675,8 +675,9 @@ __global__ void __launch_bounds__(kWarps * 32) attn_split_kernel(DevState s, int
 }
 
 // Merge the stream-K partials and the bf16 sinks of one (sequence, KV head);
-// write the bf16 outputs of its G query heads; with H2O on, add this step's
-// probabilities to the sink scores and to every pool slot's score.
+// write the bf16 outputs of its G query heads and their (M, L) to w.stats;
+// add this step's probabilities to the sink scores (kMergeSinkScores) and
+// also to the bf16 window's and every pool slot's scores (kMergeAllScores).
 __global__ void __launch_bounds__(kMergeThreads, 2) attn_merge_kernel(DevState s, int seq_begin, int batch,
                                                                      const uint16_t* __restrict__ q,
                                                                      uint16_t* __restrict__ out,
@@ -687,8 +688,8 @@ __global__ void __launch_bounds__(kMergeThreads, 2) attn_merge_kernel(DevState s
   pages_prefix(s, seq_begin, batch, cum);
   const int h = blockIdx.x;
   const int bl = blockIdx.y;
-  merge_phase(s, seq_begin, batch, cum, h, bl, q, out, qk_scale_log2, w, accumulate != 0, ms);
-  if (!accumulate) return;
+  merge_phase(s, seq_begin, batch, cum, h, bl, q, out, qk_scale_log2, w, accumulate != kMergeNoScores, ms);
+  if (accumulate != kMergeAllScores) return;
   ring_score_pass(s, w, seq_begin + bl, bl, h, ms);
   // score pass: the sequence's block-table row is staged in shared memory
   // (when it fits) and each thread handles 4 slots with all loads issued first
@@ -777,9 +778,9 @@ cudaError_t launch_attention_split(const DevState& s, int seq_begin, int batch, 
 }
 
 cudaError_t launch_attention_merge(const DevState& s, int seq_begin, int batch, const uint16_t* q, uint16_t* out,
-                                   float qk_scale_log2, const AttnWork& w, bool accumulate, cudaStream_t st) {
+                                   float qk_scale_log2, const AttnWork& w, MergeScores scores, cudaStream_t st) {
   dim3 grid(s.hkv, batch);
-  attn_merge_kernel<<<grid, kMergeThreads, 0, st>>>(s, seq_begin, batch, q, out, qk_scale_log2, w, accumulate ? 1 : 0);
+  attn_merge_kernel<<<grid, kMergeThreads, 0, st>>>(s, seq_begin, batch, q, out, qk_scale_log2, w, (int)scores);
   return cudaGetLastError();
 }
 

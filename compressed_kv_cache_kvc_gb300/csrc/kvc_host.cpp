@@ -103,6 +103,14 @@ struct kvc_cache {
   void* trace_stop = nullptr;
   int32_t last_launches = 0;
   int sm_count = 0;
+  // kvc_decode_step_overlap: the merge's completion (the eviction stream
+  // waits for it) and the eviction's completion, still pending until a later
+  // call on this cache orders itself after it (created at the first such call)
+  cudaEvent_t merge_done = nullptr;
+  cudaEvent_t evict_done = nullptr;
+  bool evict_pending = false;
+  bool evict_in_capture = false;      // recorded while the streams were being captured
+  unsigned long long evict_capture_id = 0;
 };
 
 namespace {
@@ -313,6 +321,33 @@ int plan_keep(const kvc_evict_params* p, int S, int P, int W) {
 
 extern "C" {
 
+namespace {
+
+// Every call that touches a cache first orders `st` after the eviction a
+// kvc_decode_step_overlap call left running on its eviction stream: eager
+// after eager, or within one stream capture (a graph edge).  An eviction
+// recorded eagerly is waited for from inside a capture as an external event
+// node.  An eviction recorded in a capture belongs to that graph: its
+// launches are ordered by the caller, and the graph joins its eviction
+// stream before the capture ends.
+kvc_status order_after_eviction(kvc_cache* c, cudaStream_t st) {
+  if (!c->evict_pending) return KVC_OK;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  unsigned long long id = 0;
+  if (cudaStreamGetCaptureInfo(st, &cs, &id) != cudaSuccess) return KVC_ERR_CUDA;
+  const bool cap = cs == cudaStreamCaptureStatusActive;
+  cudaError_t e = cudaSuccess;
+  if (!cap && !c->evict_in_capture)
+    e = cudaStreamWaitEvent(st, c->evict_done, 0);
+  else if (cap && !c->evict_in_capture)
+    e = cudaStreamWaitEvent(st, c->evict_done, cudaEventWaitExternal);
+  else if (cap && id == c->evict_capture_id)
+    e = cudaStreamWaitEvent(st, c->evict_done, 0);
+  return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
+}
+
+}  // namespace
+
 int32_t kvc_version(void) { return KVC_VERSION; }
 
 const char* kvc_status_string(kvc_status s) {
@@ -381,7 +416,13 @@ kvc_status kvc_cache_create(const kvc_config* cfg, void* d_state, size_t state_b
   return KVC_OK;
 }
 
-void kvc_cache_destroy(kvc_cache* cache) { delete cache; }
+void kvc_cache_destroy(kvc_cache* cache) {
+  if (!cache) return;
+  // (an event may be destroyed with work pending: it is released once done)
+  if (cache->merge_done) cudaEventDestroy(cache->merge_done);
+  if (cache->evict_done) cudaEventDestroy(cache->evict_done);
+  delete cache;
+}
 
 kvc_status kvc_cache_buffer(const kvc_cache* c, int32_t which, void** d_ptr, size_t* bytes) {
   if (!c || which < 0 || which >= KVC_BUF_COUNT) return KVC_ERR_INVALID_ARG;
@@ -399,6 +440,10 @@ kvc_status kvc_cache_lengths(const kvc_cache* c, int32_t seq, int32_t* slots, in
 
 kvc_status kvc_cache_reset(kvc_cache* c, const int32_t* h_block_order, void* stream) {
   if (!c) return KVC_ERR_INVALID_ARG;
+  {
+    const kvc_status oe = order_after_eviction(c, static_cast<cudaStream_t>(stream));
+    if (oe != KVC_OK) return oe;
+  }
   const int nb = c->cfg.num_blocks;
   if (h_block_order) {
     std::vector<char> seen(nb, 0);
@@ -431,6 +476,10 @@ kvc_status kvc_cache_reset(kvc_cache* c, const int32_t* h_block_order, void* str
 
 kvc_status kvc_release_sequences(kvc_cache* c, int32_t seq_begin, int32_t batch, void* stream) {
   if (!c) return KVC_ERR_INVALID_ARG;
+  {
+    const kvc_status oe = order_after_eviction(c, static_cast<cudaStream_t>(stream));
+    if (oe != KVC_OK) return oe;
+  }
   c->last_launches = 0;
   if (!range_ok(c, seq_begin, batch)) return KVC_ERR_INVALID_ARG;
   bool any = false;
@@ -449,6 +498,10 @@ kvc_status kvc_release_sequences(kvc_cache* c, int32_t seq_begin, int32_t batch,
 
 kvc_status kvc_cache_sync_host(kvc_cache* c, void* stream) {
   if (!c) return KVC_ERR_INVALID_ARG;
+  {
+    const kvc_status oe = order_after_eviction(c, static_cast<cudaStream_t>(stream));
+    if (oe != KVC_OK) return oe;
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int mb = c->cfg.max_batch;
   std::vector<int32_t> s(mb), p(mb);
@@ -470,6 +523,10 @@ size_t kvc_workspace_bytes(const kvc_cache* c, int32_t batch) {
 kvc_status kvc_quantize_append(kvc_cache* c, int32_t seq_begin, int32_t batch, int32_t n_new, const void* d_k,
                                const void* d_v, void* stream) {
   if (!c) return KVC_ERR_INVALID_ARG;
+  {
+    const kvc_status oe = order_after_eviction(c, static_cast<cudaStream_t>(stream));
+    if (oe != KVC_OK) return oe;
+  }
   c->last_launches = 0;
   if (!range_ok(c, seq_begin, batch) || n_new < 0) return KVC_ERR_INVALID_ARG;
   if (n_new == 0) return KVC_OK;
@@ -515,6 +572,10 @@ kvc_status kvc_decode_attention(kvc_cache* c, int32_t seq_begin, int32_t batch, 
                                 float sm_scale, int32_t flags, void* d_workspace, size_t workspace_bytes,
                                 void* stream) {
   if (!c) return KVC_ERR_INVALID_ARG;
+  {
+    const kvc_status oe = order_after_eviction(c, static_cast<cudaStream_t>(stream));
+    if (oe != KVC_OK) return oe;
+  }
   c->last_launches = 0;
   if (flags & ~KVC_ATTN_ACCUM_H2O) return KVC_ERR_INVALID_ARG;
   kvc_status st0 = attention_check(c, seq_begin, batch, d_q, d_out, sm_scale, d_workspace, workspace_bytes, 0);
@@ -531,7 +592,8 @@ kvc_status kvc_decode_attention(kvc_cache* c, int32_t seq_begin, int32_t batch, 
   st0 = launch_ring(c, seq_begin, batch, d_q, qk_scale_log2, w, st, &launches);
   if (st0 != KVC_OK) return st0;
   if (kvc::launch_attention_merge(c->dev, seq_begin, batch, static_cast<const uint16_t*>(d_q),
-                                  static_cast<uint16_t*>(d_out), qk_scale_log2, w, h2o, st) != cudaSuccess)
+                                  static_cast<uint16_t*>(d_out), qk_scale_log2, w,
+                                  h2o ? kvc::kMergeAllScores : kvc::kMergeNoScores, st) != cudaSuccess)
     return KVC_ERR_CUDA;
   ++launches;
   c->last_launches = launches;
@@ -541,6 +603,10 @@ kvc_status kvc_decode_attention(kvc_cache* c, int32_t seq_begin, int32_t batch, 
 kvc_status kvc_h2o_select_evict(kvc_cache* c, int32_t seq_begin, int32_t batch, const kvc_evict_params* p,
                                 uint8_t* d_keep_mask, void* d_workspace, size_t workspace_bytes, void* stream) {
   if (!c) return KVC_ERR_INVALID_ARG;
+  {
+    const kvc_status oe = order_after_eviction(c, static_cast<cudaStream_t>(stream));
+    if (oe != KVC_OK) return oe;
+  }
   c->last_launches = 0;
   if (!range_ok(c, seq_begin, batch) || !p || !d_keep_mask) return KVC_ERR_INVALID_ARG;
   {
@@ -599,6 +665,10 @@ kvc_status kvc_h2o_select_evict(kvc_cache* c, int32_t seq_begin, int32_t batch, 
 kvc_status kvc_compact_blocks(kvc_cache* c, int32_t seq_begin, int32_t batch, const uint8_t* d_keep_mask,
                               void* d_workspace, size_t workspace_bytes, void* stream) {
   if (!c) return KVC_ERR_INVALID_ARG;
+  {
+    const kvc_status oe = order_after_eviction(c, static_cast<cudaStream_t>(stream));
+    if (oe != KVC_OK) return oe;
+  }
   c->last_launches = 0;
   if (!range_ok(c, seq_begin, batch) || !d_keep_mask) return KVC_ERR_INVALID_ARG;
   if (!c->plan_pending || c->plan_begin != seq_begin || c->plan_batch != batch) return KVC_ERR_STATE;
@@ -633,9 +703,22 @@ kvc_status kvc_compact_blocks(kvc_cache* c, int32_t seq_begin, int32_t batch, co
   return KVC_OK;
 }
 
-kvc_status kvc_decode_step(kvc_cache* c, int32_t seq_begin, int32_t batch, const void* d_q, const void* d_k_new,
-                           const void* d_v_new, void* d_out, float sm_scale, const kvc_evict_params* params,
-                           void* d_workspace, size_t workspace_bytes, void* stream) {
+namespace {
+
+kvc_status ensure_events(kvc_cache* c) {
+  if (!c->merge_done && cudaEventCreateWithFlags(&c->merge_done, cudaEventDisableTiming) != cudaSuccess)
+    return KVC_ERR_CUDA;
+  if (!c->evict_done && cudaEventCreateWithFlags(&c->evict_done, cudaEventDisableTiming) != cudaSuccess)
+    return KVC_ERR_CUDA;
+  return KVC_OK;
+}
+
+// The one-call decode step; with `overlap`, the merge runs on `stream` and
+// the eviction (scores, selection, compaction) on `evict_stream` after it.
+kvc_status decode_step_impl(kvc_cache* c, int32_t seq_begin, int32_t batch, const void* d_q, const void* d_k_new,
+                            const void* d_v_new, void* d_out, float sm_scale, const kvc_evict_params* params,
+                            void* d_workspace, size_t workspace_bytes, void* stream, void* evict_stream,
+                            bool overlap) {
   if (!c) return KVC_ERR_INVALID_ARG;
   c->last_launches = 0;
   {
@@ -662,6 +745,20 @@ kvc_status kvc_decode_step(kvc_cache* c, int32_t seq_begin, int32_t batch, const
   if (st0 != KVC_OK) return st0;
   st0 = launch_ring(c, seq_begin, batch, d_q, qk_scale_log2, w, st, &launches);
   if (st0 != KVC_OK) return st0;
+  // overlap: the merge (outputs, per-head (M, L), sink scores) on `stream`,
+  // then the eviction stream waits for it
+  cudaStream_t est = st;
+  if (overlap) {
+    if (ensure_events(c) != KVC_OK) return KVC_ERR_CUDA;
+    if (kvc::launch_attention_merge(c->dev, seq_begin, batch, static_cast<const uint16_t*>(d_q),
+                                    static_cast<uint16_t*>(d_out), qk_scale_log2, w,
+                                    h2o ? kvc::kMergeSinkScores : kvc::kMergeNoScores, st) != cudaSuccess)
+      return KVC_ERR_CUDA;
+    ++launches;
+    est = static_cast<cudaStream_t>(evict_stream);
+    if (cudaEventRecord(c->merge_done, st) != cudaSuccess || cudaStreamWaitEvent(est, c->merge_done, 0) != cudaSuccess)
+      return KVC_ERR_CUDA;
+  }
   std::vector<int32_t> plan(batch);
   int max_s = 0;
   for (int i = 0; i < batch; ++i) {
@@ -700,33 +797,56 @@ kvc_status kvc_decode_step(kvc_cache* c, int32_t seq_begin, int32_t batch, const
   for (int i = 0; i < batch; ++i)
     max_moves = std::max(max_moves, std::min(plan[i], c->slots[seq_begin + i] - plan[i]));
   a.inline_moves = !block && max_moves <= kvc::kInlineMoves;
+  a.merged = overlap ? 1 : 0;
   if (kvc::launch_step_post(c->dev, seq_begin, batch, static_cast<const uint16_t*>(d_q),
-                            static_cast<uint16_t*>(d_out), qk_scale_log2, w, a, sm_count(c), st) != cudaSuccess)
+                            static_cast<uint16_t*>(d_out), qk_scale_log2, w, a, sm_count(c), est) != cudaSuccess)
     return KVC_ERR_CUDA;
+  ++launches;
   if (block) {
     // page keys over the whole GPU, then one CTA per sequence selects and
     // drops its pages (no rows move)
     auto* keys = reinterpret_cast<unsigned long long*>(ws + wl.keys);
     if (kvc::launch_block_keys(c->dev, seq_begin, batch, params->recent,
-                               max_block_cand(c, seq_begin, batch, params->recent), keys, st) != cudaSuccess ||
-        kvc::launch_evict_blocks(c->dev, seq_begin, batch, params->recent, params->retention, keys, st) !=
+                               max_block_cand(c, seq_begin, batch, params->recent), keys, est) != cudaSuccess ||
+        kvc::launch_evict_blocks(c->dev, seq_begin, batch, params->recent, params->retention, keys, est) !=
             cudaSuccess)
       return KVC_ERR_CUDA;
-    launches += 3;
-    for (int i = 0; i < batch; ++i) c->slots[seq_begin + i] = plan[i];
-    c->plan_pending = false;
-    c->last_launches = launches;
-    return KVC_OK;
-  }
-  if (!a.inline_moves) {
-    if (kvc::launch_step_moves(c->dev, batch, a, sm_count(c), max_moves, st) != cudaSuccess) return KVC_ERR_CUDA;
+    launches += 2;
+  } else if (!a.inline_moves) {
+    if (kvc::launch_step_moves(c->dev, batch, a, sm_count(c), max_moves, est) != cudaSuccess) return KVC_ERR_CUDA;
     ++launches;
   }
-  ++launches;
+  if (overlap) {
+    // later calls on this cache order themselves after this event
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    unsigned long long id = 0;
+    if (cudaEventRecord(c->evict_done, est) != cudaSuccess || cudaStreamGetCaptureInfo(est, &cs, &id) != cudaSuccess)
+      return KVC_ERR_CUDA;
+    c->evict_pending = true;
+    c->evict_in_capture = cs == cudaStreamCaptureStatusActive;
+    c->evict_capture_id = id;
+  }
   for (int i = 0; i < batch; ++i) c->slots[seq_begin + i] = plan[i];
   c->plan_pending = false;
   c->last_launches = launches;
   return KVC_OK;
+}
+
+}  // namespace
+
+kvc_status kvc_decode_step(kvc_cache* c, int32_t seq_begin, int32_t batch, const void* d_q, const void* d_k_new,
+                           const void* d_v_new, void* d_out, float sm_scale, const kvc_evict_params* params,
+                           void* d_workspace, size_t workspace_bytes, void* stream) {
+  return decode_step_impl(c, seq_begin, batch, d_q, d_k_new, d_v_new, d_out, sm_scale, params, d_workspace,
+                          workspace_bytes, stream, stream, false);
+}
+
+kvc_status kvc_decode_step_overlap(kvc_cache* c, int32_t seq_begin, int32_t batch, const void* d_q,
+                                   const void* d_k_new, const void* d_v_new, void* d_out, float sm_scale,
+                                   const kvc_evict_params* params, void* d_workspace, size_t workspace_bytes,
+                                   void* stream, void* evict_stream) {
+  return decode_step_impl(c, seq_begin, batch, d_q, d_k_new, d_v_new, d_out, sm_scale, params, d_workspace,
+                          workspace_bytes, stream, evict_stream, true);
 }
 
 size_t kvc_prefill_workspace_bytes(const kvc_cache* c, int32_t batch, int32_t n) {
@@ -738,6 +858,10 @@ kvc_status kvc_prefill_attention(kvc_cache* c, int32_t seq_begin, int32_t batch,
                                  const void* d_k, const void* d_v, void* d_out, float sm_scale, int32_t flags,
                                  void* d_workspace, size_t workspace_bytes, void* stream) {
   if (!c) return KVC_ERR_INVALID_ARG;
+  {
+    const kvc_status oe = order_after_eviction(c, static_cast<cudaStream_t>(stream));
+    if (oe != KVC_OK) return oe;
+  }
   c->last_launches = 0;
   if (!range_ok(c, seq_begin, batch) || n <= 0 || (flags & ~KVC_ATTN_ACCUM_H2O)) return KVC_ERR_INVALID_ARG;
   if (!d_q || !d_out || !aligned(d_q, 16) || !aligned(d_out, 16) || !d_k || !d_v || !aligned(d_k, 16) ||
@@ -790,6 +914,10 @@ kvc_status kvc_prefill_context(kvc_cache* c, int32_t seq_begin, int32_t batch, i
                                const void* d_k, const void* d_v, void* d_out, float sm_scale, int32_t flags,
                                void* d_workspace, size_t workspace_bytes, void* stream) {
   if (!c) return KVC_ERR_INVALID_ARG;
+  {
+    const kvc_status oe = order_after_eviction(c, static_cast<cudaStream_t>(stream));
+    if (oe != KVC_OK) return oe;
+  }
   c->last_launches = 0;
   if (!range_ok(c, seq_begin, batch) || n <= 0 || (flags & ~KVC_ATTN_ACCUM_H2O)) return KVC_ERR_INVALID_ARG;
   if (!d_q || !d_out || !aligned(d_q, 16) || !aligned(d_out, 16) || !d_k || !d_v || !aligned(d_k, 16) ||
@@ -819,6 +947,10 @@ kvc_status kvc_prefill_context(kvc_cache* c, int32_t seq_begin, int32_t batch, i
 
 kvc_status kvc_read_status(kvc_cache* c, int32_t* h_status, void* stream) {
   if (!c || !h_status) return KVC_ERR_INVALID_ARG;
+  {
+    const kvc_status oe = order_after_eviction(c, static_cast<cudaStream_t>(stream));
+    if (oe != KVC_OK) return oe;
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int32_t v = 0;
   if (cudaMemcpyAsync(&v, c->dev.counters + kvc::kCtrStatus, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||

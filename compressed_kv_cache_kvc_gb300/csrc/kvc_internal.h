@@ -123,9 +123,11 @@ cudaError_t launch_attention_split(const DevState& s, int seq_begin, int batch, 
 // (sequence, KV head, chunk of kRingChunk slots), logits to w.ring_lg.
 cudaError_t launch_attention_ring(const DevState& s, int seq_begin, int batch, const uint16_t* q,
                                   float qk_scale_log2, const AttnWork& w, cudaStream_t st);
+// scores: which H2O scores the merge adds (the sink scores need the query).
+enum MergeScores { kMergeNoScores = 0, kMergeAllScores = 1, kMergeSinkScores = 2 };
 cudaError_t launch_attention_merge(const DevState& s, int seq_begin, int batch, const uint16_t* q,
-                                   uint16_t* out, float qk_scale_log2, const AttnWork& w,
-                                   bool accumulate_h2o, cudaStream_t st);
+                                   uint16_t* out, float qk_scale_log2, const AttnWork& w, MergeScores scores,
+                                   cudaStream_t st);
 
 struct SelectArgs {
   int mode, budget, recent, window;
@@ -188,6 +190,7 @@ struct StepArgs {
   int32_t* g_pos;       // likewise; then the source list
   int* n_moves;         // [batch][hkv] list lengths (post kernel -> move kernel)
   int inline_moves;     // the post kernel moves the rows itself (no move kernel follows)
+  int merged;           // the merge (and the sink scores) already ran: read each head's (M, L) from w.stats
 };
 // Pairs that move at most this many rows are moved inside the post kernel
 // (the steady state moves one row per pair).

@@ -108,8 +108,20 @@ __global__ void __launch_bounds__(NT, 1024 / NT) step_post_kernel(DevState s, in
     keys = a.g_keys + pair * a.s_cap;
     pos = a.g_pos + pair * a.s_cap;
   }
-  // (the merge's barriers publish the block-table row)
-  merge_phase(s, seq_begin, batch, w.cum, h, bl, q, out, qk_scale_log2, w, h2o, ms);
+  if (a.merged) {
+    // the merge ran on the attention's stream (kvc_decode_step_overlap):
+    // its per-head (M, L), and 1 / L as the merge forms it
+    if ((int)threadIdx.x < G) {
+      const float* st = w.stats + ((size_t)bl * s.hq + h * G + threadIdx.x) * 2;
+      const float L = st[1];
+      ms.M[threadIdx.x] = st[0];
+      ms.invL[threadIdx.x] = L > 0.0f ? 1.0f / L : 0.0f;
+    }
+    __syncthreads();  // publishes ms and the block-table row
+  } else {
+    // (the merge's barriers publish the block-table row)
+    merge_phase(s, seq_begin, batch, w.cum, h, bl, q, out, qk_scale_log2, w, h2o, ms);
+  }
   if (h2o) ring_score_pass(s, w, seq_begin + bl, bl, h, ms);
 
   const int P = s.seq_pos[b];

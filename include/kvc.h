@@ -14,7 +14,9 @@
  *   kvc_compact_blocks    move the kept tokens into the evicted slots and give
  *                         the emptied pages back to the pool.
  *
- * kvc_decode_step runs those four for one layer in one call.  Around them:
+ * kvc_decode_step runs those four for one layer in one call;
+ * kvc_decode_step_overlap does the same with the eviction on a second
+ * stream.  Around them:
  * kvc_prefill_attention (a fresh prompt's causal attention and the H2O scores
  * it gives), kvc_prefill_context (a prompt over sequences that hold context,
  * each query attending to the compressed cache), kvc_release_sequences (free
@@ -368,6 +370,32 @@ kvc_status kvc_decode_step(kvc_cache* cache, int32_t seq_begin, int32_t batch, c
                            const kvc_evict_params* params, void* d_workspace, size_t workspace_bytes,
                            void* stream);
 
+/* kvc_decode_step with the eviction off the output's path: the same results,
+ * bit for bit.  On `stream`: the append, the split-K attention and the merge
+ * (the outputs in d_out, each query head's softmax max and sum, and the sink
+ * scores).  On `evict_stream`, after the merge (an event the library
+ * records): the pool's (and the bf16 window's) score update, the selection,
+ * the compaction lists and the row moves.  What the caller enqueues next on
+ * `stream` (the next layer) overlaps the eviction.
+ *   - The workspace stays in use until the eviction has run: give every
+ *     cache (layer) its own.  d_q, d_k_new and d_v_new are read on `stream`
+ *     only.
+ *   - Every later call on this cache orders itself after the eviction: when
+ *     both are eager, or both inside the same stream capture, through the
+ *     library's event; an eviction enqueued eagerly is waited for from inside
+ *     a capture as an external event node.  An eviction captured into a
+ *     graph is ordered by the graph: before its capture ends, the caller
+ *     joins `evict_stream` back into the capturing stream (an event recorded
+ *     on `evict_stream` and waited on by `stream`), as CUDA requires.
+ *   - kvc_read_status, kvc_cache_sync_host and kvc_cache_reset on this cache
+ *     wait for the eviction on their stream.
+ *   - evict_stream may equal stream (then nothing overlaps).
+ * Launches: the four or five of kvc_decode_step, plus the merge. */
+kvc_status kvc_decode_step_overlap(kvc_cache* cache, int32_t seq_begin, int32_t batch, const void* d_q,
+                                   const void* d_k_new, const void* d_v_new, void* d_out, float sm_scale,
+                                   const kvc_evict_params* params, void* d_workspace, size_t workspace_bytes,
+                                   void* stream, void* evict_stream);
+
 /* Prefill of fresh sequences (the step before the decode path): append the
  * n prompt tokens of every sequence of the slice (exactly as
  * kvc_quantize_append), run the causal attention of the n queries over the
@@ -446,8 +474,9 @@ const char* kvc_status_string(kvc_status status);
 /* Library version: major * 10000 + minor * 100 + patch.  A caller built
  * against this header checks kvc_version() == KVC_VERSION before passing
  * structures (kvc_config grew in 0.2: bf16_window, codes;
- * kvc_prefill_context_workspace_bytes took the prompt length in 0.3). */
-#define KVC_VERSION 300
+ * kvc_prefill_context_workspace_bytes took the prompt length in 0.3;
+ * 0.4 added kvc_decode_step_overlap). */
+#define KVC_VERSION 400
 int32_t kvc_version(void);
 
 #ifdef __cplusplus

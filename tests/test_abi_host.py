@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_version_and_strings(lib):
     L = lib.lib()
-    assert L.kvc_version() == lib.KVC_VERSION == 300
+    assert L.kvc_version() == lib.KVC_VERSION == 400
     assert L.kvc_status_string(lib.KVC_ERR_CAPACITY) == b"out of cache capacity"
 
 
@@ -149,6 +149,16 @@ def test_call_validation_before_any_launch(lib):
         assert L.kvc_h2o_select_evict(h, 0, 1, ctypes.byref(prm), mask, wsp, ws, None) == lib.KVC_ERR_INVALID_ARG
     # compaction needs a pending selection
     assert L.kvc_compact_blocks(h, 0, 1, mask, wsp, ws, None) == lib.KVC_ERR_STATE
+    # the overlapped step checks its arguments as the one-call step does,
+    # before anything is enqueued on either stream
+    for prm in bad[:4]:
+        assert L.kvc_decode_step_overlap(h, 0, 1, dummy, dummy, dummy, dummy, ctypes.c_float(0.088),
+                                         ctypes.byref(prm), wsp, ws, None, None) == lib.KVC_ERR_INVALID_ARG
+    ok = lib.KvcEvictParams(0, 100, 8, 0)
+    assert L.kvc_decode_step_overlap(h, 0, 1, dummy, dummy, dummy, dummy, ctypes.c_float(0.088), ctypes.byref(ok),
+                                     wsp, ws - 1, None, None) == lib.KVC_ERR_INVALID_ARG
+    assert L.kvc_decode_step_overlap(h, 0, 1, dummy, dummy, dummy, dummy, ctypes.c_float(float("nan")),
+                                     ctypes.byref(ok), wsp, ws, None, None) == lib.KVC_ERR_INVALID_ARG
     # tracing events come in pairs
     assert L.kvc_set_trace_events(h, dummy, None) == lib.KVC_ERR_INVALID_ARG
     assert L.kvc_set_trace_events(h, None, None) == lib.KVC_OK
