@@ -304,10 +304,13 @@ def gpu_arm(args):
         snaps.append(c.state_view.clone())
         inputs.append((q, kn, vn))
     torch.cuda.synchronize()
+    # the one-call step shares one workspace; the overlapped step gives each
+    # layer its own (a layer's eviction still reads it while the next attends)
     ws_buf = caches[0].workspace(B)
     for c in caches:
         c._ws[ws_buf.numel()] = ws_buf
-    mask = caches[0].new_keep_mask(B)
+    wss = [ws_buf] + [torch.empty_like(ws_buf) for _ in range(layers - 1)]
+    evict_stream = torch.cuda.Stream(device=dev)
     outs = [torch.empty(B, Hq, 128, dtype=torch.bfloat16, device=dev) for _ in range(layers)]
     slots0 = caches[0].lengths(0)[0]  # pool slots before the step's append
     kv_bytes = kv_read_bytes_per_step(w, slots0 + 1, layers, batch=B)  # this rank's
@@ -316,15 +319,27 @@ def gpu_arm(args):
         for c, s in zip(caches, snaps):
             c.state_view.copy_(s, non_blocking=True)
 
-    def step(stream=None):
-        # one library call per layer: append, split-K attention, and the fused
-        # merge + H2O scores + selection + compaction kernel
+    def step(stream=None, overlap=not args.serial):
+        # one library call per layer.  Overlapped (the default): append,
+        # split-K attention and merge on `stream`; the layer's eviction (H2O
+        # scores, selection, compaction lists, row moves) on a second stream,
+        # running while the next layer attends; the eviction stream joins
+        # `stream` after the last layer.  Serial: kvc_decode_step, append,
+        # split-K attention, then the fused merge + scores + selection +
+        # compaction kernel, all on `stream`.
         n = 0
+        s = stream if stream is not None else torch.cuda.current_stream()
         for l, c in enumerate(caches):
             q, kn, vn = inputs[l]
-            c.decode_step(q, kn, vn, mode="h2o", budget=w.budget, recent=w.recent, out=outs[l], workspace=ws_buf,
-                          stream=stream)
+            if overlap:
+                c.decode_step_overlap(q, kn, vn, evict_stream, mode="h2o", budget=w.budget, recent=w.recent,
+                                      out=outs[l], workspace=wss[l], stream=s)
+            else:
+                c.decode_step(q, kn, vn, mode="h2o", budget=w.budget, recent=w.recent, out=outs[l],
+                              workspace=ws_buf, stream=s)
             n += c.last_launch_count()
+        if overlap:
+            s.wait_stream(evict_stream)
         return n
 
     def resync():
@@ -354,30 +369,36 @@ def gpu_arm(args):
         with torch.cuda.stream(stream):
             launches = step()
         torch.cuda.synchronize()
-    # two graphs of the same step: the plain one is what the step time is
-    # taken from; the traced one has an event pair around every layer's
-    # split-K launch (event nodes add gaps between the kernels, so its step
-    # time is not used) and gives the split kernel's launch durations
-    graph = traced = None
+    # graphs of the step: the plain one is what the step time is taken from;
+    # the traced ones have an event pair around every layer's split-K launch
+    # (event nodes add gaps between the kernels, so their step times are not
+    # used): with the eviction in line the split kernel has the GPU to itself
+    # (the roofline), overlapped it shares the GPU with the previous layer's
+    # eviction (its duration inside the step, reported beside)
+    graph = traced = traced_in_step = None
     if not args.eager:
-        for on in (False, True):
+        for on, ov in ((False, not args.serial), (True, False), (True, True)):
+            if on and ov and args.serial:
+                continue
             set_tracing(on)
             restore()
             torch.cuda.synchronize()
             resync()
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                step()
+                step(overlap=ov)
             torch.cuda.synchronize()
             for _ in range(args.warmup):
                 restore()
                 torch.cuda.synchronize()
                 g.replay()
             torch.cuda.synchronize()
-            if on:
+            if not on:
+                graph = g
+            elif not ov:
                 traced = g
             else:
-                graph = g
+                traced_in_step = g
         set_tracing(False)
     else:
         set_tracing(True)
@@ -389,7 +410,7 @@ def gpu_arm(args):
     torch.cuda.synchronize()
     if sampler:
         sampler.start()
-    step_ms, attn_ms = [], []
+    step_ms, attn_ms, attn_in_step_ms = [], [], []
     with torch.cuda.stream(stream):
         for _ in range(args.steps):
             restore()
@@ -413,7 +434,31 @@ def gpu_arm(args):
             traced.replay()
             torch.cuda.synchronize()
             attn_ms.extend(a.elapsed_time(b) for a, b in tr)
+        for _ in range(args.steps if traced_in_step is not None else 0):
+            restore()
+            traced_in_step.replay()
+            torch.cuda.synchronize()
+            attn_in_step_ms.extend(a.elapsed_time(b) for a, b in tr)
     torch.cuda.synchronize()
+    # for context: the same step with the eviction in line (kvc_decode_step)
+    serial_ms, launches_serial = [], 0
+    if graph is not None and not args.serial:
+        restore()
+        torch.cuda.synchronize()
+        resync()
+        g_serial = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_serial, stream=stream):
+            launches_serial = step(overlap=False)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for _ in range(args.steps):
+                restore()
+                ev0.record(stream)
+                g_serial.replay()
+                ev1.record(stream)
+                ev1.synchronize()
+                serial_ms.append(ev0.elapsed_time(ev1))
+        del g_serial
     barrier(ws)
     clocks = sampler.stop() if sampler else None
     total_ms = sum(step_ms)
@@ -457,10 +502,17 @@ def gpu_arm(args):
 
     def e2e_step_calls():
         d_in_all.copy_(h_in_all, non_blocking=True)
+        s = torch.cuda.current_stream()
         for l, c in enumerate(caches):
             q, kn, vn = d_in[l]
-            c.decode_step(q, kn, vn, mode="h2o", budget=w.budget, recent=w.recent, out=d_out_all[l],
-                          workspace=ws_buf)
+            if args.serial:
+                c.decode_step(q, kn, vn, mode="h2o", budget=w.budget, recent=w.recent, out=d_out_all[l],
+                              workspace=ws_buf)
+            else:
+                c.decode_step_overlap(q, kn, vn, evict_stream, mode="h2o", budget=w.budget, recent=w.recent,
+                                      out=d_out_all[l], workspace=wss[l], stream=s)
+        if not args.serial:
+            s.wait_stream(evict_stream)
         h_out_all.copy_(d_out_all, non_blocking=True)
 
     e_steps = max(1, min(args.steps, 10))
@@ -535,24 +587,37 @@ def gpu_arm(args):
                    "context": T, "layers": layers, "bits": w.bits, "budget": w.budget, "recent": w.recent,
                    "parallelism": f"batch-split{ws}" if args.split == "batch" else f"replicas{ws}",
                    "l2": "state restore copy (>L2) between timed steps",
-                   "cuda_graph": graph is not None},
+                   "cuda_graph": graph is not None,
+                   "eviction": ("in line (kvc_decode_step)" if args.serial else
+                                "on a second stream (kvc_decode_step_overlap), overlapping the next layer")},
         "seq_steps_per_s": seq_steps,
         "kv_bytes_per_step": kv_bytes,
         "frac_of_hbm_peak": value / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "kernel": "attn_split_kernel<4>", "bytes_per_launch": attn_bytes,
-                     "avg_launch_ms": attn_avg_ms, "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)"},
+                     "avg_launch_ms": attn_avg_ms, "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)",
+                     "timed_in": ("the one-call step (eviction in line): the kernel has the GPU to itself"
+                                  if traced is not None else "the timed steps"),
+                     "avg_launch_ms_in_overlapped_step": (sum(attn_in_step_ms) / len(attn_in_step_ms)
+                                                          if attn_in_step_ms else None)},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_step,
-                "path": ("one H2D copy of all layers' inputs from pinned host memory, KVCache.decode_step "
-                         "per layer, one D2H copy of all outputs; captured once into a CUDA graph and "
-                         "replayed every step" if graph is not None else
-                         "one H2D copy of all layers' inputs, KVCache.decode_step per layer, one D2H "
-                         "copy of all outputs, eager"),
+                "path": (("one H2D copy of all layers' inputs from pinned host memory, %s per layer, one D2H "
+                          "copy of all outputs; captured once into a CUDA graph and replayed every step"
+                          if graph is not None else
+                          "one H2D copy of all layers' inputs, %s per layer, one D2H copy of all outputs, eager")
+                         % ("KVCache.decode_step" if args.serial
+                            else "KVCache.decode_step_overlap (eviction on a second stream)")),
                 "eager": {"value": kv_bytes * ws / (e2e_eager_step * 1e-3) / 1e9, "ms_per_step": e2e_eager_step,
                           "path": "the same calls launched one by one"}},
-        "gpu_launches": launches * args.steps * (2 if traced is not None else 1),
+        "one_call_step": ({"ms_per_step": sum(serial_ms) / len(serial_ms),
+                           "value": kv_bytes_all / (sum(serial_ms) / len(serial_ms) * 1e-3) / 1e9,
+                           "path": "kvc_decode_step per layer (eviction in line), CUDA graph"}
+                          if serial_ms else None),
+        "gpu_launches": launches * args.steps + (launches_serial or launches) * len(serial_ms)
+        + ((launches_serial or launches) * args.steps if traced is not None else 0)
+        + (launches * args.steps if traced_in_step is not None else 0),
         "clocks": clocks,
     }
     print(json.dumps(line))
@@ -748,6 +813,9 @@ def workload_report(args, name: str):
         inputs.append((q, kn, vn))
     torch.cuda.synchronize()  # the prefill ran on the default stream; the steps run on their own
     ws_buf = caches[0].workspace(B)
+    # overlapped eviction (the default): one workspace per layer
+    wss = [ws_buf] + ([torch.empty_like(ws_buf) for _ in range(layers - 1)] if not args.serial else [])
+    evict_stream = torch.cuda.Stream(device=dev)
     outs = [torch.empty(B, Hq, 128, dtype=torch.bfloat16, device=dev) for _ in range(layers)]
     budgets = [w.budget] * layers
     if args.schedule and w.mode == "h2o":
@@ -758,15 +826,22 @@ def workload_report(args, name: str):
             budgets = pyramid_budgets(layers, "quadratic", recent=w.recent, context=w.context,
                                       base_ratio=w.budget / w.context)
 
-    def step(stream=None):
+    def step(stream=None, overlap=not args.serial):
+        # overlapped: each layer's eviction on a second stream (joined after
+        # the last layer); serial: kvc_decode_step, all on `stream`
+        s = stream if stream is not None else torch.cuda.current_stream()
         for l, c in enumerate(caches):
             q, kn, vn = inputs[l]
             if args.evict == "block":
-                c.decode_step(q, kn, vn, mode="block", recent=w.recent, retention=args.retention,
-                              out=outs[l], workspace=ws_buf, stream=stream)
+                kw = dict(mode="block", recent=w.recent, retention=args.retention, out=outs[l])
             else:
-                c.decode_step(q, kn, vn, mode=w.mode, budget=budgets[l], recent=w.recent, window=w.window,
-                              out=outs[l], workspace=ws_buf, stream=stream)
+                kw = dict(mode=w.mode, budget=budgets[l], recent=w.recent, window=w.window, out=outs[l])
+            if overlap:
+                c.decode_step_overlap(q, kn, vn, evict_stream, workspace=wss[l], stream=s, **kw)
+            else:
+                c.decode_step(q, kn, vn, workspace=ws_buf, stream=s, **kw)
+        if overlap:
+            s.wait_stream(evict_stream)
 
     stream = torch.cuda.Stream(device=dev)
     if w.mode == "streaming":
@@ -817,14 +892,15 @@ def workload_report(args, name: str):
             step()
         torch.cuda.synchronize()
     # the step time from a plain graph, the split kernel's launch durations
-    # from a graph with event nodes around them (which add gaps to the step)
+    # from a graph of the step with the eviction in line and event nodes
+    # around the split launches (which add gaps to the step)
     graphs = {}
     for on in (False, True):
         set_tracing(on)
         restore()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            step()
+            step(overlap=(not args.serial) and not on)
         torch.cuda.synchronize()
         graphs[on] = g
     set_tracing(False)
@@ -868,7 +944,8 @@ def workload_report(args, name: str):
                            "split_us_per_layer": attn * 1e3,
                            "split_gbs": split_bytes / layers / (attn * 1e-3) / 1e9,
                            "split_frac_of_peak": split_bytes / layers / (attn * 1e-3) / 1e9 / peak},
-            "peak_gbs": peak, "steps_timed": args.steps}
+            "peak_gbs": peak, "steps_timed": args.steps,
+            "eviction": "in line" if args.serial else "on a second stream, overlapping the next layer"}
     if w.steps > 1:
         # the workload's consecutive steps from the prefill, without restoring
         restore()
@@ -941,6 +1018,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling only)")
     ap.add_argument("--eager", action="store_true", help="launch each call instead of replaying a CUDA graph")
+    ap.add_argument("--serial", action="store_true",
+                    help="the one-call step with the eviction in line (default: the eviction on a second stream)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=None,
                     help="report mode: time this workload (or 'all') instead of printing the bench line")

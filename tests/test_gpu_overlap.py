@@ -68,7 +68,7 @@ CASES = [
     (8, 32, 8, [700, 100, 257, 260], "streaming", 0, 0, 256, 1.0, "int", 0, 3),
     (8, 16, 4, [600, 333], "block", 0, 40, 0, 0.5, "int", 0, 3),
     (8, 16, 4, [900, 200], "h2o", 300, 64, 0, 1.0, "e4m3", 0, 3),
-    (4, 16, 4, [800, 300, 90], "h2o", 400, 64, 0, 1.0, "int", 128, 3),
+    (4, 16, 4, [800, 300, 90], "h2o", 400, 160, 0, 1.0, "int", 128, 3),  # recent >= the window
     (8, 8, 2, [21000, 300], "h2o", 2100, 256, 0, 1.0, "int", 0, 2),
     (4, 8, 2, [41000], "h2o", 4100, 512, 0, 1.0, "int", 0, 2),
 ]
