@@ -682,13 +682,12 @@ __global__ void __launch_bounds__(kMergeThreads, 2) attn_merge_kernel(DevState s
                                                                      const uint16_t* __restrict__ q,
                                                                      uint16_t* __restrict__ out,
                                                                      float qk_scale_log2, AttnWork w, int accumulate) {
-  __shared__ int cum[kMaxCallBatch + 1];
   __shared__ MergeShared ms;
   __shared__ int32_t sh_bt[kMergeBtStage];
-  pages_prefix(s, seq_begin, batch, cum);
   const int h = blockIdx.x;
   const int bl = blockIdx.y;
-  merge_phase(s, seq_begin, batch, cum, h, bl, q, out, qk_scale_log2, w, accumulate != kMergeNoScores, ms);
+  // the page prefix of the slice, as the split kernel's first CTA published it
+  merge_phase(s, seq_begin, batch, w.cum, h, bl, q, out, qk_scale_log2, w, accumulate != kMergeNoScores, ms);
   if (accumulate != kMergeAllScores) return;
   ring_score_pass(s, w, seq_begin + bl, bl, h, ms);
   // score pass: the sequence's block-table row is staged in shared memory

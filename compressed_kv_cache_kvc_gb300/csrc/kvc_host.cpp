@@ -587,7 +587,10 @@ kvc_status kvc_decode_attention(kvc_cache* c, int32_t seq_begin, int32_t batch, 
   const bool h2o = (flags & KVC_ATTN_ACCUM_H2O) != 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int launches = 0;
-  st0 = launch_split_traced(c, seq_begin, batch, d_q, qk_scale_log2, w, h2o, total_pages, st, &launches);
+  // (launched even with no pool pages: its first CTA publishes the page
+  // prefix the merge reads)
+  st0 = launch_split_traced(c, seq_begin, batch, d_q, qk_scale_log2, w, h2o, total_pages, st, &launches,
+                            /*always=*/true);
   if (st0 != KVC_OK) return st0;
   st0 = launch_ring(c, seq_begin, batch, d_q, qk_scale_log2, w, st, &launches);
   if (st0 != KVC_OK) return st0;
