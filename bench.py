@@ -315,9 +315,16 @@ def gpu_arm(args):
     slots0 = caches[0].lengths(0)[0]  # pool slots before the step's append
     kv_bytes = kv_read_bytes_per_step(w, slots0 + 1, layers, batch=B)  # this rank's
 
+    # a read of 512 MB after each restore (untimed): the restore's copy
+    # leaves L2 full of dirty lines, which would otherwise be written back
+    # while the first layer runs
+    flush_buf = torch.ones(128 * 1024 * 1024, dtype=torch.float32, device=dev)
+    flush_out = torch.empty((), dtype=torch.float32, device=dev)
+
     def restore():
         for c, s in zip(caches, snaps):
             c.state_view.copy_(s, non_blocking=True)
+        torch.sum(flush_buf, dim=0, out=flush_out)
 
     def step(stream=None, overlap=not args.serial):
         # one library call per layer.  Overlapped (the default): append,
@@ -586,7 +593,7 @@ def gpu_arm(args):
         "config": {"workload": WORKLOAD, "batch": B, "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": 128,
                    "context": T, "layers": layers, "bits": w.bits, "budget": w.budget, "recent": w.recent,
                    "parallelism": f"batch-split{ws}" if args.split == "batch" else f"replicas{ws}",
-                   "l2": "state restore copy (>L2) between timed steps",
+                   "l2": "state restore copy (>L2), then a 512 MB read, between timed steps",
                    "cuda_graph": graph is not None,
                    "eviction": ("in line (kvc_decode_step)" if args.serial else
                                 "on a second stream (kvc_decode_step_overlap), overlapping the next layer")},
@@ -867,9 +874,13 @@ def workload_report(args, name: str):
     kv_bytes = step_kv_bytes()
     split_bytes = step_kv_bytes(pool_only=True)
 
+    flush_buf = torch.ones(128 * 1024 * 1024, dtype=torch.float32, device=dev)
+    flush_out = torch.empty((), dtype=torch.float32, device=dev)
+
     def restore():
         for c, sn in zip(caches, snaps):
             c.state_view.copy_(sn, non_blocking=True)
+        torch.sum(flush_buf, dim=0, out=flush_out)  # L2: clean lines (see gpu_arm)
         torch.cuda.synchronize()
         for c in caches:
             c.sync_host()
