@@ -21,7 +21,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libkvc.so")
 
 SOURCES = ["kvc_host.cpp", "kvc_append.cu", "kvc_attention.cu", "kvc_ring.cu", "kvc_select.cu", "kvc_step.cu",
-           "kvc_prefill.cu", "kvc_context.cu", "kvc_noalloc.cu"]
+           "kvc_prefill.cu", "kvc_prefill_tc.cu", "kvc_context.cu", "kvc_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-lineinfo", f"-I{INCLUDE}", f"-I{CSRC}"]
 

@@ -64,6 +64,7 @@ constexpr int kDevBadKeepMask = 0x4;
 constexpr int kDevTableOverflow = 0x8;
 constexpr int kDevStackOverflow = 0x10;
 constexpr int kDevStaleHost = 0x20;
+constexpr int kDevWaitTimeout = 0x40;
 
 // Scratch carved from the caller's workspace for one attention call.
 //
@@ -164,6 +165,12 @@ int compact_max_smem_moves();
 // Prefill of fresh sequences: causal attention over the prompt's bf16 K/V
 // (output bf16 [batch][hq][n][128], row statistics to `stats`
 // [batch][hq][n][2]) and, with `scores`, the H2O scores of its tokens.
+// The forward on tcgen05 (kvc_prefill_tc.cu): outputs and row statistics as
+// the mma.sync forward's.
+cudaError_t launch_prefill_fwd_tc(const DevState& s, int batch, int n, const uint16_t* q, const uint16_t* k,
+                                  const uint16_t* v, uint16_t* out, float* stats, float qk_scale_log2,
+                                  cudaStream_t st);
+int prefill_fwd_tc_smem_bytes();
 cudaError_t launch_prefill(const DevState& s, int seq_begin, int batch, int n, const uint16_t* q, const uint16_t* k,
                            const uint16_t* v, uint16_t* out, float* stats, float qk_scale_log2, bool scores,
                            cudaStream_t st);

@@ -6,22 +6,15 @@
 // tokens are stored quantised (or in the bf16 window) by the append that runs
 // first, and the scores initialise the decode steps' H2O accumulation.
 //
-// Two kernels, both on mma.sync m16n8k16 with bf16 operands and fp32
-// accumulation (the query and key bits multiply exactly):
-//
-// prefill_fwd_kernel, one 128-thread CTA per (64-query tile, query head,
-// sequence): the Q tile and double-buffered 64-key K/V tiles in shared memory
-// (cp.async, rows padded to 272 bytes so ldmatrix is conflict-free); per key
-// tile S = Q K^T (each warp 16 queries x 64 keys), the causal mask, an online
-// softmax in the log2 domain, and O += P V with the S fragments reused as the
-// A operand, P split into two bf16 parts (hi = bf16(p), lo = bf16(p - hi),
-// exact in fp32) so that it carries 16 significant bits.  It writes the bf16
-// output and each query row's (max, sum).
+// Two kernels: the forward on tcgen05 (kvc_prefill_tc.cu: the bf16 output
+// and each query row's (max, sum)), then the scores here, on mma.sync
+// m16n8k16 with bf16 operands and fp32 accumulation (the query and key bits
+// multiply exactly):
 //
 // prefill_scores_kernel, one 128-thread CTA per (64-key tile, KV head,
 // sequence): the K tile stays in shared memory while the CTA walks every
 // query tile at or after it of every query head of the group (Q tiles double
-// buffered), recomputes S exactly as the forward kernel did, turns it into
+// buffered), recomputes S (the same exact products, summed in fp32), turns it into
 // probabilities with the forward's row statistics, and sums them over the
 // query rows; the column sums land in the tokens' score slots (sinks, pool
 // or bf16 window).
@@ -42,12 +35,6 @@ constexpr int kPfThreads = 128;
 constexpr int kPfTile = 64;
 constexpr int kPfRow = kHeadDim + 8;  // bf16 per staged row (272 bytes)
 typedef uint16_t PfTile[kPfTile][kPfRow];
-
-struct PfFwdSmem {
-  PfTile q;
-  PfTile k[2];
-  PfTile v[2];
-};
 
 struct PfScoreSmem {
   PfTile k;
@@ -88,12 +75,6 @@ __device__ __forceinline__ void ldsm_x4(uint32_t& a0, uint32_t& a1, uint32_t& a2
                : "r"(smem_addr(p)));
 }
 
-__device__ __forceinline__ void ldsm_x4_t(uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3, const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];\n"
-               : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
-               : "r"(smem_addr(p)));
-}
-
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -101,14 +82,6 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
       "{%0, %1, %2, %3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// bf16 pair (x low, y high) and its remainder pair
-__device__ __forceinline__ void split_bf16x2(float x, float y, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
-  const __nv_bfloat162 l = __floats2bfloat162_rn(x - __low2float(h), y - __high2float(h));
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
 // Q fragments (A operand) of this warp's 16 rows, all 8 k-steps.
@@ -131,129 +104,6 @@ __device__ __forceinline__ void qk_tile(const uint32_t (&qa)[8][4], const PfTile
       mma_bf16(sc[nt], qa[2 * kp][0], qa[2 * kp][1], qa[2 * kp][2], qa[2 * kp][3], b0, b1);
       mma_bf16(sc[nt], qa[2 * kp + 1][0], qa[2 * kp + 1][1], qa[2 * kp + 1][2], qa[2 * kp + 1][3], b2, b3);
     }
-  }
-}
-
-__global__ void __launch_bounds__(kPfThreads) prefill_fwd_kernel(DevState s, int n, const uint16_t* __restrict__ q,
-                                                                 const uint16_t* __restrict__ k,
-                                                                 const uint16_t* __restrict__ v,
-                                                                 uint16_t* __restrict__ out, float* __restrict__ stats,
-                                                                 float qk_scale_log2) {
-  extern __shared__ __align__(16) uint8_t pf_smem[];
-  PfFwdSmem& sm = *reinterpret_cast<PfFwdSmem*>(pf_smem);
-  const int qt = blockIdx.x, hqi = blockIdx.y, bl = blockIdx.z;
-  const int hkvi = hqi / s.group;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int r = lane >> 2, c = lane & 3;
-  const size_t qrow0 = ((size_t)bl * s.hq + hqi) * n;
-  const uint16_t* kb = k + ((size_t)bl * s.hkv + hkvi) * n * kHeadDim;
-  const uint16_t* vb = v + ((size_t)bl * s.hkv + hkvi) * n * kHeadDim;
-  const int q0 = qt * kPfTile;
-  const int n_kt = qt + 1;  // key tiles 0 .. qt (causal)
-
-  load_tile(sm.q, q + (qrow0 + q0) * kHeadDim, min(kPfTile, n - q0));
-  load_tile(sm.k[0], kb, min(kPfTile, n));
-  load_tile(sm.v[0], vb, min(kPfTile, n));
-  cp_commit();
-
-  uint32_t qa[8][4];
-  float o[16][4];
-#pragma unroll
-  for (int dt = 0; dt < 16; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.0f;
-  float m[2] = {kNegBig, kNegBig}, l[2] = {0.0f, 0.0f};
-  const int qi0 = q0 + 16 * warp + r;  // query of rows e < 2; +8 for e >= 2
-
-  for (int j = 0; j < n_kt; ++j) {
-    if (j + 1 < n_kt) {
-      const int k0 = (j + 1) * kPfTile;
-      load_tile(sm.k[(j + 1) & 1], kb + (size_t)k0 * kHeadDim, min(kPfTile, n - k0));
-      load_tile(sm.v[(j + 1) & 1], vb + (size_t)k0 * kHeadDim, min(kPfTile, n - k0));
-    }
-    cp_commit();
-    cp_wait<1>();
-    __syncthreads();
-    if (j == 0) load_q_frags(sm.q, warp, lane, qa);
-    const PfTile& sk = sm.k[j & 1];
-    const PfTile& sv = sm.v[j & 1];
-
-    float sc[8][4];
-    qk_tile(qa, sk, lane, sc);
-    const int k0 = j * kPfTile;
-    float mx[2] = {kNegBig, kNegBig};
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int ki = k0 + 8 * nt + 2 * c + (e & 1);
-        const int qi = qi0 + (e >= 2 ? 8 : 0);
-        const float x = (ki <= qi && ki < n) ? sc[nt][e] * qk_scale_log2 : -INFINITY;
-        sc[nt][e] = x;
-        mx[e >> 1] = fmaxf(mx[e >> 1], x);
-      }
-    }
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
-      mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
-      const float mn = fmaxf(m[rr], mx[rr]);
-      const float alpha = fast_exp2(m[rr] - mn);
-      m[rr] = mn;
-      l[rr] *= alpha;
-#pragma unroll
-      for (int dt = 0; dt < 16; ++dt) {
-        o[dt][2 * rr] *= alpha;
-        o[dt][2 * rr + 1] *= alpha;
-      }
-    }
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float p = fast_exp2(sc[nt][e] - m[e >> 1]);
-        sc[nt][e] = p;
-        l[e >> 1] += p;
-      }
-    }
-    // O += P V: the S fragments of key n-tiles 2 kk and 2 kk + 1 form the A
-    // operand of k-step kk; V by ldmatrix.trans, two 8-dim tiles per load
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      uint32_t ah[4], al[4];
-      split_bf16x2(sc[2 * kk][0], sc[2 * kk][1], ah[0], al[0]);
-      split_bf16x2(sc[2 * kk][2], sc[2 * kk][3], ah[1], al[1]);
-      split_bf16x2(sc[2 * kk + 1][0], sc[2 * kk + 1][1], ah[2], al[2]);
-      split_bf16x2(sc[2 * kk + 1][2], sc[2 * kk + 1][3], ah[3], al[3]);
-#pragma unroll
-      for (int dp = 0; dp < 8; ++dp) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(b0, b1, b2, b3, &sv[16 * kk + (lane & 7) + ((lane >> 3) & 1) * 8][16 * dp + (lane >> 4) * 8]);
-        mma_bf16(o[2 * dp], ah[0], ah[1], ah[2], ah[3], b0, b1);
-        mma_bf16(o[2 * dp], al[0], al[1], al[2], al[3], b0, b1);
-        mma_bf16(o[2 * dp + 1], ah[0], ah[1], ah[2], ah[3], b2, b3);
-        mma_bf16(o[2 * dp + 1], al[0], al[1], al[2], al[3], b2, b3);
-      }
-    }
-    __syncthreads();  // the next iteration's copies overwrite the other buffers
-  }
-  cp_wait<0>();
-
-#pragma unroll
-  for (int rr = 0; rr < 2; ++rr) {
-    l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 1);
-    l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 2);
-  }
-#pragma unroll
-  for (int rr = 0; rr < 2; ++rr) {
-    const int qi = qi0 + 8 * rr;
-    if (qi >= n) continue;
-    const float inv = 1.0f / l[rr];
-    uint16_t* orow = out + (qrow0 + qi) * kHeadDim;
-#pragma unroll
-    for (int dt = 0; dt < 16; ++dt) {
-      const __nv_bfloat162 pr = __floats2bfloat162_rn(o[dt][2 * rr] * inv, o[dt][2 * rr + 1] * inv);
-      *reinterpret_cast<__nv_bfloat162*>(orow + 8 * dt + 2 * c) = pr;
-    }
-    if (c == 0) *reinterpret_cast<float2*>(stats + (qrow0 + qi) * 2) = make_float2(m[rr], l[rr]);
   }
 }
 
@@ -362,21 +212,15 @@ __global__ void __launch_bounds__(kPfThreads) prefill_scores_kernel(DevState s, 
 
 }  // namespace
 
-int prefill_fwd_smem_bytes() { return (int)sizeof(PfFwdSmem); }
 int prefill_scores_smem_bytes() { return (int)sizeof(PfScoreSmem); }
 
 cudaError_t launch_prefill(const DevState& s, int seq_begin, int batch, int n, const uint16_t* q, const uint16_t* k,
                            const uint16_t* v, uint16_t* out, float* stats, float qk_scale_log2, bool scores,
                            cudaStream_t st) {
-  static int done_fwd[64] = {0};
   static int done_sc[64] = {0};
-  cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(prefill_fwd_kernel), prefill_fwd_smem_bytes(), done_fwd);
-  if (e != cudaSuccess) return e;
-  const int tiles = (n + kPfTile - 1) / kPfTile;
-  prefill_fwd_kernel<<<dim3(tiles, s.hq, batch), kPfThreads, prefill_fwd_smem_bytes(), st>>>(s, n, q, k, v, out,
-                                                                                            stats, qk_scale_log2);
-  e = cudaGetLastError();
+  cudaError_t e = launch_prefill_fwd_tc(s, batch, n, q, k, v, out, stats, qk_scale_log2, st);
   if (e != cudaSuccess || !scores) return e;
+  const int tiles = (n + kPfTile - 1) / kPfTile;
   e = opt_in_smem(reinterpret_cast<const void*>(prefill_scores_kernel), prefill_scores_smem_bytes(), done_sc);
   if (e != cudaSuccess) return e;
   prefill_scores_kernel<<<dim3(tiles, s.hkv, batch), kPfThreads, prefill_scores_smem_bytes(), st>>>(

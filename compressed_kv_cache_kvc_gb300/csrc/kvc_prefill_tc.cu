@@ -1,0 +1,351 @@
+// Prefill forward on the fifth-generation tensor cores: the causal attention
+// of a fresh prompt over itself (Technical Report section 1.1), with S = Q K^T
+// and O = P V by tcgen05.mma (bf16 operands, fp32 accumulators in tensor
+// memory) instead of mma.sync.  Same inputs, outputs and row statistics as
+// the mma.sync forward it replaces; the H2O scores still come from
+// prefill_scores_kernel (kvc_prefill.cu), which uses these statistics.
+//
+// One 128-thread CTA per (128-query tile, query head, sequence); thread t
+// owns query row t, which is TMEM lane t.  Per 64-key tile (up to the
+// diagonal):
+//   * K rows by cp.async into the operand layout (K-major, no swizzle:
+//     8-row x 16-byte core matrices), V rows into a padded staging tile,
+//     transposed by ldmatrix.trans into a dims x keys operand;
+//   * one thread issues S = Q K^T (M 128, N 64, 8 MMAs of K 16) into TMEM
+//     columns [0, 64), commits to an mbarrier;
+//   * each thread reads its row of S (tcgen05.ld), masks, and runs the
+//     online softmax in the log2 domain with a lazy maximum (O in TMEM is
+//     rescaled only when the row maximum grows by more than 8);
+//   * P = hi + lo (two bf16 parts, 16 significant bits) into shared memory;
+//     one thread issues O += P_hi V + P_lo V (M 128, N 128, K 64) into
+//     columns [128, 256).
+// Every mbarrier wait is bounded; a wait that runs out sets
+// KVC_DEV_WAIT_TIMEOUT, and the CTA stops after freeing its tensor memory.
+#include <cuda_bf16.h>
+
+#include "kvc_device.h"
+#include "kvc_internal.h"
+
+namespace kvc {
+namespace {
+
+using namespace dev;
+
+constexpr int kTcThreads = 128;      // one thread per query row (TMEM lane)
+constexpr int kTcQ = 128;            // queries per CTA (the MMAs' M)
+constexpr int kTcKeys = 64;          // keys per tile
+constexpr int kTcVRow = kHeadDim + 8;  // staged V rows: 272 bytes (conflict-free ldmatrix)
+constexpr float kTcLazy = 8.0f;      // log2 units the running maximum may lag
+constexpr uint32_t kTcCols = 256;    // TMEM columns: S [0, 64), O [128, 256)
+constexpr uint32_t kTcO = 128;
+constexpr int kTcWaitLimit = 1 << 22;
+
+constexpr int kOffQ = 0;                                     // 32 KB: Q, operand layout
+constexpr int kOffK = kOffQ + kTcQ * kHeadDim * 2;           // 16 KB: K, then P hi
+constexpr int kOffV = kOffK + kTcKeys * kHeadDim * 2;        // 17 KB: staged V, then P lo
+constexpr int kOffVt = kOffV + kTcKeys * kTcVRow * 2;        // 16 KB: V^T, operand layout
+constexpr int kOffBar = kOffVt + kHeadDim * kTcKeys * 2;     // mbarrier, TMEM base
+constexpr int kTcSmem = kOffBar + 16;
+
+__device__ __forceinline__ uint32_t saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// Byte offset of 16-byte chunk c (elements 8c .. 8c + 7) of row r in the
+// operand layout of a tile with `kch` chunks per row: core matrices of 8 rows
+// x 16 bytes, row groups kch * 128 bytes apart, chunks 128 bytes apart.
+__device__ __forceinline__ int core_off(int r, int c, int kch) { return ((r >> 3) * kch + c) * 128 + (r & 7) * 16; }
+
+// Shared-memory operand descriptor: K-major, no swizzle; leading byte offset
+// (between the two core matrices of a K step) 128, stride byte offset
+// `sbo` (between 8-row groups); descriptor version 1.
+__device__ __forceinline__ uint64_t op_desc(uint32_t addr, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) |
+         ((uint64_t)1 << 46);
+}
+
+// Instruction descriptor of kind::f16: f32 accumulator, bf16 A and B, both
+// K-major, N / 8 at bit 17, M / 16 at bit 24.
+__device__ __forceinline__ uint32_t instr_desc(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t dtmem, uint64_t a, uint64_t b, uint32_t idesc, bool acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(dtmem),
+      "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)acc));
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+// Bounded wait for the mbarrier's phase `parity`; true when it completed.
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done = 0;
+  for (int it = 0; it < kTcWaitLimit && !done; ++it)
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ void ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void st16(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
+      "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
+      "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15])));
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cp16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Shared-memory writes by threads, then work for the tensor cores (async proxy).
+__device__ __forceinline__ void publish_to_mma() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kTcThreads, 2) prefill_fwd_tc_kernel(DevState s, int n,
+                                                                      const uint16_t* __restrict__ q,
+                                                                      const uint16_t* __restrict__ k,
+                                                                      const uint16_t* __restrict__ v,
+                                                                      uint16_t* __restrict__ out,
+                                                                      float* __restrict__ stats, float qk_scale_log2) {
+  extern __shared__ __align__(1024) uint8_t tc_smem[];
+  uint8_t* sq = tc_smem + kOffQ;
+  uint8_t* sk = tc_smem + kOffK;
+  uint8_t* sv = tc_smem + kOffV;
+  uint8_t* svt = tc_smem + kOffVt;
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(tc_smem + kOffBar);
+  uint32_t* tbase = reinterpret_cast<uint32_t*>(tc_smem + kOffBar + 8);
+  const uint32_t bar = saddr(mbar);
+
+  // the longest (last) query tiles first
+  const int qt = gridDim.x - 1 - blockIdx.x, hqi = blockIdx.y, bl = blockIdx.z;
+  const int hkvi = hqi / s.group;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const size_t qrow0 = ((size_t)bl * s.hq + hqi) * n;
+  const uint16_t* kb = k + ((size_t)bl * s.hkv + hkvi) * n * kHeadDim;
+  const uint16_t* vb = v + ((size_t)bl * s.hkv + hkvi) * n * kHeadDim;
+  const int q0 = qt * kTcQ;
+  const int qi = q0 + tid;  // this thread's query row
+  const int n_kt = min((q0 + kTcQ - 1) / kTcKeys + 1, (n + kTcKeys - 1) / kTcKeys);
+
+  // Q tile into the operand layout (rows past n zero)
+  for (int i = tid; i < kTcQ * (kHeadDim / 8); i += kTcThreads) {
+    const int r = i >> 4, c = i & 15;
+    uint8_t* d = sq + core_off(r, c, kHeadDim / 8);
+    if (q0 + r < n)
+      cp16(saddr(d), q + (qrow0 + q0 + r) * kHeadDim + 8 * c);
+    else
+      *reinterpret_cast<uint4*>(d) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tbase)),
+                 "r"(kTcCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tbase;
+  const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's lanes
+
+  const uint32_t id_s = instr_desc(kTcQ, kTcKeys);
+  const uint32_t id_o = instr_desc(kTcQ, kHeadDim);
+  float m = kNegBig, l = 0.0f;
+  uint32_t phase = 0;
+  bool ok = true;
+
+  for (int j = 0; j < n_kt && ok; ++j) {
+    const int k0 = j * kTcKeys;
+    // K into the operand layout, V into the staging tile (rows past n zero)
+    for (int i = tid; i < kTcKeys * (kHeadDim / 8); i += kTcThreads) {
+      const int r = i >> 4, c = i & 15;
+      uint8_t* dk = sk + core_off(r, c, kHeadDim / 8);
+      uint8_t* dv = sv + (r * kTcVRow + 8 * c) * 2;
+      if (k0 + r < n) {
+        cp16(saddr(dk), kb + (size_t)(k0 + r) * kHeadDim + 8 * c);
+        cp16(saddr(dv), vb + (size_t)(k0 + r) * kHeadDim + 8 * c);
+      } else {
+        *reinterpret_cast<uint4*>(dk) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(dv) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+    // V^T (dims x keys) in the operand layout: the 8 x 8 block (key group
+    // kg, dim group dg) of V transposed is core matrix (dg, kg) of V^T
+#pragma unroll
+    for (int bi = 0; bi < 8; ++bi) {
+      const int blk = warp * 32 + bi * 4;  // 4 blocks per ldmatrix: dims 8 (dg .. dg + 3)
+      const int kg = blk >> 4, dg = blk & 15;
+      const int mi = lane >> 3, rr = lane & 7;
+      uint32_t t0, t1, t2, t3;
+      asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(t0), "=r"(t1), "=r"(t2), "=r"(t3)
+                   : "r"(saddr(sv + ((8 * kg + rr) * kTcVRow + 8 * (dg + mi)) * 2)));
+      const uint32_t tv[4] = {t0, t1, t2, t3};
+#pragma unroll
+      for (int mm = 0; mm < 4; ++mm)
+        *reinterpret_cast<uint32_t*>(svt + core_off(8 * (dg + mm) + (lane >> 2), kg, kTcKeys / 8) +
+                                     4 * (lane & 3)) = tv[mm];
+    }
+    publish_to_mma();
+    if (tid == 0) {
+#pragma unroll
+      for (int ks = 0; ks < kHeadDim / 16; ++ks)
+        mma_f16(tmem, op_desc(saddr(sq) + ks * 256, (kHeadDim / 8) * 128),
+                op_desc(saddr(sk) + ks * 256, (kHeadDim / 8) * 128), id_s, ks > 0);
+      mma_commit(bar);
+    }
+    ok = __syncthreads_and(bar_wait(bar, phase));
+    phase ^= 1u;
+    if (!ok) break;
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+
+    // this row's 64 logits, masked, in the log2 domain
+    float x[kTcKeys];
+#pragma unroll
+    for (int c0 = 0; c0 < kTcKeys; c0 += 16) {
+      float t[16];
+      ld16(trow + c0, t);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int ki = k0 + c0 + i;
+        x[c0 + i] = (ki <= qi && ki < n) ? t[i] * qk_scale_log2 : -INFINITY;
+      }
+    }
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kTcKeys; ++i) mx = fmaxf(mx, x[i]);
+    // the row maximum moved: rescale the sum and (after the first tile) O.
+    // TMEM loads and stores are warp-collective: the warp rescales when any
+    // of its rows must, the others by 1
+    const bool grow = mx > m + kTcLazy;
+    const float alpha = grow ? fast_exp2(m - mx) : 1.0f;
+    if (grow) {
+      l *= alpha;
+      m = mx;
+    }
+    if (j > 0 && __any_sync(0xffffffffu, grow)) {
+#pragma unroll 1
+      for (int c0 = 0; c0 < kHeadDim; c0 += 16) {
+        float t[16];
+        ld16(trow + kTcO + c0, t);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) t[i] *= alpha;
+        st16(trow + kTcO + c0, t);
+      }
+    }
+    // P = hi + lo into the operand layouts (P hi over K, P lo over staged V)
+#pragma unroll
+    for (int c = 0; c < kTcKeys / 8; ++c) {
+      uint32_t hw[4], lw[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float p0 = fast_exp2(x[8 * c + 2 * e] - m), p1 = fast_exp2(x[8 * c + 2 * e + 1] - m);
+        l += p0 + p1;
+        const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - __low2float(h), p1 - __high2float(h));
+        hw[e] = *reinterpret_cast<const uint32_t*>(&h);
+        lw[e] = *reinterpret_cast<const uint32_t*>(&lo);
+      }
+      const int off = core_off(tid, c, kTcKeys / 8);
+      *reinterpret_cast<uint4*>(sk + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4*>(sv + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+    publish_to_mma();
+    if (tid == 0) {
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        const uint32_t pa = saddr(part == 0 ? sk : sv);
+#pragma unroll
+        for (int ks = 0; ks < kTcKeys / 16; ++ks)
+          mma_f16(tmem + kTcO, op_desc(pa + ks * 256, (kTcKeys / 8) * 128),
+                  op_desc(saddr(svt) + ks * 256, (kTcKeys / 8) * 128), id_o, j > 0 || part > 0 || ks > 0);
+      }
+      mma_commit(bar);
+    }
+    ok = __syncthreads_and(bar_wait(bar, phase));
+    phase ^= 1u;
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  }
+
+  if (ok) {
+    // O / l to bf16, and the row's (max, sum); every lane reads (the TMEM
+    // load is warp-collective), rows past n store nothing
+    const bool row_ok = qi < n;
+    const float inv = row_ok ? 1.0f / l : 0.0f;
+    uint16_t* orow = out + (qrow0 + (row_ok ? qi : 0)) * kHeadDim;
+#pragma unroll 1
+    for (int c0 = 0; c0 < kHeadDim; c0 += 16) {
+      float t[16];
+      ld16(trow + kTcO + c0, t);
+      uint32_t w[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const __nv_bfloat162 pr = __floats2bfloat162_rn(t[2 * e] * inv, t[2 * e + 1] * inv);
+        w[e] = *reinterpret_cast<const uint32_t*>(&pr);
+      }
+      if (row_ok) {
+        *reinterpret_cast<uint4*>(orow + c0) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(orow + c0 + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+    }
+    if (row_ok) *reinterpret_cast<float2*>(stats + (qrow0 + qi) * 2) = make_float2(m, l);
+  } else {
+    if (tid == 0) atomicOr(&s.counters[kCtrStatus], kDevWaitTimeout);
+    // a last bounded wait for the MMAs whose completion did not come (the
+    // phase was flipped after the failed wait) before the columns go back
+    bar_wait(bar, phase ^ 1u);
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcCols));
+}
+
+}  // namespace
+
+int prefill_fwd_tc_smem_bytes() { return kTcSmem; }
+
+cudaError_t launch_prefill_fwd_tc(const DevState& s, int batch, int n, const uint16_t* q, const uint16_t* k,
+                                  const uint16_t* v, uint16_t* out, float* stats, float qk_scale_log2,
+                                  cudaStream_t st) {
+  static int done[64] = {0};
+  const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(prefill_fwd_tc_kernel), kTcSmem, done);
+  if (e != cudaSuccess) return e;
+  const int tiles = (n + kTcQ - 1) / kTcQ;
+  prefill_fwd_tc_kernel<<<dim3(tiles, s.hq, batch), kTcThreads, kTcSmem, st>>>(s, n, q, k, v, out, stats,
+                                                                               qk_scale_log2);
+  return cudaGetLastError();
+}
+
+}  // namespace kvc

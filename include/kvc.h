@@ -87,6 +87,9 @@ typedef enum {
                                         (state bytes restored without
                                         kvc_cache_sync_host): its selection and
                                         compaction were skipped                */
+#define KVC_DEV_WAIT_TIMEOUT    0x40 /* a tensor-core completion wait of the
+                                        prefill ran out (about a second); that
+                                        CTA's outputs are missing            */
 
 /* Geometry of one layer's cache. */
 typedef struct {
