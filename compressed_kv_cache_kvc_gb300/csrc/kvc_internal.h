@@ -65,6 +65,7 @@ constexpr int kDevTableOverflow = 0x8;
 constexpr int kDevStackOverflow = 0x10;
 constexpr int kDevStaleHost = 0x20;
 constexpr int kDevWaitTimeout = 0x40;
+constexpr int kDevPrefillRange = 0x80;
 
 // Scratch carved from the caller's workspace for one attention call.
 //

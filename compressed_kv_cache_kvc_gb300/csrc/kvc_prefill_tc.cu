@@ -1,27 +1,34 @@
 // Prefill forward on the fifth-generation tensor cores: the causal attention
 // of a fresh prompt over itself (Technical Report section 1.1), with S = Q K^T
-// and O = P V by tcgen05.mma (bf16 operands, fp32 accumulators in tensor
-// memory) instead of mma.sync.  Same inputs, outputs and row statistics as
-// the mma.sync forward it replaces; the H2O scores still come from
-// prefill_scores_kernel (kvc_prefill.cu), which uses these statistics.
+// and O = P V by tcgen05.mma (fp32 accumulators in tensor memory).  Outputs
+// and row statistics (m, l) as the decode kernels define them; the H2O
+// scores come from prefill_scores_kernel (kvc_prefill.cu), which uses these
+// statistics.
 //
 // One 128-thread CTA per (128-query tile, query head, sequence); thread t
 // owns query row t, which is TMEM lane t.  Per 64-key tile (up to the
 // diagonal):
 //   * K rows by cp.async into the operand layout (K-major, no swizzle:
-//     8-row x 16-byte core matrices), V rows into a padded staging tile,
-//     transposed by ldmatrix.trans into a dims x keys operand;
-//   * one thread issues S = Q K^T (M 128, N 64, 8 MMAs of K 16) into TMEM
-//     columns [0, 64), commits to an mbarrier;
+//     8-row x 16-byte core matrices), V rows into a staging tile (16-byte
+//     chunks XOR-swizzled by row), both double-buffered: tile j + 1's copies
+//     run while tile j is computed; V is transposed by ldmatrix.trans into a
+//     dims x keys operand and converted to fp16 on the way;
+//   * one thread issues S = Q K^T (M 128, N 64, 8 MMAs of K 16, bf16: exact
+//     products) into TMEM columns [0, 64);
 //   * each thread reads its row of S (tcgen05.ld), masks, and runs the
 //     online softmax in the log2 domain with a lazy maximum (O in TMEM is
 //     rescaled only when the row maximum grows by more than 8);
-//   * P = hi + lo (two bf16 parts, 16 significant bits) into shared memory;
-//     one thread issues O += P_hi V + P_lo V (M 128, N 128, K 64) into
-//     columns [128, 256).
+//   * P in fp16 (11 significant bits; p <= 2^8 by the lazy maximum) over the
+//     K buffer S has finished with, and one thread issues O += P V (M 128,
+//     N 128, K 64, fp16 operands) into columns [128, 256).  A bf16 P alone
+//     missed the output tolerance on rows that see few keys; P in two bf16
+//     parts (hi + lo) met it at two MMAs per tile, 12-15 % slower overall.
+//     V entries beyond fp16's range (|v| >= 65536, or not finite) saturate
+//     to +-65504 and set KVC_DEV_PREFILL_RANGE.
 // Every mbarrier wait is bounded; a wait that runs out sets
 // KVC_DEV_WAIT_TIMEOUT, and the CTA stops after freeing its tensor memory.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "kvc_device.h"
 #include "kvc_internal.h"
@@ -34,18 +41,22 @@ using namespace dev;
 constexpr int kTcThreads = 128;      // one thread per query row (TMEM lane)
 constexpr int kTcQ = 128;            // queries per CTA (the MMAs' M)
 constexpr int kTcKeys = 64;          // keys per tile
-constexpr int kTcVRow = kHeadDim + 8;  // staged V rows: 272 bytes (conflict-free ldmatrix)
 constexpr float kTcLazy = 8.0f;      // log2 units the running maximum may lag
 constexpr uint32_t kTcCols = 256;    // TMEM columns: S [0, 64), O [128, 256)
 constexpr uint32_t kTcO = 128;
 constexpr int kTcWaitLimit = 1 << 22;
 
+constexpr int kTileBytes = kTcKeys * kHeadDim * 2;          // 16 KB
 constexpr int kOffQ = 0;                                     // 32 KB: Q, operand layout
-constexpr int kOffK = kOffQ + kTcQ * kHeadDim * 2;           // 16 KB: K, then P hi
-constexpr int kOffV = kOffK + kTcKeys * kHeadDim * 2;        // 17 KB: staged V, then P lo
-constexpr int kOffVt = kOffV + kTcKeys * kTcVRow * 2;        // 16 KB: V^T, operand layout
-constexpr int kOffBar = kOffVt + kHeadDim * kTcKeys * 2;     // mbarrier, TMEM base
-constexpr int kTcSmem = kOffBar + 16;
+constexpr int kOffK = kOffQ + kTcQ * kHeadDim * 2;           // 2 x 16 KB: K, then P (operand layout)
+constexpr int kOffV = kOffK + 2 * kTileBytes;                // 2 x 16 KB: staged V
+constexpr int kOffVt = kOffV + 2 * kTileBytes;               // 16 KB: V^T in fp16, operand layout
+constexpr int kOffBar = kOffVt + kTileBytes;                 // mbarrier, TMEM base
+constexpr int kTcSmem = kOffBar + 16;                        // two CTAs per SM
+
+// Staged V: row r (a key) of 256 bytes, its 16-byte chunk c at c ^ (r % 8),
+// so the 8 rows an ldmatrix reads together lie on different banks.
+__device__ __forceinline__ int vstage_off(int r, int c) { return r * 256 + ((c ^ (r & 7)) << 4); }
 
 __device__ __forceinline__ uint32_t saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -62,10 +73,23 @@ __device__ __forceinline__ uint64_t op_desc(uint32_t addr, uint32_t sbo) {
          ((uint64_t)1 << 46);
 }
 
-// Instruction descriptor of kind::f16: f32 accumulator, bf16 A and B, both
-// K-major, N / 8 at bit 17, M / 16 at bit 24.
-__device__ __forceinline__ uint32_t instr_desc(int m, int n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+// fp16 bits of 65504, its largest finite value.  bf16 magnitudes from 65536
+// up saturate to it; 65280, the bf16 value below, converts exactly.
+constexpr uint32_t kF16Max = 0x7BFFu;
+
+// (lo, hi) to fp16x2, round to nearest, out-of-range values saturated to
+// +-65504 (NaN stays NaN).
+__device__ __forceinline__ uint32_t f16x2_sat(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Instruction descriptor of kind::f16: f32 accumulator, A and B both bf16
+// (`bf16`) or both fp16, both K-major, N / 8 at bit 17, M / 16 at bit 24.
+__device__ __forceinline__ uint32_t instr_desc(int m, int n, bool bf16) {
+  const uint32_t ab = bf16 ? ((1u << 7) | (1u << 10)) : 0u;
+  return (1u << 4) | ab | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_f16(uint32_t dtmem, uint64_t a, uint64_t b, uint32_t idesc, bool acc) {
@@ -136,8 +160,6 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_fwd_tc_kernel(DevState 
                                                                       float* __restrict__ stats, float qk_scale_log2) {
   extern __shared__ __align__(1024) uint8_t tc_smem[];
   uint8_t* sq = tc_smem + kOffQ;
-  uint8_t* sk = tc_smem + kOffK;
-  uint8_t* sv = tc_smem + kOffV;
   uint8_t* svt = tc_smem + kOffVt;
   uint64_t* mbar = reinterpret_cast<uint64_t*>(tc_smem + kOffBar);
   uint32_t* tbase = reinterpret_cast<uint32_t*>(tc_smem + kOffBar + 8);
@@ -178,19 +200,23 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_fwd_tc_kernel(DevState 
   const uint32_t tmem = *tbase;
   const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's lanes
 
-  const uint32_t id_s = instr_desc(kTcQ, kTcKeys);
-  const uint32_t id_o = instr_desc(kTcQ, kHeadDim);
+  const uint32_t id_s = instr_desc(kTcQ, kTcKeys, true);
+  const uint32_t id_o = instr_desc(kTcQ, kHeadDim, false);
   float m = kNegBig, l = 0.0f;
   uint32_t phase = 0;
   bool ok = true;
+  __half2 vmax = __floats2half2_rn(0.0f, 0.0f);  // largest |V| in fp16 (NaN kept)
 
-  for (int j = 0; j < n_kt && ok; ++j) {
-    const int k0 = j * kTcKeys;
-    // K into the operand layout, V into the staging tile (rows past n zero)
+  // copies of key tile jt into buffers jt % 2 (rows past n zero): K in the
+  // operand layout, V in the staging layout
+  auto load_kv = [&](int jt) {
+    const int k0 = jt * kTcKeys;
+    uint8_t* dkb = tc_smem + kOffK + (jt & 1) * kTileBytes;
+    uint8_t* dvb = tc_smem + kOffV + (jt & 1) * kTileBytes;
     for (int i = tid; i < kTcKeys * (kHeadDim / 8); i += kTcThreads) {
       const int r = i >> 4, c = i & 15;
-      uint8_t* dk = sk + core_off(r, c, kHeadDim / 8);
-      uint8_t* dv = sv + (r * kTcVRow + 8 * c) * 2;
+      uint8_t* dk = dkb + core_off(r, c, kHeadDim / 8);
+      uint8_t* dv = dvb + vstage_off(r, c);
       if (k0 + r < n) {
         cp16(saddr(dk), kb + (size_t)(k0 + r) * kHeadDim + 8 * c);
         cp16(saddr(dv), vb + (size_t)(k0 + r) * kHeadDim + 8 * c);
@@ -199,10 +225,21 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_fwd_tc_kernel(DevState 
         *reinterpret_cast<uint4*>(dv) = make_uint4(0u, 0u, 0u, 0u);
       }
     }
-    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+  };
+  load_kv(0);  // one copy group with Q
+  asm volatile("cp.async.commit_group;" ::: "memory");
+
+  for (int j = 0; j < n_kt && ok; ++j) {
+    const int k0 = j * kTcKeys;
+    uint8_t* sk = tc_smem + kOffK + (j & 1) * kTileBytes;
+    uint8_t* sv = tc_smem + kOffV + (j & 1) * kTileBytes;
+    // the next tile's copies into the other buffers (free: the previous
+    // tile's MMAs, which read them as P, completed), then this tile's wait
+    if (j + 1 < n_kt) load_kv(j + 1);
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 1;" ::: "memory");
     __syncthreads();
-    // V^T (dims x keys) in the operand layout: the 8 x 8 block (key group
-    // kg, dim group dg) of V transposed is core matrix (dg, kg) of V^T
+    // V^T (dims x keys) in fp16 in the operand layout: the 8 x 8 block (key
+    // group kg, dim group dg) of V transposed is core matrix (dg, kg) of V^T
 #pragma unroll
     for (int bi = 0; bi < 8; ++bi) {
       const int blk = warp * 32 + bi * 4;  // 4 blocks per ldmatrix: dims 8 (dg .. dg + 3)
@@ -211,12 +248,15 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_fwd_tc_kernel(DevState 
       uint32_t t0, t1, t2, t3;
       asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                    : "=r"(t0), "=r"(t1), "=r"(t2), "=r"(t3)
-                   : "r"(saddr(sv + ((8 * kg + rr) * kTcVRow + 8 * (dg + mi)) * 2)));
+                   : "r"(saddr(sv + vstage_off(8 * kg + rr, dg + mi))));
       const uint32_t tv[4] = {t0, t1, t2, t3};
 #pragma unroll
-      for (int mm = 0; mm < 4; ++mm)
+      for (int mm = 0; mm < 4; ++mm) {
+        const uint32_t hv = f16x2_sat(bf16f(tv[mm] & 0xFFFFu), bf16f(tv[mm] >> 16));
+        vmax = __hmax2_nan(vmax, __habs2(*reinterpret_cast<const __half2*>(&hv)));
         *reinterpret_cast<uint32_t*>(svt + core_off(8 * (dg + mm) + (lane >> 2), kg, kTcKeys / 8) +
-                                     4 * (lane & 3)) = tv[mm];
+                                     4 * (lane & 3)) = hv;
+      }
     }
     publish_to_mma();
     if (tid == 0) {
@@ -265,33 +305,26 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_fwd_tc_kernel(DevState 
         st16(trow + kTcO + c0, t);
       }
     }
-    // P = hi + lo into the operand layouts (P hi over K, P lo over staged V)
+    // P in fp16 over K of this tile (the sum adds the unrounded p, as the
+    // decode kernels do)
 #pragma unroll
     for (int c = 0; c < kTcKeys / 8; ++c) {
-      uint32_t hw[4], lw[4];
+      uint32_t hw[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float p0 = fast_exp2(x[8 * c + 2 * e] - m), p1 = fast_exp2(x[8 * c + 2 * e + 1] - m);
         l += p0 + p1;
-        const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-        const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - __low2float(h), p1 - __high2float(h));
+        const __half2 h = __floats2half2_rn(p0, p1);
         hw[e] = *reinterpret_cast<const uint32_t*>(&h);
-        lw[e] = *reinterpret_cast<const uint32_t*>(&lo);
       }
-      const int off = core_off(tid, c, kTcKeys / 8);
-      *reinterpret_cast<uint4*>(sk + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-      *reinterpret_cast<uint4*>(sv + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      *reinterpret_cast<uint4*>(sk + core_off(tid, c, kTcKeys / 8)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
     }
     publish_to_mma();
     if (tid == 0) {
 #pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        const uint32_t pa = saddr(part == 0 ? sk : sv);
-#pragma unroll
-        for (int ks = 0; ks < kTcKeys / 16; ++ks)
-          mma_f16(tmem + kTcO, op_desc(pa + ks * 256, (kTcKeys / 8) * 128),
-                  op_desc(saddr(svt) + ks * 256, (kTcKeys / 8) * 128), id_o, j > 0 || part > 0 || ks > 0);
-      }
+      for (int ks = 0; ks < kTcKeys / 16; ++ks)
+        mma_f16(tmem + kTcO, op_desc(saddr(sk) + ks * 256, (kTcKeys / 8) * 128),
+                op_desc(saddr(svt) + ks * 256, (kTcKeys / 8) * 128), id_o, j > 0 || ks > 0);
       mma_commit(bar);
     }
     ok = __syncthreads_and(bar_wait(bar, phase));
@@ -327,6 +360,11 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_fwd_tc_kernel(DevState 
     // phase was flipped after the failed wait) before the columns go back
     bar_wait(bar, phase ^ 1u);
   }
+  // a saturated V entry reads 65504 in fp16, which no bf16 value converts to
+  const uint32_t vmb = *reinterpret_cast<const uint32_t*>(&vmax);
+  if ((vmb & 0x7FFFu) >= kF16Max || ((vmb >> 16) & 0x7FFFu) >= kF16Max)
+    atomicOr(&s.counters[kCtrStatus], kDevPrefillRange);
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcCols));

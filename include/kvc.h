@@ -90,6 +90,11 @@ typedef enum {
 #define KVC_DEV_WAIT_TIMEOUT    0x40 /* a tensor-core completion wait of the
                                         prefill ran out (about a second); that
                                         CTA's outputs are missing            */
+#define KVC_DEV_PREFILL_RANGE   0x80 /* a prompt value (V) entry of magnitude
+                                        65536 or more, or not finite: the
+                                        prefill's P.V product takes V in fp16,
+                                        saturated to +-65504, so that head's
+                                        prompt outputs are inexact           */
 
 /* Geometry of one layer's cache. */
 typedef struct {

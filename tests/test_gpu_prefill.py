@@ -118,3 +118,41 @@ def test_prefill_errors():
     cache.prefill(q, k, k, seq_begin=1, accumulate_h2o=False)
     assert cache.last_launch_count() == 2
     assert cache.read_status() == 0
+
+
+PREFILL_RANGE = 0x80
+
+
+def test_prefill_value_range():
+    """The prompt's P.V product takes V in fp16.  V up to 65280 in magnitude
+    (the largest bf16 below fp16's overflow) converts without saturation: no
+    status bit, and the error stays within fp16 rounding of P and V (2^-11
+    each) on the sum of p |v|, plus the bf16 output's own rounding.  One
+    entry of 70000 saturates to 65504: the prompt's status bit is set and
+    every output stays finite."""
+    from compressed_kv_cache_kvc_gb300.cache import KVCache
+    from compressed_kv_cache_kvc_gb300.workloads import bf16_bits
+    rng = np.random.default_rng(62)
+    hq, hkv, n = 8, 2, 200
+    f = O.bf16_bits_to_f32
+    q = _bits(rng, (1, hq, n, 128))
+    k = _bits(rng, (1, hkv, n, 128))
+    vf = rng.standard_normal((1, hkv, n, 128)).astype(np.float32) * 1000.0
+    vf[0, 0, rng.integers(0, n, 40), rng.integers(0, 128, 40)] = 65280.0
+    vf[0, 1, rng.integers(0, n, 40), rng.integers(0, 128, 40)] = -65280.0
+    v = bf16_bits(vf)
+    assert np.abs(f(v)).max() == 65280.0
+    cache = KVCache(hq, hkv, 8, 2 * 15, 2, 15)
+    out = T.bf16_tensor_to_f32(cache.prefill(T.to_dev_bf16(q), T.to_dev_bf16(k), T.to_dev_bf16(v)))
+    assert cache.read_status() == 0
+    ref, _ = O.prefill_attention(f(q[0]), f(k[0]), f(v[0]), T.sm_scale())
+    mag, _ = O.prefill_attention(f(q[0]), f(k[0]), np.abs(f(v[0])), T.sm_scale())
+    err = np.abs(out[0].astype(np.float64) - ref)
+    bound = 2e-3 + 2.0 ** -8 * np.abs(ref) + 2.0 * 2.0 ** -11 * mag
+    assert (err <= bound).all(), float((err / bound).max())
+
+    vf[0, 1, 7, 3] = 70000.0
+    v2 = bf16_bits(vf)
+    out2 = T.bf16_tensor_to_f32(cache.prefill(T.to_dev_bf16(q), T.to_dev_bf16(k), T.to_dev_bf16(v2), seq_begin=1))
+    assert cache.read_status() & PREFILL_RANGE
+    assert np.isfinite(out2).all()
