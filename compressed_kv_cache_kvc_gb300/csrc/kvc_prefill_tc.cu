@@ -5,9 +5,10 @@
 // scores come from prefill_scores_kernel (kvc_prefill.cu), which uses these
 // statistics.
 //
-// One 128-thread CTA per (128-query tile, query head, sequence); thread t
-// owns query row t, which is TMEM lane t.  Per 64-key tile (up to the
-// diagonal):
+// One 256-thread CTA per (128-query tile, query head, sequence); threads t
+// and t + 128 own query row t (TMEM lane t), the first S columns [0, 32) and
+// O columns [0, 64), the second the other halves; they agree on the row
+// maximum through shared memory.  Per 64-key tile (up to the diagonal):
 //   * K rows by cp.async into the operand layout (K-major, no swizzle:
 //     8-row x 16-byte core matrices), V rows into a staging tile (16-byte
 //     chunks XOR-swizzled by row), both double-buffered: tile j + 1's copies
@@ -15,7 +16,8 @@
 //     dims x keys operand and converted to fp16 on the way;
 //   * one thread issues S = Q K^T (M 128, N 64, 8 MMAs of K 16, bf16: exact
 //     products) into TMEM columns [0, 64);
-//   * each thread reads its row of S (tcgen05.ld), masks, and runs the
+//   * each thread reads its half row of S (tcgen05.ld), masks (only tiles
+//     that cross the diagonal or the end of the prompt), and runs the
 //     online softmax in the log2 domain with a lazy maximum (O in TMEM is
 //     rescaled only when the row maximum grows by more than 8);
 //   * P in fp16 (11 significant bits; p <= 2^8 by the lazy maximum) over the
@@ -38,7 +40,7 @@ namespace {
 
 using namespace dev;
 
-constexpr int kTcThreads = 128;      // one thread per query row (TMEM lane)
+constexpr int kTcThreads = 256;      // two threads per query row (TMEM lane)
 constexpr int kTcQ = 128;            // queries per CTA (the MMAs' M)
 constexpr int kTcKeys = 64;          // keys per tile
 constexpr float kTcLazy = 8.0f;      // log2 units the running maximum may lag
@@ -169,19 +171,23 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_fwd_tc_kernel(DevState 
   const int qt = gridDim.x - 1 - blockIdx.x, hqi = blockIdx.y, bl = blockIdx.z;
   const int hkvi = hqi / s.group;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // thread (half h, row r): query row r, S columns [32 h, 32 h + 32), O
+  // columns [64 h, 64 h + 64); warps w and w + 4 share TMEM lanes 32 (w % 4) ..
+  const int half = tid >> 7, r = tid & (kTcQ - 1);
   const size_t qrow0 = ((size_t)bl * s.hq + hqi) * n;
   const uint16_t* kb = k + ((size_t)bl * s.hkv + hkvi) * n * kHeadDim;
   const uint16_t* vb = v + ((size_t)bl * s.hkv + hkvi) * n * kHeadDim;
   const int q0 = qt * kTcQ;
-  const int qi = q0 + tid;  // this thread's query row
+  const int qi = q0 + r;  // this thread's query row
   const int n_kt = min((q0 + kTcQ - 1) / kTcKeys + 1, (n + kTcKeys - 1) / kTcKeys);
 
-  // Q tile into the operand layout (rows past n zero)
+  // Q tile into the operand layout (rows past n zero); 8 consecutive threads
+  // fill one core matrix (8 rows of one 16-byte chunk: 128 contiguous bytes)
   for (int i = tid; i < kTcQ * (kHeadDim / 8); i += kTcThreads) {
-    const int r = i >> 4, c = i & 15;
-    uint8_t* d = sq + core_off(r, c, kHeadDim / 8);
-    if (q0 + r < n)
-      cp16(saddr(d), q + (qrow0 + q0 + r) * kHeadDim + 8 * c);
+    const int rr = (i & 7) | ((i >> 7) << 3), c = (i >> 3) & 15;
+    uint8_t* d = sq + core_off(rr, c, kHeadDim / 8);
+    if (q0 + rr < n)
+      cp16(saddr(d), q + (qrow0 + q0 + rr) * kHeadDim + 8 * c);
     else
       *reinterpret_cast<uint4*>(d) = make_uint4(0u, 0u, 0u, 0u);
   }
@@ -198,32 +204,37 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_fwd_tc_kernel(DevState 
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tbase;
-  const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's lanes
+  const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // this warp's lanes
 
   const uint32_t id_s = instr_desc(kTcQ, kTcKeys, true);
   const uint32_t id_o = instr_desc(kTcQ, kHeadDim, false);
-  float m = kNegBig, l = 0.0f;
+  float m = kNegBig, l = 0.0f;  // l: the sum over this thread's columns
   uint32_t phase = 0;
   bool ok = true;
   __half2 vmax = __floats2half2_rn(0.0f, 0.0f);  // largest |V| in fp16 (NaN kept)
 
   // copies of key tile jt into buffers jt % 2 (rows past n zero): K in the
-  // operand layout, V in the staging layout
+  // operand layout (8 consecutive threads per core matrix), V in the staging
+  // layout (16 consecutive threads per row)
   auto load_kv = [&](int jt) {
     const int k0 = jt * kTcKeys;
     uint8_t* dkb = tc_smem + kOffK + (jt & 1) * kTileBytes;
     uint8_t* dvb = tc_smem + kOffV + (jt & 1) * kTileBytes;
-    for (int i = tid; i < kTcKeys * (kHeadDim / 8); i += kTcThreads) {
-      const int r = i >> 4, c = i & 15;
-      uint8_t* dk = dkb + core_off(r, c, kHeadDim / 8);
-      uint8_t* dv = dvb + vstage_off(r, c);
-      if (k0 + r < n) {
-        cp16(saddr(dk), kb + (size_t)(k0 + r) * kHeadDim + 8 * c);
-        cp16(saddr(dv), vb + (size_t)(k0 + r) * kHeadDim + 8 * c);
-      } else {
+#pragma unroll
+    for (int it = 0; it < kTcKeys * (kHeadDim / 8) / kTcThreads; ++it) {
+      const int i = tid + it * kTcThreads;
+      const int rk = (i & 7) | ((i >> 7) << 3), ck = (i >> 3) & 15;
+      const int rv = i >> 4, cv = i & 15;
+      uint8_t* dk = dkb + core_off(rk, ck, kHeadDim / 8);
+      uint8_t* dv = dvb + vstage_off(rv, cv);
+      if (k0 + rk < n)
+        cp16(saddr(dk), kb + (size_t)(k0 + rk) * kHeadDim + 8 * ck);
+      else
         *reinterpret_cast<uint4*>(dk) = make_uint4(0u, 0u, 0u, 0u);
+      if (k0 + rv < n)
+        cp16(saddr(dv), vb + (size_t)(k0 + rv) * kHeadDim + 8 * cv);
+      else
         *reinterpret_cast<uint4*>(dv) = make_uint4(0u, 0u, 0u, 0u);
-      }
     }
   };
   load_kv(0);  // one copy group with Q
@@ -239,11 +250,11 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_fwd_tc_kernel(DevState 
     asm volatile("cp.async.commit_group;\ncp.async.wait_group 1;" ::: "memory");
     __syncthreads();
     // V^T (dims x keys) in fp16 in the operand layout: the 8 x 8 block (key
-    // group kg, dim group dg) of V transposed is core matrix (dg, kg) of V^T
+    // group kg, dim group dg) of V transposed is core matrix (dg, kg) of V^T;
+    // warp w transposes key group w
 #pragma unroll
-    for (int bi = 0; bi < 8; ++bi) {
-      const int blk = warp * 32 + bi * 4;  // 4 blocks per ldmatrix: dims 8 (dg .. dg + 3)
-      const int kg = blk >> 4, dg = blk & 15;
+    for (int bi = 0; bi < 4; ++bi) {
+      const int kg = warp, dg = 4 * bi;  // 4 blocks per ldmatrix: dims 8 (dg .. dg + 3)
       const int mi = lane >> 3, rr = lane & 7;
       uint32_t t0, t1, t2, t3;
       asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -271,24 +282,31 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_fwd_tc_kernel(DevState 
     if (!ok) break;
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 
-    // this row's 64 logits, masked, in the log2 domain
-    float x[kTcKeys];
+    // this thread's 32 raw logits; only tiles that cross the diagonal or
+    // the end of the prompt are masked (the test is the same for the CTA)
+    float x[kTcKeys / 2];
+    ld16(trow + 32 * half, *reinterpret_cast<float(*)[16]>(&x[0]));
+    ld16(trow + 32 * half + 16, *reinterpret_cast<float(*)[16]>(&x[16]));
+    if (k0 + kTcKeys - 1 > q0 || k0 + kTcKeys > n) {
 #pragma unroll
-    for (int c0 = 0; c0 < kTcKeys; c0 += 16) {
-      float t[16];
-      ld16(trow + c0, t);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int ki = k0 + c0 + i;
-        x[c0 + i] = (ki <= qi && ki < n) ? t[i] * qk_scale_log2 : -INFINITY;
+      for (int i = 0; i < kTcKeys / 2; ++i) {
+        const int ki = k0 + 32 * half + i;
+        if (!(ki <= qi && ki < n)) x[i] = -INFINITY;
       }
     }
     float mx = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < kTcKeys; ++i) mx = fmaxf(mx, x[i]);
+    for (int i = 0; i < kTcKeys / 2; ++i) mx = fmaxf(mx, x[i]);
+    // the row maximum from the two halves, through this tile's V staging
+    // (transposed already; the next copies into it start after two more
+    // barriers)
+    float* red = reinterpret_cast<float*>(sv);
+    red[half * kTcQ + r] = mx;
+    __syncthreads();
+    mx = fmaxf(mx, red[(half ^ 1) * kTcQ + r]) * qk_scale_log2;  // scale > 0: the max commutes
     // the row maximum moved: rescale the sum and (after the first tile) O.
     // TMEM loads and stores are warp-collective: the warp rescales when any
-    // of its rows must, the others by 1
+    // of its rows must, the others by 1; both halves decide alike
     const bool grow = mx > m + kTcLazy;
     const float alpha = grow ? fast_exp2(m - mx) : 1.0f;
     if (grow) {
@@ -297,27 +315,29 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_fwd_tc_kernel(DevState 
     }
     if (j > 0 && __any_sync(0xffffffffu, grow)) {
 #pragma unroll 1
-      for (int c0 = 0; c0 < kHeadDim; c0 += 16) {
+      for (int c0 = 0; c0 < kHeadDim / 2; c0 += 16) {
         float t[16];
-        ld16(trow + kTcO + c0, t);
+        ld16(trow + kTcO + 64 * half + c0, t);
 #pragma unroll
         for (int i = 0; i < 16; ++i) t[i] *= alpha;
-        st16(trow + kTcO + c0, t);
+        st16(trow + kTcO + 64 * half + c0, t);
       }
     }
     // P in fp16 over K of this tile (the sum adds the unrounded p, as the
     // decode kernels do)
+    const float nm = -m;
 #pragma unroll
-    for (int c = 0; c < kTcKeys / 8; ++c) {
+    for (int c = 0; c < kTcKeys / 16; ++c) {
       uint32_t hw[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float p0 = fast_exp2(x[8 * c + 2 * e] - m), p1 = fast_exp2(x[8 * c + 2 * e + 1] - m);
+        const float p0 = fast_exp2(fmaf(x[8 * c + 2 * e], qk_scale_log2, nm));
+        const float p1 = fast_exp2(fmaf(x[8 * c + 2 * e + 1], qk_scale_log2, nm));
         l += p0 + p1;
         const __half2 h = __floats2half2_rn(p0, p1);
         hw[e] = *reinterpret_cast<const uint32_t*>(&h);
       }
-      *reinterpret_cast<uint4*>(sk + core_off(tid, c, kTcKeys / 8)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4*>(sk + core_off(r, 4 * half + c, kTcKeys / 8)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
     }
     publish_to_mma();
     if (tid == 0) {
@@ -333,15 +353,20 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_fwd_tc_kernel(DevState 
   }
 
   if (ok) {
+    // the row's sum from the two halves (V^T is free: the MMAs completed)
+    float* red = reinterpret_cast<float*>(svt);
+    red[half * kTcQ + r] = l;
+    __syncthreads();
+    l += red[(half ^ 1) * kTcQ + r];
     // O / l to bf16, and the row's (max, sum); every lane reads (the TMEM
     // load is warp-collective), rows past n store nothing
     const bool row_ok = qi < n;
     const float inv = row_ok ? 1.0f / l : 0.0f;
-    uint16_t* orow = out + (qrow0 + (row_ok ? qi : 0)) * kHeadDim;
+    uint16_t* orow = out + (qrow0 + (row_ok ? qi : 0)) * kHeadDim + 64 * half;
 #pragma unroll 1
-    for (int c0 = 0; c0 < kHeadDim; c0 += 16) {
+    for (int c0 = 0; c0 < kHeadDim / 2; c0 += 16) {
       float t[16];
-      ld16(trow + kTcO + c0, t);
+      ld16(trow + kTcO + 64 * half + c0, t);
       uint32_t w[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
@@ -353,7 +378,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_fwd_tc_kernel(DevState 
         *reinterpret_cast<uint4*>(orow + c0 + 8) = make_uint4(w[4], w[5], w[6], w[7]);
       }
     }
-    if (row_ok) *reinterpret_cast<float2*>(stats + (qrow0 + qi) * 2) = make_float2(m, l);
+    if (row_ok && half == 0) *reinterpret_cast<float2*>(stats + (qrow0 + qi) * 2) = make_float2(m, l);
   } else {
     if (tid == 0) atomicOr(&s.counters[kCtrStatus], kDevWaitTimeout);
     // a last bounded wait for the MMAs whose completion did not come (the
