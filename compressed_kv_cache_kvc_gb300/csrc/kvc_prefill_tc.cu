@@ -5,30 +5,38 @@
 // scores come from prefill_scores_kernel (kvc_prefill.cu), which uses these
 // statistics.
 //
-// One 256-thread CTA per (128-query tile, query head, sequence); threads t
-// and t + 128 own query row t (TMEM lane t), the first S columns [0, 32) and
-// O columns [0, 64), the second the other halves; they agree on the row
-// maximum through shared memory.  Per 64-key tile (up to the diagonal):
-//   * K rows by cp.async into the operand layout (K-major, no swizzle:
-//     8-row x 16-byte core matrices), V rows into a staging tile (16-byte
-//     chunks XOR-swizzled by row), both double-buffered: tile j + 1's copies
-//     run while tile j is computed; V is transposed by ldmatrix.trans into a
-//     dims x keys operand and converted to fp16 on the way;
-//   * one thread issues S = Q K^T (M 128, N 64, 8 MMAs of K 16, bf16: exact
-//     products) into TMEM columns [0, 64);
-//   * each thread reads its half row of S (tcgen05.ld), masks (only tiles
-//     that cross the diagonal or the end of the prompt), and runs the
-//     online softmax in the log2 domain with a lazy maximum (O in TMEM is
-//     rescaled only when the row maximum grows by more than 8);
-//   * P in fp16 (11 significant bits; p <= 2^8 by the lazy maximum) over the
-//     K buffer S has finished with, and one thread issues O += P V (M 128,
-//     N 128, K 64, fp16 operands) into columns [128, 256).  A bf16 P alone
-//     missed the output tolerance on rows that see few keys; P in two bf16
-//     parts (hi + lo) met it at two MMAs per tile, 12-15 % slower overall.
-//     V entries beyond fp16's range (|v| >= 65536, or not finite) saturate
-//     to +-65504 and set KVC_DEV_PREFILL_RANGE.
-// Every mbarrier wait is bounded; a wait that runs out sets
-// KVC_DEV_WAIT_TIMEOUT, and the CTA stops after freeing its tensor memory.
+// One 384-thread CTA per (256-query block, query head, sequence), longest
+// blocks first, three warpgroups with fixed roles:
+//   * warpgroups 0 and 1 ("A" and "B") each own one 128-query tile; thread t
+//     of a warpgroup owns query row t of its tile, TMEM lane t.  TMEM columns:
+//     S_A [0, 64), S_B [64, 128), O_A [128, 256), O_B [256, 384);
+//   * warpgroup 2 (the producer) copies 64-key tiles into a ring of three
+//     slots by cp.async: K into the operand layout (K-major, no swizzle,
+//     8-row x 16-byte core matrices), V into a staging tile (16-byte chunks
+//     XOR-swizzled by row) that it transposes by ldmatrix.trans into a
+//     dims x keys operand in fp16.  A slot is refilled once both query tiles'
+//     P V products have read it.
+// Per key tile j a query warpgroup: waits for S(j) (its issuing thread put it
+// on the tensor cores one tile ahead), reads its S row (tcgen05.ld), lets
+// the issuing thread start S(j + 1) = Q K(j + 1)^T (M 128, N 64, bf16: exact
+// products), masks (only tiles that cross the diagonal or the end of the
+// prompt), runs the online softmax in the log2 domain with a lazy maximum (O
+// is rescaled in TMEM only when the row maximum grows by more than 8), waits
+// for P V(j - 1), writes P in fp16 (11 significant bits; p <= 2^8 by the lazy
+// maximum) and issues O += P V(j) (M 128, N 128, K 64, fp16 operands).  The
+// two query warpgroups run out of step, so one's softmax overlaps the other's
+// products and the producer's copies overlap both.  A bf16 P alone missed
+// the output tolerance on rows that see few keys.  V entries beyond fp16's
+// range (|v| >= 65536, or not finite) saturate to +-65504 and set
+// KVC_DEV_PREFILL_RANGE.
+//
+// Synchronisation: mbarriers (the producer's "slot full", the query
+// warpgroups' "slot empty", the tensor cores' completions through
+// tcgen05.commit) and named barriers inside a warpgroup.  Every mbarrier wait
+// is bounded and also ends when another thread has given up; a wait that
+// runs out sets KVC_DEV_WAIT_TIMEOUT, every warpgroup leaves its loop at its
+// next barrier, the issuing threads wait (bounded) for their products in
+// flight, and the CTA frees its tensor memory.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -40,21 +48,32 @@ namespace {
 
 using namespace dev;
 
-constexpr int kTcThreads = 256;      // two threads per query row (TMEM lane)
-constexpr int kTcQ = 128;            // queries per CTA (the MMAs' M)
-constexpr int kTcKeys = 64;          // keys per tile
-constexpr float kTcLazy = 8.0f;      // log2 units the running maximum may lag
-constexpr uint32_t kTcCols = 256;    // TMEM columns: S [0, 64), O [128, 256)
-constexpr uint32_t kTcO = 128;
+constexpr int kWg = 128;                  // threads per warpgroup
+constexpr int kTcThreads = 3 * kWg;       // query tiles A and B, producer
+constexpr int kTcQ = 128;                 // queries per tile (the MMAs' M)
+constexpr int kTcBlock = 2 * kTcQ;        // queries per CTA
+constexpr int kTcKeys = 64;               // keys per tile
+constexpr int kSlots = 3;                 // K / V^T ring
+constexpr float kTcLazy = 8.0f;           // log2 units the running maximum may lag
+constexpr uint32_t kTcCols = 512;         // TMEM columns allocated
+constexpr uint32_t kColS = 0;             // S of query tile x at kColS + 64 x
+constexpr uint32_t kColO = 128;           // O of query tile x at kColO + 128 x
 constexpr int kTcWaitLimit = 1 << 22;
 
-constexpr int kTileBytes = kTcKeys * kHeadDim * 2;          // 16 KB
-constexpr int kOffQ = 0;                                     // 32 KB: Q, operand layout
-constexpr int kOffK = kOffQ + kTcQ * kHeadDim * 2;           // 2 x 16 KB: K, then P (operand layout)
-constexpr int kOffV = kOffK + 2 * kTileBytes;                // 2 x 16 KB: staged V
-constexpr int kOffVt = kOffV + 2 * kTileBytes;               // 16 KB: V^T in fp16, operand layout
-constexpr int kOffBar = kOffVt + kTileBytes;                 // mbarrier, TMEM base
-constexpr int kTcSmem = kOffBar + 16;                        // two CTAs per SM
+constexpr int kTileBytes = kTcKeys * kHeadDim * 2;           // 16 KB
+constexpr int kOffQ = 0;                                      // 2 x 32 KB: Q_A, Q_B (operand layout)
+constexpr int kOffK = kOffQ + 2 * kTcQ * kHeadDim * 2;        // 3 x 16 KB: K ring (operand layout)
+constexpr int kOffVt = kOffK + kSlots * kTileBytes;           // 3 x 16 KB: V^T ring, fp16 (operand layout)
+constexpr int kOffVs = kOffVt + kSlots * kTileBytes;          // 2 x 16 KB: V staging (producer)
+constexpr int kOffP = kOffVs + 2 * kTileBytes;                // 2 x 16 KB: P_A, P_B (operand layout)
+constexpr int kOffBar = kOffP + 2 * kTileBytes;               // mbarriers, TMEM base, abort flag
+constexpr int kBarFull = 0, kBarEmptyA = kSlots, kBarEmptyB = 2 * kSlots, kBarS = 3 * kSlots,
+              kBarO = 3 * kSlots + 2, kNumBars = 3 * kSlots + 4;
+constexpr int kTcSmem = kOffBar + 8 * kNumBars + 16;
+
+// named barriers (0 is __syncthreads)
+constexpr int kNbQuery = 1;  // + query tile: 1, 2
+constexpr int kNbProducer = 3;
 
 // Staged V: row r (a key) of 256 bytes, its 16-byte chunk c at c ^ (r % 8),
 // so the 8 rows an ldmatrix reads together lie on different banks.
@@ -106,16 +125,43 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                : "memory");
 }
 
+__device__ __forceinline__ void bar_arrive(uint32_t bar) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}\n" ::"r"(bar) : "memory");
+}
+
 // Bounded wait for the mbarrier's phase `parity`; true when it completed.
-__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
+// With `abort` it also gives up once another thread has set that flag.
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, const volatile int* abort) {
   uint32_t done = 0;
-  for (int it = 0; it < kTcWaitLimit && !done; ++it)
+  for (int it = 0; it < kTcWaitLimit && !done; ++it) {
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(done)
         : "r"(bar), "r"(parity)
         : "memory");
+    if (!done && abort != nullptr && (it & 63) == 63 && *abort) break;
+  }
   return done != 0;
+}
+
+// A failed wait: flag it for the host and tell the other warpgroups.
+__device__ __forceinline__ void give_up(const DevState& s, volatile int* abort) {
+  if (!*abort) {
+    *abort = 1;
+    atomicOr(&s.counters[kCtrStatus], kDevWaitTimeout);
+  }
+}
+
+// Barrier over one warpgroup (named barrier `id`, 128 threads) that ANDs `v`
+// across it.
+__device__ __forceinline__ bool wg_and(int id, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, 128, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id)
+      : "memory");
+  return r != 0;
 }
 
 __device__ __forceinline__ void ld16(uint32_t taddr, float (&v)[16]) {
@@ -146,250 +192,318 @@ __device__ __forceinline__ void cp16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
-// Shared-memory writes by threads, then work for the tensor cores (async proxy).
-__device__ __forceinline__ void publish_to_mma() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-  __syncthreads();
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+// Rows [row0, row0 + rows) of a [n][128] bf16 matrix at `src` into the
+// operand layout at `dst` (rows past n zero) by `nthr` threads; 8
+// consecutive threads fill one core matrix (8 rows of one 16-byte chunk: 128
+// contiguous bytes).
+__device__ __forceinline__ void copy_operand(uint8_t* dst, const uint16_t* src, int row0, int rows, int n, int t,
+                                             int nthr) {
+  for (int i = t; i < rows * (kHeadDim / 8); i += nthr) {
+    const int rr = (i & 7) | ((i >> 7) << 3), c = (i >> 3) & 15;
+    uint8_t* d = dst + core_off(rr, c, kHeadDim / 8);
+    if (row0 + rr < n)
+      cp16(saddr(d), src + (size_t)(row0 + rr) * kHeadDim + 8 * c);
+    else
+      *reinterpret_cast<uint4*>(d) = make_uint4(0u, 0u, 0u, 0u);
+  }
 }
 
-__global__ void __launch_bounds__(kTcThreads, 2) prefill_fwd_tc_kernel(DevState s, int n,
+// Key tiles a 128-query tile starting at q0 attends to.
+__device__ __forceinline__ int key_tiles(int q0, int n) {
+  return min((q0 + kTcQ - 1) / kTcKeys + 1, (n + kTcKeys - 1) / kTcKeys);
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) prefill_fwd_tc_kernel(DevState s, int n,
                                                                       const uint16_t* __restrict__ q,
                                                                       const uint16_t* __restrict__ k,
                                                                       const uint16_t* __restrict__ v,
                                                                       uint16_t* __restrict__ out,
                                                                       float* __restrict__ stats, float qk_scale_log2) {
   extern __shared__ __align__(1024) uint8_t tc_smem[];
-  uint8_t* sq = tc_smem + kOffQ;
-  uint8_t* svt = tc_smem + kOffVt;
-  uint64_t* mbar = reinterpret_cast<uint64_t*>(tc_smem + kOffBar);
-  uint32_t* tbase = reinterpret_cast<uint32_t*>(tc_smem + kOffBar + 8);
-  const uint32_t bar = saddr(mbar);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tc_smem + kOffBar);
+  uint32_t* tbase = reinterpret_cast<uint32_t*>(tc_smem + kOffBar + 8 * kNumBars);
+  volatile int* abort = reinterpret_cast<volatile int*>(tc_smem + kOffBar + 8 * kNumBars + 4);
+  auto bar = [&](int i) { return saddr(bars + i); };
 
-  // the longest (last) query tiles first
-  const int qt = gridDim.x - 1 - blockIdx.x, hqi = blockIdx.y, bl = blockIdx.z;
+  // the longest (last) query blocks first
+  const int qb = gridDim.x - 1 - blockIdx.x, hqi = blockIdx.y, bl = blockIdx.z;
   const int hkvi = hqi / s.group;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // thread (half h, row r): query row r, S columns [32 h, 32 h + 32), O
-  // columns [64 h, 64 h + 64); warps w and w + 4 share TMEM lanes 32 (w % 4) ..
-  const int half = tid >> 7, r = tid & (kTcQ - 1);
+  const int role = tid / kWg, wt = tid % kWg;  // 0, 1: query tiles A, B; 2: producer
   const size_t qrow0 = ((size_t)bl * s.hq + hqi) * n;
   const uint16_t* kb = k + ((size_t)bl * s.hkv + hkvi) * n * kHeadDim;
   const uint16_t* vb = v + ((size_t)bl * s.hkv + hkvi) * n * kHeadDim;
-  const int q0 = qt * kTcQ;
-  const int qi = q0 + r;  // this thread's query row
-  const int n_kt = min((q0 + kTcQ - 1) / kTcKeys + 1, (n + kTcKeys - 1) / kTcKeys);
+  const int qblk = qb * kTcBlock;
+  const int n_a = key_tiles(qblk, n), n_kt = key_tiles(qblk + kTcQ, n);  // tile B sees the most keys
 
-  // Q tile into the operand layout (rows past n zero); 8 consecutive threads
-  // fill one core matrix (8 rows of one 16-byte chunk: 128 contiguous bytes)
-  for (int i = tid; i < kTcQ * (kHeadDim / 8); i += kTcThreads) {
-    const int rr = (i & 7) | ((i >> 7) << 3), c = (i >> 3) & 15;
-    uint8_t* d = sq + core_off(rr, c, kHeadDim / 8);
-    if (q0 + rr < n)
-      cp16(saddr(d), q + (qrow0 + q0 + rr) * kHeadDim + 8 * c);
-    else
-      *reinterpret_cast<uint4*>(d) = make_uint4(0u, 0u, 0u, 0u);
-  }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tbase)),
                  "r"(kTcCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if (tid == 0) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar));
+    for (int i = 0; i < kNumBars; ++i) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar(i)));
+    *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tbase;
-  const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // this warp's lanes
 
-  const uint32_t id_s = instr_desc(kTcQ, kTcKeys, true);
-  const uint32_t id_o = instr_desc(kTcQ, kHeadDim, false);
-  float m = kNegBig, l = 0.0f;  // l: the sum over this thread's columns
-  uint32_t phase = 0;
-  bool ok = true;
-  __half2 vmax = __floats2half2_rn(0.0f, 0.0f);  // largest |V| in fp16 (NaN kept)
-
-  // copies of key tile jt into buffers jt % 2 (rows past n zero): K in the
-  // operand layout (8 consecutive threads per core matrix), V in the staging
-  // layout (16 consecutive threads per row)
-  auto load_kv = [&](int jt) {
-    const int k0 = jt * kTcKeys;
-    uint8_t* dkb = tc_smem + kOffK + (jt & 1) * kTileBytes;
-    uint8_t* dvb = tc_smem + kOffV + (jt & 1) * kTileBytes;
+  if (role == 2) {
+    // ---------------------------------------------------------------- producer
+    __half2 vmax = __floats2half2_rn(0.0f, 0.0f);  // largest |V| in fp16 (NaN kept)
+    const int pw = warp - 8;
+    bool ok = true;
+    auto load = [&](int jt) {
+      const int k0 = jt * kTcKeys;
+      copy_operand(tc_smem + kOffK + (jt % kSlots) * kTileBytes, kb, k0, kTcKeys, n, wt, kWg);
+      uint8_t* dvb = tc_smem + kOffVs + (jt & 1) * kTileBytes;
 #pragma unroll
-    for (int it = 0; it < kTcKeys * (kHeadDim / 8) / kTcThreads; ++it) {
-      const int i = tid + it * kTcThreads;
-      const int rk = (i & 7) | ((i >> 7) << 3), ck = (i >> 3) & 15;
-      const int rv = i >> 4, cv = i & 15;
-      uint8_t* dk = dkb + core_off(rk, ck, kHeadDim / 8);
-      uint8_t* dv = dvb + vstage_off(rv, cv);
-      if (k0 + rk < n)
-        cp16(saddr(dk), kb + (size_t)(k0 + rk) * kHeadDim + 8 * ck);
-      else
-        *reinterpret_cast<uint4*>(dk) = make_uint4(0u, 0u, 0u, 0u);
-      if (k0 + rv < n)
-        cp16(saddr(dv), vb + (size_t)(k0 + rv) * kHeadDim + 8 * cv);
-      else
-        *reinterpret_cast<uint4*>(dv) = make_uint4(0u, 0u, 0u, 0u);
-    }
-  };
-  load_kv(0);  // one copy group with Q
-  asm volatile("cp.async.commit_group;" ::: "memory");
-
-  for (int j = 0; j < n_kt && ok; ++j) {
-    const int k0 = j * kTcKeys;
-    uint8_t* sk = tc_smem + kOffK + (j & 1) * kTileBytes;
-    uint8_t* sv = tc_smem + kOffV + (j & 1) * kTileBytes;
-    // the next tile's copies into the other buffers (free: the previous
-    // tile's MMAs, which read them as P, completed), then this tile's wait
-    if (j + 1 < n_kt) load_kv(j + 1);
-    asm volatile("cp.async.commit_group;\ncp.async.wait_group 1;" ::: "memory");
-    __syncthreads();
-    // V^T (dims x keys) in fp16 in the operand layout: the 8 x 8 block (key
-    // group kg, dim group dg) of V transposed is core matrix (dg, kg) of V^T;
-    // warp w transposes key group w
+      for (int it = 0; it < kTcKeys * (kHeadDim / 8) / kWg; ++it) {
+        const int i = wt + it * kWg;
+        const int rv = i >> 4, cv = i & 15;  // 16 consecutive threads per row
+        uint8_t* dv = dvb + vstage_off(rv, cv);
+        if (k0 + rv < n)
+          cp16(saddr(dv), vb + (size_t)(k0 + rv) * kHeadDim + 8 * cv);
+        else
+          *reinterpret_cast<uint4*>(dv) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    load(0);
+    for (int j = 0; j < n_kt; ++j) {
+      // tile j's copies (issued one tile earlier) visible to the warpgroup
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+      if (!wg_and(kNbProducer, !*abort)) break;
+      // V^T of tile j (dims x keys) in fp16: the 8 x 8 block (key group kg,
+      // dim group dg) of V transposed is core matrix (dg, kg) of V^T
+      const uint8_t* sv = tc_smem + kOffVs + (j & 1) * kTileBytes;
+      uint8_t* svt = tc_smem + kOffVt + (j % kSlots) * kTileBytes;
 #pragma unroll
-    for (int bi = 0; bi < 4; ++bi) {
-      const int kg = warp, dg = 4 * bi;  // 4 blocks per ldmatrix: dims 8 (dg .. dg + 3)
-      const int mi = lane >> 3, rr = lane & 7;
-      uint32_t t0, t1, t2, t3;
-      asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(t0), "=r"(t1), "=r"(t2), "=r"(t3)
-                   : "r"(saddr(sv + vstage_off(8 * kg + rr, dg + mi))));
-      const uint32_t tv[4] = {t0, t1, t2, t3};
+      for (int bi = 0; bi < 8; ++bi) {
+        const int blk = pw * 32 + bi * 4;  // 4 blocks per ldmatrix: dim groups dg .. dg + 3
+        const int kg = blk >> 4, dg = blk & 15;
+        const int mi = lane >> 3, rr = lane & 7;
+        uint32_t t0, t1, t2, t3;
+        asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(t0), "=r"(t1), "=r"(t2), "=r"(t3)
+                     : "r"(saddr(sv + vstage_off(8 * kg + rr, dg + mi))));
+        const uint32_t tv[4] = {t0, t1, t2, t3};
 #pragma unroll
-      for (int mm = 0; mm < 4; ++mm) {
-        const uint32_t hv = f16x2_sat(bf16f(tv[mm] & 0xFFFFu), bf16f(tv[mm] >> 16));
-        vmax = __hmax2_nan(vmax, __habs2(*reinterpret_cast<const __half2*>(&hv)));
-        *reinterpret_cast<uint32_t*>(svt + core_off(8 * (dg + mm) + (lane >> 2), kg, kTcKeys / 8) +
-                                     4 * (lane & 3)) = hv;
+        for (int mm = 0; mm < 4; ++mm) {
+          const uint32_t hv = f16x2_sat(bf16f(tv[mm] & 0xFFFFu), bf16f(tv[mm] >> 16));
+          vmax = __hmax2_nan(vmax, __habs2(*reinterpret_cast<const __half2*>(&hv)));
+          *reinterpret_cast<uint32_t*>(svt + core_off(8 * (dg + mm) + (lane >> 2), kg, kTcKeys / 8) +
+                                       4 * (lane & 3)) = hv;
+        }
+      }
+      // K (copied) and V^T (written) of tile j to the tensor cores' proxy
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      if (!wg_and(kNbProducer, !*abort)) break;
+      if (wt == 0) bar_arrive(bar(kBarFull + j % kSlots));
+      // the slot of tile j + 1 held tile j + 1 - kSlots: free once tile B's
+      // (and, if it saw that tile, A's) P V products have read it
+      if (j + 1 < n_kt) {
+        const int jp = j + 1 - kSlots, sl = (j + 1) % kSlots;
+        if (jp >= 0) {
+          const uint32_t par = (uint32_t)((jp / kSlots) & 1);
+          if (!bar_wait(bar(kBarEmptyB + sl), par, abort)) ok = false;
+          if (ok && jp < n_a && !bar_wait(bar(kBarEmptyA + sl), par, abort)) ok = false;
+          if (!ok) give_up(s, abort);
+        }
+        if (!wg_and(kNbProducer, ok)) break;
+        load(j + 1);  // its V staging buffer held tile j - 1, transposed already
       }
     }
-    publish_to_mma();
-    if (tid == 0) {
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    // a saturated V entry reads 65504 in fp16, which no bf16 value converts to
+    const uint32_t vmb = *reinterpret_cast<const uint32_t*>(&vmax);
+    if ((vmb & 0x7FFFu) >= kF16Max || ((vmb >> 16) & 0x7FFFu) >= kF16Max)
+      atomicOr(&s.counters[kCtrStatus], kDevPrefillRange);
+  } else {
+    // ------------------------------------------------------------ query tile
+    const int x = role, nb = kNbQuery + x;
+    const int q0 = qblk + x * kTcQ, nx = x == 0 ? n_a : n_kt;
+    const int qi = q0 + wt;  // this thread's query row
+    const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // this warp's lanes
+    const uint32_t col_s = kColS + 64 * x, col_o = kColO + 128 * x;
+    uint8_t* sq = tc_smem + kOffQ + x * (kTcQ * kHeadDim * 2);
+    uint8_t* sp = tc_smem + kOffP + x * kTileBytes;
+    const uint32_t bar_s = bar(kBarS + x), bar_o = bar(kBarO + x);
+    const int bar_empty = x == 0 ? kBarEmptyA : kBarEmptyB;
+    const uint32_t id_s = instr_desc(kTcQ, kTcKeys, true);
+    const uint32_t id_o = instr_desc(kTcQ, kHeadDim, false);
+    const bool issuer = wt == 0;
+    int s_issued = 0, s_seen = 0, o_issued = 0, o_seen = 0;  // commits issued / completions waited
+
+    // S(jt) = Q K(jt)^T once the producer has filled the slot (issuing thread)
+    auto issue_s = [&](int jt) -> bool {
+      if (!bar_wait(bar(kBarFull + jt % kSlots), (uint32_t)((jt / kSlots) & 1), abort)) return false;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t kaddr = saddr(tc_smem + kOffK + (jt % kSlots) * kTileBytes);
 #pragma unroll
       for (int ks = 0; ks < kHeadDim / 16; ++ks)
-        mma_f16(tmem, op_desc(saddr(sq) + ks * 256, (kHeadDim / 8) * 128),
-                op_desc(saddr(sk) + ks * 256, (kHeadDim / 8) * 128), id_s, ks > 0);
-      mma_commit(bar);
-    }
-    ok = __syncthreads_and(bar_wait(bar, phase));
-    phase ^= 1u;
-    if (!ok) break;
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        mma_f16(tmem + col_s, op_desc(saddr(sq) + ks * 256, (kHeadDim / 8) * 128),
+                op_desc(kaddr + ks * 256, (kHeadDim / 8) * 128), id_s, ks > 0);
+      mma_commit(bar_s);
+      ++s_issued;
+      return true;
+    };
 
-    // this thread's 32 raw logits; only tiles that cross the diagonal or
-    // the end of the prompt are masked (the test is the same for the CTA)
-    float x[kTcKeys / 2];
-    ld16(trow + 32 * half, *reinterpret_cast<float(*)[16]>(&x[0]));
-    ld16(trow + 32 * half + 16, *reinterpret_cast<float(*)[16]>(&x[16]));
-    if (k0 + kTcKeys - 1 > q0 || k0 + kTcKeys > n) {
-#pragma unroll
-      for (int i = 0; i < kTcKeys / 2; ++i) {
-        const int ki = k0 + 32 * half + i;
-        if (!(ki <= qi && ki < n)) x[i] = -INFINITY;
+    copy_operand(sq, q + qrow0 * kHeadDim, q0, kTcQ, n, wt, kWg);
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    bool ok = wg_and(nb, true);
+    if (issuer && !issue_s(0)) {
+      give_up(s, abort);
+      ok = false;
+    }
+    __syncwarp();
+
+    float m = kNegBig, l = 0.0f;
+    for (int j = 0; j < nx; ++j) {
+      const int k0 = j * kTcKeys;
+      // S(j) complete: read this row
+      if (bar_wait(bar_s, (uint32_t)(j & 1), abort)) {
+        ++s_seen;
+      } else {
+        give_up(s, abort);
+        ok = false;
       }
-    }
-    float mx = -INFINITY;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      float xv[kTcKeys];
 #pragma unroll
-    for (int i = 0; i < kTcKeys / 2; ++i) mx = fmaxf(mx, x[i]);
-    // the row maximum from the two halves, through this tile's V staging
-    // (transposed already; the next copies into it start after two more
-    // barriers)
-    float* red = reinterpret_cast<float*>(sv);
-    red[half * kTcQ + r] = mx;
-    __syncthreads();
-    mx = fmaxf(mx, red[(half ^ 1) * kTcQ + r]) * qk_scale_log2;  // scale > 0: the max commutes
-    // the row maximum moved: rescale the sum and (after the first tile) O.
-    // TMEM loads and stores are warp-collective: the warp rescales when any
-    // of its rows must, the others by 1; both halves decide alike
-    const bool grow = mx > m + kTcLazy;
-    const float alpha = grow ? fast_exp2(m - mx) : 1.0f;
-    if (grow) {
-      l *= alpha;
-      m = mx;
-    }
-    if (j > 0 && __any_sync(0xffffffffu, grow)) {
+      for (int c0 = 0; c0 < kTcKeys; c0 += 16) ld16(trow + col_s + c0, *reinterpret_cast<float(*)[16]>(&xv[c0]));
+      // P V(j - 1) complete (it queued behind S(j)): O may be rescaled and P
+      // overwritten, and that tile's slot goes back to the producer before
+      // this warpgroup asks for the next tile
+      if (j > 0) {
+        if (bar_wait(bar_o, (uint32_t)((j - 1) & 1), abort)) {
+          ++o_seen;
+        } else {
+          give_up(s, abort);
+          ok = false;
+        }
+      }
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      if (!wg_and(nb, ok)) {
+        ok = false;
+        break;
+      }
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      if (issuer && j > 0) bar_arrive(bar(bar_empty + (j - 1) % kSlots));
+      // every row of S(j) is in registers: S(j + 1) may overwrite it
+      if (issuer && j + 1 < nx && !issue_s(j + 1)) {
+        give_up(s, abort);
+        ok = false;
+      }
+      __syncwarp();
+      if (k0 + kTcKeys - 1 > q0 || k0 + kTcKeys > n) {
+#pragma unroll
+        for (int i = 0; i < kTcKeys; ++i) {
+          const int ki = k0 + i;
+          if (!(ki <= qi && ki < n)) xv[i] = -INFINITY;
+        }
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < kTcKeys; ++i) mx = fmaxf(mx, xv[i]);
+      mx *= qk_scale_log2;  // scale > 0: the maximum commutes with it
+      const bool grow = mx > m + kTcLazy;
+      const float alpha = grow ? fast_exp2(m - mx) : 1.0f;
+      if (grow) {
+        l *= alpha;
+        m = mx;
+      }
+      // TMEM loads and stores are warp-collective: the warp rescales when
+      // any of its rows must, the others by 1
+      if (j > 0 && __any_sync(0xffffffffu, grow)) {
 #pragma unroll 1
-      for (int c0 = 0; c0 < kHeadDim / 2; c0 += 16) {
+        for (int c0 = 0; c0 < kHeadDim; c0 += 16) {
+          float t[16];
+          ld16(trow + col_o + c0, t);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) t[i] *= alpha;
+          st16(trow + col_o + c0, t);
+        }
+      }
+      // P in fp16 (the sum adds the unrounded p, as the decode kernels do)
+      const float nm = -m;
+#pragma unroll
+      for (int c = 0; c < kTcKeys / 8; ++c) {
+        uint32_t hw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float p0 = fast_exp2(fmaf(xv[8 * c + 2 * e], qk_scale_log2, nm));
+          const float p1 = fast_exp2(fmaf(xv[8 * c + 2 * e + 1], qk_scale_log2, nm));
+          l += p0 + p1;
+          const __half2 h = __floats2half2_rn(p0, p1);
+          hw[e] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        *reinterpret_cast<uint4*>(sp + core_off(wt, c, kTcKeys / 8)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      if (!wg_and(nb, ok)) {
+        ok = false;
+        break;
+      }
+      if (issuer) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t vtaddr = saddr(tc_smem + kOffVt + (j % kSlots) * kTileBytes);
+#pragma unroll
+        for (int ks = 0; ks < kTcKeys / 16; ++ks)
+          mma_f16(tmem + col_o, op_desc(saddr(sp) + ks * 256, (kTcKeys / 8) * 128),
+                  op_desc(vtaddr + ks * 256, (kTcKeys / 8) * 128), id_o, j > 0 || ks > 0);
+        mma_commit(bar_o);
+        ++o_issued;
+      }
+      __syncwarp();
+    }
+    if (ok) {
+      // P V(last) complete; its slot goes back too (the producer may still
+      // wait for it when this tile sees fewer keys than the other)
+      if (bar_wait(bar_o, (uint32_t)((nx - 1) & 1), abort)) {
+        ++o_seen;
+      } else {
+        give_up(s, abort);
+        ok = false;
+      }
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      if (issuer && ok) bar_arrive(bar(bar_empty + (nx - 1) % kSlots));
+      ok = wg_and(nb, ok);
+    }
+    if (ok) {
+      // O / l to bf16, and the row's (max, sum); every lane reads (the TMEM
+      // load is warp-collective), rows past n store nothing
+      const bool row_ok = qi < n;
+      const float inv = row_ok ? 1.0f / l : 0.0f;
+      uint16_t* orow = out + (qrow0 + (row_ok ? qi : 0)) * kHeadDim;
+#pragma unroll 1
+      for (int c0 = 0; c0 < kHeadDim; c0 += 16) {
         float t[16];
-        ld16(trow + kTcO + 64 * half + c0, t);
+        ld16(trow + col_o + c0, t);
+        uint32_t w[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) t[i] *= alpha;
-        st16(trow + kTcO + 64 * half + c0, t);
+        for (int e = 0; e < 8; ++e) {
+          const __nv_bfloat162 pr = __floats2bfloat162_rn(t[2 * e] * inv, t[2 * e + 1] * inv);
+          w[e] = *reinterpret_cast<const uint32_t*>(&pr);
+        }
+        if (row_ok) {
+          *reinterpret_cast<uint4*>(orow + c0) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(orow + c0 + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+        }
       }
+      if (row_ok) *reinterpret_cast<float2*>(stats + (qrow0 + qi) * 2) = make_float2(m, l);
+    } else if (issuer) {
+      // gave up: a last bounded wait for this tile's products in flight
+      // before the tensor memory goes back
+      for (; s_seen < s_issued; ++s_seen) bar_wait(bar_s, (uint32_t)(s_seen & 1), nullptr);
+      for (; o_seen < o_issued; ++o_seen) bar_wait(bar_o, (uint32_t)(o_seen & 1), nullptr);
     }
-    // P in fp16 over K of this tile (the sum adds the unrounded p, as the
-    // decode kernels do)
-    const float nm = -m;
-#pragma unroll
-    for (int c = 0; c < kTcKeys / 16; ++c) {
-      uint32_t hw[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float p0 = fast_exp2(fmaf(x[8 * c + 2 * e], qk_scale_log2, nm));
-        const float p1 = fast_exp2(fmaf(x[8 * c + 2 * e + 1], qk_scale_log2, nm));
-        l += p0 + p1;
-        const __half2 h = __floats2half2_rn(p0, p1);
-        hw[e] = *reinterpret_cast<const uint32_t*>(&h);
-      }
-      *reinterpret_cast<uint4*>(sk + core_off(r, 4 * half + c, kTcKeys / 8)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    }
-    publish_to_mma();
-    if (tid == 0) {
-#pragma unroll
-      for (int ks = 0; ks < kTcKeys / 16; ++ks)
-        mma_f16(tmem + kTcO, op_desc(saddr(sk) + ks * 256, (kTcKeys / 8) * 128),
-                op_desc(saddr(svt) + ks * 256, (kTcKeys / 8) * 128), id_o, j > 0 || ks > 0);
-      mma_commit(bar);
-    }
-    ok = __syncthreads_and(bar_wait(bar, phase));
-    phase ^= 1u;
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   }
-
-  if (ok) {
-    // the row's sum from the two halves (V^T is free: the MMAs completed)
-    float* red = reinterpret_cast<float*>(svt);
-    red[half * kTcQ + r] = l;
-    __syncthreads();
-    l += red[(half ^ 1) * kTcQ + r];
-    // O / l to bf16, and the row's (max, sum); every lane reads (the TMEM
-    // load is warp-collective), rows past n store nothing
-    const bool row_ok = qi < n;
-    const float inv = row_ok ? 1.0f / l : 0.0f;
-    uint16_t* orow = out + (qrow0 + (row_ok ? qi : 0)) * kHeadDim + 64 * half;
-#pragma unroll 1
-    for (int c0 = 0; c0 < kHeadDim / 2; c0 += 16) {
-      float t[16];
-      ld16(trow + kTcO + 64 * half + c0, t);
-      uint32_t w[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const __nv_bfloat162 pr = __floats2bfloat162_rn(t[2 * e] * inv, t[2 * e + 1] * inv);
-        w[e] = *reinterpret_cast<const uint32_t*>(&pr);
-      }
-      if (row_ok) {
-        *reinterpret_cast<uint4*>(orow + c0) = make_uint4(w[0], w[1], w[2], w[3]);
-        *reinterpret_cast<uint4*>(orow + c0 + 8) = make_uint4(w[4], w[5], w[6], w[7]);
-      }
-    }
-    if (row_ok && half == 0) *reinterpret_cast<float2*>(stats + (qrow0 + qi) * 2) = make_float2(m, l);
-  } else {
-    if (tid == 0) atomicOr(&s.counters[kCtrStatus], kDevWaitTimeout);
-    // a last bounded wait for the MMAs whose completion did not come (the
-    // phase was flipped after the failed wait) before the columns go back
-    bar_wait(bar, phase ^ 1u);
-  }
-  // a saturated V entry reads 65504 in fp16, which no bf16 value converts to
-  const uint32_t vmb = *reinterpret_cast<const uint32_t*>(&vmax);
-  if ((vmb & 0x7FFFu) >= kF16Max || ((vmb >> 16) & 0x7FFFu) >= kF16Max)
-    atomicOr(&s.counters[kCtrStatus], kDevPrefillRange);
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcCols));
@@ -405,9 +519,9 @@ cudaError_t launch_prefill_fwd_tc(const DevState& s, int batch, int n, const uin
   static int done[64] = {0};
   const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(prefill_fwd_tc_kernel), kTcSmem, done);
   if (e != cudaSuccess) return e;
-  const int tiles = (n + kTcQ - 1) / kTcQ;
-  prefill_fwd_tc_kernel<<<dim3(tiles, s.hq, batch), kTcThreads, kTcSmem, st>>>(s, n, q, k, v, out, stats,
-                                                                               qk_scale_log2);
+  const int blocks = (n + kTcBlock - 1) / kTcBlock;
+  prefill_fwd_tc_kernel<<<dim3(blocks, s.hq, batch), kTcThreads, kTcSmem, st>>>(s, n, q, k, v, out, stats,
+                                                                                qk_scale_log2);
   return cudaGetLastError();
 }
 
