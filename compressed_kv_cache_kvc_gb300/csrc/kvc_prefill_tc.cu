@@ -10,12 +10,14 @@
 //   * warpgroups 0 and 1 ("A" and "B") each own one 128-query tile; thread t
 //     of a warpgroup owns query row t of its tile, TMEM lane t.  TMEM columns:
 //     S_A [0, 64), S_B [64, 128), O_A [128, 256), O_B [256, 384);
-//   * warpgroup 2 (the producer) copies 64-key tiles into a ring of three
-//     slots by cp.async: K into the operand layout (K-major, no swizzle,
-//     8-row x 16-byte core matrices), V into a staging tile (16-byte chunks
-//     XOR-swizzled by row) that it transposes by ldmatrix.trans into a
-//     dims x keys operand in fp16.  A slot is refilled once both query tiles'
-//     P V products have read it.
+//   * warpgroup 2 (the producer) brings 64-key tiles into a ring of three
+//     slots by TMA (one thread issues the tensor copies, an mbarrier counts
+//     their bytes; rows past the prompt read as zeros): K and V each as two
+//     64 x 64 boxes with the 128-byte swizzle; K is read in place by the MMA
+//     (K-major, 128-byte swizzle), V is staged and the warpgroup transposes
+//     it by ldmatrix.trans into a dims x keys operand in fp16 (K-major, no
+//     swizzle, 8-row x 16-byte core matrices).  A slot is refilled once both query tiles' P V products have
+//     read it.
 // Per key tile j a query warpgroup: waits for S(j) (its issuing thread put it
 // on the tensor cores one tile ahead), reads its S row (tcgen05.ld), lets
 // the issuing thread start S(j + 1) = Q K(j + 1)^T (M 128, N 64, bf16: exact
@@ -37,6 +39,7 @@
 // runs out sets KVC_DEV_WAIT_TIMEOUT, every warpgroup leaves its loop at its
 // next barrier, the issuing threads wait (bounded) for their products in
 // flight, and the CTA frees its tensor memory.
+#include <cuda.h>  // CUtensorMap; the encoder comes through the runtime's driver entry point
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -62,22 +65,26 @@ constexpr int kTcWaitLimit = 1 << 22;
 
 constexpr int kTileBytes = kTcKeys * kHeadDim * 2;           // 16 KB
 constexpr int kOffQ = 0;                                      // 2 x 32 KB: Q_A, Q_B (operand layout)
-constexpr int kOffK = kOffQ + 2 * kTcQ * kHeadDim * 2;        // 3 x 16 KB: K ring (operand layout)
+constexpr int kOffK = kOffQ + 2 * kTcQ * kHeadDim * 2;        // 3 x 16 KB: K ring (TMA, 128-byte swizzle)
 constexpr int kOffVt = kOffK + kSlots * kTileBytes;           // 3 x 16 KB: V^T ring, fp16 (operand layout)
-constexpr int kOffVs = kOffVt + kSlots * kTileBytes;          // 2 x 16 KB: V staging (producer)
+constexpr int kOffVs = kOffVt + kSlots * kTileBytes;          // 2 x 16 KB: V staging (producer, TMA, 1 KB aligned)
 constexpr int kOffP = kOffVs + 2 * kTileBytes;                // 2 x 16 KB: P_A, P_B (operand layout)
 constexpr int kOffBar = kOffP + 2 * kTileBytes;               // mbarriers, TMEM base, abort flag
 constexpr int kBarFull = 0, kBarEmptyA = kSlots, kBarEmptyB = 2 * kSlots, kBarS = 3 * kSlots,
-              kBarO = 3 * kSlots + 2, kNumBars = 3 * kSlots + 4;
+              kBarO = 3 * kSlots + 2, kBarTma = 3 * kSlots + 4, kNumBars = 3 * kSlots + 6;
+static_assert(kOffK % 1024 == 0 && kOffVs % 1024 == 0, "the 128-byte swizzle wants 1 KB aligned boxes");
 constexpr int kTcSmem = kOffBar + 8 * kNumBars + 16;
 
 // named barriers (0 is __syncthreads)
 constexpr int kNbQuery = 1;  // + query tile: 1, 2
 constexpr int kNbProducer = 3;
 
-// Staged V: row r (a key) of 256 bytes, its 16-byte chunk c at c ^ (r % 8),
-// so the 8 rows an ldmatrix reads together lie on different banks.
-__device__ __forceinline__ int vstage_off(int r, int c) { return r * 256 + ((c ^ (r & 7)) << 4); }
+// Staged V as TMA writes it with the 128-byte swizzle: dims [64 b, 64 b + 64)
+// in box b (8 KB), row r (a key) of 128 bytes, its 16-byte chunk c at
+// c ^ (r % 8), so the 8 rows an ldmatrix reads together lie on different banks.
+__device__ __forceinline__ int vstage_off(int r, int c) {
+  return ((c >> 3) << 13) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
 
 __device__ __forceinline__ uint32_t saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -87,11 +94,19 @@ __device__ __forceinline__ uint32_t saddr(const void* p) { return (uint32_t)__cv
 __device__ __forceinline__ int core_off(int r, int c, int kch) { return ((r >> 3) * kch + c) * 128 + (r & 7) * 16; }
 
 // Shared-memory operand descriptor: K-major, no swizzle; leading byte offset
-// (between the two core matrices of a K step) 128, stride byte offset
+// `lbo` (between the two core matrices of a K step), stride byte offset
 // `sbo` (between 8-row groups); descriptor version 1.
-__device__ __forceinline__ uint64_t op_desc(uint32_t addr, uint32_t sbo) {
-  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) |
-         ((uint64_t)1 << 46);
+__device__ __forceinline__ uint64_t op_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46);
+}
+
+// Descriptor of a K-major operand with the 128-byte swizzle (as TMA writes
+// it): 8-row groups of 128-byte rows 1 KB apart; the leading byte offset is
+// unused; layout type 2 at bit 61.  A K step of 16 elements advances the
+// start address by 32 bytes inside the 128-byte row.
+__device__ __forceinline__ uint64_t op_desc_sw128(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
 // fp16 bits of 65504, its largest finite value.  bf16 magnitudes from 65536
@@ -123,6 +138,20 @@ __device__ __forceinline__ void mma_f16(uint32_t dtmem, uint64_t a, uint64_t b, 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
+}
+
+__device__ __forceinline__ void bar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}\n" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+// One TMA box of a 3-d tensor map into shared memory, counted on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
 }
 
 __device__ __forceinline__ void bar_arrive(uint32_t bar) {
@@ -213,12 +242,10 @@ __device__ __forceinline__ int key_tiles(int q0, int n) {
   return min((q0 + kTcQ - 1) / kTcKeys + 1, (n + kTcKeys - 1) / kTcKeys);
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1) prefill_fwd_tc_kernel(DevState s, int n,
-                                                                      const uint16_t* __restrict__ q,
-                                                                      const uint16_t* __restrict__ k,
-                                                                      const uint16_t* __restrict__ v,
-                                                                      uint16_t* __restrict__ out,
-                                                                      float* __restrict__ stats, float qk_scale_log2) {
+__global__ void __launch_bounds__(kTcThreads, 1)
+    prefill_fwd_tc_kernel(DevState s, int n, const uint16_t* __restrict__ q, const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v, uint16_t* __restrict__ out,
+                          float* __restrict__ stats, float qk_scale_log2) {
   extern __shared__ __align__(1024) uint8_t tc_smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(tc_smem + kOffBar);
   uint32_t* tbase = reinterpret_cast<uint32_t*>(tc_smem + kOffBar + 8 * kNumBars);
@@ -231,8 +258,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_fwd_tc_kernel(DevState 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int role = tid / kWg, wt = tid % kWg;  // 0, 1: query tiles A, B; 2: producer
   const size_t qrow0 = ((size_t)bl * s.hq + hqi) * n;
-  const uint16_t* kb = k + ((size_t)bl * s.hkv + hkvi) * n * kHeadDim;
-  const uint16_t* vb = v + ((size_t)bl * s.hkv + hkvi) * n * kHeadDim;
+  const int zkv = bl * s.hkv + hkvi;  // the (sequence, KV head) plane of the K / V tensor maps
   const int qblk = qb * kTcBlock;
   const int n_a = key_tiles(qblk, n), n_kt = key_tiles(qblk + kTcQ, n);  // tile B sees the most keys
 
@@ -256,27 +282,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_fwd_tc_kernel(DevState 
     __half2 vmax = __floats2half2_rn(0.0f, 0.0f);  // largest |V| in fp16 (NaN kept)
     const int pw = warp - 8;
     bool ok = true;
+    int issued = 0, landed = 0;  // tiles whose copies were issued / seen complete
+    // tile jt's K into its ring slot and V into staging buffer jt % 2 (one
+    // thread; the staging buffer held tile jt - 2, transposed already)
     auto load = [&](int jt) {
-      const int k0 = jt * kTcKeys;
-      copy_operand(tc_smem + kOffK + (jt % kSlots) * kTileBytes, kb, k0, kTcKeys, n, wt, kWg);
-      uint8_t* dvb = tc_smem + kOffVs + (jt & 1) * kTileBytes;
-#pragma unroll
-      for (int it = 0; it < kTcKeys * (kHeadDim / 8) / kWg; ++it) {
-        const int i = wt + it * kWg;
-        const int rv = i >> 4, cv = i & 15;  // 16 consecutive threads per row
-        uint8_t* dv = dvb + vstage_off(rv, cv);
-        if (k0 + rv < n)
-          cp16(saddr(dv), vb + (size_t)(k0 + rv) * kHeadDim + 8 * cv);
-        else
-          *reinterpret_cast<uint4*>(dv) = make_uint4(0u, 0u, 0u, 0u);
-      }
-      asm volatile("cp.async.commit_group;" ::: "memory");
+      const uint32_t tb = bar(kBarTma + (jt & 1));
+      bar_expect_tx(tb, 2 * kTileBytes);
+      const uint32_t kdst = saddr(tc_smem + kOffK + (jt % kSlots) * kTileBytes);
+      tma_load_3d(kdst, &tm_k, 0, jt * kTcKeys, zkv, tb);
+      tma_load_3d(kdst + kTileBytes / 2, &tm_k, 64, jt * kTcKeys, zkv, tb);
+      const uint32_t vdst = saddr(tc_smem + kOffVs + (jt & 1) * kTileBytes);
+      tma_load_3d(vdst, &tm_v, 0, jt * kTcKeys, zkv, tb);
+      tma_load_3d(vdst + kTileBytes / 2, &tm_v, 64, jt * kTcKeys, zkv, tb);
     };
-    load(0);
+    if (wt == 0) load(0);
+    issued = 1;
     for (int j = 0; j < n_kt; ++j) {
-      // tile j's copies (issued one tile earlier) visible to the warpgroup
-      asm volatile("cp.async.wait_group 0;" ::: "memory");
-      if (!wg_and(kNbProducer, !*abort)) break;
+      // tile j's copies complete
+      if (bar_wait(bar(kBarTma + (j & 1)), (uint32_t)((j >> 1) & 1), abort)) {
+        ++landed;
+      } else {
+        give_up(s, abort);
+        ok = false;
+      }
+      if (!wg_and(kNbProducer, ok)) break;
       // V^T of tile j (dims x keys) in fp16: the 8 x 8 block (key group kg,
       // dim group dg) of V transposed is core matrix (dg, kg) of V^T
       const uint8_t* sv = tc_smem + kOffVs + (j & 1) * kTileBytes;
@@ -299,7 +328,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_fwd_tc_kernel(DevState 
                                        4 * (lane & 3)) = hv;
         }
       }
-      // K (copied) and V^T (written) of tile j to the tensor cores' proxy
+      // V^T (written) of tile j to the tensor cores' proxy; K came by TMA
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       if (!wg_and(kNbProducer, !*abort)) break;
       if (wt == 0) bar_arrive(bar(kBarFull + j % kSlots));
@@ -314,10 +343,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_fwd_tc_kernel(DevState 
           if (!ok) give_up(s, abort);
         }
         if (!wg_and(kNbProducer, ok)) break;
-        load(j + 1);  // its V staging buffer held tile j - 1, transposed already
+        if (wt == 0) load(j + 1);
+        ++issued;
       }
     }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    // copies in flight (left behind after a failed wait) land before the CTA
+    // goes away
+    if (wt == 0)
+      for (; landed < issued; ++landed) bar_wait(bar(kBarTma + (landed & 1)), (uint32_t)((landed >> 1) & 1), nullptr);
     // a saturated V entry reads 65504 in fp16, which no bf16 value converts to
     const uint32_t vmb = *reinterpret_cast<const uint32_t*>(&vmax);
     if ((vmb & 0x7FFFu) >= kF16Max || ((vmb >> 16) & 0x7FFFu) >= kF16Max)
@@ -345,8 +378,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_fwd_tc_kernel(DevState 
       const uint32_t kaddr = saddr(tc_smem + kOffK + (jt % kSlots) * kTileBytes);
 #pragma unroll
       for (int ks = 0; ks < kHeadDim / 16; ++ks)
-        mma_f16(tmem + col_s, op_desc(saddr(sq) + ks * 256, (kHeadDim / 8) * 128),
-                op_desc(kaddr + ks * 256, (kHeadDim / 8) * 128), id_s, ks > 0);
+        mma_f16(tmem + col_s, op_desc(saddr(sq) + ks * 256, 128, (kHeadDim / 8) * 128),
+                op_desc_sw128(kaddr + (ks >> 2) * (kTileBytes / 2) + (ks & 3) * 32), id_s, ks > 0);
       mma_commit(bar_s);
       ++s_issued;
       return true;
@@ -455,8 +488,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_fwd_tc_kernel(DevState 
         const uint32_t vtaddr = saddr(tc_smem + kOffVt + (j % kSlots) * kTileBytes);
 #pragma unroll
         for (int ks = 0; ks < kTcKeys / 16; ++ks)
-          mma_f16(tmem + col_o, op_desc(saddr(sp) + ks * 256, (kTcKeys / 8) * 128),
-                  op_desc(vtaddr + ks * 256, (kTcKeys / 8) * 128), id_o, j > 0 || ks > 0);
+          mma_f16(tmem + col_o, op_desc(saddr(sp) + ks * 256, 128, (kTcKeys / 8) * 128),
+                  op_desc(vtaddr + ks * 256, 128, (kTcKeys / 8) * 128), id_o, j > 0 || ks > 0);
         mma_commit(bar_o);
         ++o_issued;
       }
@@ -513,14 +546,52 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_fwd_tc_kernel(DevState 
 
 int prefill_fwd_tc_smem_bytes() { return kTcSmem; }
 
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn tensor_map_encoder() {
+  static const EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) !=
+            cudaSuccess ||
+        qr != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// A [planes][n][128] bf16 tensor as a 3-d tensor map with 64 x 64 x 1 boxes
+// and the 128-byte swizzle; rows past n read as zeros.
+bool encode_kv_map(CUtensorMap* map, const uint16_t* base, int n, int planes) {
+  const EncodeTiledFn enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)n, (cuuint64_t)planes};
+  const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)n * kHeadDim * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)kTcKeys, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 cudaError_t launch_prefill_fwd_tc(const DevState& s, int batch, int n, const uint16_t* q, const uint16_t* k,
                                   const uint16_t* v, uint16_t* out, float* stats, float qk_scale_log2,
                                   cudaStream_t st) {
   static int done[64] = {0};
   const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(prefill_fwd_tc_kernel), kTcSmem, done);
   if (e != cudaSuccess) return e;
+  CUtensorMap tm_k, tm_v;
+  if (!encode_kv_map(&tm_k, k, n, batch * s.hkv) || !encode_kv_map(&tm_v, v, n, batch * s.hkv))
+    return cudaErrorInvalidValue;
   const int blocks = (n + kTcBlock - 1) / kTcBlock;
-  prefill_fwd_tc_kernel<<<dim3(blocks, s.hq, batch), kTcThreads, kTcSmem, st>>>(s, n, q, k, v, out, stats,
+  prefill_fwd_tc_kernel<<<dim3(blocks, s.hq, batch), kTcThreads, kTcSmem, st>>>(s, n, q, tm_k, tm_v, out, stats,
                                                                                 qk_scale_log2);
   return cudaGetLastError();
 }
