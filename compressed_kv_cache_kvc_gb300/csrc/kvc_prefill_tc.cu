@@ -9,7 +9,8 @@
 // blocks first, three warpgroups with fixed roles:
 //   * warpgroups 0 and 1 ("A" and "B") each own one 128-query tile; thread t
 //     of a warpgroup owns query row t of its tile, TMEM lane t.  TMEM columns:
-//     S_A [0, 64), S_B [64, 128), O_A [128, 256), O_B [256, 384);
+//     S_A [0, 64), S_B [64, 128), O_A [128, 256), O_B [256, 384), P_A
+//     [384, 416), P_B [416, 448) (P in fp16, two per column);
 //   * warpgroup 2 (the producer) brings 64-key tiles into a ring of three
 //     slots by TMA (one thread issues the tensor copies, an mbarrier counts
 //     their bytes; rows past the prompt read as zeros): K and V each as two
@@ -25,7 +26,8 @@
 // prompt), runs the online softmax in the log2 domain with a lazy maximum (O
 // is rescaled in TMEM only when the row maximum grows by more than 8), waits
 // for P V(j - 1), writes P in fp16 (11 significant bits; p <= 2^8 by the lazy
-// maximum) and issues O += P V(j) (M 128, N 128, K 64, fp16 operands).  The
+// maximum) into tensor memory and issues O += P V(j) (M 128, N 128, K 64,
+// fp16 operands, P read from tensor memory as the A operand).  The
 // two query warpgroups run out of step, so one's softmax overlaps the other's
 // products and the producer's copies overlap both.  A bf16 P alone missed
 // the output tolerance on rows that see few keys.  V entries beyond fp16's
@@ -61,6 +63,7 @@ constexpr float kTcLazy = 8.0f;           // log2 units the running maximum may 
 constexpr uint32_t kTcCols = 512;         // TMEM columns allocated
 constexpr uint32_t kColS = 0;             // S of query tile x at kColS + 64 x
 constexpr uint32_t kColO = 128;           // O of query tile x at kColO + 128 x
+constexpr uint32_t kColP = 384;           // P of query tile x at kColP + 32 x
 constexpr int kTcWaitLimit = 1 << 22;
 
 constexpr int kTileBytes = kTcKeys * kHeadDim * 2;           // 16 KB
@@ -68,8 +71,7 @@ constexpr int kOffQ = 0;                                      // 2 x 32 KB: Q_A,
 constexpr int kOffK = kOffQ + 2 * kTcQ * kHeadDim * 2;        // 3 x 16 KB: K ring (TMA, 128-byte swizzle)
 constexpr int kOffVt = kOffK + kSlots * kTileBytes;           // 3 x 16 KB: V^T ring, fp16 (operand layout)
 constexpr int kOffVs = kOffVt + kSlots * kTileBytes;          // 2 x 16 KB: V staging (producer, TMA, 1 KB aligned)
-constexpr int kOffP = kOffVs + 2 * kTileBytes;                // 2 x 16 KB: P_A, P_B (operand layout)
-constexpr int kOffBar = kOffP + 2 * kTileBytes;               // mbarriers, TMEM base, abort flag
+constexpr int kOffBar = kOffVs + 2 * kTileBytes;              // mbarriers, TMEM base, abort flag
 constexpr int kBarFull = 0, kBarEmptyA = kSlots, kBarEmptyB = 2 * kSlots, kBarS = 3 * kSlots,
               kBarO = 3 * kSlots + 2, kBarTma = 3 * kSlots + 4, kNumBars = 3 * kSlots + 6;
 static_assert(kOffK % 1024 == 0 && kOffVs % 1024 == 0, "the 128-byte swizzle wants 1 KB aligned boxes");
@@ -133,6 +135,14 @@ __device__ __forceinline__ void mma_f16(uint32_t dtmem, uint64_t a, uint64_t b, 
       "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(dtmem),
       "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)acc));
+}
+
+// The same with A (M x K, K-major) read from tensor memory at `atmem`.
+__device__ __forceinline__ void mma_f16_ts(uint32_t dtmem, uint32_t atmem, uint64_t b, uint32_t idesc, bool acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(dtmem),
+      "r"(atmem), "l"(b), "r"(idesc), "r"((uint32_t)acc));
 }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -203,6 +213,15 @@ __device__ __forceinline__ void ld16(uint32_t taddr, float (&v)[16]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void st16u(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]));
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void st16(uint32_t taddr, const float (&v)[16]) {
@@ -361,9 +380,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int q0 = qblk + x * kTcQ, nx = x == 0 ? n_a : n_kt;
     const int qi = q0 + wt;  // this thread's query row
     const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // this warp's lanes
-    const uint32_t col_s = kColS + 64 * x, col_o = kColO + 128 * x;
+    const uint32_t col_s = kColS + 64 * x, col_o = kColO + 128 * x, col_p = kColP + 32 * x;
     uint8_t* sq = tc_smem + kOffQ + x * (kTcQ * kHeadDim * 2);
-    uint8_t* sp = tc_smem + kOffP + x * kTileBytes;
     const uint32_t bar_s = bar(kBarS + x), bar_o = bar(kBarO + x);
     const int bar_empty = x == 0 ? kBarEmptyA : kBarEmptyB;
     const uint32_t id_s = instr_desc(kTcQ, kTcKeys, true);
@@ -462,22 +480,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           st16(trow + col_o + c0, t);
         }
       }
-      // P in fp16 (the sum adds the unrounded p, as the decode kernels do)
+      // P in fp16 into tensor memory, keys 2c and 2c + 1 in column c (the
+      // sum adds the unrounded p, as the decode kernels do)
       const float nm = -m;
 #pragma unroll
-      for (int c = 0; c < kTcKeys / 8; ++c) {
-        uint32_t hw[4];
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pw[16];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = fast_exp2(fmaf(xv[8 * c + 2 * e], qk_scale_log2, nm));
-          const float p1 = fast_exp2(fmaf(xv[8 * c + 2 * e + 1], qk_scale_log2, nm));
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = fast_exp2(fmaf(xv[32 * h + 2 * e], qk_scale_log2, nm));
+          const float p1 = fast_exp2(fmaf(xv[32 * h + 2 * e + 1], qk_scale_log2, nm));
           l += p0 + p1;
-          const __half2 h = __floats2half2_rn(p0, p1);
-          hw[e] = *reinterpret_cast<const uint32_t*>(&h);
+          const __half2 hh = __floats2half2_rn(p0, p1);
+          pw[e] = *reinterpret_cast<const uint32_t*>(&hh);
         }
-        *reinterpret_cast<uint4*>(sp + core_off(wt, c, kTcKeys / 8)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        st16u(trow + col_p + 16 * h, pw);
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       if (!wg_and(nb, ok)) {
         ok = false;
@@ -488,8 +506,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t vtaddr = saddr(tc_smem + kOffVt + (j % kSlots) * kTileBytes);
 #pragma unroll
         for (int ks = 0; ks < kTcKeys / 16; ++ks)
-          mma_f16(tmem + col_o, op_desc(saddr(sp) + ks * 256, 128, (kTcKeys / 8) * 128),
-                  op_desc(vtaddr + ks * 256, 128, (kTcKeys / 8) * 128), id_o, j > 0 || ks > 0);
+          mma_f16_ts(tmem + col_o, tmem + col_p + 8 * ks, op_desc(vtaddr + ks * 256, 128, (kTcKeys / 8) * 128), id_o,
+                     j > 0 || ks > 0);
         mma_commit(bar_o);
         ++o_issued;
       }
