@@ -5,8 +5,8 @@
 // scores come from prefill_scores_kernel (kvc_prefill.cu), which uses these
 // statistics.
 //
-// One 384-thread CTA per (256-query block, query head, sequence), longest
-// blocks first, three warpgroups with fixed roles:
+// One 416-thread CTA per (256-query block, query head, sequence), longest
+// blocks first, warps with fixed roles:
 //   * warpgroups 0 and 1 ("A" and "B") each own one 128-query tile; thread t
 //     of a warpgroup owns query row t of its tile, TMEM lane t.  TMEM columns:
 //     S_A [0, 64), S_B [64, 128), O_A [128, 256), O_B [256, 384), P_A
@@ -17,30 +17,31 @@
 //     64 x 64 boxes with the 128-byte swizzle; K is read in place by the MMA
 //     (K-major, 128-byte swizzle), V is staged and the warpgroup transposes
 //     it by ldmatrix.trans into a dims x keys operand in fp16 (K-major, no
-//     swizzle, 8-row x 16-byte core matrices).  A slot is refilled once both query tiles' P V products have
-//     read it.
-// Per key tile j a query warpgroup: waits for S(j) (its issuing thread put it
-// on the tensor cores one tile ahead), reads its S row (tcgen05.ld), lets
-// the issuing thread start S(j + 1) = Q K(j + 1)^T (M 128, N 64, bf16: exact
-// products), masks (only tiles that cross the diagonal or the end of the
+//     swizzle, 8-row x 16-byte core matrices).  A slot is refilled once both
+//     query tiles' P V products have read it;
+//   * warp 12 issues every tensor-core product from one thread: for each
+//     key tile j, S_A(j + 1) and S_B(j + 1) = Q K(j + 1)^T (M 128, N 64,
+//     bf16: exact products) as soon as the query tiles have read S(j), then
+//     O_A += P_A V(j) and O_B += P_B V(j) (M 128, N 128, K 64, fp16, P read
+//     from tensor memory as the A operand) as soon as they have written P.
+// Per key tile j a query warpgroup waits for S(j), reads its S row
+// (tcgen05.ld), masks (only tiles that cross the diagonal or the end of the
 // prompt), runs the online softmax in the log2 domain with a lazy maximum (O
 // is rescaled in TMEM only when the row maximum grows by more than 8), waits
-// for P V(j - 1), writes P in fp16 (11 significant bits; p <= 2^8 by the lazy
-// maximum) into tensor memory and issues O += P V(j) (M 128, N 128, K 64,
-// fp16 operands, P read from tensor memory as the A operand).  The
-// two query warpgroups run out of step, so one's softmax overlaps the other's
-// products and the producer's copies overlap both.  A bf16 P alone missed
-// the output tolerance on rows that see few keys.  V entries beyond fp16's
-// range (|v| >= 65536, or not finite) saturate to +-65504 and set
-// KVC_DEV_PREFILL_RANGE.
+// for P V(j - 1), and writes P in fp16 (11 significant bits; p <= 2^8 by the
+// lazy maximum) into tensor memory.  The two query warpgroups run out of
+// step, so one's softmax overlaps the other's products and the producer's
+// copies overlap both.  A bf16 P alone missed the output tolerance on rows
+// that see few keys.  V entries beyond fp16's range (|v| >= 65536, or not
+// finite) saturate to +-65504 and set KVC_DEV_PREFILL_RANGE.
 //
-// Synchronisation: mbarriers (the producer's "slot full", the query
-// warpgroups' "slot empty", the tensor cores' completions through
-// tcgen05.commit) and named barriers inside a warpgroup.  Every mbarrier wait
-// is bounded and also ends when another thread has given up; a wait that
-// runs out sets KVC_DEV_WAIT_TIMEOUT, every warpgroup leaves its loop at its
-// next barrier, the issuing threads wait (bounded) for their products in
-// flight, and the CTA frees its tensor memory.
+// Synchronisation: mbarriers (Q loaded, S read and P written by the query
+// warpgroups, slot full from the producer, slot empty and S / P V complete
+// through tcgen05.commit) and named barriers inside a warpgroup.  Every
+// mbarrier wait is bounded and also ends when another thread has given up;
+// a wait that runs out sets KVC_DEV_WAIT_TIMEOUT, every role leaves its loop,
+// the issuing thread waits (bounded) for its products in flight, and the
+// CTA frees its tensor memory.
 #include <cuda.h>  // CUtensorMap; the encoder comes through the runtime's driver entry point
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -54,7 +55,7 @@ namespace {
 using namespace dev;
 
 constexpr int kWg = 128;                  // threads per warpgroup
-constexpr int kTcThreads = 3 * kWg;       // query tiles A and B, producer
+constexpr int kTcThreads = 3 * kWg + 32;  // query tiles A and B, producer, MMA warp
 constexpr int kTcQ = 128;                 // queries per tile (the MMAs' M)
 constexpr int kTcBlock = 2 * kTcQ;        // queries per CTA
 constexpr int kTcKeys = 64;               // keys per tile
@@ -72,8 +73,12 @@ constexpr int kOffK = kOffQ + 2 * kTcQ * kHeadDim * 2;        // 3 x 16 KB: K ri
 constexpr int kOffVt = kOffK + kSlots * kTileBytes;           // 3 x 16 KB: V^T ring, fp16 (operand layout)
 constexpr int kOffVs = kOffVt + kSlots * kTileBytes;          // 2 x 16 KB: V staging (producer, TMA, 1 KB aligned)
 constexpr int kOffBar = kOffVs + 2 * kTileBytes;              // mbarriers, TMEM base, abort flag
-constexpr int kBarFull = 0, kBarEmptyA = kSlots, kBarEmptyB = 2 * kSlots, kBarS = 3 * kSlots,
-              kBarO = 3 * kSlots + 2, kBarTma = 3 * kSlots + 4, kNumBars = 3 * kSlots + 6;
+// mbarriers: tile published / slot read (per slot), S and P V complete, S
+// read, P written, Q loaded (per query tile), TMA bytes landed (per staging
+// tile), the issuing thread's products all complete
+constexpr int kBarFull = 0, kBarEmpty = kSlots, kBarS = 2 * kSlots, kBarO = kBarS + 2, kBarSfree = kBarO + 2,
+              kBarPfull = kBarSfree + 2, kBarQ = kBarPfull + 2, kBarTma = kBarQ + 2, kBarDone = kBarTma + 2,
+              kNumBars = kBarDone + 1;
 static_assert(kOffK % 1024 == 0 && kOffVs % 1024 == 0, "the 128-byte swizzle wants 1 KB aligned boxes");
 constexpr int kTcSmem = kOffBar + 8 * kNumBars + 16;
 
@@ -166,6 +171,17 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
 
 __device__ __forceinline__ void bar_arrive(uint32_t bar) {
   asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}\n" ::"r"(bar) : "memory");
+}
+
+// Whether the mbarrier's phase `parity` has completed (does not wait).
+__device__ __forceinline__ bool bar_test(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
 }
 
 // Bounded wait for the mbarrier's phase `parity`; true when it completed.
@@ -275,7 +291,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int qb = gridDim.x - 1 - blockIdx.x, hqi = blockIdx.y, bl = blockIdx.z;
   const int hkvi = hqi / s.group;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int role = tid / kWg, wt = tid % kWg;  // 0, 1: query tiles A, B; 2: producer
+  const int role = tid / kWg, wt = tid % kWg;  // 0, 1: query tiles A, B; 2: producer; 3: MMA warp
   const size_t qrow0 = ((size_t)bl * s.hq + hqi) * n;
   const int zkv = bl * s.hkv + hkvi;  // the (sequence, KV head) plane of the K / V tensor maps
   const int qblk = qb * kTcBlock;
@@ -351,15 +367,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       if (!wg_and(kNbProducer, !*abort)) break;
       if (wt == 0) bar_arrive(bar(kBarFull + j % kSlots));
-      // the slot of tile j + 1 held tile j + 1 - kSlots: free once tile B's
-      // (and, if it saw that tile, A's) P V products have read it
+      // the slot of tile j + 1 held tile j + 1 - kSlots: free once the last
+      // P V product of that tile completed
       if (j + 1 < n_kt) {
-        const int jp = j + 1 - kSlots, sl = (j + 1) % kSlots;
-        if (jp >= 0) {
-          const uint32_t par = (uint32_t)((jp / kSlots) & 1);
-          if (!bar_wait(bar(kBarEmptyB + sl), par, abort)) ok = false;
-          if (ok && jp < n_a && !bar_wait(bar(kBarEmptyA + sl), par, abort)) ok = false;
-          if (!ok) give_up(s, abort);
+        const int jp = j + 1 - kSlots;
+        if (jp >= 0 && !bar_wait(bar(kBarEmpty + jp % kSlots), (uint32_t)((jp / kSlots) & 1), abort)) {
+          give_up(s, abort);
+          ok = false;
         }
         if (!wg_and(kNbProducer, ok)) break;
         if (wt == 0) load(j + 1);
@@ -374,6 +388,88 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t vmb = *reinterpret_cast<const uint32_t*>(&vmax);
     if ((vmb & 0x7FFFu) >= kF16Max || ((vmb >> 16) & 0x7FFFu) >= kF16Max)
       atomicOr(&s.counters[kCtrStatus], kDevPrefillRange);
+  } else if (role == 3) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_s = instr_desc(kTcQ, kTcKeys, true);
+      const uint32_t id_o = instr_desc(kTcQ, kHeadDim, false);
+      // S_x(jt) = Q_x K(jt)^T
+      auto mma_s = [&](int x, int jt) {
+        const uint32_t qaddr = saddr(tc_smem + kOffQ + x * (kTcQ * kHeadDim * 2));
+        const uint32_t kaddr = saddr(tc_smem + kOffK + (jt % kSlots) * kTileBytes);
+#pragma unroll
+        for (int ks = 0; ks < kHeadDim / 16; ++ks)
+          mma_f16(tmem + kColS + 64 * x, op_desc(qaddr + ks * 256, 128, (kHeadDim / 8) * 128),
+                  op_desc_sw128(kaddr + (ks >> 2) * (kTileBytes / 2) + (ks & 3) * 32), id_s, ks > 0);
+        mma_commit(bar(kBarS + x));
+      };
+      // O_x += P_x V(jt)
+      auto mma_pv = [&](int x, int jt) {
+        const uint32_t vtaddr = saddr(tc_smem + kOffVt + (jt % kSlots) * kTileBytes);
+#pragma unroll
+        for (int ks = 0; ks < kTcKeys / 16; ++ks)
+          mma_f16_ts(tmem + kColO + 128 * x, tmem + kColP + 32 * x + 8 * ks,
+                     op_desc(vtaddr + ks * 256, 128, (kTcKeys / 8) * 128), id_o, jt > 0 || ks > 0);
+        mma_commit(bar(kBarO + x));
+      };
+      // Issue whatever is ready, in order per query tile: S_x(t) once tile t
+      // is published and query tile x has read S_x(t - 1); P V_x(t) once it
+      // has written P_x(t); a slot's "empty" once both P V products of its
+      // tile are issued.  Counts of the completions seen on each barrier
+      // give the parities to test.
+      const int nxs[2] = {n_a, n_kt};
+      int n_full = 0, s_next[2] = {0, 0}, pv_next[2] = {0, 0}, sread[2] = {0, 0}, pwritten[2] = {0, 0};
+      int empty_next = 0, idle = 0;
+      bool qready[2] = {false, false};
+      while (empty_next < n_kt) {
+        bool progress = false;
+        if (n_full < n_kt && bar_test(bar(kBarFull + n_full % kSlots), (uint32_t)((n_full / kSlots) & 1))) {
+          ++n_full;
+          progress = true;
+        }
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          if (!qready[x] && bar_test(bar(kBarQ + x), 0)) qready[x] = progress = true;
+          if (sread[x] < s_next[x] && bar_test(bar(kBarSfree + x), (uint32_t)(sread[x] & 1))) {
+            ++sread[x];
+            progress = true;
+          }
+          if (pwritten[x] < s_next[x] && bar_test(bar(kBarPfull + x), (uint32_t)(pwritten[x] & 1))) {
+            ++pwritten[x];
+            progress = true;
+          }
+          const int ts = s_next[x];
+          if (ts < nxs[x] && ts < n_full && qready[x] && sread[x] >= ts) {
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            mma_s(x, ts);
+            ++s_next[x];
+            progress = true;
+          }
+          const int tp = pv_next[x];
+          if (tp < nxs[x] && pwritten[x] > tp) {
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            mma_pv(x, tp);
+            ++pv_next[x];
+            progress = true;
+          }
+        }
+        if (pv_next[1] > empty_next && (empty_next >= n_a || pv_next[0] > empty_next)) {
+          mma_commit(bar(kBarEmpty + empty_next % kSlots));  // every product of that tile issued
+          ++empty_next;
+          progress = true;
+        }
+        if (progress) {
+          idle = 0;
+        } else if (++idle >= kTcWaitLimit || ((idle & 63) == 0 && *abort)) {
+          give_up(s, abort);
+          break;
+        }
+      }
+      // every product issued here complete before the tensor memory goes back
+      mma_commit(bar(kBarDone));
+      bar_wait(bar(kBarDone), 0, nullptr);
+    }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ query tile
     const int x = role, nb = kNbQuery + x;
@@ -383,43 +479,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t col_s = kColS + 64 * x, col_o = kColO + 128 * x, col_p = kColP + 32 * x;
     uint8_t* sq = tc_smem + kOffQ + x * (kTcQ * kHeadDim * 2);
     const uint32_t bar_s = bar(kBarS + x), bar_o = bar(kBarO + x);
-    const int bar_empty = x == 0 ? kBarEmptyA : kBarEmptyB;
-    const uint32_t id_s = instr_desc(kTcQ, kTcKeys, true);
-    const uint32_t id_o = instr_desc(kTcQ, kHeadDim, false);
-    const bool issuer = wt == 0;
-    int s_issued = 0, s_seen = 0, o_issued = 0, o_seen = 0;  // commits issued / completions waited
-
-    // S(jt) = Q K(jt)^T once the producer has filled the slot (issuing thread)
-    auto issue_s = [&](int jt) -> bool {
-      if (!bar_wait(bar(kBarFull + jt % kSlots), (uint32_t)((jt / kSlots) & 1), abort)) return false;
-      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t kaddr = saddr(tc_smem + kOffK + (jt % kSlots) * kTileBytes);
-#pragma unroll
-      for (int ks = 0; ks < kHeadDim / 16; ++ks)
-        mma_f16(tmem + col_s, op_desc(saddr(sq) + ks * 256, 128, (kHeadDim / 8) * 128),
-                op_desc_sw128(kaddr + (ks >> 2) * (kTileBytes / 2) + (ks & 3) * 32), id_s, ks > 0);
-      mma_commit(bar_s);
-      ++s_issued;
-      return true;
-    };
 
     copy_operand(sq, q + qrow0 * kHeadDim, q0, kTcQ, n, wt, kWg);
     asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     bool ok = wg_and(nb, true);
-    if (issuer && !issue_s(0)) {
-      give_up(s, abort);
-      ok = false;
-    }
-    __syncwarp();
+    if (wt == 0) bar_arrive(bar(kBarQ + x));
 
     float m = kNegBig, l = 0.0f;
     for (int j = 0; j < nx; ++j) {
       const int k0 = j * kTcKeys;
-      // S(j) complete: read this row
-      if (bar_wait(bar_s, (uint32_t)(j & 1), abort)) {
-        ++s_seen;
-      } else {
+      // S(j) complete: read this row; then S(j + 1) may overwrite it
+      if (!bar_wait(bar_s, (uint32_t)(j & 1), abort)) {
         give_up(s, abort);
         ok = false;
       }
@@ -427,30 +498,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float xv[kTcKeys];
 #pragma unroll
       for (int c0 = 0; c0 < kTcKeys; c0 += 16) ld16(trow + col_s + c0, *reinterpret_cast<float(*)[16]>(&xv[c0]));
-      // P V(j - 1) complete (it queued behind S(j)): O may be rescaled and P
-      // overwritten, and that tile's slot goes back to the producer before
-      // this warpgroup asks for the next tile
-      if (j > 0) {
-        if (bar_wait(bar_o, (uint32_t)((j - 1) & 1), abort)) {
-          ++o_seen;
-        } else {
-          give_up(s, abort);
-          ok = false;
-        }
-      }
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       if (!wg_and(nb, ok)) {
         ok = false;
         break;
       }
-      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      if (issuer && j > 0) bar_arrive(bar(bar_empty + (j - 1) % kSlots));
-      // every row of S(j) is in registers: S(j + 1) may overwrite it
-      if (issuer && j + 1 < nx && !issue_s(j + 1)) {
-        give_up(s, abort);
-        ok = false;
-      }
-      __syncwarp();
+      if (wt == 0) bar_arrive(bar(kBarSfree + x));
       if (k0 + kTcKeys - 1 > q0 || k0 + kTcKeys > n) {
 #pragma unroll
         for (int i = 0; i < kTcKeys; ++i) {
@@ -468,6 +521,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         l *= alpha;
         m = mx;
       }
+      // P V(j - 1) complete: O may be rescaled and P overwritten
+      if (j > 0 && !bar_wait(bar_o, (uint32_t)((j - 1) & 1), abort)) {
+        give_up(s, abort);
+        ok = false;
+      }
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       // TMEM loads and stores are warp-collective: the warp rescales when
       // any of its rows must, the others by 1
       if (j > 0 && __any_sync(0xffffffffu, grow)) {
@@ -501,29 +560,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ok = false;
         break;
       }
-      if (issuer) {
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t vtaddr = saddr(tc_smem + kOffVt + (j % kSlots) * kTileBytes);
-#pragma unroll
-        for (int ks = 0; ks < kTcKeys / 16; ++ks)
-          mma_f16_ts(tmem + col_o, tmem + col_p + 8 * ks, op_desc(vtaddr + ks * 256, 128, (kTcKeys / 8) * 128), id_o,
-                     j > 0 || ks > 0);
-        mma_commit(bar_o);
-        ++o_issued;
-      }
-      __syncwarp();
+      if (wt == 0) bar_arrive(bar(kBarPfull + x));
     }
     if (ok) {
-      // P V(last) complete; its slot goes back too (the producer may still
-      // wait for it when this tile sees fewer keys than the other)
-      if (bar_wait(bar_o, (uint32_t)((nx - 1) & 1), abort)) {
-        ++o_seen;
-      } else {
+      // P V(last) complete
+      if (!bar_wait(bar_o, (uint32_t)((nx - 1) & 1), abort)) {
         give_up(s, abort);
         ok = false;
       }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      if (issuer && ok) bar_arrive(bar(bar_empty + (nx - 1) % kSlots));
       ok = wg_and(nb, ok);
     }
     if (ok) {
@@ -548,11 +593,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       if (row_ok) *reinterpret_cast<float2*>(stats + (qrow0 + qi) * 2) = make_float2(m, l);
-    } else if (issuer) {
-      // gave up: a last bounded wait for this tile's products in flight
-      // before the tensor memory goes back
-      for (; s_seen < s_issued; ++s_seen) bar_wait(bar_s, (uint32_t)(s_seen & 1), nullptr);
-      for (; o_seen < o_issued; ++o_seen) bar_wait(bar_o, (uint32_t)(o_seen & 1), nullptr);
     }
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
