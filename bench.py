@@ -665,9 +665,13 @@ def prefill_report(args, name: str):
     ws = raw[(-raw.data_ptr()) % 256:][:nbytes]
     stream = torch.cuda.Stream(device=dev)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    tr0, tr1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    tr0.record()
+    tr1.record()  # creates the underlying CUDA events
+    c.set_trace_events(tr0, tr1)  # around the attention kernel inside the call
 
     def run(scores):
-        ms = []
+        ms, ms_kernel = [], []
         for i in range(max(1, args.warmup) + args.steps):
             c.reset(stream=stream)
             with torch.cuda.stream(stream):
@@ -677,10 +681,12 @@ def prefill_report(args, name: str):
             ev1.synchronize()
             if i >= max(1, args.warmup):
                 ms.append(ev0.elapsed_time(ev1))
-        return float(np.median(ms))
+                ms_kernel.append(tr0.elapsed_time(tr1))
+        return float(np.median(ms)), float(np.median(ms_kernel))
 
-    ms_all = run(True)
-    ms_attn = run(False)
+    ms_all, _ = run(True)
+    ms_attn, ms_fwd = run(False)
+    c.set_trace_events(None, None)
     st = c.read_status()
     if st:
         raise RuntimeError(f"device status {st:#x}")
@@ -698,9 +704,12 @@ def prefill_report(args, name: str):
             "ms_with_scores": ms_all, "ms_without_scores": ms_attn,
             "attention_tflops": attn_flop / (ms_attn * 1e-3) / 1e12,
             "attention_frac_of_bf16_peak": attn_flop / (ms_attn * 1e-3) / 1e12 / peak,
+            "forward_kernel_ms": ms_fwd, "forward_kernel_tflops": attn_flop / (ms_fwd * 1e-3) / 1e12,
+            "forward_kernel_frac_of_bf16_peak": attn_flop / (ms_fwd * 1e-3) / 1e12 / peak,
             "scores_tflops": score_flop / ((ms_all - ms_attn) * 1e-3) / 1e12 if ms_all > ms_attn else None,
             "prompt_tokens_per_s": B * n / (ms_all * 1e-3), "peak_bf16_tflops": peak, "steps_timed": args.steps,
-            "note": "times include the append of the prompt (quantisation into the pool)"}
+            "note": "ms_* and attention_tflops include the append of the prompt (quantisation into the "
+                    "pool); forward_kernel_* is the attention kernel alone (CUDA events around it inside the call)"}
     print(json.dumps(line), flush=True)
 
 

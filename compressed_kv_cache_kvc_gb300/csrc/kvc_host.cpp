@@ -891,7 +891,10 @@ kvc_status kvc_prefill_attention(kvc_cache* c, int32_t seq_begin, int32_t batch,
   if (kvc::launch_prefill(c->dev, seq_begin, batch, n, static_cast<const uint16_t*>(d_q),
                           static_cast<const uint16_t*>(d_k), static_cast<const uint16_t*>(d_v),
                           static_cast<uint16_t*>(d_out), static_cast<float*>(d_workspace),
-                          sm_scale * 1.4426950408889634f, h2o, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+                          sm_scale * 1.4426950408889634f, h2o, static_cast<cudaStream_t>(stream),
+                          static_cast<cudaEvent_t>(c->trace_start && c->trace_stop ? c->trace_start : nullptr),
+                          static_cast<cudaEvent_t>(c->trace_start && c->trace_stop ? c->trace_stop : nullptr)) !=
+      cudaSuccess)
     return KVC_ERR_CUDA;
   c->last_launches += 1 + (h2o ? 1 : 0);
   return KVC_OK;

@@ -216,9 +216,12 @@ int prefill_scores_smem_bytes() { return (int)sizeof(PfScoreSmem); }
 
 cudaError_t launch_prefill(const DevState& s, int seq_begin, int batch, int n, const uint16_t* q, const uint16_t* k,
                            const uint16_t* v, uint16_t* out, float* stats, float qk_scale_log2, bool scores,
-                           cudaStream_t st) {
+                           cudaStream_t st, cudaEvent_t trace_start, cudaEvent_t trace_stop) {
   static int done_sc[64] = {0};
-  cudaError_t e = launch_prefill_fwd_tc(s, batch, n, q, k, v, out, stats, qk_scale_log2, st);
+  cudaError_t e = trace_start ? cudaEventRecord(trace_start, st) : cudaSuccess;
+  if (e != cudaSuccess) return e;
+  e = launch_prefill_fwd_tc(s, batch, n, q, k, v, out, stats, qk_scale_log2, st);
+  if (e == cudaSuccess && trace_stop) e = cudaEventRecord(trace_stop, st);
   if (e != cudaSuccess || !scores) return e;
   const int tiles = (n + kPfTile - 1) / kPfTile;
   e = opt_in_smem(reinterpret_cast<const void*>(prefill_scores_kernel), prefill_scores_smem_bytes(), done_sc);

@@ -470,8 +470,9 @@ kvc_status kvc_read_status(kvc_cache* cache, int32_t* h_status, void* stream);
 /* Tracing: when both are non-NULL, the next kvc_decode_attention calls record
  * `ev_start` (a cudaEvent_t) just before the split-K attention kernel and
  * `ev_stop` just after it, on the call's stream (kvc_decode_step and
- * kvc_prefill_context likewise, around each split launch).  NULL, NULL
- * turns it off. */
+ * kvc_prefill_context likewise, around each split launch;
+ * kvc_prefill_attention around its attention kernel, outside any stream
+ * capture).  NULL, NULL turns it off. */
 kvc_status kvc_set_trace_events(kvc_cache* cache, void* ev_start, void* ev_stop);
 
 /* Number of kernels the last call on this handle enqueued. */
