@@ -5,7 +5,7 @@
 // scores come from prefill_scores_kernel (kvc_prefill.cu), which uses these
 // statistics.
 //
-// One 416-thread CTA per (256-query block, query head, sequence), longest
+// One 448-thread CTA per (256-query block, query head, sequence), longest
 // blocks first, warps with fixed roles:
 //   * warpgroups 0 and 1 ("A" and "B") each own one 128-query tile; thread t
 //     of a warpgroup owns query row t of its tile, TMEM lane t.  TMEM columns:
@@ -19,11 +19,12 @@
 //     it by ldmatrix.trans into a dims x keys operand in fp16 (K-major, no
 //     swizzle, 8-row x 16-byte core matrices).  A slot is refilled once both
 //     query tiles' P V products have read it;
-//   * warp 12 issues every tensor-core product from one thread: for each
-//     key tile j, S_A(j + 1) and S_B(j + 1) = Q K(j + 1)^T (M 128, N 64,
-//     bf16: exact products) as soon as the query tiles have read S(j), then
-//     O_A += P_A V(j) and O_B += P_B V(j) (M 128, N 128, K 64, fp16, P read
-//     from tensor memory as the A operand) as soon as they have written P.
+//   * warps 12 and 13 issue the tensor-core products of query tiles A and B,
+//     one thread each (one thread issues a product about every 100 cycles,
+//     two threads together nearly twice as many): S(j + 1) = Q K(j + 1)^T
+//     (M 128, N 64, bf16: exact products) as soon as the query tile has read
+//     S(j), O += P V(j) (M 128, N 128, K 64, fp16, P read from tensor memory
+//     as the A operand) as soon as it has written P(j).
 // Per key tile j a query warpgroup waits for S(j), reads its S row
 // (tcgen05.ld), masks (only tiles that cross the diagonal or the end of the
 // prompt), runs the online softmax in the log2 domain with a lazy maximum (O
@@ -55,7 +56,7 @@ namespace {
 using namespace dev;
 
 constexpr int kWg = 128;                  // threads per warpgroup
-constexpr int kTcThreads = 3 * kWg + 32;  // query tiles A and B, producer, MMA warp
+constexpr int kTcThreads = 3 * kWg + 64;  // query tiles A and B, producer, two MMA warps
 constexpr int kTcQ = 128;                 // queries per tile (the MMAs' M)
 constexpr int kTcBlock = 2 * kTcQ;        // queries per CTA
 constexpr int kTcKeys = 64;               // keys per tile
@@ -73,12 +74,12 @@ constexpr int kOffK = kOffQ + 2 * kTcQ * kHeadDim * 2;        // 3 x 16 KB: K ri
 constexpr int kOffVt = kOffK + kSlots * kTileBytes;           // 3 x 16 KB: V^T ring, fp16 (operand layout)
 constexpr int kOffVs = kOffVt + kSlots * kTileBytes;          // 2 x 16 KB: V staging (producer, TMA, 1 KB aligned)
 constexpr int kOffBar = kOffVs + 2 * kTileBytes;              // mbarriers, TMEM base, abort flag
-// mbarriers: tile published / slot read (per slot), S and P V complete, S
-// read, P written, Q loaded (per query tile), TMA bytes landed (per staging
-// tile), the issuing thread's products all complete
-constexpr int kBarFull = 0, kBarEmpty = kSlots, kBarS = 2 * kSlots, kBarO = kBarS + 2, kBarSfree = kBarO + 2,
-              kBarPfull = kBarSfree + 2, kBarQ = kBarPfull + 2, kBarTma = kBarQ + 2, kBarDone = kBarTma + 2,
-              kNumBars = kBarDone + 1;
+// mbarriers: tile published, slot read by query tile A / B (per slot); S
+// and P V complete, S read, P written, Q loaded (per query tile); TMA bytes
+// landed (per staging tile); each issuing thread's products all complete
+constexpr int kBarFull = 0, kBarEmptyA = kSlots, kBarEmptyB = 2 * kSlots, kBarS = 3 * kSlots, kBarO = kBarS + 2,
+              kBarSfree = kBarO + 2, kBarPfull = kBarSfree + 2, kBarQ = kBarPfull + 2, kBarTma = kBarQ + 2,
+              kBarDone = kBarTma + 2, kNumBars = kBarDone + 2;
 static_assert(kOffK % 1024 == 0 && kOffVs % 1024 == 0, "the 128-byte swizzle wants 1 KB aligned boxes");
 constexpr int kTcSmem = kOffBar + 8 * kNumBars + 16;
 
@@ -367,13 +368,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       if (!wg_and(kNbProducer, !*abort)) break;
       if (wt == 0) bar_arrive(bar(kBarFull + j % kSlots));
-      // the slot of tile j + 1 held tile j + 1 - kSlots: free once the last
-      // P V product of that tile completed
+      // the slot of tile j + 1 held tile j + 1 - kSlots: free once tile B's
+      // P V product of that tile completed (and A's, if A saw that tile)
       if (j + 1 < n_kt) {
         const int jp = j + 1 - kSlots;
-        if (jp >= 0 && !bar_wait(bar(kBarEmpty + jp % kSlots), (uint32_t)((jp / kSlots) & 1), abort)) {
-          give_up(s, abort);
-          ok = false;
+        if (jp >= 0) {
+          const uint32_t par = (uint32_t)((jp / kSlots) & 1);
+          if (!bar_wait(bar(kBarEmptyB + jp % kSlots), par, abort) ||
+              (jp < n_a && !bar_wait(bar(kBarEmptyA + jp % kSlots), par, abort))) {
+            give_up(s, abort);
+            ok = false;
+          }
         }
         if (!wg_and(kNbProducer, ok)) break;
         if (wt == 0) load(j + 1);
@@ -389,13 +394,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if ((vmb & 0x7FFFu) >= kF16Max || ((vmb >> 16) & 0x7FFFu) >= kF16Max)
       atomicOr(&s.counters[kCtrStatus], kDevPrefillRange);
   } else if (role == 3) {
-    // ------------------------------------------------------------ MMA issuer
+    // ----------------------------------------------------------- MMA issuers
+    const int x = warp - 12;  // the query tile this warp's thread issues for
     if (lane == 0) {
       const uint32_t id_s = instr_desc(kTcQ, kTcKeys, true);
       const uint32_t id_o = instr_desc(kTcQ, kHeadDim, false);
-      // S_x(jt) = Q_x K(jt)^T
-      auto mma_s = [&](int x, int jt) {
-        const uint32_t qaddr = saddr(tc_smem + kOffQ + x * (kTcQ * kHeadDim * 2));
+      const uint32_t qaddr = saddr(tc_smem + kOffQ + x * (kTcQ * kHeadDim * 2));
+      const int nx = x == 0 ? n_a : n_kt;
+      const int bar_empty = x == 0 ? kBarEmptyA : kBarEmptyB;
+      // S(jt) = Q K(jt)^T
+      auto mma_s = [&](int jt) {
         const uint32_t kaddr = saddr(tc_smem + kOffK + (jt % kSlots) * kTileBytes);
 #pragma unroll
         for (int ks = 0; ks < kHeadDim / 16; ++ks)
@@ -403,8 +411,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                   op_desc_sw128(kaddr + (ks >> 2) * (kTileBytes / 2) + (ks & 3) * 32), id_s, ks > 0);
         mma_commit(bar(kBarS + x));
       };
-      // O_x += P_x V(jt)
-      auto mma_pv = [&](int x, int jt) {
+      // O += P V(jt)
+      auto mma_pv = [&](int jt) {
         const uint32_t vtaddr = saddr(tc_smem + kOffVt + (jt % kSlots) * kTileBytes);
 #pragma unroll
         for (int ks = 0; ks < kTcKeys / 16; ++ks)
@@ -412,50 +420,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                      op_desc(vtaddr + ks * 256, 128, (kTcKeys / 8) * 128), id_o, jt > 0 || ks > 0);
         mma_commit(bar(kBarO + x));
       };
-      // Issue whatever is ready, in order per query tile: S_x(t) once tile t
-      // is published and query tile x has read S_x(t - 1); P V_x(t) once it
-      // has written P_x(t); a slot's "empty" once both P V products of its
-      // tile are issued.  Counts of the completions seen on each barrier
-      // give the parities to test.
-      const int nxs[2] = {n_a, n_kt};
-      int n_full = 0, s_next[2] = {0, 0}, pv_next[2] = {0, 0}, sread[2] = {0, 0}, pwritten[2] = {0, 0};
-      int empty_next = 0, idle = 0;
-      bool qready[2] = {false, false};
-      while (empty_next < n_kt) {
+      // Issue whatever is ready, in order: S(t) once tile t is published and
+      // the query tile has read S(t - 1); P V(t) once it has written P(t),
+      // then that slot's "empty" (only for slots the producer refills).
+      // Counts of the completions seen on each barrier give the parities.
+      int n_full = 0, s_next = 0, pv_next = 0, sread = 0, pwritten = 0, idle = 0;
+      bool qready = false;
+      while (pv_next < nx) {
         bool progress = false;
-        if (n_full < n_kt && bar_test(bar(kBarFull + n_full % kSlots), (uint32_t)((n_full / kSlots) & 1))) {
+        if (n_full < nx && bar_test(bar(kBarFull + n_full % kSlots), (uint32_t)((n_full / kSlots) & 1))) {
           ++n_full;
           progress = true;
         }
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          if (!qready[x] && bar_test(bar(kBarQ + x), 0)) qready[x] = progress = true;
-          if (sread[x] < s_next[x] && bar_test(bar(kBarSfree + x), (uint32_t)(sread[x] & 1))) {
-            ++sread[x];
-            progress = true;
-          }
-          if (pwritten[x] < s_next[x] && bar_test(bar(kBarPfull + x), (uint32_t)(pwritten[x] & 1))) {
-            ++pwritten[x];
-            progress = true;
-          }
-          const int ts = s_next[x];
-          if (ts < nxs[x] && ts < n_full && qready[x] && sread[x] >= ts) {
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            mma_s(x, ts);
-            ++s_next[x];
-            progress = true;
-          }
-          const int tp = pv_next[x];
-          if (tp < nxs[x] && pwritten[x] > tp) {
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            mma_pv(x, tp);
-            ++pv_next[x];
-            progress = true;
-          }
+        if (!qready && bar_test(bar(kBarQ + x), 0)) qready = progress = true;
+        if (sread < s_next && bar_test(bar(kBarSfree + x), (uint32_t)(sread & 1))) {
+          ++sread;
+          progress = true;
         }
-        if (pv_next[1] > empty_next && (empty_next >= n_a || pv_next[0] > empty_next)) {
-          mma_commit(bar(kBarEmpty + empty_next % kSlots));  // every product of that tile issued
-          ++empty_next;
+        if (pwritten < s_next && bar_test(bar(kBarPfull + x), (uint32_t)(pwritten & 1))) {
+          ++pwritten;
+          progress = true;
+        }
+        if (s_next < nx && s_next < n_full && qready && sread >= s_next) {
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          mma_s(s_next);
+          ++s_next;
+          progress = true;
+        }
+        if (pwritten > pv_next) {
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          mma_pv(pv_next);
+          if (pv_next + kSlots < n_kt) mma_commit(bar(bar_empty + pv_next % kSlots));
+          ++pv_next;
           progress = true;
         }
         if (progress) {
@@ -466,8 +462,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       // every product issued here complete before the tensor memory goes back
-      mma_commit(bar(kBarDone));
-      bar_wait(bar(kBarDone), 0, nullptr);
+      mma_commit(bar(kBarDone + x));
+      bar_wait(bar(kBarDone + x), 0, nullptr);
     }
     __syncwarp();
   } else {
