@@ -172,6 +172,8 @@ cudaError_t launch_prefill_fwd_tc(const DevState& s, int batch, int n, const uin
                                   const uint16_t* v, uint16_t* out, float* stats, float qk_scale_log2,
                                   cudaStream_t st);
 int prefill_fwd_tc_smem_bytes();
+cudaError_t launch_prefill_scores_tc(const DevState& s, int seq_begin, int batch, int n, const uint16_t* q,
+                                    const uint16_t* k, const float* stats, float qk_scale_log2, cudaStream_t st);
 cudaError_t launch_prefill(const DevState& s, int seq_begin, int batch, int n, const uint16_t* q, const uint16_t* k,
                            const uint16_t* v, uint16_t* out, float* stats, float qk_scale_log2, bool scores,
                            cudaStream_t st, cudaEvent_t trace_start = nullptr,

@@ -596,6 +596,211 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcCols));
 }
 
+// ---------------------------------------------------------------------------
+// Prompt H2O scores on the tensor cores: every prompt key's score is the sum,
+// over the later queries of the query heads of its KV head, of its
+// probability exp2(s log2e / sqrt(d) - m_q) / l_q, with the forward kernel's
+// row statistics (m_q, l_q).
+//
+// One 320-thread CTA per (128-key tile, KV head, sequence), two per SM, keys
+// on the TMEM lanes: S^T (128 keys x 128 queries) = K Q^T by tcgen05.mma (M
+// 128, N 128, bf16: exact products; K from shared memory once, by TMA, with
+// the 128-byte swizzle; the query tile by TMA into a ring of two slots), so
+// thread t of a warpgroup owns key t's row and adds its probabilities in a
+// register.  Roles: warpgroups 0 and 1 take alternate query blocks (TMEM
+// columns [0, 128) and [128, 256)); warp 8 loads the query tiles and stages
+// b_q = m_q + log2(l_q) per query (+inf past the prompt, so those read as
+// zero); warp 9 issues the products from one thread.  Query blocks are (query
+// head g of the group, 128-query tile qt >= the key tile); only the diagonal
+// block needs the causal mask.  The two warpgroups' sums meet in shared
+// memory and go straight into the sink, pool or window score slot of each
+// key (one CTA owns a key tile, so no atomics).
+constexpr int kScThreads = 2 * kWg + 64;
+constexpr int kScTile = 128;                                  // keys per CTA, queries per block
+constexpr int kScTileBytes = kScTile * kHeadDim * 2;          // 32 KB
+constexpr int kScOffK = 0;                                    // 32 KB: K (TMA, 128-byte swizzle)
+constexpr int kScOffQ = kScOffK + kScTileBytes;               // 2 x 32 KB: query tiles
+constexpr int kScOffB = kScOffQ + 2 * kScTileBytes;           // 2 x 512 B: b_q per slot
+constexpr int kScOffRed = kScOffB + 2 * kScTile * 4;          // 512 B: warpgroup 0's sums
+constexpr int kScOffBar = kScOffRed + kScTile * 4;
+constexpr int kScBarK = 0, kScBarFull = 1, kScBarEmpty = 3, kScBarS = 5, kScBarSfree = 7, kScBarDone = 9,
+              kScNumBars = 10;
+constexpr int kScSmem = kScOffBar + 8 * kScNumBars + 16;
+constexpr uint32_t kScCols = 256;
+
+__global__ void __launch_bounds__(kScThreads, 2)
+    prefill_scores_tc_kernel(DevState s, int n, const __grid_constant__ CUtensorMap tm_q,
+                             const __grid_constant__ CUtensorMap tm_k, const float* __restrict__ stats,
+                             float qk_scale_log2, int seq_begin) {
+  extern __shared__ __align__(1024) uint8_t sc_smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sc_smem + kScOffBar);
+  uint32_t* tbase = reinterpret_cast<uint32_t*>(sc_smem + kScOffBar + 8 * kScNumBars);
+  volatile int* abort = reinterpret_cast<volatile int*>(sc_smem + kScOffBar + 8 * kScNumBars + 4);
+  auto bar = [&](int i) { return saddr(bars + i); };
+
+  const int kt = blockIdx.x, h = blockIdx.y, bl = blockIdx.z;  // key tile 0 sees the most queries
+  const int b = seq_begin + bl, G = s.group;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int k0 = kt * kScTile;
+  const int n_qt = (n + kScTile - 1) / kScTile;
+  const int per_head = n_qt - kt, iters = G * per_head;  // blocks (g, qt >= kt)
+
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tbase)),
+                 "r"(kScCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (tid == 0) {
+    for (int i = 0; i < kScNumBars; ++i) {
+      const uint32_t cnt = (i == kScBarFull || i == kScBarFull + 1 || i == kScBarEmpty || i == kScBarEmpty + 1) ? 2 : 1;
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar(i)), "r"(cnt));
+    }
+    *abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tbase;
+  float score = 0.0f;  // this thread's key, over this warpgroup's blocks
+
+  if (warp == 8) {
+    // ------------------------------------------------- query tiles and b_q
+    float* sb = reinterpret_cast<float*>(sc_smem + kScOffB);
+    if (lane == 0) {
+      bar_expect_tx(bar(kScBarK), kScTileBytes);
+      const uint32_t kdst = saddr(sc_smem + kScOffK);
+      tma_load_3d(kdst, &tm_k, 0, k0, bl * s.hkv + h, bar(kScBarK));
+      tma_load_3d(kdst + kScTileBytes / 2, &tm_k, 64, k0, bl * s.hkv + h, bar(kScBarK));
+    }
+    for (int it = 0; it < iters; ++it) {
+      const int x = it & 1, g = it / per_head, qt = kt + it % per_head;
+      bool ok = true;
+      // the slot's previous block read (its product complete, b_q used)
+      if (lane == 0 && it >= 2 && !bar_wait(bar(kScBarEmpty + x), (uint32_t)(((it - 2) >> 1) & 1), abort)) {
+        give_up(s, abort);
+        ok = false;
+      }
+      if (!__all_sync(0xffffffffu, ok)) break;
+      if (lane == 0) {
+        bar_expect_tx(bar(kScBarFull + x), kScTileBytes);
+        const uint32_t qdst = saddr(sc_smem + kScOffQ + x * kScTileBytes);
+        const int plane = bl * s.hq + h * G + g;
+        tma_load_3d(qdst, &tm_q, 0, qt * kScTile, plane, bar(kScBarFull + x));
+        tma_load_3d(qdst + kScTileBytes / 2, &tm_q, 64, qt * kScTile, plane, bar(kScBarFull + x));
+      }
+      const size_t srow = ((size_t)bl * s.hq + h * G + g) * n + (size_t)qt * kScTile;
+#pragma unroll
+      for (int e = 0; e < kScTile / 32; ++e) {
+        const int i = lane + 32 * e;
+        float bq = INFINITY;
+        if (qt * kScTile + i < n) {
+          const float2 st = *reinterpret_cast<const float2*>(stats + (srow + i) * 2);
+          bq = st.x + log2f(st.y);
+        }
+        sb[x * kScTile + i] = bq;
+      }
+      __syncwarp();
+      if (lane == 0) bar_arrive(bar(kScBarFull + x));
+    }
+  } else if (warp == 9) {
+    // --------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t id_s = instr_desc(kScTile, kScTile, true);
+      const uint32_t kaddr = saddr(sc_smem + kScOffK);
+      bool ok = bar_wait(bar(kScBarK), 0, abort);
+      if (!ok) give_up(s, abort);
+      for (int it = 0; ok && it < iters; ++it) {
+        const int x = it & 1;
+        if (!bar_wait(bar(kScBarFull + x), (uint32_t)((it >> 1) & 1), abort) ||
+            (it >= 2 && !bar_wait(bar(kScBarSfree + x), (uint32_t)(((it - 2) >> 1) & 1), abort))) {
+          give_up(s, abort);
+          break;
+        }
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t qaddr = saddr(sc_smem + kScOffQ + x * kScTileBytes);
+#pragma unroll
+        for (int ks = 0; ks < kHeadDim / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * (kScTileBytes / 2) + (ks & 3) * 32;
+          mma_f16(tmem + 128 * x, op_desc_sw128(kaddr + off), op_desc_sw128(qaddr + off), id_s, ks > 0);
+        }
+        mma_commit(bar(kScBarS + x));
+        mma_commit(bar(kScBarEmpty + x));
+      }
+      // every product issued here complete before the tensor memory goes back
+      mma_commit(bar(kScBarDone));
+      bar_wait(bar(kScBarDone), 0, nullptr);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ sums over the queries
+    const int x = tid / kWg, t = tid % kWg;  // warpgroup x takes blocks x, x + 2, ...
+    const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16) + 128 * x;
+    const float* sb = reinterpret_cast<const float*>(sc_smem + kScOffB) + x * kScTile;
+    bool ok = true;
+    for (int it = x; it < iters; it += 2) {
+      const int qt = kt + it % per_head;
+      if (!bar_wait(bar(kScBarS + x), (uint32_t)((it >> 1) & 1), abort) ||
+          !bar_wait(bar(kScBarFull + x), (uint32_t)((it >> 1) & 1), abort)) {
+        give_up(s, abort);
+        ok = false;
+      }
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const bool diag = qt == kt;  // queries below this key only on the diagonal block
+      float acc = 0.0f;
+#pragma unroll 1
+      for (int c0 = 0; c0 < kScTile; c0 += 16) {
+        float v[16];
+        ld16(trow + c0, v);
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) {
+          const float4 b4 = *reinterpret_cast<const float4*>(sb + c0 + i);
+          const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float p = fast_exp2(fmaf(v[i + e], qk_scale_log2, -bb[e]));
+            acc += (diag && c0 + i + e < t) ? 0.0f : p;
+          }
+        }
+      }
+      score += acc;
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      if (!wg_and(kNbQuery + x, ok)) break;
+      if (t == 0) {
+        bar_arrive(bar(kScBarSfree + x));
+        bar_arrive(bar(kScBarEmpty + x));
+      }
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  // warpgroup 0's sums meet warpgroup 1's; warpgroup 1 writes the scores
+  float* red = reinterpret_cast<float*>(sc_smem + kScOffRed);
+  if (tid < kWg) red[tid] = score;
+  __syncthreads();
+  if (tid >= kWg && tid < 2 * kWg && !*abort) {
+    const int t = tid - kWg, p = k0 + t;
+    if (p < n) {
+      const float v = score + red[t];
+      int lo, hi;
+      pool_range(0, n, s.ring, &lo, &hi);
+      if (p < kSinks) {
+        s.sink_score[((size_t)b * s.hkv + h) * kSinks + p] = v;
+      } else if (p < hi) {
+        const int slot = p - lo;
+        const int blk = s.block_table[(size_t)b * s.max_bps + slot / kPage];
+        if ((unsigned)blk < (unsigned)s.num_blocks)
+          s.score[((size_t)blk * s.hkv + h) * kPage + slot % kPage] = v;
+        else
+          atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
+      } else {
+        s.ring_score[((size_t)b * s.hkv + h) * s.ring + (p - kSinks) % s.ring] = v;
+      }
+    }
+  }
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kScCols));
+}
+
 }  // namespace
 
 int prefill_fwd_tc_smem_bytes() { return kTcSmem; }
@@ -619,14 +824,14 @@ EncodeTiledFn tensor_map_encoder() {
   return fn;
 }
 
-// A [planes][n][128] bf16 tensor as a 3-d tensor map with 64 x 64 x 1 boxes
-// and the 128-byte swizzle; rows past n read as zeros.
-bool encode_kv_map(CUtensorMap* map, const uint16_t* base, int n, int planes) {
+// A [planes][n][128] bf16 tensor as a 3-d tensor map with 64 x `rows` x 1
+// boxes (64 dims) and the 128-byte swizzle; rows past n read as zeros.
+bool encode_kv_map(CUtensorMap* map, const uint16_t* base, int n, int planes, int rows) {
   const EncodeTiledFn enc = tensor_map_encoder();
   if (!enc) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)n, (cuuint64_t)planes};
   const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)n * kHeadDim * 2};
-  const cuuint32_t box[3] = {64, (cuuint32_t)kTcKeys, 1};
+  const cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -635,6 +840,20 @@ bool encode_kv_map(CUtensorMap* map, const uint16_t* base, int n, int planes) {
 
 }  // namespace
 
+cudaError_t launch_prefill_scores_tc(const DevState& s, int seq_begin, int batch, int n, const uint16_t* q,
+                                    const uint16_t* k, const float* stats, float qk_scale_log2, cudaStream_t st) {
+  static int done[64] = {0};
+  const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(prefill_scores_tc_kernel), kScSmem, done);
+  if (e != cudaSuccess) return e;
+  CUtensorMap tm_q, tm_k;
+  if (!encode_kv_map(&tm_q, q, n, batch * s.hq, kScTile) || !encode_kv_map(&tm_k, k, n, batch * s.hkv, kScTile))
+    return cudaErrorInvalidValue;
+  const int tiles = (n + kScTile - 1) / kScTile;
+  prefill_scores_tc_kernel<<<dim3(tiles, s.hkv, batch), kScThreads, kScSmem, st>>>(s, n, tm_q, tm_k, stats,
+                                                                                    qk_scale_log2, seq_begin);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_prefill_fwd_tc(const DevState& s, int batch, int n, const uint16_t* q, const uint16_t* k,
                                   const uint16_t* v, uint16_t* out, float* stats, float qk_scale_log2,
                                   cudaStream_t st) {
@@ -642,7 +861,7 @@ cudaError_t launch_prefill_fwd_tc(const DevState& s, int batch, int n, const uin
   const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(prefill_fwd_tc_kernel), kTcSmem, done);
   if (e != cudaSuccess) return e;
   CUtensorMap tm_k, tm_v;
-  if (!encode_kv_map(&tm_k, k, n, batch * s.hkv) || !encode_kv_map(&tm_v, v, n, batch * s.hkv))
+  if (!encode_kv_map(&tm_k, k, n, batch * s.hkv, kTcKeys) || !encode_kv_map(&tm_v, v, n, batch * s.hkv, kTcKeys))
     return cudaErrorInvalidValue;
   const int blocks = (n + kTcBlock - 1) / kTcBlock;
   prefill_fwd_tc_kernel<<<dim3(blocks, s.hq, batch), kTcThreads, kTcSmem, st>>>(s, n, q, tm_k, tm_v, out, stats,
