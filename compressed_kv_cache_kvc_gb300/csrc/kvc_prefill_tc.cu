@@ -288,7 +288,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   volatile int* abort = reinterpret_cast<volatile int*>(tc_smem + kOffBar + 8 * kNumBars + 4);
   auto bar = [&](int i) { return saddr(bars + i); };
 
-  // the longest (last) query blocks first
+  // blocks launch x fastest: a (query head, sequence)'s query blocks run
+  // together, longest first, and share its K and V in L2 (ordering every
+  // head's longest block first instead spread the working set past L2 and
+  // was slower)
   const int qb = gridDim.x - 1 - blockIdx.x, hqi = blockIdx.y, bl = blockIdx.z;
   const int hkvi = hqi / s.group;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
