@@ -11,8 +11,9 @@
 //     of a warpgroup owns query row t of its tile, TMEM lane t.  TMEM columns:
 //     S_A [0, 64), S_B [64, 128), O_A [128, 256), O_B [256, 384), P_A
 //     [384, 416), P_B [416, 448) (P in fp16, two per column);
-//   * warpgroup 2 (the producer) brings 64-key tiles into a ring of three
-//     slots by TMA (one thread issues the tensor copies, an mbarrier counts
+//   * warpgroup 2 (the producer) brings both query tiles in by TMA (two
+//     64-dim x 128-row boxes each, 128-byte swizzle; the S product reads them
+//     in place) and 64-key tiles into a ring of three slots by TMA (one thread issues the tensor copies, an mbarrier counts
 //     their bytes; rows past the prompt read as zeros): K and V each as two
 //     64 x 64 boxes with the 128-byte swizzle; K is read in place by the MMA
 //     (K-major, 128-byte swizzle), V is staged and the warpgroup transposes
@@ -36,9 +37,10 @@
 // that see few keys.  V entries beyond fp16's range (|v| >= 65536, or not
 // finite) saturate to +-65504 and set KVC_DEV_PREFILL_RANGE.
 //
-// Synchronisation: mbarriers (Q loaded, S read and P written by the query
-// warpgroups, slot full from the producer, slot empty and S / P V complete
-// through tcgen05.commit) and named barriers inside a warpgroup.  Every
+// Synchronisation: mbarriers (Q and K/V tiles landed, counted in bytes; S
+// read and P written by the query warpgroups; slot full from the producer;
+// slot empty and S / P V complete through tcgen05.commit) and named barriers
+// inside a warpgroup.  Every
 // mbarrier wait is bounded and also ends when another thread has given up;
 // a wait that runs out sets KVC_DEV_WAIT_TIMEOUT, every role leaves its loop,
 // the issuing thread waits (bounded) for its products in flight, and the
@@ -69,7 +71,7 @@ constexpr uint32_t kColP = 384;           // P of query tile x at kColP + 32 x
 constexpr int kTcWaitLimit = 1 << 22;
 
 constexpr int kTileBytes = kTcKeys * kHeadDim * 2;           // 16 KB
-constexpr int kOffQ = 0;                                      // 2 x 32 KB: Q_A, Q_B (operand layout)
+constexpr int kOffQ = 0;                                      // 2 x 32 KB: Q_A, Q_B (TMA, 128-byte swizzle)
 constexpr int kOffK = kOffQ + 2 * kTcQ * kHeadDim * 2;        // 3 x 16 KB: K ring (TMA, 128-byte swizzle)
 constexpr int kOffVt = kOffK + kSlots * kTileBytes;           // 3 x 16 KB: V^T ring, fp16 (operand layout)
 constexpr int kOffVs = kOffVt + kSlots * kTileBytes;          // 2 x 16 KB: V staging (producer, TMA, 1 KB aligned)
@@ -253,35 +255,15 @@ __device__ __forceinline__ void st16(uint32_t taddr, const float (&v)[16]) {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void cp16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-
-// Rows [row0, row0 + rows) of a [n][128] bf16 matrix at `src` into the
-// operand layout at `dst` (rows past n zero) by `nthr` threads; 8
-// consecutive threads fill one core matrix (8 rows of one 16-byte chunk: 128
-// contiguous bytes).
-__device__ __forceinline__ void copy_operand(uint8_t* dst, const uint16_t* src, int row0, int rows, int n, int t,
-                                             int nthr) {
-  for (int i = t; i < rows * (kHeadDim / 8); i += nthr) {
-    const int rr = (i & 7) | ((i >> 7) << 3), c = (i >> 3) & 15;
-    uint8_t* d = dst + core_off(rr, c, kHeadDim / 8);
-    if (row0 + rr < n)
-      cp16(saddr(d), src + (size_t)(row0 + rr) * kHeadDim + 8 * c);
-    else
-      *reinterpret_cast<uint4*>(d) = make_uint4(0u, 0u, 0u, 0u);
-  }
-}
-
 // Key tiles a 128-query tile starting at q0 attends to.
 __device__ __forceinline__ int key_tiles(int q0, int n) {
   return min((q0 + kTcQ - 1) / kTcKeys + 1, (n + kTcKeys - 1) / kTcKeys);
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
-    prefill_fwd_tc_kernel(DevState s, int n, const uint16_t* __restrict__ q, const __grid_constant__ CUtensorMap tm_k,
-                          const __grid_constant__ CUtensorMap tm_v, uint16_t* __restrict__ out,
-                          float* __restrict__ stats, float qk_scale_log2) {
+    prefill_fwd_tc_kernel(DevState s, int n, const __grid_constant__ CUtensorMap tm_q,
+                          const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                          uint16_t* __restrict__ out, float* __restrict__ stats, float qk_scale_log2) {
   extern __shared__ __align__(1024) uint8_t tc_smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(tc_smem + kOffBar);
   uint32_t* tbase = reinterpret_cast<uint32_t*>(tc_smem + kOffBar + 8 * kNumBars);
@@ -334,7 +316,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tma_load_3d(vdst, &tm_v, 0, jt * kTcKeys, zkv, tb);
       tma_load_3d(vdst + kTileBytes / 2, &tm_v, 64, jt * kTcKeys, zkv, tb);
     };
-    if (wt == 0) load(0);
+    if (wt == 0) {
+      // both query tiles first (128-row boxes; rows past n read as zeros)
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const uint32_t qb_bar = bar(kBarQ + x), qdst = saddr(tc_smem + kOffQ + x * (kTcQ * kHeadDim * 2));
+        bar_expect_tx(qb_bar, kTcQ * kHeadDim * 2);
+        tma_load_3d(qdst, &tm_q, 0, qblk + x * kTcQ, bl * s.hq + hqi, qb_bar);
+        tma_load_3d(qdst + kTcQ * 128, &tm_q, 64, qblk + x * kTcQ, bl * s.hq + hqi, qb_bar);
+      }
+      load(0);
+    }
     issued = 1;
     for (int j = 0; j < n_kt; ++j) {
       // tile j's copies complete
@@ -410,7 +402,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t kaddr = saddr(tc_smem + kOffK + (jt % kSlots) * kTileBytes);
 #pragma unroll
         for (int ks = 0; ks < kHeadDim / 16; ++ks)
-          mma_f16(tmem + kColS + 64 * x, op_desc(qaddr + ks * 256, 128, (kHeadDim / 8) * 128),
+          mma_f16(tmem + kColS + 64 * x, op_desc_sw128(qaddr + (ks >> 2) * (kTcQ * 128) + (ks & 3) * 32),
                   op_desc_sw128(kaddr + (ks >> 2) * (kTileBytes / 2) + (ks & 3) * 32), id_s, ks > 0);
         mma_commit(bar(kBarS + x));
       };
@@ -476,14 +468,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int qi = q0 + wt;  // this thread's query row
     const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // this warp's lanes
     const uint32_t col_s = kColS + 64 * x, col_o = kColO + 128 * x, col_p = kColP + 32 * x;
-    uint8_t* sq = tc_smem + kOffQ + x * (kTcQ * kHeadDim * 2);
     const uint32_t bar_s = bar(kBarS + x), bar_o = bar(kBarO + x);
-
-    copy_operand(sq, q + qrow0 * kHeadDim, q0, kTcQ, n, wt, kWg);
-    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    bool ok = wg_and(nb, true);
-    if (wt == 0) bar_arrive(bar(kBarQ + x));
+    bool ok = true;
 
     float m = kNegBig, l = 0.0f;
     for (int j = 0; j < nx; ++j) {
@@ -863,11 +849,12 @@ cudaError_t launch_prefill_fwd_tc(const DevState& s, int batch, int n, const uin
   static int done[64] = {0};
   const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(prefill_fwd_tc_kernel), kTcSmem, done);
   if (e != cudaSuccess) return e;
-  CUtensorMap tm_k, tm_v;
-  if (!encode_kv_map(&tm_k, k, n, batch * s.hkv, kTcKeys) || !encode_kv_map(&tm_v, v, n, batch * s.hkv, kTcKeys))
+  CUtensorMap tm_q, tm_k, tm_v;
+  if (!encode_kv_map(&tm_q, q, n, batch * s.hq, kTcQ) || !encode_kv_map(&tm_k, k, n, batch * s.hkv, kTcKeys) ||
+      !encode_kv_map(&tm_v, v, n, batch * s.hkv, kTcKeys))
     return cudaErrorInvalidValue;
   const int blocks = (n + kTcBlock - 1) / kTcBlock;
-  prefill_fwd_tc_kernel<<<dim3(blocks, s.hq, batch), kTcThreads, kTcSmem, st>>>(s, n, q, tm_k, tm_v, out, stats,
+  prefill_fwd_tc_kernel<<<dim3(blocks, s.hq, batch), kTcThreads, kTcSmem, st>>>(s, n, tm_q, tm_k, tm_v, out, stats,
                                                                                 qk_scale_log2);
   return cudaGetLastError();
 }
