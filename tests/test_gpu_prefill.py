@@ -36,6 +36,11 @@ CASES = [
     (4, 16, 4, 2, 150, 50),    # with a bf16 window: the last 50 tokens in the ring
     (8, 64, 8, 1, 130, 0),     # the largest query group (G = 8)
     (4, 8, 1, 2, 1, 0),        # a one-token prompt, one KV head
+    # long prompts: dozens of key tiles per query block, the K/V ring wrapping
+    # many times, blocks of every length, the lazy maximum over many tiles
+    (4, 10, 2, 1, 4100, 0),    # GQA 5, a ragged last block and tile
+    (8, 4, 4, 1, 4096, 0),     # G = 1, whole blocks
+    (8, 8, 2, 1, 2050, 300),   # with a bf16 window
 ]
 
 
