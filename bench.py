@@ -188,6 +188,35 @@ def run_oracle_child(n_seq: int, reps: int):
     return json.loads(p.stdout.strip().splitlines()[-1])
 
 
+def oracle_prefill_sample(n: int) -> tuple[float, str]:
+    """The oracle's prefill attention (fp64 causal attention and column sums)
+    of one query head over its KV head at prompt length n, timed; seeded
+    inputs of the workload's distribution."""
+    import numpy as np
+
+    from oracle import kvc_oracle as O
+    rng = np.random.default_rng(77)
+    q = rng.standard_normal((1, n, 128)).astype(np.float32)
+    k = rng.standard_normal((1, n, 128)).astype(np.float32)
+    v = rng.standard_normal((1, n, 128)).astype(np.float32)
+    t0 = time.perf_counter()
+    O.prefill_attention(q, k, v)
+    return time.perf_counter() - t0, f"oracle prefill_attention of one query head at prompt length {n}, 1 thread"
+
+
+def run_oracle_prefill_child(n: int) -> tuple[float, str]:
+    """oracle_prefill_sample in a fresh single-threaded process."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"
+    p = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-prefill-child", str(n)],
+                       capture_output=True, text=True, env=env, timeout=1800)
+    if p.returncode != 0:
+        raise RuntimeError(p.stderr[-2000:])
+    r = json.loads(p.stdout.strip().splitlines()[-1])
+    return r["seconds"], r["desc"]
+
+
 def _oracle_proc(n_seq: int, reps: int, layer: int, barrier, queue):
     span = []
     secs, nbytes, desc = oracle_sample(n_seq, reps, layer, barrier, span)
@@ -699,6 +728,12 @@ def prefill_report(args, name: str):
     except (OSError, ValueError):
         pass
     peak = float(peaks.get("bf16_tflops", 1900.0))
+    cpu = None
+    if not args.no_cpu_baseline:
+        secs, desc = run_oracle_prefill_child(n)
+        head_flop = 4.0 * 128 * pairs  # one query head's attention
+        cpu = {"value": head_flop / secs / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+               "sample": desc}
     line = {"workload": name, "prefill": True, "batch": B, "n": n, "q_heads": Hq, "kv_heads": Hkv,
             "bits": w.bits, "bf16_window": args.bf16_window,
             "ms_with_scores": ms_all, "ms_without_scores": ms_attn,
@@ -708,6 +743,7 @@ def prefill_report(args, name: str):
             "forward_kernel_frac_of_bf16_peak": attn_flop / (ms_fwd * 1e-3) / 1e12 / peak,
             "scores_tflops": score_flop / ((ms_all - ms_attn) * 1e-3) / 1e12 if ms_all > ms_attn else None,
             "prompt_tokens_per_s": B * n / (ms_all * 1e-3), "peak_bf16_tflops": peak, "steps_timed": args.steps,
+            "cpu_baseline": cpu,
             "note": "ms_* and attention_tflops include the append of the prompt (quantisation into the "
                     "pool); forward_kernel_* is the attention kernel alone (CUDA events around it inside the call)"}
     print(json.dumps(line), flush=True)
@@ -1059,7 +1095,12 @@ def main():
     ap.add_argument("--split", default="replicas", choices=["replicas", "batch"],
                     help="N > 1: independent replicas (weak scaling) or the batch divided over the GPUs (strong)")
     ap.add_argument("--oracle-child", nargs=2, type=int, default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-prefill-child", type=int, default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_prefill_child is not None:
+        secs, desc = oracle_prefill_sample(args.oracle_prefill_child)
+        print(json.dumps({"seconds": secs, "desc": desc}))
+        return
     if args.oracle_child is not None:
         secs, nbytes, desc = oracle_sample(args.oracle_child[0], args.oracle_child[1])
         print(json.dumps({"seconds": secs, "bytes": nbytes, "desc": desc}))
