@@ -234,6 +234,21 @@ __device__ __forceinline__ void ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void st16u(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
@@ -735,24 +750,41 @@ __global__ void __launch_bounds__(kScThreads, 2)
         ok = false;
       }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const bool diag = qt == kt;  // queries below this key only on the diagonal block
-      float acc = 0.0f;
+      // four partial sums (independent add chains); queries below this key
+      // only on the diagonal block, which alone takes the masked loop
+      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      if (qt != kt) {
 #pragma unroll 1
-      for (int c0 = 0; c0 < kScTile; c0 += 16) {
-        float v[16];
-        ld16(trow + c0, v);
+        for (int c0 = 0; c0 < kScTile; c0 += 32) {
+          float v[32];
+          ld32(trow + c0, v);
 #pragma unroll
-        for (int i = 0; i < 16; i += 4) {
-          const float4 b4 = *reinterpret_cast<const float4*>(sb + c0 + i);
-          const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
+          for (int i = 0; i < 32; i += 4) {
+            const float4 b4 = *reinterpret_cast<const float4*>(sb + c0 + i);
+            acc[0] += fast_exp2(fmaf(v[i], qk_scale_log2, -b4.x));
+            acc[1] += fast_exp2(fmaf(v[i + 1], qk_scale_log2, -b4.y));
+            acc[2] += fast_exp2(fmaf(v[i + 2], qk_scale_log2, -b4.z));
+            acc[3] += fast_exp2(fmaf(v[i + 3], qk_scale_log2, -b4.w));
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c0 = 0; c0 < kScTile; c0 += 32) {
+          float v[32];
+          ld32(trow + c0, v);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float p = fast_exp2(fmaf(v[i + e], qk_scale_log2, -bb[e]));
-            acc += (diag && c0 + i + e < t) ? 0.0f : p;
+          for (int i = 0; i < 32; i += 4) {
+            const float4 b4 = *reinterpret_cast<const float4*>(sb + c0 + i);
+            const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float p = fast_exp2(fmaf(v[i + e], qk_scale_log2, -bb[e]));
+              acc[e] += c0 + i + e < t ? 0.0f : p;
+            }
           }
         }
       }
-      score += acc;
+      score += (acc[0] + acc[1]) + (acc[2] + acc[3]);
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       if (!wg_and(kNbQuery + x, ok)) break;
       if (t == 0) {
