@@ -511,9 +511,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (!(ki <= qi && ki < n)) xv[i] = -INFINITY;
         }
       }
-      float mx = -INFINITY;
+      // four independent chains of maxima
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int i = 0; i < kTcKeys; ++i) mx = fmaxf(mx, xv[i]);
+      for (int i = 0; i < kTcKeys; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], xv[i]);
+      float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       mx *= qk_scale_log2;  // scale > 0: the maximum commutes with it
       const bool grow = mx > m + kTcLazy;
       const float alpha = grow ? fast_exp2(m - mx) : 1.0f;
@@ -542,6 +544,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // P in fp16 into tensor memory, keys 2c and 2c + 1 in column c (the
       // sum adds the unrounded p, as the decode kernels do)
       const float nm = -m;
+      float lp[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // four independent chains of sums
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t pw[16];
@@ -549,12 +552,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int e = 0; e < 16; ++e) {
           const float p0 = fast_exp2(fmaf(xv[32 * h + 2 * e], qk_scale_log2, nm));
           const float p1 = fast_exp2(fmaf(xv[32 * h + 2 * e + 1], qk_scale_log2, nm));
-          l += p0 + p1;
+          lp[(2 * e) & 3] += p0;
+          lp[(2 * e + 1) & 3] += p1;
           const __half2 hh = __floats2half2_rn(p0, p1);
           pw[e] = *reinterpret_cast<const uint32_t*>(&hh);
         }
         st16u(trow + col_p + 16 * h, pw);
       }
+      l += (lp[0] + lp[1]) + (lp[2] + lp[3]);
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       if (!wg_and(nb, ok)) {
         ok = false;
