@@ -1,8 +1,8 @@
-// Prefill forward on the fifth-generation tensor cores: the causal attention
-// of a fresh prompt over itself (Technical Report section 1.1), with S = Q K^T
-// and O = P V by tcgen05.mma (fp32 accumulators in tensor memory).  Outputs
-// and row statistics (m, l) as the decode kernels define them; the H2O
-// scores come from prefill_scores_kernel (kvc_prefill.cu), which uses these
+// Prefill on the fifth-generation tensor cores.  The forward: the causal
+// attention of a fresh prompt over itself (Technical Report section 1.1), with
+// S = Q K^T and O = P V by tcgen05.mma (fp32 accumulators in tensor memory),
+// the outputs and row statistics (m, l) as the decode kernels define them.
+// The H2O scores: prefill_scores_tc_kernel further down, from those
 // statistics.
 //
 // One 448-thread CTA per (256-query block, query head, sequence), longest
@@ -13,9 +13,10 @@
 //     [384, 416), P_B [416, 448) (P in fp16, two per column);
 //   * warpgroup 2 (the producer) brings both query tiles in by TMA (two
 //     64-dim x 128-row boxes each, 128-byte swizzle; the S product reads them
-//     in place) and 64-key tiles into a ring of three slots by TMA (one thread issues the tensor copies, an mbarrier counts
-//     their bytes; rows past the prompt read as zeros): K and V each as two
-//     64 x 64 boxes with the 128-byte swizzle; K is read in place by the MMA
+//     in place) and 64-key tiles into a ring of three slots by TMA (one
+//     thread issues the tensor copies, an mbarrier counts their bytes; rows
+//     past the prompt read as zeros): K and V each as two 64 x 64 boxes
+//     with the 128-byte swizzle; K is read in place by the MMA
 //     (K-major, 128-byte swizzle), V is staged and the warpgroup transposes
 //     it by ldmatrix.trans into a dims x keys operand in fp16 (K-major, no
 //     swizzle, 8-row x 16-byte core matrices).  A slot is refilled once both
@@ -40,8 +41,8 @@
 // Synchronisation: mbarriers (Q and K/V tiles landed, counted in bytes; S
 // read and P written by the query warpgroups; slot full from the producer;
 // slot empty and S / P V complete through tcgen05.commit) and named barriers
-// inside a warpgroup.  Every
-// mbarrier wait is bounded and also ends when another thread has given up;
+// inside a warpgroup.  Every mbarrier wait is bounded and also ends when
+// another thread has given up;
 // a wait that runs out sets KVC_DEV_WAIT_TIMEOUT, every role leaves its loop,
 // the issuing thread waits (bounded) for its products in flight, and the
 // CTA frees its tensor memory.
