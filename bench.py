@@ -188,6 +188,59 @@ def run_oracle_child(n_seq: int, reps: int):
     return json.loads(p.stdout.strip().splitlines()[-1])
 
 
+def oracle_workload_sample(name: str, evict: str, retention: float, bf16_window: int, codes: str,
+                           reps: int) -> tuple[float, int, str]:
+    """The oracle's first decode step after the prompt (append, fp64
+    attention with H2O scores, selection, eviction) of one sequence x every
+    KV head of layer 0 of workload `name`, in the report's eviction mode,
+    bf16 window and codes; timed over `reps` repetitions from the same state.
+    Returns (seconds, KV bytes the attention reads, description)."""
+    import copy
+
+    from compressed_kv_cache_kvc_gb300 import workloads as W
+    from oracle import kvc_oracle as O
+    w = W.WORKLOADS[name]
+    d = W.gen_layer(w, 0, batch=1)
+    f = O.bf16_bits_to_f32
+    n = int(d["lengths"][0])
+    base = O.OracleCache(1, w.num_q_heads, w.num_kv_heads, w.bits, bf16_window=bf16_window, codes=codes)
+    base.append(0, f(d["k"][0][:, :n]), f(d["v"][0][:, :n]))
+    if evict == "block":
+        kw = dict(mode="block", recent=w.recent, retention=retention)
+    else:
+        kw = dict(mode=w.mode, budget=w.budget, recent=w.recent, window=w.window)
+    total = 0.0
+    for _ in range(reps):
+        c = copy.deepcopy(base)
+        t0 = time.perf_counter()
+        c.append(0, f(d["k_new"][0]), f(d["v_new"][0]))
+        c.attend(0, f(d["q"][0]))
+        c.evict(0, c.keep_masks(0, **kw))
+        total += time.perf_counter() - t0
+    per_slot = 2 * (128 * w.bits // 8) + 2 * 4
+    ring = min(bf16_window, max(0, n + 1 - 4))
+    pool = n + 1 - 4 - ring
+    nbytes = (pool * per_slot + (ring + 4) * 2 * 128 * 2) * w.num_kv_heads * reps
+    desc = (f"oracle decode step (append, fp64 attention + H2O, select, evict; {kw['mode']}) of 1 sequence x "
+            f"{w.num_kv_heads} KV heads at context {n}, {reps} rep(s), 1 thread")
+    return total, nbytes, desc
+
+
+def run_oracle_workload_child(name: str, evict: str, retention: float, bf16_window: int, codes: str,
+                              reps: int) -> tuple[float, int, str]:
+    """oracle_workload_sample in a fresh single-threaded process."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"
+    spec = json.dumps([name, evict, retention, bf16_window, codes, reps])
+    p = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-workload-child", spec],
+                       capture_output=True, text=True, env=env, timeout=1800)
+    if p.returncode != 0:
+        raise RuntimeError(p.stderr[-2000:])
+    r = json.loads(p.stdout.strip().splitlines()[-1])
+    return r["seconds"], r["bytes"], r["desc"]
+
+
 def oracle_prefill_sample(n: int) -> tuple[float, str]:
     """The oracle's prefill attention (fp64 causal attention and column sums)
     of one query head over its KV head at prompt length n, timed; seeded
@@ -1063,6 +1116,12 @@ def workload_report(args, name: str):
             st = c.read_status()
             if st:
                 raise RuntimeError(f"device status {st:#x}")
+    if not args.no_cpu_baseline:
+        # the oracle beside it: the same first step on one sequence of layer 0
+        secs, nbytes, desc = run_oracle_workload_child(name, args.evict, args.retention, args.bf16_window,
+                                                       args.codes, 3)
+        line["cpu_baseline"] = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "sample": desc}
     print(json.dumps(line), flush=True)
 
 
@@ -1096,7 +1155,12 @@ def main():
                     help="N > 1: independent replicas (weak scaling) or the batch divided over the GPUs (strong)")
     ap.add_argument("--oracle-child", nargs=2, type=int, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--oracle-prefill-child", type=int, default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-workload-child", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_workload_child is not None:
+        secs, nbytes, desc = oracle_workload_sample(*json.loads(args.oracle_workload_child))
+        print(json.dumps({"seconds": secs, "bytes": nbytes, "desc": desc}))
+        return
     if args.oracle_prefill_child is not None:
         secs, desc = oracle_prefill_sample(args.oracle_prefill_child)
         print(json.dumps({"seconds": secs, "desc": desc}))
