@@ -241,6 +241,32 @@ def run_oracle_workload_child(name: str, evict: str, retention: float, bf16_wind
     return r["seconds"], r["bytes"], r["desc"]
 
 
+def oracle_context_sample(name: str, n1: int, bf16_window: int, codes: str) -> tuple[float, float, str]:
+    """The oracle's prompt over context (prefill_chunk: append the prompt,
+    each prompt query attends to the held tokens in their stored form, H2O
+    scores) of one sequence of workload `name` at its full context, timed
+    (the context's own appends untimed).  Returns (seconds, flops, desc)."""
+    import numpy as np
+
+    from compressed_kv_cache_kvc_gb300 import workloads as W
+    from oracle import kvc_oracle as O
+    w = W.WORKLOADS[name]
+    rng = np.random.default_rng(78)
+    ctx, hq, hkv = w.context, w.num_q_heads, w.num_kv_heads
+    c = O.OracleCache(1, hq, hkv, w.bits, bf16_window=bf16_window, codes=codes)
+    c.append(0, rng.standard_normal((hkv, ctx, 128)).astype(np.float32),
+             rng.standard_normal((hkv, ctx, 128)).astype(np.float32))
+    q = rng.standard_normal((hq, n1, 128)).astype(np.float32)
+    k = rng.standard_normal((hkv, n1, 128)).astype(np.float32)
+    v = rng.standard_normal((hkv, n1, 128)).astype(np.float32)
+    t0 = time.perf_counter()
+    c.prefill_chunk(0, q, k, v)
+    secs = time.perf_counter() - t0
+    flops = 4.0 * 128 * sum(ctx + i + 1 for i in range(n1)) * hq
+    return secs, flops, (f"oracle prefill_chunk of a {n1}-token prompt over {ctx} tokens of context, one sequence x "
+                         f"{hkv} KV heads, 1 thread")
+
+
 def oracle_prefill_sample(n: int) -> tuple[float, str]:
     """The oracle's prefill attention (fp64 causal attention and column sums)
     of one query head over its KV head at prompt length n, timed; seeded
@@ -876,6 +902,18 @@ def prefill_context_report(args, name: str):
             "launches_per_call": launches, "steps_timed": args.steps,
             "note": "append + two passes of the multi-query attention (row statistics; outputs and column sums); "
                     "the time includes the append"}
+    if not args.no_cpu_baseline:
+        env = dict(os.environ)
+        for k_ in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            env[k_] = "1"
+        spec = json.dumps([name, n1, args.bf16_window, args.codes])
+        p = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-context-child", spec],
+                           capture_output=True, text=True, env=env, timeout=1800)
+        if p.returncode != 0:
+            raise RuntimeError(p.stderr[-2000:])
+        r = json.loads(p.stdout.strip().splitlines()[-1])
+        line["cpu_baseline"] = {"value": r["flops"] / r["seconds"] / 1e12, "unit": "TFLOP/s", "cores": 1,
+                                "kind": "oracle", "sample": r["desc"]}
     print(json.dumps(line), flush=True)
 
 
@@ -1156,7 +1194,12 @@ def main():
     ap.add_argument("--oracle-child", nargs=2, type=int, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--oracle-prefill-child", type=int, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--oracle-workload-child", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-context-child", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_context_child is not None:
+        secs, flops, desc = oracle_context_sample(*json.loads(args.oracle_context_child))
+        print(json.dumps({"seconds": secs, "flops": flops, "desc": desc}))
+        return
     if args.oracle_workload_child is not None:
         secs, nbytes, desc = oracle_workload_sample(*json.loads(args.oracle_workload_child))
         print(json.dumps({"seconds": secs, "bytes": nbytes, "desc": desc}))
