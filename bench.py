@@ -795,6 +795,23 @@ def prefill_report(args, name: str):
     ms_all, _ = run(True)
     ms_attn, ms_fwd = run(False)
     c.set_trace_events(None, None)
+    # the append alone (the first part of every call above): bf16 K and V in,
+    # codes, scales, positions and zeroed scores out
+    ms_app = []
+    for i in range(max(1, args.warmup) + args.steps):
+        c.reset(stream=stream)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            c.quantize_append(k, v, stream=stream)
+            ev1.record(stream)
+        ev1.synchronize()
+        if i >= max(1, args.warmup):
+            ms_app.append(ev0.elapsed_time(ev1))
+    ms_app = float(np.median(ms_app))
+    n_pool = max(n - args.bf16_window - 4, 0)  # quantised tokens; the rest are sinks or in the bf16 window
+    app_bytes = (2 * B * Hkv * n * 256  # bf16 K and V rows in
+                 + 2 * B * Hkv * n_pool * (128 * w.bits // 8 + 4) + B * Hkv * n_pool * 8  # codes, scales, pos, score
+                 + 2 * B * Hkv * (n - n_pool) * 256 + B * Hkv * (n - n_pool) * 4)  # bf16 rows, score
     st = c.read_status()
     if st:
         raise RuntimeError(f"device status {st:#x}")
@@ -807,6 +824,7 @@ def prefill_report(args, name: str):
     except (OSError, ValueError):
         pass
     peak = float(peaks.get("bf16_tflops", 1900.0))
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
     cpu = None
     if not args.no_cpu_baseline:
         secs, desc = run_oracle_prefill_child(n)
@@ -821,6 +839,8 @@ def prefill_report(args, name: str):
             "forward_kernel_ms": ms_fwd, "forward_kernel_tflops": attn_flop / (ms_fwd * 1e-3) / 1e12,
             "forward_kernel_frac_of_bf16_peak": attn_flop / (ms_fwd * 1e-3) / 1e12 / peak,
             "scores_tflops": score_flop / ((ms_all - ms_attn) * 1e-3) / 1e12 if ms_all > ms_attn else None,
+            "append_ms": ms_app, "append_gbs": app_bytes / (ms_app * 1e-3) / 1e9,
+            "append_frac_of_hbm_peak": app_bytes / (ms_app * 1e-3) / 1e9 / hbm, "peak_hbm_gbs": hbm,
             "prompt_tokens_per_s": B * n / (ms_all * 1e-3), "peak_bf16_tflops": peak, "steps_timed": args.steps,
             "cpu_baseline": cpu,
             "note": "ms_* and attention_tflops include the append of the prompt (quantisation into the "

@@ -15,6 +15,7 @@
 // KV head), slot (position - 4) mod W, and enters the pool, quantised from
 // the ring, only when a later append pushes it out of the window.
 #include "kvc_internal.h"
+#include "kvc_mma.h"
 
 namespace kvc {
 namespace {
@@ -194,7 +195,10 @@ __global__ void __launch_bounds__(512) append_kernel(DevState s, int seq_begin, 
 // scratch (slots -1 when it failed); append_rows_kernel then spreads the
 // rows over (token chunk, sequence) CTAs.  Only for appends that push no
 // window token into the pool, so no row reads what another CTA writes.
-constexpr int kBulkTokens = 64;  // tokens per CTA of append_rows_kernel
+constexpr int kBulkTokens = 32;  // tokens per CTA of append_rows_kernel
+constexpr int kBulkWarps = 16;
+constexpr int kBulkStages = 6;  // units a warp keeps in flight (1 KB each)
+constexpr int kBulkSmem = kBulkWarps * kBulkStages * 1024;
 
 __global__ void append_alloc_kernel(DevState s, int seq_begin, int batch, int n_new) {
   const int bl = blockIdx.x * blockDim.x + threadIdx.x;
@@ -231,44 +235,224 @@ __global__ void append_alloc_kernel(DevState s, int seq_begin, int batch, int n_
   s.plan[2 * b + 1] = pos;
 }
 
+// Integer codes of 8 values of a row, as words whose low byte is the
+// two's-complement 8-bit code and whose low nibble is the 4-bit one
+// (0x4B400000 + code: the fp32 bit pattern of 1.5 * 2^23 + code).
+//
+// code = round-half-even(x / scale) with x / scale the IEEE fp32 quotient,
+// clamped, as in quantize_row.  Here the code comes, where that decides it,
+// from the exact product P = x * inv, inv an approximate reciprocal of the
+// scale (relative error at most 2^-23, one ulp): P differs from the rounded
+// quotient by at most 2^-23 |x / scale| + 2^-24 |x / scale| < 2^-14.4,
+// because |x| <= amax gives |x / scale| <= qmax (1 + 2^-23) < 128 (the scale
+// is a normal number here; a subnormal one has an infinite reciprocal under
+// ftz).  One fused multiply-add rounds P + 1.5 * 2^23 to the integer r
+// nearest P (round to nearest even in the binade of unit spacing); a second
+// gives P - r.  Where |P - r| < 1/2 - 2^-12 the quotient lies in the same
+// unit interval around r and rounds to r, and |r| <= qmax needs no clamp.
+// Elsewhere (P within about 2^-12 of a half-integer, or not finite) the
+// division decides.  About one value in 2^11 takes that path.
+__device__ __forceinline__ float rcp_approx_ftz(float a) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(a));
+  return r;
+}
+
 template <int BITS>
-__global__ void __launch_bounds__(512) append_rows_kernel(DevState s, int seq_begin, int n_new,
-                                                          const uint16_t* __restrict__ kin,
-                                                          const uint16_t* __restrict__ vin) {
+__device__ __forceinline__ void int_codes8(const float* x, float scale, float inv, uint32_t (&w)[8]) {
+  constexpr float kM = 12582912.0f;  // 1.5 * 2^23
+  constexpr float kNear = 0.5f - 0x1p-12f;
+  constexpr int kLo = BITS == 8 ? -127 : -8;
+  constexpr int kHi = BITS == 8 ? 127 : 7;
+  bool slow = false;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float sm = __fmaf_rn(x[e], inv, kM);
+    w[e] = __float_as_uint(sm);
+    slow |= !(fabsf(__fmaf_rn(x[e], inv, -__fadd_rn(sm, -kM))) < kNear);
+  }
+  if (slow) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float r = __fadd_rn(__fmaf_rn(x[e], inv, kM), -kM);
+      if (!(fabsf(__fmaf_rn(x[e], inv, -r)) < kNear)) {
+        const int q = scale > 0.0f ? min(max(__float2int_rn(__fdiv_rn(x[e], scale)), kLo), kHi) : 0;
+        w[e] = 0x4B400000u + (uint32_t)q;
+      }
+    }
+  }
+}
+
+// the low bytes of four words, in order
+__device__ __forceinline__ uint32_t low_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
+}
+
+// Rows spread over (token chunk, sequence) CTAs.  A unit is 4 adjacent
+// tokens of one (KV head, K or V): 4 rows of 128 values, one per quarter of
+// a warp; a lane takes dims 8j .. 8j + 7 and 64 + 8j .. 64 + 8j + 7 of its
+// row, so a unit is one 1 KB run of the input.  Each warp streams its units
+// (u = warp, warp + 16, ...) through a ring of kBulkStages 1 KB stages in
+// shared memory with cp.async: every lane copies its own 32 bytes of a unit
+// and later reads back exactly those, so the ring needs no barrier, only
+// the lane's own wait for its copy group.  Stage layout: the lanes' first
+// 16-byte chunks, then their second ones (conflict-free reads).  The unit
+// indices advance by the warp count without divisions.
+template <int BITS>
+__global__ void __launch_bounds__(kBulkWarps * 32, 2) append_rows_kernel(DevState s, int seq_begin, int n_new,
+                                                                          const uint16_t* __restrict__ kin,
+                                                                          const uint16_t* __restrict__ vin) {
+  using namespace codes;
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ int sh_blk[4];
   const int bl = blockIdx.y;
   const int b = seq_begin + bl;
   const int slots = s.plan[2 * b];
-  if (slots < 0) return;
+  if (slots < 0) return;  // the same for the whole CTA
   const int pos = s.plan[2 * b + 1];
   int lo, hi;
   pool_range(pos, n_new, s.ring, &lo, &hi);
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  const int nwarps = blockDim.x >> 5;
+  const int qr = lane >> 3;  // which token of the unit
+  const int ql = lane & 7;   // which dims of its row
   const int hkv = s.hkv;
   const int W = s.ring;
   const int t0 = blockIdx.x * kBulkTokens;
   const int nt = min(kBulkTokens, n_new - t0);
-  for (int row = warp; row < nt * hkv * 2; row += nwarps) {
-    const int kv = row & 1;
-    const int h = (row >> 1) % hkv;
-    const int i = t0 + (row >> 1) / hkv;
-    const uint16_t* src = (kv ? vin : kin) + (((size_t)bl * hkv + h) * n_new + i) * kHeadDim;
-    const uint2 raw = *reinterpret_cast<const uint2*>(src + lane * 4);
-    const int p = pos + i;
+  const int nquad = (nt + 3) >> 2;
+  const int units = nquad * hkv * 2;  // unit u: token quad u % nquad, (KV head, K or V) u / nquad
+  const int dq = kBulkWarps / nquad, dr = kBulkWarps % nquad;
+  const bool fp8 = BITS == 8 && s.fp8;
+
+  // the block ids of the (at most 3) pool pages this chunk's tokens land in
+  const int pf = max(pos + t0, lo), pl = min(pos + t0 + nt, hi);  // pool positions [pf, pl)
+  const int page0 = pf < pl ? (slots + (pf - lo)) / kPage : 0;
+  if (threadIdx.x < 4) {
+    const int pg = page0 + threadIdx.x;
+    sh_blk[threadIdx.x] = pf < pl && pg <= (slots + (pl - 1 - lo)) / kPage ? s.block_table[(size_t)b * s.max_bps + pg] : -1;
+  }
+  __syncthreads();
+
+  const uint32_t ring_s = smem_u32(ring) + warp * (kBulkStages * 1024) + 16 * lane;
+  // issue cursor: unit warp + ki * 16 is (iquad, ihk), into stage istage
+  int iquad = warp % nquad, ihk = warp / nquad, istage = 0;
+  auto issue = [&](int ki) {
+    const int tok = t0 + 4 * iquad + qr;
+    const bool ok = warp + ki * kBulkWarps < units && tok < t0 + nt;
+    const uint16_t* src =
+        ((ihk & 1) ? vin : kin) + (((size_t)bl * hkv + (ihk >> 1)) * n_new + (ok ? tok : 0)) * kHeadDim + 8 * ql;
+    const uint32_t dst = ring_s + istage * 1024;
+    cp_async16_if(ok, dst, src);
+    cp_async16_if(ok, dst + 512, src + 64);
+    cp_async_commit();
+    istage = istage == kBulkStages - 1 ? 0 : istage + 1;
+    iquad += dr;
+    ihk += dq;
+    if (iquad >= nquad) {
+      iquad -= nquad;
+      ++ihk;
+    }
+  };
+#pragma unroll 1
+  for (int ki = 0; ki < kBulkStages - 1; ++ki) issue(ki);
+
+  int quad = warp % nquad, hk = warp / nquad, stage = 0;  // processing cursor
+#pragma unroll 1
+  for (int k = 0; warp + k * kBulkWarps < units; ++k) {
+    cp_async_wait<kBulkStages - 2>();  // this lane's copies of unit k have landed
+    issue(k + kBulkStages - 1);        // into the stage unit k - 1 was read from
+    const uint32_t st = ring_s + stage * 1024;
+    uint4 r0, r1;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(r0.x), "=r"(r0.y), "=r"(r0.z), "=r"(r0.w) : "r"(st));
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r1.x), "=r"(r1.y), "=r"(r1.z), "=r"(r1.w)
+                 : "r"(st + 512));
+    const int tok = t0 + 4 * quad + qr;
+    const int kv = hk & 1;
+    const int h = hk >> 1;
+    stage = stage == kBulkStages - 1 ? 0 : stage + 1;
+    quad += dr;
+    hk += dq;
+    if (quad >= nquad) {
+      quad -= nquad;
+      ++hk;
+    }
+
+    const uint32_t wd[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      x[2 * i] = __uint_as_float(wd[i] << 16);
+      x[2 * i + 1] = __uint_as_float(wd[i] & 0xFFFF0000u);
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (tok >= t0 + nt) continue;  // past the chunk's last token (its lanes read nothing)
+    const int p = pos + tok;
     if (p < kSinks) {
-      uint16_t* dst = (kv ? s.sink_v : s.sink_k) + (((size_t)b * hkv + h) * kSinks + p) * kHeadDim;
-      *reinterpret_cast<uint2*>(dst + lane * 4) = raw;
-      if (kv == 0 && lane == 0) s.sink_score[((size_t)b * hkv + h) * kSinks + p] = 0.0f;
-    } else if (p < hi) {
-      quantize_row<BITS>(s, b, h, kv, slots + (p - lo), p, 0.0f, raw, lane);
-    } else {
+      const size_t si = ((size_t)b * hkv + h) * kSinks + p;
+      uint16_t* dst = (kv ? s.sink_v : s.sink_k) + si * kHeadDim + 8 * ql;
+      *reinterpret_cast<uint4*>(dst) = r0;
+      *reinterpret_cast<uint4*>(dst + 64) = r1;
+      if (kv == 0 && ql == 0) s.sink_score[si] = 0.0f;
+      continue;
+    }
+    if (p >= hi) {
       const size_t ridx = ((size_t)b * hkv + h) * W + (p - kSinks) % W;
-      uint16_t* dst = (kv ? s.ring_v : s.ring_k) + ridx * kHeadDim;
-      *reinterpret_cast<uint2*>(dst + lane * 4) = raw;
-      if (kv == 0 && lane == 0) s.ring_score[ridx] = 0.0f;
+      uint16_t* dst = (kv ? s.ring_v : s.ring_k) + ridx * kHeadDim + 8 * ql;
+      *reinterpret_cast<uint4*>(dst) = r0;
+      *reinterpret_cast<uint4*>(dst + 64) = r1;
+      if (kv == 0 && ql == 0) s.ring_score[ridx] = 0.0f;
+      continue;
+    }
+    const int slot = slots + (p - lo);
+    const int blk = sh_blk[slot / kPage - page0];
+    if ((unsigned)blk >= (unsigned)s.num_blocks) {
+      if (ql == 0) atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
+      continue;
+    }
+    const float scale = __fdiv_rn(amax, fp8 ? 448.0f : (BITS == 8 ? 127.0f : 7.0f));
+    // scale 0 (an all-zero row) gives an infinite reciprocal: every value
+    // then takes the slow path, which gives code 0
+    const float inv = rcp_approx_ftz(scale);
+    const size_t sidx = ((size_t)blk * hkv + h) * kPage + slot % kPage;
+    uint8_t* codes = (kv ? s.v_codes : s.k_codes) + sidx * s.row_bytes;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {  // dims 8 ql.. (hh 0) and 64 + 8 ql.. (hh 1)
+      const float* xh = x + 8 * hh;
+      if (fp8) {
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = scale > 0.0f ? __fdiv_rn(xh[e], scale) : 0.0f;
+        *reinterpret_cast<uint2*>(codes + 64 * hh + 8 * ql) =
+            make_uint2(e4m3x4(y[0], y[1], y[2], y[3]), e4m3x4(y[4], y[5], y[6], y[7]));
+      } else {
+        uint32_t wc[8];
+        int_codes8<BITS>(xh, scale, inv, wc);
+        if (BITS == 8) {
+          *reinterpret_cast<uint2*>(codes + 64 * hh + 8 * ql) =
+              make_uint2(low_bytes(wc[0], wc[1], wc[2], wc[3]), low_bytes(wc[4], wc[5], wc[6], wc[7]));
+        } else {
+          // byte i: the nibble of value 2i low, of value 2i + 1 high
+          const uint32_t ev = low_bytes(wc[0], wc[2], wc[4], wc[6]);
+          const uint32_t od = low_bytes(wc[1], wc[3], wc[5], wc[7]);
+          *reinterpret_cast<uint32_t*>(codes + 32 * hh + 4 * ql) = (ev & 0x0F0F0F0Fu) | ((od & 0x0F0F0F0Fu) << 4);
+        }
+      }
+    }
+    if (ql == 0) {
+      (kv ? s.v_scale : s.k_scale)[sidx] = scale;
+      if (kv == 0) {
+        s.slot_pos[sidx] = p;
+        s.score[sidx] = 0.0f;
+      }
     }
   }
+  cp_async_wait<0>();  // (only empty groups can be pending here)
 }
 
 __global__ void fill_free_stack_kernel(int32_t* stack, int n) {
@@ -282,11 +466,15 @@ cudaError_t launch_append_bulk(const DevState& s, int seq_begin, int batch, int 
   append_alloc_kernel<<<(batch + 127) / 128, 128, 0, st>>>(s, seq_begin, batch, n_new);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  static int done8[64] = {0}, done4[64] = {0};
+  e = s.bits == 8 ? opt_in_smem(reinterpret_cast<const void*>(append_rows_kernel<8>), kBulkSmem, done8)
+                  : opt_in_smem(reinterpret_cast<const void*>(append_rows_kernel<4>), kBulkSmem, done4);
+  if (e != cudaSuccess) return e;
   const dim3 grid((n_new + kBulkTokens - 1) / kBulkTokens, batch);
   if (s.bits == 8)
-    append_rows_kernel<8><<<grid, 512, 0, st>>>(s, seq_begin, n_new, k, v);
+    append_rows_kernel<8><<<grid, kBulkWarps * 32, kBulkSmem, st>>>(s, seq_begin, n_new, k, v);
   else
-    append_rows_kernel<4><<<grid, 512, 0, st>>>(s, seq_begin, n_new, k, v);
+    append_rows_kernel<4><<<grid, kBulkWarps * 32, kBulkSmem, st>>>(s, seq_begin, n_new, k, v);
   return cudaGetLastError();
 }
 

@@ -554,8 +554,8 @@ kvc_status kvc_quantize_append(kvc_cache* c, int32_t seq_begin, int32_t batch, i
   }
   if (need > (long long)c->cfg.num_blocks - used_pages(c)) return KVC_ERR_CAPACITY;
   // long appends that move no window token into the pool: rows spread over
-  // (token chunk, sequence) CTAs
-  bool bulk = n_new >= kvc::kBulkAppendMin;
+  // (token chunk, sequence) CTAs, read with 16-byte loads
+  bool bulk = n_new >= kvc::kBulkAppendMin && aligned(d_k, 16) && aligned(d_v, 16);
   for (int i = 0; i < batch && bulk; ++i) {
     int lo, hi;
     kvc::pool_range(c->pos[seq_begin + i], n_new, c->cfg.bf16_window, &lo, &hi);

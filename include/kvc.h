@@ -237,7 +237,8 @@ size_t kvc_workspace_bytes(const kvc_cache* cache, int32_t batch);
  * amax / 448 and the codes FP8 E4M3 (see "Code formats"); with a bf16 window
  * the newest tokens go to the ring and the tokens they push out of it are
  * quantised into the pool (see "Hybrid precision").  Appends of 64 tokens or
- * more that push no window token out take two launches, others one.
+ * more that push no window token out, from 16-byte aligned d_k and d_v, take
+ * two launches, others one (the same results either way).
  * Errors: KVC_ERR_INVALID_ARG for a slice outside [0, max_batch), n_new < 0
  * or a null or misaligned pointer; KVC_ERR_CAPACITY when a sequence would
  * exceed max_blocks_per_seq pages or the pool has too few free blocks

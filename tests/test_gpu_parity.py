@@ -401,6 +401,112 @@ def test_bulk_append_equals_token_by_token(bits, W):
     assert ca.read_status() == 0 and cb.read_status() == 0
 
 
+def _edge_rows(bits, rng, n_rows):
+    """bf16 bit patterns of 128-value rows at the edges of the rounding:
+    exact half-integer quotients, quotients within 2^-12 of a half-integer
+    (found by enumerating every bf16 value), subnormal and near-overflow
+    scales, zero and negative-zero rows, a lone nonzero value."""
+    qmax = 127 if bits == 8 else 7
+    allb = np.arange(65536, dtype=np.uint32)
+    allf = (allb << 16).view(np.float32)
+    rows = []
+    # exact ties, scale 1 and 2^-3
+    for div in (1.0, 8.0):
+        ks = np.arange(-qmax, qmax) + 0.5
+        r = np.resize(ks, 128).astype(np.float32) / np.float32(div)
+        r[0] = np.float32(qmax / div)
+        rows.append(r)
+    # near ties for a few non-power-of-two scales
+    for amax in (100.0, 3.0, 0.0371, 5.5e-20):
+        a = np.float32((np.uint32(np.float32(amax).view(np.uint32)) & 0xFFFF0000).view(np.float32))
+        scale = np.float32(a / np.float32(qmax))
+        with np.errstate(all="ignore"):
+            t = (allf / scale).astype(np.float32)
+            d = np.abs(t - np.floor(t) - np.float32(0.5))
+        ok = np.isfinite(allf) & (np.abs(allf) <= a)
+        near = allf[ok & (d < 2.0 ** -12)]
+        assert near.size > 0
+        r = np.resize(rng.permutation(near), 128).astype(np.float32)
+        r[0] = a
+        rows.append(r)
+    sub = lambda hi: (rng.integers(0, hi, 128).astype(np.uint32) << 16).view(np.float32)
+    rows.append(sub(6) * np.where(rng.random(128) < 0.5, -1, 1).astype(np.float32))  # subnormal amax
+    rows.append(rng.uniform(-1, 1, 128).astype(np.float32) * np.float32(2.0 ** -120))  # scale in (2^-128, 2^-126)
+    rows.append(rng.uniform(-1, 1, 128).astype(np.float32) * np.float32(3.0e38))  # huge
+    rows.append(np.zeros(128, np.float32))
+    rows.append(np.full(128, -0.0, np.float32))
+    lone = np.zeros(128, np.float32)
+    lone[77] = -2.5
+    rows.append(lone)
+    from compressed_kv_cache_kvc_gb300.workloads import bf16_bits
+    out = [bf16_bits(r) for r in rows]
+    return [out[i % len(out)] for i in range(n_rows)]
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_bulk_append_rounding_edges(bits):
+    """Rows whose quotients x / scale sit on or within 2^-12 of a half-integer,
+    subnormal and near-overflow scales, zero rows: the long append (16-byte
+    loads, the product with the reciprocal deciding where it can) gives the
+    oracle's codes and scales bit for bit."""
+    rng = np.random.default_rng(400 + bits)
+    B, hq, hkv, n = 2, 4, 2, 96
+    k = _rand_bits(rng, (B, hkv, n, 128))
+    v = _rand_bits(rng, (B, hkv, n, 128))
+    edge = _edge_rows(bits, rng, 2 * B * hkv * 40)
+    i = 0
+    for b in range(B):
+        for h in range(hkv):
+            for t in range(4, 44):
+                k[b, h, t] = edge[i]
+                v[b, h, n - 1 - (t - 4)] = edge[(i + 7) % len(edge)]
+                i += 1
+    cache = _cache(hq, hkv, bits, B, n + 8)
+    _prefill(cache, k, v, [n] * B)
+    assert cache.last_launch_count() == 2
+    ora = _oracle(hq, bits, k, v, [n] * B)
+    st = T.StateView(cache)
+    for b in range(B):
+        for h in range(hkv):
+            T.check_codes(st, ora, b, h)
+    assert cache.read_status() == 0
+
+
+def test_append_8_byte_aligned_input():
+    """A long append from inputs aligned to 8 bytes but not 16 runs on the
+    one-CTA-per-sequence kernel and leaves the same state as the same rows
+    appended from aligned inputs."""
+    rng = np.random.default_rng(31)
+    B, hq, hkv, n = 2, 4, 2, 100
+    k = _rand_bits(rng, (B, hkv, n, 128))
+    v = _rand_bits(rng, (B, hkv, n, 128))
+    ca, cb = _cache(hq, hkv, 8, B, n + 8), _cache(hq, hkv, 8, B, n + 8)
+
+    def shifted(bits):
+        flat = T.to_dev_bf16(bits.reshape(-1))
+        buf = torch.empty(flat.numel() + 4, dtype=torch.bfloat16, device=flat.device)
+        view = buf[4:].view(bits.shape)
+        view.copy_(flat.view(bits.shape))
+        assert view.data_ptr() % 16 == 8
+        return view
+
+    ca.quantize_append(T.to_dev_bf16(k), T.to_dev_bf16(v))
+    assert ca.last_launch_count() == 2
+    cb.quantize_append(shifted(k), shifted(v))
+    assert cb.last_launch_count() == 1
+    torch.cuda.synchronize()
+    sa, sb = T.StateView(ca), T.StateView(cb)
+    for b in range(B):
+        for h in range(hkv):
+            for x, y in zip(sa.head(b, h), sb.head(b, h)):
+                assert np.array_equal(np.asarray(x).view(np.uint8), np.asarray(y).view(np.uint8)), (b, h)
+    # (the block ids differ: the one-CTA kernel's sequences take their pages
+    # from the free stack in launch order, not sequence order)
+    for name in ["SEQ_SLOTS", "SEQ_POS", "SINK_K", "SINK_V"]:
+        assert torch.equal(ca.buffer(name), cb.buffer(name)), name
+    assert ca.read_status() == 0 and cb.read_status() == 0
+
+
 def test_release_sequences():
     """Releasing a sequence returns its pages (no block lost or duplicated),
     empties it, leaves the others alone, is idempotent, and the freed slot
