@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(512) append_kernel(DevState s, int seq_begin, 
 // scratch (slots -1 when it failed); append_rows_kernel then spreads the
 // rows over (token chunk, sequence) CTAs.  Only for appends that push no
 // window token into the pool, so no row reads what another CTA writes.
-constexpr int kBulkTokens = 32;  // tokens per CTA of append_rows_kernel
+constexpr int kBulkTokens = 32;  // most tokens per CTA of append_rows_kernel (at most 3 pool pages)
 constexpr int kBulkWarps = 16;
 constexpr int kBulkStages = 6;  // units a warp keeps in flight (1 KB each)
 constexpr int kBulkSmem = kBulkWarps * kBulkStages * 1024;
@@ -300,6 +300,7 @@ __device__ __forceinline__ uint32_t low_bytes(uint32_t a, uint32_t b, uint32_t c
 // indices advance by the warp count without divisions.
 template <int BITS>
 __global__ void __launch_bounds__(kBulkWarps * 32, 2) append_rows_kernel(DevState s, int seq_begin, int n_new,
+                                                                          int chunk,
                                                                           const uint16_t* __restrict__ kin,
                                                                           const uint16_t* __restrict__ vin) {
   using namespace codes;
@@ -318,8 +319,8 @@ __global__ void __launch_bounds__(kBulkWarps * 32, 2) append_rows_kernel(DevStat
   const int ql = lane & 7;   // which dims of its row
   const int hkv = s.hkv;
   const int W = s.ring;
-  const int t0 = blockIdx.x * kBulkTokens;
-  const int nt = min(kBulkTokens, n_new - t0);
+  const int t0 = blockIdx.x * chunk;
+  const int nt = min(chunk, n_new - t0);
   const int nquad = (nt + 3) >> 2;
   const int units = nquad * hkv * 2;  // unit u: token quad u % nquad, (KV head, K or V) u / nquad
   const int dq = kBulkWarps / nquad, dr = kBulkWarps % nquad;
@@ -470,11 +471,26 @@ cudaError_t launch_append_bulk(const DevState& s, int seq_begin, int batch, int 
   e = s.bits == 8 ? opt_in_smem(reinterpret_cast<const void*>(append_rows_kernel<8>), kBulkSmem, done8)
                   : opt_in_smem(reinterpret_cast<const void*>(append_rows_kernel<4>), kBulkSmem, done4);
   if (e != cudaSuccess) return e;
-  const dim3 grid((n_new + kBulkTokens - 1) / kBulkTokens, batch);
+  // tokens per CTA: kBulkTokens, halved (down to one 4-token unit) while
+  // the grid would not give every SM two CTAs (short prompts)
+  static int sms[64] = {0};
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || sms[dev] == 0) {
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) sms[dev] = n;
+  }
+  const long long want = 2LL * (dev < 64 ? sms[dev] : 152);
+  int chunk = kBulkTokens;
+  while (chunk > 4 && (long long)((n_new + chunk - 1) / chunk) * batch < want) chunk /= 2;
+  const dim3 grid((n_new + chunk - 1) / chunk, batch);
   if (s.bits == 8)
-    append_rows_kernel<8><<<grid, kBulkWarps * 32, kBulkSmem, st>>>(s, seq_begin, n_new, k, v);
+    append_rows_kernel<8><<<grid, kBulkWarps * 32, kBulkSmem, st>>>(s, seq_begin, n_new, chunk, k, v);
   else
-    append_rows_kernel<4><<<grid, kBulkWarps * 32, kBulkSmem, st>>>(s, seq_begin, n_new, k, v);
+    append_rows_kernel<4><<<grid, kBulkWarps * 32, kBulkSmem, st>>>(s, seq_begin, n_new, chunk, k, v);
   return cudaGetLastError();
 }
 

@@ -472,6 +472,28 @@ def test_bulk_append_rounding_edges(bits):
     assert cache.read_status() == 0
 
 
+@pytest.mark.parametrize("B,n", [(10, 1000), (5, 1000), (4, 601), (3, 700)])
+def test_bulk_append_chunk_sizes(B, n):
+    """One batched long append whose grid takes 32, 16, 8 and 4 tokens per
+    CTA (on 152 SMs: the chunk halves while fewer than two CTAs per SM would
+    run), ragged tails included: codes and scales equal the oracle's bit for
+    bit in both code widths."""
+    for bits in (8, 4):
+        rng = np.random.default_rng(1000 * B + n + bits)
+        hq, hkv = 2, 2
+        k = _rand_bits(rng, (B, hkv, n, 128), outliers=[5])
+        v = _rand_bits(rng, (B, hkv, n, 128))
+        cache = _cache(hq, hkv, bits, B, n + 8)
+        cache.quantize_append(T.to_dev_bf16(k), T.to_dev_bf16(v))
+        assert cache.last_launch_count() == 2
+        ora = _oracle(hq, bits, k, v, [n] * B)
+        st = T.StateView(cache)
+        for b in range(B):
+            for h in range(hkv):
+                T.check_codes(st, ora, b, h)
+        assert cache.read_status() == 0
+
+
 def test_append_8_byte_aligned_input():
     """A long append from inputs aligned to 8 bytes but not 16 runs on the
     one-CTA-per-sequence kernel and leaves the same state as the same rows
