@@ -22,9 +22,9 @@ constexpr size_t kAlign = 256;
 // A split CTA has fixed costs (the page prefix, the query fragments, the
 // ring's first copies, the CTA merge and its partial): small steps (the
 // steady state of a long context, ~6500 pages) run faster on fewer, fuller
-// CTAs (at least 32 pages each: 58.1 ms for the 32k-context stack's 64 steps,
-// against 66.5 ms with 4), down to one CTA per SM; large steps fill one wave
-// either way.
+// CTAs (at least 32 pages each: 58.0 ms for the 32k-context stack's 64 steps,
+// against 66.5 ms with 4, 65.2 with 16 and 59.3 with 64), down to one CTA
+// per SM; large steps fill one wave either way.
 constexpr int kMinPagesPerCta = 32;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
