@@ -25,8 +25,9 @@ __device__ __forceinline__ float bf16_to_f32(uint32_t bits16) {
 }
 
 // Quantise one 128-value row (4 values per lane, one warp) into pool slot
-// `slot` of (sequence b, KV head h): codes, scale, and for K the position and
-// the initial score.  Integer codes, or with E4M3 codes (s.fp8) scale =
+// `slot` of a sequence's KV head h, `blk` the block id of the slot's page
+// (from its block-table row): codes, scale, and for K the position and the
+// initial score.  Integer codes, or with E4M3 codes (s.fp8) scale =
 // amax / 448 and each x / scale converted to FP8.
 // Four fp32 values -> four FP8 E4M3 codes (byte i = value i), rounded to
 // nearest even and saturated to +-448 by the conversion instruction (which
@@ -43,8 +44,8 @@ __device__ __forceinline__ uint32_t e4m3x4(float y0, float y1, float y2, float y
 }
 
 template <int BITS>
-__device__ __forceinline__ void quantize_row(const DevState& s, int b, int h, int kv, int slot, int p, float score,
-                                             uint2 raw, int lane) {
+__device__ __forceinline__ void quantize_row_blk(const DevState& s, int blk, int h, int kv, int slot, int p,
+                                                 float score, uint2 raw, int lane) {
   constexpr float kQmax = BITS == 8 ? 127.0f : 7.0f;
   constexpr int kLo = BITS == 8 ? -127 : -8;
   constexpr int kHi = BITS == 8 ? 127 : 7;
@@ -67,9 +68,7 @@ __device__ __forceinline__ void quantize_row(const DevState& s, int b, int h, in
       c[e] = min(max(q, kLo), kHi);
     }
   }
-  const int page = slot / kPage;
   const int off = slot % kPage;
-  const int blk = s.block_table[(size_t)b * s.max_bps + page];
   if ((unsigned)blk >= (unsigned)s.num_blocks) {
     if (lane == 0) atomicOr(&s.counters[kCtrStatus], kDevBadBlockId);
     return;
@@ -105,7 +104,24 @@ __global__ void __launch_bounds__(512) append_kernel(DevState s, int seq_begin, 
                                                      const uint16_t* __restrict__ vin) {
   const int bl = blockIdx.x;
   const int b = seq_begin + bl;
+  constexpr int kPagesStaged = 8;
   __shared__ int sh_slots, sh_pos, sh_ok, sh_lo, sh_hi;
+  __shared__ int sh_blk[kPagesStaged];  // block ids of the pages this append writes, from page slots / 16
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int hkv = s.hkv;
+  const int W = s.ring;
+  // this warp's first new-token row (row = warp), loaded while thread 0 takes
+  // the pages: the input does not depend on them
+  const int rows_new = n_new * hkv * 2;
+  uint2 raw0 = make_uint2(0u, 0u);
+  if (warp < rows_new) {
+    const int h = (warp >> 1) % hkv;
+    const int i = (warp >> 1) / hkv;
+    const uint16_t* src = ((warp & 1) ? vin : kin) + (((size_t)bl * hkv + h) * n_new + i) * kHeadDim;
+    raw0 = *reinterpret_cast<const uint2*>(src + lane * 4);
+  }
   if (threadIdx.x == 0) {
     const int slots = s.seq_slots[b];
     const int pos = s.seq_pos[b];
@@ -116,6 +132,7 @@ __global__ void __launch_bounds__(512) append_kernel(DevState s, int seq_begin, 
     const int new_pages = (new_slots + kPage - 1) / kPage;
     const int need = new_pages - old_pages;
     int ok = 1;
+    int32_t* row = s.block_table + (size_t)b * s.max_bps;
     if (new_pages > s.max_bps) {
       atomicOr(&s.counters[kCtrStatus], kDevTableOverflow);
       ok = 0;
@@ -126,10 +143,16 @@ __global__ void __launch_bounds__(512) append_kernel(DevState s, int seq_begin, 
         atomicOr(&s.counters[kCtrStatus], kDevOutOfBlocks);
         ok = 0;
       } else {
-        int32_t* row = s.block_table + (size_t)b * s.max_bps;
-        for (int j = 0; j < need; ++j) row[old_pages + j] = s.free_stack[top - 1 - j];
+        for (int j = 0; j < need; ++j) {
+          const int blk = s.free_stack[top - 1 - j];
+          row[old_pages + j] = blk;
+          const int k = old_pages + j - slots / kPage;
+          if (k < kPagesStaged) sh_blk[k] = blk;
+        }
       }
     }
+    // the partly filled page the first new slot lands in, if any
+    if (ok && slots % kPage != 0 && new_slots > slots) sh_blk[0] = row[slots / kPage];
     if (ok) {
       s.seq_slots[b] = new_slots;
       s.seq_pos[b] = pos + n_new;
@@ -142,12 +165,11 @@ __global__ void __launch_bounds__(512) append_kernel(DevState s, int seq_begin, 
   }
   __syncthreads();
   if (!sh_ok) return;
-
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int nwarps = blockDim.x >> 5;
-  const int hkv = s.hkv;
-  const int W = s.ring;
+  // block id of pool slot `slot` of this append (slots [sh_slots, new slots))
+  auto blk_of = [&](int slot) {
+    const int k = slot / kPage - sh_slots / kPage;
+    return k < kPagesStaged ? sh_blk[k] : s.block_table[(size_t)b * s.max_bps + slot / kPage];
+  };
 
   // ---- hybrid precision: the window tokens this append pushes out (positions
   // [lo, min(pos, hi)), all in the ring) are quantised into the pool with the
@@ -161,25 +183,27 @@ __global__ void __launch_bounds__(512) append_kernel(DevState s, int seq_begin, 
       const size_t ridx = ((size_t)b * hkv + h) * W + (a - kSinks) % W;
       const uint16_t* src = (kv ? s.ring_v : s.ring_k) + ridx * kHeadDim;
       const uint2 raw = *reinterpret_cast<const uint2*>(src + lane * 4);
-      quantize_row<BITS>(s, b, h, kv, sh_slots + (a - sh_lo), a, s.ring_score[ridx], raw, lane);
+      const int slot = sh_slots + (a - sh_lo);
+      quantize_row_blk<BITS>(s, blk_of(slot), h, kv, slot, a, s.ring_score[ridx], raw, lane);
     }
     __syncthreads();
   }
 
   // ---- the new tokens: sinks, pool (quantised), or the window ring (bf16)
-  for (int row = warp; row < n_new * hkv * 2; row += nwarps) {
+  for (int row = warp; row < rows_new; row += nwarps) {
     const int kv = row & 1;
     const int h = (row >> 1) % hkv;
     const int i = (row >> 1) / hkv;
     const uint16_t* src = (kv ? vin : kin) + (((size_t)bl * hkv + h) * n_new + i) * kHeadDim;
-    const uint2 raw = *reinterpret_cast<const uint2*>(src + lane * 4);
+    const uint2 raw = row == warp ? raw0 : *reinterpret_cast<const uint2*>(src + lane * 4);
     const int p = sh_pos + i;
     if (p < kSinks) {
       uint16_t* dst = (kv ? s.sink_v : s.sink_k) + (((size_t)b * hkv + h) * kSinks + p) * kHeadDim;
       *reinterpret_cast<uint2*>(dst + lane * 4) = raw;
       if (kv == 0 && lane == 0) s.sink_score[((size_t)b * hkv + h) * kSinks + p] = 0.0f;
     } else if (p < sh_hi) {
-      quantize_row<BITS>(s, b, h, kv, sh_slots + (p - sh_lo), p, 0.0f, raw, lane);
+      const int slot = sh_slots + (p - sh_lo);
+      quantize_row_blk<BITS>(s, blk_of(slot), h, kv, slot, p, 0.0f, raw, lane);
     } else {
       const size_t ridx = ((size_t)b * hkv + h) * W + (p - kSinks) % W;
       uint16_t* dst = (kv ? s.ring_v : s.ring_k) + ridx * kHeadDim;
