@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(512) append_kernel(DevState s, int seq_begin, 
 }
 
 // Bulk appends (a prompt) run as two launches: append_alloc_kernel, one
-// thread per sequence, takes the pages and advances the lengths exactly as
+// warp per sequence, takes the pages and advances the lengths exactly as
 // append_kernel's first thread does and leaves the old lengths in the plan
 // scratch (slots -1 when it failed); append_rows_kernel then spreads the
 // rows over (token chunk, sequence) CTAs.  Only for appends that push no
@@ -224,9 +224,12 @@ constexpr int kBulkWarps = 16;
 constexpr int kBulkStages = 6;  // units a warp keeps in flight (1 KB each)
 constexpr int kBulkSmem = kBulkWarps * kBulkStages * 1024;
 
+// One warp per sequence: lane 0 takes the pages off the free stack, the
+// lanes copy their block ids into the sequence's block-table row.
 __global__ void append_alloc_kernel(DevState s, int seq_begin, int batch, int n_new) {
-  const int bl = blockIdx.x * blockDim.x + threadIdx.x;
-  if (bl >= batch) return;
+  const int lane = threadIdx.x & 31;
+  const int bl = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  if (bl >= batch) return;  // the same for the whole warp
   const int b = seq_begin + bl;
   const int slots = s.seq_slots[b];
   const int pos = s.seq_pos[b];
@@ -238,25 +241,34 @@ __global__ void append_alloc_kernel(DevState s, int seq_begin, int batch, int n_
   const int need = new_pages - old_pages;
   int ok = 1;
   if (new_pages > s.max_bps) {
-    atomicOr(&s.counters[kCtrStatus], kDevTableOverflow);
+    if (lane == 0) atomicOr(&s.counters[kCtrStatus], kDevTableOverflow);
     ok = 0;
   } else if (need > 0) {
-    const int top = atomicSub(&s.counters[kCtrFreeTop], need);
-    if (top - need < 0 || top > s.num_blocks) {
-      atomicAdd(&s.counters[kCtrFreeTop], need);
-      atomicOr(&s.counters[kCtrStatus], kDevOutOfBlocks);
+    int top = 0;
+    if (lane == 0) {
+      top = atomicSub(&s.counters[kCtrFreeTop], need);
+      if (top - need < 0 || top > s.num_blocks) {
+        atomicAdd(&s.counters[kCtrFreeTop], need);
+        atomicOr(&s.counters[kCtrStatus], kDevOutOfBlocks);
+        top = -1;
+      }
+    }
+    top = __shfl_sync(0xffffffffu, top, 0);
+    if (top < 0) {
       ok = 0;
     } else {
       int32_t* row = s.block_table + (size_t)b * s.max_bps;
-      for (int j = 0; j < need; ++j) row[old_pages + j] = s.free_stack[top - 1 - j];
+      for (int j = lane; j < need; j += 32) row[old_pages + j] = s.free_stack[top - 1 - j];
     }
   }
-  if (ok) {
-    s.seq_slots[b] = new_slots;
-    s.seq_pos[b] = pos + n_new;
+  if (lane == 0) {
+    if (ok) {
+      s.seq_slots[b] = new_slots;
+      s.seq_pos[b] = pos + n_new;
+    }
+    s.plan[2 * b] = ok ? slots : -1;
+    s.plan[2 * b + 1] = pos;
   }
-  s.plan[2 * b] = ok ? slots : -1;
-  s.plan[2 * b + 1] = pos;
 }
 
 // Integer codes of 8 values of a row, as words whose low byte is the
@@ -488,7 +500,7 @@ __global__ void fill_free_stack_kernel(int32_t* stack, int n) {
 
 cudaError_t launch_append_bulk(const DevState& s, int seq_begin, int batch, int n_new, const uint16_t* k,
                                const uint16_t* v, cudaStream_t st) {
-  append_alloc_kernel<<<(batch + 127) / 128, 128, 0, st>>>(s, seq_begin, batch, n_new);
+  append_alloc_kernel<<<(batch * 32 + 127) / 128, 128, 0, st>>>(s, seq_begin, batch, n_new);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   static int done8[64] = {0}, done4[64] = {0};
