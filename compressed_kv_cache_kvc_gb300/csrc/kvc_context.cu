@@ -120,12 +120,16 @@ constexpr int kRingStage = 2 * 16 * kRingRow * 2;
 // held to 168 registers (three CTAs per SM, as the INT4 and FP8 forms
 // without a window reach unbounded): it is latency-bound, and unbounded it
 // took 239 and 255 registers and ran two CTAs per SM; bounded it spills
-// nothing.  The other forms keep the compiler's own choice (a minimum of 0
-// CTAs per SM states none; a minimum of 1 made it spend up to 255 registers
-// on pass 0 and INT4 pass 1; the 8-bit window forms would spill).
+// nothing.  Pass 0 over INT4 codes is held to 96 registers (five CTAs per
+// SM instead of four, no spills; over 8-bit codes that was slower).  The
+// other forms keep the compiler's own choice (a minimum of 0 CTAs per SM
+// states none; a minimum of 1 made it spend up to 255 registers on pass 0
+// and INT4 pass 1; the 8-bit window forms would spill).
 template <int BITS, bool FP8, int PASS, bool WIN>
 __global__ void __launch_bounds__(kCtxThreads,
-                                  (PASS == 1 && ((BITS == 8 && !FP8 && !WIN) || (BITS == 4 && WIN))) ? 3 : 0)
+                                  (PASS == 1 && ((BITS == 8 && !FP8 && !WIN) || (BITS == 4 && WIN)))
+                                      ? 3
+                                      : ((PASS == 0 && BITS == 4) ? 5 : 0))
     ctx_attn_kernel(DevState s, int seq_begin, CtxArgs a) {
   using Gm = CtxGeom<BITS>;
   constexpr int RB = Gm::kRowBytes;
