@@ -57,6 +57,23 @@ def dist_env():
     return ws, rank, local
 
 
+def copy_groups(layers: int) -> tuple[list, list]:
+    """The end-to-end step's copy groups, as (first, end) layer ranges: inputs
+    [0, 1), [1, 3), [3, 7), ... (doubling, so each group is copied long before
+    its first layer runs) and outputs ..., [L-4, L-2), [L-2, L-1), [L-1, L)
+    (halving toward the end, so only the last layer's output is copied after
+    the last layer)."""
+    in_groups, a = [], 0
+    while a < layers:
+        in_groups.append((a, min(layers, 2 * a + 1)))
+        a = 2 * a + 1
+    out_groups, b = [], layers
+    while b > 0:
+        out_groups.insert(0, (max(0, layers - 2 * (layers - b) - 1), b))
+        b = out_groups[0][0]
+    return in_groups, out_groups
+
+
 def shard_range(total: int, world: int, rank: int) -> tuple[int, int]:
     """Contiguous slice [begin, end) of `total` units for `rank`."""
     base, extra = divmod(total, world)
@@ -623,14 +640,7 @@ def gpu_arm(args):
     d2h = h_out_all.numel() * h_out_all.element_size()
 
     copy_stream = torch.cuda.Stream(device=dev)
-    in_groups, a = [], 0
-    while a < layers:
-        in_groups.append((a, min(layers, 2 * a + 1)))
-        a = 2 * a + 1
-    out_groups, b = [], layers
-    while b > 0:
-        out_groups.insert(0, (max(0, layers - 2 * (layers - b) - 1), b))
-        b = out_groups[0][0]
+    in_groups, out_groups = copy_groups(layers)
     in_first = {g[0]: (i, g) for i, g in enumerate(in_groups)}
     out_last = {g[1] - 1: g for g in out_groups}
     in_ready = [torch.cuda.Event() for _ in in_groups]

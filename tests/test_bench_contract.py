@@ -38,3 +38,22 @@ def test_reference_arm_other_ranks_print_nothing():
     r = _run({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def test_e2e_copy_groups_cover_every_layer_once():
+    """The end-to-end step's pipelined copies: every layer's inputs and
+    outputs are copied exactly once, in layer order; the first input group
+    is layer 0 alone (the first layer waits for one layer's inputs) and the
+    last output group is the last layer alone (one output left to copy after
+    the last layer); input groups double, output groups halve."""
+    sys.path.insert(0, ROOT)
+    import bench
+    for layers in (1, 2, 3, 5, 7, 8, 32, 48, 80):
+        ins, outs = bench.copy_groups(layers)
+        for groups in (ins, outs):
+            assert [l for a, b in groups for l in range(a, b)] == list(range(layers)), (layers, groups)
+            assert all(b > a for a, b in groups)
+        assert ins[0] == (0, 1) and outs[-1] == (layers - 1, layers)
+        assert all(ins[i + 1][1] - ins[i + 1][0] >= ins[i][1] - ins[i][0] for i in range(len(ins) - 2))
+        assert all(outs[i][1] - outs[i][0] >= outs[i + 1][1] - outs[i + 1][0] for i in range(1, len(outs) - 1))
+        assert len(ins) <= layers.bit_length() + 1 and len(outs) <= layers.bit_length() + 1
