@@ -494,6 +494,39 @@ def test_bulk_append_chunk_sizes(B, n):
         assert cache.read_status() == 0
 
 
+@pytest.mark.parametrize("bits", [8, 4])
+def test_long_window_append_equals_token_by_token(bits):
+    """A long append that pushes window tokens into the pool runs on the
+    one-CTA-per-sequence kernel and writes more pool pages than that kernel
+    stages in shared memory (13 here): the state equals the same tokens
+    appended one at a time, byte for byte."""
+    from compressed_kv_cache_kvc_gb300.cache import KVCache
+    rng = np.random.default_rng(77 + bits)
+    hkv, W, n1, n2 = 2, 40, 300, 200
+    mbps = (n1 + n2) // 16 + 2
+    ca = KVCache(4, hkv, bits, mbps, 1, mbps, bf16_window=W)
+    cb = KVCache(4, hkv, bits, mbps, 1, mbps, bf16_window=W)
+    k = _rand_bits(rng, (1, hkv, n1 + n2, 128))
+    v = _rand_bits(rng, (1, hkv, n1 + n2, 128))
+    for a, e in ((0, n1), (n1, n1 + n2)):
+        ca.quantize_append(T.to_dev_bf16(np.ascontiguousarray(k[:, :, a:e])),
+                           T.to_dev_bf16(np.ascontiguousarray(v[:, :, a:e])))
+    assert ca.last_launch_count() == 1  # window tokens pushed out: the one-CTA kernel
+    for t in range(n1 + n2):
+        cb.quantize_append(T.to_dev_bf16(np.ascontiguousarray(k[:, :, t:t + 1])),
+                           T.to_dev_bf16(np.ascontiguousarray(v[:, :, t:t + 1])))
+    torch.cuda.synchronize()
+    sa, sb = T.StateView(ca), T.StateView(cb)
+    for h in range(hkv):
+        for x, y in zip(sa.head(0, h), sb.head(0, h)):
+            assert np.array_equal(np.asarray(x).view(np.uint8), np.asarray(y).view(np.uint8)), h
+        for x, y in zip(sa.ring_head(0, h), sb.ring_head(0, h)):
+            assert np.array_equal(np.asarray(x).view(np.uint8), np.asarray(y).view(np.uint8)), h
+    for name in ["BLOCK_TABLE", "SEQ_SLOTS", "SEQ_POS", "SINK_K", "SINK_V"]:
+        assert torch.equal(ca.buffer(name), cb.buffer(name)), name
+    assert ca.read_status() == 0 and cb.read_status() == 0
+
+
 def test_append_8_byte_aligned_input():
     """A long append from inputs aligned to 8 bytes but not 16 runs on the
     one-CTA-per-sequence kernel and leaves the same state as the same rows
