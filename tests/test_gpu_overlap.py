@@ -175,3 +175,44 @@ def test_overlap_graph_over_layers_equals_eager_steps():
             c.sync_host()
             assert c.read_status() == 0
         del g
+
+
+@pytest.mark.parametrize("name", ["qwen14b_b32_gqa5_t8192_int4_h2o_48l", "llama7b_b16_h32_t4096_int8_h2o"])
+def test_overlap_equals_one_call_step_full_size(name):
+    """The benchmarked call itself, kvc_decode_step_overlap, on one full-size
+    layer of the INT4 Qwen-shaped stack (256 pairs) and of the INT8
+    LLaMA-shaped one (512 pairs, shuffled blocks), two steps back to back:
+    the same outputs bit for bit and the same logical state as the one-call
+    step, which tests/test_gpu_fullsize.py checks against the oracle at these
+    sizes.  Inputs from the bench's device-side draw of the same recipe."""
+    from compressed_kv_cache_kvc_gb300 import workloads as W
+    from compressed_kv_cache_kvc_gb300.cache import KVCache
+    w = W.WORKLOADS[name]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    q, k, v, kn, vn = W.gen_layer_torch(w, 0, dev)
+    B, hq, hkv, steps = w.batch, w.num_q_heads, w.num_kv_heads, 2
+    mbps = (w.context + steps + 15) // 16 + 1
+    order = W.block_order(w, B * mbps) if w.shuffled_blocks else None
+    ca, cb = [KVCache(hq, hkv, w.bits, B * mbps, B, mbps, block_order=order) for _ in range(2)]
+    for c in (ca, cb):
+        c.quantize_append(k, v)
+    del k, v
+    inputs = [(q, kn, vn)] + [W.gen_step_torch(w, 0, st, dev) for st in range(1, steps)]
+    s_att, s_ev = torch.cuda.Stream(), torch.cuda.Stream()
+    ws_b = cb.workspace(B)
+    s_att.wait_stream(torch.cuda.current_stream())
+    outs_a, outs_b = [], []
+    for qq, kk, vv in inputs:
+        outs_a.append(ca.decode_step(qq, kk, vv, mode=w.mode, budget=w.budget, recent=w.recent, window=w.window))
+        ob = torch.empty_like(qq)
+        cb.decode_step_overlap(qq, kk, vv, s_ev, mode=w.mode, budget=w.budget, recent=w.recent, window=w.window,
+                               out=ob, workspace=ws_b, stream=s_att)
+        outs_b.append(ob)
+    assert cb.read_status(stream=s_att) == 0
+    torch.cuda.synchronize()
+    assert ca.read_status() == 0
+    for oa, ob in zip(outs_a, outs_b):
+        assert torch.equal(oa, ob)
+    _same_state(ca, cb)
+    for b in range(B):
+        assert ca.lengths(b) == cb.lengths(b)
